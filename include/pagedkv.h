@@ -1,0 +1,163 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) PagedAttention decode library.
+ *
+ * The operations follow "An Inference Engine in 1,500 Lines of CUDA: The
+ * Map" (jaehun.me, tiny-vllm series part 1):
+ *   - "What is in the box": PagedAttention as 16-token pages plus a
+ *     block_table index array; GQA_Q_TO_K_RATIO = 4; online softmax inside
+ *     pagedAttentionKernel; RoPE with Llama 3 scaling.
+ *   - "The path of one inference": init_rope_frequencies(HEAD_DIM,
+ *     MAX_SEQ_LEN, 500000, 32, 1, 4, 8192); one 2 GB cudaMalloc cut into
+ *     16-token blocks numbered by an iota free list; a block_table of
+ *     MAX_SEQUENCES * N_LAYERS * MAX_BLOCKS_PER_SEQ ints set to -1 ("not
+ *     assigned yet"); decode handles one token per active slot per step.
+ *
+ * Fixed shapes (Llama 3.2 1B): 32 query heads, 8 kv heads (q head h reads
+ * kv head h / 4), head_dim 64, 16 tokens per block, bf16 storage.
+ *
+ * Layouts (all row-major, all device memory owned by the caller):
+ *   kv_cache     [num_blocks][2][16][8][64] bf16   (index 0 = K, 1 = V);
+ *                one block is 32 KiB, contiguous
+ *   block_table  [num_seqs][n_layers][max_blocks_per_seq] int32, -1 = none;
+ *                sequence i of a call uses row i
+ *   q, out       [num_seqs][32][64] bf16
+ *   k_new, v_new [num_seqs][8][64] bf16
+ *   context_lens [num_seqs] int32
+ *   free_list    [num_blocks] int32, a stack: entries [0, *free_count) free
+ *
+ * bf16 values are passed as their 16-bit patterns (uint16_t).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated; the library allocates and
+ *     frees nothing and keeps no pointer after the call returns.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and the call returns without synchronising.
+ *   - The return value reports host-detectable faults (PA_ERR_*).  Faults
+ *     found by the kernels (bad block id, context out of range, free-list
+ *     underflow/overflow, a wait that ran out) are OR-ed as PA_DEV_* bits into
+ *     the caller's device word `*err`; the kernels never trap.  The caller
+ *     zeroes *err when it wants a fresh report.
+ *   - num_seqs == 0 (or n_free == 0) is a no-op that returns PA_OK.
+ *   - Tensor pointers must be 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_NUM_Q_HEADS   32
+#define PA_NUM_KV_HEADS  8
+#define PA_HEAD_DIM      64
+#define PA_BLOCK_TOKENS  16
+#define PA_BLOCK_BYTES   (2 * PA_BLOCK_TOKENS * PA_NUM_KV_HEADS * PA_HEAD_DIM * 2)
+
+/* host-side return codes */
+#define PA_OK              0
+#define PA_ERR_NULL       -1   /* a required pointer is NULL */
+#define PA_ERR_ARG        -2   /* a size or count is out of range */
+#define PA_ERR_LAYER      -3   /* layer outside [0, n_layers) */
+#define PA_ERR_WORKSPACE  -4   /* workspace NULL or smaller than pa_decode_workspace_size */
+#define PA_ERR_ALIGN      -5   /* a tensor pointer is not 16-byte aligned */
+#define PA_ERR_CUDA       -6   /* a CUDA runtime call or kernel launch failed */
+#define PA_ERR_DEVICE     -7   /* no usable device, or not an sm_103 GPU */
+
+/* device-side error bits, OR-ed into *err */
+#define PA_DEV_BAD_BLOCK       1   /* block id outside [0, num_blocks) inside a context */
+#define PA_DEV_CTX_RANGE       2   /* context < 0 or beyond max_blocks_per_seq * 16 */
+#define PA_DEV_FREE_UNDERFLOW  4   /* append needed a block and the free list was empty */
+#define PA_DEV_FREE_OVERFLOW   8   /* free pushed past num_blocks entries */
+#define PA_DEV_TIMEOUT        16   /* an internal pipeline wait ran out; output invalid */
+
+/*
+ * pa_kv_append_rope -- append one new token per sequence to the paged cache.
+ *
+ * Page: "The path of one inference" (free_blocks / block_table set-up,
+ * init_rope_frequencies arguments) and "What is in the box" (RoPE with
+ * Llama 3 scaling; ropeKernelDecode is the decode-time RoPE).
+ *
+ * For each sequence s, pos = context_lens[s] (tokens already cached):
+ *   1. If pos % 16 == 0, a block is taken from the free list: sequences that
+ *      need one are served in ascending s, each taking
+ *      free_list[*free_count - 1] and decrementing *free_count; the id is
+ *      written to block_table[s][layer][pos / 16].
+ *   2. k_new[s] is rotated with rotate-half RoPE at angle pos * f_i, f_i the
+ *      Llama-3-scaled inverse frequencies (theta 500000, factor 32, low 1,
+ *      high 4, original context 8192), rounded to bf16, and stored with
+ *      v_new[s] (copied bit for bit) at slot pos % 16 of that block.
+ *   3. If q_or_null is not NULL, q[s] (all 32 heads) is rotated in place at
+ *      the same position.
+ * Device errors: PA_DEV_CTX_RANGE (pos < 0 or pos >= max_blocks_per_seq*16;
+ * nothing written), PA_DEV_FREE_UNDERFLOW (no block left; nothing written),
+ * PA_DEV_BAD_BLOCK (existing table entry invalid; nothing written).
+ * Two kernels on `stream`; the second starts early with programmatic
+ * dependent launch and waits for the first before touching the cache.
+ */
+int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                      uint16_t *kv_cache, int num_blocks,
+                      int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int layer,
+                      int32_t *free_list, int32_t *free_count, int32_t *err,
+                      void *stream);
+
+/*
+ * pa_decode_attention -- the decode step of PagedAttention for one layer.
+ *
+ * Page: "What is in the box" (pagedAttentionKernel: online softmax, warp
+ * shuffle reductions, 16-token pages + block_table; GQA ratio 4).
+ *
+ * out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t over the
+ * context_lens[s] tokens t of sequence s, K_t/V_t read from block
+ * block_table[s][layer][t / 16], slot t % 16, kv head h / 4.  fp32
+ * accumulation, output rounded to bf16.  A sequence with context 0 gets a
+ * zero output.  Long contexts are split across CTAs and merged (split
+ * context); the split only changes rounding.
+ * workspace: device scratch of at least pa_decode_workspace_size(num_seqs,
+ * max_blocks_per_seq) bytes, owned by the caller, contents need no
+ * initialisation; calls that share one workspace must not overlap in time.
+ * Device errors: PA_DEV_BAD_BLOCK (that token's contribution is dropped),
+ * PA_DEV_CTX_RANGE (context clamped), PA_DEV_TIMEOUT.
+ */
+int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                        int num_blocks, const int32_t *block_table, int n_layers,
+                        int max_blocks_per_seq, const int32_t *context_lens,
+                        int num_seqs, int layer, float scale,
+                        void *workspace, size_t workspace_bytes, int32_t *err,
+                        void *stream);
+
+/* Bytes of workspace pa_decode_attention needs on the current device. */
+size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq);
+
+/*
+ * pa_free -- return finished sequences' blocks to the free list.
+ *
+ * Page: "The path of one inference" (free_blocks numbered by iota; -1 =
+ * not assigned yet) and the slot recycling of the decode loop.
+ * For i = 0..n_free-1 in order, s = seq_ids[i] (a block_table row), every
+ * layer 0..n_layers-1 and logical block j < ceil(context_lens[s] / 16):
+ * push block_table[s][layer][j] onto the back of the free list and set the
+ * entry to -1.  num_blocks bounds the free list.  seq_ids and context_lens
+ * are device arrays.  Device errors: PA_DEV_BAD_BLOCK (entry invalid; reset
+ * to -1, not pushed), PA_DEV_FREE_OVERFLOW (free list full; entry kept),
+ * PA_DEV_CTX_RANGE (negative seq id or context out of range).
+ */
+int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_layers,
+            int max_blocks_per_seq, const int32_t *context_lens,
+            int32_t *free_list, int32_t *free_count, int num_blocks,
+            int32_t *err, void *stream);
+
+/* Cap on the CTAs one pa_decode_attention launch uses (0 = automatic: two
+ * per SM).  Process-wide; affects only how contexts are split. */
+int pa_decode_set_grid_limit(int max_ctas);
+
+/* Human-readable name of a PA_ERR_* code. */
+const char *pa_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -221,7 +221,9 @@ int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *pool
  * (free_blocks is an iota vector, "The path of one inference"; the reading
  * here pops from its back, sequences in ascending order), records it in
  * block_table[s][layer][pos / 16], then stores RoPE(k) and v at slot
- * pos % 16.  q, when given, is rotated in place at the same position. */
+ * pos % 16.  q, when given, is rotated in place at the same position; that
+ * rotation depends on the position alone, so it happens even when the K/V
+ * store is refused.  A refused allocation leaves the table entry at -1. */
 int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *q_or_null, uint16_t *pool, int num_blocks,
                           int32_t *block_table, int n_layers, int max_blocks_per_seq,
@@ -234,10 +236,24 @@ int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
     for (int s = 0; s < num_seqs; ++s) {
         int pos = context_lens[s];
         if (pos < 0 || pos >= max_blocks_per_seq * BS) { err |= PAO_ERR_CTX_RANGE; continue; }
+        if (q_or_null) {
+            /* q turns at its position whatever happens to the K/V store */
+            for (int h = 0; h < HQ; ++h) {
+                uint16_t *qh = q_or_null + ((size_t)s * HQ + h) * HD;
+                for (int d = 0; d < HD; ++d) x[d] = oracle_bf16_to_double(qh[d]);
+                oracle_rope_rotate(x, HD, (double)pos, inv_freq, y);
+                for (int d = 0; d < HD; ++d) qh[d] = oracle_double_to_bf16(y[d]);
+            }
+        }
         int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
         int blk;
         if (pos % BS == 0) {
-            if (*free_count <= 0) { err |= PAO_ERR_FREE_UNDERFLOW; continue; }
+            if (*free_count <= 0) {
+                /* refused: the page stays unassigned */
+                err |= PAO_ERR_FREE_UNDERFLOW;
+                row[pos / BS] = -1;
+                continue;
+            }
             blk = free_list[*free_count - 1];
             *free_count -= 1;
             row[pos / BS] = blk;
@@ -255,14 +271,6 @@ int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
             for (int d = 0; d < HD; ++d) {
                 pool[pool_index(blk, 0, slot, h, d)] = oracle_double_to_bf16(y[d]);
                 pool[pool_index(blk, 1, slot, h, d)] = v[d];
-            }
-        }
-        if (q_or_null) {
-            for (int h = 0; h < HQ; ++h) {
-                uint16_t *qh = q_or_null + ((size_t)s * HQ + h) * HD;
-                for (int d = 0; d < HD; ++d) x[d] = oracle_bf16_to_double(qh[d]);
-                oracle_rope_rotate(x, HD, (double)pos, inv_freq, y);
-                for (int d = 0; d < HD; ++d) qh[d] = oracle_double_to_bf16(y[d]);
             }
         }
     }

@@ -1,0 +1,371 @@
+// pa_append.cu -- KV append with Llama-3-scaled RoPE, and block release.
+//
+// Page: "An Inference Engine in 1,500 Lines of CUDA: The Map".  "The path of
+// one inference": the KV cache is one allocation cut into 16-token blocks
+// numbered by an iota free list (free_blocks), and block_table entries
+// start at -1 ("not assigned yet"); init_rope_frequencies(HEAD_DIM,
+// MAX_SEQ_LEN, 500000, 32, 1, 4, 8192) sets up RoPE.  "What is in the box":
+// RoPE with Llama 3 scaling (ropeKernel_llama3 / ropeKernelDecode).
+//
+// pa_kv_append_rope is two kernels:
+//   append_alloc_kernel  (1 CTA)  serves the sequences whose position starts
+//                                 a page, in ascending order, from the back
+//                                 of the free list; writes the table entries
+//                                 and the new free count.
+//   append_store_kernel  (1 CTA per sequence, programmatic dependent launch)
+//                                 rotates q and k while the first kernel
+//                                 runs, then waits for it and stores K/V in
+//                                 the slot the table names.
+#include <climits>
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kScanCta = 1024;
+constexpr int kStoreThreads = (kHkv + kHq) * 8;   // 8 threads per head row, 40 rows
+
+struct AppendParams {
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  uint16_t *q;                 // may be null
+  unsigned char *kv;
+  int32_t *block_table;
+  const int32_t *context_lens;
+  int32_t *free_list;
+  int32_t *free_count;
+  int32_t *err;
+  int num_blocks;
+  int n_layers;
+  int max_blocks;
+  int num_seqs;
+  int layer;
+};
+
+__device__ __forceinline__ size_t table_row(int s, int n_layers, int layer, int max_blocks) {
+  return (static_cast<size_t>(s) * n_layers + layer) * static_cast<size_t>(max_blocks);
+}
+
+// Exclusive prefix count of `flag` over a 1024-thread CTA; also returns the
+// CTA total.  `tot` is 32 ints of shared scratch.
+__device__ __forceinline__ int cta_exclusive_count(bool flag, int *tot, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, flag);
+  const int before_in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) tot[warp] = __popc(bal);
+  __syncthreads();
+  int before = 0, all = 0;
+  for (int w = 0; w < kScanCta / 32; ++w) {
+    const int t = tot[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  __syncthreads();
+  *total = all;
+  return before + before_in_warp;
+}
+
+__global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) {
+  pdl_launch_dependents();   // the store kernel may start its rotations now
+  __shared__ int tot[kScanCta / 32];
+  const int cap = p.max_blocks * kBs;
+  const int fc0 = *p.free_count;
+  int served = 0;
+  for (int base = 0; base < p.num_seqs; base += kScanCta) {
+    const int i = base + threadIdx.x;
+    int pos = 0;
+    bool need = false;
+    if (i < p.num_seqs) {
+      pos = p.context_lens[i];
+      const bool in_range = pos >= 0 && pos < cap;
+      if (!in_range) report(p.err, PA_DEV_CTX_RANGE);
+      need = in_range && (pos % kBs == 0);
+    }
+    int chunk = 0;
+    const int rank = served + cta_exclusive_count(need, tot, &chunk);
+    if (need) {
+      int32_t *entry = p.block_table + table_row(i, p.n_layers, p.layer, p.max_blocks) + pos / kBs;
+      if (rank < fc0) {
+        const int blk = p.free_list[fc0 - 1 - rank];
+        *entry = blk;
+        if (blk < 0 || blk >= p.num_blocks) report(p.err, PA_DEV_BAD_BLOCK);
+      } else {
+        *entry = -1;   // refused: the page stays unassigned
+        report(p.err, PA_DEV_FREE_UNDERFLOW);
+      }
+    }
+    served += chunk;
+  }
+  if (threadIdx.x == 0) *p.free_count = max(fc0 - served, 0);
+}
+
+// Llama 3 rescaling of the RoPE inverse frequency of pair i (head_dim 64):
+// theta 500000, factor 32, low_freq_factor 1, high_freq_factor 4, original
+// context 8192.  Wavelengths under 8192/4 keep their frequency, those over
+// 8192/1 are slowed by the factor, and the band between blends the two
+// linearly in 8192/wavelength.
+__device__ double llama3_inv_freq(int i) {
+  const double theta = 500000.0, factor = 32.0, low = 1.0, high = 4.0, orig = 8192.0;
+  const double two_pi = 6.283185307179586476925;
+  const double f = pow(theta, -static_cast<double>(2 * i) / kD);
+  const double wavelen = two_pi / f;
+  if (wavelen < orig / high) return f;
+  if (wavelen > orig / low) return f / factor;
+  const double w = (orig / wavelen - low) / (high - low);
+  return (1.0 - w) * (f / factor) + w * f;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint32_t float_to_bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Rotate 4 consecutive pairs (d, d + 32), d = 4j..4j+3, of one head row.
+__device__ __forceinline__ void rotate4(uint2 lo, uint2 hi, const float2 *cs, int j, uint2 *out_lo,
+                                        uint2 *out_hi) {
+  const uint32_t lw[2] = {lo.x, lo.y}, hw[2] = {hi.x, hi.y};
+  uint32_t ol[2], oh[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    uint32_t rl = 0, rh = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const float a = bf16_bits_to_float((lw[w] >> (16 * half)) & 0xffffu);
+      const float b = bf16_bits_to_float((hw[w] >> (16 * half)) & 0xffffu);
+      const float2 c = cs[4 * j + 2 * w + half];   // (cos, sin)
+      const float ra = fmaf(a, c.x, -b * c.y);
+      const float rb = fmaf(b, c.x, a * c.y);
+      rl |= float_to_bf16_bits(ra) << (16 * half);
+      rh |= float_to_bf16_bits(rb) << (16 * half);
+    }
+    ol[w] = rl;
+    oh[w] = rh;
+  }
+  *out_lo = make_uint2(ol[0], ol[1]);
+  *out_hi = make_uint2(oh[0], oh[1]);
+}
+
+__global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParams p) {
+  __shared__ float2 cs[kD / 2];
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int pos = p.context_lens[s];
+  const bool in_range = pos >= 0 && pos < p.max_blocks * kBs;
+  if (!in_range) {            // reported by the allocation kernel
+    pdl_wait_primary();
+    return;
+  }
+  if (tid < kD / 2) {
+    // angle in fp64 so that positions in the tens of thousands keep their
+    // phase; the rotation itself runs in fp32
+    double sn, cn;
+    sincos(static_cast<double>(pos) * llama3_inv_freq(tid), &sn, &cn);
+    cs[tid] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
+  }
+  __syncthreads();
+
+  const int head = tid >> 3;   // 0..7 k heads, 8..39 q heads
+  const int j = tid & 7;
+  uint2 klo = make_uint2(0, 0), khi = make_uint2(0, 0);
+  if (head < kHkv) {
+    const uint16_t *row = p.k_new + (static_cast<size_t>(s) * kHkv + head) * kD;
+    const uint2 lo = *reinterpret_cast<const uint2 *>(row + 4 * j);
+    const uint2 hi = *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j);
+    rotate4(lo, hi, cs, j, &klo, &khi);
+  } else if (p.q) {
+    uint16_t *row = p.q + (static_cast<size_t>(s) * kHq + (head - kHkv)) * kD;
+    const uint2 lo = *reinterpret_cast<const uint2 *>(row + 4 * j);
+    const uint2 hi = *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j);
+    uint2 rlo, rhi;
+    rotate4(lo, hi, cs, j, &rlo, &rhi);
+    *reinterpret_cast<uint2 *>(row + 4 * j) = rlo;
+    *reinterpret_cast<uint2 *>(row + kD / 2 + 4 * j) = rhi;
+  }
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (tid < kTokRowBytes / 16)
+    v = reinterpret_cast<const uint4 *>(p.v_new + static_cast<size_t>(s) * kHkv * kD)[tid];
+
+  pdl_wait_primary();   // the table entry of a new page is written by the allocation kernel
+  const int blk =
+      p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + pos / kBs];
+  if (blk < 0 || blk >= p.num_blocks) {
+    // a new page that was refused or popped invalid is reported by the
+    // allocation kernel; an invalid existing entry is reported here
+    if (tid == 0 && pos % kBs != 0) report(p.err, PA_DEV_BAD_BLOCK);
+    return;
+  }
+  unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
+  const int slot = pos % kBs;
+  if (head < kHkv) {
+    unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
+    *reinterpret_cast<uint2 *>(krow + 8 * j) = klo;
+    *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = khi;
+  }
+  if (tid < kTokRowBytes / 16)
+    reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v;
+}
+
+struct FreeParams {
+  const int32_t *seq_ids;
+  int32_t *block_table;
+  const int32_t *context_lens;
+  int32_t *free_list;
+  int32_t *free_count;
+  int32_t *err;
+  int n_free;
+  int n_layers;
+  int max_blocks;
+  int num_blocks;
+};
+
+__global__ void __launch_bounds__(kScanCta) free_kernel(FreeParams p) {
+  __shared__ int tot[kScanCta / 32];
+  const int cap = p.max_blocks * kBs;
+  const int fc0 = *p.free_count;
+  int pushed = 0;
+  for (int i = 0; i < p.n_free; ++i) {
+    const int s = p.seq_ids[i];
+    if (s < 0) {
+      if (threadIdx.x == 0) report(p.err, PA_DEV_CTX_RANGE);
+      continue;
+    }
+    int T = p.context_lens[s];
+    if (T < 0 || T > cap) {
+      if (threadIdx.x == 0) report(p.err, PA_DEV_CTX_RANGE);
+      T = min(max(T, 0), cap);
+    }
+    const int nb = (T + kBs - 1) / kBs;
+    const long long entries = static_cast<long long>(nb) * p.n_layers;
+    for (long long e0 = 0; e0 < entries; e0 += kScanCta) {
+      const long long e = e0 + threadIdx.x;
+      int32_t *entry = nullptr;
+      int blk = -1;
+      bool valid = false;
+      if (e < entries) {
+        const int layer = static_cast<int>(e / nb);
+        const int jj = static_cast<int>(e % nb);
+        entry = p.block_table + table_row(s, p.n_layers, layer, p.max_blocks) + jj;
+        blk = *entry;
+        valid = blk >= 0 && blk < p.num_blocks;
+      }
+      int chunk = 0;
+      const int rank = cta_exclusive_count(valid, tot, &chunk);
+      if (entry) {
+        if (!valid) {
+          report(p.err, PA_DEV_BAD_BLOCK);
+          *entry = -1;
+        } else {
+          const long long at = static_cast<long long>(fc0) + pushed + rank;
+          if (at < p.num_blocks) {
+            p.free_list[at] = blk;
+            *entry = -1;
+          } else {
+            report(p.err, PA_DEV_FREE_OVERFLOW);
+          }
+        }
+      }
+      pushed += chunk;
+    }
+  }
+  if (threadIdx.x == 0) {
+    const long long n = static_cast<long long>(fc0) + pushed;
+    *p.free_count = fc0 >= p.num_blocks ? fc0 : static_cast<int>(min(n, static_cast<long long>(p.num_blocks)));
+  }
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                                 uint16_t *q_or_null, uint16_t *kv_cache, int num_blocks,
+                                 int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int num_seqs, int layer,
+                                 int32_t *free_list, int32_t *free_count, int32_t *err,
+                                 void *stream) {
+  if (num_seqs < 0 || num_blocks <= 0 || n_layers <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_new || !v_new || !kv_cache || !block_table || !context_lens || !free_list ||
+      !free_count || !err)
+    return PA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kv_cache) ||
+      (q_or_null && !aligned16(q_or_null)))
+    return PA_ERR_ALIGN;
+  DeviceInfo di;
+  const int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+
+  AppendParams prm;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.q = q_or_null;
+  prm.kv = reinterpret_cast<unsigned char *>(kv_cache);
+  prm.block_table = block_table;
+  prm.context_lens = context_lens;
+  prm.free_list = free_list;
+  prm.free_count = free_count;
+  prm.err = err;
+  prm.num_blocks = num_blocks;
+  prm.n_layers = n_layers;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_seqs = num_seqs;
+  prm.layer = layer;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  append_alloc_kernel<<<1, kScanCta, 0, st>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pdl(append_store_kernel, dim3(num_seqs), dim3(kStoreThreads), 0, st, prm) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_layers,
+                       int max_blocks_per_seq, const int32_t *context_lens, int32_t *free_list,
+                       int32_t *free_count, int num_blocks, int32_t *err, void *stream) {
+  if (n_free < 0 || num_blocks <= 0 || n_layers <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (n_free == 0) return PA_OK;
+  if (!seq_ids || !block_table || !context_lens || !free_list || !free_count || !err)
+    return PA_ERR_NULL;
+  DeviceInfo di;
+  const int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  FreeParams prm;
+  prm.seq_ids = seq_ids;
+  prm.block_table = block_table;
+  prm.context_lens = context_lens;
+  prm.free_list = free_list;
+  prm.free_count = free_count;
+  prm.err = err;
+  prm.n_free = n_free;
+  prm.n_layers = n_layers;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_blocks = num_blocks;
+  free_kernel<<<1, kScanCta, 0, static_cast<cudaStream_t>(stream)>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" const char *pa_error_string(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_ARG: return "a size or count is out of range";
+    case PA_ERR_LAYER: return "layer outside [0, n_layers)";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case PA_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case PA_ERR_DEVICE: return "no usable sm_103 device";
+    default: return "unknown error";
+  }
+}

@@ -1,0 +1,47 @@
+// pa_host.h -- host-side helpers shared by the library's translation units:
+// per-device attribute cache, argument checks and launch with programmatic
+// dependent launch.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <utility>
+
+#include "../../include/pagedkv.h"
+
+namespace pa {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int major = 0;
+  int minor = 0;
+};
+
+// Current device's attributes (cached per device).  Returns PA_OK,
+// PA_ERR_CUDA or PA_ERR_DEVICE (not an sm_103 GPU).
+int current_device(DeviceInfo *info);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch `kernel` with the programmatic-stream-serialization attribute, so it
+// may start while the previous kernel on the stream finishes; the kernel
+// itself must wait (griddepcontrol.wait) before reading that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pa

@@ -1,0 +1,47 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry
+point include/pagedkv.h declares (no compute calls here)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*(pa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("pa_kv_append_rope", "pa_decode_attention", "pa_decode_workspace_size", "pa_free"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    import paged_kv_cache_205_gb300 as pk
+    lib = pk.library()
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert pk.pa_error_string(-4).startswith("workspace")
+
+
+def test_host_validation_without_a_device():
+    """Argument checks run before any CUDA call: bad sizes and layers are
+    refused with their codes even on a machine without a GPU."""
+    import ctypes
+    import paged_kv_cache_205_gb300 as pk
+    lib = pk.library()
+    P = ctypes.c_void_p
+    z = P(0)
+    assert lib.pa_decode_attention(z, z, z, 1, z, 2, 4, z, 3, 2, 0.125, z, 0, z, z) == -3
+    assert lib.pa_decode_attention(z, z, z, 1, z, 2, 4, z, -1, 0, 0.125, z, 0, z, z) == -2
+    assert lib.pa_decode_attention(z, z, z, 1, z, 2, 4, z, 0, 0, 0.125, z, 0, z, z) == 0
+    assert lib.pa_decode_attention(z, z, z, 1, z, 2, 4, z, 3, 0, 0.125, z, 0, z, z) == -1
+    assert lib.pa_kv_append_rope(z, z, z, z, 8, z, 1, 4, z, 2, 1, z, z, z, z) == -3
+    assert lib.pa_kv_append_rope(z, z, z, z, 8, z, 1, 4, z, 2, 0, z, z, z, z) == -1
+    assert lib.pa_free(z, 0, z, 1, 4, z, z, z, 8, z, z) == 0
+    assert lib.pa_free(z, 2, z, 1, 4, z, z, z, 8, z, z) == -1
+    assert lib.pa_decode_set_grid_limit(-1) == -2
+    assert lib.pa_decode_set_grid_limit(0) == 0

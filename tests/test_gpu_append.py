@@ -1,0 +1,214 @@
+"""GPU parity of pa_kv_append_rope and pa_free against the CPU oracle.
+
+Tables, free lists, free counts, V stores and untouched pool bytes must be
+bit-exact; rotated K and q within 1 bf16 ulp of the fp64 oracle (almost
+all exact).  Calls go through the C ABI.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import pa_workloads as wl
+from helpers import (assert_attention_close, dev_bf16, dev_i32, host_bits, host_f64,
+                     ulp_diff, workspace_for)
+
+pytestmark = pytest.mark.gpu
+
+N_Q, N_KV, D, BS = 32, 8, 64, 16
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "append_free_worked_example.json")
+
+
+def _pk():
+    import paged_kv_cache_205_gb300 as pk
+    return pk
+
+
+class DevState:
+    def __init__(self, pool, bt, fl, fc):
+        import torch
+        self.pool = dev_bf16(pool)
+        self.bt = dev_i32(bt)
+        self.fl = dev_i32(fl)
+        self.fc = dev_i32(np.array([fc]))
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def host(self):
+        import torch
+        torch.cuda.synchronize()
+        return (host_bits(self.pool), self.bt.cpu().numpy(), self.fl.cpu().numpy(),
+                int(self.fc.item()), int(self.err.item()))
+
+
+def _append(st, k, v, q, ctx, layer):
+    qd = None if q is None else dev_bf16(q)
+    _pk().pa_kv_append_rope(dev_bf16(k), dev_bf16(v), qd, st.pool, st.bt, dev_i32(ctx), layer,
+                            st.fl, st.fc, st.err)
+    return qd
+
+
+def _compare_pools(gpu_pool, ref_pool):
+    """V and untouched bytes exact, K within one ulp."""
+    same = gpu_pool == ref_pool
+    nan_both = (gpu_pool == wl.BF16_NAN) & (ref_pool == wl.BF16_NAN)
+    same |= nan_both
+    assert np.all(same[:, 1]), "V stores differ"
+    if not np.all(same[:, 0]):
+        d = ulp_diff(gpu_pool[:, 0], ref_pool[:, 0])
+        assert d.max() <= 1, f"K differs by {d.max()} ulp"
+        assert np.mean(d > 0) < 1e-2
+
+
+def test_worked_example_append_then_free():
+    g = json.load(open(GOLDEN))
+    rng = np.random.default_rng(0)
+    pool = wl.normal_bf16(rng, (g["num_blocks"], 2, BS, N_KV, D))
+    st = DevState(pool, np.array(g["block_table"]), np.array(g["free_list"]), g["free_count"])
+    ctx = np.array(g["append"]["context_lens"], dtype=np.int32)
+    n = len(ctx)
+    ref = (pool, np.array(g["block_table"], dtype=np.int32), np.array(g["free_list"], dtype=np.int32),
+           g["free_count"])
+    for layer in g["append"]["layers"]:
+        k = wl.normal_bf16(rng, (n, N_KV, D))
+        v = wl.normal_bf16(rng, (n, N_KV, D))
+        _append(st, k, v, None, ctx, layer)
+        _, p2, b2, f2, c2, e = oracle.kv_append_rope(k, v, None, ref[0], ref[1], ctx, layer, ref[2], ref[3])
+        assert e == 0
+        ref = (p2, b2, f2, c2)
+    gp, gb, gf, gc, ge = st.host()
+    assert ge == 0
+    assert np.array_equal(gb, np.array(g["append"]["expect_block_table"]))
+    assert np.array_equal(gb, ref[1]) and np.array_equal(gf, ref[2]) and gc == ref[3]
+    assert gc == g["append"]["expect_free_count"]
+    _compare_pools(gp, ref[0])
+
+    f = g["free"]
+    _pk().pa_free(dev_i32(f["seq_ids"]), st.bt, dev_i32(f["context_lens"]), st.fl, st.fc,
+                  g["num_blocks"], st.err)
+    _, gb, gf, gc, ge = st.host()
+    assert ge == f["expect_err"]
+    assert np.array_equal(gb, np.array(f["expect_block_table"]))
+    assert gc == f["expect_free_count"]
+    assert list(gf[:gc]) == f["expect_free_list_head"]
+
+
+def test_worked_example_underflow():
+    u = json.load(open(GOLDEN))["underflow"]
+    rng = np.random.default_rng(1)
+    pool = wl.normal_bf16(rng, (u["num_blocks"], 2, BS, N_KV, D))
+    st = DevState(pool, np.array(u["block_table"]), np.array(u["free_list"]), u["free_count"])
+    n = len(u["context_lens"])
+    k = wl.normal_bf16(rng, (n, N_KV, D))
+    v = wl.normal_bf16(rng, (n, N_KV, D))
+    _append(st, k, v, None, np.array(u["context_lens"]), 0)
+    gp, gb, gf, gc, ge = st.host()
+    assert ge == u["expect_err"]
+    assert np.array_equal(gb, np.array(u["expect_block_table"]))
+    assert gc == u["expect_free_count"]
+    _, p2, b2, _, c2, e2 = oracle.kv_append_rope(k, v, None, pool, np.array(u["block_table"]),
+                                                 u["context_lens"], 0, u["free_list"], u["free_count"])
+    assert e2 == ge and np.array_equal(b2, gb) and c2 == gc
+    _compare_pools(gp, p2)
+
+
+@pytest.mark.parametrize("seed,positions", [
+    (1, [0, 1, 15, 16, 17, 31, 32, 100, 2047, 2048, 8191, 8192]),
+    (2, list(range(0, 64))),
+    (3, [32767, 32768 - 16, 5000, 0]),
+])
+def test_append_with_q_matches_oracle(seed, positions):
+    rng = np.random.default_rng(seed)
+    ctx = np.array(positions, dtype=np.int32)
+    n = len(ctx)
+    n_layers = 2
+    mb = int(ctx.max()) // BS + 2
+    nbk = int(((ctx + 15) // 16).sum()) * n_layers + 2 * n + 5
+    w = wl.make_workload("tiny", seed=seed, context_lens=ctx, n_layers=n_layers, num_blocks=nbk,
+                         max_blocks_per_seq=mb)
+    pool = wl.make_pool_numpy(w, rng, poison=True)
+    st = DevState(pool, w.block_table, w.free_list, w.free_count)
+    ref = (pool, w.block_table, w.free_list, w.free_count)
+    for layer in range(n_layers):
+        k = wl.normal_bf16(rng, (n, N_KV, D))
+        v = wl.normal_bf16(rng, (n, N_KV, D))
+        q = wl.normal_bf16(rng, (n, N_Q, D))
+        qd = _append(st, k, v, q, ctx, layer)
+        q2, p2, b2, f2, c2, e = oracle.kv_append_rope(k, v, q, ref[0], ref[1], ctx, layer, ref[2], ref[3])
+        assert e == 0
+        ref = (p2, b2, f2, c2)
+        dq = ulp_diff(host_bits(qd), q2)
+        assert dq.max() <= 1 and np.mean(dq > 0) < 1e-2
+    gp, gb, gf, gc, ge = st.host()
+    assert ge == 0
+    assert np.array_equal(gb, ref[1]) and np.array_equal(gf, ref[2]) and gc == ref[3]
+    _compare_pools(gp, ref[0])
+
+
+def test_capacity_and_bad_entry_errors_match_oracle():
+    rng = np.random.default_rng(4)
+    w = wl.make_workload("tiny", context_lens=[64, 3, 20], max_blocks_per_seq=4)
+    pool = wl.make_pool_numpy(w, rng)
+    bt = w.block_table.copy()
+    bt[2, 0, 1] = -1                      # existing page of seq 2 is missing
+    st = DevState(pool, bt, w.free_list, w.free_count)
+    k = wl.normal_bf16(rng, (3, N_KV, D))
+    v = wl.normal_bf16(rng, (3, N_KV, D))
+    q = wl.normal_bf16(rng, (3, N_Q, D))
+    qd = _append(st, k, v, q, w.context_lens, 0)
+    gp, gb, gf, gc, ge = st.host()
+    q2, p2, b2, f2, c2, e2 = oracle.kv_append_rope(k, v, q, pool, bt, w.context_lens, 0,
+                                                   w.free_list, w.free_count)
+    assert ge == e2 == (oracle.ERR_CTX_RANGE | oracle.ERR_BAD_BLOCK)
+    assert np.array_equal(gb, b2) and gc == c2
+    _compare_pools(gp, p2)
+    assert ulp_diff(host_bits(qd)[1:], q2[1:]).max() <= 1
+    assert np.array_equal(host_bits(qd)[0], q[0])      # out-of-range position: q untouched
+
+
+def test_free_matches_oracle_with_overflow_and_bad_entries():
+    bt = np.array([[[0, 1, -1]], [[2, -1, -1]], [[5, 6, 7]]], dtype=np.int32)
+    fl = np.array([3, 4, -1, -1, -1, -1, -1, -1], dtype=np.int32)
+    ctx = np.array([20, 10, 48], dtype=np.int32)
+    for ids, fc, nbk in (([0, 1], 2, 8), ([2, 0], 6, 8), ([1, 2, 0], 2, 8)):
+        st = DevState(np.zeros((nbk, 2, BS, N_KV, D), np.uint16), bt, fl, fc)
+        _pk().pa_free(dev_i32(ids), st.bt, dev_i32(ctx), st.fl, st.fc, nbk, st.err)
+        _, gb, gf, gc, ge = st.host()
+        b2, f2, c2, e2 = oracle.free(ids, bt, ctx, fl, fc, nbk)
+        assert ge == e2 and gc == c2
+        assert np.array_equal(gb, b2) and np.array_equal(gf, f2)
+
+
+def test_decode_step_append_then_attention_over_new_token():
+    """Ragged continuous-batching step at small scale: each layer appends the
+    token at pos = ctx (RoPE on k and q), then attends over ctx + 1."""
+    import torch
+    pk = _pk()
+    rng = np.random.default_rng(6)
+    w = wl.make_workload("ragged", seed=6, num_seqs=24, max_ctx=300, n_layers=3, num_blocks=2000)
+    pool = wl.make_pool_numpy(w, rng, poison=True)
+    st = DevState(pool, w.block_table, w.free_list, w.free_count)
+    ref = (pool, w.block_table, w.free_list, w.free_count)
+    n = w.num_seqs
+    out = torch.empty((n, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    ws = workspace_for(n, w.max_blocks_per_seq)
+    ctx_attn = dev_i32(w.context_lens + 1)
+    for layer in range(w.n_layers):
+        k = wl.normal_bf16(rng, (n, N_KV, D))
+        v = wl.normal_bf16(rng, (n, N_KV, D))
+        q = wl.normal_bf16(rng, (n, N_Q, D))
+        qd = _append(st, k, v, q, w.context_lens, layer)
+        pk.pa_decode_attention(out, qd, st.pool, st.bt, ctx_attn, layer, w.scale, ws, st.err)
+        q2, p2, b2, f2, c2, e = oracle.kv_append_rope(k, v, q, ref[0], ref[1], w.context_lens,
+                                                      layer, ref[2], ref[3])
+        assert e == 0
+        ref = (p2, b2, f2, c2)
+        torch.cuda.synchronize()
+        o_ref, e = oracle.decode_attention(q2, p2, b2, w.context_lens + 1, layer)
+        assert e == 0
+        assert_attention_close(host_f64(out), o_ref, f"layer {layer}")
+    gp, gb, gf, gc, ge = st.host()
+    assert ge == 0
+    assert np.array_equal(gb, ref[1]) and np.array_equal(gf, ref[2]) and gc == ref[3]
+    _compare_pools(gp, ref[0])

@@ -1,0 +1,223 @@
+"""GPU parity of pa_decode_attention against the fp64 CPU oracle.
+
+Every call goes through the C ABI (libpagedkv.so via ctypes).  Tolerance
+(bf16 output vs fp64 oracle): max abs error <= 1e-2, mean abs <= 1e-3.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import pa_workloads as wl
+from helpers import (assert_attention_close, dev_bf16, dev_i32, gather_for_oracle,
+                     host_f64, workspace_for)
+
+pytestmark = pytest.mark.gpu
+
+N_Q, N_KV, D = 32, 8, 64
+
+
+def _pk():
+    import paged_kv_cache_205_gb300 as pk
+    return pk
+
+
+@pytest.fixture(autouse=True)
+def _reset_grid():
+    pk = _pk()
+    pk.pa_decode_set_grid_limit(0)
+    yield
+    pk.pa_decode_set_grid_limit(0)
+
+
+def _run_gpu(q_bits, pool_bits, bt, ctx, layer, scale=0.125, grid=0, pool_dev=None, num_seqs=None):
+    import torch
+    pk = _pk()
+    pk.pa_decode_set_grid_limit(grid)
+    n = bt.shape[0] if num_seqs is None else num_seqs
+    q = dev_bf16(q_bits)
+    pool = dev_bf16(pool_bits) if pool_dev is None else pool_dev
+    btd = dev_i32(bt)
+    ctxd = dev_i32(ctx)
+    out = torch.full((max(n, 1), N_Q, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(max(n, 1), bt.shape[2])
+    pk.pa_decode_attention(out, q, pool, btd, ctxd, layer, scale, ws, err, num_seqs=n)
+    torch.cuda.synchronize()
+    return host_f64(out), int(err.item())
+
+
+def _small_case(seed, ctx, n_layers=1, q_scale=1.0, extra_blocks=8):
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx, dtype=np.int32)
+    nbk = int(((ctx + 15) // 16).sum()) * n_layers + extra_blocks
+    mb = int(max(1, ((ctx + 15) // 16).max())) + 1
+    w = wl.make_workload("tiny", seed=seed, context_lens=ctx, n_layers=n_layers,
+                         num_blocks=nbk, max_blocks_per_seq=mb)
+    pool = wl.make_pool_numpy(w, rng, poison=True)
+    q = wl.normal_bf16(rng, (len(ctx), N_Q, D), scale=q_scale)
+    return w, pool, q
+
+
+def test_tiny_workload_matches_oracle():
+    """Two sequences with contexts 17 and 14 over a 64-block pool."""
+    w = wl.make_workload("tiny")
+    rng = np.random.default_rng(100)
+    pool = wl.make_pool_numpy(w, rng, poison=True)
+    q = wl.normal_bf16(rng, (w.num_seqs, N_Q, D))
+    ref, e_ref = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    assert err == 0 and e_ref == 0
+    assert_attention_close(out, ref, "tiny")
+
+
+@pytest.mark.parametrize("grid", [0, 1, 2, 3, 7, 64])
+def test_split_count_does_not_change_result(grid):
+    """The same inputs cut across 1..many CTAs (1 = no split) all match."""
+    w, pool, q = _small_case(7, [1, 15, 16, 17, 100, 250, 33, 64], q_scale=2.0)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, grid=grid)
+    assert err == 0
+    assert_attention_close(out, ref, f"grid={grid}")
+
+
+@pytest.mark.parametrize("ctx", [[1], [16], [17], [31, 32, 33], [0, 5], [0], [0, 0, 40, 0],
+                                 [2047, 1], [4096]])
+def test_edge_contexts(ctx):
+    w, pool, q = _small_case(len(ctx) * 13 + sum(ctx), ctx)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    assert err == 0
+    assert_attention_close(out, ref, f"ctx={ctx}")
+    for s, t in enumerate(ctx):
+        if t == 0:
+            assert np.all(out[s] == 0.0)
+
+
+def test_many_sequences_ragged_and_layers():
+    rng = np.random.default_rng(5)
+    ctx = rng.integers(0, 400, size=40)
+    w, pool, q = _small_case(21, ctx, n_layers=3)
+    for layer in range(3):
+        ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, layer)
+        out, err = _run_gpu(q, pool, w.block_table, w.context_lens, layer)
+        assert err == 0
+        assert_attention_close(out, ref, f"layer {layer}")
+
+
+def test_peaked_softmax_q_times_four():
+    w, pool, q = _small_case(9, [300, 1000, 77], q_scale=4.0)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, grid=5)
+    assert err == 0
+    assert_attention_close(out, ref, "peaked")
+
+
+def test_constant_value_per_kv_head_fixes_gqa_mapping():
+    w, pool, q = _small_case(10, [50, 3])
+    for g in range(N_KV):
+        pool[:, 1, :, g, :] = wl.to_bf16_bits(np.full((), g + 1.0, dtype=np.float32))
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    assert err == 0
+    for h in range(N_Q):
+        assert np.all(out[:, h] == h // 4 + 1.0)
+
+
+def test_non_default_scale():
+    w, pool, q = _small_case(11, [64, 9])
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0, scale=0.3)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, scale=0.3)
+    assert err == 0
+    assert_attention_close(out, ref, "scale 0.3")
+
+
+def test_fewer_sequences_than_table_rows():
+    w, pool, q = _small_case(12, [40, 20, 10])
+    ref, _ = oracle.decode_attention(q[:2], pool, w.block_table[:2], w.context_lens[:2], 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, num_seqs=2)
+    assert err == 0
+    assert_attention_close(out[:2], ref, "num_seqs=2")
+
+
+def test_zero_sequences_is_a_no_op():
+    w, pool, q = _small_case(13, [5])
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, num_seqs=0)
+    assert err == 0 and np.all(np.isnan(out))
+
+
+def test_device_errors_are_reported_not_trapped():
+    import torch
+    w, pool, q = _small_case(14, [40, 20])
+    bt = w.block_table.copy()
+    bt[0, 0, 1] = -1
+    _, err = _run_gpu(q, pool, bt, w.context_lens, 0)
+    assert err & _pk().PA_DEV_BAD_BLOCK
+    bt = w.block_table.copy()
+    bt[1, 0, 0] = w.num_blocks + 5
+    _, err = _run_gpu(q, pool, bt, w.context_lens, 0)
+    assert err & _pk().PA_DEV_BAD_BLOCK
+    ctx = w.context_lens.copy()
+    ctx[1] = w.max_blocks_per_seq * 16 + 3
+    _, err = _run_gpu(q, pool, w.block_table, ctx, 0)
+    assert err & _pk().PA_DEV_CTX_RANGE
+    # the context stays usable
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    assert err == 0
+    assert_attention_close(out, ref, "after errors")
+    torch.cuda.synchronize()
+
+
+def test_host_argument_errors():
+    import torch
+    pk = _pk()
+    w, pool, q = _small_case(15, [20])
+    qd, poold, btd, ctxd = dev_bf16(q), dev_bf16(pool), dev_i32(w.block_table), dev_i32(w.context_lens)
+    out = torch.empty((1, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(1, w.max_blocks_per_seq)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_decode_attention(out, qd, poold, btd, ctxd, 1, 0.125, ws, err)
+    assert e.value.code == -3
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_decode_attention(out, qd, poold, btd, ctxd, 0, 0.125, ws[:16], err)
+    assert e.value.code == -4
+    flat = torch.empty(N_Q * D + 1, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_decode_attention(flat[1:].view(1, N_Q, D), qd, poold, btd, ctxd, 0, 0.125, ws, err)
+    assert e.value.code == -5
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times:
+# device pools drawn by torch, oracle on a sample of sequences.
+FULL = [("llama1b", [0, 7, 15]), ("pool2g", [0, 31, 63]), ("long32k", [1]), ("ragged", None)]
+
+
+@pytest.mark.parametrize("name,sample", FULL)
+def test_full_size_workload_sampled(name, sample):
+    import torch
+    pk = _pk()
+    w = wl.make_workload(name)
+    pool = wl.make_pool_torch(w, "cuda", seed=w.seed)
+    ctx = w.attn_context_lens if name != "ragged" else w.context_lens
+    rng = np.random.default_rng(w.seed + 1000)
+    q = wl.normal_bf16(rng, (w.num_seqs, N_Q, D), scale=w.q_scale)
+    if sample is None:   # ragged: shortest, longest and a few in between
+        order = np.argsort(ctx)
+        sample = sorted({int(order[0]), int(order[-1]), *rng.choice(w.num_seqs, 4, replace=False).tolist()})
+    qd, btd, ctxd = dev_bf16(q), dev_i32(w.block_table), dev_i32(ctx)
+    out = torch.empty((w.num_seqs, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(w.num_seqs, w.max_blocks_per_seq)
+    for layer in (0, w.n_layers - 1):
+        pk.pa_decode_attention(out, qd, pool, btd, ctxd, layer, w.scale, ws, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = host_f64(out)
+        assert np.all(np.isfinite(got))
+        sub, bt = gather_for_oracle(pool, w.block_table, sample, ctx, layer)
+        ref, e = oracle.decode_attention(q[sample], sub, bt, ctx[sample], 0, scale=w.scale)
+        assert e == 0
+        assert_attention_close(got[sample], ref, f"{name} layer {layer}")
+    del pool
+    torch.cuda.empty_cache()
