@@ -1,0 +1,530 @@
+#!/usr/bin/env python3
+"""Benchmark of the PagedAttention decode step (C ABI, GB300).
+
+One step = the whole hot path over one batch: for each of the 16 layers,
+(ragged workload only: pa_kv_append_rope of the new token, then)
+pa_decode_attention.  Inputs live in HBM before the timed region.  Prints
+one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Workloads (pa_workloads): llama1b (default: 16 layers, 16 sequences, context
+U[256, 2048]), pool2g, long32k, ragged, tiny.
+
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (the path shards by sequence with no exchange); `value` is the
+throughput summed over ranks, timed as the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import pa_workloads as wl  # noqa: E402
+
+METRIC = "decode-attention HBM GB/s and % of GB300 peak; sequence-steps/sec"
+N_Q, N_KV, D, BS = 32, 8, 64, 16
+DESCRIPTIONS = {
+    "tiny": "1 layer, 2 sequences with contexts 17 and 14, 64-block pool",
+    "llama1b": "Llama-3.2-1B decode: 16 layers, 16 sequences, context U[256,2048], "
+               "65,536-block pool, 32/8 heads, head_dim 64, 16-token bf16 blocks",
+    "pool2g": "2 GiB pool (65,536 blocks), 16 layers, 64 sequences x 4096, per-layer random "
+              "16,384-block subsets",
+    "long32k": "16 layers, 4 sequences x 32,768, 131,072-block pool, q x4",
+    "ragged": "continuous batching: 256 sequences, context log-U[1,8192], 262,144-block pool; "
+              "per layer append (RoPE, pos = ctx) then attention over ctx+1",
+}
+
+
+# ------------------------------------------------------------ byte counts
+def attention_bytes(ctx: np.ndarray) -> int:
+    """Algorithmic HBM bytes of one decode-attention call: K and V of every
+    context token (2048 B per token over 8 kv heads), q and out (4096 B each
+    per sequence), the block ids read and the context lengths."""
+    ctx = ctx.astype(np.int64)
+    return int(ctx.sum() * 2048 + len(ctx) * (4096 + 4096) + ((ctx + 15) // 16).sum() * 4
+               + len(ctx) * 4)
+
+
+def append_bytes(n: int) -> int:
+    """Algorithmic bytes of one append call with q: k_new, v_new read (1 KiB
+    each), K and V written (1 KiB each), q read and written (4 KiB each),
+    table entry and context length."""
+    return n * (1024 * 4 + 4096 * 2 + 8)
+
+
+# --------------------------------------------------------- clock sampling
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.marking = False
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append((self.marking, parts))
+
+    def mark(self, on: bool):
+        self.marking = on
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [p for m, p in self.rows if m] or [p for _, p in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- roofline
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_205_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, valid only
+    while the kernel source hash recorded there matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"decode_split_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    mh = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
+    mt = re.search(r"dram bytes per launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash():
+        return None
+    return float(mt.group(1))
+
+
+# ------------------------------------------------- oracle (CPU baseline)
+def oracle_unit(w: wl.Workload, s: int, layer: int, rng, max_tokens=None):
+    """Host inputs of one (sequence, layer) of the workload, drawn with the
+    same distributions, for the oracle: a compact pool holding only that
+    sequence's blocks in a shuffled order."""
+    ctx = int(w.attn_context_lens[s])
+    if max_tokens is not None:
+        ctx = max(1, min(ctx, int(max_tokens)))
+    nb = (ctx + BS - 1) // BS + 1
+    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    bt = np.full((1, 1, nb), -1, dtype=np.int32)
+    bt[0, 0, :] = rng.permutation(nb).astype(np.int32)
+    q = wl.normal_bf16(rng, (1, N_Q, D), scale=w.q_scale)
+    k = wl.normal_bf16(rng, (1, N_KV, D))
+    v = wl.normal_bf16(rng, (1, N_KV, D))
+    fl = np.zeros(4, dtype=np.int32)
+    return dict(q=q, pool=pool, bt=bt, ctx=ctx, k=k, v=v, fl=fl)
+
+
+def oracle_run_unit(u, w: wl.Workload):
+    """One unit through the oracle: append (ragged) then attention.  Returns
+    the algorithmic bytes it stands for."""
+    import oracle
+    ctx = u["ctx"]
+    if w.append:
+        pos = ctx - 1   # the unit's context includes the appended token
+        bt = u["bt"].copy()
+        # the new token's page exists already unless it starts one
+        oracle.kv_append_rope(u["k"], u["v"], u["q"], u["pool"], bt, np.array([pos]), 0,
+                              u["fl"], 1 if pos % BS == 0 else 0)
+        oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale)
+        return attention_bytes(np.array([ctx])) + append_bytes(1)
+    oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale)
+    return attention_bytes(np.array([ctx]))
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0):
+    """The oracle, single-threaded, over whole (sequence, layer) units of one
+    step until the budget is spent."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(w.seed + 77)
+    units = [(s, l) for l in range(w.n_layers) for s in range(w.num_seqs)]
+    t_total, nbytes, done = 0.0, 0, 0
+    for s, l in units:
+        u = oracle_unit(w, s, l, rng)
+        t0 = time.perf_counter()
+        nbytes += oracle_run_unit(u, w)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total > budget_s:
+            break
+    seq_layers_per_s = done / t_total
+    return {
+        "value": nbytes / t_total / 1e9,
+        "unit": "GB/s",
+        "seq_steps_per_s": seq_layers_per_s / w.n_layers,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"{done} of {len(units)} (sequence, layer) units of one step "
+                  f"({done / len(units):.0%}), {t_total:.1f} s, single-threaded C, fp64",
+        "host_cores": os.cpu_count(),
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.make_workload(args.workload)
+    rng = np.random.default_rng(w.seed + 91)
+    # size each step so the whole run stays within a few minutes
+    per_step_budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
+    probe = oracle_unit(w, 0, 0, rng, max_tokens=256)
+    t0 = time.perf_counter()
+    oracle_run_unit(probe, w)
+    tok_rate = probe["ctx"] / max(time.perf_counter() - t0, 1e-6)
+    max_tokens = max(16, int(per_step_budget * tok_rate))
+    units = [(s, l) for l in range(w.n_layers) for s in range(w.num_seqs)]
+    for i in range(args.warmup):
+        s, l = units[i % len(units)]
+        oracle_run_unit(oracle_unit(w, s, l, rng, max_tokens), w)
+    t_total, nbytes, seq_layers = 0.0, 0, 0
+    for i in range(args.steps):
+        s, l = units[i % len(units)]
+        u = oracle_unit(w, s, l, rng, max_tokens)
+        t0 = time.perf_counter()
+        nbytes += oracle_run_unit(u, w)
+        t_total += time.perf_counter() - t0
+        seq_layers += 1
+    gbs = nbytes / t_total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": gbs,
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "sample_per_step": f"one (sequence, layer) unit, context capped at {max_tokens} tokens"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} units, one per step, single-threaded C (fp64)",
+                         "host_cores": os.cpu_count()},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------- GPU arm
+class DeviceStep:
+    """Device-resident state of one workload and the step over it."""
+
+    def __init__(self, w: wl.Workload, seed: int):
+        import torch
+        import paged_kv_cache_205_gb300 as pk
+        self.pk = pk
+        self.w = w
+        dev = torch.device("cuda")
+        L, n = w.n_layers, w.num_seqs
+        self.pool = wl.make_pool_torch(w, dev, seed=seed, poison=True)
+        self.bt = torch.from_numpy(w.block_table).to(dev)
+        self.ctx_host = w.context_lens.astype(np.int32)
+        self.ctx = torch.from_numpy(self.ctx_host).to(dev)
+        self.ctx_attn = torch.from_numpy(w.attn_context_lens).to(dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 1)
+        self.q = (torch.randn((L, n, N_Q, D), generator=g, device=dev) * w.q_scale).to(torch.bfloat16)
+        self.out = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(pk.pa_decode_workspace_size(n, w.max_blocks_per_seq),
+                              dtype=torch.uint8, device=dev)
+        if w.append:
+            self.k_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+            self.v_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+            self.fl = torch.from_numpy(w.free_list).to(dev)
+            self.fc0 = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
+            self.fc = self.fc0.clone()
+        self.launches_per_step = L * (2 + (2 if w.append else 0)) + (1 if w.append else 0)
+
+    def layer(self, l, q=None, out=None):
+        pk, w = self.pk, self.w
+        q = self.q[l] if q is None else q
+        out = self.out[l] if out is None else out
+        if w.append:
+            pk.pa_kv_append_rope(self.k_new[l], self.v_new[l], q, self.pool, self.bt, self.ctx, l,
+                                 self.fl, self.fc, self.err)
+        pk.pa_decode_attention(out, q, self.pool, self.bt, self.ctx_attn, l, w.scale, self.ws,
+                               self.err)
+
+    def step(self):
+        if self.w.append:
+            # every step allocates the same pages again: the free count is
+            # restored first (steady state: blocks recycled between steps)
+            self.fc.copy_(self.fc0)
+        for l in range(self.w.n_layers):
+            self.layer(l)
+
+    def bytes_per_step(self) -> int:
+        b = attention_bytes(self.w.attn_context_lens) * self.w.n_layers
+        if self.w.append:
+            b += append_bytes(self.w.num_seqs) * self.w.n_layers
+        return b
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = wl.make_workload(args.workload)
+    st = DeviceStep(w, seed=w.seed + 1000 * rank)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    if int(st.err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(st.err.item())} during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if int(st.err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(st.err.item())} in the timed region")
+
+    # dominant kernel: decode attention per launch, CUDA events on its stream
+    k_roof = min(args.steps, 200)
+    evs = []
+    for _ in range(k_roof):
+        if w.append:
+            st.fc.copy_(st.fc0)
+        for l in range(w.n_layers):
+            if w.append:
+                st.pk.pa_kv_append_rope(st.k_new[l], st.v_new[l], st.q[l], st.pool, st.bt, st.ctx,
+                                        l, st.fl, st.fc, st.err)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            st.pk.pa_decode_attention(st.out[l], st.q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
+                                      st.ws, st.err)
+            b.record(stream)
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # end to end: inputs from pinned host memory each step, result read back
+    L, n = w.n_layers, w.num_seqs
+    h_q = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16).pin_memory()
+    h_q.copy_(st.q.cpu())
+    h_ctx = torch.from_numpy(w.attn_context_lens.copy()).pin_memory()
+    h_out = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16).pin_memory()
+    d_q = torch.empty_like(st.q)
+    h_kv = None
+    if w.append:
+        h_kv = (st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(),
+                torch.from_numpy(st.ctx_host.copy()).pin_memory())
+        d_k, d_v = torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+    k_e2e = min(args.steps, 500)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        st.ctx_attn.copy_(h_ctx, non_blocking=True)
+        if w.append:
+            d_k.copy_(h_kv[0], non_blocking=True)
+            d_v.copy_(h_kv[1], non_blocking=True)
+            st.ctx.copy_(h_kv[2], non_blocking=True)
+            st.fc.copy_(st.fc0)
+        for l in range(L):
+            if w.append:
+                st.pk.pa_kv_append_rope(d_k[l], d_v[l], d_q[l], st.pool, st.bt, st.ctx, l, st.fl,
+                                        st.fc, st.err)
+            st.pk.pa_decode_attention(st.out[l], d_q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
+                                      st.ws, st.err)
+        h_out.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / k_e2e
+    h2d = h_q.numel() * 2 + h_ctx.numel() * 4
+    if w.append:
+        h2d += h_kv[0].numel() * 2 + h_kv[1].numel() * 2 + h_kv[2].numel() * 4
+    d2h = h_out.numel() * 2
+
+    stats = torch.tensor([ms, e2e_s], dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
+    ms, e2e_s = float(stats[0]), float(stats[1])
+    sampler.stop()
+    if rank != 0:
+        return
+
+    bytes_step = st.bytes_per_step()
+    gbs = world * bytes_step / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    attn_bytes = attention_bytes(w.attn_context_lens)
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC,
+        "value": gbs,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accumulate": "fp32",
+        "data": "synthetic",
+        "pct_of_peak": 100.0 * gbs / (peak * world),
+        "seq_steps_per_s": world * w.num_seqs / (ms / 1e3),
+        "config": {
+            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+            "num_seqs": w.num_seqs,
+            "n_layers": w.n_layers,
+            "algorithmic_bytes_per_step": bytes_step,
+            "l2": "inputs larger than L2: each step reads "
+                  f"{bytes_step / 2**20:.0f} MiB of distinct K/V (L2 129 MB)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode_attention (decode_split_kernel + decode_merge_kernel)",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": profiled_traffic(args.workload),
+            "bytes_per_launch": attn_bytes,
+            "ms_per_launch": attn_ms,
+        },
+        "e2e": {
+            "value": world * bytes_step / e2e_s / 1e9,
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_s * 1e3,
+        },
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama1b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("gloo")
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

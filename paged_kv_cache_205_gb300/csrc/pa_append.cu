@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) 
   pdl_launch_dependents();   // the store kernel may start its rotations now
   __shared__ int tot[kScanCta / 32];
   const int cap = p.max_blocks * kBs;
-  const int fc0 = *p.free_count;
+  // a count outside [0, num_blocks] never indexes past the free list
+  const int fc0 = min(max(*p.free_count, 0), p.num_blocks);
   int served = 0;
   for (int base = 0; base < p.num_seqs; base += kScanCta) {
     const int i = base + threadIdx.x;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kScanCta) free_kernel(FreeParams p) {
           *entry = -1;
         } else {
           const long long at = static_cast<long long>(fc0) + pushed + rank;
-          if (at < p.num_blocks) {
+          if (at >= 0 && at < p.num_blocks) {
             p.free_list[at] = blk;
             *entry = -1;
           } else {

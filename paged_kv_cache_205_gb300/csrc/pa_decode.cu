@@ -331,6 +331,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
       if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
         sm.desc[stage].flags = kEndOfWork;
         mbar_arrive(&sm.full[stage]);
+        // this arrive is now the stage's last phase; the copy before it on
+        // the same stage has completed, or the consumers could not have freed it
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       } else {
         report(p.err, PA_DEV_TIMEOUT);
       }
