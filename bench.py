@@ -305,7 +305,7 @@ class DeviceStep:
             self.fl = torch.from_numpy(w.free_list).to(dev)
             self.fc0 = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
             self.fc = self.fc0.clone()
-        self.launches_per_step = L * (2 + (2 if w.append else 0)) + (1 if w.append else 0)
+        self.launches_per_step = L * (2 + (2 if w.append else 0))
 
     def layer(self, l, q=None, out=None):
         pk, w = self.pk, self.w
@@ -338,17 +338,34 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.set_device(local)
     w = wl.make_workload(args.workload)
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
-    stream = torch.cuda.current_stream()
+    L, n = w.n_layers, w.num_seqs
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
-    for _ in range(args.warmup):
+    def check(where):
+        torch.cuda.synchronize()
+        if int(st.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(st.err.item())} {where}")
+
+    # eager warm-up (also sets the library's per-device attributes)
+    for _ in range(3):
         st.step()
-    torch.cuda.synchronize()
-    if int(st.err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(st.err.item())} during warm-up")
+    check("during eager warm-up")
+
+    # one step = one CUDA graph of the 16 layers' launches
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_step, stream=side):
+            st.step()
+    torch.cuda.current_stream().wait_stream(side)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g_step.replay()
+    check("during warm-up")
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -359,37 +376,39 @@ def run_gpu(args, rank, world, dist):
     sampler.mark(True)
     e0.record(stream)
     for _ in range(args.steps):
-        st.step()
+        g_step.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark(False)
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
-    if int(st.err.item()) != 0:
-        raise RuntimeError(f"device error bits {int(st.err.item())} in the timed region")
+    check("in the timed region")
 
-    # dominant kernel: decode attention per launch, CUDA events on its stream
-    k_roof = min(args.steps, 200)
-    evs = []
-    for _ in range(k_roof):
-        if w.append:
-            st.fc.copy_(st.fc0)
-        for l in range(w.n_layers):
-            if w.append:
-                st.pk.pa_kv_append_rope(st.k_new[l], st.v_new[l], st.q[l], st.pool, st.bt, st.ctx,
-                                        l, st.fl, st.fc, st.err)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            st.pk.pa_decode_attention(st.out[l], st.q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
-                                      st.ws, st.err)
-            b.record(stream)
-            evs.append((a, b))
+    # dominant kernel: the 16 decode-attention launches of a step alone,
+    # back to back in one graph, CUDA events on the replay stream
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_attn, stream=side):
+            for l in range(L):
+                st.pk.pa_decode_attention(st.out[l], st.q[l], st.pool, st.bt, st.ctx_attn, l,
+                                          w.scale, st.ws, st.err)
+    torch.cuda.current_stream().wait_stream(side)
+    k_roof = min(args.steps, 500)
+    for _ in range(3):
+        g_attn.replay()
     torch.cuda.synchronize()
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(k_roof):
+        g_attn.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / (k_roof * L)
+    check("in the roofline pass")
 
-    # end to end: inputs from pinned host memory each step, result read back
-    L, n = w.n_layers, w.num_seqs
+    # end to end: the step's inputs from pinned host memory, the step, the
+    # outputs back to pinned host memory -- captured as one graph
     h_q = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16).pin_memory()
     h_q.copy_(st.q.cpu())
     h_ctx = torch.from_numpy(w.attn_context_lens.copy()).pin_memory()
@@ -400,7 +419,6 @@ def run_gpu(args, rank, world, dist):
         h_kv = (st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(),
                 torch.from_numpy(st.ctx_host.copy()).pin_memory())
         d_k, d_v = torch.empty_like(st.k_new), torch.empty_like(st.v_new)
-    k_e2e = min(args.steps, 500)
 
     def e2e_step():
         d_q.copy_(h_q, non_blocking=True)
@@ -418,15 +436,22 @@ def run_gpu(args, rank, world, dist):
                                       st.ws, st.err)
         h_out.copy_(st.out, non_blocking=True)
 
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_e2e, stream=side):
+            e2e_step()
+    torch.cuda.current_stream().wait_stream(side)
+    k_e2e = min(args.steps, 500)
     for _ in range(3):
-        e2e_step()
+        g_e2e.replay()
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     for _ in range(k_e2e):
-        e2e_step()
+        g_e2e.replay()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / k_e2e
+    check("in the end-to-end pass")
     h2d = h_q.numel() * 2 + h_ctx.numel() * 4
     if w.append:
         h2d += h_kv[0].numel() * 2 + h_kv[1].numel() * 2 + h_kv[2].numel() * 4
@@ -469,6 +494,7 @@ def run_gpu(args, rank, world, dist):
             "algorithmic_bytes_per_step": bytes_step,
             "l2": "inputs larger than L2: each step reads "
                   f"{bytes_step / 2**20:.0f} MiB of distinct K/V (L2 129 MB)",
+            "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
@@ -482,6 +508,8 @@ def run_gpu(args, rank, world, dist):
             "traffic": profiled_traffic(args.workload),
             "bytes_per_launch": attn_bytes,
             "ms_per_launch": attn_ms,
+            "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "
+                      "replay stream",
         },
         "e2e": {
             "value": world * bytes_step / e2e_s / 1e9,
@@ -489,6 +517,8 @@ def run_gpu(args, rank, world, dist):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "ms_per_step": e2e_s * 1e3,
+            "how": "pinned H2D of the step inputs + the step + D2H of all outputs, one graph "
+                   "replay per step, host wall clock",
         },
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks,

@@ -192,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int c = blockIdx.x;
+  // everything this kernel reads may come from the previous kernel on the
+  // stream; with programmatic launch only the CTA start-up overlaps it
+  pdl_wait_primary();
 
   // ---- total number of blocks over all sequences ---------------------------
   long long mine = 0;
@@ -456,31 +459,73 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
 }
 
 // Combines the partials of every sequence split across CTAs.  Grid
-// (num_seqs, 8 kv heads), 128 threads: warp = q head of the group, lane =
-// 2 output dims.
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p) {
+// (num_seqs, 32 q heads), 256 threads.  All partials of one (sequence, head)
+// are loaded in parallel: first the maxima (one per thread), then the
+// weighted accumulators, 8 partials at a time across the warps.
+constexpr int kMergeThreads = 256;
+constexpr int kMaxParts = 1024;   // the grid never exceeds this many CTAs
+
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
   pdl_wait_primary();
+  __shared__ float wpart[kMaxParts];
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float2 osum[kMergeThreads / 32][32];
   const int s = blockIdx.x;
-  const int h = blockIdx.y * kGqa + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int2 mt = p.meta[s];
-  if (mt.y <= 1) return;
+  const int np = mt.y;
+  if (np <= 1) return;
   const size_t slot0 = static_cast<size_t>(mt.x);
-  float M = neg_inf();
-  for (int k = 0; k < mt.y; ++k) M = fmaxf(M, p.ml[(slot0 + k) * kHq + h].x);
-  float L = 0.f;
-  float2 O = make_float2(0.f, 0.f);
-  for (int k = 0; k < mt.y; ++k) {
+
+  float mloc = neg_inf();
+  for (int k = tid; k < np; k += kMergeThreads) mloc = fmaxf(mloc, p.ml[(slot0 + k) * kHq + h].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+  if (lane == 0) red[warp] = mloc;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+
+  float lloc = 0.f;
+  for (int k = tid; k < np; k += kMergeThreads) {
     const float2 mlk = p.ml[(slot0 + k) * kHq + h];
-    const float w = fast_exp2(mlk.x - M);
-    const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
-    L = fmaf(w, mlk.y, L);
-    O.x = fmaf(w, a.x, O.x);
-    O.y = fmaf(w, a.y, O.y);
+    const float wk = fast_exp2(mlk.x - M);
+    wpart[k] = wk;
+    lloc = fmaf(wk, mlk.y, lloc);
   }
-  const float inv = 1.f / L;
-  uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD);
-  dst[lane] = float2_to_bf16x2(O.x * inv, O.y * inv);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+  if (lane == 0) red[warp] = lloc;
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
+
+  float2 o = make_float2(0.f, 0.f);
+  constexpr int kGroups = kMergeThreads / 32;
+#pragma unroll 4
+  for (int k = warp; k < np; k += kGroups) {
+    const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
+    const float wk = wpart[k];
+    o.x = fmaf(wk, a.x, o.x);
+    o.y = fmaf(wk, a.y, o.y);
+  }
+  osum[warp][lane] = o;
+  __syncthreads();
+  if (warp == 0) {
+    float2 t = osum[0][lane];
+#pragma unroll
+    for (int w = 1; w < kGroups; ++w) {
+      t.x += osum[w][lane].x;
+      t.y += osum[w][lane].y;
+    }
+    const float inv = 1.f / L;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD);
+    dst[lane] = float2_to_bf16x2(t.x * inv, t.y * inv);
+  }
 }
 
 int g_grid_limit = 0;
@@ -504,6 +549,7 @@ int auto_grid(const DeviceInfo &di, int num_seqs, int max_blocks) {
   long long g = static_cast<long long>(di.sm_count) * kCtasPerSm;
   if (g_grid_limit > 0) g = min(g, static_cast<long long>(g_grid_limit));
   g = min(g, static_cast<long long>(num_seqs) * max_blocks);
+  g = min(g, static_cast<long long>(kMaxParts));
   return static_cast<int>(max(g, 1LL));
 }
 
@@ -601,9 +647,10 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   prm.qscale = scale * kLog2e;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  decode_split_kernel<<<G, kThreads, smem, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_pdl(decode_merge_kernel, dim3(num_seqs, kHkv), dim3(128), 0, st, prm) != cudaSuccess)
+  if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_pdl(decode_merge_kernel, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm) !=
+      cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
