@@ -297,8 +297,7 @@ class DeviceStep:
         self.q = (torch.randn((L, n, N_Q, D), generator=g, device=dev) * w.q_scale).to(torch.bfloat16)
         self.out = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(pk.pa_decode_workspace_size(n, w.max_blocks_per_seq),
-                              dtype=torch.uint8, device=dev)
+        self.ws = pk.decode_workspace(n, w.max_blocks_per_seq)
         if w.append:
             self.k_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
             self.v_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)

@@ -117,9 +117,12 @@ int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_
  * zero output.  Long contexts are split across CTAs and merged (split
  * context); the split only changes rounding.
  * workspace: device scratch of at least pa_decode_workspace_size(num_seqs,
- * max_blocks_per_seq) bytes, owned by the caller, contents need no
- * initialisation; calls that share one workspace must not overlap in time.
- * Device errors: PA_DEV_BAD_BLOCK (that token's contribution is dropped),
+ * max_blocks_per_seq) bytes, owned by the caller.  It must be zero-filled
+ * once before its first use (it holds the work counter that spreads blocks
+ * over CTAs); every call returns it to a state the next call accepts.
+ * Calls that share one workspace must not overlap in time.
+ * num_seqs is at most 2048 per call.
+ * Device errors: PA_DEV_BAD_BLOCK (that block's tokens are dropped),
  * PA_DEV_CTX_RANGE (context clamped), PA_DEV_TIMEOUT.
  */
 int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     PA_NUM_KV_HEADS,
     PA_NUM_Q_HEADS,
     PagedKVError,
+    decode_workspace,
     exported_symbols,
     library,
     library_path,

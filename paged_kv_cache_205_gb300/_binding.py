@@ -153,6 +153,14 @@ def pa_decode_workspace_size(num_seqs: int, max_blocks_per_seq: int) -> int:
     return int(library().pa_decode_workspace_size(int(num_seqs), int(max_blocks_per_seq)))
 
 
+def decode_workspace(num_seqs: int, max_blocks_per_seq: int, device=None):
+    """A zero-filled uint8 CUDA tensor of pa_decode_workspace_size bytes, the
+    state pa_decode_attention expects on first use."""
+    torch = _torch()
+    n = pa_decode_workspace_size(num_seqs, max_blocks_per_seq)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
 def pa_decode_attention(out, q, kv_cache, block_table, context_lens, layer, scale, workspace,
                         err, stream=None, num_seqs=None):
     """out/q [n][32][64] bf16; workspace: a CUDA uint8 tensor of at least

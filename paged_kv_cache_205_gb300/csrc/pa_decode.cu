@@ -3,29 +3,32 @@
 // Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "What is in
 // the box": pagedAttentionKernel computes one query token's attention over
 // K/V stored in 16-token pages found through block_table, with an online
-// softmax and __shfl_down_sync reductions; GQA_Q_TO_K_RATIO = 4.
+// softmax and warp-shuffle reductions; GQA_Q_TO_K_RATIO = 4.
 //
 // Design (GB300-first, not the page's kernel):
-//  * Work is balanced by BLOCKS, not by sequences: the blocks of all
-//    sequences are laid end to end and cut into gridDim.x equal ranges, one
-//    per CTA ("stream-K" style).  A sequence whose blocks span several CTAs
-//    gets one fp32 partial (m, l, acc) per CTA, merged by a second kernel
-//    (split-context / flash-decoding merge).  Any length mix keeps every SM
-//    busy.
-//  * One physical block (16 tokens x 8 kv heads x K,V = 32 KiB, contiguous)
-//    is fetched with ONE bulk async copy (TMA, non-tensor form) into a
-//    shared-memory stage; a producer warp keeps kStages copies in flight
-//    (mbarrier full/empty pipeline).  Each block is read from HBM once and
-//    serves all 8 kv heads; each kv head's slice serves its 4 q heads.
-//  * Eight consumer warps, one per kv head.  QK: lane (token t, dim quarter)
-//    does 16-dim dot products for 4 heads with packed fp32x2 FMAs, then a
-//    3-shuffle reduce-scatter leaves one (token, head) score per lane.  The
-//    online softmax keeps (m, l) per head in the log2 domain.  PV: lane owns
-//    2 output dims for all 4 heads, weights come from shared memory as one
-//    broadcast float4 per token.
+//  * Work is balanced by BLOCKS, not by sequences.  The blocks of all
+//    sequences are laid end to end and cut into chunks of C blocks; CTAs take
+//    chunks from an atomic counter (the first one is their own index), so a
+//    slow SM simply ends up with fewer chunks.  Every (chunk, sequence) piece
+//    leaves an fp32 partial (m, l, acc); a second kernel merges the partials
+//    of sequences that span several chunks (split-context merge).
+//  * A producer warp streams whole physical blocks (16 tokens x 8 kv heads x
+//    K,V = 32 KiB, one contiguous page) into a ring of shared-memory stages
+//    with TMA tensor copies, one 4 KiB copy per kv head; the 128-byte swizzle
+//    of the tensor map lays every head's [token][64] tile out so that the
+//    warps read it without bank conflicts.  Each block crosses HBM once.
+//  * Eight consumer warps, one per kv head.  The 4 query heads of a GQA group
+//    are the M rows of m16n8k16 bf16 tensor-core MMAs (rows 4..15 are zero):
+//    S = Q K^T and O += P V take 16 MMAs per block, fed by ldmatrix.  The
+//    online softmax runs on the S fragments in fp32 (log2 domain, 2 shuffles
+//    per block); P is rounded to bf16 for the PV MMA and l sums the rounded
+//    weights so numerator and denominator agree.
 #include <cfloat>
 #include <climits>
 #include <cstdio>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
@@ -38,48 +41,52 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;        // + producer warp
 constexpr int kStages = 3;
 constexpr int kCtasPerSm = 2;
 constexpr int kScanThreads = kConsumerWarps * 32;          // 256
+constexpr int kMaxSeqs = 2048;                             // block prefix kept in shared memory
+constexpr int kMaxGrid = 512;
+constexpr int kChunksPerCta = 4;                           // average chunks a CTA takes
+constexpr int kMaxParts = kChunksPerCta * kMaxGrid + 2;    // partials of one sequence, at most
+constexpr int kHeadTileBytes = 2 * kBs * kHeadRowBytes;    // K and V of one kv head: 4 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int kSegStart = 1;   // first block of this CTA's share of a sequence
-constexpr int kSegEnd = 2;     // last block of that share
-constexpr int kEndOfWork = 4;  // no more blocks; stage carries no data
+constexpr int kSegStart = 1;   // first block of a (chunk, sequence) piece
+constexpr int kSegEnd = 2;     // last block of that piece
+constexpr int kEndOfWork = 4;  // no more blocks; the stage carries no data
 
 struct StageDesc {
   int seq;
-  int n_valid;   // tokens of the block inside the context, 1..16
+  int n_valid;   // tokens of the block inside the context, 1..16 (negative: block skipped)
   int flags;
-  int n_parts;   // CTAs sharing this sequence
+  int n_parts;   // pieces the sequence is cut into
+  int slot;      // partial slot of this piece
 };
 
-struct __align__(16) Smem {
-  unsigned char kv[kStages][kBlockBytes];          // offset 0: 32 KiB-aligned stages
-  float p[kConsumerWarps][kBs][kGqa];              // softmax weights, per warp
-  float alpha[kConsumerWarps][kGqa];               // rescale factors, per warp
+// One stage = one physical block, as 8 kv-head tiles of [K|V][16 tokens][64],
+// each 128-byte row swizzled (16-byte chunk c stored at c ^ (token & 7)).
+struct __align__(1024) Smem {
+  unsigned char kv[kStages][kBlockBytes];
+  int prefix[kMaxSeqs + 1];      // prefix[s] = blocks of sequences 0..s-1
   StageDesc desc[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  long long warp_sum[kConsumerWarps];
-  long long nb_total;
-  long long first_b;
-  int first_seq;
+  int warp_sum[kConsumerWarps];
 };
 
 struct DecodeParams {
   __nv_bfloat16 *out;
   const uint16_t *q;
-  const unsigned char *kv;
   const int32_t *block_table;
   const int32_t *context_lens;
-  int2 *meta;        // [num_seqs] (first partial slot, number of partials)
-  float2 *ml;        // [slots][32] (m, l), m in the log2 domain
-  float2 *acc;       // [slots][32][32] unnormalised output, 2 dims per float2
+  int *chunk_counter;  // zero between calls; reset by the merge kernel
+  int2 *meta;          // [num_seqs] (first partial slot, number of partials)
+  float2 *ml;          // [slots][32] (m, l), m in the log2 domain
+  float2 *acc;         // [slots][32][32] unnormalised output, 2 dims per float2
   int32_t *err;
   int num_blocks;
   int n_layers;
   int max_blocks;
   int num_seqs;
   int layer;
-  float qscale;      // scale * log2(e), folded into q
+  float qscale;        // scale * log2(e), applied to the fp32 scores
 };
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -90,169 +97,78 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Context length clamped into [0, max_blocks * 16].
 __device__ __forceinline__ int clamped_ctx(const DecodeParams &p, int s) {
-  int t = p.context_lens[s];
+  const int t = p.context_lens[s];
   return min(max(t, 0), p.max_blocks * kBs);
 }
 
-// CTA whose block range [floor(c*NB/G), floor((c+1)*NB/G)) holds block b.
-__device__ __forceinline__ int cta_of(long long b, long long nb_total, int g) {
-  return static_cast<int>(((b + 1) * g + nb_total - 1) / nb_total) - 1;
+// Chunk length in blocks: about kChunksPerCta chunks per CTA, at least 8
+// blocks (or one CTA's fair share when that is smaller).
+__device__ __forceinline__ int chunk_blocks(int nb_total, int g) {
+  const int fair = (nb_total + g - 1) / g;
+  const int min_c = min(8, fair);
+  const int c = (nb_total + kChunksPerCta * g - 1) / (kChunksPerCta * g);
+  return max(1, max(min_c, c));
 }
 
-__device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    long long n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
+// First sequence s with prefix[s+1] > b or prefix[s] >= b (a sequence that
+// reaches past block b, or an empty one starting at b or later).
+__device__ __forceinline__ int first_seq_at(const int *prefix, int n, int b) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid + 1] > b || prefix[mid] >= b) hi = mid;
+    else lo = mid + 1;
   }
-  return v;
+  return lo;
 }
 
-struct QRegs {
-  float2 a[kGqa][4];   // q pairs matching the lane's first K load
-  float2 b[kGqa][4];   // q pairs matching the lane's second K load
-};
-
-__device__ __forceinline__ float2 scaled_pair(uint32_t u, float sc) {
-  float2 f = bf16x2_to_float2(u);
-  return make_float2(f.x * sc, f.y * sc);
-}
-
-// Lane (t8 = lane/4, qq = lane%4) handles dims [8qq, 8qq+8) and
-// [32+8qq, 32+8qq+8).  Lanes with odd t8 read the upper half first, which
-// makes the shared-memory K reads bank-conflict free.
-__device__ __forceinline__ void load_q(QRegs &qr, const DecodeParams &p, int s, int g, int lane) {
-  const int qq = lane & 3;
-  const bool odd = (lane >> 2) & 1;
-#pragma unroll
-  for (int h = 0; h < kGqa; ++h) {
-    const uint4 *row =
-        reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(s) * kHq + g * kGqa + h) * kD);
-    uint4 lo = __ldg(row + qq);
-    uint4 hi = __ldg(row + 4 + qq);
-    uint4 A = odd ? hi : lo;
-    uint4 B = odd ? lo : hi;
-    qr.a[h][0] = scaled_pair(A.x, p.qscale);
-    qr.a[h][1] = scaled_pair(A.y, p.qscale);
-    qr.a[h][2] = scaled_pair(A.z, p.qscale);
-    qr.a[h][3] = scaled_pair(A.w, p.qscale);
-    qr.b[h][0] = scaled_pair(B.x, p.qscale);
-    qr.b[h][1] = scaled_pair(B.y, p.qscale);
-    qr.b[h][2] = scaled_pair(B.z, p.qscale);
-    qr.b[h][3] = scaled_pair(B.w, p.qscale);
-  }
-}
-
-// Score of token t (row of the stage) for this lane's head after the
-// reduce-scatter over the 4 lanes that share t.
-__device__ __forceinline__ float qk_score(const QRegs &qr, const unsigned char *krow, int lane) {
-  const int qq = lane & 3;
-  const bool odd = (lane >> 2) & 1;
-  const uint4 ka = *reinterpret_cast<const uint4 *>(krow + qq * 16 + (odd ? 64 : 0));
-  const uint4 kb = *reinterpret_cast<const uint4 *>(krow + qq * 16 + (odd ? 0 : 64));
-  const float2 k0 = bf16x2_to_float2(ka.x), k1 = bf16x2_to_float2(ka.y);
-  const float2 k2 = bf16x2_to_float2(ka.z), k3 = bf16x2_to_float2(ka.w);
-  const float2 k4 = bf16x2_to_float2(kb.x), k5 = bf16x2_to_float2(kb.y);
-  const float2 k6 = bf16x2_to_float2(kb.z), k7 = bf16x2_to_float2(kb.w);
-  float v[kGqa];
-#pragma unroll
-  for (int h = 0; h < kGqa; ++h) {
-    float2 acc = make_float2(0.f, 0.f);
-    acc = fma2(qr.a[h][0], k0, acc);
-    acc = fma2(qr.a[h][1], k1, acc);
-    acc = fma2(qr.a[h][2], k2, acc);
-    acc = fma2(qr.a[h][3], k3, acc);
-    acc = fma2(qr.b[h][0], k4, acc);
-    acc = fma2(qr.b[h][1], k5, acc);
-    acc = fma2(qr.b[h][2], k6, acc);
-    acc = fma2(qr.b[h][3], k7, acc);
-    v[h] = acc.x + acc.y;
-  }
-  // reduce-scatter: after two exchange steps lane qq holds head qq's sum
-  const bool b1 = qq & 2;
-  float send0 = b1 ? v[0] : v[2];
-  float send1 = b1 ? v[1] : v[3];
-  float keep0 = b1 ? v[2] : v[0];
-  float keep1 = b1 ? v[3] : v[1];
-  keep0 += __shfl_xor_sync(0xffffffffu, send0, 2);
-  keep1 += __shfl_xor_sync(0xffffffffu, send1, 2);
-  const bool b0 = qq & 1;
-  float send = b0 ? keep0 : keep1;
-  float keep = b0 ? keep1 : keep0;
-  keep += __shfl_xor_sync(0xffffffffu, send, 1);
-  return keep;
-}
-
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(DecodeParams p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int c = blockIdx.x;
-  // everything this kernel reads may come from the previous kernel on the
-  // stream; with programmatic launch only the CTA start-up overlaps it
+  const int G = gridDim.x;
+  if (tid == 0) prefetch_tensormap(&kv_map);
+  // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
-  // ---- total number of blocks over all sequences ---------------------------
-  long long mine = 0;
-  if (tid < kScanThreads) {
-    for (int i = tid; i < p.num_seqs; i += kScanThreads) {
-      int t = p.context_lens[i];
-      if ((t < 0 || t > p.max_blocks * kBs) && c == 0) report(p.err, PA_DEV_CTX_RANGE);
-      mine += (clamped_ctx(p, i) + kBs - 1) / kBs;
-    }
-    #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-    if (lane == 0) sm.warp_sum[warp] = mine;
-  }
-  if (tid == 0) sm.first_seq = INT_MAX;
-  __syncthreads();
-  long long nb_total = 0;
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) nb_total += sm.warp_sum[w];
-  const int G = static_cast<int>(min(static_cast<long long>(gridDim.x), max(nb_total, 1LL)));
-  if (c >= G) return;
-  const long long lo = nb_total * c / G;
-  const long long hi = nb_total * (c + 1) / G;
-  __syncthreads();   // warp_sum is reused below
-
-  // ---- first sequence touching [lo, hi): smallest s with B[s+1] > lo or B[s] >= lo
-  long long carry = 0;
+  // ---- block prefix over all sequences -------------------------------------
+  int carry = 0;
   for (int base = 0; base < p.num_seqs; base += kScanThreads) {
     const int i = base + tid;
-    long long nb = 0;
-    if (tid < kScanThreads && i < p.num_seqs) nb = (clamped_ctx(p, i) + kBs - 1) / kBs;
-    long long incl = 0;
+    int nb = 0;
+    if (tid < kScanThreads && i < p.num_seqs) {
+      const int t = p.context_lens[i];
+      if ((t < 0 || t > p.max_blocks * kBs) && blockIdx.x == 0) report(p.err, PA_DEV_CTX_RANGE);
+      nb = (clamped_ctx(p, i) + kBs - 1) / kBs;
+    }
+    int incl = nb;
     if (tid < kScanThreads) {
-      incl = warp_incl_scan(nb, lane);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
       if (lane == 31) sm.warp_sum[warp] = incl;
     }
     __syncthreads();
-    long long woff = 0, chunk = 0;
+    int before = 0, chunk = 0;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      long long ws = sm.warp_sum[w];
-      if (w < warp) woff += ws;
-      chunk += ws;
+      const int v = sm.warp_sum[w];
+      if (w < warp) before += v;
+      chunk += v;
     }
-    const long long b_i = carry + woff + incl - nb;
-    const bool cond = tid < kScanThreads && i < p.num_seqs && (b_i + nb > lo || b_i >= lo);
-    if (cond) atomicMin(&sm.first_seq, i);
-    __syncthreads();
-    const int f = sm.first_seq;
-    if (f != INT_MAX) {
-      if (i == f && tid < kScanThreads) sm.first_b = b_i;
-      __syncthreads();
-      break;
-    }
+    if (tid < kScanThreads && i < p.num_seqs) sm.prefix[i + 1] = carry + before + incl;
     carry += chunk;
-    __syncthreads();   // warp_sum is rewritten by the next chunk
+    __syncthreads();
   }
-
   if (tid == 0) {
+    sm.prefix[0] = 0;
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&sm.full[st], 1);
       mbar_init(&sm.empty[st], kConsumerWarps);
@@ -260,82 +176,98 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
     fence_mbar_init();
   }
   __syncthreads();
-
-  const int s_first = sm.first_seq == INT_MAX ? p.num_seqs : sm.first_seq;
+  const int nb_total = carry;
+  const int C = chunk_blocks(nb_total, G);
+  const int n_chunks = max(1, (nb_total + C - 1) / C);
 
   if (warp == kConsumerWarps) {
     // ===================================================== producer warp ==
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    uint32_t issued = 0, issued_parity = 0;   // per stage: used / last phase parity
-    long long B = (s_first < p.num_seqs) ? sm.first_b : nb_total;
-    for (int s = s_first; s < p.num_seqs && ok; ++s) {
-      if (B >= hi && c != G - 1) break;
-      const int T = clamped_ctx(p, s);
-      const int nb = (T + kBs - 1) / kBs;
-      if (nb == 0) {
-        // empty context: this CTA owns it, the output is zero
-        uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(s) * kHq * kD);
-        for (int k = lane; k < kHq * kD * 2 / 16; k += 32) o[k] = make_uint4(0, 0, 0, 0);
-        if (lane == 0) p.meta[s] = make_int2(0, 0);
-        continue;
+    uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
+    int k = blockIdx.x;
+    while (k < n_chunks && ok) {
+      int next = 0;
+      if (lane == 0) {
+        next = G + atomicAdd(p.chunk_counter, 1);   // lands while chunk k streams
+        if (next < G) next = n_chunks;               // a counter that was never zeroed
       }
-      const long long jb = max(lo, B) - B;
-      const long long je = min(hi, B + nb) - B;
-      const int c_first = cta_of(B, nb_total, G);
-      const int c_last = cta_of(B + nb - 1, nb_total, G);
-      const int n_parts = c_last - c_first + 1;
-      if (c == c_first && lane == 0) p.meta[s] = make_int2(c_first + s, n_parts);
-      const int32_t *row =
-          p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
-      for (long long j0 = jb; j0 < je && ok; j0 += 32) {
-        const long long jj = j0 + lane;
-        const int my_blk = (jj < je) ? row[jj] : 0;
-        const int cnt = static_cast<int>(min(32LL, je - j0));
-        for (int k = 0; k < cnt; ++k) {
-          const int blk = __shfl_sync(0xffffffffu, my_blk, k);
-          const long long j = j0 + k;
-          int good = 1;
-          if (lane == 0) {
-            if (!mbar_wait(&sm.empty[stage], phase ^ 1)) {
-              good = 0;
-            } else {
+      const int b0 = k * C;
+      const int b1 = min(nb_total, b0 + C);
+      const bool last_chunk = (k == n_chunks - 1);
+      for (int s = first_seq_at(sm.prefix, p.num_seqs, b0); s < p.num_seqs && ok; ++s) {
+        const int B = sm.prefix[s];
+        if (B >= b1 && !last_chunk) break;
+        const int nb = sm.prefix[s + 1] - B;
+        if (nb == 0) {
+          // empty context: the chunk holding its start owns it; output zero
+          uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(s) * kHq * kD);
+          for (int e = lane; e < kHq * kD * 2 / 16; e += 32) o[e] = make_uint4(0, 0, 0, 0);
+          if (lane == 0) p.meta[s] = make_int2(0, 0);
+          continue;
+        }
+        if (B >= b1) break;   // last chunk: only empty sequences may follow
+        const int T = clamped_ctx(p, s);
+        const int jb = max(b0, B) - B;
+        const int je = min(b1, B + nb) - B;
+        const int k_first = B / C;
+        const int n_parts = (B + nb - 1) / C - k_first + 1;
+        const int slot = k + s;
+        if (k == k_first && lane == 0) p.meta[s] = make_int2(k_first + s, n_parts);
+        const int32_t *row =
+            p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+        for (int j0 = jb; j0 < je && ok; j0 += 32) {
+          const int my_blk = (j0 + lane < je) ? row[j0 + lane] : 0;
+          const int cnt = min(32, je - j0);
+          for (int e = 0; e < cnt; ++e) {
+            const int blk = __shfl_sync(0xffffffffu, my_blk, e);
+            const int j = j0 + e;
+            int good = 1;
+            if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+              ok = false;
+              break;
+            }
+            const bool valid = blk >= 0 && blk < p.num_blocks;
+            if (lane == 0) {
               StageDesc d;
               d.seq = s;
-              d.n_valid = min(kBs, T - static_cast<int>(j) * kBs);
+              d.n_valid = min(kBs, T - j * kBs);
+              if (!valid) d.n_valid = -d.n_valid;   // consumers skip it
               d.flags = (j == jb ? kSegStart : 0) | (j == je - 1 ? kSegEnd : 0);
               d.n_parts = n_parts;
+              d.slot = slot;
               sm.desc[stage] = d;
-              if (blk >= 0 && blk < p.num_blocks) {
+              if (valid) {
                 mbar_arrive_expect_tx(&sm.full[stage], kBlockBytes);
-                bulk_g2s(sm.kv[stage], p.kv + static_cast<size_t>(blk) * kBlockBytes, kBlockBytes,
-                         &sm.full[stage]);
               } else {
                 report(p.err, PA_DEV_BAD_BLOCK);
-                sm.desc[stage].n_valid = -sm.desc[stage].n_valid;   // consumers skip it
                 mbar_arrive(&sm.full[stage]);
               }
               issued |= 1u << stage;
               issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
-          }
-          ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-          if (!ok) break;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+            __syncwarp();
+            if (valid && lane < kHkv)   // one 4 KiB tile per kv head, 8 lanes in parallel
+              tma_load_5d(sm.kv[stage] + lane * kHeadTileBytes, &kv_map, 0, lane, 0, 0, blk,
+                          &sm.full[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
       }
-      B += nb;
+      k = __shfl_sync(0xffffffffu, next, 0);
     }
     if (lane == 0) {
       if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
         sm.desc[stage].flags = kEndOfWork;
         mbar_arrive(&sm.full[stage]);
         // this arrive is now the stage's last phase; the copy before it on
-        // the same stage has completed, or the consumers could not have freed it
+        // the same stage has landed, or the consumers could not have freed it
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       } else {
@@ -349,17 +281,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
     __syncwarp();
   } else {
     // ===================================================== consumer warps ==
-    const int g = warp;                 // kv head
-    const int t8 = lane >> 2;           // token within a half block
-    const int qq = lane & 3;            // head within the group (after reduce-scatter)
-    const unsigned char *khead = nullptr;
-    QRegs qr;
-    float2 o[kGqa];
+    const int g = warp;                    // kv head
+    const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
+    const int c2 = 2 * (lane & 3);         // fragment column pair
+    const bool real_row = r < kGqa;
+    // ldmatrix row addresses: matrix lm_i = lane / 8 takes row lm_r = lane % 8;
+    // the 16-byte chunk c of token row t sits at c ^ (t & 7)
+    const int lm_i = lane >> 3, lm_r = lane & 7;
+    uint32_t qa[4], qc[4];                 // Q fragments: row r, cols 16ks + c2 (qa), + 8 (qc)
+    float o[8][4];                         // O fragments, 8 tiles of 8 dims
     float m = neg_inf(), l = 0.f;
     int stage = 0;
     uint32_t phase = 0;
 #pragma unroll
-    for (int h = 0; h < kGqa; ++h) o[h] = make_float2(0.f, 0.f);
+    for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
     while (true) {
       if (!mbar_wait(&sm.full[stage], phase)) {
         report(p.err, PA_DEV_TIMEOUT);
@@ -368,85 +305,100 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
       const StageDesc d = sm.desc[stage];
       if (d.flags & kEndOfWork) break;
       if (d.flags & kSegStart) {
-        load_q(qr, p, d.seq, g, lane);
+        if (real_row) {
+          const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+              p.q + (static_cast<size_t>(d.seq) * kHq + g * kGqa + r) * kD);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
+            qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
+          }
+        }
         m = neg_inf();
         l = 0.f;
 #pragma unroll
-        for (int h = 0; h < kGqa; ++h) o[h] = make_float2(0.f, 0.f);
+        for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
       }
       const int n_valid = d.n_valid;
       if (n_valid > 0) {
-        khead = sm.kv[stage] + g * kHeadRowBytes;
-        // ---- scores of tokens t8 and t8 + 8 for head qq (log2 domain)
-        float s0 = qk_score(qr, khead + t8 * kTokRowBytes, lane);
-        float s1 = qk_score(qr, khead + (t8 + 8) * kTokRowBytes, lane);
-        s0 = (t8 < n_valid) ? s0 : neg_inf();
-        s1 = (t8 + 8 < n_valid) ? s1 : neg_inf();
-        // ---- online softmax
-        float bm = fmaxf(s0, s1);
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        const float m_new = fmaxf(m, bm);
-        const float alpha = fast_exp2(m - m_new);
-        const float p0 = fast_exp2(s0 - m_new);
-        const float p1 = fast_exp2(s1 - m_new);
-        l = l * alpha + p0 + p1;
-        m = m_new;
-        sm.p[g][t8][qq] = p0;
-        sm.p[g][t8 + 8][qq] = p1;
-        if (t8 == 0) sm.alpha[g][qq] = alpha;
-        __syncwarp();
-        // ---- PV: this lane owns dims 2*lane, 2*lane+1 of all 4 heads
-        const float4 al = *reinterpret_cast<const float4 *>(sm.alpha[g]);
-        o[0] = make_float2(o[0].x * al.x, o[0].y * al.x);
-        o[1] = make_float2(o[1].x * al.y, o[1].y * al.y);
-        o[2] = make_float2(o[2].x * al.z, o[2].y * al.z);
-        o[3] = make_float2(o[3].x * al.w, o[3].y * al.w);
-        const unsigned char *vcol = sm.kv[stage] + kHalfBlockBytes + g * kHeadRowBytes + lane * 4;
-        if (n_valid == kBs) {
+        unsigned char *tile = sm.kv[stage] + g * kHeadTileBytes;
+        const uint32_t ktile = smem_u32(tile);
+        const uint32_t vtile = ktile + kBs * kHeadRowBytes;
+        if (n_valid < kBs) {
+          // rows past the context may hold anything (NaN included): zero the
+          // V rows, the K rows are masked in the scores
+          uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
+          for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        // ---- S = Q K^T for tokens 0..7 (s0) and 8..15 (s1)
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int t = 0; t < kBs; ++t) {
-            const float4 pw = *reinterpret_cast<const float4 *>(sm.p[g][t]);
-            const float2 v = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vcol + t * kTokRowBytes));
-            o[0] = fma2(make_float2(pw.x, pw.x), v, o[0]);
-            o[1] = fma2(make_float2(pw.y, pw.y), v, o[1]);
-            o[2] = fma2(make_float2(pw.z, pw.z), v, o[2]);
-            o[3] = fma2(make_float2(pw.w, pw.w), v, o[3]);
-          }
-        } else {
-          for (int t = 0; t < n_valid; ++t) {
-            const float4 pw = *reinterpret_cast<const float4 *>(sm.p[g][t]);
-            const float2 v = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vcol + t * kTokRowBytes));
-            o[0] = fma2(make_float2(pw.x, pw.x), v, o[0]);
-            o[1] = fma2(make_float2(pw.y, pw.y), v, o[1]);
-            o[2] = fma2(make_float2(pw.z, pw.z), v, o[2]);
-            o[3] = fma2(make_float2(pw.w, pw.w), v, o[3]);
-          }
+        for (int ks = 0; ks < 4; ++ks) {
+          const int tok = (lm_i >> 1) * 8 + lm_r;
+          const int chunk = 2 * ks + (lm_i & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
+          mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
+          mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
+        }
+        // ---- online softmax on row r (q head), columns c2, c2+1, 8+c2, 9+c2
+        float x0 = s0[0] * p.qscale, x1 = s0[1] * p.qscale;
+        float x2 = s1[0] * p.qscale, x3 = s1[1] * p.qscale;
+        x0 = (c2 < n_valid) ? x0 : neg_inf();
+        x1 = (c2 + 1 < n_valid) ? x1 : neg_inf();
+        x2 = (c2 + 8 < n_valid) ? x2 : neg_inf();
+        x3 = (c2 + 9 < n_valid) ? x3 : neg_inf();
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - m_new);
+        const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
+        const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
+        const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
+        l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
+        m = m_new;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          o[t][0] *= alpha;
+          o[t][1] *= alpha;
+        }
+        // ---- O += P V, dims in 4 pairs of 8-dim tiles
+#pragma unroll
+        for (int dp = 0; dp < 4; ++dp) {
+          const int tok = (lm_i & 1) * 8 + lm_r;
+          const int chunk = 2 * dp + (lm_i >> 1);
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
+          mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
+          mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
       if (d.flags & kSegEnd) {
-        // ---- finish this CTA's share of sequence d.seq
+        // ---- finish this piece of sequence d.seq: row sums over the quad
         float lt = l;
-        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
-        if (d.n_parts == 1) {
-#pragma unroll
-          for (int h = 0; h < kGqa; ++h) {
-            const float inv = 1.f / __shfl_sync(0xffffffffu, lt, h);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        if (real_row) {
+          const int h = g * kGqa + r;
+          if (d.n_parts == 1) {
+            const float inv = 1.f / lt;
             uint32_t *dst = reinterpret_cast<uint32_t *>(
-                p.out + (static_cast<size_t>(d.seq) * kHq + g * kGqa + h) * kD);
-            dst[lane] = float2_to_bf16x2(o[h].x * inv, o[h].y * inv);
-          }
-        } else {
-          const size_t slot = static_cast<size_t>(c) + d.seq;
+                p.out + (static_cast<size_t>(d.seq) * kHq + h) * kD);
 #pragma unroll
-          for (int h = 0; h < kGqa; ++h)
-            p.acc[(slot * kHq + g * kGqa + h) * (kD / 2) + lane] = o[h];
-          if (lane < kGqa) p.ml[slot * kHq + g * kGqa + lane] = make_float2(m, lt);
+            for (int t = 0; t < 8; ++t)
+              dst[(8 * t + c2) / 2] = float2_to_bf16x2(o[t][0] * inv, o[t][1] * inv);
+          } else {
+            const size_t slot = static_cast<size_t>(d.slot);
+            float2 *dst = p.acc + (slot * kHq + h) * (kD / 2);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(o[t][0], o[t][1]);
+            if ((lane & 3) == 0) p.ml[slot * kHq + h] = make_float2(m, lt);
+          }
         }
       }
       if (++stage == kStages) {
@@ -458,12 +410,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(Deco
   pdl_launch_dependents();
 }
 
-// Combines the partials of every sequence split across CTAs.  Grid
-// (num_seqs, 32 q heads), 256 threads.  All partials of one (sequence, head)
-// are loaded in parallel: first the maxima (one per thread), then the
-// weighted accumulators, 8 partials at a time across the warps.
+// Combines the partials of every sequence cut into several pieces.  Grid
+// (num_seqs, 32 q heads), 256 threads: the maxima are read one per thread,
+// then the weighted accumulators 8 partials at a time across the warps.
+// Also returns the chunk counter to zero for the next call.
 constexpr int kMergeThreads = 256;
-constexpr int kMaxParts = 1024;   // the grid never exceeds this many CTAs
 
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
   pdl_wait_primary();
@@ -473,6 +424,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   const int s = blockIdx.x;
   const int h = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (s == 0 && h == 0 && tid == 0) *p.chunk_counter = 0;   // the split kernel has finished
   const int2 mt = p.meta[s];
   const int np = mt.y;
   if (np <= 1) return;
@@ -504,16 +456,16 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
 #pragma unroll
   for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
 
-  float2 o = make_float2(0.f, 0.f);
+  float2 acc = make_float2(0.f, 0.f);
   constexpr int kGroups = kMergeThreads / 32;
 #pragma unroll 4
   for (int k = warp; k < np; k += kGroups) {
     const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
     const float wk = wpart[k];
-    o.x = fmaf(wk, a.x, o.x);
-    o.y = fmaf(wk, a.y, o.y);
+    acc.x = fmaf(wk, a.x, acc.x);
+    acc.y = fmaf(wk, a.y, acc.y);
   }
-  osum[warp][lane] = o;
+  osum[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
     float2 t = osum[0][lane];
@@ -531,15 +483,20 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
 int g_grid_limit = 0;
 
 struct WsLayout {
-  size_t meta_off, ml_off, acc_off, total;
+  size_t counter_off, meta_off, ml_off, acc_off, total;
 };
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+long long max_slots(int num_seqs, int grid) {
+  return static_cast<long long>(kChunksPerCta) * grid + 2 + num_seqs;
+}
+
 WsLayout ws_layout(int num_seqs, long long slots) {
   WsLayout w;
-  w.meta_off = 0;
-  w.ml_off = align256(sizeof(int2) * static_cast<size_t>(num_seqs));
+  w.counter_off = 0;
+  w.meta_off = 256;
+  w.ml_off = w.meta_off + align256(sizeof(int2) * static_cast<size_t>(num_seqs));
   w.acc_off = w.ml_off + align256(sizeof(float2) * kHq * static_cast<size_t>(slots));
   w.total = w.acc_off + align256(sizeof(float) * kHq * kD * static_cast<size_t>(slots));
   return w;
@@ -549,8 +506,37 @@ int auto_grid(const DeviceInfo &di, int num_seqs, int max_blocks) {
   long long g = static_cast<long long>(di.sm_count) * kCtasPerSm;
   if (g_grid_limit > 0) g = min(g, static_cast<long long>(g_grid_limit));
   g = min(g, static_cast<long long>(num_seqs) * max_blocks);
-  g = min(g, static_cast<long long>(kMaxParts));
+  g = min(g, static_cast<long long>(kMaxGrid));
   return static_cast<int>(max(g, 1LL));
+}
+
+// Tensor map over the whole pool: dims (d 64, kv head 8, token 16, K|V 2,
+// block), box (64, 1, 16, 2, 1) = one kv head's K and V tiles, 128B swizzle.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const cuuint64_t dims[5] = {kD, kHkv, kBs, 2, static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kHeadRowBytes, kTokRowBytes, kHalfBlockBytes, kBlockBytes};
+  const cuuint32_t box[5] = {kD, 1, kBs, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -582,9 +568,9 @@ using namespace pa;
 extern "C" size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq) {
   if (num_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
   DeviceInfo di;
-  if (current_device(&di) != PA_OK) di.sm_count = 1024;   // generous when no device answers
+  if (current_device(&di) != PA_OK) di.sm_count = kMaxGrid;   // generous when no device answers
   const int G = auto_grid(di, num_seqs, max_blocks_per_seq);
-  return ws_layout(num_seqs, static_cast<long long>(G) + num_seqs).total;
+  return ws_layout(num_seqs, max_slots(num_seqs, G)).total;
 }
 
 extern "C" int pa_decode_set_grid_limit(int max_ctas) {
@@ -598,9 +584,12 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
                                    int max_blocks_per_seq, const int32_t *context_lens,
                                    int num_seqs, int layer, float scale, void *workspace,
                                    size_t workspace_bytes, int32_t *err, void *stream) {
-  if (num_seqs < 0 || num_blocks <= 0 || n_layers <= 0 || max_blocks_per_seq <= 0)
+  if (num_seqs < 0 || num_seqs > kMaxSeqs || num_blocks <= 0 || n_layers <= 0 ||
+      max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX ||
+      static_cast<long long>(num_seqs) * max_blocks_per_seq > INT_MAX)
+    return PA_ERR_ARG;
   if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !kv_cache || !block_table || !context_lens || !err) return PA_ERR_NULL;
@@ -612,15 +601,15 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   if (rc != PA_OK) return rc;
 
   int G = auto_grid(di, num_seqs, max_blocks_per_seq);
-  WsLayout w = ws_layout(num_seqs, static_cast<long long>(G) + num_seqs);
+  WsLayout w = ws_layout(num_seqs, max_slots(num_seqs, G));
   while (w.total > workspace_bytes && G > 1) {
     G = G / 2;
-    w = ws_layout(num_seqs, static_cast<long long>(G) + num_seqs);
+    w = ws_layout(num_seqs, max_slots(num_seqs, G));
   }
   if (w.total > workspace_bytes) return PA_ERR_WORKSPACE;
 
   static bool attr_done[64] = {};
-  const size_t smem = sizeof(Smem);
+  const size_t smem = sizeof(Smem) + 1024;   // + room to align the base to 1 KiB
   if (!attr_done[di.device]) {
     if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
@@ -628,13 +617,24 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
     attr_done[di.device] = true;
   }
 
+  // the tensor map describes the pool; rebuilt only when the pool changes
+  static thread_local const void *map_pool = nullptr;
+  static thread_local int map_blocks = 0;
+  alignas(64) static thread_local CUtensorMap map;
+  if (map_pool != kv_cache || map_blocks != num_blocks) {
+    rc = make_kv_map(&map, kv_cache, num_blocks);
+    if (rc != PA_OK) return rc;
+    map_pool = kv_cache;
+    map_blocks = num_blocks;
+  }
+
   DecodeParams prm;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.q = q;
-  prm.kv = reinterpret_cast<const unsigned char *>(kv_cache);
   prm.block_table = block_table;
   prm.context_lens = context_lens;
+  prm.chunk_counter = reinterpret_cast<int *>(ws + w.counter_off);
   prm.meta = reinterpret_cast<int2 *>(ws + w.meta_off);
   prm.ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   prm.acc = reinterpret_cast<float2 *>(ws + w.acc_off);
@@ -647,7 +647,7 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   prm.qscale = scale * kLog2e;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, prm) != cudaSuccess)
+  if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(decode_merge_kernel, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm) !=
       cudaSuccess)

@@ -53,8 +53,7 @@ def assert_attention_close(gpu_out_f64: np.ndarray, ref: np.ndarray, what: str =
 def workspace_for(n, max_blocks):
     import torch
     import paged_kv_cache_205_gb300 as pk
-    nbytes = pk.pa_decode_workspace_size(n, max_blocks)
-    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    return pk.decode_workspace(n, max_blocks)
 
 
 def gather_for_oracle(pool_dev, block_table: np.ndarray, seqs, ctx, layer):

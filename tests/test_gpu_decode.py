@@ -221,3 +221,69 @@ def test_full_size_workload_sampled(name, sample):
         assert_attention_close(got[sample], ref, f"{name} layer {layer}")
     del pool
     torch.cuda.empty_cache()
+
+
+def test_workspace_reused_across_calls_and_grids():
+    """One zero-filled workspace serves many calls in a row (the work counter
+    is returned to zero by every call), whatever the split."""
+    import torch
+    pk = _pk()
+    rng = np.random.default_rng(31)
+    ws = workspace_for(12, 40)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for trial, grid in enumerate([0, 3, 0, 17, 1, 0]):
+        ctx = rng.integers(0, 600, size=12)
+        w, pool, q = _small_case(40 + trial, ctx)
+        pk.pa_decode_set_grid_limit(grid)
+        out = torch.empty((12, N_Q, D), dtype=torch.bfloat16, device="cuda")
+        bt = np.zeros((12, 1, 40), dtype=np.int32) - 1
+        bt[:, :, :w.block_table.shape[2]] = w.block_table
+        pk.pa_decode_attention(out, dev_bf16(q), dev_bf16(pool), dev_i32(bt), dev_i32(w.context_lens),
+                               0, 0.125, ws, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+        assert_attention_close(host_f64(out), ref, f"trial {trial}")
+
+
+def test_graph_replay_matches_oracle():
+    """The call captured in a CUDA graph and replayed gives the same result
+    every replay."""
+    import torch
+    pk = _pk()
+    w, pool, q = _small_case(51, [700, 33, 1, 250, 0, 1900], n_layers=2)
+    qd, poold, btd, ctxd = dev_bf16(q), dev_bf16(pool), dev_i32(w.block_table), dev_i32(w.context_lens)
+    out = torch.zeros((w.num_seqs, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(w.num_seqs, w.max_blocks_per_seq)
+    pk.pa_decode_attention(out, qd, poold, btd, ctxd, 1, 0.125, ws, err)   # warm-up
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            pk.pa_decode_attention(out, qd, poold, btd, ctxd, 1, 0.125, ws, err)
+    torch.cuda.current_stream().wait_stream(side)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 1)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attention_close(host_f64(out), ref, "graph replay")
+
+
+def test_too_many_sequences_is_refused():
+    import torch
+    pk = _pk()
+    n = 2049
+    bt = torch.full((n, 1, 1), -1, dtype=torch.int32, device="cuda")
+    ctx = torch.zeros(n, dtype=torch.int32, device="cuda")
+    q = torch.zeros((n, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros((1, 2, 16, 8, 64), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_decode_attention(q, q, pool, bt, ctx, 0, 0.125, ws, err)
+    assert e.value.code == -2
