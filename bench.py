@@ -304,7 +304,7 @@ class DeviceStep:
             self.fl = torch.from_numpy(w.free_list).to(dev)
             self.fc0 = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
             self.fc = self.fc0.clone()
-        self.launches_per_step = L * (2 + (2 if w.append else 0))
+        self.launches_per_step = L * (1 + (2 if w.append else 0))
 
     def layer(self, l, q=None, out=None):
         pk, w = self.pk, self.w
@@ -498,7 +498,7 @@ def run_gpu(args, rank, world, dist):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode_attention (decode_split_kernel + decode_merge_kernel)",
+            "kernel": "pa_decode_attention (decode_split_kernel, one launch per call)",
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
