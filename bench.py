@@ -304,7 +304,7 @@ class DeviceStep:
             self.fl = torch.from_numpy(w.free_list).to(dev)
             self.fc0 = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
             self.fc = self.fc0.clone()
-        self.launches_per_step = L * (1 + (2 if w.append else 0))
+        self.launches_per_step = L * (2 + (2 if w.append else 0))
 
     def layer(self, l, q=None, out=None):
         pk, w = self.pk, self.w
@@ -337,6 +337,7 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.set_device(local)
     w = wl.make_workload(args.workload)
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
+    st.pk.pa_decode_set_grid_limit(args.grid)
     L, n = w.n_layers, w.num_seqs
 
     def barrier():
@@ -495,10 +496,11 @@ def run_gpu(args, rank, world, dist):
                   f"{bytes_step / 2**20:.0f} MiB of distinct K/V (L2 129 MB)",
             "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
+            "decode_grid_cap": args.grid,
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode_attention (decode_split_kernel, one launch per call)",
+            "kernel": "pa_decode_attention (decode_split_kernel + decode_merge_kernel)",
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
@@ -535,6 +537,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama1b", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grid", type=int, default=0,
+                    help="cap on decode CTAs per launch (0 = two per SM)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -9,10 +9,11 @@
 //  * Work is balanced by BLOCKS, not by sequences.  The blocks of all
 //    sequences are laid end to end and cut into chunks of C blocks; CTAs take
 //    chunks from an atomic counter (the first one is their own index), so a
-//    slow SM simply ends up with fewer chunks.  A sequence spread over
-//    several chunks leaves one fp32 partial (m, l, acc) per piece; the warp
-//    that finishes the last piece of a group merges the group, and the last
-//    group merges the groups (split-context merge, no second kernel).
+//    slow SM simply ends up with fewer chunks.  Every (chunk, sequence) piece
+//    leaves an fp32 partial (m, l, acc); a second kernel merges the partials
+//    of sequences that span several chunks (split-context merge), launched
+//    with programmatic dependent launch so its start-up hides under the
+//    first kernel's tail.
 //  * A producer warp streams whole physical blocks (16 tokens x 8 kv heads x
 //    K,V = 32 KiB, one contiguous page) into a ring of shared-memory stages
 //    with TMA tensor copies, one 4 KiB copy per kv head; the 128-byte swizzle
@@ -45,7 +46,6 @@ constexpr int kScanThreads = kConsumerWarps * 32;          // 256
 constexpr int kMaxSeqs = 2048;                             // block prefix kept in shared memory
 constexpr int kMaxGrid = 512;
 constexpr int kChunksPerCta = 4;                           // average chunks a CTA takes
-constexpr int kMergeGroup = 32;                            // pieces merged by one warp at once
 constexpr int kHeadTileBytes = 2 * kBs * kHeadRowBytes;    // K and V of one kv head: 4 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -59,7 +59,6 @@ struct StageDesc {
   int flags;
   int n_parts;   // pieces the sequence is cut into
   int slot;      // partial slot of this piece
-  int first_slot;  // slot of the sequence's first piece
 };
 
 // One stage = one physical block, as 8 kv-head tiles of [K|V][16 tokens][64],
@@ -78,11 +77,10 @@ struct DecodeParams {
   const uint16_t *q;
   const int32_t *block_table;
   const int32_t *context_lens;
-  int *counters;       // [0] next chunk, [1] CTAs done; zero between calls
-  int *group_count;    // [slots][8] pieces of a group finished, per kv head
-  int *seq_count;      // [num_seqs][8] groups of a sequence merged, per kv head
+  int *chunk_counter;  // zero between calls; reset by the merge kernel
+  int2 *meta;          // [num_seqs] (first partial slot, number of partials)
   float2 *ml;          // [slots][32] (m, l), m in the log2 domain
-  float4 *acc;         // [slots][32][16] unnormalised output, 4 dims per float4
+  float2 *acc;         // [slots][32][32] unnormalised output, 2 dims per float2
   int32_t *err;
   int num_blocks;
   int n_layers;
@@ -124,89 +122,6 @@ __device__ __forceinline__ int first_seq_at(const int *prefix, int n, int b) {
     else lo = mid + 1;
   }
   return lo;
-}
-
-// Online merge of partials (m, l, acc) into a running (mm, ll, o[8]) for
-// one q head and 8 dims.  Partials are read through L2: other CTAs wrote them.
-__device__ __forceinline__ void merge_slot(const DecodeParams &p, size_t slot, int h, int part,
-                                           float &mm, float &ll, float (&o)[8]) {
-  const float2 mk = __ldcg(p.ml + slot * kHq + h);
-  const float4 a0 = __ldcg(p.acc + (slot * kHq + h) * (kD / 4) + 2 * part);
-  const float4 a1 = __ldcg(p.acc + (slot * kHq + h) * (kD / 4) + 2 * part + 1);
-  const float mn = fmaxf(mm, mk.x);
-  const float s_old = fast_exp2(mm - mn), s_new = fast_exp2(mk.x - mn);
-  ll = fmaf(ll, s_old, mk.y * s_new);
-  o[0] = fmaf(o[0], s_old, a0.x * s_new);
-  o[1] = fmaf(o[1], s_old, a0.y * s_new);
-  o[2] = fmaf(o[2], s_old, a0.z * s_new);
-  o[3] = fmaf(o[3], s_old, a0.w * s_new);
-  o[4] = fmaf(o[4], s_old, a1.x * s_new);
-  o[5] = fmaf(o[5], s_old, a1.y * s_new);
-  o[6] = fmaf(o[6], s_old, a1.z * s_new);
-  o[7] = fmaf(o[7], s_old, a1.w * s_new);
-  mm = mn;
-}
-
-// Called by the warp of kv head g after it stored its partial for piece
-// d.slot.  Pieces are counted per group of kMergeGroup; the warp that
-// completes a group merges it (into the group's first slot when there are
-// several groups), and the warp that completes the last group merges the
-// group results into the output.  Lane = (q head lane/8, dims 8*(lane%8)..).
-__device__ __forceinline__ void merge_pieces(const DecodeParams &p, const StageDesc &d, int g,
-                                          int lane) {
-  const int piece = d.slot - d.first_slot;
-  const int group = piece / kMergeGroup;
-  const int g_first = group * kMergeGroup;
-  const int g_size = min(kMergeGroup, d.n_parts - g_first);
-  const int n_groups = (d.n_parts + kMergeGroup - 1) / kMergeGroup;
-  const int h = g * kGqa + (lane >> 3);
-  const int part = lane & 7;
-
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  int *gc = &p.group_count[(static_cast<size_t>(d.first_slot) + group) * kHkv + g];
-  if (lane == 0) last = (atomicAdd(gc, 1) == g_size - 1);
-  if (!__shfl_sync(0xffffffffu, last, 0)) return;
-  __threadfence();
-  if (lane == 0) *gc = 0;
-
-  float mm = neg_inf(), ll = 0.f, o[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = 0.f;
-  for (int k = 0; k < g_size; ++k)
-    merge_slot(p, static_cast<size_t>(d.first_slot) + g_first + k, h, part, mm, ll, o);
-
-  if (n_groups > 1) {
-    // the group's result replaces the partial of its first piece
-    const size_t gslot = static_cast<size_t>(d.first_slot) + g_first;
-    __syncwarp();   // every lane has read that slot
-    float4 *dst = p.acc + (gslot * kHq + h) * (kD / 4) + 2 * part;
-    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-    if (part == 0) p.ml[gslot * kHq + h] = make_float2(mm, ll);
-    __threadfence();
-    __syncwarp();
-    int *sc = &p.seq_count[static_cast<size_t>(d.seq) * kHkv + g];
-    if (lane == 0) last = (atomicAdd(sc, 1) == n_groups - 1);
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
-    if (lane == 0) *sc = 0;
-    mm = neg_inf();
-    ll = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = 0.f;
-    for (int j = 0; j < n_groups; ++j)
-      merge_slot(p, static_cast<size_t>(d.first_slot) + static_cast<size_t>(j) * kMergeGroup, h,
-                 part, mm, ll, o);
-  }
-  const float inv = 1.f / ll;
-  uint4 v;
-  v.x = float2_to_bf16x2(o[0] * inv, o[1] * inv);
-  v.y = float2_to_bf16x2(o[2] * inv, o[3] * inv);
-  v.z = float2_to_bf16x2(o[4] * inv, o[5] * inv);
-  v.w = float2_to_bf16x2(o[6] * inv, o[7] * inv);
-  *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(d.seq) * kHq + h) * kD + 8 * part) = v;
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -276,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     while (k < n_chunks && ok) {
       int next = 0;
       if (lane == 0) {
-        next = G + atomicAdd(&p.counters[0], 1);   // lands while chunk k streams
+        next = G + atomicAdd(p.chunk_counter, 1);   // lands while chunk k streams
         if (next < G) next = n_chunks;               // a counter that was never zeroed
       }
       const int b0 = k * C;
@@ -290,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // empty context: the chunk holding its start owns it; output zero
           uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(s) * kHq * kD);
           for (int e = lane; e < kHq * kD * 2 / 16; e += 32) o[e] = make_uint4(0, 0, 0, 0);
+          if (lane == 0) p.meta[s] = make_int2(0, 0);
           continue;
         }
         if (B >= b1) break;   // last chunk: only empty sequences may follow
@@ -299,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int k_first = B / C;
         const int n_parts = (B + nb - 1) / C - k_first + 1;
         const int slot = k + s;
+        if (k == k_first && lane == 0) p.meta[s] = make_int2(k_first + s, n_parts);
         const int32_t *row =
             p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
         for (int j0 = jb; j0 < je && ok; j0 += 32) {
@@ -323,7 +240,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               d.flags = (j == jb ? kSegStart : 0) | (j == je - 1 ? kSegEnd : 0);
               d.n_parts = n_parts;
               d.slot = slot;
-              d.first_slot = k_first + s;
               sm.desc[stage] = d;
               if (valid) {
                 mbar_arrive_expect_tx(&sm.full[stage], kBlockBytes);
@@ -468,25 +384,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         float lt = l;
         lt += __shfl_xor_sync(0xffffffffu, lt, 1);
         lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-        if (d.n_parts == 1) {
-          if (real_row) {
+        if (real_row) {
+          const int h = g * kGqa + r;
+          if (d.n_parts == 1) {
             const float inv = 1.f / lt;
             uint32_t *dst = reinterpret_cast<uint32_t *>(
-                p.out + (static_cast<size_t>(d.seq) * kHq + g * kGqa + r) * kD);
+                p.out + (static_cast<size_t>(d.seq) * kHq + h) * kD);
 #pragma unroll
             for (int t = 0; t < 8; ++t)
               dst[(8 * t + c2) / 2] = float2_to_bf16x2(o[t][0] * inv, o[t][1] * inv);
-          }
-        } else {
-          if (real_row) {
-            const int h = g * kGqa + r;
+          } else {
             const size_t slot = static_cast<size_t>(d.slot);
-            float2 *dst = reinterpret_cast<float2 *>(p.acc + (slot * kHq + h) * (kD / 4));
+            float2 *dst = p.acc + (slot * kHq + h) * (kD / 2);
 #pragma unroll
             for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(o[t][0], o[t][1]);
             if ((lane & 3) == 0) p.ml[slot * kHq + h] = make_float2(m, lt);
           }
-          merge_pieces(p, d, g, lane);
         }
       }
       if (++stage == kStages) {
@@ -495,22 +408,120 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
   }
-  // the last CTA to leave returns the chunk counter to zero for the next call
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&p.counters[1], 1) == G - 1) {
-      p.counters[0] = 0;
-      p.counters[1] = 0;
-    }
-  }
   pdl_launch_dependents();
 }
+
+// Combines the partials of every sequence cut into several pieces, and
+// returns the chunk counter to zero for the next call.  Each thread folds
+// its share of the partials into a running (m, l, o) as it loads them (one
+// round of independent loads), then the shares are combined in shared
+// memory.  Two shapes:
+//   per head  grid (num_seqs, 32), 8 warps = 8 interleaved shares of the
+//             partials, lane = 2 dims: few sequences, many partials each;
+//   per seq   grid (num_seqs), thread = (q head, 8 dims), one share: many
+//             sequences with a few partials each.
+constexpr int kMergeThreads = 256;
+constexpr int kShares = kMergeThreads / 32;
+
+__device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, float &s_old,
+                                     float &s_new) {
+  const float mn = fmaxf(m, mk);
+  s_old = fast_exp2(m - mn);
+  s_new = fast_exp2(mk - mn);
+  l = fmaf(l, s_old, lk * s_new);
+  m = mn;
+}
+
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_per_head(DecodeParams p) {
+  pdl_wait_primary();
+  __shared__ float sm_m[kShares], sm_l[kShares];
+  __shared__ float2 sm_o[kShares][32];
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int lane = threadIdx.x & 31, share = threadIdx.x >> 5;
+  if (s == 0 && h == 0 && threadIdx.x == 0) *p.chunk_counter = 0;   // the split kernel is done
+  const int2 mt = p.meta[s];
+  const int np = mt.y;
+  if (np <= 1) return;
+  const size_t slot0 = static_cast<size_t>(mt.x);
+  float m = neg_inf(), l = 0.f, so, sn;
+  float2 o = make_float2(0.f, 0.f);
+#pragma unroll 4
+  for (int k = share; k < np; k += kShares) {
+    const float2 mk = p.ml[(slot0 + k) * kHq + h];
+    const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
+    fold(mk.x, mk.y, m, l, so, sn);
+    o.x = fmaf(o.x, so, a.x * sn);
+    o.y = fmaf(o.y, so, a.y * sn);
+  }
+  if (lane == 0) {
+    sm_m[share] = m;
+    sm_l[share] = l;
+  }
+  sm_o[share][lane] = o;
+  __syncthreads();
+  if (share == 0) {
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < kShares; ++w) M = fmaxf(M, sm_m[w]);
+    float L = 0.f;
+    float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kShares; ++w) {
+      const float sc = fast_exp2(sm_m[w] - M);   // empty shares carry m = -inf: weight 0
+      L = fmaf(sm_l[w], sc, L);
+      t.x = fmaf(sm_o[w][lane].x, sc, t.x);
+      t.y = fmaf(sm_o[w][lane].y, sc, t.y);
+    }
+    const float inv = 1.f / L;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD);
+    dst[lane] = float2_to_bf16x2(t.x * inv, t.y * inv);
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_per_seq(DecodeParams p) {
+  pdl_wait_primary();
+  const int s = blockIdx.x;
+  const int h = threadIdx.x >> 3, part = threadIdx.x & 7;   // 32 heads x 8 dim groups
+  if (s == 0 && threadIdx.x == 0) *p.chunk_counter = 0;     // the split kernel is done
+  const int2 mt = p.meta[s];
+  const int np = mt.y;
+  if (np <= 1) return;
+  const size_t slot0 = static_cast<size_t>(mt.x);
+  float m = neg_inf(), l = 0.f, so, sn, o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = 0.f;
+  const float4 *acc4 = reinterpret_cast<const float4 *>(p.acc);
+#pragma unroll 2
+  for (int k = 0; k < np; ++k) {
+    const float2 mk = p.ml[(slot0 + k) * kHq + h];
+    const float4 a0 = acc4[((slot0 + k) * kHq + h) * (kD / 4) + 2 * part];
+    const float4 a1 = acc4[((slot0 + k) * kHq + h) * (kD / 4) + 2 * part + 1];
+    fold(mk.x, mk.y, m, l, so, sn);
+    o[0] = fmaf(o[0], so, a0.x * sn);
+    o[1] = fmaf(o[1], so, a0.y * sn);
+    o[2] = fmaf(o[2], so, a0.z * sn);
+    o[3] = fmaf(o[3], so, a0.w * sn);
+    o[4] = fmaf(o[4], so, a1.x * sn);
+    o[5] = fmaf(o[5], so, a1.y * sn);
+    o[6] = fmaf(o[6], so, a1.z * sn);
+    o[7] = fmaf(o[7], so, a1.w * sn);
+  }
+  const float inv = 1.f / l;
+  uint4 v;
+  v.x = float2_to_bf16x2(o[0] * inv, o[1] * inv);
+  v.y = float2_to_bf16x2(o[2] * inv, o[3] * inv);
+  v.z = float2_to_bf16x2(o[4] * inv, o[5] * inv);
+  v.w = float2_to_bf16x2(o[6] * inv, o[7] * inv);
+  *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD + 8 * part) = v;
+}
+
+// Sequences at or above this count take the per-sequence merge shape.
+constexpr int kMergePerSeqFrom = 64;
 
 int g_grid_limit = 0;
 
 struct WsLayout {
-  size_t counters_off, group_off, seq_off, ml_off, acc_off, total;
+  size_t counter_off, meta_off, ml_off, acc_off, total;
 };
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -521,10 +532,9 @@ long long max_slots(int num_seqs, int grid) {
 
 WsLayout ws_layout(int num_seqs, long long slots) {
   WsLayout w;
-  w.counters_off = 0;
-  w.group_off = 256;
-  w.seq_off = w.group_off + align256(sizeof(int) * kHkv * static_cast<size_t>(slots));
-  w.ml_off = w.seq_off + align256(sizeof(int) * kHkv * static_cast<size_t>(num_seqs));
+  w.counter_off = 0;
+  w.meta_off = 256;
+  w.ml_off = w.meta_off + align256(sizeof(int2) * static_cast<size_t>(num_seqs));
   w.acc_off = w.ml_off + align256(sizeof(float2) * kHq * static_cast<size_t>(slots));
   w.total = w.acc_off + align256(sizeof(float) * kHq * kD * static_cast<size_t>(slots));
   return w;
@@ -662,11 +672,10 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   prm.q = q;
   prm.block_table = block_table;
   prm.context_lens = context_lens;
-  prm.counters = reinterpret_cast<int *>(ws + w.counters_off);
-  prm.group_count = reinterpret_cast<int *>(ws + w.group_off);
-  prm.seq_count = reinterpret_cast<int *>(ws + w.seq_off);
+  prm.chunk_counter = reinterpret_cast<int *>(ws + w.counter_off);
+  prm.meta = reinterpret_cast<int2 *>(ws + w.meta_off);
   prm.ml = reinterpret_cast<float2 *>(ws + w.ml_off);
-  prm.acc = reinterpret_cast<float4 *>(ws + w.acc_off);
+  prm.acc = reinterpret_cast<float2 *>(ws + w.acc_off);
   prm.err = err;
   prm.num_blocks = num_blocks;
   prm.n_layers = n_layers;
@@ -678,5 +687,10 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
+  const cudaError_t e =
+      num_seqs >= kMergePerSeqFrom
+          ? launch_pdl(decode_merge_per_seq, dim3(num_seqs), dim3(kMergeThreads), 0, st, prm)
+          : launch_pdl(decode_merge_per_head, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
