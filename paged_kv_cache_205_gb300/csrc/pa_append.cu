@@ -152,6 +152,7 @@ __device__ __forceinline__ void rotate4(uint2 lo, uint2 hi, const float2 *cs, in
 
 __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParams p) {
   __shared__ float2 cs[kD / 2];
+  pdl_launch_dependents();   // the next kernel may start its own set-up
   const int s = blockIdx.x;
   const int tid = threadIdx.x;
   const int pos = p.context_lens[s];

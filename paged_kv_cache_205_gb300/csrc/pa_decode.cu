@@ -133,7 +133,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int G = gridDim.x;
-  if (tid == 0) prefetch_tensormap(&kv_map);
+  // ---- before the previous kernel on the stream has finished: nothing is
+  // read into registers, only L2 prefetches of what the CTA needs first
+  if (tid == 0) {
+    prefetch_tensormap(&kv_map);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&sm.full[st], 1);
+      mbar_init(&sm.empty[st], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid * 32; i < p.num_seqs; i += kThreads * 32) prefetch_l2(p.context_lens + i);
+  {
+    // this layer's table rows, shared out over the CTAs
+    const int row_lines = (p.max_blocks * 4 + 127) / 128;
+    for (int i = blockIdx.x * kThreads + tid; i < p.num_seqs * row_lines; i += G * kThreads) {
+      const int s = i / row_lines, line = i % row_lines;
+      prefetch_l2(p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks +
+                  line * 32);
+    }
+  }
+  pdl_launch_dependents();   // the merge kernel may take its place in the queue
   // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
@@ -168,14 +188,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     carry += chunk;
     __syncthreads();
   }
-  if (tid == 0) {
-    sm.prefix[0] = 0;
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(&sm.full[st], 1);
-      mbar_init(&sm.empty[st], kConsumerWarps);
-    }
-    fence_mbar_init();
-  }
+  if (tid == 0) sm.prefix[0] = 0;
   __syncthreads();
   const int nb_total = carry;
   const int C = chunk_blocks(nb_total, G);
@@ -408,18 +421,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
   }
-  pdl_launch_dependents();
 }
 
 // Combines the partials of every sequence cut into several pieces, and
-// returns the chunk counter to zero for the next call.  Each thread folds
-// its share of the partials into a running (m, l, o) as it loads them (one
-// round of independent loads), then the shares are combined in shared
-// memory.  Two shapes:
-//   per head  grid (num_seqs, 32), 8 warps = 8 interleaved shares of the
-//             partials, lane = 2 dims: few sequences, many partials each;
-//   per seq   grid (num_seqs), thread = (q head, 8 dims), one share: many
-//             sequences with a few partials each.
+// returns the chunk counter to zero for the next call.  Grid (num_seqs, 32
+// q heads), 8 warps = 8 interleaved shares of the partials, lane = 2 dims.
+// Each thread folds its share into a running (m, l, o) as it loads it (one
+// round of independent loads), then the 8 shares are combined in shared
+// memory.
 constexpr int kMergeThreads = 256;
 constexpr int kShares = kMergeThreads / 32;
 
@@ -432,7 +441,8 @@ __device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, flo
   m = mn;
 }
 
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_per_head(DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
+  pdl_launch_dependents();   // the next kernel may start its own set-up
   pdl_wait_primary();
   __shared__ float sm_m[kShares], sm_l[kShares];
   __shared__ float2 sm_o[kShares][32];
@@ -478,45 +488,6 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_per_head(DecodePar
   }
 }
 
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_per_seq(DecodeParams p) {
-  pdl_wait_primary();
-  const int s = blockIdx.x;
-  const int h = threadIdx.x >> 3, part = threadIdx.x & 7;   // 32 heads x 8 dim groups
-  if (s == 0 && threadIdx.x == 0) *p.chunk_counter = 0;     // the split kernel is done
-  const int2 mt = p.meta[s];
-  const int np = mt.y;
-  if (np <= 1) return;
-  const size_t slot0 = static_cast<size_t>(mt.x);
-  float m = neg_inf(), l = 0.f, so, sn, o[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = 0.f;
-  const float4 *acc4 = reinterpret_cast<const float4 *>(p.acc);
-#pragma unroll 2
-  for (int k = 0; k < np; ++k) {
-    const float2 mk = p.ml[(slot0 + k) * kHq + h];
-    const float4 a0 = acc4[((slot0 + k) * kHq + h) * (kD / 4) + 2 * part];
-    const float4 a1 = acc4[((slot0 + k) * kHq + h) * (kD / 4) + 2 * part + 1];
-    fold(mk.x, mk.y, m, l, so, sn);
-    o[0] = fmaf(o[0], so, a0.x * sn);
-    o[1] = fmaf(o[1], so, a0.y * sn);
-    o[2] = fmaf(o[2], so, a0.z * sn);
-    o[3] = fmaf(o[3], so, a0.w * sn);
-    o[4] = fmaf(o[4], so, a1.x * sn);
-    o[5] = fmaf(o[5], so, a1.y * sn);
-    o[6] = fmaf(o[6], so, a1.z * sn);
-    o[7] = fmaf(o[7], so, a1.w * sn);
-  }
-  const float inv = 1.f / l;
-  uint4 v;
-  v.x = float2_to_bf16x2(o[0] * inv, o[1] * inv);
-  v.y = float2_to_bf16x2(o[2] * inv, o[3] * inv);
-  v.z = float2_to_bf16x2(o[4] * inv, o[5] * inv);
-  v.w = float2_to_bf16x2(o[6] * inv, o[7] * inv);
-  *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD + 8 * part) = v;
-}
-
-// Sequences at or above this count take the per-sequence merge shape.
-constexpr int kMergePerSeqFrom = 64;
 
 int g_grid_limit = 0;
 
@@ -687,10 +658,8 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  const cudaError_t e =
-      num_seqs >= kMergePerSeqFrom
-          ? launch_pdl(decode_merge_per_seq, dim3(num_seqs), dim3(kMergeThreads), 0, st, prm)
-          : launch_pdl(decode_merge_per_head, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pdl(decode_merge_kernel, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -135,6 +135,12 @@ __device__ __forceinline__ void tma_load_5d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// Hint: bring the 128-byte line holding `p` into L2.  Reads nothing into
+// registers, so it is safe on data another kernel may still be writing.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
