@@ -425,11 +425,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 // Combines the partials of every sequence cut into several pieces, and
 // returns the chunk counter to zero for the next call.  Grid (num_seqs, 32
-// q heads), 8 warps = 8 interleaved shares of the partials, lane = 2 dims.
+// q heads), 16 warps = 16 interleaved shares of the partials, lane = 2 dims.
 // Each thread folds its share into a running (m, l, o) as it loads it (one
-// round of independent loads), then the 8 shares are combined in shared
+// round of independent loads), then the 16 shares are combined in shared
 // memory.
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;
 constexpr int kShares = kMergeThreads / 32;
 
 __device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, float &s_old,
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   const size_t slot0 = static_cast<size_t>(mt.x);
   float m = neg_inf(), l = 0.f, so, sn;
   float2 o = make_float2(0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
   for (int k = share; k < np; k += kShares) {
     const float2 mk = p.ml[(slot0 + k) * kHq + h];
     const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
