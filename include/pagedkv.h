@@ -132,6 +132,33 @@ int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cac
                         void *workspace, size_t workspace_bytes, int32_t *err,
                         void *stream);
 
+/*
+ * pa_decode_attention_static -- pa_decode_attention for callers that cannot
+ * allocate device memory where they run the decode step.
+ *
+ * The pages have no counterpart: tiny-vllm allocates its buffers once in
+ * main().  This entry point serves callers that may not call cudaMalloc at
+ * that point -- an engine whose memory map is fixed at start-up, a serving
+ * thread that must not trigger the device-wide synchronisation an allocation
+ * can cause, a plugin handed only its tensors.  It computes exactly what
+ * pa_decode_attention computes, with the same arguments minus the workspace:
+ * the scratch is a 16 MiB array in the library's device memory, held by every
+ * GPU that loads the library until the process exits.
+ *   - num_seqs at most PA_STATIC_MAX_SEQS; more returns PA_ERR_WORKSPACE.
+ *   - Allocates nothing: no cudaMalloc / cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; each call clears its work counter on `stream` first.  Calls
+ *     whose kernels could overlap on the GPU race on the array: serialise them.
+ */
+#define PA_STATIC_MAX_SEQS 512
+int pa_decode_attention_static(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                               int num_blocks, const int32_t *block_table, int n_layers,
+                               int max_blocks_per_seq, const int32_t *context_lens,
+                               int num_seqs, int layer, float scale, int32_t *err,
+                               void *stream);
+
 /* Bytes of workspace pa_decode_attention needs on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq);
 

@@ -663,3 +663,68 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
     return PA_ERR_CUDA;
   return PA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Decode attention without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// decode step: an engine whose memory map is fixed when it starts, a caller
+// that may not call cudaMalloc on its serving thread because that call can
+// synchronise the whole device, or a plugin handed only the tensors it works
+// on.  For them the split partials live in one file-scope device array that
+// every GPU loading this library holds until the process exits.  The array
+// is shared by all calls on a device, so calls whose kernels overlap on the
+// GPU (two streams, two host threads) race on it and must be serialised by
+// the caller.  Its work counter is cleared at the start of every call; the
+// rest is rewritten before it is read.
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB per device
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of the array on the current device, looked up once per
+// device (host code may not use the symbol itself: on the host it names a
+// stand-in, not device memory).
+int static_scratch(int device, void **ptr) {
+  static void *addr[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
+    addr[device] = p;
+  }
+  *ptr = addr[device];
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_attention_static(uint16_t *out, const uint16_t *q,
+                                          const uint16_t *kv_cache, int num_blocks,
+                                          const int32_t *block_table, int n_layers,
+                                          int max_blocks_per_seq, const int32_t *context_lens,
+                                          int num_seqs, int layer, float scale, int32_t *err,
+                                          void *stream) {
+  if (num_seqs < 0 || num_seqs > PA_STATIC_MAX_SEQS) return PA_ERR_WORKSPACE;
+  if (num_seqs == 0) return pa_decode_attention(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                                max_blocks_per_seq, context_lens, 0, layer, scale,
+                                                nullptr, 0, err, stream);
+  DeviceInfo di;
+  int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  void *scratch = nullptr;
+  rc = static_scratch(di.device, &scratch);
+  if (rc != PA_OK) return rc;
+  // the work counter (first 256 bytes) must read zero when the kernels start
+  if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return pa_decode_attention(out, q, kv_cache, num_blocks, block_table, n_layers,
+                             max_blocks_per_seq, context_lens, num_seqs, layer, scale, scratch,
+                             kStaticScratchBytes, err, stream);
+}
