@@ -17,6 +17,7 @@
 //                                 runs, then waits for it and stores K/V in
 //                                 the slot the table names.
 #include <climits>
+#include <cmath>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
@@ -27,7 +28,14 @@ namespace {
 constexpr int kScanCta = 1024;
 constexpr int kStoreThreads = (kHkv + kHq) * 8;   // 8 threads per head row, 40 rows
 
+// Llama-3-scaled RoPE inverse frequencies of the 32 pairs, computed on the
+// host in fp64 and passed by value (no device memory involved).
+struct RopeFreqs {
+  double f[PA_HEAD_DIM / 2];
+};
+
 struct AppendParams {
+  RopeFreqs freqs;
   const uint16_t *k_new;
   const uint16_t *v_new;
   uint16_t *q;                 // may be null
@@ -68,8 +76,9 @@ __device__ __forceinline__ int cta_exclusive_count(bool flag, int *tot, int *tot
 }
 
 __global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) {
-  pdl_launch_dependents();   // the store kernel may start its rotations now
   __shared__ int tot[kScanCta / 32];
+  pdl_wait_primary();        // the table and free list may come from the previous kernel
+  pdl_launch_dependents();   // the store kernel may start its rotations now
   const int cap = p.max_blocks * kBs;
   // a count outside [0, num_blocks] never indexes past the free list
   const int fc0 = min(max(*p.free_count, 0), p.num_blocks);
@@ -106,16 +115,24 @@ __global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) 
 // theta 500000, factor 32, low_freq_factor 1, high_freq_factor 4, original
 // context 8192.  Wavelengths under 8192/4 keep their frequency, those over
 // 8192/1 are slowed by the factor, and the band between blends the two
-// linearly in 8192/wavelength.
-__device__ double llama3_inv_freq(int i) {
+// linearly in 8192/wavelength.  Host code, run once.
+RopeFreqs llama3_freqs() {
+  RopeFreqs r;
   const double theta = 500000.0, factor = 32.0, low = 1.0, high = 4.0, orig = 8192.0;
   const double two_pi = 6.283185307179586476925;
-  const double f = pow(theta, -static_cast<double>(2 * i) / kD);
-  const double wavelen = two_pi / f;
-  if (wavelen < orig / high) return f;
-  if (wavelen > orig / low) return f / factor;
-  const double w = (orig / wavelen - low) / (high - low);
-  return (1.0 - w) * (f / factor) + w * f;
+  for (int i = 0; i < kD / 2; ++i) {
+    const double f = std::pow(theta, -static_cast<double>(2 * i) / kD);
+    const double wavelen = two_pi / f;
+    if (wavelen < orig / high) {
+      r.f[i] = f;
+    } else if (wavelen > orig / low) {
+      r.f[i] = f / factor;
+    } else {
+      const double w = (orig / wavelen - low) / (high - low);
+      r.f[i] = (1.0 - w) * (f / factor) + w * f;
+    }
+  }
+  return r;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
@@ -162,11 +179,16 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
     return;
   }
   if (tid < kD / 2) {
-    // angle in fp64 so that positions in the tens of thousands keep their
-    // phase; the rotation itself runs in fp32
-    double sn, cn;
-    sincos(static_cast<double>(pos) * llama3_inv_freq(tid), &sn, &cn);
-    cs[tid] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
+    // the angle pos * f is formed and reduced modulo 2*pi in fp64, so that
+    // positions in the tens of thousands keep their phase; the reduced angle
+    // (|r| <= pi) goes through fp32 sincosf and the rotation runs in fp32
+    const double two_pi_hi = 6.283185307179586232, two_pi_lo = 2.4492935982947064e-16;
+    const double a = static_cast<double>(pos) * p.freqs.f[tid];
+    const double k = rint(a * 0.15915494309189533577);
+    const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, a));
+    float sn, cn;
+    sincosf(static_cast<float>(red), &sn, &cn);
+    cs[tid] = make_float2(cn, sn);
   }
   __syncthreads();
 
@@ -191,13 +213,16 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
   if (tid < kTokRowBytes / 16)
     v = reinterpret_cast<const uint4 *>(p.v_new + static_cast<size_t>(s) * kHkv * kD)[tid];
 
-  pdl_wait_primary();   // the table entry of a new page is written by the allocation kernel
+  // the entry of a page that starts now is written by the allocation kernel;
+  // an existing page's entry was written before that kernel started
+  if (pos % kBs == 0) pdl_wait_primary();
   const int blk =
       p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + pos / kBs];
   if (blk < 0 || blk >= p.num_blocks) {
     // a new page that was refused or popped invalid is reported by the
     // allocation kernel; an invalid existing entry is reported here
     if (tid == 0 && pos % kBs != 0) report(p.err, PA_DEV_BAD_BLOCK);
+    pdl_wait_primary();   // this grid ends after the allocation kernel
     return;
   }
   unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
@@ -209,6 +234,7 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
   }
   if (tid < kTokRowBytes / 16)
     reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v;
+  pdl_wait_primary();   // this grid ends after the allocation kernel
 }
 
 struct FreeParams {
@@ -305,7 +331,9 @@ extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
   const int rc = current_device(&di);
   if (rc != PA_OK) return rc;
 
+  static const RopeFreqs freqs = llama3_freqs();
   AppendParams prm;
+  prm.freqs = freqs;
   prm.k_new = k_new;
   prm.v_new = v_new;
   prm.q = q_or_null;
@@ -322,8 +350,8 @@ extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
   prm.layer = layer;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  append_alloc_kernel<<<1, kScanCta, 0, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pdl(append_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (launch_pdl(append_store_kernel, dim3(num_seqs), dim3(kStoreThreads), 0, st, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;

@@ -425,12 +425,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 // Combines the partials of every sequence cut into several pieces, and
 // returns the chunk counter to zero for the next call.  Grid (num_seqs, 32
-// q heads), 16 warps = 16 interleaved shares of the partials, lane = 2 dims.
-// Each thread folds its share into a running (m, l, o) as it loads it (one
-// round of independent loads), then the 16 shares are combined in shared
-// memory.
-constexpr int kMergeThreads = 512;
-constexpr int kShares = kMergeThreads / 32;
+// q heads), kShares warps = interleaved shares of the partials, lane = 2
+// dims.  Each thread folds its share into a running (m, l, o) as it loads it
+// (one round of independent loads), then the shares are combined in shared
+// memory.  There are about 4 partials per CTA of the split kernel in all, so
+// a few sequences have many partials each (16 shares) and a large batch has
+// a few each (4 shares, so the many small CTAs fit in one wave).
 
 __device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, float &s_old,
                                      float &s_new) {
@@ -441,7 +441,8 @@ __device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, flo
   m = mn;
 }
 
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
+template <int kShares>
+__global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams p) {
   pdl_launch_dependents();   // the next kernel may start its own set-up
   pdl_wait_primary();
   __shared__ float sm_m[kShares], sm_l[kShares];
@@ -658,9 +659,10 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_pdl(decode_merge_kernel, dim3(num_seqs, kHq), dim3(kMergeThreads), 0, st, prm) !=
-      cudaSuccess)
-    return PA_ERR_CUDA;
+  const cudaError_t e =
+      num_seqs >= 32 ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
+                     : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 
