@@ -68,6 +68,27 @@ def append_bytes(n: int) -> int:
     return n * (1024 * 4 + 4096 * 2 + 8)
 
 
+# ------------------------------------------------------ replica aggregation
+def aggregate_ranks(ms_per_step: float, e2e_s: float, bytes_per_step: int, seqs: int, dist=None):
+    """Whole-job numbers over independent replicas: every rank ran the same
+    workload on its own GPU; the job's step time is the slowest rank's, and
+    the throughput counts the work of all ranks."""
+    import torch
+    world = dist.get_world_size() if dist is not None else 1
+    t = torch.tensor([ms_per_step, e2e_s], dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e = float(t[0]), float(t[1])
+    return {
+        "ms_per_step": ms,
+        "e2e_s": e2e,
+        "gbs": world * bytes_per_step / (ms / 1e3) / 1e9,
+        "e2e_gbs": world * bytes_per_step / e2e / 1e9,
+        "seq_steps_per_s": world * seqs / (ms / 1e3),
+        "world": world,
+    }
+
+
 # --------------------------------------------------------- clock sampling
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -457,16 +478,13 @@ def run_gpu(args, rank, world, dist):
         h2d += h_kv[0].numel() * 2 + h_kv[1].numel() * 2 + h_kv[2].numel() * 4
     d2h = h_out.numel() * 2
 
-    stats = torch.tensor([ms, e2e_s], dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(stats, op=dist.ReduceOp.MAX)
-    ms, e2e_s = float(stats[0]), float(stats[1])
+    bytes_step = st.bytes_per_step()
+    agg = aggregate_ranks(ms, e2e_s, bytes_step, w.num_seqs, dist)
+    ms, e2e_s, gbs = agg["ms_per_step"], agg["e2e_s"], agg["gbs"]
     sampler.stop()
     if rank != 0:
         return
 
-    bytes_step = st.bytes_per_step()
-    gbs = world * bytes_step / (ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
     attn_bytes = attention_bytes(w.attn_context_lens)
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
@@ -486,7 +504,7 @@ def run_gpu(args, rank, world, dist):
         "accumulate": "fp32",
         "data": "synthetic",
         "pct_of_peak": 100.0 * gbs / (peak * world),
-        "seq_steps_per_s": world * w.num_seqs / (ms / 1e3),
+        "seq_steps_per_s": agg["seq_steps_per_s"],
         "config": {
             "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
             "num_seqs": w.num_seqs,
@@ -513,7 +531,7 @@ def run_gpu(args, rank, world, dist):
                       "replay stream",
         },
         "e2e": {
-            "value": world * bytes_step / e2e_s / 1e9,
+            "value": agg["e2e_gbs"],
             "unit": "GB/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,

@@ -75,6 +75,7 @@ struct __align__(1024) Smem {
 struct DecodeParams {
   __nv_bfloat16 *out;
   const uint16_t *q;
+  const unsigned char *kv;   // the pool, for L2 prefetches (loads go through the tensor map)
   const int32_t *block_table;
   const int32_t *context_lens;
   int *chunk_counter;  // zero between calls; reset by the merge kernel
@@ -124,6 +125,54 @@ __device__ __forceinline__ int first_seq_at(const int *prefix, int n, int b) {
   return lo;
 }
 
+// Block prefix over all sequences into sm.prefix[1..num_seqs] (prefix[0] is
+// set by the caller); returns the total.  Every thread of the CTA calls it.
+__device__ __forceinline__ int block_prefix(const DecodeParams &p, Smem &sm, int tid, int warp,
+                                            int lane, bool report_range) {
+  int carry = 0;
+  for (int base = 0; base < p.num_seqs; base += kScanThreads) {
+    const int i = base + tid;
+    int nb = 0;
+    if (tid < kScanThreads && i < p.num_seqs) {
+      const int t = p.context_lens[i];
+      if (report_range && (t < 0 || t > p.max_blocks * kBs)) report(p.err, PA_DEV_CTX_RANGE);
+      nb = (clamped_ctx(p, i) + kBs - 1) / kBs;
+    }
+    int incl = nb;
+    if (tid < kScanThreads) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (lane == 31) sm.warp_sum[warp] = incl;
+    }
+    __syncthreads();
+    int before = 0, chunk = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const int v = sm.warp_sum[w];
+      if (w < warp) before += v;
+      chunk += v;
+    }
+    if (tid < kScanThreads && i < p.num_seqs) sm.prefix[i + 1] = carry + before + incl;
+    carry += chunk;
+    __syncthreads();
+  }
+  return carry;
+}
+
+// Sequence holding global block b (b < total): smallest s with prefix[s+1] > b.
+__device__ __forceinline__ int seq_of_block(const int *prefix, int n, int b) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid + 1] > b) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -153,44 +202,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                   line * 32);
     }
   }
+  // A plan from the context lengths as they read now steers L2 prefetches of
+  // this CTA's first blocks, so HBM starts streaming while the previous
+  // kernel finishes.  The lengths or table may still change: the values only
+  // pick which valid pool lines to prefetch; the real plan is made after the
+  // wait.
+  if (tid == 0) sm.prefix[0] = 0;
+  {
+    const int nb_spec = block_prefix(p, sm, tid, warp, lane, false);
+    if (warp == kConsumerWarps && lane < kStages && nb_spec > 0) {
+      const int c_spec = chunk_blocks(nb_spec, G);
+      const int b = blockIdx.x * c_spec + lane;
+      if (blockIdx.x < (nb_spec + c_spec - 1) / c_spec && b < min(nb_spec, (blockIdx.x + 1) * c_spec)) {
+        const int s = seq_of_block(sm.prefix, p.num_seqs, b);
+        const int j = b - sm.prefix[s];
+        if (j >= 0 && j < p.max_blocks) {
+          const int blk =
+              p.block_table[(static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks + j];
+          if (blk >= 0 && blk < p.num_blocks)
+            prefetch_bulk_l2(p.kv + static_cast<size_t>(blk) * kBlockBytes, kBlockBytes);
+        }
+      }
+    }
+  }
   pdl_launch_dependents();   // the merge kernel may take its place in the queue
   // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
-  // ---- block prefix over all sequences -------------------------------------
-  int carry = 0;
-  for (int base = 0; base < p.num_seqs; base += kScanThreads) {
-    const int i = base + tid;
-    int nb = 0;
-    if (tid < kScanThreads && i < p.num_seqs) {
-      const int t = p.context_lens[i];
-      if ((t < 0 || t > p.max_blocks * kBs) && blockIdx.x == 0) report(p.err, PA_DEV_CTX_RANGE);
-      nb = (clamped_ctx(p, i) + kBs - 1) / kBs;
-    }
-    int incl = nb;
-    if (tid < kScanThreads) {
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (lane == 31) sm.warp_sum[warp] = incl;
-    }
-    __syncthreads();
-    int before = 0, chunk = 0;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const int v = sm.warp_sum[w];
-      if (w < warp) before += v;
-      chunk += v;
-    }
-    if (tid < kScanThreads && i < p.num_seqs) sm.prefix[i + 1] = carry + before + incl;
-    carry += chunk;
-    __syncthreads();
-  }
-  if (tid == 0) sm.prefix[0] = 0;
-  __syncthreads();
-  const int nb_total = carry;
+  const int nb_total = block_prefix(p, sm, tid, warp, lane, blockIdx.x == 0);
   const int C = chunk_blocks(nb_total, G);
   const int n_chunks = max(1, (nb_total + C - 1) / C);
 
@@ -642,6 +681,7 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.q = q;
+  prm.kv = reinterpret_cast<const unsigned char *>(kv_cache);
   prm.block_table = block_table;
   prm.context_lens = context_lens;
   prm.chunk_counter = reinterpret_cast<int *>(ws + w.counter_off);
