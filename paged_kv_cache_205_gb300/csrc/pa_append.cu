@@ -186,9 +186,12 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
     const double a = static_cast<double>(pos) * p.freqs.f[tid];
     const double k = rint(a * 0.15915494309189533577);
     const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, a));
+    const float rf = static_cast<float>(red);
+    const float rerr = static_cast<float>(red - static_cast<double>(rf));   // |rerr| <= 2^-23
     float sn, cn;
-    sincosf(static_cast<float>(red), &sn, &cn);
-    cs[tid] = make_float2(cn, sn);
+    sincosf(rf, &sn, &cn);
+    // first-order correction for the part of the angle fp32 could not hold
+    cs[tid] = make_float2(fmaf(-sn, rerr, cn), fmaf(cn, rerr, sn));
   }
   __syncthreads();
 

@@ -49,16 +49,29 @@ def _append(st, k, v, q, ctx, layer):
     return qd
 
 
+# The kernels rotate in fp32: a rotated element a*c - b*s carries an absolute
+# error up to about 2^-22 (|a| + |b|) before its bf16 rounding, so where the
+# two terms cancel it may sit more than one bf16 ulp from the fp64 oracle.
+# Inputs here are N(0,1) in bf16 (|a|, |b| < 6): allow one ulp, or 1.5e-5.
+ROPE_ABS = 1.5e-5
+
+
+def assert_rope_close(gpu_bits, ref_bits, what):
+    d = ulp_diff(gpu_bits, ref_bits)
+    absd = np.abs(oracle.bf16_to_f64(gpu_bits) - oracle.bf16_to_f64(ref_bits))
+    bad = (d > 1) & ~(absd <= ROPE_ABS)
+    assert not np.any(bad), f"{what}: {int(bad.sum())} elements off by up to {d.max()} ulp / {absd.max():.2e}"
+    assert np.mean(d > 0) < 1e-2, f"{what}: {np.mean(d > 0):.3%} elements differ"
+
+
 def _compare_pools(gpu_pool, ref_pool):
-    """V and untouched bytes exact, K within one ulp."""
+    """V and untouched bytes exact; K within the fp32 rotation bound."""
     same = gpu_pool == ref_pool
     nan_both = (gpu_pool == wl.BF16_NAN) & (ref_pool == wl.BF16_NAN)
     same |= nan_both
     assert np.all(same[:, 1]), "V stores differ"
     if not np.all(same[:, 0]):
-        d = ulp_diff(gpu_pool[:, 0], ref_pool[:, 0])
-        assert d.max() <= 1, f"K differs by {d.max()} ulp"
-        assert np.mean(d > 0) < 1e-2
+        assert_rope_close(gpu_pool[:, 0], ref_pool[:, 0], "K")
 
 
 def test_worked_example_append_then_free():
@@ -138,8 +151,7 @@ def test_append_with_q_matches_oracle(seed, positions):
         q2, p2, b2, f2, c2, e = oracle.kv_append_rope(k, v, q, ref[0], ref[1], ctx, layer, ref[2], ref[3])
         assert e == 0
         ref = (p2, b2, f2, c2)
-        dq = ulp_diff(host_bits(qd), q2)
-        assert dq.max() <= 1 and np.mean(dq > 0) < 1e-2
+        assert_rope_close(host_bits(qd), q2, f"q layer {layer}")
     gp, gb, gf, gc, ge = st.host()
     assert ge == 0
     assert np.array_equal(gb, ref[1]) and np.array_equal(gf, ref[2]) and gc == ref[3]
@@ -163,7 +175,7 @@ def test_capacity_and_bad_entry_errors_match_oracle():
     assert ge == e2 == (oracle.ERR_CTX_RANGE | oracle.ERR_BAD_BLOCK)
     assert np.array_equal(gb, b2) and gc == c2
     _compare_pools(gp, p2)
-    assert ulp_diff(host_bits(qd)[1:], q2[1:]).max() <= 1
+    assert_rope_close(host_bits(qd)[1:], q2[1:], "q")
     assert np.array_equal(host_bits(qd)[0], q[0])      # out-of-range position: q untouched
 
 
