@@ -47,6 +47,7 @@ constexpr int kMaxSeqs = 2048;                             // block prefix kept 
 constexpr int kMaxGrid = 512;
 constexpr int kChunksPerCta = 4;                           // average chunks a CTA takes
 constexpr int kHeadTileBytes = 2 * kBs * kHeadRowBytes;    // K and V of one kv head: 4 KiB
+constexpr int kPrefetchBlocks = 4;                         // first blocks prefetched before the wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kSegStart = 1;   // first block of a (chunk, sequence) piece
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (tid == 0) sm.prefix[0] = 0;
   {
     const int nb_spec = block_prefix(p, sm, tid, warp, lane, false);
-    if (warp == kConsumerWarps && lane < kStages && nb_spec > 0) {
+    if (warp == kConsumerWarps && lane < kPrefetchBlocks && nb_spec > 0) {
       const int c_spec = chunk_blocks(nb_spec, G);
       const int b = blockIdx.x * c_spec + lane;
       if (blockIdx.x < (nb_spec + c_spec - 1) / c_spec && b < min(nb_spec, (blockIdx.x + 1) * c_spec)) {
@@ -242,10 +243,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int k = blockIdx.x;
     while (k < n_chunks && ok) {
       int next = 0;
-      if (lane == 0) {
-        next = G + atomicAdd(p.chunk_counter, 1);   // lands while chunk k streams
-        if (next < G) next = n_chunks;               // a counter that was never zeroed
-      }
+      // the next chunk's index lands while chunk k streams; nothing may test
+      // it before the chunk is issued, or lane 0 stalls on the round trip
+      if (lane == 0) next = G + atomicAdd(p.chunk_counter, 1);
       const int b0 = k * C;
       const int b1 = min(nb_total, b0 + C);
       const bool last_chunk = (k == n_chunks - 1);
@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
       k = __shfl_sync(0xffffffffu, next, 0);
+      if (k < G) k = n_chunks;   // a counter that was never zeroed
     }
     if (lane == 0) {
       if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
@@ -468,8 +469,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // dims.  Each thread folds its share into a running (m, l, o) as it loads it
 // (one round of independent loads), then the shares are combined in shared
 // memory.  There are about 4 partials per CTA of the split kernel in all, so
-// a few sequences have many partials each (16 shares) and a large batch has
-// a few each (4 shares, so the many small CTAs fit in one wave).
+// a few sequences have many partials each (16 shares) and a larger batch a
+// few each (4 shares: small CTAs, which leave room on the SMs for the next
+// split kernel's CTAs to start their prefetches).
 
 __device__ __forceinline__ void fold(float mk, float lk, float &m, float &l, float &s_old,
                                      float &s_new) {
@@ -495,13 +497,29 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
   const size_t slot0 = static_cast<size_t>(mt.x);
   float m = neg_inf(), l = 0.f, so, sn;
   float2 o = make_float2(0.f, 0.f);
-#pragma unroll 8
-  for (int k = share; k < np; k += kShares) {
-    const float2 mk = p.ml[(slot0 + k) * kHq + h];
-    const float2 a = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
-    fold(mk.x, mk.y, m, l, so, sn);
-    o.x = fmaf(o.x, so, a.x * sn);
-    o.y = fmaf(o.y, so, a.y * sn);
+  // loads are issued kBatch partials at a time before any of them is folded,
+  // so a share costs one L2 round trip per kBatch partials
+  constexpr int kBatch = 8;
+  for (int k0 = share; k0 < np; k0 += kShares * kBatch) {
+    float2 mk[kBatch], a[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int k = k0 + b * kShares;
+      if (k < np) {
+        mk[b] = p.ml[(slot0 + k) * kHq + h];
+        a[b] = p.acc[((slot0 + k) * kHq + h) * (kD / 2) + lane];
+      } else {
+        mk[b] = make_float2(neg_inf(), 0.f);
+        a[b] = make_float2(0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (mk[b].x == neg_inf()) continue;
+      fold(mk[b].x, mk[b].y, m, l, so, sn);
+      o.x = fmaf(o.x, so, a[b].x * sn);
+      o.y = fmaf(o.y, so, a[b].y * sn);
+    }
   }
   if (lane == 0) {
     sm_m[share] = m;
@@ -700,8 +718,8 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   const cudaError_t e =
-      num_seqs >= 32 ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
-                     : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
+      num_seqs >= 8 ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
+                    : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
