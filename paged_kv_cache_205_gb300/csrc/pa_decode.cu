@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // pick which valid pool lines to prefetch; the real plan is made after the
   // wait.
   if (tid == 0) sm.prefix[0] = 0;
+  const int nb_spec = block_prefix(p, sm, tid, warp, lane, false);
   {
-    const int nb_spec = block_prefix(p, sm, tid, warp, lane, false);
     if (warp == kConsumerWarps && lane < kPrefetchBlocks && nb_spec > 0) {
       const int c_spec = chunk_blocks(nb_spec, G);
       const int b = blockIdx.x * c_spec + lane;
@@ -230,7 +230,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
-  const int nb_total = block_prefix(p, sm, tid, warp, lane, blockIdx.x == 0);
+  // ---- the real plan.  The producer reads the block ids of its first chunk
+  // at the places the speculative plan puts them (these reads come after the
+  // wait, so they are current) while every thread checks that each
+  // sequence's block count still matches the speculative prefix.  If all
+  // match, that prefix is the real one and the ids are used as read;
+  // otherwise the prefix is rebuilt and the ids are read again.
+  int pre_blk = -1;
+  const int c_spec = nb_spec > 0 ? chunk_blocks(nb_spec, G) : 1;
+  const int b_pre = blockIdx.x * c_spec + lane;
+  if (warp == kConsumerWarps && nb_spec > 0 && b_pre < min(nb_spec, (blockIdx.x + 1) * c_spec)) {
+    const int s = seq_of_block(sm.prefix, p.num_seqs, b_pre);
+    const int j = b_pre - sm.prefix[s];
+    if (j >= 0 && j < p.max_blocks)
+      pre_blk = p.block_table[(static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks + j];
+  }
+  int changed = 0;
+  for (int i = tid; i < p.num_seqs; i += kThreads) {
+    const int t = p.context_lens[i];
+    if (blockIdx.x == 0 && (t < 0 || t > p.max_blocks * kBs)) report(p.err, PA_DEV_CTX_RANGE);
+    const int nb = (min(max(t, 0), p.max_blocks * kBs) + kBs - 1) / kBs;
+    changed |= (nb != sm.prefix[i + 1] - sm.prefix[i]);
+  }
+  const bool plan_kept = __syncthreads_or(changed) == 0;
+  const int nb_total = plan_kept ? nb_spec : block_prefix(p, sm, tid, warp, lane, false);
   const int C = chunk_blocks(nb_total, G);
   const int n_chunks = max(1, (nb_total + C - 1) / C);
 
@@ -271,10 +294,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int32_t *row =
             p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
         for (int j0 = jb; j0 < je && ok; j0 += 32) {
-          const int my_blk = (j0 + lane < je) ? row[j0 + lane] : 0;
           const int cnt = min(32, je - j0);
+          // the first 32 ids of this CTA's first chunk were read with the plan
+          const int off0 = B + j0 - b0;
+          const bool use_pre =
+              plan_kept && k == static_cast<int>(blockIdx.x) && off0 + cnt <= 32;
+          int my_blk = 0;
+          if (!use_pre && j0 + lane < je) my_blk = row[j0 + lane];
           for (int e = 0; e < cnt; ++e) {
-            const int blk = __shfl_sync(0xffffffffu, my_blk, e);
+            const int blk = use_pre ? __shfl_sync(0xffffffffu, pre_blk, off0 + e)
+                                    : __shfl_sync(0xffffffffu, my_blk, e);
             const int j = j0 + e;
             int good = 1;
             if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
