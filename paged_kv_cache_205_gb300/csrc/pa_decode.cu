@@ -67,6 +67,7 @@ struct StageDesc {
 struct __align__(1024) Smem {
   unsigned char kv[kStages][kBlockBytes];
   int prefix[kMaxSeqs + 1];      // prefix[s] = blocks of sequences 0..s-1
+  unsigned char tail[kMaxSeqs];  // tokens in the last block of sequence s (1..16)
   StageDesc desc[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -249,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   for (int i = tid; i < p.num_seqs; i += kThreads) {
     const int t = p.context_lens[i];
     if (blockIdx.x == 0 && (t < 0 || t > p.max_blocks * kBs)) report(p.err, PA_DEV_CTX_RANGE);
-    const int nb = (min(max(t, 0), p.max_blocks * kBs) + kBs - 1) / kBs;
+    const int tc = min(max(t, 0), p.max_blocks * kBs);
+    const int nb = (tc + kBs - 1) / kBs;
+    sm.tail[i] = static_cast<unsigned char>(tc - (nb - 1) * kBs);
     changed |= (nb != sm.prefix[i + 1] - sm.prefix[i]);
   }
   const bool plan_kept = __syncthreads_or(changed) == 0;
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           continue;
         }
         if (B >= b1) break;   // last chunk: only empty sequences may follow
-        const int T = clamped_ctx(p, s);
+        const int tail = sm.tail[s];
         const int jb = max(b0, B) - B;
         const int je = min(b1, B + nb) - B;
         const int k_first = B / C;
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (lane == 0) {
               StageDesc d;
               d.seq = s;
-              d.n_valid = min(kBs, T - j * kBs);
+              d.n_valid = (j == nb - 1) ? tail : kBs;
               if (!valid) d.n_valid = -d.n_valid;   // consumers skip it
               d.flags = (j == jb ? kSegStart : 0) | (j == je - 1 ? kSegEnd : 0);
               d.n_parts = n_parts;
