@@ -56,25 +56,32 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// One potentially blocking test of the phase with the given parity: the
+// thread is suspended (it issues nothing) until the phase completes or about
+// `suspend_ns` pass.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity,
+                                              uint32_t suspend_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait on the phase with the given parity.  Returns false when the
-// time limit ran out (the caller then reports PA_DEV_TIMEOUT).
+// Bounded wait on the phase with the given parity.  Waiting warps sleep in
+// the barrier instead of spinning, so they leave the issue slots to the warps
+// doing work.  Returns false when the time limit ran out (the caller then
+// reports PA_DEV_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  constexpr uint32_t kSuspendNs = 200000;   // re-check the time limit every 0.2 ms
+  if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
