@@ -268,10 +268,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
     int k = blockIdx.x;
     while (k < n_chunks && ok) {
+      // the next chunk's index is asked for once the chunk's first copy is in
+      // flight (every CTA asks at about the same moment, and the answers
+      // queue at one L2 address), and lands while the chunk streams
       int next = 0;
-      // the next chunk's index lands while chunk k streams; nothing may test
-      // it before the chunk is issued, or lane 0 stalls on the round trip
-      if (lane == 0) next = G + atomicAdd(p.chunk_counter, 1);
+      bool asked = false;
       const int b0 = k * C;
       const int b1 = min(nb_total, b0 + C);
       const bool last_chunk = (k == n_chunks - 1);
@@ -338,6 +339,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (valid && lane < kHkv)   // one 4 KiB tile per kv head, 8 lanes in parallel
               tma_load_5d(sm.kv[stage] + lane * kHeadTileBytes, &kv_map, 0, lane, 0, 0, blk,
                           &sm.full[stage]);
+            if (!asked) {
+              if (lane == 0) next = G + atomicAdd(p.chunk_counter, 1);
+              asked = true;
+            }
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
@@ -345,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
         }
       }
+      if (!asked && lane == 0) next = G + atomicAdd(p.chunk_counter, 1);
       k = __shfl_sync(0xffffffffu, next, 0);
       if (k < G) k = n_chunks;   // a counter that was never zeroed
     }
