@@ -287,3 +287,16 @@ def test_too_many_sequences_is_refused():
     with pytest.raises(pk.PagedKVError) as e:
         pk.pa_decode_attention(q, q, pool, bt, ctx, 0, 0.125, ws, err)
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("grid", [0, 40, 7])
+def test_large_batch_merge_shape(grid):
+    """From 128 sequences on, partials are merged one CTA per sequence; a
+    small grid forces many sequences to be split into several pieces."""
+    rng = np.random.default_rng(61 + grid)
+    ctx = rng.integers(0, 300, size=160)
+    w, pool, q = _small_case(62 + grid, ctx, q_scale=2.0)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, grid=grid)
+    assert err == 0
+    assert_attention_close(out, ref, f"160 sequences, grid {grid}")
