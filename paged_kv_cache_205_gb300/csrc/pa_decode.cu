@@ -585,64 +585,6 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
 }
 
 
-// The same merge for a large batch, where sequences have a few partials
-// each: one CTA per sequence, thread = (q head, 8 dims), partials loaded 8
-// at a time.  256 CTAs instead of 8192 for 256 sequences.
-constexpr int kMergeSeqThreads = kHq * 8;
-
-__global__ void __launch_bounds__(kMergeSeqThreads) decode_merge_per_seq(DecodeParams p) {
-  pdl_launch_dependents();   // the next kernel may start its own set-up
-  pdl_wait_primary();
-  const int s = blockIdx.x;
-  const int h = threadIdx.x >> 3, part = threadIdx.x & 7;
-  if (s == 0 && threadIdx.x == 0) *p.chunk_counter = 0;   // the split kernel is done
-  const int2 mt = p.meta[s];
-  const int np = mt.y;
-  if (np <= 1) return;
-  const size_t slot0 = static_cast<size_t>(mt.x);
-  const float4 *acc4 = reinterpret_cast<const float4 *>(p.acc);
-  float m = neg_inf(), l = 0.f, so, sn, o[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = 0.f;
-  constexpr int kBatch = 8;
-  for (int k0 = 0; k0 < np; k0 += kBatch) {
-    float2 mk[kBatch];
-    float4 a0[kBatch], a1[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const size_t row = (slot0 + k0 + b) * kHq + h;
-      if (k0 + b < np) {
-        mk[b] = p.ml[row];
-        a0[b] = acc4[row * (kD / 4) + 2 * part];
-        a1[b] = acc4[row * (kD / 4) + 2 * part + 1];
-      } else {
-        mk[b] = make_float2(neg_inf(), 0.f);
-        a0[b] = a1[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (mk[b].x == neg_inf()) continue;
-      fold(mk[b].x, mk[b].y, m, l, so, sn);
-      o[0] = fmaf(o[0], so, a0[b].x * sn);
-      o[1] = fmaf(o[1], so, a0[b].y * sn);
-      o[2] = fmaf(o[2], so, a0[b].z * sn);
-      o[3] = fmaf(o[3], so, a0[b].w * sn);
-      o[4] = fmaf(o[4], so, a1[b].x * sn);
-      o[5] = fmaf(o[5], so, a1[b].y * sn);
-      o[6] = fmaf(o[6], so, a1[b].z * sn);
-      o[7] = fmaf(o[7], so, a1[b].w * sn);
-    }
-  }
-  const float inv = 1.f / l;
-  uint4 v;
-  v.x = float2_to_bf16x2(o[0] * inv, o[1] * inv);
-  v.y = float2_to_bf16x2(o[2] * inv, o[3] * inv);
-  v.z = float2_to_bf16x2(o[4] * inv, o[5] * inv);
-  v.w = float2_to_bf16x2(o[6] * inv, o[7] * inv);
-  *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(s) * kHq + h) * kD + 8 * part) = v;
-}
-
 int g_grid_limit = 0;
 
 struct WsLayout {
@@ -813,14 +755,9 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  // about 4 partials per split CTA in all: the batch size says how many a
-  // sequence has, and so which merge shape has the shortest chain of loads
   const cudaError_t e =
-      num_seqs >= 128
-          ? launch_pdl(decode_merge_per_seq, dim3(num_seqs), dim3(kMergeSeqThreads), 0, st, prm)
-      : num_seqs >= 8
-          ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
-          : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
+      num_seqs >= 8 ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
+                    : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -291,8 +291,8 @@ def test_too_many_sequences_is_refused():
 
 @pytest.mark.parametrize("grid", [0, 40, 7])
 def test_large_batch_merge_shape(grid):
-    """From 128 sequences on, partials are merged one CTA per sequence; a
-    small grid forces many sequences to be split into several pieces."""
+    """A large batch where a small grid forces many sequences to be split
+    into several pieces, each merged per q head."""
     rng = np.random.default_rng(61 + grid)
     ctx = rng.integers(0, 300, size=160)
     w, pool, q = _small_case(62 + grid, ctx, q_scale=2.0)
