@@ -224,3 +224,64 @@ def test_decode_step_append_then_attention_over_new_token():
     assert ge == 0
     assert np.array_equal(gb, ref[1]) and np.array_equal(gf, ref[2]) and gc == ref[3]
     _compare_pools(gp, ref[0])
+
+
+def test_whole_decode_step_captured_in_one_graph():
+    """A ragged decode step (append with RoPE, then attention over ctx + 1,
+    for every layer) captured as one CUDA graph and replayed: each replay
+    re-appends the same token and must match the oracle."""
+    import torch
+    pk = _pk()
+    rng = np.random.default_rng(8)
+    w = wl.make_workload("ragged", seed=8, num_seqs=20, max_ctx=200, n_layers=3, num_blocks=1200)
+    pool = wl.make_pool_numpy(w, rng, poison=True)
+    st = DevState(pool, w.block_table, w.free_list, w.free_count)
+    n, L = w.num_seqs, w.n_layers
+    k = wl.normal_bf16(rng, (L, n, N_KV, D))
+    v = wl.normal_bf16(rng, (L, n, N_KV, D))
+    q = wl.normal_bf16(rng, (L, n, N_Q, D))
+    kd, vd = dev_bf16(k), dev_bf16(v)
+    q_in = dev_bf16(q)
+    qd = q_in.clone()
+    fc0 = st.fc.clone()
+    ctx, ctx1 = dev_i32(w.context_lens), dev_i32(w.context_lens + 1)
+    out = torch.zeros((L, n, N_Q, D), dtype=torch.bfloat16, device="cuda")
+    ws = workspace_for(n, w.max_blocks_per_seq)
+
+    def step():
+        qd.copy_(q_in)           # fresh q every replay (rotated in place)
+        st.fc.copy_(fc0)         # the same pages are taken again
+        for l in range(L):
+            pk.pa_kv_append_rope(kd[l], vd[l], qd[l], st.pool, st.bt, ctx, l, st.fl, st.fc, st.err)
+            pk.pa_decode_attention(out[l], qd[l], st.pool, st.bt, ctx1, l, w.scale, ws, st.err)
+
+    step()                        # eager warm-up outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+
+    ref = (pool, w.block_table, w.free_list, w.free_count)
+    outs = []
+    for l in range(L):
+        q2, p2, b2, f2, c2, e = oracle.kv_append_rope(k[l], v[l], q[l], ref[0], ref[1],
+                                                      w.context_lens, l, ref[2], ref[3])
+        assert e == 0
+        ref = (p2, b2, f2, c2)
+        o_ref, e = oracle.decode_attention(q2, p2, b2, w.context_lens + 1, l)
+        assert e == 0
+        outs.append(o_ref)
+    for rep in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(st.err.item()) == 0
+        for l in range(L):
+            assert_attention_close(host_f64(out[l]), outs[l], f"replay {rep} layer {l}")
+        gp, gb, gf, gc, ge = st.host()
+        assert np.array_equal(gb, ref[1]) and gc == ref[3]
+        _compare_pools(gp, ref[0])
