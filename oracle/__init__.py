@@ -88,6 +88,10 @@ def _load():
         lib.oracle_merge_partials.restype = None
         lib.oracle_kv_append_rope.argtypes = [P, P, P, P, I, P, I, I, P, I, I, P, P, P]
         lib.oracle_kv_append_rope.restype = I
+        lib.oracle_prefill_append_rope.argtypes = [P, P, P, P, P, I, P, I, I, P, I, I, P, P, P]
+        lib.oracle_prefill_append_rope.restype = I
+        lib.oracle_prefill_attention.argtypes = [P, P, P, P, I, P, I, I, P, I, I, D]
+        lib.oracle_prefill_attention.restype = I
         lib.oracle_free.argtypes = [P, I, P, I, I, P, P, P, I]
         lib.oracle_free.restype = I
         _lib = lib
@@ -201,6 +205,46 @@ def kv_append_rope(k_new, v_new, q, pool, block_table, context_lens, layer,
                                         _ptr(btc), n_layers, max_blocks, _ptr(ctx), n, layer,
                                         _ptr(flc), _ptr(fc), _ptr(inv))
     return qc, poolc, btc, flc, int(fc[0]), err
+
+
+def prefill_append_rope(k_new, v_new, q, cu_tokens, pool, block_table, context_lens, layer,
+                        free_list, free_count, num_blocks=None):
+    """Returns (q_rot or None, pool, block_table, free_list, free_count, err)
+    on copies; the inputs are not modified."""
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    qc = None if q is None else np.array(q, dtype=np.uint16, copy=True, order="C")
+    cu = _c(cu_tokens, np.int32)
+    poolc = np.array(pool, dtype=np.uint16, copy=True, order="C")
+    btc = np.array(block_table, dtype=np.int32, copy=True, order="C")
+    flc = np.array(free_list, dtype=np.int32, copy=True, order="C")
+    fc = np.array([free_count], dtype=np.int32)
+    ctx = _c(context_lens, np.int32)
+    inv = llama3_inv_freq()
+    n, n_layers, max_blocks = btc.shape
+    nb = poolc.shape[0] if num_blocks is None else num_blocks
+    err = _load().oracle_prefill_append_rope(_ptr(k_new), _ptr(v_new), _ptr(qc), _ptr(cu),
+                                             _ptr(poolc), nb, _ptr(btc), n_layers, max_blocks,
+                                             _ptr(ctx), n, layer, _ptr(flc), _ptr(fc), _ptr(inv))
+    return qc, poolc, btc, flc, int(fc[0]), err
+
+
+def prefill_attention(q, cu_tokens, pool, block_table, context_lens, layer, scale=0.125,
+                      num_blocks=None):
+    """out[rows][32][64] fp64 and the error bits."""
+    q = _c(q, np.uint16)
+    cu = _c(cu_tokens, np.int32)
+    pool = _c(pool, np.uint16)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    n, n_layers, max_blocks = bt.shape
+    nb = pool.shape[0] if num_blocks is None else num_blocks
+    out = np.zeros((q.shape[0], N_Q, HEAD_DIM), dtype=np.float64)
+    err = _load().oracle_prefill_attention(_ptr(out), _ptr(q), _ptr(cu), _ptr(pool), nb, _ptr(bt),
+                                           n_layers, max_blocks, _ptr(ctx), n, layer, float(scale))
+    if err < 0:
+        raise MemoryError("oracle allocation failed")
+    return out, err
 
 
 def free(seq_ids, block_table, context_lens, free_list, free_count, num_blocks):

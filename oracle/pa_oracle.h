@@ -85,6 +85,34 @@ int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
                           int32_t *free_list, int32_t *free_count,
                           const double *inv_freq);
 
+/* Prefill (a prompt chunk per sequence).  Tokens of all sequences are
+ * packed: those of sequence s are rows cu_tokens[s] .. cu_tokens[s+1]-1 of
+ * k_new / v_new [rows][8][64] and q [rows][32][64]; token i of s sits at
+ * position context_lens[s] + i.
+ *
+ * Append: positions are taken in (sequence, position) order; a position that
+ * starts a page pops the back of the free list.  A chunk that does not fit
+ * the sequence's table (context < 0 or context + tokens > max_blocks * 16)
+ * is refused whole (PAO_ERR_CTX_RANGE: nothing popped, stored or rotated).
+ * A refused page (free list empty) is -1 in the table and its tokens are not
+ * stored; q is rotated for every token of an accepted chunk. */
+int oracle_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                               uint16_t *q_or_null, const int32_t *cu_tokens,
+                               uint16_t *pool, int num_blocks, int32_t *block_table,
+                               int n_layers, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int layer,
+                               int32_t *free_list, int32_t *free_count,
+                               const double *inv_freq);
+
+/* Causal attention of every chunk token over positions 0..context+i of its
+ * sequence (the cached tokens and the chunk's tokens up to itself).
+ * out[rows][32][64] fp64. */
+int oracle_prefill_attention(double *out, const uint16_t *q, const int32_t *cu_tokens,
+                             const uint16_t *pool, int num_blocks,
+                             const int32_t *block_table, int n_layers,
+                             int max_blocks_per_seq, const int32_t *context_lens,
+                             int num_seqs, int layer, double scale);
+
 /* Release the blocks of finished sequences.  Returns error bits. */
 int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
                 int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
