@@ -159,6 +159,70 @@ int pa_decode_attention_static(uint16_t *out, const uint16_t *q, const uint16_t 
                                int num_seqs, int layer, float scale, int32_t *err,
                                void *stream);
 
+/*
+ * pa_prefill_append_rope -- append a prompt chunk per sequence to the paged
+ * cache (the prefill counterpart of pa_kv_append_rope).
+ *
+ * Page: "The path of one inference" (prefill pushes the whole prompt through
+ * at once, matrix x matrix; ropeKernel_llama3 is the prefill RoPE, paired with
+ * ropeKernelDecode) and "What is in the box" (16-token pages + block_table).
+ *
+ * Packed tokens: cu_tokens[num_seqs + 1] (device) is non-decreasing with
+ * cu_tokens[0] = 0 and cu_tokens[num_seqs] = total_tokens; the chunk of
+ * sequence s is rows cu_tokens[s] .. cu_tokens[s+1]-1 of
+ *   k_new, v_new [total_tokens][8][64] bf16, q [total_tokens][32][64] bf16,
+ * and row cu_tokens[s] + i sits at position context_lens[s] + i
+ * (context_lens[s] = tokens already cached for s; 0 for a fresh prompt).
+ *   1. Every position of a chunk that starts a page (position % 16 == 0)
+ *      takes a block from the back of the free list, in (sequence, position)
+ *      order, and writes it to block_table[s][layer][position / 16].
+ *   2. Each k_new row is rotated (rotate-half RoPE with the Llama-3-scaled
+ *      frequencies of pa_kv_append_rope), rounded to bf16 and stored with its
+ *      v_new row at slot position % 16 of its page.
+ *   3. If q_or_null is not NULL, every q row of an accepted chunk is rotated
+ *      in place at its position.
+ * Device errors: PA_DEV_CTX_RANGE (context < 0, context + chunk beyond
+ * max_blocks_per_seq * 16, or rows outside [0, total_tokens): the whole chunk
+ * is refused, nothing popped, stored or rotated), PA_DEV_FREE_UNDERFLOW (no
+ * block left: that page stays -1 and its tokens are not stored),
+ * PA_DEV_BAD_BLOCK (a table entry the chunk writes into is invalid: its
+ * tokens are not stored).  Two kernels on `stream`, the second started early
+ * with programmatic dependent launch.
+ */
+int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                           int total_tokens, const int32_t *cu_tokens,
+                           uint16_t *kv_cache, int num_blocks, int32_t *block_table,
+                           int n_layers, int max_blocks_per_seq,
+                           const int32_t *context_lens, int num_seqs, int layer,
+                           int32_t *free_list, int32_t *free_count, int32_t *err,
+                           void *stream);
+
+/*
+ * pa_prefill_attention -- causal attention of a prompt chunk per sequence
+ * over its pages (the prefill counterpart of pa_decode_attention).
+ *
+ * Page: "The path of one inference" (prefill: the whole prompt at once,
+ * matrix x matrix) and "What is in the box" (16-token pages + block_table;
+ * GQA ratio 4; online softmax).
+ *
+ * With the packed layout of pa_prefill_append_rope (q and out
+ * [total_tokens][32][64] bf16), for row r = cu_tokens[s] + i:
+ *   out[r][h] = sum_t softmax_t(scale * q[r][h] . K_t) V_t
+ * over positions t = 0 .. context_lens[s] + i of sequence s, read from block
+ * block_table[s][layer][t / 16], slot t % 16, kv head h / 4.  The chunk's own
+ * K/V must already be in the cache (pa_prefill_append_rope before this call
+ * on the same stream).  fp32 accumulation, output rounded to bf16.
+ * num_seqs is at most 2048 per call; no workspace.
+ * Device errors: PA_DEV_CTX_RANGE (a chunk that does not fit its table, or
+ * rows outside [0, total_tokens): its rows are not written),
+ * PA_DEV_BAD_BLOCK (that block's tokens are dropped), PA_DEV_TIMEOUT.
+ */
+int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_tokens,
+                         const int32_t *cu_tokens, const uint16_t *kv_cache, int num_blocks,
+                         const int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int layer, float scale,
+                         int32_t *err, void *stream);
+
 /* Bytes of workspace pa_decode_attention needs on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq);
 

@@ -30,4 +30,6 @@ from ._binding import (  # noqa: F401
     pa_error_string,
     pa_free,
     pa_kv_append_rope,
+    pa_prefill_append_rope,
+    pa_prefill_attention,
 )

@@ -26,6 +26,9 @@ PA_DEV_TIMEOUT = 16
 _EXPORTS = (
     "pa_kv_append_rope",
     "pa_decode_attention",
+    "pa_decode_attention_static",
+    "pa_prefill_append_rope",
+    "pa_prefill_attention",
     "pa_decode_workspace_size",
     "pa_free",
     "pa_decode_set_grid_limit",
@@ -64,6 +67,10 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_kv_append_rope.restype = I
         lib.pa_decode_attention.argtypes = [P, P, P, I, P, I, I, P, I, I, F, P, Z, P, P]
         lib.pa_decode_attention.restype = I
+        lib.pa_prefill_append_rope.argtypes = [P, P, P, I, P, P, I, P, I, I, P, I, I, P, P, P, P]
+        lib.pa_prefill_append_rope.restype = I
+        lib.pa_prefill_attention.argtypes = [P, P, I, P, P, I, P, I, I, P, I, I, F, P, P]
+        lib.pa_prefill_attention.restype = I
         lib.pa_decode_workspace_size.argtypes = [I, I]
         lib.pa_decode_workspace_size.restype = Z
         lib.pa_free.argtypes = [P, I, P, I, I, P, P, P, I, P, P]
@@ -147,6 +154,41 @@ def pa_kv_append_rope(k_new, v_new, q_or_null, kv_cache, block_table, context_le
         _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
         _dev(err, "err", _i32()), _stream(stream))
     _check("pa_kv_append_rope", rc)
+
+
+def pa_prefill_append_rope(k_new, v_new, q_or_null, cu_tokens, kv_cache, block_table,
+                           context_lens, layer, free_list, free_count, err, stream=None):
+    """Packed prompt chunks: k_new/v_new [T][8][64], q_or_null [T][32][64] or None,
+    cu_tokens int32 [n+1] (rows of sequence s: cu_tokens[s] .. cu_tokens[s+1]-1);
+    block_table [n][L][max_blocks] int32."""
+    n, n_layers, max_blocks = block_table.shape
+    if cu_tokens.numel() != n + 1:
+        raise ValueError("cu_tokens must hold num_seqs + 1 entries")
+    rc = library().pa_prefill_append_rope(
+        _dev(k_new, "k_new", _bf16()), _dev(v_new, "v_new", _bf16()),
+        _dev(q_or_null, "q_or_null", _bf16(), optional=True), int(k_new.shape[0]),
+        _dev(cu_tokens, "cu_tokens", _i32()),
+        _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]),
+        _dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+        _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
+        _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
+        _dev(err, "err", _i32()), _stream(stream))
+    _check("pa_prefill_append_rope", rc)
+
+
+def pa_prefill_attention(out, q, cu_tokens, kv_cache, block_table, context_lens, layer, scale,
+                         err, stream=None):
+    """out/q [T][32][64] bf16, packed as for pa_prefill_append_rope."""
+    n, n_layers, max_blocks = block_table.shape
+    if cu_tokens.numel() != n + 1:
+        raise ValueError("cu_tokens must hold num_seqs + 1 entries")
+    rc = library().pa_prefill_attention(
+        _dev(out, "out", _bf16()), _dev(q, "q", _bf16()), int(q.shape[0]),
+        _dev(cu_tokens, "cu_tokens", _i32()), _dev(kv_cache, "kv_cache", _bf16()),
+        int(kv_cache.shape[0]), _dev(block_table, "block_table", _i32()), int(n_layers),
+        int(max_blocks), _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
+        float(scale), _dev(err, "err", _i32()), _stream(stream))
+    _check("pa_prefill_attention", rc)
 
 
 def pa_decode_workspace_size(num_seqs: int, max_blocks_per_seq: int) -> int:

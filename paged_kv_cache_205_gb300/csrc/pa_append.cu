@@ -16,6 +16,9 @@
 //                                 rotates q and k while the first kernel
 //                                 runs, then waits for it and stores K/V in
 //                                 the slot the table names.
+// pa_prefill_append_rope does the same for a prompt chunk per sequence
+// ("The path of one inference": prefill pushes the whole prompt through at
+// once; ropeKernel_llama3 is the prefill RoPE).
 #include <climits>
 #include <cmath>
 
@@ -167,6 +170,22 @@ __device__ __forceinline__ void rotate4(uint2 lo, uint2 hi, const float2 *cs, in
   *out_hi = make_uint2(oh[0], oh[1]);
 }
 
+// (cos, sin) of the angle pos * f.  The angle is formed and reduced modulo
+// 2*pi in fp64, so that positions in the tens of thousands keep their phase;
+// the reduced angle (|r| <= pi) goes through fp32 sincosf, with a first-order
+// correction for the part of it fp32 could not hold.
+__device__ __forceinline__ float2 rope_cos_sin(int pos, double f) {
+  const double two_pi_hi = 6.283185307179586232, two_pi_lo = 2.4492935982947064e-16;
+  const double a = static_cast<double>(pos) * f;
+  const double k = rint(a * 0.15915494309189533577);
+  const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, a));
+  const float rf = static_cast<float>(red);
+  const float rerr = static_cast<float>(red - static_cast<double>(rf));   // |rerr| <= 2^-23
+  float sn, cn;
+  sincosf(rf, &sn, &cn);
+  return make_float2(fmaf(-sn, rerr, cn), fmaf(cn, rerr, sn));
+}
+
 __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParams p) {
   __shared__ float2 cs[kD / 2];
   pdl_launch_dependents();   // the next kernel may start its own set-up
@@ -178,21 +197,7 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
     pdl_wait_primary();
     return;
   }
-  if (tid < kD / 2) {
-    // the angle pos * f is formed and reduced modulo 2*pi in fp64, so that
-    // positions in the tens of thousands keep their phase; the reduced angle
-    // (|r| <= pi) goes through fp32 sincosf and the rotation runs in fp32
-    const double two_pi_hi = 6.283185307179586232, two_pi_lo = 2.4492935982947064e-16;
-    const double a = static_cast<double>(pos) * p.freqs.f[tid];
-    const double k = rint(a * 0.15915494309189533577);
-    const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, a));
-    const float rf = static_cast<float>(red);
-    const float rerr = static_cast<float>(red - static_cast<double>(rf));   // |rerr| <= 2^-23
-    float sn, cn;
-    sincosf(rf, &sn, &cn);
-    // first-order correction for the part of the angle fp32 could not hold
-    cs[tid] = make_float2(fmaf(-sn, rerr, cn), fmaf(cn, rerr, sn));
-  }
+  if (tid < kD / 2) cs[tid] = rope_cos_sin(pos, p.freqs.f[tid]);
   __syncthreads();
 
   const int head = tid >> 3;   // 0..7 k heads, 8..39 q heads
@@ -226,6 +231,169 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
     // allocation kernel; an invalid existing entry is reported here
     if (tid == 0 && pos % kBs != 0) report(p.err, PA_DEV_BAD_BLOCK);
     pdl_wait_primary();   // this grid ends after the allocation kernel
+    return;
+  }
+  unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
+  const int slot = pos % kBs;
+  if (head < kHkv) {
+    unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
+    *reinterpret_cast<uint2 *>(krow + 8 * j) = klo;
+    *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = khi;
+  }
+  if (tid < kTokRowBytes / 16)
+    reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v;
+  pdl_wait_primary();   // this grid ends after the allocation kernel
+}
+
+// ------------------------------------------------------------------ prefill
+// A prompt chunk per sequence: the tokens of sequence s are rows
+// cu_tokens[s] .. cu_tokens[s+1]-1, at positions context_lens[s] + i.
+//   prefill_alloc_kernel  (1 CTA)  ranks every page the chunks open over the
+//                                  sequences in order and pops them from the
+//                                  back of the free list.
+//   prefill_store_kernel  (1 CTA per token row, programmatic dependent
+//                                  launch) rotates the row's k and q, then
+//                                  stores K/V in the slot the table names.
+
+struct PrefillAppendParams {
+  RopeFreqs freqs;
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  uint16_t *q;                 // may be null
+  unsigned char *kv;
+  int32_t *block_table;
+  const int32_t *cu_tokens;
+  const int32_t *context_lens;
+  int32_t *free_list;
+  int32_t *free_count;
+  int32_t *err;
+  int total_tokens;
+  int num_blocks;
+  int n_layers;
+  int max_blocks;
+  int num_seqs;
+  int layer;
+};
+
+// Whether sequence s's chunk is accepted: it fits the sequence's table and
+// its rows lie inside [0, total_tokens).  Sets the context and chunk length.
+__device__ __forceinline__ bool chunk_fits(const PrefillAppendParams &p, int s, int *ctx, int *n) {
+  const int c0 = p.cu_tokens[s], c1 = p.cu_tokens[s + 1];
+  *ctx = p.context_lens[s];
+  *n = c1 - c0;
+  return *ctx >= 0 && *n >= 0 && c0 >= 0 && c1 <= p.total_tokens &&
+         static_cast<long long>(*ctx) + *n <= static_cast<long long>(p.max_blocks) * kBs;
+}
+
+__global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendParams p) {
+  __shared__ int tot[kScanCta / 32];
+  pdl_wait_primary();        // the table and free list may come from the previous kernel
+  pdl_launch_dependents();   // the store kernel may start its rotations now
+  const int fc0 = min(max(*p.free_count, 0), p.num_blocks);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int served = 0;
+  for (int base = 0; base < p.num_seqs; base += kScanCta) {
+    const int s = base + threadIdx.x;
+    int ctx = 0, n = 0, first = 0, pages = 0;
+    if (s < p.num_seqs) {
+      if (!chunk_fits(p, s, &ctx, &n)) {
+        report(p.err, PA_DEV_CTX_RANGE);
+      } else {
+        first = (ctx + kBs - 1) / kBs;                 // pages already open
+        pages = (ctx + n + kBs - 1) / kBs - first;     // pages this chunk opens
+      }
+    }
+    // pages are ranked over the sequences in order: an exclusive prefix sum
+    int incl = pages;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) tot[warp] = incl;
+    __syncthreads();
+    int before = 0, chunk = 0;
+    for (int w = 0; w < kScanCta / 32; ++w) {
+      const int t = tot[w];
+      if (w < warp) before += t;
+      chunk += t;
+    }
+    __syncthreads();
+    const int rank0 = served + before + incl - pages;
+    if (pages > 0) {
+      int32_t *row = p.block_table + table_row(s, p.n_layers, p.layer, p.max_blocks);
+      for (int j = 0; j < pages; ++j) {
+        const int rank = rank0 + j;
+        if (rank < fc0) {
+          const int blk = p.free_list[fc0 - 1 - rank];
+          row[first + j] = blk;
+          if (blk < 0 || blk >= p.num_blocks) report(p.err, PA_DEV_BAD_BLOCK);
+        } else {
+          row[first + j] = -1;   // refused: the page stays unassigned
+          report(p.err, PA_DEV_FREE_UNDERFLOW);
+        }
+      }
+    }
+    served += chunk;
+  }
+  if (threadIdx.x == 0) *p.free_count = max(fc0 - served, 0);
+}
+
+__global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillAppendParams p) {
+  __shared__ float2 cs[kD / 2];
+  __shared__ int seq_found;
+  pdl_launch_dependents();   // the next kernel may start its own set-up
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  // the row's sequence: the largest s with cu_tokens[s] <= r (an empty
+  // chunk's start equals the next one's, so the search passes over it)
+  if (tid == 0) {
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cu_tokens[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    seq_found = lo;
+  }
+  __syncthreads();
+  const int s = seq_found;
+  int ctx, n;
+  const bool fits = chunk_fits(p, s, &ctx, &n);
+  if (!fits || r < p.cu_tokens[s] || r >= p.cu_tokens[s + 1]) {
+    pdl_wait_primary();   // refused chunk (reported by the allocation kernel) or a row outside every chunk
+    return;
+  }
+  const int pos = ctx + (r - p.cu_tokens[s]);
+  if (tid < kD / 2) cs[tid] = rope_cos_sin(pos, p.freqs.f[tid]);
+  __syncthreads();
+  const int head = tid >> 3;   // 0..7 k heads, 8..39 q heads
+  const int j = tid & 7;
+  uint2 klo = make_uint2(0, 0), khi = make_uint2(0, 0);
+  if (head < kHkv) {
+    const uint16_t *row = p.k_new + (static_cast<size_t>(r) * kHkv + head) * kD;
+    rotate4(*reinterpret_cast<const uint2 *>(row + 4 * j),
+            *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j), cs, j, &klo, &khi);
+  } else if (p.q) {
+    uint16_t *row = p.q + (static_cast<size_t>(r) * kHq + (head - kHkv)) * kD;
+    uint2 rlo, rhi;
+    rotate4(*reinterpret_cast<const uint2 *>(row + 4 * j),
+            *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j), cs, j, &rlo, &rhi);
+    *reinterpret_cast<uint2 *>(row + 4 * j) = rlo;
+    *reinterpret_cast<uint2 *>(row + kD / 2 + 4 * j) = rhi;
+  }
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (tid < kTokRowBytes / 16)
+    v = reinterpret_cast<const uint4 *>(p.v_new + static_cast<size_t>(r) * kHkv * kD)[tid];
+  const int page = pos / kBs;
+  const bool new_page = page >= (ctx + kBs - 1) / kBs;   // opened by this chunk
+  if (new_page) pdl_wait_primary();                       // its entry comes from the allocation kernel
+  const int blk = p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + page];
+  if (blk < 0 || blk >= p.num_blocks) {
+    // a page of this chunk that was refused or popped invalid is reported by
+    // the allocation kernel; an invalid page from before is reported here
+    if (tid == 0 && !new_page) report(p.err, PA_DEV_BAD_BLOCK);
+    pdl_wait_primary();
     return;
   }
   unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
@@ -356,6 +524,56 @@ extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
   if (launch_pdl(append_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(append_store_kernel, dim3(num_seqs), dim3(kStoreThreads), 0, st, prm) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                                      uint16_t *q_or_null, int total_tokens,
+                                      const int32_t *cu_tokens, uint16_t *kv_cache, int num_blocks,
+                                      int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int layer,
+                                      int32_t *free_list, int32_t *free_count, int32_t *err,
+                                      void *stream) {
+  if (num_seqs < 0 || total_tokens < 0 || num_blocks <= 0 || n_layers <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
+  if (num_seqs == 0 || total_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !cu_tokens || !kv_cache || !block_table || !context_lens ||
+      !free_list || !free_count || !err)
+    return PA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kv_cache) ||
+      (q_or_null && !aligned16(q_or_null)))
+    return PA_ERR_ALIGN;
+  DeviceInfo di;
+  const int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  static const RopeFreqs freqs = llama3_freqs();
+  PrefillAppendParams prm;
+  prm.freqs = freqs;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.q = q_or_null;
+  prm.kv = reinterpret_cast<unsigned char *>(kv_cache);
+  prm.block_table = block_table;
+  prm.cu_tokens = cu_tokens;
+  prm.context_lens = context_lens;
+  prm.free_list = free_list;
+  prm.free_count = free_count;
+  prm.err = err;
+  prm.total_tokens = total_tokens;
+  prm.num_blocks = num_blocks;
+  prm.n_layers = n_layers;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_seqs = num_seqs;
+  prm.layer = layer;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_pdl(prefill_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_pdl(prefill_store_kernel, dim3(total_tokens), dim3(kStoreThreads), 0, st, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;

@@ -631,6 +631,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
@@ -643,8 +645,6 @@ int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
-
-}  // namespace
 
 int current_device(DeviceInfo *info) {
   static DeviceInfo cache[64];

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <utility>
 
@@ -24,6 +25,11 @@ struct DeviceInfo {
 int current_device(DeviceInfo *info);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over a pool of num_blocks blocks: dims (d 64, kv head 8, token
+// 16, K|V 2, block), box (64, 1, 16, 2, 1) = one kv head's K and V tiles of
+// one block, 128-byte swizzle.  Returns PA_OK or PA_ERR_CUDA.
+int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 
 // Launch `kernel` with the programmatic-stream-serialization attribute, so it
 // may start while the previous kernel on the stream finishes; the kernel

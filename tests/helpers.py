@@ -41,11 +41,27 @@ def ulp_diff(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return np.abs(bf16_ordinal(a_bits) - bf16_ordinal(b_bits))
 
 
-def assert_attention_close(gpu_out_f64: np.ndarray, ref: np.ndarray, what: str = ""):
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |x| (8 significant bits): the
+    largest error of rounding x to bf16."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
+def assert_attention_close(gpu_out_f64: np.ndarray, ref: np.ndarray, what: str = "",
+                           output_rounding: bool = False):
+    """Max and mean absolute error of a bf16 output against the fp64 oracle.
+    With output_rounding, each element may also carry the rounding of its
+    exact value to bf16 (half an ulp at |ref|), which alone exceeds ATOL_MAX
+    once |ref| >= 4: outputs that large come from rows attending over a few
+    keys (the first tokens of a prompt)."""
     assert gpu_out_f64.shape == ref.shape, (gpu_out_f64.shape, ref.shape)
     assert np.all(np.isfinite(gpu_out_f64)), f"{what}: non-finite output"
     d = np.abs(gpu_out_f64 - ref)
-    assert d.max() <= ATOL_MAX, f"{what}: max abs err {d.max():.3e}"
+    dm = d - bf16_half_ulp(ref) if output_rounding else d
+    assert dm.max() <= ATOL_MAX, \
+        f"{what}: max abs err {d.max():.3e} ({dm.max():.3e} beyond the output rounding)"
     assert d.mean() <= ATOL_MEAN, f"{what}: mean abs err {d.mean():.3e}"
     return float(d.max()), float(d.mean())
 
