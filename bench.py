@@ -8,6 +8,13 @@ one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
+  python bench.py --path prefill [--workload prefill8x2k|chunked32x512]
+
+With --path prefill one step is a whole prefill of one batch of prompt
+chunks: for each of the 16 layers pa_prefill_append_rope (pages, RoPE on k
+and q, K/V stores) then pa_prefill_attention (causal, over the pages); the
+metric is prefill tokens/s and the roofline is the attention kernel's
+tensor throughput.
 
 Workloads (pa_workloads): llama1b (default: 16 layers, 16 sequences, context
 U[256, 2048]), pool2g, long32k, ragged, tiny.
@@ -158,25 +165,36 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s of the GB300s, burst (a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def kernel_source_hash(sources=("pa_decode.cu", "pa_device.cuh")) -> str:
     h = hashlib.sha256()
-    for name in ("pa_decode.cu", "pa_device.cuh"):
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_205_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, valid only
-    while the kernel source hash recorded there matches the current source."""
-    path = os.path.join(ROOT, "profiles", f"decode_split_kernel_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "decode_split_kernel",
+                     sources=("pa_decode.cu", "pa_device.cuh")):
+    """DRAM bytes per launch from the committed ncu summary, valid only while
+    the kernel source hash recorded there matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     mh = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
     mt = re.search(r"dram bytes per launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != kernel_source_hash():
+    if not mh or not mt or mh.group(1) != kernel_source_hash(sources):
         return None
     return float(mt.group(1))
 
@@ -547,19 +565,359 @@ def run_gpu(args, rank, world, dist):
     print(json.dumps(line))
 
 
+# ================================================================ prefill
+PREFILL_METRIC = "prefill tokens/s (paged append + causal paged attention, 16 layers)"
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_device.cuh")
+
+
+def prefill_keys(ctx: np.ndarray, lens: np.ndarray) -> int:
+    """Query-key pairs of one causal prefill call: row i of a chunk after ctx
+    cached tokens sees ctx + i + 1 keys."""
+    ctx = ctx.astype(np.int64)
+    n = lens.astype(np.int64)
+    return int((n * ctx + n * (n + 1) // 2).sum())
+
+
+def prefill_attention_flops(ctx: np.ndarray, lens: np.ndarray) -> float:
+    """Algorithmic FLOPs of one prefill-attention call: per query-key pair
+    and q head, 2*64 for q.k and 2*64 for p*v."""
+    return 4.0 * D * N_Q * prefill_keys(ctx, lens)
+
+
+def prefill_oracle_sample(w, rng, max_tokens: int):
+    """One (sequence, layer) of a prefill workload for the oracle, drawn with
+    the same distributions: the sequence's cached context and the first
+    max_tokens tokens of its chunk, on a compact pool.  Returns the inputs
+    and the attention FLOPs they stand for."""
+    ctx = int(w.context_lens[0])
+    n = max(1, min(int(w.chunk_lens[0]), int(max_tokens)))
+    old = (ctx + BS - 1) // BS
+    need = (ctx + n + BS - 1) // BS
+    nb = need + 1
+    ids = rng.permutation(nb).astype(np.int32)
+    bt = np.full((1, 1, need + 1), -1, dtype=np.int32)
+    bt[0, 0, :old] = ids[:old]
+    free = ids[old:]
+    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    k = wl.normal_bf16(rng, (n, N_KV, D))
+    v = wl.normal_bf16(rng, (n, N_KV, D))
+    q = wl.normal_bf16(rng, (n, N_Q, D))
+    u = dict(k=k, v=v, q=q, pool=pool, bt=bt, ctx=np.array([ctx], np.int32),
+             cu=np.array([0, n], np.int32), fl=free, fc=len(free))
+    return u, prefill_attention_flops(np.array([ctx]), np.array([n]))
+
+
+def prefill_oracle_run(u, scale):
+    import oracle
+    q2, p2, b2, _, _, _ = oracle.prefill_append_rope(u["k"], u["v"], u["q"], u["cu"], u["pool"],
+                                                     u["bt"], u["ctx"], 0, u["fl"], u["fc"])
+    oracle.prefill_attention(q2, u["cu"], p2, b2, u["ctx"], 0, scale)
+
+
+def prefill_cpu_rate(w, rng, budget_s: float):
+    """Oracle attention FLOP/s on samples of the workload, growing the sample
+    until one takes about budget_s."""
+    import oracle
+    oracle.build()
+    m, t, flops = 16, 0.0, 0.0
+    while True:
+        u, f = prefill_oracle_sample(w, rng, m)
+        t0 = time.perf_counter()
+        prefill_oracle_run(u, w.scale)
+        dt = time.perf_counter() - t0
+        t, flops = dt, f
+        if dt > budget_s / 4 or m >= int(w.chunk_lens[0]):
+            return flops / t, m, t
+        m *= 2
+
+
+def prefill_cpu_baseline(w, budget_s: float = 12.0):
+    rng = np.random.default_rng(w.seed + 77)
+    rate, m, t = prefill_cpu_rate(w, rng, budget_s)
+    flops_step = prefill_attention_flops(w.context_lens, w.chunk_lens) * w.n_layers
+    return {
+        "value": w.total_tokens / (flops_step / rate),
+        "unit": "tokens/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"append + attention of the first {m} tokens of one sequence's chunk in one "
+                  f"layer ({t:.1f} s, single-threaded C, fp64), scaled to the step by "
+                  "attention FLOPs",
+        "host_cores": os.cpu_count(),
+    }
+
+
+def run_prefill_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = wl.make_prefill_workload(args.workload)
+    rng = np.random.default_rng(w.seed + 91)
+    per_step_budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
+    _, m, _ = prefill_cpu_rate(w, rng, per_step_budget * 4)
+    for _ in range(args.warmup):
+        u, _ = prefill_oracle_sample(w, rng, m)
+        prefill_oracle_run(u, w.scale)
+    t_total, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        u, f = prefill_oracle_sample(w, rng, m)
+        t0 = time.perf_counter()
+        prefill_oracle_run(u, w.scale)
+        t_total += time.perf_counter() - t0
+        flops += f
+    flops_step = prefill_attention_flops(w.context_lens, w.chunk_lens) * w.n_layers
+    tps = w.total_tokens / (flops_step / (flops / t_total))
+    line = {
+        "impl": "reference",
+        "metric": PREFILL_METRIC,
+        "value": tps,
+        "unit": "tokens/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {PREFILL_DESCRIPTIONS[args.workload]}",
+                   "sample_per_step": f"the first {m} tokens of one chunk in one layer, "
+                                      "scaled to the step by attention FLOPs"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} samples, one per step, single-threaded C (fp64)",
+                         "host_cores": os.cpu_count()},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+PREFILL_DESCRIPTIONS = {
+    "prompts17_14": "the page's two prompts (17 and 14 tokens), 1 layer, 64-block pool",
+    "prefill8x2k": "8 fresh 2048-token prompts, 16 layers, 65,536-block pool, Llama-3.2-1B "
+                   "heads (32 q / 8 kv, head_dim 64), 16-token bf16 pages",
+    "chunked32x512": "32 sequences with 4096 tokens paged append a 512-token chunk each, 16 "
+                     "layers, 262,144-block pool",
+}
+
+
+def run_prefill_gpu(args, rank, world, dist):
+    import torch
+    import paged_kv_cache_205_gb300 as pk
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda")
+    w = wl.make_prefill_workload(args.workload)
+    L, T, n = w.n_layers, w.total_tokens, w.num_seqs
+    seed = w.seed + 1000 * rank
+    pool = wl.make_prefill_pool_torch(w, dev, seed)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    fl = torch.from_numpy(w.free_list).to(dev)
+    fc0 = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
+    fc = fc0.clone()
+    cu = torch.from_numpy(w.cu_tokens).to(dev)
+    ctx = torch.from_numpy(w.context_lens).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 1)
+    q = torch.randn((L, T, N_Q, D), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((L, T, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((L, T, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(qs=q, ks=k, vs=v):
+        # every step pages the same chunks again: the free count is restored
+        # first (steady state: the pages are recycled between steps)
+        fc.copy_(fc0)
+        for l in range(L):
+            pk.pa_prefill_append_rope(ks[l], vs[l], qs[l], cu, pool, bt, ctx, l, fl, fc, err)
+            pk.pa_prefill_attention(out[l], qs[l], cu, pool, bt, ctx, l, w.scale, err)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def check(where):
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item())} {where}")
+
+    for _ in range(3):
+        step()
+    check("during eager warm-up")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_step, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g_step.replay()
+    check("during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g_step.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    check("in the timed region")
+
+    # dominant kernel: the step's attention launches alone, one graph
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_attn, stream=side):
+            for l in range(L):
+                pk.pa_prefill_attention(out[l], q[l], cu, pool, bt, ctx, l, w.scale, err)
+    torch.cuda.current_stream().wait_stream(side)
+    k_roof = max(3, min(args.steps, 50))
+    for _ in range(3):
+        g_attn.replay()
+    torch.cuda.synchronize()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(k_roof):
+        g_attn.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / (k_roof * L)
+    check("in the roofline pass")
+
+    # end to end: the chunks' q/k/v from pinned host memory, the step, all
+    # outputs back to pinned host memory, one graph per step
+    h_q, h_k, h_v = (x.cpu().pin_memory() for x in (q, k, v))
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        step(d_q, d_k, d_v)
+        h_out.copy_(out, non_blocking=True)
+
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_e2e, stream=side):
+            e2e_step()
+    torch.cuda.current_stream().wait_stream(side)
+    k_e2e = max(3, min(args.steps, 20))
+    for _ in range(2):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / k_e2e
+    check("in the end-to-end pass")
+    h2d = (h_q.numel() + h_k.numel() + h_v.numel()) * 2
+    d2h = h_out.numel() * 2
+
+    agg = aggregate_ranks(ms, e2e_s, 0, n, dist)
+    ms, e2e_s, world = agg["ms_per_step"], agg["e2e_s"], agg["world"]
+    sampler.stop()
+    if rank != 0:
+        return
+    flops = prefill_attention_flops(w.context_lens, w.chunk_lens)
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (attn_ms / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": world * T / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accumulate": "fp32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {PREFILL_DESCRIPTIONS[args.workload]}",
+            "num_seqs": n,
+            "n_layers": L,
+            "tokens_per_step": T,
+            "attention_flops_per_step": flops * L,
+            "l2": "inputs larger than L2: each step reads and writes "
+                  f"{(q.numel() + out.numel() + k.numel() + v.numel()) * 2 / 2**20:.0f} MiB "
+                  "of q/k/v/out (L2 129 MB)",
+            "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "pa_prefill_attention (prefill_attention_kernel)",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} dense bf16 (burst: the kernel timed alone)",
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "traffic": profiled_traffic(args.workload, "prefill_attention_kernel",
+                                        PREFILL_SOURCES),
+            "flops_per_launch": flops,
+            "ms_per_launch": attn_ms,
+            "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "
+                      "replay stream",
+        },
+        "e2e": {
+            "value": world * T / e2e_s,
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_s * 1e3,
+            "how": "pinned H2D of every layer's q/k/v + the step + D2H of all outputs, one "
+                   "graph replay per step, host wall clock",
+        },
+        "gpu_launches": 3 * L * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w)
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000 for decode, 200 for prefill)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama1b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--path", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--workload", default=None,
+                    help="decode: " + ", ".join(sorted(DESCRIPTIONS)) + " (default llama1b); "
+                         "prefill: " + ", ".join(sorted(PREFILL_DESCRIPTIONS)) +
+                         " (default prefill8x2k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.steps is None:
+        args.steps = 2000 if args.path == "decode" else 200
+    names = DESCRIPTIONS if args.path == "decode" else PREFILL_DESCRIPTIONS
+    if args.workload is None:
+        args.workload = "llama1b" if args.path == "decode" else "prefill8x2k"
+    if args.workload not in names:
+        ap.error(f"--workload {args.workload} is not a {args.path} workload")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None
@@ -568,7 +926,12 @@ def main():
         tdist.init_process_group("gloo")
         dist = tdist
     try:
-        if args.impl == "reference":
+        if args.path == "prefill":
+            if args.impl == "reference":
+                run_prefill_reference(args, rank, world)
+            else:
+                run_prefill_gpu(args, rank, world, dist)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_gpu(args, rank, world, dist)

@@ -25,6 +25,10 @@ sizes the benchmark is specified on:
   ragged    16 layers, 256 sequences, contexts floor(exp(U(0, ln 8192)))
             clamped to [1, 8192], 262,144-block pool, shuffled free list; each
             layer first appends one token, then attends over ctx + 1.
+
+Prefill workloads (make_prefill_workload) pack a prompt chunk per sequence:
+the page's two prompts, eight fresh 2048-token prompts, and 512-token
+chunks after 4096 cached tokens.
 """
 from __future__ import annotations
 
@@ -183,6 +187,60 @@ def make_workload(name: str, seed: int | None = None, **over) -> Workload:
     raise ValueError(f"unknown workload {name!r}")
 
 
+@dataclasses.dataclass
+class PrefillWorkload:
+    """Prompt chunks per sequence: chunk_lens[s] tokens appended after the
+    context_lens[s] tokens already paged (0 for a fresh prompt)."""
+    name: str
+    n_layers: int
+    context_lens: np.ndarray          # int32 [num_seqs], tokens cached before the chunk
+    chunk_lens: np.ndarray            # int32 [num_seqs]
+    num_blocks: int
+    max_blocks_per_seq: int
+    block_table: np.ndarray           # int32 [num_seqs][n_layers][max_blocks_per_seq]
+    free_list: np.ndarray             # int32 [num_blocks]; entries >= free_count unused
+    free_count: int
+    scale: float = 0.125
+    seed: int = 0
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.chunk_lens.shape[0])
+
+    @property
+    def cu_tokens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk_lens.astype(np.int64))]).astype(np.int32)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.chunk_lens.astype(np.int64).sum())
+
+
+PREFILL_WORKLOADS = {
+    # name: (seed, layers, cached context per sequence, chunk per sequence, pool blocks)
+    "prompts17_14": (6, 1, [0, 0], [17, 14], 64),
+    "prefill8x2k": (7, 16, [0] * 8, [2048] * 8, 65536),
+    "chunked32x512": (8, 16, [4096] * 32, [512] * 32, 262144),
+}
+
+
+def make_prefill_workload(name: str, seed: int | None = None) -> PrefillWorkload:
+    """prompts17_14: the page's two prompts (17 and 14 tokens), one layer.
+    prefill8x2k: 8 fresh 2048-token prompts through 16 layers, 65,536-block
+    pool.  chunked32x512: 32 sequences with 4096 tokens paged already append
+    a 512-token chunk each, 16 layers, 262,144-block pool.  Cached pages are
+    popped from a shuffled free list; the chunks' pages come from what is
+    left of it."""
+    sd, n_layers, ctx, lens, num_blocks = PREFILL_WORKLOADS[name]
+    rng = np.random.default_rng(sd if seed is None else seed)
+    ctx = np.array(ctx, dtype=np.int32)
+    lens = np.array(lens, dtype=np.int32)
+    max_blocks = int(((ctx + lens + BLOCK - 1) // BLOCK).max()) + 1
+    bt, free_list, top = _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks)
+    return PrefillWorkload(name, n_layers, ctx, lens, num_blocks, max_blocks, bt, free_list, top,
+                           seed=sd if seed is None else seed)
+
+
 def live_mask(w: Workload, context_lens=None) -> np.ndarray:
     """bool [num_blocks][16]: slots that hold a live token of some sequence."""
     ctx = w.context_lens if context_lens is None else context_lens
@@ -252,4 +310,23 @@ def make_pool_torch(w: Workload, device, seed: int, poison: bool = True):
             sub = pool[tb]                                       # [n_tail][2][16][8][64]
             sub = torch.where(mask[:, None, :, None, None], nan, sub)
             pool[tb] = sub
+    return pool
+
+
+def make_prefill_pool_torch(w: PrefillWorkload, device, seed: int):
+    """Device pool for a prefill workload: N(0,1) bf16 from torch's seeded
+    CUDA generator, with every block still on the free list set to NaN, so
+    the slots past a chunk's last token in its last page read as NaN."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    pool = torch.empty((w.num_blocks, 2, BLOCK, N_KV, HEAD_DIM), dtype=torch.bfloat16,
+                       device=device)
+    flat = pool.view(-1)
+    chunk = 1 << 28
+    for i in range(0, flat.numel(), chunk):
+        flat[i:i + chunk].normal_(0.0, 1.0, generator=g)
+    free = torch.from_numpy(w.free_list[:w.free_count].astype(np.int64)).to(device)
+    for i in range(0, free.numel(), 16384):
+        pool[free[i:i + 16384]] = float("nan")
     return pool

@@ -305,3 +305,65 @@ def test_prefill_attention_long_prompt_sampled_rows():
                                          np.array(poss, dtype=np.int32) + 1, 0, SCALE)
     assert e_ref == 0
     _close(got[np.array(rows)], ref, "sampled rows")
+
+
+@pytest.mark.parametrize("name", ["prefill8x2k", "chunked32x512"])
+def test_bench_prefill_workload_sampled(name):
+    """The benchmark's prefill step at full size, launched as the benchmark
+    launches it (every layer: append then attention, one stream): the
+    appended pages hold no error, the rotated q rows match the oracle's RoPE,
+    and sampled output rows match the oracle's attention over the pages the
+    GPU wrote."""
+    import torch
+    from helpers import gather_for_oracle
+    w = wl.make_prefill_workload(name)
+    dev = torch.device("cuda")
+    L, T = w.n_layers, w.total_tokens
+    pool = wl.make_prefill_pool_torch(w, dev, seed=w.seed)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    fl = torch.from_numpy(w.free_list).to(dev)
+    fc = torch.tensor([w.free_count], dtype=torch.int32, device=dev)
+    cu = torch.from_numpy(w.cu_tokens).to(dev)
+    ctx = torch.from_numpy(w.context_lens).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 1)
+    q = torch.randn((L, T, N_Q, D), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((L, T, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((L, T, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+    q_in = q.clone()
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for l in range(L):
+        _pk().pa_prefill_append_rope(k[l], v[l], q[l], cu, pool, bt, ctx, l, fl, fc, err)
+        _pk().pa_prefill_attention(out[l], q[l], cu, pool, bt, ctx, l, w.scale, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    n_pages = ((w.context_lens + w.chunk_lens + BS - 1) // BS - (w.context_lens + BS - 1) // BS)
+    assert int(fc.item()) == w.free_count - int(n_pages.sum()) * L
+    table = bt.cpu().numpy()
+    ctx_after = (w.context_lens + w.chunk_lens).astype(np.int32)
+    rng = np.random.default_rng(5)
+    cu_h = w.cu_tokens
+    for layer in (0, L - 1):
+        seqs = sorted({0, w.num_seqs - 1, int(rng.integers(w.num_seqs))})
+        sub, sub_bt = gather_for_oracle(pool, table, seqs, ctx_after, layer)
+        rows, pos, which = [], [], []
+        for i, s in enumerate(seqs):
+            n = int(w.chunk_lens[s])
+            for t in sorted({0, n - 1, *rng.integers(n, size=6).tolist()}):
+                rows.append(int(cu_h[s]) + t)
+                pos.append(int(w.context_lens[s]) + t)
+                which.append(i)
+        rows = np.array(rows)
+        q_rot = host_bits(q[layer][torch.from_numpy(rows).to(dev)])
+        q_orig = host_bits(q_in[layer][torch.from_numpy(rows).to(dev)])
+        ref_q = np.stack([
+            np.stack([oracle.f64_to_bf16(oracle.rope_rotate(oracle.bf16_to_f64(q_orig[i, h]),
+                                                            pos[i]))
+                      for h in range(N_Q)]) for i in range(len(rows))])
+        assert_rope_close(q_rot, ref_q, f"{name} layer {layer} q")
+        ref, e_ref = oracle.decode_attention(q_rot, sub, sub_bt[np.array(which)],
+                                             np.array(pos, dtype=np.int32) + 1, 0, w.scale)
+        assert e_ref == 0
+        got = host_f64(out[layer][torch.from_numpy(rows).to(dev)])
+        _close(got, ref, f"{name} layer {layer}")
