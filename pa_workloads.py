@@ -330,3 +330,60 @@ def make_prefill_pool_torch(w: PrefillWorkload, device, seed: int):
     for i in range(0, free.numel(), 16384):
         pool[free[i:i + 16384]] = float("nan")
     return pool
+
+
+# ------------------------------------------------------ continuous batching
+@dataclasses.dataclass
+class ServeWorkload:
+    """Requests (id, prompt tokens, decode steps) fed to the serving loop."""
+    name: str
+    n_layers: int
+    max_slots: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    prefill_budget: int               # prompt tokens prefilled per step at most
+    requests: list                    # [(rid, prompt_len, decode_steps)]
+    scale: float = 0.125
+    seed: int = 0
+
+
+SERVE_WORKLOADS = {
+    # name: (seed, layers, slots, pool blocks, prefill budget, requests,
+    #        prompt range, decode-step range)
+    "serve_tiny": (9, 2, 3, 12, 32, 7, (1, 40), (1, 20)),
+    "serve256": (10, 16, 64, 65536, 8192, 256, (16, 2048), (16, 512)),
+}
+
+
+def make_serve_workload(name: str) -> ServeWorkload:
+    """serve_tiny: 7 requests through 3 slots of a 2-layer model with a
+    12-page pool and 32 prompt tokens per step, so admissions wait for
+    slots, for pages and for the prefill budget.  serve256: 256
+    requests through 64 slots of the 16-layer model, prompts and decode
+    lengths log-uniform in [16, 2048] and [16, 512], a 65,536-block pool and
+    8192 prompt tokens per step."""
+    sd, L, slots, nb, budget, n_req, (p0, p1), (g0, g1) = SERVE_WORKLOADS[name]
+    rng = np.random.default_rng(sd)
+    p = np.floor(np.exp(rng.uniform(np.log(p0), np.log(p1 + 1), size=n_req))).astype(int)
+    g = np.floor(np.exp(rng.uniform(np.log(g0), np.log(g1 + 1), size=n_req))).astype(int)
+    p = np.clip(p, p0, p1)
+    g = np.clip(g, g0, g1)
+    reqs = [(i, int(p[i]), int(g[i])) for i in range(n_req)]
+    mb = int(max((a + b + BLOCK - 1) // BLOCK for _, a, b in reqs)) + 1
+    return ServeWorkload(name, L, slots, nb, mb, budget, reqs, seed=sd)
+
+
+def request_token_inputs(seed: int, rid: int, layer: int, positions):
+    """q [n][32][64], k [n][8][64], v [n][8][64] bf16 bits of request rid's
+    tokens at `positions` in `layer`: N(0,1) from a generator keyed by
+    (seed, rid, layer, position), so any token can be drawn on its own."""
+    positions = np.asarray(positions, dtype=np.int64).ravel()
+    q = np.empty((len(positions), N_Q, HEAD_DIM), dtype=np.uint16)
+    k = np.empty((len(positions), N_KV, HEAD_DIM), dtype=np.uint16)
+    v = np.empty((len(positions), N_KV, HEAD_DIM), dtype=np.uint16)
+    for i, pos in enumerate(positions):
+        rng = np.random.default_rng([seed, rid, layer, int(pos)])
+        q[i] = normal_bf16(rng, (N_Q, HEAD_DIM))
+        k[i] = normal_bf16(rng, (N_KV, HEAD_DIM))
+        v[i] = normal_bf16(rng, (N_KV, HEAD_DIM))
+    return q, k, v
