@@ -9,6 +9,7 @@ one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
   python bench.py --path prefill [--workload prefill8x2k|chunked32x512]
+  python bench.py --path serve [--workload serve256]
 
 With --path prefill one step is a whole prefill of one batch of prompt
 chunks: for each of the 16 layers pa_prefill_append_rope (pages, RoPE on k
@@ -893,6 +894,345 @@ def run_prefill_gpu(args, rank, world, dist):
     print(json.dumps(line))
 
 
+# ======================================================= continuous batching
+SERVE_METRIC = ("serving output tokens/s (continuous batching over the paged cache: queue, "
+                "slots, prefill + decode, 16 layers)")
+SERVE_DESCRIPTIONS = {
+    "serve_tiny": "7 requests, 3 slots, 2 layers, 12-page pool, 32 prompt tokens per step",
+    "serve256": "256 requests (prompts log-U[16,2048], decode steps log-U[16,512]) through 64 "
+                "slots, 16 layers, 65,536-block pool, 8192 prompt tokens per step",
+}
+
+
+def serve_totals(w):
+    """Output tokens (the prefill's first token + one per decode step), prompt
+    tokens, and the decode-attention and prefill-attention work of one run."""
+    out_tokens = sum(1 + g for _, p, g in w.requests)
+    prompt_tokens = sum(p for _, p, g in w.requests)
+    flops = sum(prefill_attention_flops(np.array([0]), np.array([p])) for _, p, g in w.requests)
+    kv_bytes = 0
+    for _, p, g in w.requests:
+        ctx = np.arange(p + 1, p + g + 1, dtype=np.int64)   # attention context of each decode step
+        kv_bytes += attention_bytes(ctx)
+    return out_tokens, prompt_tokens, flops * w.n_layers, kv_bytes * w.n_layers
+
+
+class ServeLoop:
+    """Device buffers of the batcher and one complete serving run."""
+
+    def __init__(self, w, seed):
+        import torch
+        import paged_kv_cache_205_gb300 as pk
+        self.pk, self.w = pk, w
+        dev = torch.device("cuda")
+        S, L, mb, B = w.max_slots, w.n_layers, w.max_blocks_per_seq, w.prefill_budget
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.pool = torch.randn((w.num_blocks, 2, BS, N_KV, D), generator=g,
+                                device=dev).to(torch.bfloat16)
+        self.fl0 = torch.from_numpy(
+            np.random.default_rng(seed).permutation(w.num_blocks).astype(np.int32)).to(dev)
+        self.bt = torch.full((S, L, mb), -1, dtype=torch.int32, device=dev)
+        self.bt_tmp = torch.empty_like(self.bt)
+        self.ctl = torch.zeros(pk.pa_batcher_ctl_bytes(S), dtype=torch.uint8, device=dev)
+        self.fl = self.fl0.clone()
+        self.fc = torch.tensor([w.num_blocks], dtype=torch.int32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = pk.decode_workspace(S, mb)
+        bf = torch.bfloat16
+
+        def rnd(shape):
+            return torch.randn(shape, generator=g, device=dev).to(bf)
+        self.pq, self.pk_, self.pv = rnd((L, B, N_Q, D)), rnd((L, B, N_KV, D)), rnd((L, B, N_KV, D))
+        self.po = torch.empty((L, B, N_Q, D), dtype=bf, device=dev)
+        self.dq, self.dk, self.dv = rnd((L, S, N_Q, D)), rnd((L, S, N_KV, D)), rnd((L, S, N_KV, D))
+        self.do = torch.empty((L, S, N_Q, D), dtype=bf, device=dev)
+        self.bufs = pk.batch_buffers(self.pool, self.bt, self.bt_tmp, self.ctl, self.fl, self.fc,
+                                     self.err, self.ws, self.pq, self.pk_, self.pv, self.po,
+                                     self.dq, self.dk, self.dv, self.do, w.scale)
+
+    def reset(self):
+        self.bt.fill_(-1)
+        self.fl.copy_(self.fl0)
+        self.fc.fill_(self.w.num_blocks)
+
+    def run(self, on_step=None):
+        """One complete serving run of the workload; returns the steps taken
+        and the launches enqueued.  on_step(plan, before) is called around
+        each pa_batcher_run."""
+        w = self.w
+        b = self.pk.Batcher(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
+                            w.prefill_budget)
+        for r in w.requests:
+            b.submit(*r)
+        steps = launches = 0
+        while True:
+            p = b.plan()
+            if p.done:
+                break
+            if on_step:
+                on_step(p, True)
+            b.run(self.bufs)
+            if on_step:
+                on_step(p, False)
+            steps += 1
+            launches += 1 + (3 if p.n_retired else 0) + 3 * w.n_layers * (p.n_admitted > 0) \
+                + 4 * w.n_layers * (p.n_rows > 0)
+        b.close()
+        return steps, launches
+
+
+def serve_cpu_baseline(w, budget_s: float = 12.0):
+    """The oracle's attention rates, sampled on this workload's shapes (a
+    decode unit at the median decode context, a prefill unit at the median
+    prompt), applied to the run's decode bytes and prefill FLOPs."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(w.seed + 77)
+    out_tokens, _, flops, kv_bytes = serve_totals(w)
+    P = np.array([p for _, p, g in w.requests])
+    G = np.array([g for _, p, g in w.requests])
+    ctx_med = int(np.median(P + G // 2))
+    nb = (ctx_med + BS) // BS + 1
+    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    bt = rng.permutation(nb).astype(np.int32).reshape(1, 1, nb)
+    q = wl.normal_bf16(rng, (1, N_Q, D))
+    t_dec, n_dec = 0.0, 0
+    while t_dec < budget_s / 2:
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, pool, bt, np.array([ctx_med], np.int32), 0, w.scale)
+        t_dec += time.perf_counter() - t0
+        n_dec += 1
+    dec_rate = attention_bytes(np.array([ctx_med])) * n_dec / t_dec
+    pw = wl.make_prefill_workload("prefill8x2k")
+    pw.chunk_lens = np.array([int(np.median(P))] * 8, dtype=np.int32)
+    pre_rate, m, t_pre = prefill_cpu_rate(pw, rng, budget_s / 2)
+    t_run = kv_bytes / dec_rate + flops / pre_rate
+    return {
+        "value": out_tokens / t_run,
+        "unit": "tokens/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"{n_dec} decode units at context {ctx_med} ({t_dec:.1f} s) and a {m}-token "
+                  f"prefill unit ({t_pre:.1f} s), single-threaded C, fp64; the run's KV bytes "
+                  "and prefill FLOPs at those rates",
+        "host_cores": os.cpu_count(),
+    }
+
+
+def run_serve_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = wl.make_serve_workload(args.workload)
+    base = serve_cpu_baseline(w, budget_s=min(20.0, 2.0 + 0.5 * args.steps))
+    out_tokens = serve_totals(w)[0]
+    line = {
+        "impl": "reference",
+        "metric": SERVE_METRIC,
+        "value": base["value"],
+        "unit": "tokens/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": out_tokens / base["value"] * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {SERVE_DESCRIPTIONS[args.workload]}",
+                   "sample_per_step": base["sample"]},
+        "cpu_baseline": base,
+        "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_serve_gpu(args, rank, world, dist):
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = wl.make_serve_workload(args.workload)
+    loop = ServeLoop(w, seed=w.seed + 1000 * rank)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def check(where):
+        torch.cuda.synchronize()
+        if int(loop.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(loop.err.item())} {where}")
+        if int(loop.fc.item()) != w.num_blocks:
+            raise RuntimeError(f"pages not all returned {where}")
+
+    for _ in range(args.warmup):
+        loop.reset()
+        loop.run()
+    check("during warm-up")
+
+    # timed: K complete runs; the resets (three small fills) sit between runs
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    total_ms, launches, steps_per_run = 0.0, 0, 0
+    sampler.mark(True)
+    for _ in range(args.steps):
+        loop.reset()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        steps_per_run, n_launch = loop.run()
+        e1.record(stream)
+        e1.synchronize()
+        total_ms += e0.elapsed_time(e1)
+        launches += n_launch
+    sampler.mark(False)
+    barrier()
+    check("in the timed region")
+    ms = total_ms / args.steps
+
+    # dominant work: the loop's decode-only steps (no request leaves or
+    # enters), timed one by one with events around pa_batcher_run
+    rec = []
+
+    def on_step(p, before):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        if before:
+            rec.append([p.n_retired, p.n_admitted, p.n_rows, ev, None])
+        else:
+            rec[-1][4] = ev
+
+    loop.reset()
+    loop.run(on_step)
+    torch.cuda.synchronize()
+    check("in the roofline pass")
+    # decode-only steps: their algorithmic bytes need the rows' contexts,
+    # which the plan does not return; recompute them from the policy's
+    # book-keeping (the oracle-free count: every row advances one token)
+    dec_ms, dec_bytes = 0.0, 0
+    sim = loop.pk.Batcher(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
+                          w.prefill_budget)
+    for r in w.requests:
+        sim.submit(*r)
+    i = 0
+    while True:
+        p = sim.plan()
+        if p.done:
+            break
+        _, pos = sim.rows()
+        n_ret, n_adm, n_rows, ev0, ev1 = rec[i]
+        if n_ret == 0 and n_adm == 0 and n_rows > 0:
+            dec_ms += ev0.elapsed_time(ev1)
+            dec_bytes += w.n_layers * (attention_bytes(pos.astype(np.int64) + 1)
+                                       + append_bytes(n_rows))
+        sim.commit()
+        i += 1
+    sim.close()
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9 if dec_ms > 0 else 0.0
+
+    # end to end: every step's q/k/v from pinned host memory, outputs back
+    h = {name: getattr(loop, name).cpu().pin_memory() for name in ("pq", "pk_", "pv", "dq", "dk", "dv")}
+    h_po = torch.empty_like(loop.po, device="cpu").pin_memory()
+    h_do = torch.empty_like(loop.do, device="cpu").pin_memory()
+    io = {"h2d": 0, "d2h": 0}
+
+    def e2e_step(p, before):
+        if before:
+            if p.n_admitted:
+                t = p.prefill_tokens
+                for name in ("pq", "pk_", "pv"):
+                    getattr(loop, name)[:, :t].copy_(h[name][:, :t], non_blocking=True)
+                    io["h2d"] += h[name][:, :t].numel() * 2
+            if p.n_rows:
+                n = p.n_rows
+                for name in ("dq", "dk", "dv"):
+                    getattr(loop, name)[:, :n].copy_(h[name][:, :n], non_blocking=True)
+                    io["h2d"] += h[name][:, :n].numel() * 2
+        else:
+            if p.n_admitted:
+                h_po[:, :p.prefill_tokens].copy_(loop.po[:, :p.prefill_tokens], non_blocking=True)
+                io["d2h"] += h_po[:, :p.prefill_tokens].numel() * 2
+            if p.n_rows:
+                h_do[:, :p.n_rows].copy_(loop.do[:, :p.n_rows], non_blocking=True)
+                io["d2h"] += h_do[:, :p.n_rows].numel() * 2
+
+    loop.reset()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    loop.run(e2e_step)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    check("in the end-to-end pass")
+
+    out_tokens, prompt_tokens, flops, kv_bytes = serve_totals(w)
+    agg = aggregate_ranks(ms, e2e_s, 0, len(w.requests), dist)
+    ms, e2e_s, world = agg["ms_per_step"], agg["e2e_s"], agg["world"]
+    sampler.stop()
+    if rank != 0:
+        return
+    peak, peak_kind = measured_hbm_peak()
+    line = {
+        "metric": SERVE_METRIC,
+        "value": world * out_tokens / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accumulate": "fp32",
+        "data": "synthetic",
+        "prompt_tokens_per_s": world * prompt_tokens / (ms / 1e3),
+        "config": {
+            "workload": f"{args.workload}: {SERVE_DESCRIPTIONS[args.workload]}",
+            "step": "one complete serving run of the workload (every request admitted, "
+                    "prefilled, decoded and released)",
+            "loop_steps_per_run": steps_per_run,
+            "output_tokens_per_run": out_tokens,
+            "prompt_tokens_per_run": prompt_tokens,
+            "l2": f"each run reads {kv_bytes / 2**30:.1f} GiB of K/V over its decode steps "
+                  "(L2 129 MB)",
+            "launch": "host loop: pa_batcher_plan + pa_batcher_run per loop step, one stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "decode-only loop steps (pa_kv_append_rope + pa_decode_attention, "
+                      f"{w.n_layers} layers), timed one by one",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": None,
+            "decode_only_ms_per_run": dec_ms,
+            "run_ms": ms,
+        },
+        "e2e": {
+            "value": world * out_tokens / e2e_s,
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": io["h2d"],
+            "d2h_bytes_per_step": io["d2h"],
+            "ms_per_step": e2e_s * 1e3,
+            "how": "one run with every loop step's q/k/v copied from pinned host memory and its "
+                   "outputs copied back, host wall clock",
+        },
+        "gpu_launches": launches,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = serve_cpu_baseline(w)
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -900,11 +1240,12 @@ def main():
                     help="timed steps (default 2000 for decode, 200 for prefill)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--path", default="decode", choices=["decode", "prefill", "serve"])
     ap.add_argument("--workload", default=None,
                     help="decode: " + ", ".join(sorted(DESCRIPTIONS)) + " (default llama1b); "
                          "prefill: " + ", ".join(sorted(PREFILL_DESCRIPTIONS)) +
-                         " (default prefill8x2k)")
+                         " (default prefill8x2k); serve: " +
+                         ", ".join(sorted(SERVE_DESCRIPTIONS)) + " (default serve256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")
@@ -912,10 +1253,12 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps is None:
-        args.steps = 2000 if args.path == "decode" else 200
-    names = DESCRIPTIONS if args.path == "decode" else PREFILL_DESCRIPTIONS
+        args.steps = {"decode": 2000, "prefill": 200, "serve": 5}[args.path]
+    names = {"decode": DESCRIPTIONS, "prefill": PREFILL_DESCRIPTIONS,
+             "serve": SERVE_DESCRIPTIONS}[args.path]
     if args.workload is None:
-        args.workload = "llama1b" if args.path == "decode" else "prefill8x2k"
+        args.workload = {"decode": "llama1b", "prefill": "prefill8x2k",
+                         "serve": "serve256"}[args.path]
     if args.workload not in names:
         ap.error(f"--workload {args.workload} is not a {args.path} workload")
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -926,7 +1269,12 @@ def main():
         tdist.init_process_group("gloo")
         dist = tdist
     try:
-        if args.path == "prefill":
+        if args.path == "serve":
+            if args.impl == "reference":
+                run_serve_reference(args, rank, world)
+            else:
+                run_serve_gpu(args, rank, world, dist)
+        elif args.path == "prefill":
             if args.impl == "reference":
                 run_prefill_reference(args, rank, world)
             else:

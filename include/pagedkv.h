@@ -65,6 +65,7 @@ extern "C" {
 #define PA_ERR_ALIGN      -5   /* a tensor pointer is not 16-byte aligned */
 #define PA_ERR_CUDA       -6   /* a CUDA runtime call or kernel launch failed */
 #define PA_ERR_DEVICE     -7   /* no usable device, or not an sm_103 GPU */
+#define PA_ERR_STATE      -8   /* batcher call out of order (run without a plan, plan twice) */
 
 /* device-side error bits, OR-ed into *err */
 #define PA_DEV_BAD_BLOCK       1   /* block id outside [0, num_blocks) inside a context */
@@ -246,6 +247,116 @@ int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_laye
 
 /* Cap on the CTAs one pa_decode_attention launch uses (0 = automatic: two
  * per SM).  Process-wide; affects only how contexts are split. */
+/*
+ * Continuous batching -- the host loop that feeds prefill and decode from a
+ * queue of requests through a fixed set of block-table rows (slots).
+ *
+ * Page: "The path of one inference": prompts wait in a queue; while a slot
+ * is free and a prompt is queued, prefill() takes the whole prompt at once;
+ * otherwise one decode step produces one token for every active slot; a
+ * finished slot is free again; the loop ends when no slot is active and the
+ * queue is empty.  Where the page is silent:
+ *   - A request is (request_id, prompt_len P >= 1, decode_steps G >= 1); it
+ *     is finished after its G-th decode step (a generation length stands in
+ *     for the end-of-text token: no model runs here).
+ *   - Active requests hold block-table rows 0..n-1 in admission order.  A
+ *     step first releases the requests that finished in the step before
+ *     (pa_free over their rows, ascending), then closes the gaps keeping the
+ *     order (the rows' table entries move with them).
+ *   - Admission is first-in first-out and stops at the first queued request
+ *     that lacks a free row, n_layers * ceil((P + G) / 16) pages not yet
+ *     promised to admitted requests (so decode never runs out of pages), or
+ *     P tokens of the step's prefill budget.
+ *   - The step prefills the admitted prompts together (every layer:
+ *     pa_prefill_append_rope then pa_prefill_attention on their rows), then
+ *     every active row takes one decode step (every layer:
+ *     pa_kv_append_rope at position = tokens cached, pa_decode_attention
+ *     over position + 1).
+ * A batcher is host memory (created and owned by the library, freed by
+ * pa_batcher_destroy); it is not thread-safe.  Use per step:
+ *   pa_batcher_plan   decides the step (host only);
+ *   pa_batcher_rows   tells which request each row holds and its decode
+ *                     position, so the caller can fill the step's q/k/v;
+ *   pa_batcher_run    enqueues the step's device work on `stream`
+ *                     (or pa_batcher_commit, when the caller runs it).
+ * After a failed pa_batcher_run the batcher's state is undefined: destroy it.
+ */
+typedef struct pa_batcher pa_batcher;
+
+typedef struct pa_batch_plan {
+    int n_retired;       /* requests released at the start of the step */
+    int n_keep;          /* rows active before admission: 0 .. n_keep-1 */
+    int n_admitted;      /* rows n_keep .. n_rows-1, prefilled this step */
+    int n_rows;          /* rows taking the decode step: 0 .. n_rows-1 */
+    int prefill_tokens;  /* prompt tokens of the admitted rows, packed in row order */
+    int done;            /* 1: queue empty and nothing active; nothing to run */
+} pa_batch_plan;
+
+typedef struct pa_batch_buffers {
+    uint16_t *kv_cache;            /* the pool (pa_decode_attention's layout) */
+    int num_blocks;
+    int32_t *block_table;          /* [max_slots][n_layers][max_blocks_per_seq], -1 filled */
+    int32_t *block_table_tmp;      /* same size: rows move through it */
+    void *ctl;                     /* device control area of pa_batcher_ctl_bytes */
+    size_t ctl_bytes;
+    int32_t *free_list;            /* holds at least the pages the batcher was given */
+    int32_t *free_count;
+    int32_t *err;                  /* device error word (PA_DEV_* bits) */
+    void *decode_workspace;        /* pa_decode_workspace_size(max_slots, max_blocks_per_seq) bytes, zeroed once */
+    size_t decode_workspace_bytes;
+    /* the step's inputs and outputs, bf16, layer-major:
+     *   prefill_*  [n_layers][prefill_budget][32 or 8][64]: row t of a layer
+     *              is packed prompt token t (pa_prefill_attention's layout);
+     *   decode_*   [n_layers][max_slots][32 or 8][64]: row i is block-table
+     *              row i's token of the step.
+     * q is rotated in place; out receives the attention outputs. */
+    uint16_t *prefill_q, *prefill_k, *prefill_v, *prefill_out;
+    uint16_t *decode_q, *decode_k, *decode_v, *decode_out;
+    float scale;
+} pa_batch_buffers;
+
+/* Bytes of the device control area a batcher with max_slots rows uses. */
+size_t pa_batcher_ctl_bytes(int max_slots);
+
+/* max_slots rows (at most 2048) of a block table with n_layers and
+ * max_blocks_per_seq; pages_free = pages on the free list when the loop
+ * starts (the batcher promises no more than that); prefill_budget = prompt
+ * tokens prefilled per step at most.  PA_ERR_ARG on bad sizes. */
+int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per_seq, int pages_free,
+                      int prefill_budget, pa_batcher **out);
+int pa_batcher_destroy(pa_batcher *b);
+
+/* Queue a request.  PA_ERR_ARG when it could never run: P < 1, G < 1,
+ * P > prefill_budget, P + G beyond max_blocks_per_seq * 16, or more pages
+ * than pages_free. */
+int pa_batcher_submit(pa_batcher *b, int64_t request_id, int prompt_len, int decode_steps);
+
+/* Decide the next step.  PA_ERR_STATE if the previous plan was not run. */
+int pa_batcher_plan(pa_batcher *b, pa_batch_plan *plan);
+
+/* Request id and decode position (tokens cached before the step's token)
+ * of rows 0..n_rows-1 of the planned step; returns n_rows, or PA_ERR_ARG if
+ * cap is smaller.  Either output may be NULL. */
+int pa_batcher_rows(const pa_batcher *b, int64_t *request_ids, int32_t *positions, int cap);
+
+/* Request ids released by the planned step; returns their number. */
+int pa_batcher_retired(const pa_batcher *b, int64_t *request_ids, int cap);
+
+/* Requests still queued. */
+int pa_batcher_pending(const pa_batcher *b);
+
+/* Enqueue the planned step on `stream`: one host-to-device copy of the
+ * control block, pa_free and two row-moving kernels when requests leave, the
+ * prefill of the admitted rows, the decode step; then pa_batcher_commit.
+ * Host faults as PA_ERR_*; device faults OR-ed into buf->err.  The buffers
+ * must stay untouched until the stream reaches the end of the step. */
+int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *stream);
+
+/* Mark the planned step as done without enqueuing anything, for callers
+ * that run the step's device work with their own kernels: the admitted
+ * prompts count as cached and every row as one decode step further. */
+int pa_batcher_commit(pa_batcher *b);
+
 int pa_decode_set_grid_limit(int max_ctas);
 
 /* Human-readable name of a PA_ERR_* code. */

@@ -9,6 +9,11 @@ PyTorch fallback, and a missing or unloadable library raises.
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    BatchBuffers,
+    Batcher,
+    BatchPlan,
+    batch_buffers,
+    pa_batcher_ctl_bytes,
     PA_BLOCK_BYTES,
     PA_BLOCK_TOKENS,
     PA_DEV_BAD_BLOCK,

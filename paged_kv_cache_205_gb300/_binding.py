@@ -33,10 +33,40 @@ _EXPORTS = (
     "pa_free",
     "pa_decode_set_grid_limit",
     "pa_error_string",
+    "pa_batcher_ctl_bytes",
+    "pa_batcher_create",
+    "pa_batcher_destroy",
+    "pa_batcher_submit",
+    "pa_batcher_plan",
+    "pa_batcher_rows",
+    "pa_batcher_retired",
+    "pa_batcher_pending",
+    "pa_batcher_run",
+    "pa_batcher_commit",
 )
 
 _lock = threading.Lock()
 _lib = None
+
+
+class BatchPlan(ctypes.Structure):
+    _fields_ = [("n_retired", ctypes.c_int), ("n_keep", ctypes.c_int),
+                ("n_admitted", ctypes.c_int), ("n_rows", ctypes.c_int),
+                ("prefill_tokens", ctypes.c_int), ("done", ctypes.c_int)]
+
+
+class BatchBuffers(ctypes.Structure):
+    _fields_ = [("kv_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int),
+                ("block_table", ctypes.c_void_p), ("block_table_tmp", ctypes.c_void_p),
+                ("ctl", ctypes.c_void_p), ("ctl_bytes", ctypes.c_size_t),
+                ("free_list", ctypes.c_void_p), ("free_count", ctypes.c_void_p),
+                ("err", ctypes.c_void_p), ("decode_workspace", ctypes.c_void_p),
+                ("decode_workspace_bytes", ctypes.c_size_t),
+                ("prefill_q", ctypes.c_void_p), ("prefill_k", ctypes.c_void_p),
+                ("prefill_v", ctypes.c_void_p), ("prefill_out", ctypes.c_void_p),
+                ("decode_q", ctypes.c_void_p), ("decode_k", ctypes.c_void_p),
+                ("decode_v", ctypes.c_void_p), ("decode_out", ctypes.c_void_p),
+                ("scale", ctypes.c_float)]
 
 
 class PagedKVError(RuntimeError):
@@ -79,6 +109,27 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_set_grid_limit.restype = I
         lib.pa_error_string.argtypes = [I]
         lib.pa_error_string.restype = ctypes.c_char_p
+        PP = ctypes.POINTER(ctypes.c_void_p)
+        lib.pa_batcher_ctl_bytes.argtypes = [I]
+        lib.pa_batcher_ctl_bytes.restype = Z
+        lib.pa_batcher_create.argtypes = [I, I, I, I, I, PP]
+        lib.pa_batcher_create.restype = I
+        lib.pa_batcher_destroy.argtypes = [P]
+        lib.pa_batcher_destroy.restype = I
+        lib.pa_batcher_submit.argtypes = [P, ctypes.c_int64, I, I]
+        lib.pa_batcher_submit.restype = I
+        lib.pa_batcher_plan.argtypes = [P, ctypes.POINTER(BatchPlan)]
+        lib.pa_batcher_plan.restype = I
+        lib.pa_batcher_rows.argtypes = [P, P, P, I]
+        lib.pa_batcher_rows.restype = I
+        lib.pa_batcher_retired.argtypes = [P, P, I]
+        lib.pa_batcher_retired.restype = I
+        lib.pa_batcher_pending.argtypes = [P]
+        lib.pa_batcher_pending.restype = I
+        lib.pa_batcher_run.argtypes = [P, ctypes.POINTER(BatchBuffers), P]
+        lib.pa_batcher_run.restype = I
+        lib.pa_batcher_commit.argtypes = [P]
+        lib.pa_batcher_commit.restype = I
         _lib = lib
         return lib
 
@@ -232,3 +283,98 @@ def pa_free(seq_ids, block_table, context_lens, free_list, free_count, num_block
 
 def pa_decode_set_grid_limit(max_ctas: int) -> None:
     _check("pa_decode_set_grid_limit", library().pa_decode_set_grid_limit(int(max_ctas)))
+
+
+# -------------------------------------------------------- continuous batching
+def pa_batcher_ctl_bytes(max_slots: int) -> int:
+    return int(library().pa_batcher_ctl_bytes(int(max_slots)))
+
+
+class Batcher:
+    """The library's continuous-batching loop (pa_batcher_*): a queue of
+    requests, block-table rows as slots, one planned step at a time."""
+
+    def __init__(self, max_slots, n_layers, max_blocks_per_seq, pages_free, prefill_budget):
+        h = ctypes.c_void_p()
+        _check("pa_batcher_create", library().pa_batcher_create(
+            int(max_slots), int(n_layers), int(max_blocks_per_seq), int(pages_free),
+            int(prefill_budget), ctypes.byref(h)))
+        self._h = h
+        self.max_slots = int(max_slots)
+        self.n_layers = int(n_layers)
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+        self.prefill_budget = int(prefill_budget)
+
+    def close(self):
+        if self._h:
+            library().pa_batcher_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def submit(self, request_id: int, prompt_len: int, decode_steps: int):
+        _check("pa_batcher_submit", library().pa_batcher_submit(
+            self._h, int(request_id), int(prompt_len), int(decode_steps)))
+
+    def plan(self) -> BatchPlan:
+        p = BatchPlan()
+        _check("pa_batcher_plan", library().pa_batcher_plan(self._h, ctypes.byref(p)))
+        return p
+
+    def rows(self):
+        """(request id per row, decode position per row) of the planned step."""
+        import numpy as np
+        ids = np.zeros(self.max_slots, dtype=np.int64)
+        pos = np.zeros(self.max_slots, dtype=np.int32)
+        n = library().pa_batcher_rows(self._h, ids.ctypes.data, pos.ctypes.data, self.max_slots)
+        if n < 0:
+            raise PagedKVError("pa_batcher_rows", n)
+        return ids[:n], pos[:n]
+
+    def retired(self):
+        import numpy as np
+        ids = np.zeros(self.max_slots, dtype=np.int64)
+        n = library().pa_batcher_retired(self._h, ids.ctypes.data, self.max_slots)
+        if n < 0:
+            raise PagedKVError("pa_batcher_retired", n)
+        return ids[:n].tolist()
+
+    def pending(self) -> int:
+        return int(library().pa_batcher_pending(self._h))
+
+    def commit(self):
+        _check("pa_batcher_commit", library().pa_batcher_commit(self._h))
+
+    def run(self, bufs: "BatchBuffers", stream=None):
+        _check("pa_batcher_run", library().pa_batcher_run(self._h, ctypes.byref(bufs),
+                                                          _stream(stream)))
+
+
+def batch_buffers(kv_cache, block_table, block_table_tmp, ctl, free_list, free_count, err,
+                  decode_workspace, prefill_q, prefill_k, prefill_v, prefill_out,
+                  decode_q, decode_k, decode_v, decode_out, scale) -> BatchBuffers:
+    """The pa_batch_buffers of a batcher from torch CUDA tensors (see
+    include/pagedkv.h for shapes).  The tensors must outlive every step run
+    with the returned structure."""
+    b = BatchBuffers()
+    b.kv_cache = _dev(kv_cache, "kv_cache", _bf16())
+    b.num_blocks = int(kv_cache.shape[0])
+    b.block_table = _dev(block_table, "block_table", _i32())
+    b.block_table_tmp = _dev(block_table_tmp, "block_table_tmp", _i32())
+    b.ctl = _dev(ctl, "ctl")
+    b.ctl_bytes = int(ctl.numel() * ctl.element_size())
+    b.free_list = _dev(free_list, "free_list", _i32())
+    b.free_count = _dev(free_count, "free_count", _i32())
+    b.err = _dev(err, "err", _i32())
+    b.decode_workspace = _dev(decode_workspace, "decode_workspace")
+    b.decode_workspace_bytes = int(decode_workspace.numel() * decode_workspace.element_size())
+    for name, t in (("prefill_q", prefill_q), ("prefill_k", prefill_k), ("prefill_v", prefill_v),
+                    ("prefill_out", prefill_out), ("decode_q", decode_q), ("decode_k", decode_k),
+                    ("decode_v", decode_v), ("decode_out", decode_out)):
+        setattr(b, name, _dev(t, name, _bf16()))
+    b.scale = float(scale)
+    return b

@@ -617,6 +617,7 @@ extern "C" const char *pa_error_string(int code) {
     case PA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
     case PA_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case PA_ERR_DEVICE: return "no usable sm_103 device";
+    case PA_ERR_STATE: return "batcher call out of order";
     default: return "unknown error";
   }
 }

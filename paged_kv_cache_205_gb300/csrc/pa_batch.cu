@@ -1,0 +1,359 @@
+// pa_batch.cu -- continuous batching over the paged cache: the host loop
+// that feeds prefill and decode from a queue of requests through a fixed set
+// of block-table rows (slots).
+//
+// Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "The path of
+// one inference": prompts wait in a queue; while a slot is free and a prompt
+// is queued, prefill() takes the whole prompt at once; otherwise one decode
+// step produces one token per active slot; a finished slot is free again;
+// the loop ends when no slot is active and the queue is empty.
+//
+// What the page leaves open is fixed as follows.
+//   * A request is (id, P prompt tokens, G decode steps), G >= 1; it is
+//     finished after its G-th decode step (no model here: a generation length
+//     stands in for the end-of-text token).
+//   * Active requests hold rows 0..n-1 in admission order.  A step first
+//     releases the requests that finished in the step before (pa_free over
+//     their rows, ascending), then closes the gaps keeping the order.
+//   * Admission is first-in first-out and stops at the first request that
+//     lacks a free row, L * ceil((P + G) / 16) pages not yet promised to the
+//     admitted requests (so a decode step never runs out of pages), or P
+//     tokens of the step's prefill budget.
+//   * The admitted prompts are prefilled together (all layers:
+//     pa_prefill_append_rope, pa_prefill_attention), then every active row
+//     takes one decode step (all layers: pa_kv_append_rope at position ctx,
+//     pa_decode_attention over ctx + 1).
+//
+// The loop's decisions are host code; every step's device work is enqueued
+// on one stream from here: one host-to-device copy of the step's control
+// block, the release, two row-moving kernels, then the library's entry points.
+#include <algorithm>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <vector>
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kMoveThreads = 256;
+
+// Control block of one step, one copy to the device (int32 words):
+//   [0, S)        rows released this step, ascending
+//   [S, 2S)       cached tokens per row before the release (pa_free's context)
+//   [2S, 3S)      source row of each kept row, after the gaps close
+//   [3S, 4S)      decode position per row (tokens cached before the step's token)
+//   [4S, 5S)      decode attention context per row (position + 1)
+//   [5S, 6S + 1)  cu_tokens of the admitted prompts
+//   [6S + 1, 7S + 1) zeros: the admitted rows' cached context
+struct CtlLayout {
+  int S;
+  size_t retired() const { return 0; }
+  size_t free_ctx() const { return static_cast<size_t>(S); }
+  size_t keep() const { return 2 * static_cast<size_t>(S); }
+  size_t pos() const { return 3 * static_cast<size_t>(S); }
+  size_t attn() const { return 4 * static_cast<size_t>(S); }
+  size_t cu() const { return 5 * static_cast<size_t>(S); }
+  size_t zero() const { return 6 * static_cast<size_t>(S) + 1; }
+  size_t words() const { return 7 * static_cast<size_t>(S) + 1; }
+  size_t bytes() const { return (words() * 4 + 255) & ~static_cast<size_t>(255); }
+};
+
+// Rows [first, n_keep) of `tmp` take rows keep[first..n_keep) of `table`.
+__global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(
+    const int32_t *__restrict__ table, int32_t *__restrict__ tmp, const int32_t *__restrict__ keep,
+    int first, int n_keep, int row_words) {
+  const int r = first + blockIdx.y;
+  if (r >= n_keep) return;
+  const int32_t *src = table + static_cast<size_t>(keep[r]) * row_words;
+  int32_t *dst = tmp + static_cast<size_t>(r) * row_words;
+  for (int i = blockIdx.x * kMoveThreads + threadIdx.x; i < row_words; i += gridDim.x * kMoveThreads)
+    dst[i] = src[i];
+}
+
+// Rows [first, n_keep) of `table` take them back from `tmp`; rows
+// [n_keep, n_prev) (left behind by the moves) become -1.
+__global__ void __launch_bounds__(kMoveThreads) place_rows_kernel(
+    int32_t *__restrict__ table, const int32_t *__restrict__ tmp, int first, int n_keep,
+    int n_prev, int row_words) {
+  const int r = first + blockIdx.y;
+  if (r >= n_prev) return;
+  int32_t *dst = table + static_cast<size_t>(r) * row_words;
+  const int32_t *src = tmp + static_cast<size_t>(r) * row_words;
+  for (int i = blockIdx.x * kMoveThreads + threadIdx.x; i < row_words; i += gridDim.x * kMoveThreads)
+    dst[i] = (r < n_keep) ? src[i] : -1;
+}
+
+struct Request {
+  int64_t id;
+  int prompt_len;
+  int decode_steps;
+};
+
+struct Row {
+  Request req;
+  int ctx = 0;    // tokens cached
+  int done = 0;   // decode steps taken
+};
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+struct pa_batcher {
+  int max_slots, n_layers, max_blocks, pages_free, prefill_budget;
+  std::deque<Request> queue;
+  std::vector<Row> rows;
+  long long promised = 0;
+  // the planned step
+  bool planned = false;
+  pa_batch_plan plan{};
+  std::vector<int64_t> retired_ids;
+  int first_moved = 0;
+  int n_prev = 0;
+  std::vector<int32_t> ctl;   // host image of the control block
+};
+
+namespace {
+
+long long pages_needed(const pa_batcher *b, int prompt_len, int decode_steps) {
+  return static_cast<long long>(b->n_layers) * ((prompt_len + decode_steps + kBs - 1) / kBs);
+}
+
+}  // namespace
+
+extern "C" size_t pa_batcher_ctl_bytes(int max_slots) {
+  if (max_slots <= 0) return 0;
+  return CtlLayout{max_slots}.bytes();
+}
+
+extern "C" int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per_seq,
+                                 int pages_free, int prefill_budget, pa_batcher **out) {
+  if (!out) return PA_ERR_NULL;
+  *out = nullptr;
+  if (max_slots <= 0 || max_slots > 2048 || n_layers <= 0 || max_blocks_per_seq <= 0 ||
+      pages_free < 0 || prefill_budget <= 0)
+    return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * kBs > (1LL << 30)) return PA_ERR_ARG;
+  pa_batcher *b = new (std::nothrow) pa_batcher;
+  if (!b) return PA_ERR_ARG;
+  b->max_slots = max_slots;
+  b->n_layers = n_layers;
+  b->max_blocks = max_blocks_per_seq;
+  b->pages_free = pages_free;
+  b->prefill_budget = prefill_budget;
+  b->ctl.assign(CtlLayout{max_slots}.words(), 0);
+  *out = b;
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_destroy(pa_batcher *b) {
+  delete b;
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_submit(pa_batcher *b, int64_t request_id, int prompt_len,
+                                 int decode_steps) {
+  if (!b) return PA_ERR_NULL;
+  if (prompt_len < 1 || decode_steps < 1 || prompt_len > b->prefill_budget) return PA_ERR_ARG;
+  if (static_cast<long long>(prompt_len) + decode_steps >
+      static_cast<long long>(b->max_blocks) * kBs)
+    return PA_ERR_ARG;
+  if (pages_needed(b, prompt_len, decode_steps) > b->pages_free) return PA_ERR_ARG;
+  b->queue.push_back(Request{request_id, prompt_len, decode_steps});
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_plan(pa_batcher *b, pa_batch_plan *plan) {
+  if (!b || !plan) return PA_ERR_NULL;
+  if (b->planned) return PA_ERR_STATE;
+  const CtlLayout L{b->max_slots};
+  int32_t *ctl = b->ctl.data();
+  std::fill(b->ctl.begin(), b->ctl.end(), 0);
+  // 1. release what finished in the step before; the rest keep their order
+  b->retired_ids.clear();
+  std::vector<Row> kept;
+  kept.reserve(b->rows.size());
+  int n_ret = 0;
+  for (int i = 0; i < static_cast<int>(b->rows.size()); ++i) {
+    const Row &r = b->rows[i];
+    if (r.done >= r.req.decode_steps) {
+      ctl[L.retired() + n_ret++] = i;
+      ctl[L.free_ctx() + i] = r.ctx;
+      b->retired_ids.push_back(r.req.id);
+      b->promised -= pages_needed(b, r.req.prompt_len, r.req.decode_steps);
+    } else {
+      ctl[L.keep() + kept.size()] = i;
+      kept.push_back(r);
+    }
+  }
+  b->n_prev = static_cast<int>(b->rows.size());
+  const int n_keep = static_cast<int>(kept.size());
+  int first = 0;
+  while (first < n_keep && ctl[L.keep() + first] == first) ++first;
+  b->first_moved = first;
+  b->rows.swap(kept);
+  // 2. admit from the head of the queue while it fits
+  int budget = b->prefill_budget, tokens = 0;
+  while (!b->queue.empty()) {
+    const Request &q = b->queue.front();
+    const long long need = pages_needed(b, q.prompt_len, q.decode_steps);
+    if (static_cast<int>(b->rows.size()) >= b->max_slots || b->promised + need > b->pages_free ||
+        q.prompt_len > budget)
+      break;
+    Row r;
+    r.req = q;
+    b->rows.push_back(r);
+    b->promised += need;
+    budget -= q.prompt_len;
+    tokens += q.prompt_len;
+    b->queue.pop_front();
+  }
+  const int n_rows = static_cast<int>(b->rows.size());
+  // 3. the step's positions and packed prompts
+  for (int i = 0; i < n_rows; ++i) {
+    const int pos = (i >= n_keep) ? b->rows[i].req.prompt_len : b->rows[i].ctx;
+    ctl[L.pos() + i] = pos;
+    ctl[L.attn() + i] = pos + 1;
+  }
+  int acc = 0;
+  for (int i = n_keep; i < n_rows; ++i) {
+    ctl[L.cu() + (i - n_keep)] = acc;
+    acc += b->rows[i].req.prompt_len;
+  }
+  ctl[L.cu() + (n_rows - n_keep)] = acc;
+  pa_batch_plan p{};
+  p.n_retired = n_ret;
+  p.n_keep = n_keep;
+  p.n_admitted = n_rows - n_keep;
+  p.n_rows = n_rows;
+  p.prefill_tokens = tokens;
+  p.done = (n_rows == 0 && n_ret == 0) ? 1 : 0;
+  b->plan = p;
+  b->planned = !p.done;
+  *plan = p;
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_rows(const pa_batcher *b, int64_t *request_ids, int32_t *positions,
+                               int cap) {
+  if (!b) return PA_ERR_NULL;
+  const int n = static_cast<int>(b->rows.size());
+  if (cap < n) return PA_ERR_ARG;
+  const CtlLayout L{b->max_slots};
+  for (int i = 0; i < n; ++i) {
+    if (request_ids) request_ids[i] = b->rows[i].req.id;
+    if (positions)
+      positions[i] = b->planned ? b->ctl[L.pos() + i] : b->rows[i].ctx;
+  }
+  return n;
+}
+
+extern "C" int pa_batcher_retired(const pa_batcher *b, int64_t *request_ids, int cap) {
+  if (!b) return PA_ERR_NULL;
+  const int n = static_cast<int>(b->retired_ids.size());
+  if (cap < n) return PA_ERR_ARG;
+  for (int i = 0; i < n; ++i)
+    if (request_ids) request_ids[i] = b->retired_ids[i];
+  return n;
+}
+
+extern "C" int pa_batcher_pending(const pa_batcher *b) {
+  if (!b) return PA_ERR_NULL;
+  return static_cast<int>(b->queue.size());
+}
+
+extern "C" int pa_batcher_commit(pa_batcher *b) {
+  if (!b) return PA_ERR_NULL;
+  if (!b->planned) return PA_ERR_STATE;
+  // prompts are cached, every row took its decode step
+  const pa_batch_plan &p = b->plan;
+  for (int i = 0; i < p.n_rows; ++i) {
+    Row &r = b->rows[i];
+    if (i >= p.n_keep) r.ctx = r.req.prompt_len;
+    r.ctx += 1;
+    r.done += 1;
+  }
+  b->planned = false;
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *stream) {
+  if (!b || !buf) return PA_ERR_NULL;
+  if (!b->planned) return PA_ERR_STATE;
+  const pa_batch_plan &p = b->plan;
+  const CtlLayout L{b->max_slots};
+  if (!buf->kv_cache || !buf->block_table || !buf->block_table_tmp || !buf->ctl ||
+      !buf->free_list || !buf->free_count || !buf->err)
+    return PA_ERR_NULL;
+  if (buf->ctl_bytes < L.bytes()) return PA_ERR_ARG;
+  if (p.n_admitted > 0 &&
+      (!buf->prefill_q || !buf->prefill_k || !buf->prefill_v || !buf->prefill_out))
+    return PA_ERR_NULL;
+  if (p.n_rows > 0 && (!buf->decode_q || !buf->decode_k || !buf->decode_v || !buf->decode_out))
+    return PA_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t *ctl = static_cast<int32_t *>(buf->ctl);
+  // the control block: pageable host memory, staged by the copy before it returns
+  if (cudaMemcpyAsync(ctl, b->ctl.data(), L.words() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int Lyr = b->n_layers, mb = b->max_blocks;
+  const int row_words = Lyr * mb;
+  int rc;
+  // 1. release, then close the gaps
+  if (p.n_retired > 0) {
+    rc = pa_free(ctl + L.retired(), p.n_retired, buf->block_table, Lyr, mb, ctl + L.free_ctx(),
+                 buf->free_list, buf->free_count, buf->num_blocks, buf->err, stream);
+    if (rc != PA_OK) return rc;
+    const int first = b->first_moved;
+    if (first < b->n_prev) {
+      const int gx = std::min((row_words + kMoveThreads - 1) / kMoveThreads, 64);
+      if (first < p.n_keep) {
+        gather_rows_kernel<<<dim3(gx, p.n_keep - first), kMoveThreads, 0, st>>>(
+            buf->block_table, buf->block_table_tmp, ctl + L.keep(), first, p.n_keep, row_words);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+      }
+      place_rows_kernel<<<dim3(gx, b->n_prev - first), kMoveThreads, 0, st>>>(
+          buf->block_table, buf->block_table_tmp, first, p.n_keep, b->n_prev, row_words);
+      if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+  }
+  // 2. prefill of the admitted prompts
+  const size_t tq = static_cast<size_t>(b->prefill_budget) * kHq * kD;
+  const size_t tk = static_cast<size_t>(b->prefill_budget) * kHkv * kD;
+  int32_t *table_new = buf->block_table + static_cast<size_t>(p.n_keep) * row_words;
+  for (int l = 0; l < Lyr && p.n_admitted > 0; ++l) {
+    rc = pa_prefill_append_rope(buf->prefill_k + l * tk, buf->prefill_v + l * tk,
+                                buf->prefill_q + l * tq, p.prefill_tokens, ctl + L.cu(),
+                                buf->kv_cache, buf->num_blocks, table_new, Lyr, mb,
+                                ctl + L.zero(), p.n_admitted, l, buf->free_list, buf->free_count,
+                                buf->err, stream);
+    if (rc != PA_OK) return rc;
+    rc = pa_prefill_attention(buf->prefill_out + l * tq, buf->prefill_q + l * tq,
+                              p.prefill_tokens, ctl + L.cu(), buf->kv_cache, buf->num_blocks,
+                              table_new, Lyr, mb, ctl + L.zero(), p.n_admitted, l, buf->scale,
+                              buf->err, stream);
+    if (rc != PA_OK) return rc;
+  }
+  // 3. one decode step for every active row
+  const size_t dq = static_cast<size_t>(b->max_slots) * kHq * kD;
+  const size_t dk = static_cast<size_t>(b->max_slots) * kHkv * kD;
+  for (int l = 0; l < Lyr && p.n_rows > 0; ++l) {
+    rc = pa_kv_append_rope(buf->decode_k + l * dk, buf->decode_v + l * dk, buf->decode_q + l * dq,
+                           buf->kv_cache, buf->num_blocks, buf->block_table, Lyr, mb,
+                           ctl + L.pos(), p.n_rows, l, buf->free_list, buf->free_count, buf->err,
+                           stream);
+    if (rc != PA_OK) return rc;
+    rc = pa_decode_attention(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
+                             buf->num_blocks, buf->block_table, Lyr, mb, ctl + L.attn(),
+                             p.n_rows, l, buf->scale, buf->decode_workspace,
+                             buf->decode_workspace_bytes, buf->err, stream);
+    if (rc != PA_OK) return rc;
+  }
+  return pa_batcher_commit(b);
+}
