@@ -80,20 +80,20 @@ def _load():
         lib.oracle_bf16_to_double.restype = D
         lib.oracle_double_to_bf16.argtypes = [D]
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
-        lib.oracle_decode_attention.argtypes = [P, P, P, I, P, I, I, P, I, I, D]
-        lib.oracle_decode_attention.restype = I
-        lib.oracle_attention_partial.argtypes = [P, P, I, P, I, I, I, D, P, P, P]
-        lib.oracle_attention_partial.restype = I
+        lib.oracle_decode_attention_bt.argtypes = [P, P, P, I, P, I, I, P, I, I, D, I]
+        lib.oracle_decode_attention_bt.restype = I
+        lib.oracle_attention_partial_bt.argtypes = [P, P, I, P, I, I, I, D, P, P, P, I]
+        lib.oracle_attention_partial_bt.restype = I
         lib.oracle_merge_partials.argtypes = [I, P, P, P, P]
         lib.oracle_merge_partials.restype = None
-        lib.oracle_kv_append_rope.argtypes = [P, P, P, P, I, P, I, I, P, I, I, P, P, P]
-        lib.oracle_kv_append_rope.restype = I
+        lib.oracle_kv_append_rope_bt.argtypes = [P, P, P, P, I, P, I, I, P, I, I, P, P, P, I]
+        lib.oracle_kv_append_rope_bt.restype = I
         lib.oracle_prefill_append_rope.argtypes = [P, P, P, P, P, I, P, I, I, P, I, I, P, P, P]
         lib.oracle_prefill_append_rope.restype = I
         lib.oracle_prefill_attention.argtypes = [P, P, P, P, I, P, I, I, P, I, I, D]
         lib.oracle_prefill_attention.restype = I
-        lib.oracle_free.argtypes = [P, I, P, I, I, P, P, P, I]
-        lib.oracle_free.restype = I
+        lib.oracle_free_bt.argtypes = [P, I, P, I, I, P, P, P, I, I]
+        lib.oracle_free_bt.restype = I
         _lib = lib
         return lib
 
@@ -147,8 +147,9 @@ def f64_to_bf16(x: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------- attention
 def decode_attention(q, pool, block_table, context_lens, layer, scale=0.125,
-                     num_blocks=None):
-    """out[num_seqs][32][64] fp64, plus the error bits."""
+                     num_blocks=None, block_tokens=BLOCK):
+    """out[num_seqs][32][64] fp64, plus the error bits.  pool
+    [num_blocks][2][block_tokens][8][64]."""
     q = _c(q, np.uint16)
     pool = _c(pool, np.uint16)
     bt = _c(block_table, np.int32)
@@ -156,23 +157,25 @@ def decode_attention(q, pool, block_table, context_lens, layer, scale=0.125,
     n, n_layers, max_blocks = bt.shape
     nb = pool.shape[0] if num_blocks is None else num_blocks
     out = np.zeros((n, N_Q, HEAD_DIM), dtype=np.float64)
-    err = _load().oracle_decode_attention(_ptr(out), _ptr(q), _ptr(pool), nb, _ptr(bt),
-                                          n_layers, max_blocks, _ptr(ctx), n, layer, float(scale))
+    err = _load().oracle_decode_attention_bt(_ptr(out), _ptr(q), _ptr(pool), nb, _ptr(bt),
+                                             n_layers, max_blocks, _ptr(ctx), n, layer,
+                                             float(scale), int(block_tokens))
     if err < 0:
         raise MemoryError("oracle allocation failed")
     return out, err
 
 
-def attention_partial(q_head, pool, bt_row, kv_head, t_begin, t_end, scale=0.125):
+def attention_partial(q_head, pool, bt_row, kv_head, t_begin, t_end, scale=0.125,
+                      block_tokens=BLOCK):
     q_head = _c(q_head, np.uint16)
     pool = _c(pool, np.uint16)
     row = _c(bt_row, np.int32)
     m = np.zeros(1)
     l = np.zeros(1)
     acc = np.zeros(HEAD_DIM)
-    err = _load().oracle_attention_partial(_ptr(q_head), _ptr(pool), pool.shape[0], _ptr(row),
-                                           kv_head, t_begin, t_end, float(scale),
-                                           _ptr(m), _ptr(l), _ptr(acc))
+    err = _load().oracle_attention_partial_bt(_ptr(q_head), _ptr(pool), pool.shape[0],
+                                              _ptr(row), kv_head, t_begin, t_end, float(scale),
+                                              _ptr(m), _ptr(l), _ptr(acc), int(block_tokens))
     return float(m[0]), float(l[0]), acc, err
 
 
@@ -187,7 +190,7 @@ def merge_partials(m, l, acc):
 
 # ---------------------------------------------------------------- append
 def kv_append_rope(k_new, v_new, q, pool, block_table, context_lens, layer,
-                   free_list, free_count, num_blocks=None):
+                   free_list, free_count, num_blocks=None, block_tokens=BLOCK):
     """In-place on copies: returns (q_rot or None, pool, block_table, free_list,
     free_count, err).  Inputs are not modified."""
     k_new = _c(k_new, np.uint16)
@@ -201,9 +204,9 @@ def kv_append_rope(k_new, v_new, q, pool, block_table, context_lens, layer,
     inv = llama3_inv_freq()
     n, n_layers, max_blocks = btc.shape
     nb = poolc.shape[0] if num_blocks is None else num_blocks
-    err = _load().oracle_kv_append_rope(_ptr(k_new), _ptr(v_new), _ptr(qc), _ptr(poolc), nb,
-                                        _ptr(btc), n_layers, max_blocks, _ptr(ctx), n, layer,
-                                        _ptr(flc), _ptr(fc), _ptr(inv))
+    err = _load().oracle_kv_append_rope_bt(_ptr(k_new), _ptr(v_new), _ptr(qc), _ptr(poolc), nb,
+                                           _ptr(btc), n_layers, max_blocks, _ptr(ctx), n, layer,
+                                           _ptr(flc), _ptr(fc), _ptr(inv), int(block_tokens))
     return qc, poolc, btc, flc, int(fc[0]), err
 
 
@@ -247,7 +250,8 @@ def prefill_attention(q, cu_tokens, pool, block_table, context_lens, layer, scal
     return out, err
 
 
-def free(seq_ids, block_table, context_lens, free_list, free_count, num_blocks):
+def free(seq_ids, block_table, context_lens, free_list, free_count, num_blocks,
+         block_tokens=BLOCK):
     """Returns (block_table, free_list, free_count, err) on copies."""
     ids = _c(seq_ids, np.int32)
     btc = np.array(block_table, dtype=np.int32, copy=True, order="C")
@@ -255,6 +259,6 @@ def free(seq_ids, block_table, context_lens, free_list, free_count, num_blocks):
     fc = np.array([free_count], dtype=np.int32)
     ctx = _c(context_lens, np.int32)
     n, n_layers, max_blocks = btc.shape
-    err = _load().oracle_free(_ptr(ids), len(ids), _ptr(btc), n_layers, max_blocks,
-                              _ptr(ctx), _ptr(flc), _ptr(fc), num_blocks)
+    err = _load().oracle_free_bt(_ptr(ids), len(ids), _ptr(btc), n_layers, max_blocks,
+                                 _ptr(ctx), _ptr(flc), _ptr(fc), num_blocks, int(block_tokens))
     return btc, flc, int(fc[0]), err

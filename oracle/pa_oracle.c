@@ -22,9 +22,10 @@
 #define HD    64   /* head_dim */
 #define GQA    4
 
-static size_t pool_index(int blk, int kv, int tok, int head, int d)
+/* Element (blk, K=0|V=1, tok, head, d) of a pool whose pages hold bt tokens. */
+static size_t pool_index(int blk, int kv, int tok, int head, int d, int bt)
 {
-    return ((((size_t)blk * 2 + kv) * BS + tok) * HKV + head) * HD + d;
+    return ((((size_t)blk * 2 + kv) * bt + tok) * HKV + head) * HD + d;
 }
 
 static size_t bt_row(int seq, int n_layers, int layer, int max_blocks)
@@ -124,10 +125,10 @@ static int check_block(int blk, int num_blocks)
     return blk >= 0 && blk < num_blocks;
 }
 
-int oracle_attention_partial(const uint16_t *q_head, const uint16_t *pool,
-                             int num_blocks, const int32_t *row, int kv_head,
-                             int t_begin, int t_end, double scale,
-                             double *m_out, double *l_out, double *acc)
+int oracle_attention_partial_bt(const uint16_t *q_head, const uint16_t *pool,
+                                int num_blocks, const int32_t *row, int kv_head,
+                                int t_begin, int t_end, double scale,
+                                double *m_out, double *l_out, double *acc, int bt)
 {
     int n = t_end - t_begin;
     for (int d = 0; d < HD; ++d) acc[d] = 0.0;
@@ -139,29 +140,38 @@ int oracle_attention_partial(const uint16_t *q_head, const uint16_t *pool,
     if (!score) return -1;
     int err = 0;
     for (int t = t_begin; t < t_end; ++t) {
-        int blk = row[t / BS];
+        int blk = row[t / bt];
         if (!check_block(blk, num_blocks)) { err |= PAO_ERR_BAD_BLOCK; score[t - t_begin] = -INFINITY; continue; }
         double dot = 0.0;
         for (int d = 0; d < HD; ++d)
             dot += oracle_bf16_to_double(q_head[d]) *
-                   oracle_bf16_to_double(pool[pool_index(blk, 0, t % BS, kv_head, d)]);
+                   oracle_bf16_to_double(pool[pool_index(blk, 0, t % bt, kv_head, d, bt)]);
         score[t - t_begin] = scale * dot;
     }
     double m = -INFINITY;
     for (int i = 0; i < n; ++i) if (score[i] > m) m = score[i];
     double l = 0.0;
     for (int t = t_begin; t < t_end; ++t) {
-        int blk = row[t / BS];
+        int blk = row[t / bt];
         if (!check_block(blk, num_blocks)) continue;
         double p = exp(score[t - t_begin] - m);
         l += p;
         for (int d = 0; d < HD; ++d)
-            acc[d] += p * oracle_bf16_to_double(pool[pool_index(blk, 1, t % BS, kv_head, d)]);
+            acc[d] += p * oracle_bf16_to_double(pool[pool_index(blk, 1, t % bt, kv_head, d, bt)]);
     }
     free(score);
     *m_out = m;
     *l_out = l;
     return err;
+}
+
+int oracle_attention_partial(const uint16_t *q_head, const uint16_t *pool,
+                             int num_blocks, const int32_t *row, int kv_head,
+                             int t_begin, int t_end, double scale,
+                             double *m_out, double *l_out, double *acc)
+{
+    return oracle_attention_partial_bt(q_head, pool, num_blocks, row, kv_head, t_begin, t_end,
+                                       scale, m_out, l_out, acc, BS);
 }
 
 /* Split-context merge: the partials of disjoint token ranges combine into
@@ -183,26 +193,26 @@ void oracle_merge_partials(int n_parts, const double *m, const double *l,
     for (int d = 0; d < HD; ++d) out[d] /= lsum;
 }
 
-int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *pool,
-                            int num_blocks, const int32_t *block_table,
-                            int n_layers, int max_blocks_per_seq,
-                            const int32_t *context_lens, int num_seqs, int layer,
-                            double scale)
+int oracle_decode_attention_bt(double *out, const uint16_t *q, const uint16_t *pool,
+                               int num_blocks, const int32_t *block_table,
+                               int n_layers, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int layer,
+                               double scale, int bt)
 {
     int err = 0;
     for (int s = 0; s < num_seqs; ++s) {
         int ctx = context_lens[s];
-        if (ctx < 0 || ctx > max_blocks_per_seq * BS) {
+        if (ctx < 0 || ctx > max_blocks_per_seq * bt) {
             err |= PAO_ERR_CTX_RANGE;
-            ctx = ctx < 0 ? 0 : max_blocks_per_seq * BS;
+            ctx = ctx < 0 ? 0 : max_blocks_per_seq * bt;
         }
         const int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
         for (int h = 0; h < HQ; ++h) {
             double *o = out + ((size_t)s * HQ + h) * HD;
             double m, l;
-            int e = oracle_attention_partial(q + ((size_t)s * HQ + h) * HD, pool,
-                                             num_blocks, row, h / GQA, 0, ctx,
-                                             scale, &m, &l, o);
+            int e = oracle_attention_partial_bt(q + ((size_t)s * HQ + h) * HD, pool,
+                                                num_blocks, row, h / GQA, 0, ctx,
+                                                scale, &m, &l, o, bt);
             if (e < 0) return e;
             err |= e;
             if (ctx == 0 || l == 0.0) {           /* empty context: zeros */
@@ -215,6 +225,17 @@ int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *pool
     return err;
 }
 
+int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *pool,
+                            int num_blocks, const int32_t *block_table,
+                            int n_layers, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs, int layer,
+                            double scale)
+{
+    return oracle_decode_attention_bt(out, q, pool, num_blocks, block_table, n_layers,
+                                      max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                      BS);
+}
+
 /* -------------------------------------------------------------- append ---
  * Each sequence adds the token at position pos = context_lens[s].  When pos
  * starts a new 16-token page the sequence takes a block from the free list
@@ -224,18 +245,18 @@ int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *pool
  * pos % 16.  q, when given, is rotated in place at the same position; that
  * rotation depends on the position alone, so it happens even when the K/V
  * store is refused.  A refused allocation leaves the table entry at -1. */
-int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
-                          uint16_t *q_or_null, uint16_t *pool, int num_blocks,
-                          int32_t *block_table, int n_layers, int max_blocks_per_seq,
-                          const int32_t *context_lens, int num_seqs, int layer,
-                          int32_t *free_list, int32_t *free_count,
-                          const double *inv_freq)
+int oracle_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                             uint16_t *q_or_null, uint16_t *pool, int num_blocks,
+                             int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int layer,
+                             int32_t *free_list, int32_t *free_count,
+                             const double *inv_freq, int bt)
 {
     int err = 0;
     double x[HD], y[HD];
     for (int s = 0; s < num_seqs; ++s) {
         int pos = context_lens[s];
-        if (pos < 0 || pos >= max_blocks_per_seq * BS) { err |= PAO_ERR_CTX_RANGE; continue; }
+        if (pos < 0 || pos >= max_blocks_per_seq * bt) { err |= PAO_ERR_CTX_RANGE; continue; }
         if (q_or_null) {
             /* q turns at its position whatever happens to the K/V store */
             for (int h = 0; h < HQ; ++h) {
@@ -247,34 +268,46 @@ int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
         }
         int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
         int blk;
-        if (pos % BS == 0) {
+        if (pos % bt == 0) {
             if (*free_count <= 0) {
                 /* refused: the page stays unassigned */
                 err |= PAO_ERR_FREE_UNDERFLOW;
-                row[pos / BS] = -1;
+                row[pos / bt] = -1;
                 continue;
             }
             blk = free_list[*free_count - 1];
             *free_count -= 1;
-            row[pos / BS] = blk;
+            row[pos / bt] = blk;
         } else {
-            blk = row[pos / BS];
+            blk = row[pos / bt];
         }
         if (!check_block(blk, num_blocks)) { err |= PAO_ERR_BAD_BLOCK; continue; }
 
-        int slot = pos % BS;
+        int slot = pos % bt;
         for (int h = 0; h < HKV; ++h) {
             const uint16_t *k = k_new + ((size_t)s * HKV + h) * HD;
             const uint16_t *v = v_new + ((size_t)s * HKV + h) * HD;
             for (int d = 0; d < HD; ++d) x[d] = oracle_bf16_to_double(k[d]);
             oracle_rope_rotate(x, HD, (double)pos, inv_freq, y);
             for (int d = 0; d < HD; ++d) {
-                pool[pool_index(blk, 0, slot, h, d)] = oracle_double_to_bf16(y[d]);
-                pool[pool_index(blk, 1, slot, h, d)] = v[d];
+                pool[pool_index(blk, 0, slot, h, d, bt)] = oracle_double_to_bf16(y[d]);
+                pool[pool_index(blk, 1, slot, h, d, bt)] = v[d];
             }
         }
     }
     return err;
+}
+
+int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                          uint16_t *q_or_null, uint16_t *pool, int num_blocks,
+                          int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                          const int32_t *context_lens, int num_seqs, int layer,
+                          int32_t *free_list, int32_t *free_count,
+                          const double *inv_freq)
+{
+    return oracle_kv_append_rope_bt(k_new, v_new, q_or_null, pool, num_blocks, block_table,
+                                    n_layers, max_blocks_per_seq, context_lens, num_seqs, layer,
+                                    free_list, free_count, inv_freq, BS);
 }
 
 /* ------------------------------------------------------------- prefill ---
@@ -329,8 +362,8 @@ int oracle_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
                 for (int d = 0; d < HD; ++d) x[d] = oracle_bf16_to_double(k[d]);
                 oracle_rope_rotate(x, HD, (double)pos, inv_freq, y);
                 for (int d = 0; d < HD; ++d) {
-                    pool[pool_index(blk, 0, slot, h, d)] = oracle_double_to_bf16(y[d]);
-                    pool[pool_index(blk, 1, slot, h, d)] = v[d];
+                    pool[pool_index(blk, 0, slot, h, d, BS)] = oracle_double_to_bf16(y[d]);
+                    pool[pool_index(blk, 1, slot, h, d, BS)] = v[d];
                 }
             }
         }
@@ -371,19 +404,19 @@ int oracle_prefill_attention(double *out, const uint16_t *q, const int32_t *cu_t
  * given order, layer 0..n_layers-1, logical block 0..ceil(ctx/16)-1, push the
  * block onto the back of the free list and mark the table entry -1 (the
  * "not assigned yet" value). */
-int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
-                int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
-                int32_t *free_list, int32_t *free_count, int num_blocks)
+int oracle_free_bt(const int32_t *seq_ids, int n_free, int32_t *block_table,
+                   int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                   int32_t *free_list, int32_t *free_count, int num_blocks, int bt)
 {
     int err = 0;
     for (int i = 0; i < n_free; ++i) {
         int s = seq_ids[i];
         int ctx = context_lens[s];
-        if (ctx < 0 || ctx > max_blocks_per_seq * BS) {
+        if (ctx < 0 || ctx > max_blocks_per_seq * bt) {
             err |= PAO_ERR_CTX_RANGE;
-            ctx = ctx < 0 ? 0 : max_blocks_per_seq * BS;
+            ctx = ctx < 0 ? 0 : max_blocks_per_seq * bt;
         }
-        int nb = (ctx + BS - 1) / BS;
+        int nb = (ctx + bt - 1) / bt;
         for (int layer = 0; layer < n_layers; ++layer) {
             int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
             for (int j = 0; j < nb; ++j) {
@@ -397,4 +430,12 @@ int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
         }
     }
     return err;
+}
+
+int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
+                int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                int32_t *free_list, int32_t *free_count, int num_blocks)
+{
+    return oracle_free_bt(seq_ids, n_free, block_table, n_layers, max_blocks_per_seq,
+                          context_lens, free_list, free_count, num_blocks, BS);
 }

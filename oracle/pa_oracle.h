@@ -113,6 +113,29 @@ int oracle_prefill_attention(double *out, const uint16_t *q, const int32_t *cu_t
                              int max_blocks_per_seq, const int32_t *context_lens,
                              int num_seqs, int layer, double scale);
 
+/* The same with pages of bt tokens (the page's BLOCK_SIZE, 16, being a
+ * tunable: pool [num_blocks][2][bt][8][64], token t of a sequence in block
+ * row[t / bt], slot t % bt; a page starts at positions that are multiples
+ * of bt).  The functions above are these with bt = 16. */
+int oracle_attention_partial_bt(const uint16_t *q_head, const uint16_t *pool,
+                                int num_blocks, const int32_t *bt_row, int kv_head,
+                                int t_begin, int t_end, double scale,
+                                double *m, double *l, double *acc, int bt);
+int oracle_decode_attention_bt(double *out, const uint16_t *q, const uint16_t *pool,
+                               int num_blocks, const int32_t *block_table,
+                               int n_layers, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int layer,
+                               double scale, int bt);
+int oracle_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                             uint16_t *q_or_null, uint16_t *pool, int num_blocks,
+                             int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int layer,
+                             int32_t *free_list, int32_t *free_count,
+                             const double *inv_freq, int bt);
+int oracle_free_bt(const int32_t *seq_ids, int n_free, int32_t *block_table,
+                   int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                   int32_t *free_list, int32_t *free_count, int num_blocks, int bt);
+
 /* Release the blocks of finished sequences.  Returns error bits. */
 int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
                 int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
