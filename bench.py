@@ -60,12 +60,12 @@ DESCRIPTIONS = {
 
 
 # ------------------------------------------------------------ byte counts
-def attention_bytes(ctx: np.ndarray) -> int:
+def attention_bytes(ctx: np.ndarray, page: int = BS) -> int:
     """Algorithmic HBM bytes of one decode-attention call: K and V of every
     context token (2048 B per token over 8 kv heads), q and out (4096 B each
     per sequence), the block ids read and the context lengths."""
     ctx = ctx.astype(np.int64)
-    return int(ctx.sum() * 2048 + len(ctx) * (4096 + 4096) + ((ctx + 15) // 16).sum() * 4
+    return int(ctx.sum() * 2048 + len(ctx) * (4096 + 4096) + ((ctx + page - 1) // page).sum() * 4
                + len(ctx) * 4)
 
 
@@ -337,7 +337,7 @@ class DeviceStep:
         self.q = (torch.randn((L, n, N_Q, D), generator=g, device=dev) * w.q_scale).to(torch.bfloat16)
         self.out = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = pk.decode_workspace(n, w.max_blocks_per_seq)
+        self.ws = pk.decode_workspace(n, w.max_blocks_per_seq, block_tokens=w.block_tokens)
         if w.append:
             self.k_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
             self.v_new = torch.randn((L, n, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
@@ -365,7 +365,7 @@ class DeviceStep:
             self.layer(l)
 
     def bytes_per_step(self) -> int:
-        b = attention_bytes(self.w.attn_context_lens) * self.w.n_layers
+        b = attention_bytes(self.w.attn_context_lens, self.w.block_tokens) * self.w.n_layers
         if self.w.append:
             b += append_bytes(self.w.num_seqs) * self.w.n_layers
         return b
@@ -375,7 +375,7 @@ def run_gpu(args, rank, world, dist):
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    w = wl.make_workload(args.workload)
+    w = wl.make_workload(args.workload, block_tokens=args.block_tokens)
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
     st.pk.pa_decode_set_grid_limit(args.grid)
     L, n = w.n_layers, w.num_seqs
@@ -505,7 +505,10 @@ def run_gpu(args, rank, world, dist):
         return
 
     peak, peak_kind = measured_hbm_peak()
-    attn_bytes = attention_bytes(w.attn_context_lens)
+    attn_bytes = attention_bytes(w.attn_context_lens, w.block_tokens)
+    ctx_a = w.attn_context_lens.astype(np.int64)
+    page_fill = float(ctx_a.sum() / (((ctx_a + w.block_tokens - 1) // w.block_tokens).sum()
+                                     * w.block_tokens))
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
     clocks = sampler.summary()
     line = {
@@ -534,6 +537,8 @@ def run_gpu(args, rank, world, dist):
             "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
             "decode_grid_cap": args.grid,
+            "block_tokens": w.block_tokens,
+            "page_fill": page_fill,
         },
         "roofline": {
             "bound": "hbm",
@@ -1247,6 +1252,8 @@ def main():
                          " (default prefill8x2k); serve: " +
                          ", ".join(sorted(SERVE_DESCRIPTIONS)) + " (default serve256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block-tokens", type=int, default=BS, choices=[8, 16, 32],
+                    help="decode path: tokens per page (the page size as a tunable)")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")
     args = ap.parse_args()

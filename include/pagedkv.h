@@ -161,6 +161,37 @@ int pa_decode_attention_static(uint16_t *out, const uint16_t *q, const uint16_t 
                                void *stream);
 
 /*
+ * Page size as a tunable: pa_kv_append_rope_bt, pa_decode_attention_bt,
+ * pa_free_bt and pa_decode_workspace_size_bt are the entry points above with
+ * pages of block_tokens = 8, 16 or 32 tokens (the page's BLOCK_SIZE is 16,
+ * "What is in the box": 16-token pages; the four calls above are these with
+ * 16).  The pool is then [num_blocks][2][block_tokens][8][64] bf16 (a block
+ * is block_tokens * 2 KiB), token t of a sequence lives in block
+ * block_table[s][layer][t / block_tokens], slot t % block_tokens, and an
+ * append at position pos takes a new block when pos % block_tokens == 0.
+ * Everything else (arguments, layouts, errors) is as above; another
+ * block_tokens returns PA_ERR_ARG (0 from the workspace size).  The prefill
+ * entry points and the batcher use 16-token pages.
+ */
+int pa_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                         uint16_t *kv_cache, int num_blocks, int block_tokens,
+                         int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int layer,
+                         int32_t *free_list, int32_t *free_count, int32_t *err,
+                         void *stream);
+int pa_decode_attention_bt(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                           int num_blocks, int block_tokens, const int32_t *block_table,
+                           int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                           int num_seqs, int layer, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *err,
+                           void *stream);
+int pa_free_bt(const int32_t *seq_ids, int n_free, int block_tokens, int32_t *block_table,
+               int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+               int32_t *free_list, int32_t *free_count, int num_blocks,
+               int32_t *err, void *stream);
+size_t pa_decode_workspace_size_bt(int num_seqs, int max_blocks_per_seq, int block_tokens);
+
+/*
  * pa_prefill_append_rope -- append a prompt chunk per sequence to the paged
  * cache (the prefill counterpart of pa_kv_append_rope).
  *

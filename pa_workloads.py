@@ -73,6 +73,7 @@ class Workload:
     append: bool = False              # step = append(pos=ctx) then attention over ctx+1
     scale: float = 0.125              # 1/sqrt(64)
     seed: int = 0
+    block_tokens: int = BLOCK         # tokens per page (the page's BLOCK_SIZE, a tunable)
 
     @property
     def num_seqs(self) -> int:
@@ -87,12 +88,13 @@ class Workload:
         return int(self.attn_context_lens.astype(np.int64).sum()) * N_KV * HEAD_DIM * 2 * 2
 
 
-def _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks, per_layer_subset=None):
-    """Give every (sequence, layer) ceil(ctx/16) physical blocks popped from a
+def _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks, per_layer_subset=None,
+                   block_tokens=BLOCK):
+    """Give every (sequence, layer) ceil(ctx/page) physical blocks popped from a
     shuffled free list.  With per_layer_subset, each layer instead draws its
     own random subset of the pool (blocks may then repeat across layers)."""
     n = len(ctx)
-    nb = (ctx + BLOCK - 1) // BLOCK
+    nb = (ctx + block_tokens - 1) // block_tokens
     bt = np.full((n, n_layers, max_blocks), -1, dtype=np.int32)
     if per_layer_subset is None:
         free = rng.permutation(num_blocks).astype(np.int32)
@@ -121,11 +123,29 @@ def _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks, per_layer_subset=
     return bt, free_list, 0
 
 
-def make_workload(name: str, seed: int | None = None, **over) -> Workload:
-    """Table-level description of one of the five workloads (no tensors)."""
+def make_workload(name: str, seed: int | None = None, block_tokens: int = BLOCK,
+                  **over) -> Workload:
+    """Table-level description of one of the five workloads (no tensors).
+    With block_tokens other than 16 the pool keeps its bytes (16 / page
+    times the blocks) and the tables hold pages of that many tokens."""
     seeds = {"tiny": 1, "llama1b": 2, "pool2g": 3, "long32k": 4, "ragged": 5}
     if seed is None:
         seed = seeds.get(name, 0)
+    if block_tokens != BLOCK:
+        if name == "tiny" or block_tokens not in (8, 32):
+            raise ValueError("page sizes 8 and 32 are given for the full-size workloads")
+        w = make_workload(name, seed=seed, **over)
+        rng = np.random.default_rng(seed)
+        ctx = w.context_lens
+        nb_pool = w.num_blocks * BLOCK // block_tokens
+        max_ctx = {"llama1b": 2048, "ragged": over.get("max_ctx", 8192)}.get(
+            name, int(ctx.max()))
+        mb = max_ctx // block_tokens + 1
+        subset = True if (name == "pool2g" and over.get("alias", True)) else None
+        bt, fl, fc = _assign_tables(rng, ctx, w.n_layers, nb_pool, mb, per_layer_subset=subset,
+                                    block_tokens=block_tokens)
+        return dataclasses.replace(w, num_blocks=nb_pool, max_blocks_per_seq=mb, block_table=bt,
+                                   free_list=fl, free_count=fc, block_tokens=block_tokens)
     rng = np.random.default_rng(seed)
     if name == "tiny":
         ctx = np.array(over.get("context_lens", [17, 14]), dtype=np.int32)
@@ -242,22 +262,23 @@ def make_prefill_workload(name: str, seed: int | None = None) -> PrefillWorkload
 
 
 def live_mask(w: Workload, context_lens=None) -> np.ndarray:
-    """bool [num_blocks][16]: slots that hold a live token of some sequence."""
+    """bool [num_blocks][page]: slots that hold a live token of some sequence."""
     ctx = w.context_lens if context_lens is None else context_lens
-    live = np.zeros((w.num_blocks, BLOCK), dtype=bool)
+    B = w.block_tokens
+    live = np.zeros((w.num_blocks, B), dtype=bool)
     for s in range(w.num_seqs):
         for layer in range(w.n_layers):
             row = w.block_table[s, layer]
-            for t0 in range(0, int(ctx[s]), BLOCK):
-                blk = row[t0 // BLOCK]
-                live[blk, : min(BLOCK, int(ctx[s]) - t0)] = True
+            for t0 in range(0, int(ctx[s]), B):
+                blk = row[t0 // B]
+                live[blk, : min(B, int(ctx[s]) - t0)] = True
     return live
 
 
 def make_pool_numpy(w: Workload, rng: np.random.Generator, poison: bool = True) -> np.ndarray:
     """Host pool [num_blocks][2][16][8][64] of bf16 bits; slots that hold no
     live token are NaN when poison is set."""
-    pool = normal_bf16(rng, (w.num_blocks, 2, BLOCK, N_KV, HEAD_DIM))
+    pool = normal_bf16(rng, (w.num_blocks, 2, w.block_tokens, N_KV, HEAD_DIM))
     if poison:
         dead = ~live_mask(w)
         pool.transpose(0, 2, 1, 3, 4)[dead] = BF16_NAN
@@ -283,7 +304,8 @@ def make_pool_torch(w: Workload, device, seed: int, poison: bool = True):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
-    pool = torch.empty((w.num_blocks, 2, BLOCK, N_KV, HEAD_DIM), dtype=torch.bfloat16,
+    B = w.block_tokens
+    pool = torch.empty((w.num_blocks, 2, B, N_KV, HEAD_DIM), dtype=torch.bfloat16,
                        device=device)
     flat = pool.view(-1)
     chunk = 1 << 28
@@ -295,17 +317,17 @@ def make_pool_torch(w: Workload, device, seed: int, poison: bool = True):
         ctx = w.context_lens
         tail_blocks, tail_from = [], []
         for s in range(w.num_seqs):
-            r = int(ctx[s]) % BLOCK
+            r = int(ctx[s]) % B
             if r == 0:
                 continue
             for layer in range(w.n_layers):
-                tail_blocks.append(int(w.block_table[s, layer, int(ctx[s]) // BLOCK]))
+                tail_blocks.append(int(w.block_table[s, layer, int(ctx[s]) // B]))
                 tail_from.append(r)
         if tail_blocks:
             tb = torch.tensor(tail_blocks, device=device, dtype=torch.long)
             tf = torch.tensor(tail_from, device=device, dtype=torch.long)
-            slot = torch.arange(BLOCK, device=device)
-            mask = slot[None, :] >= tf[:, None]                  # [n_tail][16]
+            slot = torch.arange(B, device=device)
+            mask = slot[None, :] >= tf[:, None]                  # [n_tail][page]
             nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device=device)
             sub = pool[tb]                                       # [n_tail][2][16][8][64]
             sub = torch.where(mask[:, None, :, None, None], nan, sub)

@@ -31,6 +31,10 @@ _EXPORTS = (
     "pa_prefill_attention",
     "pa_decode_workspace_size",
     "pa_free",
+    "pa_kv_append_rope_bt",
+    "pa_decode_attention_bt",
+    "pa_free_bt",
+    "pa_decode_workspace_size_bt",
     "pa_decode_set_grid_limit",
     "pa_error_string",
     "pa_batcher_ctl_bytes",
@@ -101,6 +105,14 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_prefill_append_rope.restype = I
         lib.pa_prefill_attention.argtypes = [P, P, I, P, P, I, P, I, I, P, I, I, F, P, P]
         lib.pa_prefill_attention.restype = I
+        lib.pa_kv_append_rope_bt.argtypes = [P, P, P, P, I, I, P, I, I, P, I, I, P, P, P, P]
+        lib.pa_kv_append_rope_bt.restype = I
+        lib.pa_decode_attention_bt.argtypes = [P, P, P, I, I, P, I, I, P, I, I, F, P, Z, P, P]
+        lib.pa_decode_attention_bt.restype = I
+        lib.pa_free_bt.argtypes = [P, I, I, P, I, I, P, P, P, I, P, P]
+        lib.pa_free_bt.restype = I
+        lib.pa_decode_workspace_size_bt.argtypes = [I, I, I]
+        lib.pa_decode_workspace_size_bt.restype = Z
         lib.pa_decode_workspace_size.argtypes = [I, I]
         lib.pa_decode_workspace_size.restype = Z
         lib.pa_free.argtypes = [P, I, P, I, I, P, P, P, I, P, P]
@@ -191,20 +203,29 @@ def _i32():
 
 
 # ------------------------------------------------------------- entry points
+def _page_tokens(kv_cache) -> int:
+    """Tokens per page of a pool [num_blocks][2][page][8][64]."""
+    return int(kv_cache.shape[2]) if kv_cache.dim() == 5 else PA_BLOCK_TOKENS
+
+
 def pa_kv_append_rope(k_new, v_new, q_or_null, kv_cache, block_table, context_lens, layer,
                       free_list, free_count, err, stream=None):
-    """kv_cache [num_blocks][2][16][8][64] bf16; block_table [n][L][max_blocks] int32;
+    """kv_cache [num_blocks][2][page][8][64] bf16 (page 16: pa_kv_append_rope;
+    8 or 32: pa_kv_append_rope_bt); block_table [n][L][max_blocks] int32;
     k_new/v_new [n][8][64]; q_or_null [n][32][64] or None; free_count, err: int32[1]."""
     n, n_layers, max_blocks = block_table.shape
-    rc = library().pa_kv_append_rope(
-        _dev(k_new, "k_new", _bf16()), _dev(v_new, "v_new", _bf16()),
-        _dev(q_or_null, "q_or_null", _bf16(), optional=True),
-        _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]),
-        _dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
-        _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
-        _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
-        _dev(err, "err", _i32()), _stream(stream))
-    _check("pa_kv_append_rope", rc)
+    page = _page_tokens(kv_cache)
+    args = (_dev(k_new, "k_new", _bf16()), _dev(v_new, "v_new", _bf16()),
+            _dev(q_or_null, "q_or_null", _bf16(), optional=True),
+            _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]))
+    rest = (_dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+            _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
+            _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
+            _dev(err, "err", _i32()), _stream(stream))
+    if page == PA_BLOCK_TOKENS:
+        _check("pa_kv_append_rope", library().pa_kv_append_rope(*args, *rest))
+    else:
+        _check("pa_kv_append_rope_bt", library().pa_kv_append_rope_bt(*args, page, *rest))
 
 
 def pa_prefill_append_rope(k_new, v_new, q_or_null, cu_tokens, kv_cache, block_table,
@@ -242,15 +263,20 @@ def pa_prefill_attention(out, q, cu_tokens, kv_cache, block_table, context_lens,
     _check("pa_prefill_attention", rc)
 
 
-def pa_decode_workspace_size(num_seqs: int, max_blocks_per_seq: int) -> int:
-    return int(library().pa_decode_workspace_size(int(num_seqs), int(max_blocks_per_seq)))
+def pa_decode_workspace_size(num_seqs: int, max_blocks_per_seq: int,
+                             block_tokens: int = PA_BLOCK_TOKENS) -> int:
+    if block_tokens == PA_BLOCK_TOKENS:
+        return int(library().pa_decode_workspace_size(int(num_seqs), int(max_blocks_per_seq)))
+    return int(library().pa_decode_workspace_size_bt(int(num_seqs), int(max_blocks_per_seq),
+                                                     int(block_tokens)))
 
 
-def decode_workspace(num_seqs: int, max_blocks_per_seq: int, device=None):
+def decode_workspace(num_seqs: int, max_blocks_per_seq: int, device=None,
+                     block_tokens: int = PA_BLOCK_TOKENS):
     """A zero-filled uint8 CUDA tensor of pa_decode_workspace_size bytes, the
     state pa_decode_attention expects on first use."""
     torch = _torch()
-    n = pa_decode_workspace_size(num_seqs, max_blocks_per_seq)
+    n = pa_decode_workspace_size(num_seqs, max_blocks_per_seq, block_tokens)
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
@@ -260,25 +286,31 @@ def pa_decode_attention(out, q, kv_cache, block_table, context_lens, layer, scal
     pa_decode_workspace_size bytes.  num_seqs defaults to block_table rows."""
     n_rows, n_layers, max_blocks = block_table.shape
     n = n_rows if num_seqs is None else int(num_seqs)
-    rc = library().pa_decode_attention(
-        _dev(out, "out", _bf16()), _dev(q, "q", _bf16()), _dev(kv_cache, "kv_cache", _bf16()),
-        int(kv_cache.shape[0]), _dev(block_table, "block_table", _i32()), int(n_layers),
-        int(max_blocks), _dev(context_lens, "context_lens", _i32()), n, int(layer),
-        float(scale), _dev(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _dev(err, "err", _i32()), _stream(stream))
-    _check("pa_decode_attention", rc)
+    page = _page_tokens(kv_cache)
+    head = (_dev(out, "out", _bf16()), _dev(q, "q", _bf16()),
+            _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]))
+    rest = (_dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+            _dev(context_lens, "context_lens", _i32()), n, int(layer), float(scale),
+            _dev(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+            _dev(err, "err", _i32()), _stream(stream))
+    if page == PA_BLOCK_TOKENS:
+        _check("pa_decode_attention", library().pa_decode_attention(*head, *rest))
+    else:
+        _check("pa_decode_attention_bt", library().pa_decode_attention_bt(*head, page, *rest))
 
 
 def pa_free(seq_ids, block_table, context_lens, free_list, free_count, num_blocks, err,
-            stream=None):
+            stream=None, block_tokens=PA_BLOCK_TOKENS):
     n, n_layers, max_blocks = block_table.shape
-    rc = library().pa_free(
-        _dev(seq_ids, "seq_ids", _i32()), int(seq_ids.numel()),
-        _dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
-        _dev(context_lens, "context_lens", _i32()), _dev(free_list, "free_list", _i32()),
-        _dev(free_count, "free_count", _i32()), int(num_blocks), _dev(err, "err", _i32()),
-        _stream(stream))
-    _check("pa_free", rc)
+    ids = (_dev(seq_ids, "seq_ids", _i32()), int(seq_ids.numel()))
+    rest = (_dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+            _dev(context_lens, "context_lens", _i32()), _dev(free_list, "free_list", _i32()),
+            _dev(free_count, "free_count", _i32()), int(num_blocks), _dev(err, "err", _i32()),
+            _stream(stream))
+    if block_tokens == PA_BLOCK_TOKENS:
+        _check("pa_free", library().pa_free(*ids, *rest))
+    else:
+        _check("pa_free_bt", library().pa_free_bt(*ids, int(block_tokens), *rest))
 
 
 def pa_decode_set_grid_limit(max_ctas: int) -> None:

@@ -78,11 +78,12 @@ __device__ __forceinline__ int cta_exclusive_count(bool flag, int *tot, int *tot
   return before + before_in_warp;
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) {
   __shared__ int tot[kScanCta / 32];
   pdl_wait_primary();        // the table and free list may come from the previous kernel
   pdl_launch_dependents();   // the store kernel may start its rotations now
-  const int cap = p.max_blocks * kBs;
+  const int cap = p.max_blocks * BT;
   // a count outside [0, num_blocks] never indexes past the free list
   const int fc0 = min(max(*p.free_count, 0), p.num_blocks);
   int served = 0;
@@ -94,12 +95,12 @@ __global__ void __launch_bounds__(kScanCta) append_alloc_kernel(AppendParams p) 
       pos = p.context_lens[i];
       const bool in_range = pos >= 0 && pos < cap;
       if (!in_range) report(p.err, PA_DEV_CTX_RANGE);
-      need = in_range && (pos % kBs == 0);
+      need = in_range && (pos % BT == 0);
     }
     int chunk = 0;
     const int rank = served + cta_exclusive_count(need, tot, &chunk);
     if (need) {
-      int32_t *entry = p.block_table + table_row(i, p.n_layers, p.layer, p.max_blocks) + pos / kBs;
+      int32_t *entry = p.block_table + table_row(i, p.n_layers, p.layer, p.max_blocks) + pos / BT;
       if (rank < fc0) {
         const int blk = p.free_list[fc0 - 1 - rank];
         *entry = blk;
@@ -186,13 +187,16 @@ __device__ __forceinline__ float2 rope_cos_sin(int pos, double f) {
   return make_float2(fmaf(-sn, rerr, cn), fmaf(cn, rerr, sn));
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParams p) {
+  constexpr size_t kHalfPageBytes = static_cast<size_t>(BT) * kTokRowBytes;
+  constexpr size_t kPageBytes = 2 * kHalfPageBytes;
   __shared__ float2 cs[kD / 2];
   pdl_launch_dependents();   // the next kernel may start its own set-up
   const int s = blockIdx.x;
   const int tid = threadIdx.x;
   const int pos = p.context_lens[s];
-  const bool in_range = pos >= 0 && pos < p.max_blocks * kBs;
+  const bool in_range = pos >= 0 && pos < p.max_blocks * BT;
   if (!in_range) {            // reported by the allocation kernel
     pdl_wait_primary();
     return;
@@ -223,25 +227,25 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
 
   // the entry of a page that starts now is written by the allocation kernel;
   // an existing page's entry was written before that kernel started
-  if (pos % kBs == 0) pdl_wait_primary();
+  if (pos % BT == 0) pdl_wait_primary();
   const int blk =
-      p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + pos / kBs];
+      p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + pos / BT];
   if (blk < 0 || blk >= p.num_blocks) {
     // a new page that was refused or popped invalid is reported by the
     // allocation kernel; an invalid existing entry is reported here
-    if (tid == 0 && pos % kBs != 0) report(p.err, PA_DEV_BAD_BLOCK);
+    if (tid == 0 && pos % BT != 0) report(p.err, PA_DEV_BAD_BLOCK);
     pdl_wait_primary();   // this grid ends after the allocation kernel
     return;
   }
-  unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
-  const int slot = pos % kBs;
+  unsigned char *block = p.kv + static_cast<size_t>(blk) * kPageBytes;
+  const int slot = pos % BT;
   if (head < kHkv) {
     unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
     *reinterpret_cast<uint2 *>(krow + 8 * j) = klo;
     *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = khi;
   }
   if (tid < kTokRowBytes / 16)
-    reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v;
+    reinterpret_cast<uint4 *>(block + kHalfPageBytes + slot * kTokRowBytes)[tid] = v;
   pdl_wait_primary();   // this grid ends after the allocation kernel
 }
 
@@ -421,9 +425,10 @@ struct FreeParams {
   int num_blocks;
 };
 
+template <int BT>
 __global__ void __launch_bounds__(kScanCta) free_kernel(FreeParams p) {
   __shared__ int tot[kScanCta / 32];
-  const int cap = p.max_blocks * kBs;
+  const int cap = p.max_blocks * BT;
   const int fc0 = *p.free_count;
   int pushed = 0;
   for (int i = 0; i < p.n_free; ++i) {
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kScanCta) free_kernel(FreeParams p) {
       if (threadIdx.x == 0) report(p.err, PA_DEV_CTX_RANGE);
       T = min(max(T, 0), cap);
     }
-    const int nb = (T + kBs - 1) / kBs;
+    const int nb = (T + BT - 1) / BT;
     const long long entries = static_cast<long long>(nb) * p.n_layers;
     for (long long e0 = 0; e0 < entries; e0 += kScanCta) {
       const long long e = e0 + threadIdx.x;
@@ -481,15 +486,17 @@ __global__ void __launch_bounds__(kScanCta) free_kernel(FreeParams p) {
 
 using namespace pa;
 
-extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
-                                 uint16_t *q_or_null, uint16_t *kv_cache, int num_blocks,
-                                 int32_t *block_table, int n_layers, int max_blocks_per_seq,
-                                 const int32_t *context_lens, int num_seqs, int layer,
-                                 int32_t *free_list, int32_t *free_count, int32_t *err,
-                                 void *stream) {
+namespace {
+
+template <int BT>
+int kv_append_rope_impl(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                        uint16_t *kv_cache, int num_blocks, int32_t *block_table, int n_layers,
+                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                        int layer, int32_t *free_list, int32_t *free_count, int32_t *err,
+                        void *stream) {
   if (num_seqs < 0 || num_blocks <= 0 || n_layers <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * BT > INT_MAX) return PA_ERR_ARG;
   if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
   if (num_seqs == 0) return PA_OK;
   if (!k_new || !v_new || !kv_cache || !block_table || !context_lens || !free_list ||
@@ -521,12 +528,49 @@ extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
   prm.layer = layer;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(append_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
+  if (launch_pdl(append_alloc_kernel<BT>, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_pdl(append_store_kernel, dim3(num_seqs), dim3(kStoreThreads), 0, st, prm) !=
+  if (launch_pdl(append_store_kernel<BT>, dim3(num_seqs), dim3(kStoreThreads), 0, st, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                                 uint16_t *q_or_null, uint16_t *kv_cache, int num_blocks,
+                                 int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int num_seqs, int layer,
+                                 int32_t *free_list, int32_t *free_count, int32_t *err,
+                                 void *stream) {
+  return kv_append_rope_impl<kBs>(k_new, v_new, q_or_null, kv_cache, num_blocks, block_table,
+                                  n_layers, max_blocks_per_seq, context_lens, num_seqs, layer,
+                                  free_list, free_count, err, stream);
+}
+
+extern "C" int pa_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                                    uint16_t *q_or_null, uint16_t *kv_cache, int num_blocks,
+                                    int block_tokens, int32_t *block_table, int n_layers,
+                                    int max_blocks_per_seq, const int32_t *context_lens,
+                                    int num_seqs, int layer, int32_t *free_list,
+                                    int32_t *free_count, int32_t *err, void *stream) {
+  switch (block_tokens) {
+    case 8:
+      return kv_append_rope_impl<8>(k_new, v_new, q_or_null, kv_cache, num_blocks, block_table,
+                                    n_layers, max_blocks_per_seq, context_lens, num_seqs, layer,
+                                    free_list, free_count, err, stream);
+    case 16:
+      return kv_append_rope_impl<16>(k_new, v_new, q_or_null, kv_cache, num_blocks, block_table,
+                                     n_layers, max_blocks_per_seq, context_lens, num_seqs, layer,
+                                     free_list, free_count, err, stream);
+    case 32:
+      return kv_append_rope_impl<32>(k_new, v_new, q_or_null, kv_cache, num_blocks, block_table,
+                                     n_layers, max_blocks_per_seq, context_lens, num_seqs, layer,
+                                     free_list, free_count, err, stream);
+    default:
+      return PA_ERR_ARG;
+  }
 }
 
 extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
@@ -579,12 +623,15 @@ extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_n
   return PA_OK;
 }
 
-extern "C" int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_layers,
-                       int max_blocks_per_seq, const int32_t *context_lens, int32_t *free_list,
-                       int32_t *free_count, int num_blocks, int32_t *err, void *stream) {
+namespace {
+
+template <int BT>
+int free_impl(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_layers,
+              int max_blocks_per_seq, const int32_t *context_lens, int32_t *free_list,
+              int32_t *free_count, int num_blocks, int32_t *err, void *stream) {
   if (n_free < 0 || num_blocks <= 0 || n_layers <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * BT > INT_MAX) return PA_ERR_ARG;
   if (n_free == 0) return PA_OK;
   if (!seq_ids || !block_table || !context_lens || !free_list || !free_count || !err)
     return PA_ERR_NULL;
@@ -602,9 +649,37 @@ extern "C" int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table,
   prm.n_layers = n_layers;
   prm.max_blocks = max_blocks_per_seq;
   prm.num_blocks = num_blocks;
-  free_kernel<<<1, kScanCta, 0, static_cast<cudaStream_t>(stream)>>>(prm);
+  free_kernel<BT><<<1, kScanCta, 0, static_cast<cudaStream_t>(stream)>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_layers,
+                       int max_blocks_per_seq, const int32_t *context_lens, int32_t *free_list,
+                       int32_t *free_count, int num_blocks, int32_t *err, void *stream) {
+  return free_impl<kBs>(seq_ids, n_free, block_table, n_layers, max_blocks_per_seq, context_lens,
+                        free_list, free_count, num_blocks, err, stream);
+}
+
+extern "C" int pa_free_bt(const int32_t *seq_ids, int n_free, int block_tokens,
+                          int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t *free_list, int32_t *free_count,
+                          int num_blocks, int32_t *err, void *stream) {
+  switch (block_tokens) {
+    case 8:
+      return free_impl<8>(seq_ids, n_free, block_table, n_layers, max_blocks_per_seq,
+                          context_lens, free_list, free_count, num_blocks, err, stream);
+    case 16:
+      return free_impl<16>(seq_ids, n_free, block_table, n_layers, max_blocks_per_seq,
+                           context_lens, free_list, free_count, num_blocks, err, stream);
+    case 32:
+      return free_impl<32>(seq_ids, n_free, block_table, n_layers, max_blocks_per_seq,
+                           context_lens, free_list, free_count, num_blocks, err, stream);
+    default:
+      return PA_ERR_ARG;
+  }
 }
 
 extern "C" const char *pa_error_string(int code) {

@@ -56,16 +56,22 @@ constexpr int kEndOfWork = 4;  // no more blocks; the stage carries no data
 
 struct StageDesc {
   int seq;
-  int n_valid;   // tokens of the block inside the context, 1..16 (negative: block skipped)
+  int n_valid;   // tokens of the tile inside the context, 1..16 (negative: tile skipped)
   int flags;
   int n_parts;   // pieces the sequence is cut into
   int slot;      // partial slot of this piece
+  int vmask;     // 8-token pages: rows of the tile that were loaded (bit t = token t)
 };
 
-// One stage = one physical block, as 8 kv-head tiles of [K|V][16 tokens][64],
-// each 128-byte row swizzled (16-byte chunk c stored at c ^ (token & 7)).
+// The unit of work is a 16-token tile of a sequence: one page of 16 tokens,
+// two pages of 8, or half a page of 32.  One stage = one tile, as 8 kv-head
+// tiles of [K|V][16 tokens][64], each 128-byte row swizzled (16-byte chunk c
+// stored at c ^ (token & 7)).
+constexpr int kTileTokens = 16;
+constexpr int kStageBytes = kHkv * kHeadTileBytes;   // 32 KiB
+
 struct __align__(1024) Smem {
-  unsigned char kv[kStages][kBlockBytes];
+  unsigned char kv[kStages][kStageBytes];
   int prefix[kMaxSeqs + 1];      // prefix[s] = blocks of sequences 0..s-1
   unsigned char tail[kMaxSeqs];  // tokens in the last block of sequence s (1..16)
   StageDesc desc[kStages];
@@ -90,6 +96,7 @@ struct DecodeParams {
   int max_blocks;
   int num_seqs;
   int layer;
+  int cap_tokens;      // max_blocks * tokens per page: the largest context
   float qscale;        // scale * log2(e), applied to the fp32 scores
 };
 
@@ -103,7 +110,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ int clamped_ctx(const DecodeParams &p, int s) {
   const int t = p.context_lens[s];
-  return min(max(t, 0), p.max_blocks * kBs);
+  return min(max(t, 0), p.cap_tokens);
 }
 
 // Chunk length in blocks: about kChunksPerCta chunks per CTA, at least 8
@@ -137,7 +144,7 @@ __device__ __forceinline__ int block_prefix(const DecodeParams &p, Smem &sm, int
     int nb = 0;
     if (tid < kScanThreads && i < p.num_seqs) {
       const int t = p.context_lens[i];
-      if (report_range && (t < 0 || t > p.max_blocks * kBs)) report(p.err, PA_DEV_CTX_RANGE);
+      if (report_range && (t < 0 || t > p.cap_tokens)) report(p.err, PA_DEV_CTX_RANGE);
       nb = (clamped_ctx(p, i) + kBs - 1) / kBs;
     }
     int incl = nb;
@@ -175,8 +182,20 @@ __device__ __forceinline__ int seq_of_block(const int *prefix, int n, int b) {
   return lo;
 }
 
+// Page ids of tile j of a table row, for pages of BT tokens: the tile's page
+// (BT = 16), the page holding it (BT = 32, the tile is half of it), or its
+// two pages (BT = 8; the second only exists when the tile has more than 8
+// tokens, n_pages8 = ceil(context / 8)).
+template <int BT>
+__device__ __forceinline__ int tile_page(const int32_t *row, int j) {
+  return BT == 32 ? row[j >> 1] : (BT == 8 ? row[2 * j] : row[j]);
+}
+
+template <int BT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeParams p) {
+  static_assert(BT == 8 || BT == 16 || BT == 32, "pages of 8, 16 or 32 tokens");
+  constexpr size_t kPageBytes = static_cast<size_t>(BT) * kTokRowBytes * 2;
   extern __shared__ unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
@@ -218,11 +237,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (blockIdx.x < (nb_spec + c_spec - 1) / c_spec && b < min(nb_spec, (blockIdx.x + 1) * c_spec)) {
         const int s = seq_of_block(sm.prefix, p.num_seqs, b);
         const int j = b - sm.prefix[s];
-        if (j >= 0 && j < p.max_blocks) {
-          const int blk =
-              p.block_table[(static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks + j];
+        const int32_t *row =
+            p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+        if (j >= 0 && j * kTileTokens < p.cap_tokens) {
+          const int blk = tile_page<BT>(row, j);
           if (blk >= 0 && blk < p.num_blocks)
-            prefetch_bulk_l2(p.kv + static_cast<size_t>(blk) * kBlockBytes, kBlockBytes);
+            prefetch_bulk_l2(p.kv + static_cast<size_t>(blk) * kPageBytes, kPageBytes);
+          if (BT == 8 && 2 * j + 1 < p.max_blocks) {
+            const int blk2 = row[2 * j + 1];
+            if (blk2 >= 0 && blk2 < p.num_blocks)
+              prefetch_bulk_l2(p.kv + static_cast<size_t>(blk2) * kPageBytes, kPageBytes);
+          }
         }
       }
     }
@@ -237,20 +262,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // sequence's block count still matches the speculative prefix.  If all
   // match, that prefix is the real one and the ids are used as read;
   // otherwise the prefix is rebuilt and the ids are read again.
-  int pre_blk = -1;
+  int pre_blk = -1, pre_blk2 = -1;
   const int c_spec = nb_spec > 0 ? chunk_blocks(nb_spec, G) : 1;
   const int b_pre = blockIdx.x * c_spec + lane;
   if (warp == kConsumerWarps && nb_spec > 0 && b_pre < min(nb_spec, (blockIdx.x + 1) * c_spec)) {
     const int s = seq_of_block(sm.prefix, p.num_seqs, b_pre);
     const int j = b_pre - sm.prefix[s];
-    if (j >= 0 && j < p.max_blocks)
-      pre_blk = p.block_table[(static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks + j];
+    const int32_t *row =
+        p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+    if (j >= 0 && j * kTileTokens < p.cap_tokens) {
+      pre_blk = tile_page<BT>(row, j);
+      if (BT == 8 && 2 * j + 1 < p.max_blocks) pre_blk2 = row[2 * j + 1];
+    }
   }
   int changed = 0;
   for (int i = tid; i < p.num_seqs; i += kThreads) {
     const int t = p.context_lens[i];
-    if (blockIdx.x == 0 && (t < 0 || t > p.max_blocks * kBs)) report(p.err, PA_DEV_CTX_RANGE);
-    const int tc = min(max(t, 0), p.max_blocks * kBs);
+    if (blockIdx.x == 0 && (t < 0 || t > p.cap_tokens)) report(p.err, PA_DEV_CTX_RANGE);
+    const int tc = min(max(t, 0), p.cap_tokens);
     const int nb = (tc + kBs - 1) / kBs;
     sm.tail[i] = static_cast<unsigned char>(tc - (nb - 1) * kBs);
     changed |= (nb != sm.prefix[i + 1] - sm.prefix[i]);
@@ -303,12 +332,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const int off0 = B + j0 - b0;
           const bool use_pre =
               plan_kept && k == static_cast<int>(blockIdx.x) && off0 + cnt <= 32;
-          int my_blk = 0;
-          if (!use_pre && j0 + lane < je) my_blk = row[j0 + lane];
+          int my_blk = 0, my_blk2 = -1;
+          if (!use_pre && j0 + lane < je) {
+            my_blk = tile_page<BT>(row, j0 + lane);
+            // the second 8-token page exists when the tile holds more than 8 tokens
+            if (BT == 8 && (j0 + lane < nb - 1 || tail > 8)) my_blk2 = row[2 * (j0 + lane) + 1];
+          }
           for (int e = 0; e < cnt; ++e) {
             const int blk = use_pre ? __shfl_sync(0xffffffffu, pre_blk, off0 + e)
                                     : __shfl_sync(0xffffffffu, my_blk, e);
             const int j = j0 + e;
+            int blk2 = -1;
+            if (BT == 8) {
+              blk2 = use_pre ? __shfl_sync(0xffffffffu, pre_blk2, off0 + e)
+                             : __shfl_sync(0xffffffffu, my_blk2, e);
+            }
             int good = 1;
             if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
             good = __shfl_sync(0xffffffffu, good, 0);
@@ -316,29 +354,56 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               ok = false;
               break;
             }
-            const bool valid = blk >= 0 && blk < p.num_blocks;
+            const int n_tok = (j == nb - 1) ? tail : kTileTokens;
+            const bool valid_a = blk >= 0 && blk < p.num_blocks;
+            // 8-token pages: the second page, when the tile reaches into it
+            const bool has_b = BT == 8 && n_tok > 8;
+            const bool valid_b = has_b && blk2 >= 0 && blk2 < p.num_blocks;
+            const bool valid = valid_a || valid_b;
             if (lane == 0) {
               StageDesc d;
               d.seq = s;
-              d.n_valid = (j == nb - 1) ? tail : kBs;
-              if (!valid) d.n_valid = -d.n_valid;   // consumers skip it
+              d.n_valid = valid ? n_tok : -n_tok;   // negative: consumers skip it
               d.flags = (j == jb ? kSegStart : 0) | (j == je - 1 ? kSegEnd : 0);
               d.n_parts = n_parts;
               d.slot = slot;
+              d.vmask = (valid_a ? 0x00ff : 0) | (valid_b ? 0xff00 : 0);
               sm.desc[stage] = d;
+              if (!valid_a || (has_b && !valid_b)) report(p.err, PA_DEV_BAD_BLOCK);
               if (valid) {
-                mbar_arrive_expect_tx(&sm.full[stage], kBlockBytes);
+                const uint32_t bytes =
+                    BT == 8 ? (valid_a ? kStageBytes / 2 : 0) + (valid_b ? kStageBytes / 2 : 0)
+                            : kStageBytes;
+                mbar_arrive_expect_tx(&sm.full[stage], bytes);
               } else {
-                report(p.err, PA_DEV_BAD_BLOCK);
                 mbar_arrive(&sm.full[stage]);
               }
               issued |= 1u << stage;
               issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
             __syncwarp();
-            if (valid && lane < kHkv)   // one 4 KiB tile per kv head, 8 lanes in parallel
-              tma_load_5d(sm.kv[stage] + lane * kHeadTileBytes, &kv_map, 0, lane, 0, 0, blk,
-                          &sm.full[stage]);
+            if (BT == 16) {
+              if (valid && lane < kHkv)   // one 4 KiB tile per kv head, 8 lanes in parallel
+                tma_load_5d(sm.kv[stage] + lane * kHeadTileBytes, &kv_map, 0, lane, 0, 0, blk,
+                            &sm.full[stage]);
+            } else if (BT == 32) {
+              // K (lanes 0..7) and V (lanes 8..15) halves of the page, 2 KiB each
+              if (valid && lane < 2 * kHkv) {
+                const int h = lane & 7, kv = lane >> 3;
+                tma_load_5d(sm.kv[stage] + h * kHeadTileBytes + kv * (kHeadTileBytes / 2),
+                            &kv_map, 0, h, (j & 1) * kTileTokens, kv, blk, &sm.full[stage]);
+              }
+            } else {
+              // K and V of each 8-token page, 1 KiB each: lane = head + 8 * part,
+              // part 0/1 = K/V of the first page, 2/3 = K/V of the second
+              const int h = lane & 7, part = lane >> 3;
+              const bool second = part >= 2;
+              const int kv = part & 1;
+              if (second ? valid_b : valid_a)
+                tma_load_5d(sm.kv[stage] + h * kHeadTileBytes + kv * (kHeadTileBytes / 2) +
+                                (second ? kHeadTileBytes / 4 : 0),
+                            &kv_map, 0, h, 0, kv, second ? blk2 : blk, &sm.full[stage]);
+            }
             if (!asked) {
               if (lane == 0) next = G + atomicAdd(p.chunk_counter, 1);
               asked = true;
@@ -416,11 +481,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         unsigned char *tile = sm.kv[stage] + g * kHeadTileBytes;
         const uint32_t ktile = smem_u32(tile);
         const uint32_t vtile = ktile + kBs * kHeadRowBytes;
-        if (n_valid < kBs) {
-          // rows past the context may hold anything (NaN included): zero the
-          // V rows, the K rows are masked in the scores
+        // rows to use: the tile's tokens inside the context, less (8-token
+        // pages) a page that was out of range
+        const int use = (BT == 8) ? (d.vmask & ((1 << n_valid) - 1)) : ((1 << n_valid) - 1);
+        if (use != 0xffff) {
+          // rows past the context or not loaded may hold anything (NaN
+          // included): zero the V rows, the K rows are masked in the scores
           uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
-          for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
+          if (BT == 8) {
+            for (int e = lane; e < kBs * 8; e += 32)
+              if (!((use >> (e >> 3)) & 1)) vrow[e] = make_uint4(0, 0, 0, 0);
+          } else {
+            for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
+          }
           fence_proxy_async_smem();
           __syncwarp();
         }
@@ -438,10 +511,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // ---- online softmax on row r (q head), columns c2, c2+1, 8+c2, 9+c2
         float x0 = s0[0] * p.qscale, x1 = s0[1] * p.qscale;
         float x2 = s1[0] * p.qscale, x3 = s1[1] * p.qscale;
-        x0 = (c2 < n_valid) ? x0 : neg_inf();
-        x1 = (c2 + 1 < n_valid) ? x1 : neg_inf();
-        x2 = (c2 + 8 < n_valid) ? x2 : neg_inf();
-        x3 = (c2 + 9 < n_valid) ? x3 : neg_inf();
+        if (BT == 8) {
+          x0 = ((use >> c2) & 1) ? x0 : neg_inf();
+          x1 = ((use >> (c2 + 1)) & 1) ? x1 : neg_inf();
+          x2 = ((use >> (c2 + 8)) & 1) ? x2 : neg_inf();
+          x3 = ((use >> (c2 + 9)) & 1) ? x3 : neg_inf();
+        } else {
+          x0 = (c2 < n_valid) ? x0 : neg_inf();
+          x1 = (c2 + 1 < n_valid) ? x1 : neg_inf();
+          x2 = (c2 + 8 < n_valid) ? x2 : neg_inf();
+          x3 = (c2 + 9 < n_valid) ? x3 : neg_inf();
+        }
         float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -607,10 +687,11 @@ WsLayout ws_layout(int num_seqs, long long slots) {
   return w;
 }
 
-int auto_grid(const DeviceInfo &di, int num_seqs, int max_blocks) {
+// max_tiles: 16-token tiles of the longest context a table row can hold
+int auto_grid(const DeviceInfo &di, int num_seqs, int max_tiles) {
   long long g = static_cast<long long>(di.sm_count) * kCtasPerSm;
   if (g_grid_limit > 0) g = min(g, static_cast<long long>(g_grid_limit));
-  g = min(g, static_cast<long long>(num_seqs) * max_blocks);
+  g = min(g, static_cast<long long>(num_seqs) * max_tiles);
   g = min(g, static_cast<long long>(kMaxGrid));
   return static_cast<int>(max(g, 1LL));
 }
@@ -634,11 +715,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
+  return make_kv_map_bt(map, kv_cache, num_blocks, kBs);
+}
+
+// Pages of bt tokens: dims (d 64, kv head 8, token bt, K|V 2, block); box one
+// kv head's K and V of a 16-token page (64, 1, 16, 2, 1), or, for 8- and
+// 32-token pages, one kv head's K or V rows of a tile's page (64, 1, 8 or
+// 16, 1, 1).
+int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
-  const cuuint64_t dims[5] = {kD, kHkv, kBs, 2, static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[4] = {kHeadRowBytes, kTokRowBytes, kHalfBlockBytes, kBlockBytes};
-  const cuuint32_t box[5] = {kD, 1, kBs, 2, 1};
+  const cuuint64_t row = kTokRowBytes;
+  const cuuint64_t dims[5] = {kD, kHkv, static_cast<cuuint64_t>(bt), 2,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kHeadRowBytes, row, row * bt, row * bt * 2};
+  const cuuint32_t box_tok = bt == 8 ? 8u : 16u;
+  const cuuint32_t box_kv = bt == 16 ? 2u : 1u;
+  const cuuint32_t box[5] = {kD, 1, box_tok, box_kv, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -670,12 +763,28 @@ int current_device(DeviceInfo *info) {
 
 using namespace pa;
 
-extern "C" size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq) {
-  if (num_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
+namespace {
+
+bool page_size_ok(int bt) { return bt == 8 || bt == 16 || bt == 32; }
+
+long long max_tiles(int max_blocks_per_seq, int bt) {
+  return (static_cast<long long>(max_blocks_per_seq) * bt + kTileTokens - 1) / kTileTokens;
+}
+
+}  // namespace
+
+extern "C" size_t pa_decode_workspace_size_bt(int num_seqs, int max_blocks_per_seq,
+                                              int block_tokens) {
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0 || !page_size_ok(block_tokens)) return 0;
   DeviceInfo di;
   if (current_device(&di) != PA_OK) di.sm_count = kMaxGrid;   // generous when no device answers
-  const int G = auto_grid(di, num_seqs, max_blocks_per_seq);
+  const long long tiles = max_tiles(max_blocks_per_seq, block_tokens);
+  const int G = auto_grid(di, num_seqs, static_cast<int>(min(tiles, static_cast<long long>(INT_MAX))));
   return ws_layout(num_seqs, max_slots(num_seqs, G)).total;
+}
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq) {
+  return pa_decode_workspace_size_bt(num_seqs, max_blocks_per_seq, kBs);
 }
 
 extern "C" int pa_decode_set_grid_limit(int max_ctas) {
@@ -684,16 +793,20 @@ extern "C" int pa_decode_set_grid_limit(int max_ctas) {
   return PA_OK;
 }
 
-extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
-                                   int num_blocks, const int32_t *block_table, int n_layers,
-                                   int max_blocks_per_seq, const int32_t *context_lens,
-                                   int num_seqs, int layer, float scale, void *workspace,
-                                   size_t workspace_bytes, int32_t *err, void *stream) {
+namespace {
+
+template <int BT>
+int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                          int num_blocks, const int32_t *block_table, int n_layers,
+                          int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                          int layer, float scale, void *workspace, size_t workspace_bytes,
+                          int32_t *err, void *stream) {
   if (num_seqs < 0 || num_seqs > kMaxSeqs || num_blocks <= 0 || n_layers <= 0 ||
       max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX ||
-      static_cast<long long>(num_seqs) * max_blocks_per_seq > INT_MAX)
+  const long long tiles = max_tiles(max_blocks_per_seq, BT);
+  if (static_cast<long long>(max_blocks_per_seq) * BT > INT_MAX ||
+      static_cast<long long>(num_seqs) * tiles > INT_MAX)
     return PA_ERR_ARG;
   if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
   if (num_seqs == 0) return PA_OK;
@@ -705,7 +818,7 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   int rc = current_device(&di);
   if (rc != PA_OK) return rc;
 
-  int G = auto_grid(di, num_seqs, max_blocks_per_seq);
+  int G = auto_grid(di, num_seqs, static_cast<int>(tiles));
   WsLayout w = ws_layout(num_seqs, max_slots(num_seqs, G));
   while (w.total > workspace_bytes && G > 1) {
     G = G / 2;
@@ -716,18 +829,19 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   static bool attr_done[64] = {};
   const size_t smem = sizeof(Smem) + 1024;   // + room to align the base to 1 KiB
   if (!attr_done[di.device]) {
-    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_split_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_done[di.device] = true;
   }
 
   // the tensor map describes the pool; rebuilt only when the pool changes
+  // (one cache per page size: each instance of this function has its own)
   static thread_local const void *map_pool = nullptr;
   static thread_local int map_blocks = 0;
   alignas(64) static thread_local CUtensorMap map;
   if (map_pool != kv_cache || map_blocks != num_blocks) {
-    rc = make_kv_map(&map, kv_cache, num_blocks);
+    rc = make_kv_map_bt(&map, kv_cache, num_blocks, BT);
     if (rc != PA_OK) return rc;
     map_pool = kv_cache;
     map_blocks = num_blocks;
@@ -750,16 +864,54 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
   prm.max_blocks = max_blocks_per_seq;
   prm.num_seqs = num_seqs;
   prm.layer = layer;
+  prm.cap_tokens = max_blocks_per_seq * BT;
   prm.qscale = scale * kLog2e;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(decode_split_kernel, dim3(G), dim3(kThreads), smem, st, map, prm) != cudaSuccess)
+  if (launch_pdl(decode_split_kernel<BT>, dim3(G), dim3(kThreads), smem, st, map, prm) !=
+      cudaSuccess)
     return PA_ERR_CUDA;
   const cudaError_t e =
       num_seqs >= 8 ? launch_pdl(decode_merge_kernel<4>, dim3(num_seqs, kHq), dim3(4 * 32), 0, st, prm)
                     : launch_pdl(decode_merge_kernel<16>, dim3(num_seqs, kHq), dim3(16 * 32), 0, st, prm);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                                   int num_blocks, const int32_t *block_table, int n_layers,
+                                   int max_blocks_per_seq, const int32_t *context_lens,
+                                   int num_seqs, int layer, float scale, void *workspace,
+                                   size_t workspace_bytes, int32_t *err, void *stream) {
+  return decode_attention_impl<kBs>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                    max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                    workspace, workspace_bytes, err, stream);
+}
+
+extern "C" int pa_decode_attention_bt(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                                      int num_blocks, int block_tokens,
+                                      const int32_t *block_table, int n_layers,
+                                      int max_blocks_per_seq, const int32_t *context_lens,
+                                      int num_seqs, int layer, float scale, void *workspace,
+                                      size_t workspace_bytes, int32_t *err, void *stream) {
+  switch (block_tokens) {
+    case 8:
+      return decode_attention_impl<8>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                      max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                      workspace, workspace_bytes, err, stream);
+    case 16:
+      return decode_attention_impl<16>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                       workspace, workspace_bytes, err, stream);
+    case 32:
+      return decode_attention_impl<32>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                       workspace, workspace_bytes, err, stream);
+    default:
+      return PA_ERR_ARG;
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -31,6 +31,11 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // one block, 128-byte swizzle.  Returns PA_OK or PA_ERR_CUDA.
 int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 
+// The same over a pool of bt-token pages (8, 16 or 32): box (64, 1, 16, 2, 1)
+// for 16, one kv head's K or V rows of a 16-token tile (64, 1, 8 or 16, 1, 1)
+// for 8 and 32.
+int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt);
+
 // Launch `kernel` with the programmatic-stream-serialization attribute, so it
 // may start while the previous kernel on the stream finishes; the kernel
 // itself must wait (griddepcontrol.wait) before reading that kernel's output.

@@ -74,22 +74,24 @@ def workspace_for(n, max_blocks):
 
 def gather_for_oracle(pool_dev, block_table: np.ndarray, seqs, ctx, layer):
     """Copy the blocks that sequences `seqs` read in `layer` from a device pool
-    into a compact host pool, with the table rows renumbered to it."""
+    [num_blocks][2][page][8][64] into a compact host pool, with the table rows
+    renumbered to it."""
     import torch
+    page = int(pool_dev.shape[2])
     rows = []
     ids = []
     for s in seqs:
-        nb = (int(ctx[s]) + wl.BLOCK - 1) // wl.BLOCK
+        nb = (int(ctx[s]) + page - 1) // page
         rows.append(block_table[s, layer, :nb])
         ids.extend(block_table[s, layer, :nb].tolist())
     uniq = sorted(set(ids))
     remap = {b: i for i, b in enumerate(uniq)}
     idx = torch.tensor(uniq, dtype=torch.long, device=pool_dev.device)
-    sub = host_bits(pool_dev.index_select(0, idx)) if uniq else np.zeros((0, 2, 16, 8, 64), np.uint16)
+    sub = host_bits(pool_dev.index_select(0, idx)) if uniq else np.zeros((0, 2, page, 8, 64), np.uint16)
     mb = max(1, max((len(r) for r in rows), default=1))
     bt = np.full((len(seqs), 1, mb), -1, dtype=np.int32)
     for i, r in enumerate(rows):
         bt[i, 0, :len(r)] = [remap[b] for b in r.tolist()]
     if sub.shape[0] == 0:
-        sub = np.zeros((1, 2, 16, 8, 64), np.uint16)
+        sub = np.zeros((1, 2, page, 8, 64), np.uint16)
     return sub, bt

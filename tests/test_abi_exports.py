@@ -45,3 +45,17 @@ def test_host_validation_without_a_device():
     assert lib.pa_free(z, 2, z, 1, 4, z, z, z, 8, z, z) == -1
     assert lib.pa_decode_set_grid_limit(-1) == -2
     assert lib.pa_decode_set_grid_limit(0) == 0
+
+
+def test_page_size_entry_points_refuse_other_sizes():
+    """Only 8-, 16- and 32-token pages are built; anything else is refused
+    before any CUDA call."""
+    import ctypes
+    import paged_kv_cache_205_gb300 as pk
+    lib = pk.library()
+    z = ctypes.c_void_p(0)
+    assert lib.pa_decode_attention_bt(z, z, z, 4, 12, z, 1, 4, z, 1, 0, 0.125, z, 0, z, z) == -2
+    assert lib.pa_kv_append_rope_bt(z, z, z, z, 4, 64, z, 1, 4, z, 1, 0, z, z, z, z) == -2
+    assert lib.pa_free_bt(z, 1, 4, z, 1, 4, z, z, z, 4, z, z) == -2
+    assert lib.pa_decode_workspace_size_bt(4, 4, 24) == 0
+    assert pk.pa_decode_workspace_size(4, 4, 8) > 0
