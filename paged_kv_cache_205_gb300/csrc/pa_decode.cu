@@ -739,6 +739,19 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const cuuint64_t dims[5] = {kD, kHkv, kBs, 2, static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kHeadRowBytes, kTokRowBytes, kHalfBlockBytes, kBlockBytes};
+  const cuuint32_t box[5] = {kD, 1, kBs, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int current_device(DeviceInfo *info) {
   static DeviceInfo cache[64];
   int dev = 0;

@@ -36,6 +36,10 @@ int make_kv_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 // for 8 and 32.
 int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt);
 
+// Over a pool of 16-token pages, box (64, 1, 16, 1, 1): one kv head's K rows
+// (or V rows) of one page, 2 KiB.
+int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
+
 // Launch `kernel` with the programmatic-stream-serialization attribute, so it
 // may start while the previous kernel on the stream finishes; the kernel
 // itself must wait (griddepcontrol.wait) before reading that kernel's output.

@@ -1,5 +1,6 @@
 // pa_prefill.cu -- causal attention of a prompt chunk over its sequence's
-// paged cache (the prefill side of the paged path) on sm_103a.
+// paged cache (the prefill side of the paged path) on the sm_103a tensor
+// cores: tcgen05 MMAs from shared memory into TMEM accumulators.
 //
 // Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "The path of
 // one inference": prefill pushes the whole prompt through at once (matrix x
@@ -10,33 +11,51 @@
 // context_lens[s] + i and attends over positions 0..context_lens[s] + i of its
 // sequence, whose K/V (the chunk's own included) are already in the cache.
 //
-// One CTA per (16-token query tile, kv head).  A producer warp streams the
-// kv head's [K|V][16 tokens][64] tiles of blocks 0..(last position)/16 with
-// TMA tensor copies into a ring of stages; four consumer warps, one per q
-// head of the GQA group, each own the tile's 16 query rows and run m16n8k16
-// bf16 MMAs with every row real: S = Q K^T (8 MMAs per block), a causal mask
-// on the diagonal blocks, the online softmax in fp32 (log2 domain), O += P V
-// (8 MMAs).  The tiles of one sequence are read by all its query tiles and
-// stay L2-resident.
+// One CTA per (32-token query tile, kv head): its 128 MMA rows are the 32
+// tokens x the 4 q heads of the GQA group (row = 4 * token + head), so every
+// K/V byte brought into shared memory serves 128 query rows.  Keys go in
+// chunks of 128 (8 pages).  Warp roles (192 threads):
+//   warp 4      producer: the Q tile (one TMA), then per chunk 16 TMA copies
+//               (K rows and V rows of 8 pages) into a 3-stage ring;
+//   warp 5      one thread issues the MMAs: S_j = Q K_j^T (M 128, N 128, 4
+//               k-steps) into one of two TMEM buffers, and, once the
+//               softmax has written P_j, O_j = P_j V_j (M 128, N 64, 8
+//               k-steps, V read as an MN-major operand) into a third;
+//   warps 0-3   softmax, one thread per row (TMEM lane): S_j from TMEM,
+//               causal mask, running max and sum in fp32 (log2 domain), P_j
+//               rounded to bf16 into shared memory (128-byte swizzle, the
+//               layout the MMA reads), the previous chunk's O_j folded into
+//               registers with the max correction, and the output row at the
+//               end.
+// S_{j+1} is computed while the softmax works on S_j.
 #include <climits>
+#include <cudaTypedefs.h>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kQTile = 16;                         // query tokens per CTA
-constexpr int kPWarps = kGqa;                      // consumer warps: one per q head of the group
-constexpr int kPThreads = (kPWarps + 1) * 32;
-constexpr int kPStages = 8;
-constexpr int kTileBytes = 2 * kBs * kHeadRowBytes;   // K and V of one kv head: 4 KiB
+constexpr int kQTok = 32;                     // query tokens per CTA
+constexpr int kRows = kQTok * kGqa;           // 128 MMA rows
+constexpr int kChunk = 128;                   // keys per chunk
+constexpr int kPagesPerChunk = kChunk / kBs;  // 8
+constexpr int kStagesP = 3;
+constexpr int kSoftWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kPThreads = 6 * 32;
+constexpr int kTileRowBytes = kHeadRowBytes;             // 128-byte rows
+constexpr int kOperandBytes = kChunk * kTileRowBytes;    // 16 KiB: 128 rows x 64 bf16
+constexpr uint32_t kTmemCols = 512;                      // S x2 (256) + O (64), rounded up
+constexpr uint32_t kTmemO = 256;
 constexpr int kMaxSeqsP = 2048;
 constexpr float kLog2eP = 1.4426950408889634f;
 
 struct PrefillParams {
   __nv_bfloat16 *out;
-  const uint16_t *q;
   const int32_t *cu_tokens;
   const int32_t *block_table;
   const int32_t *context_lens;
@@ -51,11 +70,19 @@ struct PrefillParams {
 };
 
 struct __align__(1024) PSmem {
-  unsigned char kv[kPStages][kTileBytes];
+  unsigned char q[kOperandBytes];                  // [32 tok][4 heads][64], swizzled
+  unsigned char k[kStagesP][kOperandBytes];        // [128 keys][64]
+  unsigned char v[kStagesP][kOperandBytes];        // [128 keys][64]
+  unsigned char p[2][kOperandBytes];               // P: keys 0-63, 64-127, [128 rows][64]
   int tile_prefix[kMaxSeqsP + 1];
-  int blk_of_stage[kPStages];   // < 0: the block was not loaded
-  uint64_t full[kPStages];
-  uint64_t empty[kPStages];
+  uint64_t q_full;
+  uint64_t kv_full[kStagesP];
+  uint64_t kv_empty[kStagesP];
+  uint64_t s_full[2];
+  uint64_t p_full;
+  uint64_t o_full;
+  uint32_t tmem_base;
+  int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
   int seq, t0, valid;
 };
@@ -68,8 +95,18 @@ __device__ __forceinline__ float p_exp2(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(kPThreads) prefill_attention_kernel(
-    const __grid_constant__ CUtensorMap kv_map, PrefillParams p) {
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
+    const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+    PrefillParams p) {
   extern __shared__ unsigned char smem_raw[];
   PSmem &sm = *reinterpret_cast<PSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -77,10 +114,16 @@ __global__ void __launch_bounds__(kPThreads) prefill_attention_kernel(
   const int g = blockIdx.y;   // kv head
   if (tid == 0) {
     prefetch_tensormap(&kv_map);
-    for (int st = 0; st < kPStages; ++st) {
-      mbar_init(&sm.full[st], 1);
-      mbar_init(&sm.empty[st], kPWarps);
+    prefetch_tensormap(&q_map);
+    mbar_init(&sm.q_full, 1);
+    for (int st = 0; st < kStagesP; ++st) {
+      mbar_init(&sm.kv_full[st], 1);
+      mbar_init(&sm.kv_empty[st], 1);
     }
+    mbar_init(&sm.s_full[0], 1);
+    mbar_init(&sm.s_full[1], 1);
+    mbar_init(&sm.p_full, kSoftWarps * 32);
+    mbar_init(&sm.o_full, 1);
     fence_mbar_init();
   }
   pdl_launch_dependents();
@@ -99,7 +142,7 @@ __global__ void __launch_bounds__(kPThreads) prefill_attention_kernel(
       // a chunk that does not fit its table, or rows outside [0, total_tokens), is refused
       if (ctx >= 0 && n >= 0 && c0 >= 0 && c1 <= p.total_tokens &&
           static_cast<long long>(ctx) + n <= cap)
-        tiles = (n + kQTile - 1) / kQTile;
+        tiles = (n + kQTok - 1) / kQTok;
       else if (blockIdx.x == 0 && blockIdx.y == 0)
         report(p.err, PA_DEV_CTX_RANGE);
     }
@@ -135,7 +178,7 @@ __global__ void __launch_bounds__(kPThreads) prefill_attention_kernel(
         else hi = mid - 1;
       }
       sm.seq = lo;
-      sm.t0 = (t - sm.tile_prefix[lo]) * kQTile;
+      sm.t0 = (t - sm.tile_prefix[lo]) * kQTok;
       sm.valid = 1;
     }
   }
@@ -146,193 +189,283 @@ __global__ void __launch_bounds__(kPThreads) prefill_attention_kernel(
   const int ctx = p.context_lens[s];
   const int row0 = p.cu_tokens[s];
   const int n = p.cu_tokens[s + 1] - row0;
-  const int rows = min(kQTile, n - t0);
-  const int last_pos = ctx + t0 + rows - 1;   // the tile's last query position
-  const int n_blocks = last_pos / kBs + 1;
+  const int rows = min(kQTok, n - t0);                  // real query tokens of the tile
+  const int last_pos = ctx + t0 + rows - 1;             // the tile's last query position
+  const int n_keys = last_pos + 1;
+  const int n_chunks = (n_keys + kChunk - 1) / kChunk;
 
-  if (warp == kPWarps) {
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kProducerWarp) {
     // ===================================================== producer warp ==
     const int32_t *row =
         p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
-    uint32_t issued = 0, issued_parity = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sm.q_full, kOperandBytes);
+      tma_load_3d(sm.q, &q_map, 0, g * kGqa, row0 + t0, &sm.q_full);
+    }
     bool ok = true;
-    for (int j0 = 0; j0 < n_blocks && ok; j0 += 32) {
-      const int my_blk = (j0 + lane < n_blocks) ? row[j0 + lane] : 0;
-      const int cnt = min(32, n_blocks - j0);
-      for (int e = 0; e < cnt; ++e) {
-        const int j = j0 + e;
-        const int stage = j % kPStages;
-        const uint32_t phase = (j / kPStages) & 1;
-        const int blk = __shfl_sync(0xffffffffu, my_blk, e);
-        int good = 1;
-        if (lane == 0) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1)) {
-            good = 0;
-          } else {
-            const bool valid = blk >= 0 && blk < p.num_blocks;
-            sm.blk_of_stage[stage] = valid ? blk : -1;
-            if (valid) {
-              mbar_arrive_expect_tx(&sm.full[stage], kTileBytes);
-              tma_load_5d(sm.kv[stage], &kv_map, 0, g, 0, 0, blk, &sm.full[stage]);
-            } else {
-              report(p.err, PA_DEV_BAD_BLOCK);
-              mbar_arrive(&sm.full[stage]);
-            }
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          }
+    uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
+    for (int j = 0; j < n_chunks && ok; ++j) {
+      const int st = j % kStagesP;
+      const uint32_t ph = (j / kStagesP) & 1;
+      // lane l < 8 looks up page j * 8 + l
+      const int pg = j * kPagesPerChunk + (lane & 7);
+      int blk = -1;
+      const bool needed = lane < kPagesPerChunk && pg * kBs < n_keys;
+      if (needed) blk = row[pg];
+      const bool valid = needed && blk >= 0 && blk < p.num_blocks;
+      const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
+      const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
+      int good = 1;
+      if (lane == 0) {
+        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
+          good = 0;
+        } else {
+          if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
+          sm.pmask[st] = static_cast<int>(vm);
+          mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
+          issued |= 1u << st;
+          issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
         }
-        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-        if (!ok) break;
+      }
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
+      const int pl = lane & 7, kv = (lane >> 3) & 1;
+      const int pblk = __shfl_sync(0xffffffffu, blk, pl);
+      if (lane < 16 && ((vm >> pl) & 1u)) {
+        unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
+        tma_load_5d(dst, &kv_map, 0, g, 0, kv, pblk, &sm.kv_full[st]);
       }
     }
     if (lane == 0) {
       if (!ok) report(p.err, PA_DEV_TIMEOUT);
       // no copy may still be landing in shared memory when the CTA exits
-      for (int st = 0; st < kPStages; ++st)
+      if (!mbar_wait(&sm.q_full, 0)) report(p.err, PA_DEV_TIMEOUT);
+      for (int st = 0; st < kStagesP; ++st)
         if ((issued >> st) & 1u)
-          if (!mbar_wait(&sm.full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
-    }
-    return;
-  }
-
-  // ===================================================== consumer warps ==
-  const int h = g * kGqa + warp;   // q head
-  const int r = lane >> 2, c2 = 2 * (lane & 3);
-  const int lm_i = lane >> 3, lm_r = lane & 7;
-  // the fragment rows r and r + 8 are query tokens t0 + r and t0 + r + 8
-  const bool row_a = r < rows, row_b = r + 8 < rows;
-  const int qpos_a = ctx + t0 + r, qpos_b = ctx + t0 + r + 8;
-  // A fragments per k-step: (row r, k c2), (row r+8, c2), (row r, c2+8), (row r+8, c2+8)
-  uint32_t qa[4][4];
-  {
-    const uint32_t *qra = reinterpret_cast<const uint32_t *>(
-        p.q + ((static_cast<size_t>(row0) + t0 + r) * kHq + h) * kD);
-    const uint32_t *qrb = reinterpret_cast<const uint32_t *>(
-        p.q + ((static_cast<size_t>(row0) + t0 + r + 8) * kHq + h) * kD);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[ks][0] = row_a ? __ldg(qra + (16 * ks + c2) / 2) : 0u;
-      qa[ks][1] = row_b ? __ldg(qrb + (16 * ks + c2) / 2) : 0u;
-      qa[ks][2] = row_a ? __ldg(qra + (16 * ks + 8 + c2) / 2) : 0u;
-      qa[ks][3] = row_b ? __ldg(qrb + (16 * ks + 8 + c2) / 2) : 0u;
-    }
-  }
-  float o[8][4];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m_a = p_neg_inf(), m_b = p_neg_inf(), l_a = 0.f, l_b = 0.f;
-  bool ok = true;
-  for (int j = 0; j < n_blocks; ++j) {
-    const int stage = j % kPStages;
-    const uint32_t phase = (j / kPStages) & 1;
-    if (!mbar_wait(&sm.full[stage], phase)) {
-      report(p.err, PA_DEV_TIMEOUT);
-      ok = false;
-      break;
-    }
-    if (sm.blk_of_stage[stage] >= 0) {
-      unsigned char *tile = sm.kv[stage];
-      const uint32_t ktile = smem_u32(tile);
-      const uint32_t vtile = ktile + kBs * kHeadRowBytes;
-      const int n_valid = min(kBs, last_pos + 1 - j * kBs);   // keys any row of the tile may see
-      if (n_valid < kBs) {
-        // slots past the tile's last position may hold anything (NaN
-        // included) and meet P = 0: every warp writes the same zeros over
-        // those V rows before it reads them
-        uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
-        for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const int tok = (lm_i >> 1) * 8 + lm_r;
-        const int chunk = 2 * ks + (lm_i & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16_16816(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-      }
-      // s0: keys j*16 + c2, +1 (rows r, r+8); s1: the same keys + 8
-      const int kp = j * kBs + c2;
-      const float ninf = p_neg_inf();
-      float xa0 = s0[0] * p.qscale, xa1 = s0[1] * p.qscale;
-      float xa2 = s1[0] * p.qscale, xa3 = s1[1] * p.qscale;
-      float xb0 = s0[2] * p.qscale, xb1 = s0[3] * p.qscale;
-      float xb2 = s1[2] * p.qscale, xb3 = s1[3] * p.qscale;
-      xa0 = (kp <= qpos_a) ? xa0 : ninf;
-      xa1 = (kp + 1 <= qpos_a) ? xa1 : ninf;
-      xa2 = (kp + 8 <= qpos_a) ? xa2 : ninf;
-      xa3 = (kp + 9 <= qpos_a) ? xa3 : ninf;
-      xb0 = (kp <= qpos_b) ? xb0 : ninf;
-      xb1 = (kp + 1 <= qpos_b) ? xb1 : ninf;
-      xb2 = (kp + 8 <= qpos_b) ? xb2 : ninf;
-      xb3 = (kp + 9 <= qpos_b) ? xb3 : ninf;
-      float mxa = fmaxf(fmaxf(xa0, xa1), fmaxf(xa2, xa3));
-      float mxb = fmaxf(fmaxf(xb0, xb1), fmaxf(xb2, xb3));
-      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-      // a row with no visible key so far (only after refused blocks) keeps
-      // an empty state: its scale and its exponent base stay finite
-      const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
-      const float ala = (mna == ninf) ? 1.f : p_exp2(m_a - mna);
-      const float alb = (mnb == ninf) ? 1.f : p_exp2(m_b - mnb);
-      const float sa = (mna == ninf) ? 0.f : mna, sb = (mnb == ninf) ? 0.f : mnb;
-      const uint32_t pa0 = float2_to_bf16x2(p_exp2(xa0 - sa), p_exp2(xa1 - sa));
-      const uint32_t pa2 = float2_to_bf16x2(p_exp2(xa2 - sa), p_exp2(xa3 - sa));
-      const uint32_t pb0 = float2_to_bf16x2(p_exp2(xb0 - sb), p_exp2(xb1 - sb));
-      const uint32_t pb2 = float2_to_bf16x2(p_exp2(xb2 - sb), p_exp2(xb3 - sb));
-      // l sums the probabilities as rounded for the P V product
-      const float2 fa0 = bf16x2_to_float2(pa0), fa2 = bf16x2_to_float2(pa2);
-      const float2 fb0 = bf16x2_to_float2(pb0), fb2 = bf16x2_to_float2(pb2);
-      l_a = fmaf(l_a, ala, (fa0.x + fa0.y) + (fa2.x + fa2.y));
-      l_b = fmaf(l_b, alb, (fb0.x + fb0.y) + (fb2.x + fb2.y));
-      m_a = mna;
-      m_b = mnb;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        o[t][0] *= ala;
-        o[t][1] *= ala;
-        o[t][2] *= alb;
-        o[t][3] *= alb;
-      }
-#pragma unroll
-      for (int dp = 0; dp < 4; ++dp) {
-        const int tok = (lm_i & 1) * 8 + lm_r;
-        const int chunk = 2 * dp + (lm_i >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * dp], pa0, pb0, pa2, pb2, v0, v1);
-        mma_bf16_16816(o[2 * dp + 1], pa0, pb0, pa2, pb2, v2, v3);
-      }
+          if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);
-  }
-  if (!ok) return;
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  // l == 0 only when every block the row sees was refused as out of range
-  if (row_a) {
-    const float inv = (l_a > 0.f) ? 1.f / l_a : 0.f;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(
-        p.out + ((static_cast<size_t>(row0) + t0 + r) * kHq + h) * kD);
+  } else if (warp == kMmaWarp) {
+    // ========================================================= MMA warp ==
+    if (lane == 0) {
+      const uint32_t id_s = tc::idesc_bf16(kRows, kChunk, false);
+      const uint32_t id_o = tc::idesc_bf16(kRows, kD, true);
+      const uint32_t q_addr = smem_u32(sm.q);
+      bool ok = mbar_wait(&sm.q_full, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStagesP;
+        if (!mbar_wait(&sm.kv_full[st], (j / kStagesP) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t k_addr = smem_u32(sm.k[st]);
+        const uint32_t d = tmem + (j & 1) * kChunk;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = float2_to_bf16x2(o[t][0] * inv, o[t][1] * inv);
-  }
-  if (row_b) {
-    const float inv = (l_b > 0.f) ? 1.f / l_b : 0.f;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(
-        p.out + ((static_cast<size_t>(row0) + t0 + r + 8) * kHq + h) * kD);
+        for (int ks = 0; ks < kD / 16; ++ks)
+          tc::mma_bf16(d, tc::sdesc_sw128(q_addr + 32 * ks, 16, 1024),
+                       tc::sdesc_sw128(k_addr + 32 * ks, 16, 1024), id_s, ks > 0);
+        tc::mma_commit(&sm.s_full[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_chunks > 1) ok = issue_s(1);
+      for (int j = 0; j < n_chunks && ok; ++j) {
+        const int st = j % kStagesP;
+        // the softmax has written P_j (and read S_j and O_{j-1})
+        if (!mbar_wait(&sm.p_full, j & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t v_addr = smem_u32(sm.v[st]);
 #pragma unroll
-    for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = float2_to_bf16x2(o[t][2] * inv, o[t][3] * inv);
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+          const uint32_t pa = smem_u32(sm.p[ks >> 2]) + 32 * (ks & 3);
+          tc::mma_bf16(tmem + kTmemO, tc::sdesc_sw128(pa, 16, 1024),
+                       tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o, ks > 0);
+        }
+        tc::mma_commit(&sm.o_full);
+        tc::mma_commit(&sm.kv_empty[st]);
+        if (j + 2 < n_chunks) ok = issue_s(j + 2);
+      }
+      if (!ok) report(p.err, PA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ==================================================== softmax warps ==
+    const int r = tid;                        // MMA row = TMEM lane
+    const int tok = r >> 2, hh = r & 3;
+    const int qpos = min(ctx + t0 + tok, last_pos);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float o[kD];
+#pragma unroll
+    for (int d = 0; d < kD; ++d) o[d] = 0.f;
+    float m = p_neg_inf(), l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+    for (int j = 0; j < n_chunks; ++j) {
+      const int st = j % kStagesP;
+      if (!mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1) ||
+          !mbar_wait(&sm.kv_full[st], (j / kStagesP) & 1)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const int pm = sm.pmask[st];
+      const int kbase = j * kChunk;
+      // every key of the chunk is visible to every row and was loaded
+      const bool full = pm == 0xff && kbase + kChunk - 1 <= ctx + t0;
+      const uint32_t s_addr = lane_addr + (j & 1) * kChunk;
+      // pass 1: the chunk's row maximum
+      float mx = p_neg_inf();
+#pragma unroll
+      for (int c0 = 0; c0 < kChunk; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(s_addr + c0, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int kp = kbase + c0 + c;
+          const bool vis = full || (kp <= qpos && ((pm >> ((c0 + c) >> 4)) & 1));
+          mx = vis ? fmaxf(mx, __uint_as_float(v[c]) * p.qscale) : mx;
+        }
+      }
+      const float m_new = fmaxf(m, mx);
+      const float alpha = (m_new == p_neg_inf()) ? 1.f : p_exp2(m - m_new);
+      const float base = (m_new == p_neg_inf()) ? 0.f : m_new;
+      // O_{j-1} into the registers (P_{j-1} has been consumed, P may be rewritten)
+      if (j > 0) {
+        if (!mbar_wait(&sm.o_full, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(lane_addr + kTmemO + c0, v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c0 + c] = fmaf(o[c0 + c], alpha_prev, __uint_as_float(v[c]));
+        }
+      }
+      // keys past the tile's last position, or in a page that was not
+      // loaded, meet P = 0 but their V rows may hold anything: zero them
+      {
+        const int key = r;   // this thread's V row of the stage
+        const int kp = kbase + key;
+        if (kp >= n_keys || !((pm >> (key >> 4)) & 1)) {
+          uint4 *vr = reinterpret_cast<uint4 *>(sm.v[st] + key * kTileRowBytes);
+#pragma unroll
+          for (int e = 0; e < kTileRowBytes / 16; ++e) vr[e] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // pass 2: P = exp2(s * qscale - m) in bf16; l sums the rounded values
+      float lsum = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < kChunk; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(s_addr + c0, v);
+        tc::tmem_ld_wait();
+        uint32_t packed[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int kp = kbase + c0 + c;
+          const bool vis0 = full || (kp <= qpos && ((pm >> ((c0 + c) >> 4)) & 1));
+          const bool vis1 = full || (kp + 1 <= qpos && ((pm >> ((c0 + c + 1) >> 4)) & 1));
+          const float e0 = vis0 ? p_exp2(fmaf(__uint_as_float(v[c]), p.qscale, -base)) : 0.f;
+          const float e1 = vis1 ? p_exp2(fmaf(__uint_as_float(v[c + 1]), p.qscale, -base)) : 0.f;
+          const uint32_t pk = float2_to_bf16x2(e0, e1);
+          const float2 back = bf16x2_to_float2(pk);
+          lsum += back.x + back.y;
+          packed[c >> 1] = pk;
+        }
+        // 32 keys = 4 chunks of 16 bytes, in region (c0 / 64), chunk c0 % 64 / 8 + i
+        unsigned char *region = sm.p[c0 >> 6] + r * kTileRowBytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = ((c0 & 63) >> 3) + i;
+          *reinterpret_cast<uint4 *>(region + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+      }
+      l = fmaf(l, alpha, lsum);
+      m = m_new;
+      alpha_prev = alpha;
+      fence_proxy_async_smem();   // P and the zeroed V rows, for the tensor core
+      tc::fence_before_sync();
+      mbar_arrive(&sm.p_full);
+    }
+    if (ok && n_chunks > 0) {
+      if (mbar_wait(&sm.o_full, (n_chunks - 1) & 1)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(lane_addr + kTmemO + c0, v);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c0 + c] = fmaf(o[c0 + c], alpha_prev, __uint_as_float(v[c]));
+        }
+        if (tok < rows) {
+          const float inv = (l > 0.f) ? 1.f / l : 0.f;
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              p.out + ((static_cast<size_t>(row0) + t0 + tok) * kHq + g * kGqa + hh) * kD);
+#pragma unroll
+          for (int e = 0; e < kD / 8; ++e)
+            dst[e] = make_uint4(float2_to_bf16x2(o[8 * e] * inv, o[8 * e + 1] * inv),
+                                float2_to_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
+                                float2_to_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv),
+                                float2_to_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) report(p.err, PA_DEV_TIMEOUT);
   }
+  // every TMEM read and MMA is done (or given up on) before the columns go back
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Tensor map over q [total_tokens][32][64] bf16: box (64, 4 heads, 32 tokens)
+// = one GQA group's rows of a query tile, 128-byte swizzle; rows past the
+// end read as zeros.
+int make_q_map(CUtensorMap *map, const void *q, int total_tokens) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return PA_ERR_CUDA;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  const cuuint64_t dims[3] = {kD, kHq, static_cast<cuuint64_t>(total_tokens)};
+  const cuuint64_t strides[2] = {kHeadRowBytes, static_cast<cuuint64_t>(kHq) * kHeadRowBytes};
+  const cuuint32_t box[3] = {kD, kGqa, kQTok};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult rr = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rr == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -367,21 +500,31 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
       return PA_ERR_CUDA;
     attr_done[di.device] = true;
   }
+  // the pool's map (one page's K or V rows per copy) changes with the pool,
+  // q's with q and the token count
   static thread_local const void *map_pool = nullptr;
   static thread_local int map_blocks = 0;
-  alignas(64) static thread_local CUtensorMap map;
+  alignas(64) static thread_local CUtensorMap kv_map;
   if (map_pool != kv_cache || map_blocks != num_blocks) {
-    rc = make_kv_map(&map, kv_cache, num_blocks);
+    rc = make_kv_rows_map(&kv_map, kv_cache, num_blocks);
     if (rc != PA_OK) return rc;
     map_pool = kv_cache;
     map_blocks = num_blocks;
   }
+  static thread_local const void *map_q = nullptr;
+  static thread_local int map_q_tokens = 0;
+  alignas(64) static thread_local CUtensorMap q_map;
+  if (map_q != q || map_q_tokens != total_tokens) {
+    rc = make_q_map(&q_map, q, total_tokens);
+    if (rc != PA_OK) return rc;
+    map_q = q;
+    map_q_tokens = total_tokens;
+  }
   // every sequence's chunk ends in at most one partial tile
-  const long long tiles = (static_cast<long long>(total_tokens) + kQTile - 1) / kQTile + num_seqs;
+  const long long tiles = (static_cast<long long>(total_tokens) + kQTok - 1) / kQTok + num_seqs;
   if (tiles > INT_MAX) return PA_ERR_ARG;
   PrefillParams prm;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
-  prm.q = q;
   prm.cu_tokens = cu_tokens;
   prm.block_table = block_table;
   prm.context_lens = context_lens;
@@ -394,7 +537,7 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   prm.total_tokens = total_tokens;
   prm.qscale = scale * kLog2eP;
   if (launch_pdl(prefill_attention_kernel, dim3(static_cast<unsigned>(tiles), kHkv),
-                 dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), map, prm) !=
+                 dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
