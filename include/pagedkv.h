@@ -244,7 +244,8 @@ int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new, uint16_
  * block_table[s][layer][t / 16], slot t % 16, kv head h / 4.  The chunk's own
  * K/V must already be in the cache (pa_prefill_append_rope before this call
  * on the same stream).  fp32 accumulation, output rounded to bf16.
- * num_seqs is at most 2048 per call; no workspace.
+ * num_seqs is at most 2048 per call; scale must be positive and finite
+ * (PA_ERR_ARG otherwise); no workspace.
  * Device errors: PA_DEV_CTX_RANGE (a chunk that does not fit its table, or
  * rows outside [0, total_tokens): its rows are not written),
  * PA_DEV_BAD_BLOCK (that block's tokens are dropped), PA_DEV_TIMEOUT.

@@ -86,6 +86,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// The same for hand-offs expected within microseconds: try_wait without a
+// suspend-time hint (the hardware's own short wait), so the waiter resumes as
+// soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_short(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_short(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait_short(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_short(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ------------------------------------------------- bulk async copy (TMA)
 // Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) whose completion is counted as transaction bytes on `bar`.

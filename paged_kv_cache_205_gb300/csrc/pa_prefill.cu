@@ -11,23 +11,27 @@
 // context_lens[s] + i and attends over positions 0..context_lens[s] + i of its
 // sequence, whose K/V (the chunk's own included) are already in the cache.
 //
-// One CTA per (32-token query tile, kv head): its 128 MMA rows are the 32
-// tokens x the 4 q heads of the GQA group (row = 4 * token + head), so every
-// K/V byte brought into shared memory serves 128 query rows.  Keys go in
-// chunks of 128 (8 pages).  Warp roles (192 threads):
-//   warp 4      producer: the Q tile (one TMA), then per chunk 16 TMA copies
+// One CTA per (64-token query tile, kv head), in two halves of 32 tokens:
+// each half's 128 MMA rows are its 32 tokens x the 4 q heads of the GQA group
+// (row = 4 * token + head), so every K/V byte brought into shared memory
+// serves 256 query rows.  Keys go in chunks of 128 (8 pages).  Warp roles
+// (320 threads):
+//   warp 8      producer: the two Q tiles (TMA), then per chunk 16 TMA copies
 //               (K rows and V rows of 8 pages) into a 3-stage ring;
-//   warp 5      one thread issues the MMAs: S_j = Q K_j^T (M 128, N 128, 4
-//               k-steps) into one of two TMEM buffers, and, once the
+//   warp 9      MMA warp: zeroes the V rows of a chunk that lie past the
+//               tile's last key or in a page that was not loaded, then one
+//               thread issues, per half, S_j = Q K_j^T (M 128, N 128, 4
+//               k-steps) into the half's TMEM S columns and, once the half's
 //               softmax has written P_j, O_j = P_j V_j (M 128, N 64, 8
-//               k-steps, V read as an MN-major operand) into a third;
-//   warps 0-3   softmax, one thread per row (TMEM lane): S_j from TMEM,
-//               causal mask, running max and sum in fp32 (log2 domain), P_j
-//               rounded to bf16 into shared memory (128-byte swizzle, the
-//               layout the MMA reads), the previous chunk's O_j folded into
-//               registers with the max correction, and the output row at the
-//               end.
-// S_{j+1} is computed while the softmax works on S_j.
+//               k-steps, V read as an MN-major operand) into its O columns;
+//   warps 0-3, 4-7   softmax of half 0 / half 1, one thread per row (TMEM
+//               lane): S_j from TMEM in one round trip, causal mask, row
+//               maximum and sum in fp32 (log2 domain), P_j rounded to bf16
+//               into shared memory (128-byte swizzle, the layout the MMA
+//               reads); O accumulates in TMEM and is rescaled only when the
+//               row maximum grows by more than 2^8; the output row at the end.
+// The tensor core alternates between the halves: one half's MMAs run while
+// the other half's softmax works.
 #include <climits>
 #include <cudaTypedefs.h>
 
@@ -38,18 +42,29 @@
 namespace pa {
 namespace {
 
-constexpr int kQTok = 32;                     // query tokens per CTA
-constexpr int kRows = kQTok * kGqa;           // 128 MMA rows
+constexpr int kQTok = 32;                     // query tokens per half
+constexpr int kHalves = 2;
+constexpr int kCtaTok = kQTok * kHalves;      // query tokens per CTA
+constexpr int kRows = kQTok * kGqa;           // 128 MMA rows per half
 constexpr int kChunk = 128;                   // keys per chunk
 constexpr int kPagesPerChunk = kChunk / kBs;  // 8
 constexpr int kStagesP = 3;
-constexpr int kSoftWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kPThreads = 6 * 32;
+constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kPThreads = 12 * 32;            // 3 warpgroups; warps 10-11 only rebalance registers
+// Register budget: 384 threads x 168 at launch = 64,512.  The producer/MMA
+// warpgroup gives up to 56 and each softmax warpgroup takes 224:
+// 2 x 128 x 224 + 128 x 56 = 64,512 (every SM sub-partition: 2 x 224 + 56
+// registers per lane, within its 512).
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoft = 224;
+constexpr int kRegsOther = 56;
+static_assert(2 * 128 * kRegsSoft + 128 * kRegsOther <= kPThreads * kRegsLaunch,
+              "register split above the launch budget");
 constexpr int kTileRowBytes = kHeadRowBytes;             // 128-byte rows
 constexpr int kOperandBytes = kChunk * kTileRowBytes;    // 16 KiB: 128 rows x 64 bf16
-constexpr uint32_t kTmemCols = 512;                      // S x2 (256) + O (64), rounded up
+constexpr uint32_t kTmemCols = 512;                      // S x2 (256) + O x2 (128), rounded up
 constexpr uint32_t kTmemO = 256;
 constexpr int kMaxSeqsP = 2048;
 constexpr float kLog2eP = 1.4426950408889634f;
@@ -70,17 +85,17 @@ struct PrefillParams {
 };
 
 struct __align__(1024) PSmem {
-  unsigned char q[kOperandBytes];                  // [32 tok][4 heads][64], swizzled
+  unsigned char q[kHalves][kOperandBytes];         // per half [32 tok][4 heads][64], swizzled
   unsigned char k[kStagesP][kOperandBytes];        // [128 keys][64]
   unsigned char v[kStagesP][kOperandBytes];        // [128 keys][64]
-  unsigned char p[2][kOperandBytes];               // P: keys 0-63, 64-127, [128 rows][64]
+  unsigned char p[kHalves][2][kOperandBytes];      // per half, P: keys 0-63, 64-127
   int tile_prefix[kMaxSeqsP + 1];
   uint64_t q_full;
   uint64_t kv_full[kStagesP];
   uint64_t kv_empty[kStagesP];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_full;
+  uint64_t s_full[kHalves];
+  uint64_t p_full[kHalves];
+  uint64_t o_full[kHalves];
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
@@ -104,6 +119,56 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// MMA warp: chunk c has landed.  Its V rows past the CTA's last key, or in a
+// page that was not loaded, meet P = 0 but may hold anything (NaN
+// included): the warp zeroes them before any MMA reads the stage.
+__device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int c, int n_keys, int lane) {
+  const int st = c % kStagesP;
+  int good = 1;
+  if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (c / kStagesP) & 1) ? 1 : 0;
+  good = __shfl_sync(0xffffffffu, good, 0);
+  if (!good) return false;
+  __syncwarp();
+  const int pm = sm.pmask[st];
+  const int kbase = c * kChunk;
+  if (pm != 0xff || kbase + kChunk > n_keys) {
+    for (int e = lane; e < kChunk * (kTileRowBytes / 16); e += 32) {
+      const int key = e >> 3;
+      if (kbase + key >= n_keys || !((pm >> (key >> 4)) & 1))
+        reinterpret_cast<uint4 *>(sm.v[st])[e] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  return true;
+}
+
+// S_c of half h = Q_h K_c^T into the half's S columns (one thread).
+__device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int c,
+                                            uint32_t id_s) {
+  const uint32_t k_addr = smem_u32(sm.k[c % kStagesP]);
+  const uint32_t q_addr = smem_u32(sm.q[h]);
+#pragma unroll
+  for (int ks = 0; ks < kD / 16; ++ks)
+    tc::mma_bf16(tmem + h * kChunk, tc::sdesc_sw128(q_addr + 32 * ks, 16, 1024),
+                 tc::sdesc_sw128(k_addr + 32 * ks, 16, 1024), id_s, ks > 0);
+  tc::mma_commit(&sm.s_full[h]);
+}
+
+// O of half h += P_h V_c in the half's O columns (one thread); chunk 0
+// starts the sum.
+__device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, int c,
+                                             uint32_t id_o) {
+  const uint32_t v_addr = smem_u32(sm.v[c % kStagesP]);
+#pragma unroll
+  for (int ks = 0; ks < kChunk / 16; ++ks) {
+    const uint32_t pa = smem_u32(sm.p[h][ks >> 2]) + 32 * (ks & 3);
+    tc::mma_bf16(tmem + kTmemO + h * kD, tc::sdesc_sw128(pa, 16, 1024),
+                 tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o, (c > 0 || ks > 0) ? 1u : 0u);
+  }
+  tc::mma_commit(&sm.o_full[h]);
+}
+
 __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
     PrefillParams p) {
@@ -120,10 +185,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.kv_full[st], 1);
       mbar_init(&sm.kv_empty[st], 1);
     }
-    mbar_init(&sm.s_full[0], 1);
-    mbar_init(&sm.s_full[1], 1);
-    mbar_init(&sm.p_full, kSoftWarps * 32);
-    mbar_init(&sm.o_full, 1);
+    for (int h = 0; h < kHalves; ++h) {
+      mbar_init(&sm.s_full[h], 1);
+      mbar_init(&sm.p_full[h], kSoftThreads);
+      mbar_init(&sm.o_full[h], 1);
+    }
     fence_mbar_init();
   }
   pdl_launch_dependents();
@@ -142,7 +208,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       // a chunk that does not fit its table, or rows outside [0, total_tokens), is refused
       if (ctx >= 0 && n >= 0 && c0 >= 0 && c1 <= p.total_tokens &&
           static_cast<long long>(ctx) + n <= cap)
-        tiles = (n + kQTok - 1) / kQTok;
+        tiles = (n + kCtaTok - 1) / kCtaTok;
       else if (blockIdx.x == 0 && blockIdx.y == 0)
         report(p.err, PA_DEV_CTX_RANGE);
     }
@@ -178,7 +244,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         else hi = mid - 1;
       }
       sm.seq = lo;
-      sm.t0 = (t - sm.tile_prefix[lo]) * kQTok;
+      sm.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
       sm.valid = 1;
     }
   }
@@ -189,10 +255,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   const int ctx = p.context_lens[s];
   const int row0 = p.cu_tokens[s];
   const int n = p.cu_tokens[s + 1] - row0;
-  const int rows = min(kQTok, n - t0);                  // real query tokens of the tile
-  const int last_pos = ctx + t0 + rows - 1;             // the tile's last query position
-  const int n_keys = last_pos + 1;
+  // half h holds tokens t0 + 32h .. t0 + 32h + rows_h - 1 (rows_h <= 0: no work)
+  const int rows0 = min(kQTok, n - t0);
+  const int rows1 = min(kQTok, n - t0 - kQTok);
+  const int halves = rows1 > 0 ? 2 : 1;
+  const int n_keys0 = ctx + t0 + rows0;                        // half 0 sees keys < n_keys0
+  const int n_keys1 = ctx + t0 + kQTok + max(rows1, 0);
+  const int n_keys = halves == 2 ? n_keys1 : n_keys0;         // the CTA's keys
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
+  const int nc0 = (n_keys0 + kChunk - 1) / kChunk;
+  const int nc1 = halves == 2 ? n_chunks : 0;
 
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -202,232 +274,222 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-
-  if (warp == kProducerWarp) {
-    // ===================================================== producer warp ==
-    const int32_t *row =
-        p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sm.q_full, kOperandBytes);
-      tma_load_3d(sm.q, &q_map, 0, g * kGqa, row0 + t0, &sm.q_full);
-    }
-    bool ok = true;
-    uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
-    for (int j = 0; j < n_chunks && ok; ++j) {
-      const int st = j % kStagesP;
-      const uint32_t ph = (j / kStagesP) & 1;
-      // lane l < 8 looks up page j * 8 + l
-      const int pg = j * kPagesPerChunk + (lane & 7);
-      int blk = -1;
-      const bool needed = lane < kPagesPerChunk && pg * kBs < n_keys;
-      if (needed) blk = row[pg];
-      const bool valid = needed && blk >= 0 && blk < p.num_blocks;
-      const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
-      const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
-      int good = 1;
+  if (warp >= 8) {
+    // the producer/MMA warpgroup gives registers to the softmax warpgroups
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+    if (warp == kProducerWarp) {
+      // ===================================================== producer warp ==
+      const int32_t *row =
+          p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
       if (lane == 0) {
-        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
-          good = 0;
-        } else {
-          if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
-          sm.pmask[st] = static_cast<int>(vm);
-          mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
-          issued |= 1u << st;
-          issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
-        }
+        mbar_arrive_expect_tx(&sm.q_full, halves * kOperandBytes);
+        for (int h = 0; h < halves; ++h)
+          tma_load_3d(sm.q[h], &q_map, 0, g * kGqa, row0 + t0 + h * kQTok, &sm.q_full);
       }
-      good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) {
-        ok = false;
-        break;
-      }
-      __syncwarp();
-      // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
-      const int pl = lane & 7, kv = (lane >> 3) & 1;
-      const int pblk = __shfl_sync(0xffffffffu, blk, pl);
-      if (lane < 16 && ((vm >> pl) & 1u)) {
-        unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
-        tma_load_5d(dst, &kv_map, 0, g, 0, kv, pblk, &sm.kv_full[st]);
-      }
-    }
-    if (lane == 0) {
-      if (!ok) report(p.err, PA_DEV_TIMEOUT);
-      // no copy may still be landing in shared memory when the CTA exits
-      if (!mbar_wait(&sm.q_full, 0)) report(p.err, PA_DEV_TIMEOUT);
-      for (int st = 0; st < kStagesP; ++st)
-        if ((issued >> st) & 1u)
-          if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ========================================================= MMA warp ==
-    if (lane == 0) {
-      const uint32_t id_s = tc::idesc_bf16(kRows, kChunk, false);
-      const uint32_t id_o = tc::idesc_bf16(kRows, kD, true);
-      const uint32_t q_addr = smem_u32(sm.q);
-      bool ok = mbar_wait(&sm.q_full, 0);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kStagesP;
-        if (!mbar_wait(&sm.kv_full[st], (j / kStagesP) & 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t k_addr = smem_u32(sm.k[st]);
-        const uint32_t d = tmem + (j & 1) * kChunk;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-          tc::mma_bf16(d, tc::sdesc_sw128(q_addr + 32 * ks, 16, 1024),
-                       tc::sdesc_sw128(k_addr + 32 * ks, 16, 1024), id_s, ks > 0);
-        tc::mma_commit(&sm.s_full[j & 1]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_chunks > 1) ok = issue_s(1);
+      bool ok = true;
+      uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
       for (int j = 0; j < n_chunks && ok; ++j) {
         const int st = j % kStagesP;
-        // the softmax has written P_j (and read S_j and O_{j-1})
-        if (!mbar_wait(&sm.p_full, j & 1)) {
+        const uint32_t ph = (j / kStagesP) & 1;
+        // lane l < 8 looks up page j * 8 + l
+        const int pg = j * kPagesPerChunk + (lane & 7);
+        int blk = -1;
+        const bool needed = lane < kPagesPerChunk && pg * kBs < n_keys;
+        if (needed) blk = row[pg];
+        const bool valid = needed && blk >= 0 && blk < p.num_blocks;
+        const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
+        const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
+        int good = 1;
+        if (lane == 0) {
+          if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
+            good = 0;
+          } else {
+            if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
+            sm.pmask[st] = static_cast<int>(vm);
+            mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
+            issued |= 1u << st;
+            issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(sm.v[st]);
-#pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-          const uint32_t pa = smem_u32(sm.p[ks >> 2]) + 32 * (ks & 3);
-          tc::mma_bf16(tmem + kTmemO, tc::sdesc_sw128(pa, 16, 1024),
-                       tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o, ks > 0);
+        __syncwarp();
+        // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
+        const int pl = lane & 7, kv = (lane >> 3) & 1;
+        const int pblk = __shfl_sync(0xffffffffu, blk, pl);
+        if (lane < 16 && ((vm >> pl) & 1u)) {
+          unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
+          tma_load_5d(dst, &kv_map, 0, g, 0, kv, pblk, &sm.kv_full[st]);
         }
-        tc::mma_commit(&sm.o_full);
-        tc::mma_commit(&sm.kv_empty[st]);
-        if (j + 2 < n_chunks) ok = issue_s(j + 2);
       }
-      if (!ok) report(p.err, PA_DEV_TIMEOUT);
+      if (lane == 0) {
+        if (!ok) report(p.err, PA_DEV_TIMEOUT);
+        // no copy may still be landing in shared memory when the CTA exits
+        if (!mbar_wait(&sm.q_full, 0)) report(p.err, PA_DEV_TIMEOUT);
+        for (int st = 0; st < kStagesP; ++st)
+          if ((issued >> st) & 1u)
+            if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ========================================================= MMA warp ==
+      const uint32_t id_s = tc::idesc_bf16(kRows, kChunk, false);
+      const uint32_t id_o = tc::idesc_bf16(kRows, kD, true);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sm.q_full, 0) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok && n_chunks > 0) ok = mma_prepare_chunk(sm, 0, n_keys, lane);
+      if (ok && lane == 0) {
+        tc::fence_after_sync();
+        mma_issue_s(sm, tmem, 0, 0, id_s);
+        if (halves == 2) mma_issue_s(sm, tmem, 1, 0, id_s);
+      }
+      for (int j = 0; j < n_chunks && ok; ++j) {
+        if (j + 1 < n_chunks && !mma_prepare_chunk(sm, j + 1, n_keys, lane)) {
+          ok = 0;
+          break;
+        }
+        for (int h = 0; h < halves && ok; ++h) {
+          const int nch = h == 0 ? nc0 : nc1;
+          if (j >= nch) continue;
+          int good = 1;
+          if (lane == 0) {
+            // the half's softmax has written P_j (and read S_j and O_{j-1})
+            if (!mbar_wait_short(&sm.p_full[h], j & 1)) {
+              good = 0;
+            } else {
+              tc::fence_after_sync();
+              mma_issue_pv(sm, tmem, h, j, id_o);
+              if (j + 1 < nch) mma_issue_s(sm, tmem, h, j + 1, id_s);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, good, 0);
+        }
+        if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[j % kStagesP]);
+        __syncwarp();
+      }
+      if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
     // ==================================================== softmax warps ==
-    const int r = tid;                        // MMA row = TMEM lane
+    // O accumulates in TMEM.  Each row keeps the reference maximum m its
+    // P values are taken against; it moves (and O, l are rescaled) only
+    // when a chunk's maximum exceeds it by more than kRescale (log2 units),
+    // so P stays below 2^kRescale and most chunks touch O not at all.
+    // S_j's commit comes after PV_{j-1}'s, so once S_j is there O and P
+    // are free.
+    constexpr float kRescale = 8.f;
+    const int h = tid >> 7;                   // half
+    const int r = tid & (kRows - 1);          // MMA row = TMEM lane
     const int tok = r >> 2, hh = r & 3;
-    const int qpos = min(ctx + t0 + tok, last_pos);
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float o[kD];
-#pragma unroll
-    for (int d = 0; d < kD; ++d) o[d] = 0.f;
-    float m = p_neg_inf(), l = 0.f, alpha_prev = 1.f;
+    const int rows = h == 0 ? rows0 : rows1;
+    const int nch = h == 0 ? nc0 : nc1;
+    const int first_pos = ctx + t0 + h * kQTok;           // the half's first query position
+    const int last_pos = first_pos + max(rows, 1) - 1;
+    const int qpos = min(first_pos + tok, last_pos);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_addr + h * kChunk, o_addr = lane_addr + kTmemO + h * kD;
+    float m = p_neg_inf(), l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_chunks; ++j) {
+    for (int j = 0; j < nch; ++j) {
       const int st = j % kStagesP;
-      if (!mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1) ||
-          !mbar_wait(&sm.kv_full[st], (j / kStagesP) & 1)) {
+      if (!mbar_wait_short(&sm.s_full[h], j & 1) ||
+          !mbar_wait_short(&sm.kv_full[st], (j / kStagesP) & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
       const int pm = sm.pmask[st];
       const int kbase = j * kChunk;
-      // every key of the chunk is visible to every row and was loaded
-      const bool full = pm == 0xff && kbase + kChunk - 1 <= ctx + t0;
-      const uint32_t s_addr = lane_addr + (j & 1) * kChunk;
-      // pass 1: the chunk's row maximum
-      float mx = p_neg_inf();
+      // every key of the chunk is visible to every row of the half and was loaded
+      const bool full = pm == 0xff && kbase + kChunk - 1 <= first_pos;
+      const int lim = qpos - kbase;           // keys c <= lim are at or before the row
+      uint32_t v[kChunk];
 #pragma unroll
-      for (int c0 = 0; c0 < kChunk; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(s_addr + c0, v);
-        tc::tmem_ld_wait();
+      for (int c0 = 0; c0 < kChunk; c0 += 32)
+        tc::tmem_ld32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
+      tc::tmem_ld_wait();
+      if (!full) {
+        // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int kp = kbase + c0 + c;
-          const bool vis = full || (kp <= qpos && ((pm >> ((c0 + c) >> 4)) & 1));
-          mx = vis ? fmaxf(mx, __uint_as_float(v[c]) * p.qscale) : mx;
-        }
+        for (int c = 0; c < kChunk; ++c)
+          if (!((c <= lim) && ((pm >> (c >> 4)) & 1))) v[c] = 0xff800000u;
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = (m_new == p_neg_inf()) ? 1.f : p_exp2(m - m_new);
-      const float base = (m_new == p_neg_inf()) ? 0.f : m_new;
-      // O_{j-1} into the registers (P_{j-1} has been consumed, P may be rewritten)
-      if (j > 0) {
-        if (!mbar_wait(&sm.o_full, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
+      float mx8[8];
 #pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = p_neg_inf();
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+      const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.qscale;
+      const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
+      if (__any_sync(0xffffffffu, move) && j > 0) {
+        // rescale O (the whole warp takes part in the TMEM round trip)
+        const float alpha = move ? p_exp2(m - mc) : 1.f;
+#pragma unroll 1
         for (int c0 = 0; c0 < kD; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(lane_addr + kTmemO + c0, v);
+          uint32_t ov[32];
+          tc::tmem_ld32(o_addr + c0, ov);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c0 + c] = fmaf(o[c0 + c], alpha_prev, __uint_as_float(v[c]));
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tc::tmem_st32(o_addr + c0, ov);
         }
+        tc::tmem_st_wait();
+        l *= alpha;
       }
-      // keys past the tile's last position, or in a page that was not
-      // loaded, meet P = 0 but their V rows may hold anything: zero them
-      {
-        const int key = r;   // this thread's V row of the stage
-        const int kp = kbase + key;
-        if (kp >= n_keys || !((pm >> (key >> 4)) & 1)) {
-          uint4 *vr = reinterpret_cast<uint4 *>(sm.v[st] + key * kTileRowBytes);
+      if (move) m = mc;
+      const float base = (m == p_neg_inf()) ? 0.f : m;
+      const float2 qs2 = make_float2(p.qscale, p.qscale), nb2 = make_float2(-base, -base);
+      // P = exp2(s * qscale - m) in bf16, stored swizzled; 4 partial sums
+      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int e = 0; e < kTileRowBytes / 16; ++e) vr[e] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // pass 2: P = exp2(s * qscale - m) in bf16; l sums the rounded values
-      float lsum = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < kChunk; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(s_addr + c0, v);
-        tc::tmem_ld_wait();
-        uint32_t packed[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int kp = kbase + c0 + c;
-          const bool vis0 = full || (kp <= qpos && ((pm >> ((c0 + c) >> 4)) & 1));
-          const bool vis1 = full || (kp + 1 <= qpos && ((pm >> ((c0 + c + 1) >> 4)) & 1));
-          const float e0 = vis0 ? p_exp2(fmaf(__uint_as_float(v[c]), p.qscale, -base)) : 0.f;
-          const float e1 = vis1 ? p_exp2(fmaf(__uint_as_float(v[c + 1]), p.qscale, -base)) : 0.f;
-          const uint32_t pk = float2_to_bf16x2(e0, e1);
-          const float2 back = bf16x2_to_float2(pk);
-          lsum += back.x + back.y;
-          packed[c >> 1] = pk;
-        }
-        // 32 keys = 4 chunks of 16 bytes, in region (c0 / 64), chunk c0 % 64 / 8 + i
-        unsigned char *region = sm.p[c0 >> 6] + r * kTileRowBytes;
+      for (int ch = 0; ch < kChunk / 8; ++ch) {
+        uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int ch = ((c0 & 63) >> 3) + i;
-          *reinterpret_cast<uint4 *>(region + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          const int c = 8 * ch + 2 * i;
+          const float2 x = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                qs2, nb2);
+          const float e0 = p_exp2(x.x), e1 = p_exp2(x.y);
+          ls[i] = make_float2(ls[i].x + e0, ls[i].y + e1);
+          pk[i] = float2_to_bf16x2(e0, e1);
         }
+        unsigned char *region = sm.p[h][ch >> 3] + r * kTileRowBytes;
+        *reinterpret_cast<uint4 *>(region + (((ch & 7) ^ (r & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l = fmaf(l, alpha, lsum);
-      m = m_new;
-      alpha_prev = alpha;
-      fence_proxy_async_smem();   // P and the zeroed V rows, for the tensor core
+      l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+      fence_proxy_async_smem();   // P, for the tensor core
       tc::fence_before_sync();
-      mbar_arrive(&sm.p_full);
+      mbar_arrive(&sm.p_full[h]);
     }
-    if (ok && n_chunks > 0) {
-      if (mbar_wait(&sm.o_full, (n_chunks - 1) & 1)) {
+    if (ok && nch > 0) {
+      if (mbar_wait_short(&sm.o_full[h], (nch - 1) & 1)) {
         tc::fence_after_sync();
-#pragma unroll
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(lane_addr + kTmemO + c0, v);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c0 + c] = fmaf(o[c0 + c], alpha_prev, __uint_as_float(v[c]));
-        }
+        uint32_t ov[kD];
+        tc::tmem_ld32(o_addr, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+        tc::tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+        tc::tmem_ld_wait();
         if (tok < rows) {
           const float inv = (l > 0.f) ? 1.f / l : 0.f;
           uint4 *dst = reinterpret_cast<uint4 *>(
-              p.out + ((static_cast<size_t>(row0) + t0 + tok) * kHq + g * kGqa + hh) * kD);
+              p.out + ((static_cast<size_t>(row0) + t0 + h * kQTok + tok) * kHq + g * kGqa + hh) *
+                          kD);
 #pragma unroll
-          for (int e = 0; e < kD / 8; ++e)
-            dst[e] = make_uint4(float2_to_bf16x2(o[8 * e] * inv, o[8 * e + 1] * inv),
-                                float2_to_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
-                                float2_to_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv),
-                                float2_to_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
+          for (int e = 0; e < kD / 8; ++e) {
+            const float *f = reinterpret_cast<const float *>(&ov[8 * e]);
+            dst[e] = make_uint4(float2_to_bf16x2(f[0] * inv, f[1] * inv),
+                                float2_to_bf16x2(f[2] * inv, f[3] * inv),
+                                float2_to_bf16x2(f[4] * inv, f[5] * inv),
+                                float2_to_bf16x2(f[6] * inv, f[7] * inv));
+          }
         }
       } else {
         ok = false;
@@ -445,7 +507,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
 }
 
 // Tensor map over q [total_tokens][32][64] bf16: box (64, 4 heads, 32 tokens)
-// = one GQA group's rows of a query tile, 128-byte swizzle; rows past the
+// = one GQA group's rows of a half tile, 128-byte swizzle; rows past the
 // end read as zeros.
 int make_q_map(CUtensorMap *map, const void *q, int total_tokens) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -488,6 +550,7 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   if (!out || !q || !cu_tokens || !kv_cache || !block_table || !context_lens || !err)
     return PA_ERR_NULL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(kv_cache)) return PA_ERR_ALIGN;
+  if (!(scale > 0.f) || scale > 3.0e38f) return PA_ERR_ARG;   // the row maximum is taken before scaling
   DeviceInfo di;
   int rc = current_device(&di);
   if (rc != PA_OK) return rc;
@@ -521,7 +584,7 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
     map_q_tokens = total_tokens;
   }
   // every sequence's chunk ends in at most one partial tile
-  const long long tiles = (static_cast<long long>(total_tokens) + kQTok - 1) / kQTok + num_seqs;
+  const long long tiles = (static_cast<long long>(total_tokens) + kCtaTok - 1) / kCtaTok + num_seqs;
   if (tiles > INT_MAX) return PA_ERR_ARG;
   PrefillParams prm;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
