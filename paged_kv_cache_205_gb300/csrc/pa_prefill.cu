@@ -11,7 +11,8 @@
 // context_lens[s] + i and attends over positions 0..context_lens[s] + i of its
 // sequence, whose K/V (the chunk's own included) are already in the cache.
 //
-// One CTA per (64-token query tile, kv head), in two halves of 32 tokens:
+// Persistent CTAs (one per SM) work through (64-token query tile, kv head)
+// items, each tile in two halves of 32 tokens:
 // each half's 128 MMA rows are its 32 tokens x the 4 q heads of the GQA group
 // (row = 4 * token + head), so every K/V byte brought into shared memory
 // serves 256 query rows.  Keys go in chunks of 128 (8 pages).  Warp roles
@@ -54,12 +55,12 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPThreads = 12 * 32;            // 3 warpgroups; warps 10-11 only rebalance registers
 // Register budget: 384 threads x 168 at launch = 64,512.  The producer/MMA
-// warpgroup gives up to 56 and each softmax warpgroup takes 224:
-// 2 x 128 x 224 + 128 x 56 = 64,512 (every SM sub-partition: 2 x 224 + 56
+// warpgroup gives up to 80 and each softmax warpgroup takes 200:
+// 2 x 128 x 200 + 128 x 80 = 61,440 (every SM sub-partition: 2 x 200 + 80
 // registers per lane, within its 512).
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsSoft = 224;
-constexpr int kRegsOther = 56;
+constexpr int kRegsSoft = 200;
+constexpr int kRegsOther = 80;
 static_assert(2 * 128 * kRegsSoft + 128 * kRegsOther <= kPThreads * kRegsLaunch,
               "register split above the launch budget");
 constexpr int kTileRowBytes = kHeadRowBytes;             // 128-byte rows
@@ -91,15 +92,16 @@ struct __align__(1024) PSmem {
   unsigned char p[kHalves][2][kOperandBytes];      // per half, P: keys 0-63, 64-127
   int tile_prefix[kMaxSeqsP + 1];
   uint64_t q_full;
+  uint64_t q_empty;
   uint64_t kv_full[kStagesP];
   uint64_t kv_empty[kStagesP];
   uint64_t s_full[kHalves];
   uint64_t p_full[kHalves];
   uint64_t o_full[kHalves];
+  uint64_t o_free[kHalves];
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
-  int seq, t0, valid;
 };
 
 __device__ __forceinline__ float p_neg_inf() { return -__int_as_float(0x7f800000); }
@@ -119,18 +121,60 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
-// MMA warp: chunk c has landed.  Its V rows past the CTA's last key, or in a
+// A work item is (64-token query tile, kv head).  Items go heavy first (the
+// last tiles of a sequence see the most keys); CTA b takes items b, b + G,
+// b + 2G, ... of that order and keeps its pipeline running from one item into
+// the next.
+struct Item {
+  int g;                    // kv head
+  int ctx, row0, t0;        // the tile's sequence: cached tokens, first row; tile start
+  int rows0, rows1;         // query tokens of half 0 / half 1 (<= 0: no work)
+  int halves;
+  int n_keys0, n_keys;      // keys half 0 / the whole tile sees
+  int n_chunks, nc0, nc1;   // 128-key chunks: the tile's, half 0's, half 1's
+  int s;
+};
+
+__device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams &p,
+                                            int total_tiles, int i) {
+  Item it;
+  const int t = total_tiles - 1 - i / kHkv;
+  it.g = i % kHkv;
+  int lo = 0, hi = p.num_seqs - 1;   // the sequence s with prefix[s] <= t < prefix[s+1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sm.tile_prefix[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  it.s = lo;
+  it.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
+  it.ctx = p.context_lens[lo];
+  it.row0 = p.cu_tokens[lo];
+  const int n = p.cu_tokens[lo + 1] - it.row0;
+  it.rows0 = min(kQTok, n - it.t0);
+  it.rows1 = min(kQTok, n - it.t0 - kQTok);
+  it.halves = it.rows1 > 0 ? 2 : 1;
+  it.n_keys0 = it.ctx + it.t0 + it.rows0;
+  it.n_keys = it.halves == 2 ? it.ctx + it.t0 + kQTok + it.rows1 : it.n_keys0;
+  it.n_chunks = (it.n_keys + kChunk - 1) / kChunk;
+  it.nc0 = (it.n_keys0 + kChunk - 1) / kChunk;
+  it.nc1 = it.halves == 2 ? it.n_chunks : 0;
+  return it;
+}
+
+// MMA warp: chunk gc (counted over the CTA's items) has landed; kbase is its
+// first key within its item.  Its V rows past the tile's last key, or in a
 // page that was not loaded, meet P = 0 but may hold anything (NaN
 // included): the warp zeroes them before any MMA reads the stage.
-__device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int c, int n_keys, int lane) {
-  const int st = c % kStagesP;
+__device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, int n_keys,
+                                                  int lane) {
+  const int st = gc % kStagesP;
   int good = 1;
-  if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (c / kStagesP) & 1) ? 1 : 0;
+  if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (gc / kStagesP) & 1) ? 1 : 0;
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   __syncwarp();
   const int pm = sm.pmask[st];
-  const int kbase = c * kChunk;
   if (pm != 0xff || kbase + kChunk > n_keys) {
     for (int e = lane; e < kChunk * (kTileRowBytes / 16); e += 32) {
       const int key = e >> 3;
@@ -143,10 +187,10 @@ __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int c, int n_keys, 
   return true;
 }
 
-// S_c of half h = Q_h K_c^T into the half's S columns (one thread).
-__device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int c,
+// S of half h = Q_h K^T for chunk gc into the half's S columns (one thread).
+__device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int gc,
                                             uint32_t id_s) {
-  const uint32_t k_addr = smem_u32(sm.k[c % kStagesP]);
+  const uint32_t k_addr = smem_u32(sm.k[gc % kStagesP]);
   const uint32_t q_addr = smem_u32(sm.q[h]);
 #pragma unroll
   for (int ks = 0; ks < kD / 16; ++ks)
@@ -155,16 +199,17 @@ __device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int
   tc::mma_commit(&sm.s_full[h]);
 }
 
-// O of half h += P_h V_c in the half's O columns (one thread); chunk 0
-// starts the sum.
-__device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, int c,
+// O of half h += P_h V for chunk gc in the half's O columns (one thread);
+// the item's first chunk starts the sum.
+__device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, int gc, bool first,
                                              uint32_t id_o) {
-  const uint32_t v_addr = smem_u32(sm.v[c % kStagesP]);
+  const uint32_t v_addr = smem_u32(sm.v[gc % kStagesP]);
 #pragma unroll
   for (int ks = 0; ks < kChunk / 16; ++ks) {
     const uint32_t pa = smem_u32(sm.p[h][ks >> 2]) + 32 * (ks & 3);
     tc::mma_bf16(tmem + kTmemO + h * kD, tc::sdesc_sw128(pa, 16, 1024),
-                 tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o, (c > 0 || ks > 0) ? 1u : 0u);
+                 tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o,
+                 (!first || ks > 0) ? 1u : 0u);
   }
   tc::mma_commit(&sm.o_full[h]);
 }
@@ -176,11 +221,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   PSmem &sm = *reinterpret_cast<PSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.y;   // kv head
   if (tid == 0) {
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int st = 0; st < kStagesP; ++st) {
       mbar_init(&sm.kv_full[st], 1);
       mbar_init(&sm.kv_empty[st], 1);
@@ -189,13 +234,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.s_full[h], 1);
       mbar_init(&sm.p_full[h], kSoftThreads);
       mbar_init(&sm.o_full[h], 1);
+      mbar_init(&sm.o_free[h], kSoftThreads);
     }
     fence_mbar_init();
   }
   pdl_launch_dependents();
   pdl_wait_primary();   // q and the cache come from the kernels before
 
-  // ---- query tiles per sequence, laid end to end; the last ones go first
+  // ---- query tiles per sequence, laid end to end
   const long long cap = static_cast<long long>(p.max_blocks) * kBs;
   int carry = 0;
   for (int base = 0; base < p.num_seqs; base += kPThreads) {
@@ -209,7 +255,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       if (ctx >= 0 && n >= 0 && c0 >= 0 && c1 <= p.total_tokens &&
           static_cast<long long>(ctx) + n <= cap)
         tiles = (n + kCtaTok - 1) / kCtaTok;
-      else if (blockIdx.x == 0 && blockIdx.y == 0)
+      else if (blockIdx.x == 0)
         report(p.err, PA_DEV_CTX_RANGE);
     }
     int incl = tiles;
@@ -231,40 +277,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     carry += chunk;
     __syncthreads();
   }
+  if (tid == 0) sm.tile_prefix[0] = 0;
   const int total_tiles = carry;
-  if (tid == 0) {
-    sm.tile_prefix[0] = 0;
-    sm.valid = 0;
-    const int t = total_tiles - 1 - static_cast<int>(blockIdx.x);
-    if (t >= 0) {
-      int lo = 0, hi = p.num_seqs - 1;   // the sequence s with prefix[s] <= t < prefix[s+1]
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sm.tile_prefix[mid] <= t) lo = mid;
-        else hi = mid - 1;
-      }
-      sm.seq = lo;
-      sm.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
-      sm.valid = 1;
-    }
-  }
+  const int n_items = total_tiles * kHkv;
   __syncthreads();
-  if (!sm.valid) return;
-  const int s = sm.seq;
-  const int t0 = sm.t0;
-  const int ctx = p.context_lens[s];
-  const int row0 = p.cu_tokens[s];
-  const int n = p.cu_tokens[s + 1] - row0;
-  // half h holds tokens t0 + 32h .. t0 + 32h + rows_h - 1 (rows_h <= 0: no work)
-  const int rows0 = min(kQTok, n - t0);
-  const int rows1 = min(kQTok, n - t0 - kQTok);
-  const int halves = rows1 > 0 ? 2 : 1;
-  const int n_keys0 = ctx + t0 + rows0;                        // half 0 sees keys < n_keys0
-  const int n_keys1 = ctx + t0 + kQTok + max(rows1, 0);
-  const int n_keys = halves == 2 ? n_keys1 : n_keys0;         // the CTA's keys
-  const int n_chunks = (n_keys + kChunk - 1) / kChunk;
-  const int nc0 = (n_keys0 + kChunk - 1) / kChunk;
-  const int nc1 = halves == 2 ? n_chunks : 0;
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
 
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -274,64 +291,75 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  const int G = gridDim.x;
   if (warp >= 8) {
     // the producer/MMA warpgroup gives registers to the softmax warpgroups
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (warp == kProducerWarp) {
       // ===================================================== producer warp ==
-      const int32_t *row =
-          p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&sm.q_full, halves * kOperandBytes);
-        for (int h = 0; h < halves; ++h)
-          tma_load_3d(sm.q[h], &q_map, 0, g * kGqa, row0 + t0 + h * kQTok, &sm.q_full);
-      }
       bool ok = true;
+      int gc = 0, k = 0;
       uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
-      for (int j = 0; j < n_chunks && ok; ++j) {
-        const int st = j % kStagesP;
-        const uint32_t ph = (j / kStagesP) & 1;
-        // lane l < 8 looks up page j * 8 + l
-        const int pg = j * kPagesPerChunk + (lane & 7);
-        int blk = -1;
-        const bool needed = lane < kPagesPerChunk && pg * kBs < n_keys;
-        if (needed) blk = row[pg];
-        const bool valid = needed && blk >= 0 && blk < p.num_blocks;
-        const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
-        const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
+      for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
+        const Item it = decode_item(sm, p, total_tiles, i);
+        const int32_t *row =
+            p.block_table + (static_cast<size_t>(it.s) * p.n_layers + p.layer) * p.max_blocks;
         int good = 1;
         if (lane == 0) {
-          if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
+          // the previous item's Q has been read by all its MMAs
+          if (k > 0 && !mbar_wait(&sm.q_empty, (k - 1) & 1)) {
             good = 0;
           } else {
-            if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
-            sm.pmask[st] = static_cast<int>(vm);
-            mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
-            issued |= 1u << st;
-            issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
+            mbar_arrive_expect_tx(&sm.q_full, it.halves * kOperandBytes);
+            for (int h = 0; h < it.halves; ++h)
+              tma_load_3d(sm.q[h], &q_map, 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok,
+                          &sm.q_full);
           }
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
-          ok = false;
-          break;
-        }
-        __syncwarp();
-        // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
-        const int pl = lane & 7, kv = (lane >> 3) & 1;
-        const int pblk = __shfl_sync(0xffffffffu, blk, pl);
-        if (lane < 16 && ((vm >> pl) & 1u)) {
-          unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
-          tma_load_5d(dst, &kv_map, 0, g, 0, kv, pblk, &sm.kv_full[st]);
+        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+        for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
+          const int st = gc % kStagesP;
+          const uint32_t ph = (gc / kStagesP) & 1;
+          // lane l < 8 looks up page j * 8 + l
+          const int pg = j * kPagesPerChunk + (lane & 7);
+          int blk = -1;
+          const bool needed = lane < kPagesPerChunk && pg * kBs < it.n_keys;
+          if (needed) blk = row[pg];
+          const bool valid = needed && blk >= 0 && blk < p.num_blocks;
+          const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
+          const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
+          good = 1;
+          if (lane == 0) {
+            if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
+              good = 0;
+            } else {
+              if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
+              sm.pmask[st] = static_cast<int>(vm);
+              mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
+              issued |= 1u << st;
+              issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+          if (!ok) break;
+          __syncwarp();
+          // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
+          const int pl = lane & 7, kv = (lane >> 3) & 1;
+          const int pblk = __shfl_sync(0xffffffffu, blk, pl);
+          if (lane < 16 && ((vm >> pl) & 1u)) {
+            unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
+            tma_load_5d(dst, &kv_map, 0, it.g, 0, kv, pblk, &sm.kv_full[st]);
+          }
         }
       }
       if (lane == 0) {
         if (!ok) report(p.err, PA_DEV_TIMEOUT);
         // no copy may still be landing in shared memory when the CTA exits
-        if (!mbar_wait(&sm.q_full, 0)) report(p.err, PA_DEV_TIMEOUT);
+        if (k > 0 && !mbar_wait(&sm.q_full, (k - 1) & 1)) report(p.err, PA_DEV_TIMEOUT);
         for (int st = 0; st < kStagesP; ++st)
           if ((issued >> st) & 1u)
-            if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
+            if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u))
+              report(p.err, PA_DEV_TIMEOUT);
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -339,37 +367,49 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       const uint32_t id_s = tc::idesc_bf16(kRows, kChunk, false);
       const uint32_t id_o = tc::idesc_bf16(kRows, kD, true);
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&sm.q_full, 0) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok && n_chunks > 0) ok = mma_prepare_chunk(sm, 0, n_keys, lane);
-      if (ok && lane == 0) {
-        tc::fence_after_sync();
-        mma_issue_s(sm, tmem, 0, 0, id_s);
-        if (halves == 2) mma_issue_s(sm, tmem, 1, 0, id_s);
-      }
-      for (int j = 0; j < n_chunks && ok; ++j) {
-        if (j + 1 < n_chunks && !mma_prepare_chunk(sm, j + 1, n_keys, lane)) {
-          ok = 0;
-          break;
+      int gc = 0, k = 0;
+      int n_p[kHalves] = {0, 0};        // P chunks consumed per half
+      int n_active[kHalves] = {0, 0};   // items in which the half had work
+      for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
+        const Item it = decode_item(sm, p, total_tiles, i);
+        if (lane == 0) ok = mbar_wait_short(&sm.q_full, k & 1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) ok = mma_prepare_chunk(sm, gc, 0, it.n_keys, lane);
+        if (ok && lane == 0) {
+          tc::fence_after_sync();
+          mma_issue_s(sm, tmem, 0, gc, id_s);
+          if (it.halves == 2) mma_issue_s(sm, tmem, 1, gc, id_s);
         }
-        for (int h = 0; h < halves && ok; ++h) {
-          const int nch = h == 0 ? nc0 : nc1;
-          if (j >= nch) continue;
-          int good = 1;
-          if (lane == 0) {
-            // the half's softmax has written P_j (and read S_j and O_{j-1})
-            if (!mbar_wait_short(&sm.p_full[h], j & 1)) {
-              good = 0;
-            } else {
-              tc::fence_after_sync();
-              mma_issue_pv(sm, tmem, h, j, id_o);
-              if (j + 1 < nch) mma_issue_s(sm, tmem, h, j + 1, id_s);
-            }
+        for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
+          if (j + 1 < it.n_chunks && !mma_prepare_chunk(sm, gc + 1, (j + 1) * kChunk, it.n_keys, lane)) {
+            ok = 0;
+            break;
           }
-          ok = __shfl_sync(0xffffffffu, good, 0);
+          for (int h = 0; h < it.halves && ok; ++h) {
+            const int nch = h == 0 ? it.nc0 : it.nc1;
+            if (j >= nch) continue;
+            int good = 1;
+            if (lane == 0) {
+              // the half's previous item has read its O (the first PV clears it)
+              if (j == 0 && n_active[h] > 0 &&
+                  !mbar_wait_short(&sm.o_free[h], (n_active[h] - 1) & 1))
+                good = 0;
+              // the half's softmax has written P (and read S)
+              if (good && !mbar_wait_short(&sm.p_full[h], n_p[h] & 1)) good = 0;
+              if (good) {
+                tc::fence_after_sync();
+                mma_issue_pv(sm, tmem, h, gc, j == 0, id_o);
+                if (j + 1 < nch) mma_issue_s(sm, tmem, h, gc + 1, id_s);
+              }
+            }
+            ++n_p[h];
+            ok = __shfl_sync(0xffffffffu, good, 0);
+          }
+          if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[gc % kStagesP]);
+          __syncwarp();
         }
-        if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[j % kStagesP]);
-        __syncwarp();
+        if (ok && lane == 0) tc::mma_commit(&sm.q_empty);   // every MMA that reads Q is issued
+        for (int h = 0; h < it.halves; ++h) ++n_active[h];
       }
       if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
       __syncwarp();
@@ -387,113 +427,125 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const int h = tid >> 7;                   // half
     const int r = tid & (kRows - 1);          // MMA row = TMEM lane
     const int tok = r >> 2, hh = r & 3;
-    const int rows = h == 0 ? rows0 : rows1;
-    const int nch = h == 0 ? nc0 : nc1;
-    const int first_pos = ctx + t0 + h * kQTok;           // the half's first query position
-    const int last_pos = first_pos + max(rows, 1) - 1;
-    const int qpos = min(first_pos + tok, last_pos);
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_addr + h * kChunk, o_addr = lane_addr + kTmemO + h * kD;
-    float m = p_neg_inf(), l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nch; ++j) {
-      const int st = j % kStagesP;
-      if (!mbar_wait_short(&sm.s_full[h], j & 1) ||
-          !mbar_wait_short(&sm.kv_full[st], (j / kStagesP) & 1)) {
+    int gc = 0, n_s = 0, n_pv = 0;
+    for (int i = blockIdx.x; i < n_items && ok; i += G) {
+      const Item it = decode_item(sm, p, total_tiles, i);
+      const int rows = h == 0 ? it.rows0 : it.rows1;
+      const int nch = h == 0 ? it.nc0 : it.nc1;
+      if (nch == 0) {
+        gc += it.n_chunks;
+        continue;
+      }
+      const int first_pos = it.ctx + it.t0 + h * kQTok;   // the half's first query position
+      const int last_pos = first_pos + rows - 1;
+      const int qpos = min(first_pos + tok, last_pos);
+      float m = p_neg_inf(), l = 0.f;
+      for (int j = 0; j < nch; ++j) {
+        const int st = (gc + j) % kStagesP;
+        if (!mbar_wait_short(&sm.s_full[h], n_s & 1) ||
+            !mbar_wait_short(&sm.kv_full[st], ((gc + j) / kStagesP) & 1)) {
+          ok = false;
+          break;
+        }
+        ++n_s;
+        tc::fence_after_sync();
+        const int pm = sm.pmask[st];
+        const int kbase = j * kChunk;
+        // every key of the chunk is visible to every row of the half and was loaded
+        const bool full = pm == 0xff && kbase + kChunk - 1 <= first_pos;
+        const int lim = qpos - kbase;           // keys c <= lim are at or before the row
+        uint32_t v[kChunk];
+#pragma unroll
+        for (int c0 = 0; c0 < kChunk; c0 += 32)
+          tc::tmem_ld32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
+        tc::tmem_ld_wait();
+        if (!full) {
+          // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
+#pragma unroll
+          for (int c = 0; c < kChunk; ++c)
+            if (!((c <= lim) && ((pm >> (c >> 4)) & 1))) v[c] = 0xff800000u;
+        }
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = p_neg_inf();
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+        const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.qscale;
+        const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
+        if (__any_sync(0xffffffffu, move) && j > 0) {
+          // rescale O (the whole warp takes part in the TMEM round trip)
+          const float alpha = move ? p_exp2(m - mc) : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t ov[32];
+            tc::tmem_ld32(o_addr + c0, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tc::tmem_st32(o_addr + c0, ov);
+          }
+          tc::tmem_st_wait();
+          l *= alpha;
+        }
+        if (move) m = mc;
+        const float base = (m == p_neg_inf()) ? 0.f : m;
+        const float2 qs2 = make_float2(p.qscale, p.qscale), nb2 = make_float2(-base, -base);
+        // P = exp2(s * qscale - m) in bf16, stored swizzled; 4 partial sums
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int ch = 0; ch < kChunk / 8; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 8 * ch + 2 * q;
+            const float2 x = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                  qs2, nb2);
+            const float e0 = p_exp2(x.x), e1 = p_exp2(x.y);
+            ls[q] = make_float2(ls[q].x + e0, ls[q].y + e1);
+            pk[q] = float2_to_bf16x2(e0, e1);
+          }
+          unsigned char *region = sm.p[h][ch >> 3] + r * kTileRowBytes;
+          *reinterpret_cast<uint4 *>(region + (((ch & 7) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+        fence_proxy_async_smem();   // P, for the tensor core
+        tc::fence_before_sync();
+        mbar_arrive(&sm.p_full[h]);
+      }
+      if (!ok) break;
+      n_pv += nch;
+      if (!mbar_wait_short(&sm.o_full[h], (n_pv - 1) & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const int pm = sm.pmask[st];
-      const int kbase = j * kChunk;
-      // every key of the chunk is visible to every row of the half and was loaded
-      const bool full = pm == 0xff && kbase + kChunk - 1 <= first_pos;
-      const int lim = qpos - kbase;           // keys c <= lim are at or before the row
-      uint32_t v[kChunk];
-#pragma unroll
-      for (int c0 = 0; c0 < kChunk; c0 += 32)
-        tc::tmem_ld32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
+      uint32_t ov[kD];
+      tc::tmem_ld32(o_addr, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+      tc::tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
       tc::tmem_ld_wait();
-      if (!full) {
-        // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
-#pragma unroll
-        for (int c = 0; c < kChunk; ++c)
-          if (!((c <= lim) && ((pm >> (c >> 4)) & 1))) v[c] = 0xff800000u;
-      }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = p_neg_inf();
-#pragma unroll
-      for (int c = 0; c < kChunk; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
-      const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.qscale;
-      const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
-      if (__any_sync(0xffffffffu, move) && j > 0) {
-        // rescale O (the whole warp takes part in the TMEM round trip)
-        const float alpha = move ? p_exp2(m - mc) : 1.f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-          uint32_t ov[32];
-          tc::tmem_ld32(o_addr + c0, ov);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          tc::tmem_st32(o_addr + c0, ov);
-        }
-        tc::tmem_st_wait();
-        l *= alpha;
-      }
-      if (move) m = mc;
-      const float base = (m == p_neg_inf()) ? 0.f : m;
-      const float2 qs2 = make_float2(p.qscale, p.qscale), nb2 = make_float2(-base, -base);
-      // P = exp2(s * qscale - m) in bf16, stored swizzled; 4 partial sums
-      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int ch = 0; ch < kChunk / 8; ++ch) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 8 * ch + 2 * i;
-          const float2 x = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                qs2, nb2);
-          const float e0 = p_exp2(x.x), e1 = p_exp2(x.y);
-          ls[i] = make_float2(ls[i].x + e0, ls[i].y + e1);
-          pk[i] = float2_to_bf16x2(e0, e1);
-        }
-        unsigned char *region = sm.p[h][ch >> 3] + r * kTileRowBytes;
-        *reinterpret_cast<uint4 *>(region + (((ch & 7) ^ (r & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-      fence_proxy_async_smem();   // P, for the tensor core
       tc::fence_before_sync();
-      mbar_arrive(&sm.p_full[h]);
-    }
-    if (ok && nch > 0) {
-      if (mbar_wait_short(&sm.o_full[h], (nch - 1) & 1)) {
-        tc::fence_after_sync();
-        uint32_t ov[kD];
-        tc::tmem_ld32(o_addr, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-        tc::tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
-        tc::tmem_ld_wait();
-        if (tok < rows) {
-          const float inv = (l > 0.f) ? 1.f / l : 0.f;
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              p.out + ((static_cast<size_t>(row0) + t0 + h * kQTok + tok) * kHq + g * kGqa + hh) *
-                          kD);
+      mbar_arrive(&sm.o_free[h]);   // the next item's first PV may clear O
+      if (tok < rows) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            p.out + ((static_cast<size_t>(it.row0) + it.t0 + h * kQTok + tok) * kHq +
+                     it.g * kGqa + hh) * kD);
 #pragma unroll
-          for (int e = 0; e < kD / 8; ++e) {
-            const float *f = reinterpret_cast<const float *>(&ov[8 * e]);
-            dst[e] = make_uint4(float2_to_bf16x2(f[0] * inv, f[1] * inv),
-                                float2_to_bf16x2(f[2] * inv, f[3] * inv),
-                                float2_to_bf16x2(f[4] * inv, f[5] * inv),
-                                float2_to_bf16x2(f[6] * inv, f[7] * inv));
-          }
+        for (int e = 0; e < kD / 8; ++e) {
+          const float *f = reinterpret_cast<const float *>(&ov[8 * e]);
+          dst[e] = make_uint4(float2_to_bf16x2(f[0] * inv, f[1] * inv),
+                              float2_to_bf16x2(f[2] * inv, f[3] * inv),
+                              float2_to_bf16x2(f[4] * inv, f[5] * inv),
+                              float2_to_bf16x2(f[6] * inv, f[7] * inv));
         }
-      } else {
-        ok = false;
       }
+      gc += it.n_chunks;
     }
     if (!ok) report(p.err, PA_DEV_TIMEOUT);
   }
@@ -583,9 +635,11 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
     map_q = q;
     map_q_tokens = total_tokens;
   }
-  // every sequence's chunk ends in at most one partial tile
+  // every sequence's chunk ends in at most one partial tile; one CTA per SM
+  // works through the (tile, kv head) items
   const long long tiles = (static_cast<long long>(total_tokens) + kCtaTok - 1) / kCtaTok + num_seqs;
-  if (tiles > INT_MAX) return PA_ERR_ARG;
+  if (tiles * kHkv > INT_MAX) return PA_ERR_ARG;
+  const int grid = static_cast<int>(min(static_cast<long long>(di.sm_count), tiles * kHkv));
   PrefillParams prm;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.cu_tokens = cu_tokens;
@@ -599,7 +653,7 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   prm.layer = layer;
   prm.total_tokens = total_tokens;
   prm.qscale = scale * kLog2eP;
-  if (launch_pdl(prefill_attention_kernel, dim3(static_cast<unsigned>(tiles), kHkv),
+  if (launch_pdl(prefill_attention_kernel, dim3(static_cast<unsigned>(grid)),
                  dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
