@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
 // cu_tokens[s] .. cu_tokens[s+1]-1, at positions context_lens[s] + i.
 //   prefill_alloc_kernel  (1 CTA)  ranks every page the chunks open over the
 //                                  sequences in order and pops them from the
-//                                  back of the free list.
+//                                  back of the free list, pages spread over
+//                                  the threads.
 //   prefill_store_kernel  (1 CTA per token row, programmatic dependent
 //                                  launch) rotates the row's k and q, then
 //                                  stores K/V in the slot the table names.
@@ -291,6 +292,8 @@ __device__ __forceinline__ bool chunk_fits(const PrefillAppendParams &p, int s, 
 
 __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendParams p) {
   __shared__ int tot[kScanCta / 32];
+  __shared__ int incl_s[kScanCta];    // pages of the batch's sequences up to and including each
+  __shared__ int first_s[kScanCta];   // each sequence's first new page
   pdl_wait_primary();        // the table and free list may come from the previous kernel
   pdl_launch_dependents();   // the store kernel may start its rotations now
   const int fc0 = min(max(*p.free_count, 0), p.num_blocks);
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendPa
         pages = (ctx + n + kBs - 1) / kBs - first;     // pages this chunk opens
       }
     }
-    // pages are ranked over the sequences in order: an exclusive prefix sum
+    // pages are ranked over the sequences in order: a prefix sum
     int incl = pages;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -322,23 +325,33 @@ __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendPa
       if (w < warp) before += t;
       chunk += t;
     }
+    incl_s[threadIdx.x] = before + incl;
+    first_s[threadIdx.x] = first;
     __syncthreads();
-    const int rank0 = served + before + incl - pages;
-    if (pages > 0) {
-      int32_t *row = p.block_table + table_row(s, p.n_layers, p.layer, p.max_blocks);
-      for (int j = 0; j < pages; ++j) {
-        const int rank = rank0 + j;
-        if (rank < fc0) {
-          const int blk = p.free_list[fc0 - 1 - rank];
-          row[first + j] = blk;
-          if (blk < 0 || blk >= p.num_blocks) report(p.err, PA_DEV_BAD_BLOCK);
-        } else {
-          row[first + j] = -1;   // refused: the page stays unassigned
-          report(p.err, PA_DEV_FREE_UNDERFLOW);
-        }
+    // every thread takes pages e, e + 1024, ... of the batch: page e belongs
+    // to the first sequence k of the batch with incl_s[k] > e
+    for (int e = threadIdx.x; e < chunk; e += kScanCta) {
+      int lo = 0, hi = kScanCta - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (incl_s[mid] > e) hi = mid;
+        else lo = mid + 1;
+      }
+      const int j = e - (lo > 0 ? incl_s[lo - 1] : 0);
+      int32_t *entry =
+          p.block_table + table_row(base + lo, p.n_layers, p.layer, p.max_blocks) + first_s[lo] + j;
+      const int rank = served + e;
+      if (rank < fc0) {
+        const int blk = p.free_list[fc0 - 1 - rank];
+        *entry = blk;
+        if (blk < 0 || blk >= p.num_blocks) report(p.err, PA_DEV_BAD_BLOCK);
+      } else {
+        *entry = -1;   // refused: the page stays unassigned
+        report(p.err, PA_DEV_FREE_UNDERFLOW);
       }
     }
     served += chunk;
+    __syncthreads();
   }
   if (threadIdx.x == 0) *p.free_count = max(fc0 - served, 0);
 }
