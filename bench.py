@@ -1205,7 +1205,8 @@ def run_serve_gpu(args, rank, world, dist):
             "prompt_tokens_per_run": prompt_tokens,
             "l2": f"each run reads {kv_bytes / 2**30:.1f} GiB of K/V over its decode steps "
                   "(L2 129 MB)",
-            "launch": "host loop: pa_batcher_plan + pa_batcher_run per loop step, one stream",
+            "launch": "host loop: pa_batcher_plan + pa_batcher_run per loop step, one stream; "
+                      "decode-only steps replayed from CUDA graphs (one per batch size)",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {

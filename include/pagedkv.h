@@ -384,6 +384,15 @@ int pa_batcher_pending(const pa_batcher *b);
  * must stay untouched until the stream reaches the end of the step. */
 int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *stream);
 
+/* Decode-only steps (no request leaves or enters) are replayed from CUDA
+ * graphs once one such step has run eagerly: one graph per batch size and
+ * buffer set, captured on first use, its control-block copy fed from a
+ * small ring of pinned host buffers the batcher owns.  Enabled by default;
+ * enable = 0 runs every step by direct launches.  If capture is not
+ * possible (for instance, `stream` is being captured by the caller) the
+ * batcher switches to direct launches for good. */
+int pa_batcher_set_graphs(pa_batcher *b, int enable);
+
 /* Mark the planned step as done without enqueuing anything, for callers
  * that run the step's device work with their own kernels: the admitted
  * prompts count as cached and every row as one decode step further. */

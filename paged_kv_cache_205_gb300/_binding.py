@@ -47,6 +47,7 @@ _EXPORTS = (
     "pa_batcher_pending",
     "pa_batcher_run",
     "pa_batcher_commit",
+    "pa_batcher_set_graphs",
 )
 
 _lock = threading.Lock()
@@ -142,6 +143,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_batcher_run.restype = I
         lib.pa_batcher_commit.argtypes = [P]
         lib.pa_batcher_commit.restype = I
+        lib.pa_batcher_set_graphs.argtypes = [P, I]
+        lib.pa_batcher_set_graphs.restype = I
         _lib = lib
         return lib
 
@@ -380,6 +383,10 @@ class Batcher:
 
     def commit(self):
         _check("pa_batcher_commit", library().pa_batcher_commit(self._h))
+
+    def set_graphs(self, enable: bool):
+        """Replay decode-only steps from CUDA graphs (the default) or not."""
+        _check("pa_batcher_set_graphs", library().pa_batcher_set_graphs(self._h, int(bool(enable))))
 
     def run(self, bufs: "BatchBuffers", stream=None):
         _check("pa_batcher_run", library().pa_batcher_run(self._h, ctypes.byref(bufs),

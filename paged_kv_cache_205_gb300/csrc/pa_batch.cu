@@ -104,6 +104,23 @@ struct Row {
 
 using namespace pa;
 
+namespace {
+
+constexpr int kCtlRing = 4;   // pinned control blocks in flight for replayed steps
+
+// A decode-only step captured as a CUDA graph, for one batch size and one
+// set of buffers.
+struct DecodeGraph {
+  int n_rows = 0;
+  int device = -1;
+  pa_batch_buffers bufs{};
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t ctl_copy = nullptr;   // the control-block copy, repointed per replay
+};
+
+}  // namespace
+
 struct pa_batcher {
   int max_slots, n_layers, max_blocks, pages_free, prefill_budget;
   std::deque<Request> queue;
@@ -116,6 +133,14 @@ struct pa_batcher {
   int first_moved = 0;
   int n_prev = 0;
   std::vector<int32_t> ctl;   // host image of the control block
+  // decode-only steps replayed from CUDA graphs
+  bool graphs = true;
+  bool eager_decode_done = false;   // the kernels' one-time set-up has run
+  std::vector<DecodeGraph> decode_graphs;
+  int32_t *pinned[kCtlRing] = {};
+  cudaEvent_t ring_done[kCtlRing] = {};
+  int ring_next = 0;
+  cudaStream_t capture_stream = nullptr;
 };
 
 namespace {
@@ -152,7 +177,26 @@ extern "C" int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per
 }
 
 extern "C" int pa_batcher_destroy(pa_batcher *b) {
+  if (!b) return PA_OK;
+  for (DecodeGraph &g : b->decode_graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  for (int i = 0; i < kCtlRing; ++i) {
+    if (b->ring_done[i]) {
+      cudaEventSynchronize(b->ring_done[i]);
+      cudaEventDestroy(b->ring_done[i]);
+    }
+    if (b->pinned[i]) cudaFreeHost(b->pinned[i]);
+  }
+  if (b->capture_stream) cudaStreamDestroy(b->capture_stream);
   delete b;
+  return PA_OK;
+}
+
+extern "C" int pa_batcher_set_graphs(pa_batcher *b, int enable) {
+  if (!b) return PA_ERR_NULL;
+  b->graphs = enable != 0;
   return PA_OK;
 }
 
@@ -282,6 +326,111 @@ extern "C" int pa_batcher_commit(pa_batcher *b) {
   return PA_OK;
 }
 
+namespace {
+
+// The decode step of rows 0..n_rows-1, every layer: append, then attention.
+int enqueue_decode(pa_batcher *b, const pa_batch_buffers *buf, int32_t *ctl, int n_rows,
+                   void *stream) {
+  const CtlLayout L{b->max_slots};
+  const int Lyr = b->n_layers, mb = b->max_blocks;
+  const size_t dq = static_cast<size_t>(b->max_slots) * kHq * kD;
+  const size_t dk = static_cast<size_t>(b->max_slots) * kHkv * kD;
+  for (int l = 0; l < Lyr && n_rows > 0; ++l) {
+    int rc = pa_kv_append_rope(buf->decode_k + l * dk, buf->decode_v + l * dk,
+                               buf->decode_q + l * dq, buf->kv_cache, buf->num_blocks,
+                               buf->block_table, Lyr, mb, ctl + L.pos(), n_rows, l,
+                               buf->free_list, buf->free_count, buf->err, stream);
+    if (rc != PA_OK) return rc;
+    rc = pa_decode_attention(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
+                             buf->num_blocks, buf->block_table, Lyr, mb, ctl + L.attn(),
+                             n_rows, l, buf->scale, buf->decode_workspace,
+                             buf->decode_workspace_bytes, buf->err, stream);
+    if (rc != PA_OK) return rc;
+  }
+  return PA_OK;
+}
+
+bool same_buffers(const pa_batch_buffers &a, const pa_batch_buffers &b) {
+  return std::memcmp(&a, &b, sizeof(pa_batch_buffers)) == 0;
+}
+
+// A decode-only step from a CUDA graph: the control block goes through a
+// ring of pinned host buffers (the graph's copy node is repointed at the
+// buffer of this step), the graph is captured the first time a batch size
+// and buffer set is seen.  Returns PA_OK, or an error before anything was
+// enqueued on `stream` (the caller then runs the step eagerly).
+int run_decode_graph(pa_batcher *b, const pa_batch_buffers *buf, void *stream) {
+  const CtlLayout L{b->max_slots};
+  const size_t bytes = L.words() * sizeof(int32_t);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (!b->pinned[0]) {
+    for (int i = 0; i < kCtlRing; ++i) {
+      if (cudaHostAlloc(reinterpret_cast<void **>(&b->pinned[i]), bytes, cudaHostAllocDefault) !=
+              cudaSuccess ||
+          cudaEventCreateWithFlags(&b->ring_done[i], cudaEventDisableTiming) != cudaSuccess)
+        return PA_ERR_CUDA;
+    }
+  }
+  if (!b->capture_stream &&
+      cudaStreamCreateWithFlags(&b->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int slot = b->ring_next;
+  if (cudaEventSynchronize(b->ring_done[slot]) != cudaSuccess) return PA_ERR_CUDA;
+  std::memcpy(b->pinned[slot], b->ctl.data(), bytes);
+  const int n_rows = b->plan.n_rows;
+  DecodeGraph *g = nullptr;
+  for (DecodeGraph &c : b->decode_graphs)
+    if (c.n_rows == n_rows && c.device == dev && same_buffers(c.bufs, *buf)) g = &c;
+  int32_t *ctl = static_cast<int32_t *>(buf->ctl);
+  if (!g) {
+    DecodeGraph ng;
+    ng.n_rows = n_rows;
+    ng.device = dev;
+    ng.bufs = *buf;
+    cudaStream_t cs = b->capture_stream;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      return PA_ERR_CUDA;
+    const bool copied =
+        cudaMemcpyAsync(ctl, b->pinned[slot], bytes, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    const int rc = copied ? enqueue_decode(b, buf, ctl, n_rows, cs) : PA_ERR_CUDA;
+    const cudaError_t ec = cudaStreamEndCapture(cs, &ng.graph);
+    if (rc != PA_OK || ec != cudaSuccess) {
+      if (ng.graph) cudaGraphDestroy(ng.graph);
+      cudaGetLastError();
+      return rc != PA_OK ? rc : PA_ERR_CUDA;
+    }
+    size_t n_nodes = 0;
+    cudaGraphGetNodes(ng.graph, nullptr, &n_nodes);
+    std::vector<cudaGraphNode_t> nodes(n_nodes);
+    cudaGraphGetNodes(ng.graph, nodes.data(), &n_nodes);
+    for (cudaGraphNode_t nd : nodes) {
+      cudaGraphNodeType t;
+      if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeMemcpy) {
+        ng.ctl_copy = nd;
+        break;
+      }
+    }
+    if (!ng.ctl_copy || cudaGraphInstantiate(&ng.exec, ng.graph, 0) != cudaSuccess) {
+      cudaGraphDestroy(ng.graph);
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
+    b->decode_graphs.push_back(ng);
+    g = &b->decode_graphs.back();
+  } else if (cudaGraphExecMemcpyNodeSetParams1D(g->exec, g->ctl_copy, ctl, b->pinned[slot], bytes,
+                                                cudaMemcpyHostToDevice) != cudaSuccess) {
+    return PA_ERR_CUDA;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaGraphLaunch(g->exec, st) != cudaSuccess) return PA_ERR_CUDA;
+  cudaEventRecord(b->ring_done[slot], st);
+  b->ring_next = (slot + 1) % kCtlRing;
+  return PA_OK;
+}
+
+}  // namespace
+
 extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *stream) {
   if (!b || !buf) return PA_ERR_NULL;
   if (!b->planned) return PA_ERR_STATE;
@@ -296,6 +445,13 @@ extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *
     return PA_ERR_NULL;
   if (p.n_rows > 0 && (!buf->decode_q || !buf->decode_k || !buf->decode_v || !buf->decode_out))
     return PA_ERR_NULL;
+  // a decode-only step (nothing leaves, nothing enters) replays a graph once
+  // the kernels' one-time set-up has run eagerly
+  if (b->graphs && b->eager_decode_done && p.n_rows > 0 && p.n_retired == 0 &&
+      p.n_admitted == 0) {
+    if (run_decode_graph(b, buf, stream) == PA_OK) return pa_batcher_commit(b);
+    b->graphs = false;   // graphs unavailable here: every step runs eagerly from now on
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t *ctl = static_cast<int32_t *>(buf->ctl);
   // the control block: pageable host memory, staged by the copy before it returns
@@ -341,19 +497,8 @@ extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *
     if (rc != PA_OK) return rc;
   }
   // 3. one decode step for every active row
-  const size_t dq = static_cast<size_t>(b->max_slots) * kHq * kD;
-  const size_t dk = static_cast<size_t>(b->max_slots) * kHkv * kD;
-  for (int l = 0; l < Lyr && p.n_rows > 0; ++l) {
-    rc = pa_kv_append_rope(buf->decode_k + l * dk, buf->decode_v + l * dk, buf->decode_q + l * dq,
-                           buf->kv_cache, buf->num_blocks, buf->block_table, Lyr, mb,
-                           ctl + L.pos(), p.n_rows, l, buf->free_list, buf->free_count, buf->err,
-                           stream);
-    if (rc != PA_OK) return rc;
-    rc = pa_decode_attention(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
-                             buf->num_blocks, buf->block_table, Lyr, mb, ctl + L.attn(),
-                             p.n_rows, l, buf->scale, buf->decode_workspace,
-                             buf->decode_workspace_bytes, buf->err, stream);
-    if (rc != PA_OK) return rc;
-  }
+  rc = enqueue_decode(b, buf, ctl, p.n_rows, stream);
+  if (rc != PA_OK) return rc;
+  if (p.n_rows > 0 && p.n_retired == 0 && p.n_admitted == 0) b->eager_decode_done = true;
   return pa_batcher_commit(b);
 }

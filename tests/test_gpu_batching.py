@@ -180,3 +180,44 @@ def test_serve256_full_size_sampled():
     assert dl.b.pending() == 0 and steps > 100 and checked >= 4
     assert int(dl.fc.item()) == w.num_blocks and (dl.bt.cpu().numpy() == -1).all()
     dl.b.close()
+
+
+def test_graph_replayed_steps_equal_direct_launches():
+    """Decode-only steps replayed from CUDA graphs (the default) give
+    bit-identical tables, free lists and outputs to the same loop run with
+    direct launches, step by step (batch sizes change as requests come and
+    go, so several graphs are captured and replayed)."""
+    import torch
+    w = wl.make_serve_workload("serve_tiny")
+    rng = np.random.default_rng(w.seed)
+    free_list = rng.permutation(w.num_blocks).astype(np.int32)
+    runs = []
+    for graphs in (False, True):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        pool = torch.randn((w.num_blocks, 2, BS, N_KV, D), generator=g,
+                           device="cuda").to(torch.bfloat16)
+        dl = DeviceLoop(w, pool, free_list)
+        dl.b.set_graphs(graphs)
+        steps = []
+        while True:
+            p = dl.b.plan()
+            if p.done:
+                break
+            for t in (dl.pq, dl.pk_, dl.pv, dl.dq, dl.dk, dl.dv):
+                t.normal_(generator=g)
+            dl.b.run(dl.bufs)
+            torch.cuda.synchronize()
+            steps.append((p.n_rows, p.n_admitted, p.n_retired, dl.bt.cpu().numpy().copy(),
+                          int(dl.fc.item()), host_bits(dl.do[:, :p.n_rows]),
+                          host_bits(dl.po[:, :p.prefill_tokens]), int(dl.err.item())))
+        dl.b.close()
+        runs.append(steps)
+    assert len(runs[0]) == len(runs[1]) > 10
+    decode_only = 0
+    for a, b in zip(*runs):
+        assert a[:3] == b[:3] and a[4] == b[4] and a[7] == b[7] == 0
+        assert np.array_equal(a[3], b[3]) and np.array_equal(a[5], b[5])
+        assert np.array_equal(a[6], b[6])
+        decode_only += a[1] == 0 and a[2] == 0 and a[0] > 0
+    assert decode_only > 5
