@@ -317,6 +317,11 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------- GPU arm
+def attn_launches(cluster: bool) -> int:
+    """Kernel launches of one pa_decode_attention call."""
+    return 1 if cluster else 2
+
+
 class DeviceStep:
     """Device-resident state of one workload and the step over it."""
 
@@ -378,6 +383,12 @@ def run_gpu(args, rank, world, dist):
     w = wl.make_workload(args.workload, block_tokens=args.block_tokens)
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
     st.pk.pa_decode_set_grid_limit(args.grid)
+    st.pk.pa_decode_set_path({"auto": st.pk.PA_DECODE_AUTO, "split": st.pk.PA_DECODE_SPLIT,
+                              "cluster": st.pk.PA_DECODE_CLUSTER}[args.decode_kernel])
+    # which decode kernel the library runs for this batch: one cluster per
+    # (sequence, kv head), or split-context chunks + a merge kernel
+    cluster = st.pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens) == st.pk.PA_DECODE_CLUSTER
+    st.launches_per_step = attn_launches(cluster) * w.n_layers + (2 * w.n_layers if w.append else 0)
     L, n = w.n_layers, w.num_seqs
 
     def barrier():
@@ -537,18 +548,23 @@ def run_gpu(args, rank, world, dist):
             "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
             "decode_grid_cap": args.grid,
+            "decode_kernel": "cluster" if cluster else "split",
             "block_tokens": w.block_tokens,
             "page_fill": page_fill,
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode_attention (decode_split_kernel + decode_merge_kernel)",
+            "kernel": ("pa_decode_attention (decode_pair_kernel: one thread-block cluster per "
+                       "(sequence, kv head))" if cluster else
+                       "pa_decode_attention (decode_split_kernel + decode_merge_kernel)"),
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": profiled_traffic(args.workload),
+            "traffic": (profiled_traffic(args.workload, "decode_pair_kernel",
+                                         ("pa_decode_pair.cu", "pa_device.cuh")) if cluster
+                        else profiled_traffic(args.workload)),
             "bytes_per_launch": attn_bytes,
             "ms_per_launch": attn_ms,
             "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "
@@ -981,8 +997,11 @@ class ServeLoop:
             if on_step:
                 on_step(p, False)
             steps += 1
+            attn = 0
+            if p.n_rows > 0:
+                attn = attn_launches(self.pk.pa_decode_kernel_for(p.n_rows) == self.pk.PA_DECODE_CLUSTER)
             launches += 1 + (3 if p.n_retired else 0) + 3 * w.n_layers * (p.n_admitted > 0) \
-                + 4 * w.n_layers * (p.n_rows > 0)
+                + (2 + attn) * w.n_layers * (p.n_rows > 0)
         b.close()
         return steps, launches
 
@@ -1255,6 +1274,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block-tokens", type=int, default=BS, choices=[8, 16, 32],
                     help="decode path: tokens per page (the page size as a tunable)")
+    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "split", "cluster"],
+                    help="decode-attention kernel (pa_decode_set_path): automatic choice, the "
+                         "split-context kernel, or one cluster per (sequence, kv head)")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")
     args = ap.parse_args()

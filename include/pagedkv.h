@@ -116,7 +116,8 @@ int pa_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_
  * block_table[s][layer][t / 16], slot t % 16, kv head h / 4.  fp32
  * accumulation, output rounded to bf16.  A sequence with context 0 gets a
  * zero output.  Long contexts are split across CTAs and merged (split
- * context); the split only changes rounding.
+ * context); the split only changes rounding.  Which kernel runs is set by
+ * pa_decode_set_path (automatic by default).
  * workspace: device scratch of at least pa_decode_workspace_size(num_seqs,
  * max_blocks_per_seq) bytes, owned by the caller.  It must be zero-filled
  * once before its first use (it holds the work counter that spreads blocks
@@ -277,8 +278,6 @@ int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_laye
             int32_t *free_list, int32_t *free_count, int num_blocks,
             int32_t *err, void *stream);
 
-/* Cap on the CTAs one pa_decode_attention launch uses (0 = automatic: two
- * per SM).  Process-wide; affects only how contexts are split. */
 /*
  * Continuous batching -- the host loop that feeds prefill and decode from a
  * queue of requests through a fixed set of block-table rows (slots).
@@ -398,7 +397,37 @@ int pa_batcher_set_graphs(pa_batcher *b, int enable);
  * prompts count as cached and every row as one decode step further. */
 int pa_batcher_commit(pa_batcher *b);
 
+/* Cap on the CTAs one pa_decode_attention launch uses (0 = automatic: two
+ * per SM).  Process-wide; affects only how contexts are split. */
 int pa_decode_set_grid_limit(int max_ctas);
+
+/*
+ * Which decode-attention kernel pa_decode_attention runs (process-wide).
+ * Both compute the same attention and differ only in rounding order.
+ *   PA_DECODE_AUTO     the cluster kernel when every (sequence, kv head)
+ *                      pair of the call fits on the GPU at once (num_seqs *
+ *                      8 <= 2 CTAs per SM, within the grid limit) and pages
+ *                      hold 16 tokens; the split-context kernel otherwise.
+ *   PA_DECODE_SPLIT    always the split-context kernel: the batch's blocks
+ *                      laid end to end and cut into chunks over all CTAs,
+ *                      fp32 partials merged by a second kernel.
+ *   PA_DECODE_CLUSTER  the cluster kernel (16-token pages; other page sizes
+ *                      use the split-context kernel): one thread-block
+ *                      cluster of 1, 2, 4 or 8 CTAs per (sequence, kv head),
+ *                      its CTAs combined in shared memory; no workspace use.
+ * Returns PA_ERR_ARG for any other value.
+ */
+#define PA_DECODE_AUTO     0
+#define PA_DECODE_SPLIT    1
+#define PA_DECODE_CLUSTER  2
+int pa_decode_set_path(int path);
+
+/* The kernel (PA_DECODE_SPLIT or PA_DECODE_CLUSTER) that pa_decode_attention
+ * (block_tokens 16) or pa_decode_attention_bt would run for num_seqs
+ * sequences on the current device under the current path and grid limit;
+ * PA_ERR_ARG for a bad count or page size, PA_ERR_CUDA / PA_ERR_DEVICE when
+ * no sm_103 device answers. */
+int pa_decode_kernel_for(int num_seqs, int block_tokens);
 
 /* Human-readable name of a PA_ERR_* code. */
 const char *pa_error_string(int code);

@@ -31,6 +31,11 @@ from ._binding import (  # noqa: F401
     library_path,
     pa_decode_attention,
     pa_decode_set_grid_limit,
+    pa_decode_set_path,
+    pa_decode_kernel_for,
+    PA_DECODE_AUTO,
+    PA_DECODE_SPLIT,
+    PA_DECODE_CLUSTER,
     pa_decode_workspace_size,
     pa_error_string,
     pa_free,

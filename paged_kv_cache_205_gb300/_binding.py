@@ -120,6 +120,10 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_free.restype = I
         lib.pa_decode_set_grid_limit.argtypes = [I]
         lib.pa_decode_set_grid_limit.restype = I
+        lib.pa_decode_set_path.argtypes = [I]
+        lib.pa_decode_set_path.restype = I
+        lib.pa_decode_kernel_for.argtypes = [I, I]
+        lib.pa_decode_kernel_for.restype = I
         lib.pa_error_string.argtypes = [I]
         lib.pa_error_string.restype = ctypes.c_char_p
         PP = ctypes.POINTER(ctypes.c_void_p)
@@ -318,6 +322,23 @@ def pa_free(seq_ids, block_table, context_lens, free_list, free_count, num_block
 
 def pa_decode_set_grid_limit(max_ctas: int) -> None:
     _check("pa_decode_set_grid_limit", library().pa_decode_set_grid_limit(int(max_ctas)))
+
+
+PA_DECODE_AUTO, PA_DECODE_SPLIT, PA_DECODE_CLUSTER = 0, 1, 2
+
+
+def pa_decode_kernel_for(num_seqs: int, block_tokens: int = PA_BLOCK_TOKENS) -> int:
+    """PA_DECODE_SPLIT or PA_DECODE_CLUSTER: the kernel a decode call on
+    num_seqs sequences would run now."""
+    r = library().pa_decode_kernel_for(int(num_seqs), int(block_tokens))
+    _check("pa_decode_kernel_for", min(r, 0))
+    return int(r)
+
+
+def pa_decode_set_path(path: int) -> None:
+    """Selects the decode-attention kernel: PA_DECODE_AUTO (default),
+    PA_DECODE_SPLIT or PA_DECODE_CLUSTER (process-wide)."""
+    _check("pa_decode_set_path", library().pa_decode_set_path(int(path)))
 
 
 # -------------------------------------------------------- continuous batching

@@ -666,6 +666,7 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
 
 
 int g_grid_limit = 0;
+int g_decode_path = 0;   // 0 automatic, 1 split-context kernel, 2 cluster kernel
 
 struct WsLayout {
   size_t counter_off, meta_off, ml_off, acc_off, total;
@@ -806,6 +807,23 @@ extern "C" int pa_decode_set_grid_limit(int max_ctas) {
   return PA_OK;
 }
 
+extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
+  if (num_seqs < 0 || !page_size_ok(block_tokens)) return PA_ERR_ARG;
+  if (block_tokens != kBs || g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
+  if (g_decode_path == PA_DECODE_CLUSTER) return PA_DECODE_CLUSTER;
+  DeviceInfo di;
+  const int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  return decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit) > 0 ? PA_DECODE_CLUSTER
+                                                                      : PA_DECODE_SPLIT;
+}
+
+extern "C" int pa_decode_set_path(int path) {
+  if (path < PA_DECODE_AUTO || path > PA_DECODE_CLUSTER) return PA_ERR_ARG;
+  g_decode_path = path;
+  return PA_OK;
+}
+
 namespace {
 
 template <int BT>
@@ -860,6 +878,17 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
     map_blocks = num_blocks;
   }
 
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // a batch whose (sequence, kv head) pairs all fit on the GPU at once runs
+  // one cluster per pair (16-token pages)
+  if (BT == kBs && g_decode_path != PA_DECODE_SPLIT) {
+    int c = decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit);
+    if (c == 0 && g_decode_path == PA_DECODE_CLUSTER) c = 1;
+    if (c > 0)
+      return launch_decode_pair(map, out, q, num_blocks, block_table, n_layers, max_blocks_per_seq,
+                                context_lens, num_seqs, layer, scale, err, c, st);
+  }
+
   DecodeParams prm;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
@@ -880,7 +909,6 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
   prm.cap_tokens = max_blocks_per_seq * BT;
   prm.qscale = scale * kLog2e;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(decode_split_kernel<BT>, dim3(G), dim3(kThreads), smem, st, map, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;

@@ -1,0 +1,586 @@
+// pa_decode_pair.cu -- decode step of PagedAttention for batches whose
+// (sequence, kv head) pairs fit on the GPU at once.
+//
+// Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "What is in
+// the box": one query token's attention over K/V stored in 16-token pages
+// found through block_table, online softmax, GQA_Q_TO_K_RATIO = 4.
+//
+// Design (GB300-first):
+//  * One thread-block cluster of c CTAs (c = 1, 2, 4 or 8) per (sequence, kv
+//    head).  The c CTAs cut the head's 16-token tiles into c equal ranges, so
+//    a small batch still puts every SM to work, and they combine their
+//    results through distributed shared memory: no split partials in global
+//    memory, no merge kernel, no prefix over the batch, no work counter.
+//  * A producer warp streams the range's tiles with TMA tensor copies, one
+//    4 KiB copy (K and V of the head, 16 tokens) per tile, 8 tiles per 32 KiB
+//    stage, 3 stages.  Eight consumer warps take one tile of each stage each
+//    and keep their own online-softmax state (the 4 q heads of the group are
+//    the M rows of m16n8k16 bf16 MMAs, as in the split-context kernel); at the
+//    end the 8 warp states are combined in shared memory, then the c CTA
+//    states in the cluster leader's shared memory.
+//  * Before the dependency wait the CTA reads its sequence's context length
+//    and first page ids as they are then and prefetches those tiles into L2.
+//    Right after the wait the first stages are fetched from those ids while
+//    the length and ids are read again; if either changed, the consumers drop
+//    what they accumulated (a reset stage) and the range is streamed again
+//    from the current values.  Nothing is written before that check.
+#include <cfloat>
+#include <climits>
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kPairWarps = 8;                              // consumer warps
+constexpr int kPairThreads = (kPairWarps + 1) * 32;        // + producer warp
+constexpr int kPairStages = 3;
+constexpr int kPairCtasPerSm = 2;
+constexpr int kSlotBytes = 2 * kBs * kHeadRowBytes;        // one tile of one head, K and V: 4 KiB
+constexpr int kPairStageBytes = kPairWarps * kSlotBytes;   // 32 KiB
+constexpr int kMaxCluster = 8;
+constexpr int kIdBatch = 32;                               // page ids read at a time (4 stages)
+constexpr int kPrefetchTiles = 24;                         // tiles prefetched before the wait
+static_assert(kPrefetchTiles <= kIdBatch, "prefetched tiles come from the first id batch");
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr int kReset = 1;   // consumers drop their state before this stage
+constexpr int kEnd = 2;     // no more tiles; the stage carries no data
+
+struct PairStage {
+  int j0;      // tile of slot 0
+  int n;       // slots holding a tile (slot w: tile j0 + w)
+  int last;    // the sequence's last tile
+  int tail;    // tokens in it (1..16)
+  int bad;     // bit w: slot w's page id was out of range (tile skipped)
+  int flags;
+};
+
+struct __align__(1024) PairSmem {
+  unsigned char kv[kPairStages][kPairStageBytes];
+  float part_o[kMaxCluster][kGqa][kD];   // cluster leader: each CTA's unnormalised result
+  float2 part_ml[kMaxCluster][kGqa];     // and its (m, l), m in the log2 domain
+  PairStage desc[kPairStages];
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
+  uint64_t parts_full;                   // cluster leader: every CTA's result has landed
+};
+
+struct PairParams {
+  __nv_bfloat16 *out;
+  const uint16_t *q;
+  const int32_t *block_table;
+  const int32_t *context_lens;
+  int32_t *err;
+  int num_blocks;
+  int n_layers;
+  int max_blocks;
+  int layer;
+  int cap_tokens;
+  float qscale;
+};
+
+__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t i;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(i));
+  return i;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+
+// Arrival on an mbarrier in another CTA of the cluster; orders this thread's
+// earlier writes before it at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (as mbar_wait) with cluster-scope acquire: the writes other
+// CTAs released with their arrivals are visible afterwards.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// L2 prefetch of one tile: the box of the tensor map at (head h, page blk).
+__device__ __forceinline__ void prefetch_tile_l2(const void *tmap, int h, int blk) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(0), "r"(h), "r"(0), "r"(0), "r"(blk)
+      : "memory");
+}
+
+// Tiles [t0, t1) of a head with nb tiles, for CTA `rank` of c.
+__device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int &t1) {
+  t0 = static_cast<int>(static_cast<long long>(nb) * rank / c);
+  t1 = static_cast<int>(static_cast<long long>(nb) * (rank + 1) / c);
+}
+
+// One stage: wait until it is free, write its descriptor, issue the copies
+// of tiles j0 .. j0+n-1 (lane w < n holds the page id of tile j0 + w).
+// Returns the slots whose page id is out of range, or -1 if the wait timed out.
+__device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *map, int stage,
+                                             uint32_t phase, int h, int j0, int n, int blk,
+                                             int last, int tail, int flags, int num_blocks,
+                                             int lane) {
+  int good = 1;
+  if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
+  good = __shfl_sync(0xffffffffu, good, 0);
+  if (!good) return -1;
+  const bool mine = lane < n;
+  const bool valid = mine && blk >= 0 && blk < num_blocks;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  const unsigned bad = __ballot_sync(0xffffffffu, mine && !valid);
+  if (lane == 0) {
+    PairStage d;
+    d.j0 = j0;
+    d.n = n;
+    d.last = last;
+    d.tail = tail;
+    d.bad = static_cast<int>(bad);
+    d.flags = flags;
+    sm.desc[stage] = d;
+    const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * kSlotBytes;
+    if (bytes) mbar_arrive_expect_tx(&sm.full[stage], bytes);
+    else mbar_arrive(&sm.full[stage]);
+  }
+  __syncwarp();
+  if (valid) tma_load_5d(sm.kv[stage] + lane * kSlotBytes, map, 0, h, 0, 0, blk, &sm.full[stage]);
+  return static_cast<int>(bad);
+}
+
+__global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, PairParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  PairSmem &sm = *reinterpret_cast<PairSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_rank());
+  const int pair = static_cast<int>(cluster_id());
+  const int s = pair / kHkv, h = pair % kHkv;
+  const int32_t *row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+
+  // ---- before the previous kernel on the stream has finished
+  if (tid == 0) {
+    prefetch_tensormap(&kv_map);
+    for (int st = 0; st < kPairStages; ++st) {
+      mbar_init(&sm.full[st], 1);
+      mbar_init(&sm.empty[st], kPairWarps);
+    }
+    mbar_init(&sm.parts_full, c * kPairWarps * 32);
+    fence_mbar_init();
+  }
+  // the speculative plan: this CTA's range under the context length as it
+  // reads now, and its first page ids; their tiles are prefetched into L2
+  int spec_ctx = 0, spec_t0 = 0, spec_t1 = 0, spec_blk = -1;
+  if (warp == kPairWarps) {
+    spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
+    tile_range((spec_ctx + kBs - 1) / kBs, rank, c, spec_t0, spec_t1);
+    // (the first 32 ids are kept for the first stages; the prefetches share
+    // the SM's TMA unit with the copies, so only the first 3 stages' worth)
+    const int j = spec_t0 + lane;
+    if (j < spec_t1) {
+      spec_blk = row[j];
+      if (lane < kPrefetchTiles && spec_blk >= 0 && spec_blk < p.num_blocks)
+        prefetch_tile_l2(&kv_map, h, spec_blk);
+    }
+  }
+  if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
+  else __syncthreads();
+  pdl_launch_dependents();
+  // everything read below may come from the previous kernel on the stream
+  pdl_wait_primary();
+
+  if (warp == kPairWarps) {
+    // ===================================================== producer warp ==
+    // current values, read now and checked against the speculative ones
+    // once the first stages are on their way
+    const int ctx_raw = p.context_lens[s];
+    const int blk_now = spec_t0 + lane < spec_t1 ? row[spec_t0 + lane] : -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
+    bool ok = true;
+    int bad_seen = 0;
+    const int spec_nb = (spec_ctx + kBs - 1) / kBs;
+    const int spec_stages = min(kPairStages, (spec_t1 - spec_t0 + kPairWarps - 1) / kPairWarps);
+    for (int e = 0; e < spec_stages && ok; ++e) {
+      const int j0 = spec_t0 + e * kPairWarps;
+      const int blk = __shfl_sync(0xffffffffu, spec_blk, (e * kPairWarps + lane) & 31);
+      const int bad = publish_stage(sm, &kv_map, stage, phase, h, j0, min(kPairWarps, spec_t1 - j0),
+                                    blk, spec_nb - 1, spec_ctx - (spec_nb - 1) * kBs, 0,
+                                    p.num_blocks, lane);
+      if (bad < 0) {
+        ok = false;
+        break;
+      }
+      bad_seen |= bad;
+      if (lane == 0) {
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      }
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    const int ctx = min(max(ctx_raw, 0), p.cap_tokens);
+    if (lane == 0 && rank == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
+      report(p.err, PA_DEV_CTX_RANGE);
+    const bool same = ctx == spec_ctx && __all_sync(0xffffffffu, blk_now == spec_blk);
+    const int nb = (ctx + kBs - 1) / kBs;
+    const int last = nb - 1, tail = ctx - (nb - 1) * kBs;
+    int t0 = spec_t0, t1 = spec_t1, j = spec_t0 + spec_stages * kPairWarps, base = spec_t0;
+    int ids = blk_now, flags = 0;
+    if (!same) {
+      // the plan moved: stream the current range from its start; the
+      // consumers drop what they accumulated from the speculative stages
+      tile_range(nb, rank, c, t0, t1);
+      j = base = t0;
+      ids = t0 + lane < t1 ? row[t0 + lane] : -1;
+      flags = kReset;
+    } else if (bad_seen && lane == 0) {
+      report(p.err, PA_DEV_BAD_BLOCK);
+    }
+    int ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+    while (ok && j < t1) {
+      if (j >= base + kIdBatch) {
+        base += kIdBatch;
+        ids = ids_next;
+        ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+      }
+      const int blk = __shfl_sync(0xffffffffu, ids, (j - base + lane) & 31);
+      const int bad = publish_stage(sm, &kv_map, stage, phase, h, j, min(kPairWarps, t1 - j), blk,
+                                    last, tail, flags, p.num_blocks, lane);
+      if (bad < 0) {
+        ok = false;
+        break;
+      }
+      if (bad && lane == 0) report(p.err, PA_DEV_BAD_BLOCK);
+      flags = 0;
+      if (lane == 0) {
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      }
+      j += kPairWarps;
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (lane == 0) {
+      if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
+        PairStage d;
+        d.j0 = 0;
+        d.n = 0;
+        d.last = -1;
+        d.tail = 0;
+        d.bad = 0;
+        d.flags = kEnd | flags;
+        sm.desc[stage] = d;
+        mbar_arrive(&sm.full[stage]);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      } else {
+        report(p.err, PA_DEV_TIMEOUT);
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int st = 0; st < kPairStages; ++st)
+        if ((issued >> st) & 1u)
+          if (!mbar_wait(&sm.full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ======================================================= consumer warps ==
+  const int w = warp;                    // slot of every stage this warp takes
+  const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
+  const int c2 = 2 * (lane & 3);         // fragment column pair
+  const bool real_row = r < kGqa;
+  const int lm_i = lane >> 3, lm_r = lane & 7;
+  uint32_t qa[4], qc[4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
+  if (real_row) {
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        p.q + (static_cast<size_t>(s) * kHq + h * kGqa + r) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
+      qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
+    }
+  }
+  float o[8][4];
+  float m = neg_inf(), l = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  int stage = 0;
+  uint32_t phase = 0;
+  bool timed_out = false;
+  while (true) {
+    if (!mbar_wait(&sm.full[stage], phase)) {
+      report(p.err, PA_DEV_TIMEOUT);
+      timed_out = true;
+      break;
+    }
+    const PairStage d = sm.desc[stage];
+    if (d.flags & kReset) {
+      m = neg_inf();
+      l = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    }
+    if (d.flags & kEnd) break;
+    if (w < d.n && !((d.bad >> w) & 1)) {
+      const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
+      unsigned char *tile = sm.kv[stage] + w * kSlotBytes;
+      const uint32_t ktile = smem_u32(tile);
+      const uint32_t vtile = ktile + kBs * kHeadRowBytes;
+      if (n_valid < kBs) {
+        // rows past the context may hold anything (NaN included): zero the V
+        // rows, the K rows are masked in the scores
+        uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
+        for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // ---- S = Q K^T for tokens 0..7 (s0) and 8..15 (s1)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int tok = (lm_i >> 1) * 8 + lm_r;
+        const int chunk = 2 * ks + (lm_i & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
+        mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
+      }
+      // ---- online softmax on row r, columns c2, c2+1, 8+c2, 9+c2
+      float x0 = (c2 < n_valid) ? s0[0] * p.qscale : neg_inf();
+      float x1 = (c2 + 1 < n_valid) ? s0[1] * p.qscale : neg_inf();
+      float x2 = (c2 + 8 < n_valid) ? s1[0] * p.qscale : neg_inf();
+      float x3 = (c2 + 9 < n_valid) ? s1[1] * p.qscale : neg_inf();
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - m_new);
+      const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
+      const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
+      const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
+      l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
+      m = m_new;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        o[t][0] *= alpha;
+        o[t][1] *= alpha;
+      }
+      // ---- O += P V, dims in 4 pairs of 8-dim tiles
+#pragma unroll
+      for (int dp = 0; dp < 4; ++dp) {
+        const int tok = (lm_i & 1) * 8 + lm_r;
+        const int chunk = 2 * dp + (lm_i >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
+        mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
+        mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    if (++stage == kPairStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+
+  // ---- the 8 warp states -> one CTA state.  Each warp parks its state in
+  // its own slot of stage 0: every copy has landed (the warp has waited on
+  // every stage up to the end), and no other warp reads that slot any more.
+  float lt = l;
+  lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+  lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+  {
+    float *my_o = reinterpret_cast<float *>(sm.kv[0] + w * kSlotBytes);   // [4 rows][64]
+    float2 *my_ml = reinterpret_cast<float2 *>(my_o + kGqa * kD);
+    if (real_row) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        *reinterpret_cast<float2 *>(my_o + r * kD + 8 * t + c2) = make_float2(o[t][0], o[t][1]);
+      if ((lane & 3) == 0) my_ml[r] = make_float2(timed_out ? neg_inf() : m, timed_out ? 0.f : lt);
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kPairWarps * 32) : "memory");
+  const int ct = tid;               // 0..255: row ct / 64, dim ct % 64
+  const int rr = ct >> 6, dd = ct & 63;
+  float M = neg_inf();
+#pragma unroll
+  for (int k = 0; k < kPairWarps; ++k) {
+    const float2 ml = reinterpret_cast<const float2 *>(
+        reinterpret_cast<const float *>(sm.kv[0] + k * kSlotBytes) + kGqa * kD)[rr];
+    M = fmaxf(M, ml.x);
+  }
+  float L = 0.f, O = 0.f;
+  if (M != neg_inf()) {
+#pragma unroll
+    for (int k = 0; k < kPairWarps; ++k) {
+      const float *ko = reinterpret_cast<const float *>(sm.kv[0] + k * kSlotBytes);
+      const float2 ml = reinterpret_cast<const float2 *>(ko + kGqa * kD)[rr];
+      const float sc = fast_exp2(ml.x - M);   // empty warp states carry m = -inf: weight 0
+      L = fmaf(ml.y, sc, L);
+      O = fmaf(ko[rr * kD + dd], sc, O);
+    }
+  }
+  __nv_bfloat16 *dst = p.out + (static_cast<size_t>(s) * kHq + h * kGqa + rr) * kD + dd;
+  if (c == 1) {
+    *dst = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    return;
+  }
+
+  // ---- the c CTA states -> the output, in the cluster leader's shared memory
+  st_cluster_f32(map_to_rank(&sm.part_o[rank][rr][dd], 0), O);
+  if (dd == 0) st_cluster_f32x2(map_to_rank(&sm.part_ml[rank][rr], 0), make_float2(M, L));
+  mbar_arrive_cluster(map_to_rank(&sm.parts_full, 0));
+  if (rank != 0) return;
+  if (!mbar_wait_cluster(&sm.parts_full, 0)) {
+    report(p.err, PA_DEV_TIMEOUT);
+    return;
+  }
+  float Mc = neg_inf();
+  for (int k = 0; k < c; ++k) Mc = fmaxf(Mc, sm.part_ml[k][rr].x);
+  float Lc = 0.f, Oc = 0.f;
+  if (Mc != neg_inf()) {
+    for (int k = 0; k < c; ++k) {
+      const float sc = fast_exp2(sm.part_ml[k][rr].x - Mc);
+      Lc = fmaf(sm.part_ml[k][rr].y, sc, Lc);
+      Oc = fmaf(sm.part_o[k][rr][dd], sc, Oc);
+    }
+  }
+  *dst = __float2bfloat16_rn(Lc > 0.f ? Oc / Lc : 0.f);
+}
+
+}  // namespace
+
+size_t decode_pair_smem_bytes() { return sizeof(PairSmem) + 1024; }
+
+int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas) {
+  const long long pairs = static_cast<long long>(num_seqs) * kHkv;
+  long long cap = static_cast<long long>(sm_count) * kPairCtasPerSm;
+  if (max_ctas > 0) cap = min(cap, static_cast<long long>(max_ctas));
+  if (pairs > cap) return 0;   // the pairs do not fit at once
+  int c = 1;
+  while (c < kMaxCluster && pairs * (2 * c) <= cap) c *= 2;
+  return c;
+}
+
+int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
+                       int num_blocks, const int32_t *block_table, int n_layers,
+                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                       int layer, float scale, int32_t *err, int cluster, cudaStream_t stream) {
+  if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return PA_ERR_ARG;
+  DeviceInfo di;
+  int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  static bool attr_done[64] = {};
+  const size_t smem = decode_pair_smem_bytes();
+  if (!attr_done[di.device]) {
+    if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_done[di.device] = true;
+  }
+  PairParams prm;
+  prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  prm.q = q;
+  prm.block_table = block_table;
+  prm.context_lens = context_lens;
+  prm.err = err;
+  prm.num_blocks = num_blocks;
+  prm.n_layers = n_layers;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.layer = layer;
+  prm.cap_tokens = max_blocks_per_seq * kBs;
+  prm.qscale = scale * kLog2e;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_seqs) * kHkv * cluster);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, decode_pair_kernel, map, prm) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace pa

@@ -40,6 +40,16 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
 // (or V rows) of one page, 2 KiB.
 int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 
+// Decode attention with one thread-block cluster per (sequence, kv head)
+// (pa_decode_pair.cu), for 16-token pages.  decode_pair_cluster: the cluster
+// size for a batch (1, 2, 4 or 8 CTAs per pair), or 0 when the pairs do not
+// all fit on the GPU at once (max_ctas > 0 caps the CTAs).
+int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas);
+int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
+                       int num_blocks, const int32_t *block_table, int n_layers,
+                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                       int layer, float scale, int32_t *err, int cluster, cudaStream_t stream);
+
 // Launch `kernel` with the programmatic-stream-serialization attribute, so it
 // may start while the previous kernel on the stream finishes; the kernel
 // itself must wait (griddepcontrol.wait) before reading that kernel's output.

@@ -47,6 +47,27 @@ def test_host_validation_without_a_device():
     assert lib.pa_decode_set_grid_limit(0) == 0
 
 
+def test_decode_path_switch_without_a_device():
+    """The kernel choice: only the three path values are accepted; pages
+    other than 16 tokens always take the split-context kernel; a forced path
+    is reported as is; a bad count or page size is refused."""
+    import paged_kv_cache_205_gb300 as pk
+    lib = pk.library()
+    assert lib.pa_decode_set_path(3) == -2 and lib.pa_decode_set_path(-1) == -2
+    try:
+        assert lib.pa_decode_kernel_for(-1, 16) == -2
+        assert lib.pa_decode_kernel_for(4, 12) == -2
+        assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_set_path(pk.PA_DECODE_SPLIT) == 0
+        assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_set_path(pk.PA_DECODE_CLUSTER) == 0
+        assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_CLUSTER
+        assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
+    finally:
+        assert lib.pa_decode_set_path(pk.PA_DECODE_AUTO) == 0
+
+
 def test_page_size_entry_points_refuse_other_sizes():
     """Only 8-, 16- and 32-token pages are built; anything else is refused
     before any CUDA call."""

@@ -21,11 +21,15 @@ def _pk():
     return pk
 
 
-@pytest.fixture(autouse=True)
-def _reset_grid():
+@pytest.fixture(autouse=True, params=["split", "cluster"])
+def decode_path(request):
+    """Every test runs on both decode kernels: the split-context kernel and
+    the one-cluster-per-(sequence, kv head) kernel."""
     pk = _pk()
     pk.pa_decode_set_grid_limit(0)
-    yield
+    pk.pa_decode_set_path(pk.PA_DECODE_SPLIT if request.param == "split" else pk.PA_DECODE_CLUSTER)
+    yield request.param
+    pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
     pk.pa_decode_set_grid_limit(0)
 
 
@@ -300,3 +304,21 @@ def test_large_batch_merge_shape(grid):
     out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, grid=grid)
     assert err == 0
     assert_attention_close(out, ref, f"160 sequences, grid {grid}")
+
+
+def test_automatic_kernel_choice(decode_path):
+    """Automatic choice: the cluster kernel while every (sequence, kv head)
+    pair fits at two CTAs per SM, the split-context kernel beyond; a grid
+    limit below the pair count also selects the split kernel."""
+    import torch
+    pk = _pk()
+    pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fit = (2 * sms) // 8
+    assert pk.pa_decode_kernel_for(1) == pk.PA_DECODE_CLUSTER
+    assert pk.pa_decode_kernel_for(fit) == pk.PA_DECODE_CLUSTER
+    assert pk.pa_decode_kernel_for(fit + 1) == pk.PA_DECODE_SPLIT
+    assert pk.pa_decode_kernel_for(16, 8) == pk.PA_DECODE_SPLIT
+    pk.pa_decode_set_grid_limit(64)
+    assert pk.pa_decode_kernel_for(8) == pk.PA_DECODE_CLUSTER
+    assert pk.pa_decode_kernel_for(9) == pk.PA_DECODE_SPLIT
