@@ -285,3 +285,78 @@ def test_whole_decode_step_captured_in_one_graph():
         gp, gb, gf, gc, ge = st.host()
         assert np.array_equal(gb, ref[1]) and gc == ref[3]
         _compare_pools(gp, ref[0])
+
+
+@pytest.mark.parametrize("path", ["split", "cluster"])
+def test_attention_right_after_appends_that_open_pages(path):
+    """Every sequence's new token opens a page, and each replay starts from
+    the table as it was before the appends.  The allocation kernel lets the
+    kernels after it start before it writes the new entries, so the
+    attention's reads before its dependency wait may see the old -1 entries
+    (the cluster kernel then streams its range again from the current
+    values).  Whatever those early reads saw, every replay matches the
+    oracle on both decode kernels."""
+    import torch
+    pk = _pk()
+    pk.pa_decode_set_path(pk.PA_DECODE_SPLIT if path == "split" else pk.PA_DECODE_CLUSTER)
+    try:
+        ctx = np.array([16, 32, 48, 64, 96, 128, 160, 192, 256, 320, 384, 512], dtype=np.int32)
+        n, L = len(ctx), 2
+        mb = int(ctx.max()) // 16 + 2
+        nbk = int(((ctx + 16) // 16).sum()) * L + 16
+        rng = np.random.default_rng(21)
+        w = wl.make_workload("tiny", seed=21, context_lens=ctx, n_layers=L, num_blocks=nbk,
+                             max_blocks_per_seq=mb)
+        pool = wl.make_pool_numpy(w, rng, poison=True)
+        st = DevState(pool, w.block_table, w.free_list, w.free_count)
+        k = wl.normal_bf16(rng, (L, n, N_KV, D))
+        v = wl.normal_bf16(rng, (L, n, N_KV, D))
+        q = wl.normal_bf16(rng, (L, n, N_Q, D))
+        kd, vd, q_in = dev_bf16(k), dev_bf16(v), dev_bf16(q)
+        qd = q_in.clone()
+        bt0, fc0 = st.bt.clone(), st.fc.clone()
+        ctxd, ctx1 = dev_i32(ctx), dev_i32(ctx + 1)
+        out = torch.zeros((L, n, N_Q, D), dtype=torch.bfloat16, device="cuda")
+        ws = workspace_for(n, mb)
+
+        def step():
+            st.bt.copy_(bt0)          # the new pages' entries are -1 again
+            st.fc.copy_(fc0)
+            qd.copy_(q_in)
+            for l in range(L):
+                pk.pa_kv_append_rope(kd[l], vd[l], qd[l], st.pool, st.bt, ctxd, l, st.fl, st.fc,
+                                     st.err)
+                pk.pa_decode_attention(out[l], qd[l], st.pool, st.bt, ctx1, l, w.scale, ws, st.err)
+
+        step()
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                step()
+        torch.cuda.current_stream().wait_stream(side)
+
+        ref = (pool, w.block_table, w.free_list, w.free_count)
+        outs = []
+        for l in range(L):
+            q2, p2, b2, f2, c2, e = oracle.kv_append_rope(k[l], v[l], q[l], ref[0], ref[1], ctx, l,
+                                                          ref[2], ref[3])
+            assert e == 0
+            ref = (p2, b2, f2, c2)
+            o_ref, e = oracle.decode_attention(q2, p2, b2, ctx + 1, l)
+            assert e == 0
+            outs.append(o_ref)
+        assert np.all(ref[1][np.arange(n), :, ctx // 16] >= 0)   # every sequence opened a page
+        for rep in range(8):
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert int(st.err.item()) == 0
+            for l in range(L):
+                assert_attention_close(host_f64(out[l]), outs[l], f"replay {rep} layer {l}")
+            gp, gb, gf, gc, ge = st.host()
+            assert np.array_equal(gb, ref[1]) and gc == ref[3]
+    finally:
+        pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
