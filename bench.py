@@ -384,10 +384,12 @@ def run_gpu(args, rank, world, dist):
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
     st.pk.pa_decode_set_grid_limit(args.grid)
     st.pk.pa_decode_set_path({"auto": st.pk.PA_DECODE_AUTO, "split": st.pk.PA_DECODE_SPLIT,
-                              "cluster": st.pk.PA_DECODE_CLUSTER}[args.decode_kernel])
+                              "cluster": st.pk.PA_DECODE_CLUSTER,
+                              "seq": st.pk.PA_DECODE_SEQ}[args.decode_kernel])
     # which decode kernel the library runs for this batch: one cluster per
     # (sequence, kv head), or split-context chunks + a merge kernel
-    cluster = st.pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens) == st.pk.PA_DECODE_CLUSTER
+    kern = st.pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens)
+    cluster = kern in (st.pk.PA_DECODE_CLUSTER, st.pk.PA_DECODE_SEQ)
     st.launches_per_step = attn_launches(cluster) * w.n_layers + (2 * w.n_layers if w.append else 0)
     L, n = w.n_layers, w.num_seqs
 
@@ -548,7 +550,7 @@ def run_gpu(args, rank, world, dist):
             "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
             "decode_grid_cap": args.grid,
-            "decode_kernel": "cluster" if cluster else "split",
+            "decode_kernel": {1: "split", 2: "cluster", 3: "seq"}.get(kern, str(kern)),
             "block_tokens": w.block_tokens,
             "page_fill": page_fill,
         },
@@ -1274,7 +1276,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--block-tokens", type=int, default=BS, choices=[8, 16, 32],
                     help="decode path: tokens per page (the page size as a tunable)")
-    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "split", "cluster"],
+    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "split", "cluster", "seq"],
                     help="decode-attention kernel (pa_decode_set_path): automatic choice, the "
                          "split-context kernel, or one cluster per (sequence, kv head)")
     ap.add_argument("--grid", type=int, default=0,

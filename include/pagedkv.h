@@ -403,26 +403,35 @@ int pa_decode_set_grid_limit(int max_ctas);
 
 /*
  * Which decode-attention kernel pa_decode_attention runs (process-wide).
- * Both compute the same attention and differ only in rounding order.
- *   PA_DECODE_AUTO     the cluster kernel when every (sequence, kv head)
- *                      pair of the call fits on the GPU at once (num_seqs *
- *                      8 <= 2 CTAs per SM, within the grid limit) and pages
- *                      hold 16 tokens; the split-context kernel otherwise.
+ * All compute the same attention and differ only in rounding order.
+ *   PA_DECODE_AUTO     the per-head cluster kernel when every (sequence, kv
+ *                      head) pair of the call gets at least two CTAs at once
+ *                      (num_seqs * 16 <= 2 CTAs per SM, within the grid
+ *                      limit) and pages hold 16 tokens; the split-context
+ *                      kernel otherwise.
  *   PA_DECODE_SPLIT    always the split-context kernel: the batch's blocks
  *                      laid end to end and cut into chunks over all CTAs,
- *                      fp32 partials merged by a second kernel.
- *   PA_DECODE_CLUSTER  the cluster kernel (16-token pages; other page sizes
- *                      use the split-context kernel): one thread-block
- *                      cluster of 1, 2, 4 or 8 CTAs per (sequence, kv head),
- *                      its CTAs combined in shared memory; no workspace use.
- * Returns PA_ERR_ARG for any other value.
+ *                      fp32 partials merged by a second kernel.  Balances any
+ *                      mix of context lengths.
+ *   PA_DECODE_CLUSTER  the per-head cluster kernel: one thread-block cluster
+ *                      of 1, 2, 4 or 8 CTAs per (sequence, kv head), its CTAs
+ *                      combined in shared memory; no workspace use.
+ *   PA_DECODE_SEQ      the per-sequence cluster kernel: one cluster of 1 to
+ *                      16 CTAs per sequence, one 32 KiB copy per page, each
+ *                      CTA combining the q heads it owns; no workspace use.
+ *                      Fastest when the batch's contexts are of similar
+ *                      length; slow when a few contexts are much longer
+ *                      than the rest (their clusters finish last).
+ * The cluster kernels need 16-token pages; with other page sizes every path
+ * runs the split-context kernel.  Returns PA_ERR_ARG for any other value.
  */
 #define PA_DECODE_AUTO     0
 #define PA_DECODE_SPLIT    1
 #define PA_DECODE_CLUSTER  2
+#define PA_DECODE_SEQ      3
 int pa_decode_set_path(int path);
 
-/* The kernel (PA_DECODE_SPLIT or PA_DECODE_CLUSTER) that pa_decode_attention
+/* The kernel (PA_DECODE_SPLIT, _CLUSTER or _SEQ) that pa_decode_attention
  * (block_tokens 16) or pa_decode_attention_bt would run for num_seqs
  * sequences on the current device under the current path and grid limit;
  * PA_ERR_ARG for a bad count or page size, PA_ERR_CUDA / PA_ERR_DEVICE when

@@ -36,6 +36,7 @@ from ._binding import (  # noqa: F401
     PA_DECODE_AUTO,
     PA_DECODE_SPLIT,
     PA_DECODE_CLUSTER,
+    PA_DECODE_SEQ,
     pa_decode_workspace_size,
     pa_error_string,
     pa_free,

@@ -324,7 +324,7 @@ def pa_decode_set_grid_limit(max_ctas: int) -> None:
     _check("pa_decode_set_grid_limit", library().pa_decode_set_grid_limit(int(max_ctas)))
 
 
-PA_DECODE_AUTO, PA_DECODE_SPLIT, PA_DECODE_CLUSTER = 0, 1, 2
+PA_DECODE_AUTO, PA_DECODE_SPLIT, PA_DECODE_CLUSTER, PA_DECODE_SEQ = 0, 1, 2, 3
 
 
 def pa_decode_kernel_for(num_seqs: int, block_tokens: int = PA_BLOCK_TOKENS) -> int:

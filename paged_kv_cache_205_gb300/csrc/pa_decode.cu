@@ -740,6 +740,21 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_kv_page_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  // the token dimension comes before the head dimension although its stride
+  // is the larger one: the copy then writes each head's token rows together
+  const cuuint64_t dims[5] = {kD, kBs, kHkv, 2, static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kTokRowBytes, kHeadRowBytes, kHalfBlockBytes, kBlockBytes};
+  const cuuint32_t box[5] = {kD, kBs, kHkv, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
@@ -810,7 +825,7 @@ extern "C" int pa_decode_set_grid_limit(int max_ctas) {
 extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
   if (num_seqs < 0 || !page_size_ok(block_tokens)) return PA_ERR_ARG;
   if (block_tokens != kBs || g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
-  if (g_decode_path == PA_DECODE_CLUSTER) return PA_DECODE_CLUSTER;
+  if (g_decode_path == PA_DECODE_CLUSTER || g_decode_path == PA_DECODE_SEQ) return g_decode_path;
   DeviceInfo di;
   const int rc = current_device(&di);
   if (rc != PA_OK) return rc;
@@ -819,7 +834,7 @@ extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
 }
 
 extern "C" int pa_decode_set_path(int path) {
-  if (path < PA_DECODE_AUTO || path > PA_DECODE_CLUSTER) return PA_ERR_ARG;
+  if (path < PA_DECODE_AUTO || path > PA_DECODE_SEQ) return PA_ERR_ARG;
   g_decode_path = path;
   return PA_OK;
 }
@@ -881,6 +896,21 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // a batch whose (sequence, kv head) pairs all fit on the GPU at once runs
   // one cluster per pair (16-token pages)
+  if (BT == kBs && g_decode_path == PA_DECODE_SEQ) {
+    static thread_local const void *pmap_pool = nullptr;
+    static thread_local int pmap_blocks = 0;
+    alignas(64) static thread_local CUtensorMap pmap;
+    if (pmap_pool != kv_cache || pmap_blocks != num_blocks) {
+      rc = make_kv_page_map(&pmap, kv_cache, num_blocks);
+      if (rc != PA_OK) return rc;
+      pmap_pool = kv_cache;
+      pmap_blocks = num_blocks;
+    }
+    int c = decode_seq_cluster(num_seqs, di.sm_count, g_grid_limit);
+    if (c == 0) c = 1;
+    return launch_decode_seq(pmap, out, q, kv_cache, num_blocks, block_table, n_layers,
+                             max_blocks_per_seq, context_lens, num_seqs, layer, scale, err, c, st);
+  }
   if (BT == kBs && g_decode_path != PA_DECODE_SPLIT) {
     int c = decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit);
     if (c == 0 && g_decode_path == PA_DECODE_CLUSTER) c = 1;

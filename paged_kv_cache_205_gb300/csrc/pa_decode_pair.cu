@@ -69,6 +69,7 @@ struct __align__(1024) PairSmem {
 };
 
 struct PairParams {
+  const unsigned char *kv;   // the pool (L2 prefetches; copies go through the tensor map)
   __nv_bfloat16 *out;
   const uint16_t *q;
   const int32_t *block_table;
@@ -522,16 +523,400 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   *dst = __float2bfloat16_rn(Lc > 0.f ? Oc / Lc : 0.f);
 }
 
+// ===========================================================================
+// One cluster of c CTAs (c = 1 .. 16) per sequence.  A CTA streams a range
+// of the sequence's pages, one 32 KiB copy per page (all 8 kv heads, through
+// the page tensor map: [K|V][head][token][64] in shared memory, each head's
+// token rows 128-byte swizzled), and warp h computes kv head h.  CTA r owns
+// q heads [r * 32/c, (r + 1) * 32/c): every CTA sends its state for those
+// heads to their owner's shared memory, and the owner combines and writes.
+constexpr int kSeqPrefetchPages = 4;
+constexpr int kBadPage = 4;   // the stage's page id was out of range (no data)
+
+struct SeqStage {
+  int j;       // tile (page) of the sequence
+  int last;    // the sequence's last tile
+  int tail;    // tokens in it (1..16)
+  int flags;   // kReset, kEnd, kBadPage
+};
+
+struct __align__(1024) SeqSmem {
+  unsigned char kv[kPairStages][kPairStageBytes];
+  float part_o[kHq][kD];     // owner: row (sender rank * 32/c + owned head) -> unnormalised state
+  float2 part_ml[kHq];       // and its (m, l)
+  SeqStage desc[kPairStages];
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
+  uint64_t parts_full;       // owner: every sender's states have landed
+};
+
+// One page into a stage (lane 0 of the producer warp).  False if the wait
+// for the stage timed out.
+__device__ __forceinline__ bool publish_page(SeqSmem &sm, const CUtensorMap *map, int stage,
+                                             uint32_t phase, int j, int blk, int last, int tail,
+                                             int flags, int num_blocks) {
+  if (!mbar_wait(&sm.empty[stage], phase ^ 1)) return false;
+  const bool valid = blk >= 0 && blk < num_blocks;
+  SeqStage d;
+  d.j = j;
+  d.last = last;
+  d.tail = tail;
+  d.flags = flags | (valid ? 0 : kBadPage);
+  sm.desc[stage] = d;
+  if (valid) {
+    mbar_arrive_expect_tx(&sm.full[stage], kPairStageBytes);
+    tma_load_5d(sm.kv[stage], map, 0, 0, 0, 0, blk, &sm.full[stage]);
+  } else {
+    mbar_arrive(&sm.full[stage]);
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
+    decode_seq_kernel(const __grid_constant__ CUtensorMap page_map, PairParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  SeqSmem &sm = *reinterpret_cast<SeqSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_rank());
+  const int s = static_cast<int>(cluster_id());
+  const int qpo = kHq / c;   // q heads each CTA owns
+  const int32_t *row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+
+  // ---- before the previous kernel on the stream has finished
+  if (tid == 0) {
+    prefetch_tensormap(&page_map);
+    for (int st = 0; st < kPairStages; ++st) {
+      mbar_init(&sm.full[st], 1);
+      mbar_init(&sm.empty[st], kPairWarps);
+    }
+    mbar_init(&sm.parts_full, c * qpo * 4);   // per sender and owned head: one lane quad
+    fence_mbar_init();
+  }
+  int spec_ctx = 0, spec_t0 = 0, spec_t1 = 0, spec_blk = -1;
+  if (warp == kPairWarps) {
+    spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
+    tile_range((spec_ctx + kBs - 1) / kBs, rank, c, spec_t0, spec_t1);
+    const int j = spec_t0 + lane;
+    if (j < spec_t1) {
+      spec_blk = row[j];
+      if (lane < kSeqPrefetchPages && spec_blk >= 0 && spec_blk < p.num_blocks)
+        prefetch_bulk_l2(p.kv + static_cast<size_t>(spec_blk) * kBlockBytes, kBlockBytes);
+    }
+  }
+  if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
+  else __syncthreads();
+  pdl_launch_dependents();
+  // everything read below may come from the previous kernel on the stream
+  pdl_wait_primary();
+
+  if (warp == kPairWarps) {
+    // ===================================================== producer warp ==
+    const int ctx_raw = p.context_lens[s];
+    const int blk_now = spec_t0 + lane < spec_t1 ? row[spec_t0 + lane] : -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;
+    bool ok = true;
+    const int spec_nb = (spec_ctx + kBs - 1) / kBs;
+    const int spec_pages = min(kPairStages, spec_t1 - spec_t0);
+    bool spec_bad_page = false;
+    for (int e = 0; e < spec_pages; ++e) {
+      const int blk = __shfl_sync(0xffffffffu, spec_blk, e);
+      spec_bad_page |= !(blk >= 0 && blk < p.num_blocks);
+      int good = 1;
+      if (lane == 0)
+        good = publish_page(sm, &page_map, stage, phase, spec_t0 + e, blk, spec_nb - 1,
+                            spec_ctx - (spec_nb - 1) * kBs, 0, p.num_blocks);
+      if (!__shfl_sync(0xffffffffu, good, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      }
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    const int ctx = min(max(ctx_raw, 0), p.cap_tokens);
+    if (lane == 0 && rank == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
+      report(p.err, PA_DEV_CTX_RANGE);
+    const bool same = ctx == spec_ctx && __all_sync(0xffffffffu, blk_now == spec_blk);
+    const int nb = (ctx + kBs - 1) / kBs;
+    const int last = nb - 1, tail = ctx - (nb - 1) * kBs;
+    int t0 = spec_t0, t1 = spec_t1, j = spec_t0 + spec_pages, base = spec_t0;
+    int ids = blk_now, flags = 0;
+    if (!same) {
+      tile_range(nb, rank, c, t0, t1);
+      j = base = t0;
+      ids = t0 + lane < t1 ? row[t0 + lane] : -1;
+      flags = kReset;
+    } else if (spec_bad_page && lane == 0) {
+      report(p.err, PA_DEV_BAD_BLOCK);
+    }
+    int ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+    while (ok && j < t1) {
+      if (j >= base + kIdBatch) {
+        base += kIdBatch;
+        ids = ids_next;
+        ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+      }
+      const int blk = __shfl_sync(0xffffffffu, ids, (j - base) & 31);
+      int good = 1;
+      if (lane == 0) {
+        good = publish_page(sm, &page_map, stage, phase, j, blk, last, tail, flags, p.num_blocks);
+        if (good && !(blk >= 0 && blk < p.num_blocks)) report(p.err, PA_DEV_BAD_BLOCK);
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) {
+        ok = false;
+        break;
+      }
+      flags = 0;
+      if (lane == 0) {
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      }
+      ++j;
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (lane == 0) {
+      if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
+        SeqStage d;
+        d.j = 0;
+        d.last = -1;
+        d.tail = 0;
+        d.flags = kEnd | flags;
+        sm.desc[stage] = d;
+        mbar_arrive(&sm.full[stage]);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      } else {
+        report(p.err, PA_DEV_TIMEOUT);
+      }
+      for (int st = 0; st < kPairStages; ++st)
+        if ((issued >> st) & 1u)
+          if (!mbar_wait(&sm.full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ======================================================= consumer warps ==
+  const int h = warp;                    // kv head
+  const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
+  const int c2 = 2 * (lane & 3);
+  const bool real_row = r < kGqa;
+  const int lm_i = lane >> 3, lm_r = lane & 7;
+  uint32_t qa[4], qc[4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
+  if (real_row) {
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        p.q + (static_cast<size_t>(s) * kHq + h * kGqa + r) * kD);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
+      qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
+    }
+  }
+  float o[8][4];
+  float m = neg_inf(), l = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  int stage = 0;
+  uint32_t phase = 0;
+  bool timed_out = false;
+  while (true) {
+    if (!mbar_wait(&sm.full[stage], phase)) {
+      report(p.err, PA_DEV_TIMEOUT);
+      timed_out = true;
+      break;
+    }
+    const SeqStage d = sm.desc[stage];
+    if (d.flags & kReset) {
+      m = neg_inf();
+      l = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    }
+    if (d.flags & kEnd) break;
+    if (!(d.flags & kBadPage)) {
+      const int n_valid = (d.j == d.last) ? d.tail : kBs;
+      unsigned char *ktp = sm.kv[stage] + h * (kBs * kHeadRowBytes);
+      unsigned char *vtp = ktp + kPairStageBytes / 2;
+      const uint32_t ktile = smem_u32(ktp);
+      const uint32_t vtile = smem_u32(vtp);
+      if (n_valid < kBs) {
+        uint4 *vrow = reinterpret_cast<uint4 *>(vtp);
+        for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int tok = (lm_i >> 1) * 8 + lm_r;
+        const int chunk = 2 * ks + (lm_i & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
+        mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
+      }
+      float x0 = (c2 < n_valid) ? s0[0] * p.qscale : neg_inf();
+      float x1 = (c2 + 1 < n_valid) ? s0[1] * p.qscale : neg_inf();
+      float x2 = (c2 + 8 < n_valid) ? s1[0] * p.qscale : neg_inf();
+      float x3 = (c2 + 9 < n_valid) ? s1[1] * p.qscale : neg_inf();
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - m_new);
+      const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
+      const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
+      const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
+      l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
+      m = m_new;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        o[t][0] *= alpha;
+        o[t][1] *= alpha;
+      }
+#pragma unroll
+      for (int dp = 0; dp < 4; ++dp) {
+        const int tok = (lm_i & 1) * 8 + lm_r;
+        const int chunk = 2 * dp + (lm_i >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
+        mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
+        mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    if (++stage == kPairStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+
+  // ---- each q head's state to the CTA that owns it
+  float lt = l;
+  lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+  lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+  if (real_row) {
+    const int qh = h * kGqa + r;
+    const int owner = qh / qpo, slot = rank * qpo + qh % qpo;
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      st_cluster_f32x2(map_to_rank(&sm.part_o[slot][8 * t + c2], owner), make_float2(o[t][0], o[t][1]));
+    if ((lane & 3) == 0)
+      st_cluster_f32x2(map_to_rank(&sm.part_ml[slot], owner),
+                       make_float2(timed_out ? neg_inf() : m, timed_out ? 0.f : lt));
+    mbar_arrive_cluster(map_to_rank(&sm.parts_full, owner));
+  }
+  if (!mbar_wait_cluster(&sm.parts_full, 0)) {
+    report(p.err, PA_DEV_TIMEOUT);
+    return;
+  }
+  for (int e = tid; e < qpo * kD; e += kPairWarps * 32) {
+    const int oh = e / kD, dd = e % kD;   // owned head, dim
+    float M = neg_inf();
+    for (int k = 0; k < c; ++k) M = fmaxf(M, sm.part_ml[k * qpo + oh].x);
+    float L = 0.f, O = 0.f;
+    if (M != neg_inf()) {
+      for (int k = 0; k < c; ++k) {
+        const float2 ml = sm.part_ml[k * qpo + oh];
+        const float sc = fast_exp2(ml.x - M);
+        L = fmaf(ml.y, sc, L);
+        O = fmaf(sm.part_o[k * qpo + oh][dd], sc, O);
+      }
+    }
+    p.out[(static_cast<size_t>(s) * kHq + rank * qpo + oh) * kD + dd] =
+        __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+  }
+}
+
 }  // namespace
 
 size_t decode_pair_smem_bytes() { return sizeof(PairSmem) + 1024; }
+
+int decode_seq_cluster(int num_seqs, int sm_count, int max_ctas) {
+  long long cap = static_cast<long long>(sm_count) * kPairCtasPerSm;
+  if (max_ctas > 0) cap = min(cap, static_cast<long long>(max_ctas));
+  if (num_seqs <= 0 || num_seqs > cap) return 0;
+  int c = 1;
+  while (c < 16 && static_cast<long long>(num_seqs) * (2 * c) <= cap) c *= 2;
+  return c;
+}
+
+int launch_decode_seq(const CUtensorMap &page_map, uint16_t *out, const uint16_t *q,
+                      const void *kv_cache, int num_blocks, const int32_t *block_table,
+                      int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                      int num_seqs, int layer, float scale, int32_t *err, int cluster,
+                      cudaStream_t stream) {
+  if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8 && cluster != 16)
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  static bool attr_done[64] = {};
+  const size_t smem = sizeof(SeqSmem) + 1024;
+  if (!attr_done[di.device]) {
+    if (cudaFuncSetAttribute(decode_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_seq_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_done[di.device] = true;
+  }
+  PairParams prm;
+  prm.kv = static_cast<const unsigned char *>(kv_cache);
+  prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  prm.q = q;
+  prm.block_table = block_table;
+  prm.context_lens = context_lens;
+  prm.err = err;
+  prm.num_blocks = num_blocks;
+  prm.n_layers = n_layers;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.layer = layer;
+  prm.cap_tokens = max_blocks_per_seq * kBs;
+  prm.qscale = scale * kLog2e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_seqs) * cluster);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, decode_seq_kernel, page_map, prm) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
 
 int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas) {
   const long long pairs = static_cast<long long>(num_seqs) * kHkv;
   long long cap = static_cast<long long>(sm_count) * kPairCtasPerSm;
   if (max_ctas > 0) cap = min(cap, static_cast<long long>(max_ctas));
-  if (pairs > cap) return 0;   // the pairs do not fit at once
-  int c = 1;
+  // at least two CTAs per pair: with one, a batch of uneven contexts leaves
+  // its longest heads on single CTAs and the split-context kernel is faster
+  if (pairs * 2 > cap) return 0;
+  int c = 2;
   while (c < kMaxCluster && pairs * (2 * c) <= cap) c *= 2;
   return c;
 }
@@ -553,6 +938,7 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
     attr_done[di.device] = true;
   }
   PairParams prm;
+  prm.kv = nullptr;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.q = q;
   prm.block_table = block_table;

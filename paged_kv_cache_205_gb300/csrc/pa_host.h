@@ -45,6 +45,18 @@ int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 // size for a batch (1, 2, 4 or 8 CTAs per pair), or 0 when the pairs do not
 // all fit on the GPU at once (max_ctas > 0 caps the CTAs).
 int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas);
+// One cluster per sequence (pa_decode_pair.cu): cluster size 1..16 for a
+// batch (0: more sequences than CTAs), and the launch over a page map.
+int decode_seq_cluster(int num_seqs, int sm_count, int max_ctas);
+int launch_decode_seq(const CUtensorMap &page_map, uint16_t *out, const uint16_t *q,
+                      const void *kv_cache, int num_blocks, const int32_t *block_table,
+                      int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                      int num_seqs, int layer, float scale, int32_t *err, int cluster,
+                      cudaStream_t stream);
+// Tensor map over a pool of 16-token pages whose box is one whole page:
+// dims (d 64, token 16, kv head 8, K|V 2, page), so that shared memory holds
+// [K|V][head][token][64] with each head's 16 token rows 128-byte swizzled.
+int make_kv_page_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
                        int num_blocks, const int32_t *block_table, int n_layers,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,

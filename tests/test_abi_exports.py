@@ -53,7 +53,7 @@ def test_decode_path_switch_without_a_device():
     is reported as is; a bad count or page size is refused."""
     import paged_kv_cache_205_gb300 as pk
     lib = pk.library()
-    assert lib.pa_decode_set_path(3) == -2 and lib.pa_decode_set_path(-1) == -2
+    assert lib.pa_decode_set_path(4) == -2 and lib.pa_decode_set_path(-1) == -2
     try:
         assert lib.pa_decode_kernel_for(-1, 16) == -2
         assert lib.pa_decode_kernel_for(4, 12) == -2

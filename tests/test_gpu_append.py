@@ -287,7 +287,7 @@ def test_whole_decode_step_captured_in_one_graph():
         _compare_pools(gp, ref[0])
 
 
-@pytest.mark.parametrize("path", ["split", "cluster"])
+@pytest.mark.parametrize("path", ["split", "cluster", "seq"])
 def test_attention_right_after_appends_that_open_pages(path):
     """Every sequence's new token opens a page, and each replay starts from
     the table as it was before the appends.  The allocation kernel lets the
@@ -298,7 +298,8 @@ def test_attention_right_after_appends_that_open_pages(path):
     oracle on both decode kernels."""
     import torch
     pk = _pk()
-    pk.pa_decode_set_path(pk.PA_DECODE_SPLIT if path == "split" else pk.PA_DECODE_CLUSTER)
+    pk.pa_decode_set_path({"split": pk.PA_DECODE_SPLIT, "cluster": pk.PA_DECODE_CLUSTER,
+                           "seq": pk.PA_DECODE_SEQ}[path])
     try:
         ctx = np.array([16, 32, 48, 64, 96, 128, 160, 192, 256, 320, 384, 512], dtype=np.int32)
         n, L = len(ctx), 2

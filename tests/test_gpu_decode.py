@@ -21,13 +21,14 @@ def _pk():
     return pk
 
 
-@pytest.fixture(autouse=True, params=["split", "cluster"])
+@pytest.fixture(autouse=True, params=["split", "cluster", "seq"])
 def decode_path(request):
-    """Every test runs on both decode kernels: the split-context kernel and
-    the one-cluster-per-(sequence, kv head) kernel."""
+    """Every test runs on each decode kernel: the split-context kernel, one
+    cluster per (sequence, kv head), one cluster per sequence."""
     pk = _pk()
     pk.pa_decode_set_grid_limit(0)
-    pk.pa_decode_set_path(pk.PA_DECODE_SPLIT if request.param == "split" else pk.PA_DECODE_CLUSTER)
+    pk.pa_decode_set_path({"split": pk.PA_DECODE_SPLIT, "cluster": pk.PA_DECODE_CLUSTER,
+                           "seq": pk.PA_DECODE_SEQ}[request.param])
     yield request.param
     pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
     pk.pa_decode_set_grid_limit(0)
@@ -307,18 +308,21 @@ def test_large_batch_merge_shape(grid):
 
 
 def test_automatic_kernel_choice(decode_path):
-    """Automatic choice: the cluster kernel while every (sequence, kv head)
-    pair fits at two CTAs per SM, the split-context kernel beyond; a grid
-    limit below the pair count also selects the split kernel."""
+    """Automatic choice: the per-head cluster kernel while every (sequence,
+    kv head) pair gets two CTAs (two CTAs per SM in all), the split-context
+    kernel beyond; a grid limit lowers the bound; other page sizes always
+    take the split kernel; a forced path is reported as forced."""
     import torch
     pk = _pk()
     pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    fit = (2 * sms) // 8
+    fit = (2 * sms) // 16
     assert pk.pa_decode_kernel_for(1) == pk.PA_DECODE_CLUSTER
     assert pk.pa_decode_kernel_for(fit) == pk.PA_DECODE_CLUSTER
     assert pk.pa_decode_kernel_for(fit + 1) == pk.PA_DECODE_SPLIT
     assert pk.pa_decode_kernel_for(16, 8) == pk.PA_DECODE_SPLIT
     pk.pa_decode_set_grid_limit(64)
-    assert pk.pa_decode_kernel_for(8) == pk.PA_DECODE_CLUSTER
-    assert pk.pa_decode_kernel_for(9) == pk.PA_DECODE_SPLIT
+    assert pk.pa_decode_kernel_for(4) == pk.PA_DECODE_CLUSTER
+    assert pk.pa_decode_kernel_for(5) == pk.PA_DECODE_SPLIT
+    pk.pa_decode_set_path(pk.PA_DECODE_SEQ)
+    assert pk.pa_decode_kernel_for(300) == pk.PA_DECODE_SEQ
