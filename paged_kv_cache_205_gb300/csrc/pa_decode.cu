@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 
+#include "pa_decode_tile.cuh"
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -99,14 +100,6 @@ struct DecodeParams {
   int cap_tokens;      // max_blocks * tokens per page: the largest context
   float qscale;        // scale * log2(e), applied to the fp32 scores
 };
-
-__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ int clamped_ctx(const DecodeParams &p, int s) {
   const int t = p.context_lens[s];
@@ -442,18 +435,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
     const int c2 = 2 * (lane & 3);         // fragment column pair
     const bool real_row = r < kGqa;
-    // ldmatrix row addresses: matrix lm_i = lane / 8 takes row lm_r = lane % 8;
-    // the 16-byte chunk c of token row t sits at c ^ (t & 7)
-    const int lm_i = lane >> 3, lm_r = lane & 7;
-    uint32_t qa[4], qc[4];                 // Q fragments: row r, cols 16ks + c2 (qa), + 8 (qc)
-    float o[8][4];                         // O fragments, 8 tiles of 8 dims
-    float m = neg_inf(), l = 0.f;
-    int stage = 0;
-    uint32_t phase = 0;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    uint32_t qa[4], qc[4];                 // Q fragments of the current sequence
+    TileState ts;
+    ts.reset();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
+    int stage = 0;
+    uint32_t phase = 0;
     while (true) {
       if (!mbar_wait(&sm.full[stage], phase)) {
         report(p.err, PA_DEV_TIMEOUT);
@@ -462,99 +450,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const StageDesc d = sm.desc[stage];
       if (d.flags & kEndOfWork) break;
       if (d.flags & kSegStart) {
-        if (real_row) {
-          const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-              p.q + (static_cast<size_t>(d.seq) * kHq + g * kGqa + r) * kD);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
-            qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
-          }
-        }
-        m = neg_inf();
-        l = 0.f;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+        load_q_fragments(p.q + static_cast<size_t>(d.seq) * kHq * kD, g, lane, qa, qc);
+        ts.reset();
       }
       const int n_valid = d.n_valid;
       if (n_valid > 0) {
-        unsigned char *tile = sm.kv[stage] + g * kHeadTileBytes;
-        const uint32_t ktile = smem_u32(tile);
+        const uint32_t ktile = smem_u32(sm.kv[stage] + g * kHeadTileBytes);
         const uint32_t vtile = ktile + kBs * kHeadRowBytes;
         // rows to use: the tile's tokens inside the context, less (8-token
         // pages) a page that was out of range
-        const int use = (BT == 8) ? (d.vmask & ((1 << n_valid) - 1)) : ((1 << n_valid) - 1);
-        if (use != 0xffff) {
-          // rows past the context or not loaded may hold anything (NaN
-          // included): zero the V rows, the K rows are masked in the scores
-          uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
-          if (BT == 8) {
-            for (int e = lane; e < kBs * 8; e += 32)
-              if (!((use >> (e >> 3)) & 1)) vrow[e] = make_uint4(0, 0, 0, 0);
-          } else {
-            for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        // ---- S = Q K^T for tokens 0..7 (s0) and 8..15 (s1)
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const int tok = (lm_i >> 1) * 8 + lm_r;
-          const int chunk = 2 * ks + (lm_i & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
-          mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
-          mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
-        }
-        // ---- online softmax on row r (q head), columns c2, c2+1, 8+c2, 9+c2
-        float x0 = s0[0] * p.qscale, x1 = s0[1] * p.qscale;
-        float x2 = s1[0] * p.qscale, x3 = s1[1] * p.qscale;
-        if (BT == 8) {
-          x0 = ((use >> c2) & 1) ? x0 : neg_inf();
-          x1 = ((use >> (c2 + 1)) & 1) ? x1 : neg_inf();
-          x2 = ((use >> (c2 + 8)) & 1) ? x2 : neg_inf();
-          x3 = ((use >> (c2 + 9)) & 1) ? x3 : neg_inf();
-        } else {
-          x0 = (c2 < n_valid) ? x0 : neg_inf();
-          x1 = (c2 + 1 < n_valid) ? x1 : neg_inf();
-          x2 = (c2 + 8 < n_valid) ? x2 : neg_inf();
-          x3 = (c2 + 9 < n_valid) ? x3 : neg_inf();
-        }
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m, mx);
-        const float alpha = fast_exp2(m - m_new);
-        const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
-        const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
-        const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
-        l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
-        m = m_new;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          o[t][0] *= alpha;
-          o[t][1] *= alpha;
-        }
-        // ---- O += P V, dims in 4 pairs of 8-dim tiles
-#pragma unroll
-        for (int dp = 0; dp < 4; ++dp) {
-          const int tok = (lm_i & 1) * 8 + lm_r;
-          const int chunk = 2 * dp + (lm_i >> 1);
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
-          mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
-          mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
-        }
+        const unsigned use = (BT == 8) ? (d.vmask & ((1u << n_valid) - 1u)) : 0u;
+        attend_tile<BT == 8>(ktile, vtile, n_valid, use, qa, qc, p.qscale, lane, ts);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
       if (d.flags & kSegEnd) {
-        // ---- finish this piece of sequence d.seq: row sums over the quad
-        float lt = l;
-        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        // ---- finish this piece of sequence d.seq
+        const float lt = row_sum(ts);
         if (real_row) {
           const int h = g * kGqa + r;
           if (d.n_parts == 1) {
@@ -563,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 p.out + (static_cast<size_t>(d.seq) * kHq + h) * kD);
 #pragma unroll
             for (int t = 0; t < 8; ++t)
-              dst[(8 * t + c2) / 2] = float2_to_bf16x2(o[t][0] * inv, o[t][1] * inv);
+              dst[(8 * t + c2) / 2] = float2_to_bf16x2(ts.o[t][0] * inv, ts.o[t][1] * inv);
           } else {
             const size_t slot = static_cast<size_t>(d.slot);
             float2 *dst = p.acc + (slot * kHq + h) * (kD / 2);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(o[t][0], o[t][1]);
-            if ((lane & 3) == 0) p.ml[slot * kHq + h] = make_float2(m, lt);
+            for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(ts.o[t][0], ts.o[t][1]);
+            if ((lane & 3) == 0) p.ml[slot * kHq + h] = make_float2(ts.m, lt);
           }
         }
       }

@@ -28,6 +28,7 @@
 #include <climits>
 #include <cuda.h>
 
+#include "pa_decode_tile.cuh"
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -82,14 +83,6 @@ struct PairParams {
   int cap_tokens;
   float qscale;
 };
-
-__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // ------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -361,23 +354,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
   const int c2 = 2 * (lane & 3);         // fragment column pair
   const bool real_row = r < kGqa;
-  const int lm_i = lane >> 3, lm_r = lane & 7;
   uint32_t qa[4], qc[4];
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
-  if (real_row) {
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        p.q + (static_cast<size_t>(s) * kHq + h * kGqa + r) * kD);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
-      qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
-    }
-  }
-  float o[8][4];
-  float m = neg_inf(), l = 0.f;
-#pragma unroll
-  for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  load_q_fragments(p.q + static_cast<size_t>(s) * kHq * kD, h, lane, qa, qc);
+  TileState ts;
+  ts.reset();
   int stage = 0;
   uint32_t phase = 0;
   bool timed_out = false;
@@ -388,67 +368,13 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       break;
     }
     const PairStage d = sm.desc[stage];
-    if (d.flags & kReset) {
-      m = neg_inf();
-      l = 0.f;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    }
+    if (d.flags & kReset) ts.reset();
     if (d.flags & kEnd) break;
     if (w < d.n && !((d.bad >> w) & 1)) {
       const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
-      unsigned char *tile = sm.kv[stage] + w * kSlotBytes;
-      const uint32_t ktile = smem_u32(tile);
-      const uint32_t vtile = ktile + kBs * kHeadRowBytes;
-      if (n_valid < kBs) {
-        // rows past the context may hold anything (NaN included): zero the V
-        // rows, the K rows are masked in the scores
-        uint4 *vrow = reinterpret_cast<uint4 *>(tile + kBs * kHeadRowBytes);
-        for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      // ---- S = Q K^T for tokens 0..7 (s0) and 8..15 (s1)
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const int tok = (lm_i >> 1) * 8 + lm_r;
-        const int chunk = 2 * ks + (lm_i & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
-        mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
-      }
-      // ---- online softmax on row r, columns c2, c2+1, 8+c2, 9+c2
-      float x0 = (c2 < n_valid) ? s0[0] * p.qscale : neg_inf();
-      float x1 = (c2 + 1 < n_valid) ? s0[1] * p.qscale : neg_inf();
-      float x2 = (c2 + 8 < n_valid) ? s1[0] * p.qscale : neg_inf();
-      float x3 = (c2 + 9 < n_valid) ? s1[1] * p.qscale : neg_inf();
-      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
-      const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
-      const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
-      const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
-      l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
-      m = m_new;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        o[t][0] *= alpha;
-        o[t][1] *= alpha;
-      }
-      // ---- O += P V, dims in 4 pairs of 8-dim tiles
-#pragma unroll
-      for (int dp = 0; dp < 4; ++dp) {
-        const int tok = (lm_i & 1) * 8 + lm_r;
-        const int chunk = 2 * dp + (lm_i >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
-        mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
-      }
+      const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
+      attend_tile<false>(ktile, ktile + kBs * kHeadRowBytes, n_valid, 0u, qa, qc, p.qscale, lane,
+                         ts);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
@@ -461,17 +387,15 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   // ---- the 8 warp states -> one CTA state.  Each warp parks its state in
   // its own slot of stage 0: every copy has landed (the warp has waited on
   // every stage up to the end), and no other warp reads that slot any more.
-  float lt = l;
-  lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-  lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+  const float lt = row_sum(ts);
   {
     float *my_o = reinterpret_cast<float *>(sm.kv[0] + w * kSlotBytes);   // [4 rows][64]
     float2 *my_ml = reinterpret_cast<float2 *>(my_o + kGqa * kD);
     if (real_row) {
 #pragma unroll
       for (int t = 0; t < 8; ++t)
-        *reinterpret_cast<float2 *>(my_o + r * kD + 8 * t + c2) = make_float2(o[t][0], o[t][1]);
-      if ((lane & 3) == 0) my_ml[r] = make_float2(timed_out ? neg_inf() : m, timed_out ? 0.f : lt);
+        *reinterpret_cast<float2 *>(my_o + r * kD + 8 * t + c2) = make_float2(ts.o[t][0], ts.o[t][1]);
+      if ((lane & 3) == 0) my_ml[r] = make_float2(timed_out ? neg_inf() : ts.m, timed_out ? 0.f : lt);
     }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kPairWarps * 32) : "memory");
@@ -715,23 +639,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int r = lane >> 2;               // fragment row = q head within the group (0..3 real)
   const int c2 = 2 * (lane & 3);
   const bool real_row = r < kGqa;
-  const int lm_i = lane >> 3, lm_r = lane & 7;
   uint32_t qa[4], qc[4];
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) qa[ks] = qc[ks] = 0u;
-  if (real_row) {
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        p.q + (static_cast<size_t>(s) * kHq + h * kGqa + r) * kD);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[ks] = __ldg(qrow + (16 * ks + c2) / 2);
-      qc[ks] = __ldg(qrow + (16 * ks + 8 + c2) / 2);
-    }
-  }
-  float o[8][4];
-  float m = neg_inf(), l = 0.f;
-#pragma unroll
-  for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  load_q_fragments(p.q + static_cast<size_t>(s) * kHq * kD, h, lane, qa, qc);
+  TileState ts;
+  ts.reset();
   int stage = 0;
   uint32_t phase = 0;
   bool timed_out = false;
@@ -742,63 +653,14 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       break;
     }
     const SeqStage d = sm.desc[stage];
-    if (d.flags & kReset) {
-      m = neg_inf();
-      l = 0.f;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    }
+    if (d.flags & kReset) ts.reset();
     if (d.flags & kEnd) break;
     if (!(d.flags & kBadPage)) {
       const int n_valid = (d.j == d.last) ? d.tail : kBs;
-      unsigned char *ktp = sm.kv[stage] + h * (kBs * kHeadRowBytes);
-      unsigned char *vtp = ktp + kPairStageBytes / 2;
-      const uint32_t ktile = smem_u32(ktp);
-      const uint32_t vtile = smem_u32(vtp);
-      if (n_valid < kBs) {
-        uint4 *vrow = reinterpret_cast<uint4 *>(vtp);
-        for (int e = n_valid * 8 + lane; e < kBs * 8; e += 32) vrow[e] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const int tok = (lm_i >> 1) * 8 + lm_r;
-        const int chunk = 2 * ks + (lm_i & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ktile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s0, qa[ks], 0u, qc[ks], 0u, b0, b1);
-        mma_bf16_16816(s1, qa[ks], 0u, qc[ks], 0u, b2, b3);
-      }
-      float x0 = (c2 < n_valid) ? s0[0] * p.qscale : neg_inf();
-      float x1 = (c2 + 1 < n_valid) ? s0[1] * p.qscale : neg_inf();
-      float x2 = (c2 + 8 < n_valid) ? s1[0] * p.qscale : neg_inf();
-      float x3 = (c2 + 9 < n_valid) ? s1[1] * p.qscale : neg_inf();
-      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
-      const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
-      const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
-      const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
-      l = fmaf(l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
-      m = m_new;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        o[t][0] *= alpha;
-        o[t][1] *= alpha;
-      }
-#pragma unroll
-      for (int dp = 0; dp < 4; ++dp) {
-        const int tok = (lm_i & 1) * 8 + lm_r;
-        const int chunk = 2 * dp + (lm_i >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * dp], pa, 0u, pc, 0u, v0, v1);
-        mma_bf16_16816(o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
-      }
+      // [K|V][head][token][64]: head h's K rows, then (16 KiB on) its V rows
+      const uint32_t ktile = smem_u32(sm.kv[stage] + h * (kBs * kHeadRowBytes));
+      attend_tile<false>(ktile, ktile + kPairStageBytes / 2, n_valid, 0u, qa, qc, p.qscale, lane,
+                         ts);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
@@ -809,18 +671,17 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   }
 
   // ---- each q head's state to the CTA that owns it
-  float lt = l;
-  lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-  lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+  const float lt = row_sum(ts);
   if (real_row) {
     const int qh = h * kGqa + r;
     const int owner = qh / qpo, slot = rank * qpo + qh % qpo;
 #pragma unroll
     for (int t = 0; t < 8; ++t)
-      st_cluster_f32x2(map_to_rank(&sm.part_o[slot][8 * t + c2], owner), make_float2(o[t][0], o[t][1]));
+      st_cluster_f32x2(map_to_rank(&sm.part_o[slot][8 * t + c2], owner),
+                       make_float2(ts.o[t][0], ts.o[t][1]));
     if ((lane & 3) == 0)
       st_cluster_f32x2(map_to_rank(&sm.part_ml[slot], owner),
-                       make_float2(timed_out ? neg_inf() : m, timed_out ? 0.f : lt));
+                       make_float2(timed_out ? neg_inf() : ts.m, timed_out ? 0.f : lt));
     mbar_arrive_cluster(map_to_rank(&sm.parts_full, owner));
   }
   if (!mbar_wait_cluster(&sm.parts_full, 0)) {
