@@ -53,6 +53,8 @@ DESCRIPTIONS = {
                "65,536-block pool, 32/8 heads, head_dim 64, 16-token bf16 blocks",
     "pool2g": "2 GiB pool (65,536 blocks), 16 layers, 64 sequences x 4096, per-layer random "
               "16,384-block subsets",
+    "pool8g": "pool2g's batch (16 layers, 64 sequences x 4096) in an 8 GiB pool (262,144 "
+              "blocks): every layer's pages distinct, no aliasing",
     "long32k": "16 layers, 4 sequences x 32,768, 131,072-block pool, q x4",
     "ragged": "continuous batching: 256 sequences, context log-U[1,8192], 262,144-block pool; "
               "per layer append (RoPE, pos = ctx) then attention over ctx+1",

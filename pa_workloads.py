@@ -128,7 +128,15 @@ def make_workload(name: str, seed: int | None = None, block_tokens: int = BLOCK,
     """Table-level description of one of the five workloads (no tensors).
     With block_tokens other than 16 the pool keeps its bytes (16 / page
     times the blocks) and the tables hold pages of that many tokens."""
-    seeds = {"tiny": 1, "llama1b": 2, "pool2g": 3, "long32k": 4, "ragged": 5}
+    seeds = {"tiny": 1, "llama1b": 2, "pool2g": 3, "long32k": 4, "ragged": 5, "pool8g": 3}
+    if name == "pool8g":
+        # pool2g's batch in a pool large enough for every layer's pages
+        # (262,144 blocks = 8 GiB): no page is shared between layers
+        over = dict(over)
+        over.setdefault("num_blocks", 262144)
+        over["alias"] = False
+        return dataclasses.replace(make_workload("pool2g", seed=seed, block_tokens=block_tokens,
+                                                 **over), name="pool8g")
     if seed is None:
         seed = seeds.get(name, 0)
     if block_tokens != BLOCK:
