@@ -1,11 +1,15 @@
-// pa_decode_pair.cu -- decode step of PagedAttention for batches whose
-// (sequence, kv head) pairs fit on the GPU at once.
+// pa_decode_pair.cu -- the two cluster kernels of the decode step of
+// PagedAttention: one thread-block cluster per (sequence, kv head)
+// (decode_pair_kernel, small batches) and one per sequence
+// (decode_seq_kernel, batches of similar context lengths).  Both combine the
+// pieces of a context inside the cluster, through distributed shared memory,
+// instead of through partials in global memory and a merge kernel.
 //
 // Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "What is in
 // the box": one query token's attention over K/V stored in 16-token pages
 // found through block_table, online softmax, GQA_Q_TO_K_RATIO = 4.
 //
-// Design (GB300-first):
+// decode_pair_kernel (GB300-first):
 //  * One thread-block cluster of c CTAs (c = 1, 2, 4 or 8) per (sequence, kv
 //    head).  The c CTAs cut the head's 16-token tiles into c equal ranges, so
 //    a small batch still puts every SM to work, and they combine their
@@ -730,6 +734,7 @@ int launch_decode_seq(const CUtensorMap &page_map, uint16_t *out, const uint16_t
   int rc = current_device(&di);
   if (rc != PA_OK) return rc;
   static bool attr_done[64] = {};
+  static int c16_fits[64] = {};   // 0 not asked yet, 1 clusters of 16 schedule, 2 they do not
   const size_t smem = sizeof(SeqSmem) + 1024;
   if (!attr_done[di.device]) {
     if (cudaFuncSetAttribute(decode_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -738,6 +743,28 @@ int launch_decode_seq(const CUtensorMap &page_map, uint16_t *out, const uint16_t
                              1) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_done[di.device] = true;
+  }
+  if (cluster == 16) {
+    // 16 CTAs is beyond the portable cluster size: use it only where the
+    // device reports that such clusters of this kernel can be resident
+    if (c16_fits[di.device] == 0) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(16);
+      qc.blockDim = dim3(kPairThreads);
+      qc.dynamicSmemBytes = smem;
+      cudaLaunchAttribute qa;
+      qa.id = cudaLaunchAttributeClusterDimension;
+      qa.val.clusterDim.x = 16;
+      qa.val.clusterDim.y = 1;
+      qa.val.clusterDim.z = 1;
+      qc.attrs = &qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      const bool ok = cudaOccupancyMaxActiveClusters(&n, decode_seq_kernel, &qc) == cudaSuccess;
+      cudaGetLastError();
+      c16_fits[di.device] = ok && n > 0 ? 1 : 2;
+    }
+    if (c16_fits[di.device] == 2) cluster = 8;
   }
   PairParams prm;
   prm.kv = static_cast<const unsigned char *>(kv_cache);
