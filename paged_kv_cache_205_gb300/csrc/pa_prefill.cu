@@ -24,13 +24,15 @@
 //               thread issues, per half, S_j = Q K_j^T (M 128, N 128, 4
 //               k-steps) into the half's TMEM S columns and, once the half's
 //               softmax has written P_j, O_j = P_j V_j (M 128, N 64, 8
-//               k-steps, V read as an MN-major operand) into its O columns;
+//               k-steps, P from TMEM, V read from shared memory as an
+//               MN-major operand) into its O columns;
 //   warps 0-3, 4-7   softmax of half 0 / half 1, one thread per row (TMEM
 //               lane): S_j from TMEM in one round trip, causal mask, row
 //               maximum and sum in fp32 (log2 domain), P_j rounded to bf16
-//               into shared memory (128-byte swizzle, the layout the MMA
-//               reads); O accumulates in TMEM and is rescaled only when the
-//               row maximum grows by more than 2^8; the output row at the end.
+//               into the half's own 64 TMEM columns (two keys per column),
+//               from which the PV MMA reads its A operand; O accumulates in
+//               TMEM and is rescaled only when the row maximum grows by more
+//               than 2^8; the output row at the end.
 // The tensor core alternates between the halves: one half's MMAs run while
 // the other half's softmax works.
 #include <climits>
@@ -49,7 +51,7 @@ constexpr int kCtaTok = kQTok * kHalves;      // query tokens per CTA
 constexpr int kRows = kQTok * kGqa;           // 128 MMA rows per half
 constexpr int kChunk = 128;                   // keys per chunk
 constexpr int kPagesPerChunk = kChunk / kBs;  // 8
-constexpr int kStagesP = 3;
+constexpr int kStagesP = 5;
 constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -65,8 +67,9 @@ static_assert(2 * 128 * kRegsSoft + 128 * kRegsOther <= kPThreads * kRegsLaunch,
               "register split above the launch budget");
 constexpr int kTileRowBytes = kHeadRowBytes;             // 128-byte rows
 constexpr int kOperandBytes = kChunk * kTileRowBytes;    // 16 KiB: 128 rows x 64 bf16
-constexpr uint32_t kTmemCols = 512;                      // S x2 (256) + O x2 (128), rounded up
+constexpr uint32_t kTmemCols = 512;                      // S x2 (256) + O x2 (128) + P x2 (128)
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;                         // P of half h: 64 columns of bf16 pairs
 constexpr int kMaxSeqsP = 2048;
 constexpr float kLog2eP = 1.4426950408889634f;
 
@@ -89,7 +92,6 @@ struct __align__(1024) PSmem {
   unsigned char q[kHalves][kOperandBytes];         // per half [32 tok][4 heads][64], swizzled
   unsigned char k[kStagesP][kOperandBytes];        // [128 keys][64]
   unsigned char v[kStagesP][kOperandBytes];        // [128 keys][64]
-  unsigned char p[kHalves][2][kOperandBytes];      // per half, P: keys 0-63, 64-127
   int tile_prefix[kMaxSeqsP + 1];
   uint64_t q_full;
   uint64_t q_empty;
@@ -199,18 +201,17 @@ __device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int
   tc::mma_commit(&sm.s_full[h]);
 }
 
-// O of half h += P_h V for chunk gc in the half's O columns (one thread);
-// the item's first chunk starts the sum.
+// O of half h += P_h V for chunk gc in the half's O columns (one thread),
+// P read from the half's P columns of tensor memory (16 keys = 8 columns per
+// k-step); the item's first chunk starts the sum.
 __device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, int gc, bool first,
                                              uint32_t id_o) {
   const uint32_t v_addr = smem_u32(sm.v[gc % kStagesP]);
 #pragma unroll
-  for (int ks = 0; ks < kChunk / 16; ++ks) {
-    const uint32_t pa = smem_u32(sm.p[h][ks >> 2]) + 32 * (ks & 3);
-    tc::mma_bf16(tmem + kTmemO + h * kD, tc::sdesc_sw128(pa, 16, 1024),
-                 tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o,
-                 (!first || ks > 0) ? 1u : 0u);
-  }
+  for (int ks = 0; ks < kChunk / 16; ++ks)
+    tc::mma_bf16_ts(tmem + kTmemO + h * kD, tmem + kTmemP + h * (kChunk / 2) + 8 * ks,
+                    tc::sdesc_sw128(v_addr + 2048 * ks, 16, 1024), id_o,
+                    (!first || ks > 0) ? 1u : 0u);
   tc::mma_commit(&sm.o_full[h]);
 }
 
@@ -429,6 +430,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const int tok = r >> 2, hh = r & 3;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_addr + h * kChunk, o_addr = lane_addr + kTmemO + h * kD;
+    const uint32_t p_addr = lane_addr + kTmemP + h * (kChunk / 2);
     bool ok = true;
     int gc = 0, n_s = 0, n_pv = 0;
     for (int i = blockIdx.x; i < n_items && ok; i += G) {
@@ -494,12 +496,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (move) m = mc;
         const float base = (m == p_neg_inf()) ? 0.f : m;
         const float2 qs2 = make_float2(p.qscale, p.qscale), nb2 = make_float2(-base, -base);
-        // P = exp2(s * qscale - m) in bf16, stored swizzled; 4 partial sums
+        // P = exp2(s * qscale - m) in bf16 pairs (key 2c in the low half of
+        // column c) into the half's P columns of tensor memory; 4 partial sums
         float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
+        uint32_t pw[kChunk / 2];
 #pragma unroll
         for (int ch = 0; ch < kChunk / 8; ++ch) {
-          uint32_t pk[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = 8 * ch + 2 * q;
@@ -507,15 +510,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
                                   qs2, nb2);
             const float e0 = p_exp2(x.x), e1 = p_exp2(x.y);
             ls[q] = make_float2(ls[q].x + e0, ls[q].y + e1);
-            pk[q] = float2_to_bf16x2(e0, e1);
+            pw[c >> 1] = float2_to_bf16x2(e0, e1);
           }
-          unsigned char *region = sm.p[h][ch >> 3] + r * kTileRowBytes;
-          *reinterpret_cast<uint4 *>(region + (((ch & 7) ^ (r & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        tc::tmem_st32(p_addr, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        tc::tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
         l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-        fence_proxy_async_smem();   // P, for the tensor core
-        tc::fence_before_sync();
+        tc::tmem_st_wait();
+        tc::fence_before_sync();    // P, for the tensor core
         mbar_arrive(&sm.p_full[h]);
       }
       if (!ok) break;
