@@ -219,6 +219,9 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int pair = static_cast<int>(cluster_id());
   const int s = pair / kHkv, h = pair % kHkv;
   const int32_t *row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+  // the next kernel on the stream may be scheduled at once: it waits for
+  // this one to finish before it reads anything this one writes
+  pdl_launch_dependents();
 
   // ---- before the previous kernel on the stream has finished
   if (tid == 0) {
@@ -247,7 +250,6 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   }
   if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
   else __syncthreads();
-  pdl_launch_dependents();
   // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
@@ -513,6 +515,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int s = static_cast<int>(cluster_id());
   const int qpo = kHq / c;   // q heads each CTA owns
   const int32_t *row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+  pdl_launch_dependents();   // the next kernel waits for this one before reading its output
 
   // ---- before the previous kernel on the stream has finished
   if (tid == 0) {
@@ -537,7 +540,6 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   }
   if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
   else __syncthreads();
-  pdl_launch_dependents();
   // everything read below may come from the previous kernel on the stream
   pdl_wait_primary();
 
