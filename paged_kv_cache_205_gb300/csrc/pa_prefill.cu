@@ -16,23 +16,28 @@
 // each half's 128 MMA rows are its 32 tokens x the 4 q heads of the GQA group
 // (row = 4 * token + head), so every K/V byte brought into shared memory
 // serves 256 query rows.  Keys go in chunks of 128 (8 pages).  Warp roles
-// (320 threads):
+// (384 threads):
 //   warp 8      producer: the two Q tiles (TMA), then per chunk 16 TMA copies
-//               (K rows and V rows of 8 pages) into a 3-stage ring;
-//   warp 9      MMA warp: zeroes the V rows of a chunk that lie past the
-//               tile's last key or in a page that was not loaded, then one
-//               thread issues, per half, S_j = Q K_j^T (M 128, N 128, 4
-//               k-steps) into the half's TMEM S columns and, once the half's
-//               softmax has written P_j, O_j = P_j V_j (M 128, N 64, 8
-//               k-steps, P from TMEM, V read from shared memory as an
-//               MN-major operand) into its O columns;
+//               (K rows and V rows of 8 pages) into a 5-stage ring;
+//   warps 9, 10 MMA warps, one per half: one thread issues the half's
+//               S_{j+1} = Q K_{j+1}^T (M 128, N 128, 4 k-steps) into its TMEM
+//               S columns as soon as the half's softmax has read S_j, and,
+//               once the softmax has written P_j, O += P_j V_j (M 128, N 64,
+//               8 k-steps, P from TMEM, V read from shared memory as an
+//               MN-major operand) into its O columns.  S_{j+1} is thus
+//               computed while the softmax works on S_j.  A tcgen05.mma issue
+//               blocks while the tensor core's queue is full, so each half
+//               has its own issuing thread.  The warp of the half that sees
+//               every chunk also zeroes the V rows that lie past the tile's
+//               last key or in a page that was not loaded;
 //   warps 0-3, 4-7   softmax of half 0 / half 1, one thread per row (TMEM
 //               lane): S_j from TMEM in one round trip, causal mask, row
 //               maximum and sum in fp32 (log2 domain), P_j rounded to bf16
 //               into the half's own 64 TMEM columns (two keys per column),
-//               from which the PV MMA reads its A operand; O accumulates in
-//               TMEM and is rescaled only when the row maximum grows by more
-//               than 2^8; the output row at the end.
+//               from which the PV MMA reads its A operand, once PV_{j-1} has
+//               completed; O accumulates in TMEM and is rescaled only when
+//               the row maximum grows by more than 2^8; the output row at
+//               the end.
 // The tensor core alternates between the halves: one half's MMAs run while
 // the other half's softmax works.
 #include <climits>
@@ -55,7 +60,7 @@ constexpr int kStagesP = 5;
 constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kPThreads = 12 * 32;            // 3 warpgroups; warps 10-11 only rebalance registers
+constexpr int kPThreads = 12 * 32;            // 3 warpgroups; warp 11 only rebalances registers
 // Register budget: 384 threads x 168 at launch = 64,512.  The producer/MMA
 // warpgroup gives up to 80 and each softmax warpgroup takes 200:
 // 2 x 128 x 200 + 128 x 80 = 61,440 (every SM sub-partition: 2 x 200 + 80
@@ -98,9 +103,11 @@ struct __align__(1024) PSmem {
   uint64_t kv_full[kStagesP];
   uint64_t kv_empty[kStagesP];
   uint64_t s_full[kHalves];
+  uint64_t s_free[kHalves];                        // the softmax has read S: the next S may land
   uint64_t p_full[kHalves];
   uint64_t o_full[kHalves];
   uint64_t o_free[kHalves];
+  uint64_t v_zeroed[kStagesP];                     // zeroing warp -> the other half's MMA warp
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
@@ -164,26 +171,37 @@ __device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams
   return it;
 }
 
-// MMA warp: chunk gc (counted over the CTA's items) has landed; kbase is its
-// first key within its item.  Its V rows past the tile's last key, or in a
-// page that was not loaded, meet P = 0 but may hold anything (NaN
-// included): the warp zeroes them before any MMA reads the stage.
+// Chunk gc (counted over the CTA's items; kbase: its first key within its
+// item) has V rows that must be zeroed: rows past the tile's last key or in
+// a page that was not loaded meet P = 0 but may hold anything (NaN
+// included).
+__device__ __forceinline__ bool chunk_needs_zero(const PSmem &sm, int gc, int kbase, int n_keys) {
+  return sm.pmask[gc % kStagesP] != 0xff || kbase + kChunk > n_keys;
+}
+
+// MMA warp: waits until chunk gc has landed (every MMA warp does, for every
+// chunk of the item, before it releases the stage: so neither warp's release
+// can run ahead of the stage's fill).  The zeroing warp clears the rows above
+// before any MMA reads the stage and, with `handover`, signals the other
+// half's MMA warp through v_zeroed.
 __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, int n_keys,
-                                                  int lane) {
+                                                  bool zeroer, bool handover, int lane) {
   const int st = gc % kStagesP;
   int good = 1;
   if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (gc / kStagesP) & 1) ? 1 : 0;
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   __syncwarp();
-  const int pm = sm.pmask[st];
-  if (pm != 0xff || kbase + kChunk > n_keys) {
+  if (zeroer && chunk_needs_zero(sm, gc, kbase, n_keys)) {
+    const int pm = sm.pmask[st];
     for (int e = lane; e < kChunk * (kTileRowBytes / 16); e += 32) {
       const int key = e >> 3;
       if (kbase + key >= n_keys || !((pm >> (key >> 4)) & 1))
         reinterpret_cast<uint4 *>(sm.v[st])[e] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
+    __syncwarp();
+    if (handover && lane == 0) mbar_arrive(&sm.v_zeroed[st]);
   }
   __syncwarp();
   return true;
@@ -226,13 +244,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_empty, kHalves);
     for (int st = 0; st < kStagesP; ++st) {
       mbar_init(&sm.kv_full[st], 1);
-      mbar_init(&sm.kv_empty[st], 1);
+      mbar_init(&sm.kv_empty[st], kHalves);     // one release per MMA warp
+      mbar_init(&sm.v_zeroed[st], 1);
     }
     for (int h = 0; h < kHalves; ++h) {
       mbar_init(&sm.s_full[h], 1);
+      mbar_init(&sm.s_free[h], kSoftThreads);
       mbar_init(&sm.p_full[h], kSoftThreads);
       mbar_init(&sm.o_full[h], 1);
       mbar_init(&sm.o_free[h], kSoftThreads);
@@ -301,10 +321,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       bool ok = true;
       int gc = 0, k = 0;
       uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
+      // Lane l < 8 holds the block id of page l of a chunk.  The ids of the
+      // next chunk (of this item or the next) are read while this chunk's
+      // copies are issued, so the table read is off the producer's path.
+      auto chunk_ids = [&](const Item &x, int j) -> int {
+        const int32_t *row =
+            p.block_table + (static_cast<size_t>(x.s) * p.n_layers + p.layer) * p.max_blocks;
+        const int pg = j * kPagesPerChunk + (lane & 7);
+        return (lane < kPagesPerChunk && pg * kBs < x.n_keys) ? row[pg] : -1;
+      };
+      int blk_next = -1;
+      bool next_read = false;
       for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
         const Item it = decode_item(sm, p, total_tiles, i);
-        const int32_t *row =
-            p.block_table + (static_cast<size_t>(it.s) * p.n_layers + p.layer) * p.max_blocks;
+        if (!next_read && it.n_chunks > 0) blk_next = chunk_ids(it, 0);
+        next_read = false;
         int good = 1;
         if (lane == 0) {
           // the previous item's Q has been read by all its MMAs
@@ -321,11 +352,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
           const int st = gc % kStagesP;
           const uint32_t ph = (gc / kStagesP) & 1;
-          // lane l < 8 looks up page j * 8 + l
           const int pg = j * kPagesPerChunk + (lane & 7);
-          int blk = -1;
           const bool needed = lane < kPagesPerChunk && pg * kBs < it.n_keys;
-          if (needed) blk = row[pg];
+          const int blk = blk_next;
+          if (j + 1 < it.n_chunks) {
+            blk_next = chunk_ids(it, j + 1);
+          } else if (i + G < n_items) {
+            const Item nx = decode_item(sm, p, total_tiles, i + G);
+            if (nx.n_chunks > 0) blk_next = chunk_ids(nx, 0);
+            next_read = true;
+          }
           const bool valid = needed && blk >= 0 && blk < p.num_blocks;
           const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
           const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
@@ -363,54 +399,76 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
               report(p.err, PA_DEV_TIMEOUT);
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ========================================================= MMA warp ==
+    } else if (warp < kMmaWarp + kHalves) {
+      // ======================================================== MMA warps ==
+      const int h = warp - kMmaWarp;     // the half whose MMAs this warp issues
       const uint32_t id_s = tc::idesc_bf16(kRows, kChunk, false);
       const uint32_t id_o = tc::idesc_bf16(kRows, kD, true);
       int ok = 1;
       int gc = 0, k = 0;
-      int n_p[kHalves] = {0, 0};        // P chunks consumed per half
-      int n_active[kHalves] = {0, 0};   // items in which the half had work
+      int n_p = 0;             // P chunks of this half consumed
+      int n_active = 0;        // items in which the half had work
+      uint32_t vz_parity = 0;  // per stage: parity of the next zeroing hand-over
+      int n_s = 0;             // S chunks issued
+      // S of chunk gcs once the softmax has read the previous S (lane 0)
+      auto issue_s = [&](int gcs) -> bool {
+        if (n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) return false;
+        tc::fence_after_sync();
+        mma_issue_s(sm, tmem, h, gcs, id_s);
+        ++n_s;
+        return true;
+      };
       for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
         const Item it = decode_item(sm, p, total_tiles, i);
+        const int nch = h == 0 ? it.nc0 : it.nc1;
+        // half 1 sees every chunk of a two-half tile, half 0 every chunk of
+        // a one-half tile: that half's warp zeroes, and with two halves hands
+        // the chunks half 0 also reads over to it
+        const bool zeroer = h == (it.halves == 2 ? 1 : 0);
         if (lane == 0) ok = mbar_wait_short(&sm.q_full, k & 1) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ok = mma_prepare_chunk(sm, gc, 0, it.n_keys, lane);
-        if (ok && lane == 0) {
-          tc::fence_after_sync();
-          mma_issue_s(sm, tmem, 0, gc, id_s);
-          if (it.halves == 2) mma_issue_s(sm, tmem, 1, gc, id_s);
+        if (ok) ok = mma_prepare_chunk(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
+        if (ok && nch > 0) {
+          int good = 1;
+          if (lane == 0) good = issue_s(gc) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, good, 0);
         }
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
-          if (j + 1 < it.n_chunks && !mma_prepare_chunk(sm, gc + 1, (j + 1) * kChunk, it.n_keys, lane)) {
+          if (j + 1 < it.n_chunks &&
+              !mma_prepare_chunk(sm, gc + 1, (j + 1) * kChunk, it.n_keys, zeroer,
+                                 it.halves == 2 && j + 1 < it.nc0, lane)) {
             ok = 0;
             break;
           }
-          for (int h = 0; h < it.halves && ok; ++h) {
-            const int nch = h == 0 ? it.nc0 : it.nc1;
-            if (j >= nch) continue;
+          if (j < nch) {
             int good = 1;
             if (lane == 0) {
+              const int st = gc % kStagesP;
+              if (j + 1 < nch && !issue_s(gc + 1)) good = 0;
               // the half's previous item has read its O (the first PV clears it)
-              if (j == 0 && n_active[h] > 0 &&
-                  !mbar_wait_short(&sm.o_free[h], (n_active[h] - 1) & 1))
+              if (good && j == 0 && n_active > 0 &&
+                  !mbar_wait_short(&sm.o_free[h], (n_active - 1) & 1))
                 good = 0;
-              // the half's softmax has written P (and read S)
-              if (good && !mbar_wait_short(&sm.p_full[h], n_p[h] & 1)) good = 0;
+              // the half's softmax has written P
+              if (good && !mbar_wait_short(&sm.p_full[h], n_p & 1)) good = 0;
+              // V rows zeroed by the other half's warp
+              if (good && !zeroer && chunk_needs_zero(sm, gc, j * kChunk, it.n_keys)) {
+                if (!mbar_wait_short(&sm.v_zeroed[st], (vz_parity >> st) & 1u)) good = 0;
+                vz_parity ^= 1u << st;
+              }
               if (good) {
                 tc::fence_after_sync();
                 mma_issue_pv(sm, tmem, h, gc, j == 0, id_o);
-                if (j + 1 < nch) mma_issue_s(sm, tmem, h, gc + 1, id_s);
               }
             }
-            ++n_p[h];
+            ++n_p;
             ok = __shfl_sync(0xffffffffu, good, 0);
           }
           if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[gc % kStagesP]);
           __syncwarp();
         }
         if (ok && lane == 0) tc::mma_commit(&sm.q_empty);   // every MMA that reads Q is issued
-        for (int h = 0; h < it.halves; ++h) ++n_active[h];
+        if (nch > 0) ++n_active;
       }
       if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
       __syncwarp();
@@ -422,8 +480,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     // P values are taken against; it moves (and O, l are rescaled) only
     // when a chunk's maximum exceeds it by more than kRescale (log2 units),
     // so P stays below 2^kRescale and most chunks touch O not at all.
-    // S_j's commit comes after PV_{j-1}'s, so once S_j is there O and P
-    // are free.
+    // S_{j+1} is issued before PV_j, so O (for a rescale) and the P
+    // columns are touched only once PV_{j-1}'s commit is there.
     constexpr float kRescale = 8.f;
     const int h = tid >> 7;                   // half
     const int r = tid & (kRows - 1);          // MMA row = TMEM lane
@@ -432,7 +490,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const uint32_t s_addr = lane_addr + h * kChunk, o_addr = lane_addr + kTmemO + h * kD;
     const uint32_t p_addr = lane_addr + kTmemP + h * (kChunk / 2);
     bool ok = true;
-    int gc = 0, n_s = 0, n_pv = 0;
+    int gc = 0, n_s = 0, n_o = 0;   // S chunks read; PV commits waited for
     for (int i = blockIdx.x; i < n_items && ok; i += G) {
       const Item it = decode_item(sm, p, total_tiles, i);
       const int rows = h == 0 ? it.rows0 : it.rows1;
@@ -464,6 +522,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         for (int c0 = 0; c0 < kChunk; c0 += 32)
           tc::tmem_ld32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
         tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        mbar_arrive(&sm.s_free[h]);             // S_{j+1} may land in the S columns
         if (!full) {
           // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
 #pragma unroll
@@ -478,7 +538,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.qscale;
         const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
+        bool pv_done = j == 0;                  // PV_{j-1} complete: O stable, P columns read
         if (__any_sync(0xffffffffu, move) && j > 0) {
+          if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
+            ok = false;
+            break;
+          }
+          ++n_o;
+          pv_done = true;
+          tc::fence_after_sync();
           // rescale O (the whole warp takes part in the TMEM round trip)
           const float alpha = move ? p_exp2(m - mc) : 1.f;
 #pragma unroll 1
@@ -513,6 +581,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
             pw[c >> 1] = float2_to_bf16x2(e0, e1);
           }
         }
+        if (!pv_done) {
+          if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
+            ok = false;
+            break;
+          }
+          ++n_o;
+          tc::fence_after_sync();
+        }
         tc::tmem_st32(p_addr, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
         tc::tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
         l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
@@ -521,11 +597,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         mbar_arrive(&sm.p_full[h]);
       }
       if (!ok) break;
-      n_pv += nch;
-      if (!mbar_wait_short(&sm.o_full[h], (n_pv - 1) & 1)) {
+      // O is complete once the item's last PV is
+      if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
         ok = false;
         break;
       }
+      ++n_o;
       tc::fence_after_sync();
       uint32_t ov[kD];
       tc::tmem_ld32(o_addr, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
