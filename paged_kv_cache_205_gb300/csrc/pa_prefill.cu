@@ -108,6 +108,7 @@ struct __align__(1024) PSmem {
   uint64_t o_full[kHalves];
   uint64_t o_free[kHalves];
   uint64_t v_zeroed[kStagesP];                     // zeroing warp -> the other half's MMA warp
+  uint64_t h0_started;                             // half 0 has read an item's first S
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.o_full[h], 1);
       mbar_init(&sm.o_free[h], kSoftThreads);
     }
+    mbar_init(&sm.h0_started, kSoftThreads);
     fence_mbar_init();
   }
   pdl_launch_dependents();
@@ -410,6 +412,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       int n_active = 0;        // items in which the half had work
       uint32_t vz_parity = 0;  // per stage: parity of the next zeroing hand-over
       int n_s = 0;             // S chunks issued
+      int n_started = 0;       // two-half items (half 1's warp)
       // S of chunk gcs once the softmax has read the previous S (lane 0)
       auto issue_s = [&](int gcs) -> bool {
         if (n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) return false;
@@ -430,7 +433,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (ok) ok = mma_prepare_chunk(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
         if (ok && nch > 0) {
           int good = 1;
-          if (lane == 0) good = issue_s(gc) ? 1 : 0;
+          if (lane == 0) {
+            // half 1 starts an item once half 0 is under way: the halves'
+            // softmax passes then alternate instead of running side by side
+            if (h == 1 && !mbar_wait_short(&sm.h0_started, n_started & 1)) good = 0;
+            if (good) good = issue_s(gc) ? 1 : 0;
+          }
+          if (h == 1) ++n_started;
           ok = __shfl_sync(0xffffffffu, good, 0);
         }
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
@@ -524,6 +533,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         mbar_arrive(&sm.s_free[h]);             // S_{j+1} may land in the S columns
+        if (h == 0 && j == 0 && it.halves == 2) mbar_arrive(&sm.h0_started);
         if (!full) {
           // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
 #pragma unroll
