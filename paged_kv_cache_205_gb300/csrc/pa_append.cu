@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kScanCta = 1024;
 constexpr int kStoreThreads = (kHkv + kHq) * 8;   // 8 threads per head row, 40 rows
+constexpr int kStoreRows = 8;                      // token rows per CTA of the prefill store
 
 // Llama-3-scaled RoPE inverse frequencies of the 32 pairs, computed on the
 // host in fp64 and passed by value (no device memory involved).
@@ -256,9 +257,11 @@ __global__ void __launch_bounds__(kStoreThreads) append_store_kernel(AppendParam
 //                                  sequences in order and pops them from the
 //                                  back of the free list, pages spread over
 //                                  the threads.
-//   prefill_store_kernel  (1 CTA per token row, programmatic dependent
-//                                  launch) rotates the row's k and q, then
-//                                  stores K/V in the slot the table names.
+//   prefill_store_kernel  (1 CTA per 8 token rows, programmatic
+//                                  dependent launch) rotates the rows' k and
+//                                  q, then stores K/V in the slots the table
+//                                  names; the rows' loads are all in flight
+//                                  before the table is read.
 
 struct PrefillAppendParams {
   RopeFreqs freqs;
@@ -357,71 +360,107 @@ __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendPa
 }
 
 __global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillAppendParams p) {
-  __shared__ float2 cs[kD / 2];
-  __shared__ int seq_found;
+  __shared__ float2 cs[kStoreRows][kD / 2];
+  __shared__ int row_seq[kStoreRows];     // -1: the row lies in no accepted chunk
+  __shared__ int row_pos[kStoreRows];
+  __shared__ int row_open[kStoreRows];    // the sequence's first page opened by this chunk
+  __shared__ int row_blk[kStoreRows];     // -1: no valid page for the row
   pdl_launch_dependents();   // the next kernel may start its own set-up
-  const int r = blockIdx.x;
   const int tid = threadIdx.x;
-  // the row's sequence: the largest s with cu_tokens[s] <= r (an empty
-  // chunk's start equals the next one's, so the search passes over it)
-  if (tid == 0) {
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.cu_tokens[mid] <= r) lo = mid;
-      else hi = mid - 1;
+  const int r0 = blockIdx.x * kStoreRows;
+  // thread i < kStoreRows: row r0 + i's sequence (the largest s with
+  // cu_tokens[s] <= r: an empty chunk's start equals the next one's, so the
+  // search passes over it) and position
+  if (tid < kStoreRows) {
+    const int r = r0 + tid;
+    int seq = -1, pos = 0, open = 0;
+    if (r < p.total_tokens) {
+      int lo = 0, hi = p.num_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cu_tokens[mid] <= r) lo = mid;
+        else hi = mid - 1;
+      }
+      int ctx, n;
+      // a refused chunk is reported by the allocation kernel
+      if (chunk_fits(p, lo, &ctx, &n) && r >= p.cu_tokens[lo] && r < p.cu_tokens[lo + 1]) {
+        seq = lo;
+        pos = ctx + (r - p.cu_tokens[lo]);
+        open = (ctx + kBs - 1) / kBs;
+      }
     }
-    seq_found = lo;
+    row_seq[tid] = seq;
+    row_pos[tid] = pos;
+    row_open[tid] = open;
   }
-  __syncthreads();
-  const int s = seq_found;
-  int ctx, n;
-  const bool fits = chunk_fits(p, s, &ctx, &n);
-  if (!fits || r < p.cu_tokens[s] || r >= p.cu_tokens[s + 1]) {
-    pdl_wait_primary();   // refused chunk (reported by the allocation kernel) or a row outside every chunk
-    return;
-  }
-  const int pos = ctx + (r - p.cu_tokens[s]);
-  if (tid < kD / 2) cs[tid] = rope_cos_sin(pos, p.freqs.f[tid]);
-  __syncthreads();
+  // every row's k / q half-rows and v, in flight before anything waits on them
   const int head = tid >> 3;   // 0..7 k heads, 8..39 q heads
   const int j = tid & 7;
-  uint2 klo = make_uint2(0, 0), khi = make_uint2(0, 0);
-  if (head < kHkv) {
-    const uint16_t *row = p.k_new + (static_cast<size_t>(r) * kHkv + head) * kD;
-    rotate4(*reinterpret_cast<const uint2 *>(row + 4 * j),
-            *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j), cs, j, &klo, &khi);
-  } else if (p.q) {
-    uint16_t *row = p.q + (static_cast<size_t>(r) * kHq + (head - kHkv)) * kD;
+  uint2 lo[kStoreRows], hi[kStoreRows];
+  uint4 v[kStoreRows];
+#pragma unroll
+  for (int i = 0; i < kStoreRows; ++i) {
+    const int r = r0 + i;
+    lo[i] = hi[i] = make_uint2(0, 0);
+    v[i] = make_uint4(0, 0, 0, 0);
+    if (r < p.total_tokens) {
+      const uint16_t *row = nullptr;
+      if (head < kHkv) row = p.k_new + (static_cast<size_t>(r) * kHkv + head) * kD;
+      else if (p.q) row = p.q + (static_cast<size_t>(r) * kHq + (head - kHkv)) * kD;
+      if (row) {
+        lo[i] = *reinterpret_cast<const uint2 *>(row + 4 * j);
+        hi[i] = *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j);
+      }
+      if (tid < kTokRowBytes / 16)
+        v[i] = reinterpret_cast<const uint4 *>(p.v_new + static_cast<size_t>(r) * kHkv * kD)[tid];
+    }
+  }
+  __syncthreads();
+  // (cos, sin) of every row's position; thread i < kStoreRows: the row's page
+  for (int e = tid; e < kStoreRows * (kD / 2); e += kStoreThreads) {
+    const int i = e / (kD / 2), c = e % (kD / 2);
+    if (row_seq[i] >= 0) cs[i][c] = rope_cos_sin(row_pos[i], p.freqs.f[c]);
+  }
+  if (tid < kStoreRows) {
+    int blk = -1;
+    const int s = row_seq[tid];
+    if (s >= 0) {
+      const int page = row_pos[tid] / kBs;
+      const bool new_page = page >= row_open[tid];
+      if (new_page) pdl_wait_primary();   // its entry comes from the allocation kernel
+      blk = p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + page];
+      if (blk < 0 || blk >= p.num_blocks) {
+        // a page of this chunk that was refused or popped invalid is reported
+        // by the allocation kernel; an invalid page from before is reported here
+        if (!new_page) report(p.err, PA_DEV_BAD_BLOCK);
+        blk = -1;
+      }
+    }
+    row_blk[tid] = blk;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kStoreRows; ++i) {
+    if (row_seq[i] < 0) continue;
     uint2 rlo, rhi;
-    rotate4(*reinterpret_cast<const uint2 *>(row + 4 * j),
-            *reinterpret_cast<const uint2 *>(row + kD / 2 + 4 * j), cs, j, &rlo, &rhi);
-    *reinterpret_cast<uint2 *>(row + 4 * j) = rlo;
-    *reinterpret_cast<uint2 *>(row + kD / 2 + 4 * j) = rhi;
+    if (head < kHkv || p.q) rotate4(lo[i], hi[i], cs[i], j, &rlo, &rhi);
+    if (head >= kHkv && p.q) {   // q rotates in place whether or not the row's page is valid
+      uint16_t *row = p.q + (static_cast<size_t>(r0 + i) * kHq + (head - kHkv)) * kD;
+      *reinterpret_cast<uint2 *>(row + 4 * j) = rlo;
+      *reinterpret_cast<uint2 *>(row + kD / 2 + 4 * j) = rhi;
+    }
+    const int blk = row_blk[i];
+    if (blk < 0) continue;
+    unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
+    const int slot = row_pos[i] % kBs;
+    if (head < kHkv) {
+      unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
+      *reinterpret_cast<uint2 *>(krow + 8 * j) = rlo;
+      *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = rhi;
+    }
+    if (tid < kTokRowBytes / 16)
+      reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v[i];
   }
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (tid < kTokRowBytes / 16)
-    v = reinterpret_cast<const uint4 *>(p.v_new + static_cast<size_t>(r) * kHkv * kD)[tid];
-  const int page = pos / kBs;
-  const bool new_page = page >= (ctx + kBs - 1) / kBs;   // opened by this chunk
-  if (new_page) pdl_wait_primary();                       // its entry comes from the allocation kernel
-  const int blk = p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + page];
-  if (blk < 0 || blk >= p.num_blocks) {
-    // a page of this chunk that was refused or popped invalid is reported by
-    // the allocation kernel; an invalid page from before is reported here
-    if (tid == 0 && !new_page) report(p.err, PA_DEV_BAD_BLOCK);
-    pdl_wait_primary();
-    return;
-  }
-  unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
-  const int slot = pos % kBs;
-  if (head < kHkv) {
-    unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
-    *reinterpret_cast<uint2 *>(krow + 8 * j) = klo;
-    *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = khi;
-  }
-  if (tid < kTokRowBytes / 16)
-    reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v;
   pdl_wait_primary();   // this grid ends after the allocation kernel
 }
 
@@ -630,7 +669,8 @@ extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_n
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(prefill_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_pdl(prefill_store_kernel, dim3(total_tokens), dim3(kStoreThreads), 0, st, prm) !=
+  if (launch_pdl(prefill_store_kernel, dim3((total_tokens + kStoreRows - 1) / kStoreRows),
+                 dim3(kStoreThreads), 0, st, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
