@@ -88,10 +88,11 @@ def _load():
         lib.oracle_merge_partials.restype = None
         lib.oracle_kv_append_rope_bt.argtypes = [P, P, P, P, I, P, I, I, P, I, I, P, P, P, I]
         lib.oracle_kv_append_rope_bt.restype = I
-        lib.oracle_prefill_append_rope.argtypes = [P, P, P, P, P, I, P, I, I, P, I, I, P, P, P]
-        lib.oracle_prefill_append_rope.restype = I
-        lib.oracle_prefill_attention.argtypes = [P, P, P, P, I, P, I, I, P, I, I, D]
-        lib.oracle_prefill_attention.restype = I
+        lib.oracle_prefill_append_rope_bt.argtypes = [P, P, P, P, P, I, P, I, I, P, I, I, P, P, P,
+                                                       I]
+        lib.oracle_prefill_append_rope_bt.restype = I
+        lib.oracle_prefill_attention_bt.argtypes = [P, P, P, P, I, P, I, I, P, I, I, D, I]
+        lib.oracle_prefill_attention_bt.restype = I
         lib.oracle_free_bt.argtypes = [P, I, P, I, I, P, P, P, I, I]
         lib.oracle_free_bt.restype = I
         _lib = lib
@@ -211,9 +212,10 @@ def kv_append_rope(k_new, v_new, q, pool, block_table, context_lens, layer,
 
 
 def prefill_append_rope(k_new, v_new, q, cu_tokens, pool, block_table, context_lens, layer,
-                        free_list, free_count, num_blocks=None):
+                        free_list, free_count, num_blocks=None, block_tokens=BLOCK):
     """Returns (q_rot or None, pool, block_table, free_list, free_count, err)
-    on copies; the inputs are not modified."""
+    on copies; the inputs are not modified.  Pages of block_tokens tokens:
+    pool [num_blocks][2][block_tokens][8][64]."""
     k_new = _c(k_new, np.uint16)
     v_new = _c(v_new, np.uint16)
     qc = None if q is None else np.array(q, dtype=np.uint16, copy=True, order="C")
@@ -226,15 +228,16 @@ def prefill_append_rope(k_new, v_new, q, cu_tokens, pool, block_table, context_l
     inv = llama3_inv_freq()
     n, n_layers, max_blocks = btc.shape
     nb = poolc.shape[0] if num_blocks is None else num_blocks
-    err = _load().oracle_prefill_append_rope(_ptr(k_new), _ptr(v_new), _ptr(qc), _ptr(cu),
-                                             _ptr(poolc), nb, _ptr(btc), n_layers, max_blocks,
-                                             _ptr(ctx), n, layer, _ptr(flc), _ptr(fc), _ptr(inv))
+    err = _load().oracle_prefill_append_rope_bt(_ptr(k_new), _ptr(v_new), _ptr(qc), _ptr(cu),
+                                                _ptr(poolc), nb, _ptr(btc), n_layers, max_blocks,
+                                                _ptr(ctx), n, layer, _ptr(flc), _ptr(fc), _ptr(inv),
+                                                int(block_tokens))
     return qc, poolc, btc, flc, int(fc[0]), err
 
 
 def prefill_attention(q, cu_tokens, pool, block_table, context_lens, layer, scale=0.125,
-                      num_blocks=None):
-    """out[rows][32][64] fp64 and the error bits."""
+                      num_blocks=None, block_tokens=BLOCK):
+    """out[rows][32][64] fp64 and the error bits; pages of block_tokens tokens."""
     q = _c(q, np.uint16)
     cu = _c(cu_tokens, np.int32)
     pool = _c(pool, np.uint16)
@@ -243,8 +246,9 @@ def prefill_attention(q, cu_tokens, pool, block_table, context_lens, layer, scal
     n, n_layers, max_blocks = bt.shape
     nb = pool.shape[0] if num_blocks is None else num_blocks
     out = np.zeros((q.shape[0], N_Q, HEAD_DIM), dtype=np.float64)
-    err = _load().oracle_prefill_attention(_ptr(out), _ptr(q), _ptr(cu), _ptr(pool), nb, _ptr(bt),
-                                           n_layers, max_blocks, _ptr(ctx), n, layer, float(scale))
+    err = _load().oracle_prefill_attention_bt(_ptr(out), _ptr(q), _ptr(cu), _ptr(pool), nb,
+                                              _ptr(bt), n_layers, max_blocks, _ptr(ctx), n, layer,
+                                              float(scale), int(block_tokens))
     if err < 0:
         raise MemoryError("oracle allocation failed")
     return out, err

@@ -315,20 +315,20 @@ int oracle_kv_append_rope(const uint16_t *k_new, const uint16_t *v_new,
  * ("The path of one inference": prefill() is matrix x matrix, decode is
  * vector x matrix; ropeKernel_llama3 rotates all prompt tokens).  Here a
  * prompt chunk is appended to the paged cache and attends causally. */
-int oracle_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
-                               uint16_t *q_or_null, const int32_t *cu_tokens,
-                               uint16_t *pool, int num_blocks, int32_t *block_table,
-                               int n_layers, int max_blocks_per_seq,
-                               const int32_t *context_lens, int num_seqs, int layer,
-                               int32_t *free_list, int32_t *free_count,
-                               const double *inv_freq)
+int oracle_prefill_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                                  uint16_t *q_or_null, const int32_t *cu_tokens,
+                                  uint16_t *pool, int num_blocks, int32_t *block_table,
+                                  int n_layers, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int num_seqs, int layer,
+                                  int32_t *free_list, int32_t *free_count,
+                                  const double *inv_freq, int bt)
 {
     int err = 0;
     double x[HD], y[HD];
     for (int s = 0; s < num_seqs; ++s) {
         int ctx = context_lens[s];
         int n = cu_tokens[s + 1] - cu_tokens[s];
-        if (ctx < 0 || n < 0 || ctx + n > max_blocks_per_seq * BS) { err |= PAO_ERR_CTX_RANGE; continue; }
+        if (ctx < 0 || n < 0 || ctx + n > max_blocks_per_seq * bt) { err |= PAO_ERR_CTX_RANGE; continue; }
         int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
         int refused = -1;   /* page of this chunk the free list could not give */
         for (int i = 0; i < n; ++i) {
@@ -342,33 +342,75 @@ int oracle_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
                     for (int d = 0; d < HD; ++d) qh[d] = oracle_double_to_bf16(y[d]);
                 }
             }
-            if (pos % BS == 0) {
+            if (pos % bt == 0) {
                 if (*free_count <= 0) {
                     err |= PAO_ERR_FREE_UNDERFLOW;
-                    row[pos / BS] = -1;
-                    refused = pos / BS;
+                    row[pos / bt] = -1;
+                    refused = pos / bt;
                     continue;
                 }
-                row[pos / BS] = free_list[*free_count - 1];
+                row[pos / bt] = free_list[*free_count - 1];
                 *free_count -= 1;
             }
-            if (pos / BS == refused) continue;          /* already reported */
-            int blk = row[pos / BS];
+            if (pos / bt == refused) continue;          /* already reported */
+            int blk = row[pos / bt];
             if (!check_block(blk, num_blocks)) { err |= PAO_ERR_BAD_BLOCK; continue; }
-            int slot = pos % BS;
+            int slot = pos % bt;
             for (int h = 0; h < HKV; ++h) {
                 const uint16_t *k = k_new + (r * HKV + h) * HD;
                 const uint16_t *v = v_new + (r * HKV + h) * HD;
                 for (int d = 0; d < HD; ++d) x[d] = oracle_bf16_to_double(k[d]);
                 oracle_rope_rotate(x, HD, (double)pos, inv_freq, y);
                 for (int d = 0; d < HD; ++d) {
-                    pool[pool_index(blk, 0, slot, h, d, BS)] = oracle_double_to_bf16(y[d]);
-                    pool[pool_index(blk, 1, slot, h, d, BS)] = v[d];
+                    pool[pool_index(blk, 0, slot, h, d, bt)] = oracle_double_to_bf16(y[d]);
+                    pool[pool_index(blk, 1, slot, h, d, bt)] = v[d];
                 }
             }
         }
     }
     return err;
+}
+
+int oracle_prefill_attention_bt(double *out, const uint16_t *q, const int32_t *cu_tokens,
+                                const uint16_t *pool, int num_blocks,
+                                const int32_t *block_table, int n_layers,
+                                int max_blocks_per_seq, const int32_t *context_lens,
+                                int num_seqs, int layer, double scale, int bt)
+{
+    int err = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        int ctx = context_lens[s];
+        int n = cu_tokens[s + 1] - cu_tokens[s];
+        if (ctx < 0 || n < 0 || ctx + n > max_blocks_per_seq * bt) { err |= PAO_ERR_CTX_RANGE; continue; }
+        const int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
+        for (int i = 0; i < n; ++i) {
+            size_t r = (size_t)cu_tokens[s] + (size_t)i;
+            for (int h = 0; h < HQ; ++h) {
+                double *o = out + (r * HQ + h) * HD;
+                double m, l;
+                int e = oracle_attention_partial_bt(q + (r * HQ + h) * HD, pool, num_blocks, row,
+                                                    h / GQA, 0, ctx + i + 1, scale, &m, &l, o, bt);
+                if (e < 0) return e;
+                err |= e;
+                for (int d = 0; d < HD; ++d) o[d] = (l > 0.0) ? o[d] / l : 0.0;
+            }
+        }
+    }
+    return err;
+}
+
+int oracle_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                               uint16_t *q_or_null, const int32_t *cu_tokens,
+                               uint16_t *pool, int num_blocks, int32_t *block_table,
+                               int n_layers, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int layer,
+                               int32_t *free_list, int32_t *free_count,
+                               const double *inv_freq)
+{
+    return oracle_prefill_append_rope_bt(k_new, v_new, q_or_null, cu_tokens, pool, num_blocks,
+                                         block_table, n_layers, max_blocks_per_seq,
+                                         context_lens, num_seqs, layer, free_list, free_count,
+                                         inv_freq, BS);
 }
 
 int oracle_prefill_attention(double *out, const uint16_t *q, const int32_t *cu_tokens,
@@ -377,26 +419,9 @@ int oracle_prefill_attention(double *out, const uint16_t *q, const int32_t *cu_t
                              int max_blocks_per_seq, const int32_t *context_lens,
                              int num_seqs, int layer, double scale)
 {
-    int err = 0;
-    for (int s = 0; s < num_seqs; ++s) {
-        int ctx = context_lens[s];
-        int n = cu_tokens[s + 1] - cu_tokens[s];
-        if (ctx < 0 || n < 0 || ctx + n > max_blocks_per_seq * BS) { err |= PAO_ERR_CTX_RANGE; continue; }
-        const int32_t *row = block_table + bt_row(s, n_layers, layer, max_blocks_per_seq);
-        for (int i = 0; i < n; ++i) {
-            size_t r = (size_t)cu_tokens[s] + (size_t)i;
-            for (int h = 0; h < HQ; ++h) {
-                double *o = out + (r * HQ + h) * HD;
-                double m, l;
-                int e = oracle_attention_partial(q + (r * HQ + h) * HD, pool, num_blocks, row,
-                                                 h / GQA, 0, ctx + i + 1, scale, &m, &l, o);
-                if (e < 0) return e;
-                err |= e;
-                for (int d = 0; d < HD; ++d) o[d] = (l > 0.0) ? o[d] / l : 0.0;
-            }
-        }
-    }
-    return err;
+    return oracle_prefill_attention_bt(out, q, cu_tokens, pool, num_blocks, block_table, n_layers,
+                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                       BS);
 }
 
 /* ---------------------------------------------------------------- free ---

@@ -135,6 +135,18 @@ int oracle_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
 int oracle_free_bt(const int32_t *seq_ids, int n_free, int32_t *block_table,
                    int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
                    int32_t *free_list, int32_t *free_count, int num_blocks, int bt);
+int oracle_prefill_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                                  uint16_t *q_or_null, const int32_t *cu_tokens,
+                                  uint16_t *pool, int num_blocks, int32_t *block_table,
+                                  int n_layers, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int num_seqs, int layer,
+                                  int32_t *free_list, int32_t *free_count,
+                                  const double *inv_freq, int bt);
+int oracle_prefill_attention_bt(double *out, const uint16_t *q, const int32_t *cu_tokens,
+                                const uint16_t *pool, int num_blocks,
+                                const int32_t *block_table, int n_layers,
+                                int max_blocks_per_seq, const int32_t *context_lens,
+                                int num_seqs, int layer, double scale, int bt);
 
 /* Release the blocks of finished sequences.  Returns error bits. */
 int oracle_free(const int32_t *seq_ids, int n_free, int32_t *block_table,

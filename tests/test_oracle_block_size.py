@@ -7,7 +7,9 @@ list and the -1 entries).  The pins: attention over the same tokens is the
 same whatever the page size (bit for bit: the oracle sums in token order),
 and equal to torch's attention on the contiguous tokens; hand-worked appends
 at 8 and 32 tokens per page; token-by-token appends read back at every
-position; free returns ceil(ctx / page) pages per layer.
+position; free returns ceil(ctx / page) pages per layer; prefill attention
+the same at every page size and equal to causal attention on the contiguous
+tokens; a prefill append equal to single-token appends of the same tokens.
 """
 import json
 import os
@@ -135,3 +137,88 @@ def test_free_returns_ceil_pages(bt):
                                   block_tokens=bt)
     assert err == 0 and c2 == nb and (b2 == -1).all()
     assert sorted(f2.tolist()) == list(range(nb))
+
+
+# ---------------------------------------------------------------- prefill
+def _cu(lens):
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+
+def test_prefill_attention_is_the_same_for_every_page_size():
+    """Prompt chunks after cached contexts: the same tokens in pools of 8-,
+    16- and 32-token pages give the same output bit for bit, equal to causal
+    attention over the contiguous tokens."""
+    rng = np.random.default_rng(3)
+    ctxs, lens = [0, 5, 31, 40], [9, 20, 2, 33]
+    tot = [c + n for c, n in zip(ctxs, lens)]
+    K = [wl.normal_bf16(rng, (t, N_KV, D)) for t in tot]
+    V = [wl.normal_bf16(rng, (t, N_KV, D)) for t in tot]
+    q = wl.normal_bf16(rng, (sum(lens), N_Q, D), scale=2.0)
+    cu = _cu(lens)
+    outs = {}
+    for bt in (8, 16, 32):
+        pool, table = _paged(rng, K, V, tot, bt)
+        out, err = oracle.prefill_attention(q, cu, pool, table, np.array(ctxs, np.int32), 0,
+                                            block_tokens=bt)
+        assert err == 0
+        outs[bt] = out
+    assert np.array_equal(outs[8], outs[16]) and np.array_equal(outs[32], outs[16])
+    for s, (c, n) in enumerate(zip(ctxs, lens)):
+        qs = torch.from_numpy(oracle.bf16_to_f64(q[cu[s]:cu[s + 1]]))      # [n][32][64]
+        ks = torch.from_numpy(oracle.bf16_to_f64(K[s]))                      # [c+n][8][64]
+        vs = torch.from_numpy(oracle.bf16_to_f64(V[s]))
+        qh = qs.permute(1, 0, 2)                                             # [32][n][64]
+        kh = ks.permute(1, 0, 2).repeat_interleave(4, dim=0)                 # [32][c+n][64]
+        vh = vs.permute(1, 0, 2).repeat_interleave(4, dim=0)
+        # row i sees keys 0 .. c + i
+        mask = torch.arange(c + n)[None, :] <= (c + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask,
+                                                               scale=0.125)
+        assert np.allclose(outs[16][cu[s]:cu[s + 1]], ref.permute(1, 0, 2).numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("bt", [8, 16, 32])
+def test_prefill_append_equals_token_by_token_appends(bt):
+    """A chunk per sequence appended at once leaves the table, free list and
+    pool exactly as single-token appends of the same tokens, sequence by
+    sequence in position order, do."""
+    rng = np.random.default_rng(10 + bt)
+    ctxs, lens = [0, bt - 1, bt, 2 * bt + 3], [bt + 5, 1, 2 * bt, 3]
+    mb = max((c + n + bt - 1) // bt for c, n in zip(ctxs, lens)) + 1
+    old = [(c + bt - 1) // bt for c in ctxs]
+    nb = sum(old) + sum((c + n + bt - 1) // bt - o for c, n, o in zip(ctxs, lens, old)) + 3
+    ids = rng.permutation(nb).astype(np.int32)
+    table = np.full((len(ctxs), 1, mb), -1, np.int32)
+    used = 0
+    for s, o in enumerate(old):
+        table[s, 0, :o] = ids[used:used + o]
+        used += o
+    fl = np.full(nb, -1, np.int32)
+    fl[:nb - used] = ids[used:]
+    fc = nb - used
+    pool = wl.normal_bf16(rng, (nb, 2, bt, N_KV, D))
+    T = sum(lens)
+    k = wl.normal_bf16(rng, (T, N_KV, D))
+    v = wl.normal_bf16(rng, (T, N_KV, D))
+    q = wl.normal_bf16(rng, (T, N_Q, D))
+    cu = _cu(lens)
+    q1, p1, b1, f1, c1, err = oracle.prefill_append_rope(k, v, q, cu, pool, table, ctxs, 0, fl, fc,
+                                                         block_tokens=bt)
+    assert err == 0
+    p2, b2, f2, c2 = pool, table, fl, fc
+    q2 = np.empty_like(q)
+    for s, (c, n) in enumerate(zip(ctxs, lens)):
+        for i in range(n):
+            r = cu[s] + i
+            one = [s]   # a one-sequence call on table row s
+            qr, p2, bs, f2, c2, e = oracle.kv_append_rope(k[r:r + 1], v[r:r + 1], q[r:r + 1], p2,
+                                                          b2[one], [c + i], 0, f2, c2,
+                                                          block_tokens=bt)
+            assert e == 0
+            b2 = b2.copy()
+            b2[s] = bs[0]
+            q2[r] = qr[0]
+    assert np.array_equal(b1, b2) and c1 == c2 and np.array_equal(f1[:c1], f2[:c2])
+    assert np.array_equal(p1, p2) and np.array_equal(q1, q2)
+    # pages opened per sequence: ceil((ctx + n) / bt) - ceil(ctx / bt)
+    assert fc - c1 == sum((c + n + bt - 1) // bt - (c + bt - 1) // bt for c, n in zip(ctxs, lens))
