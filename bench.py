@@ -617,27 +617,29 @@ def prefill_oracle_sample(w, rng, max_tokens: int):
     and the attention FLOPs they stand for."""
     ctx = int(w.context_lens[0])
     n = max(1, min(int(w.chunk_lens[0]), int(max_tokens)))
-    old = (ctx + BS - 1) // BS
-    need = (ctx + n + BS - 1) // BS
+    page = w.block_tokens
+    old = (ctx + page - 1) // page
+    need = (ctx + n + page - 1) // page
     nb = need + 1
     ids = rng.permutation(nb).astype(np.int32)
     bt = np.full((1, 1, need + 1), -1, dtype=np.int32)
     bt[0, 0, :old] = ids[:old]
     free = ids[old:]
-    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    pool = wl.normal_bf16(rng, (nb, 2, page, N_KV, D))
     k = wl.normal_bf16(rng, (n, N_KV, D))
     v = wl.normal_bf16(rng, (n, N_KV, D))
     q = wl.normal_bf16(rng, (n, N_Q, D))
     u = dict(k=k, v=v, q=q, pool=pool, bt=bt, ctx=np.array([ctx], np.int32),
-             cu=np.array([0, n], np.int32), fl=free, fc=len(free))
+             cu=np.array([0, n], np.int32), fl=free, fc=len(free), page=page)
     return u, prefill_attention_flops(np.array([ctx]), np.array([n]))
 
 
 def prefill_oracle_run(u, scale):
     import oracle
     q2, p2, b2, _, _, _ = oracle.prefill_append_rope(u["k"], u["v"], u["q"], u["cu"], u["pool"],
-                                                     u["bt"], u["ctx"], 0, u["fl"], u["fc"])
-    oracle.prefill_attention(q2, u["cu"], p2, b2, u["ctx"], 0, scale)
+                                                     u["bt"], u["ctx"], 0, u["fl"], u["fc"],
+                                                     block_tokens=u["page"])
+    oracle.prefill_attention(q2, u["cu"], p2, b2, u["ctx"], 0, scale, block_tokens=u["page"])
 
 
 def prefill_cpu_rate(w, rng, budget_s: float):
@@ -676,7 +678,7 @@ def prefill_cpu_baseline(w, budget_s: float = 12.0):
 def run_prefill_reference(args, rank, world):
     if rank != 0:
         return
-    w = wl.make_prefill_workload(args.workload)
+    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens)
     rng = np.random.default_rng(w.seed + 91)
     per_step_budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
     _, m, _ = prefill_cpu_rate(w, rng, per_step_budget * 4)
@@ -706,7 +708,7 @@ def run_prefill_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {PREFILL_DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{args.workload}: {prefill_description(args.workload, w)}",
                    "sample_per_step": f"the first {m} tokens of one chunk in one layer, "
                                       "scaled to the step by attention FLOPs"},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -727,13 +729,20 @@ PREFILL_DESCRIPTIONS = {
 }
 
 
+def prefill_description(name, w):
+    d = PREFILL_DESCRIPTIONS[name]
+    if w.block_tokens != BS:
+        d += f"; here {w.block_tokens}-token pages ({w.num_blocks:,} blocks, the same bytes)"
+    return d
+
+
 def run_prefill_gpu(args, rank, world, dist):
     import torch
     import paged_kv_cache_205_gb300 as pk
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda")
-    w = wl.make_prefill_workload(args.workload)
+    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens)
     L, T, n = w.n_layers, w.total_tokens, w.num_seqs
     seed = w.seed + 1000 * rank
     pool = wl.make_prefill_pool_torch(w, dev, seed)
@@ -876,10 +885,11 @@ def run_prefill_gpu(args, rank, world, dist):
         "accumulate": "fp32",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {PREFILL_DESCRIPTIONS[args.workload]}",
+            "workload": f"{args.workload}: {prefill_description(args.workload, w)}",
             "num_seqs": n,
             "n_layers": L,
             "tokens_per_step": T,
+            "block_tokens": w.block_tokens,
             "attention_flops_per_step": flops * L,
             "l2": "inputs larger than L2: each step reads and writes "
                   f"{(q.numel() + out.numel() + k.numel() + v.numel()) * 2 / 2**20:.0f} MiB "
@@ -895,8 +905,8 @@ def run_prefill_gpu(args, rank, world, dist):
             "peak_kind": f"{peak_kind} dense bf16 (burst: the kernel timed alone)",
             "unit": "TFLOP/s",
             "frac": achieved / peak,
-            "traffic": profiled_traffic(args.workload, "prefill_attention_kernel",
-                                        PREFILL_SOURCES),
+            "traffic": (profiled_traffic(args.workload, "prefill_attention_kernel",
+                                         PREFILL_SOURCES) if w.block_tokens == BS else None),
             "flops_per_launch": flops,
             "ms_per_launch": attn_ms,
             "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "

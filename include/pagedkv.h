@@ -172,7 +172,9 @@ int pa_decode_attention_static(uint16_t *out, const uint16_t *q, const uint16_t 
  * append at position pos takes a new block when pos % block_tokens == 0.
  * Everything else (arguments, layouts, errors) is as above; another
  * block_tokens returns PA_ERR_ARG (0 from the workspace size).  The prefill
- * entry points and the batcher use 16-token pages.
+ * entry points have the same variants (pa_prefill_append_rope_bt,
+ * pa_prefill_attention_bt, declared with them below); the batcher uses
+ * 16-token pages.
  */
 int pa_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
                          uint16_t *kv_cache, int num_blocks, int block_tokens,
@@ -256,6 +258,28 @@ int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_tokens,
                          const int32_t *block_table, int n_layers, int max_blocks_per_seq,
                          const int32_t *context_lens, int num_seqs, int layer, float scale,
                          int32_t *err, void *stream);
+
+/*
+ * pa_prefill_append_rope_bt / pa_prefill_attention_bt -- the two prefill
+ * entry points above with pages of block_tokens = 8, 16 or 32 tokens (the
+ * page's BLOCK_SIZE, 16, as a tunable; the pool [num_blocks][2][block_tokens]
+ * [8][64] bf16, token t of a sequence in block block_table[s][layer]
+ * [t / block_tokens], slot t % block_tokens; a chunk opens a page at every
+ * position that is a multiple of block_tokens).  Arguments, layouts, errors
+ * and stream behaviour are those of the calls above; another block_tokens
+ * returns PA_ERR_ARG before any launch.
+ */
+int pa_prefill_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                              int total_tokens, const int32_t *cu_tokens, uint16_t *kv_cache,
+                              int num_blocks, int block_tokens, int32_t *block_table,
+                              int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                              int num_seqs, int layer, int32_t *free_list, int32_t *free_count,
+                              int32_t *err, void *stream);
+int pa_prefill_attention_bt(uint16_t *out, const uint16_t *q, int total_tokens,
+                            const int32_t *cu_tokens, const uint16_t *kv_cache, int num_blocks,
+                            int block_tokens, const int32_t *block_table, int n_layers,
+                            int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                            int layer, float scale, int32_t *err, void *stream);
 
 /* Bytes of workspace pa_decode_attention needs on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq);

@@ -230,6 +230,7 @@ class PrefillWorkload:
     free_count: int
     scale: float = 0.125
     seed: int = 0
+    block_tokens: int = BLOCK         # tokens per page
 
     @property
     def num_seqs(self) -> int:
@@ -252,21 +253,28 @@ PREFILL_WORKLOADS = {
 }
 
 
-def make_prefill_workload(name: str, seed: int | None = None) -> PrefillWorkload:
+def make_prefill_workload(name: str, seed: int | None = None,
+                          block_tokens: int = BLOCK) -> PrefillWorkload:
     """prompts17_14: the page's two prompts (17 and 14 tokens), one layer.
     prefill8x2k: 8 fresh 2048-token prompts through 16 layers, 65,536-block
     pool.  chunked32x512: 32 sequences with 4096 tokens paged already append
     a 512-token chunk each, 16 layers, 262,144-block pool.  Cached pages are
     popped from a shuffled free list; the chunks' pages come from what is
-    left of it."""
+    left of it.  With block_tokens other than 16 the pool keeps its bytes
+    (16 / page times the blocks) and the tables hold pages of that many
+    tokens."""
+    if block_tokens not in (8, 16, 32):
+        raise ValueError("pages of 8, 16 or 32 tokens")
     sd, n_layers, ctx, lens, num_blocks = PREFILL_WORKLOADS[name]
+    num_blocks = num_blocks * BLOCK // block_tokens
     rng = np.random.default_rng(sd if seed is None else seed)
     ctx = np.array(ctx, dtype=np.int32)
     lens = np.array(lens, dtype=np.int32)
-    max_blocks = int(((ctx + lens + BLOCK - 1) // BLOCK).max()) + 1
-    bt, free_list, top = _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks)
+    max_blocks = int(((ctx + lens + block_tokens - 1) // block_tokens).max()) + 1
+    bt, free_list, top = _assign_tables(rng, ctx, n_layers, num_blocks, max_blocks,
+                                        block_tokens=block_tokens)
     return PrefillWorkload(name, n_layers, ctx, lens, num_blocks, max_blocks, bt, free_list, top,
-                           seed=sd if seed is None else seed)
+                           seed=sd if seed is None else seed, block_tokens=block_tokens)
 
 
 def live_mask(w: Workload, context_lens=None) -> np.ndarray:
@@ -350,7 +358,7 @@ def make_prefill_pool_torch(w: PrefillWorkload, device, seed: int):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
-    pool = torch.empty((w.num_blocks, 2, BLOCK, N_KV, HEAD_DIM), dtype=torch.bfloat16,
+    pool = torch.empty((w.num_blocks, 2, w.block_tokens, N_KV, HEAD_DIM), dtype=torch.bfloat16,
                        device=device)
     flat = pool.view(-1)
     chunk = 1 << 28

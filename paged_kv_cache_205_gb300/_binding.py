@@ -35,6 +35,8 @@ _EXPORTS = (
     "pa_decode_attention_bt",
     "pa_free_bt",
     "pa_decode_workspace_size_bt",
+    "pa_prefill_append_rope_bt",
+    "pa_prefill_attention_bt",
     "pa_decode_set_grid_limit",
     "pa_error_string",
     "pa_batcher_ctl_bytes",
@@ -110,6 +112,11 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_kv_append_rope_bt.restype = I
         lib.pa_decode_attention_bt.argtypes = [P, P, P, I, I, P, I, I, P, I, I, F, P, Z, P, P]
         lib.pa_decode_attention_bt.restype = I
+        lib.pa_prefill_append_rope_bt.argtypes = [P, P, P, I, P, P, I, I, P, I, I, P, I, I, P, P, P,
+                                                  P]
+        lib.pa_prefill_append_rope_bt.restype = I
+        lib.pa_prefill_attention_bt.argtypes = [P, P, I, P, P, I, I, P, I, I, P, I, I, F, P, P]
+        lib.pa_prefill_attention_bt.restype = I
         lib.pa_free_bt.argtypes = [P, I, I, P, I, I, P, P, P, I, P, P]
         lib.pa_free_bt.restype = I
         lib.pa_decode_workspace_size_bt.argtypes = [I, I, I]
@@ -239,35 +246,46 @@ def pa_prefill_append_rope(k_new, v_new, q_or_null, cu_tokens, kv_cache, block_t
                            context_lens, layer, free_list, free_count, err, stream=None):
     """Packed prompt chunks: k_new/v_new [T][8][64], q_or_null [T][32][64] or None,
     cu_tokens int32 [n+1] (rows of sequence s: cu_tokens[s] .. cu_tokens[s+1]-1);
-    block_table [n][L][max_blocks] int32."""
+    kv_cache [num_blocks][2][page][8][64] bf16 (page 16: pa_prefill_append_rope;
+    8 or 32: pa_prefill_append_rope_bt); block_table [n][L][max_blocks] int32."""
     n, n_layers, max_blocks = block_table.shape
     if cu_tokens.numel() != n + 1:
         raise ValueError("cu_tokens must hold num_seqs + 1 entries")
-    rc = library().pa_prefill_append_rope(
-        _dev(k_new, "k_new", _bf16()), _dev(v_new, "v_new", _bf16()),
-        _dev(q_or_null, "q_or_null", _bf16(), optional=True), int(k_new.shape[0]),
-        _dev(cu_tokens, "cu_tokens", _i32()),
-        _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]),
-        _dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
-        _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
-        _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
-        _dev(err, "err", _i32()), _stream(stream))
-    _check("pa_prefill_append_rope", rc)
+    page = _page_tokens(kv_cache)
+    args = (_dev(k_new, "k_new", _bf16()), _dev(v_new, "v_new", _bf16()),
+            _dev(q_or_null, "q_or_null", _bf16(), optional=True), int(k_new.shape[0]),
+            _dev(cu_tokens, "cu_tokens", _i32()),
+            _dev(kv_cache, "kv_cache", _bf16()), int(kv_cache.shape[0]))
+    rest = (_dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+            _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
+            _dev(free_list, "free_list", _i32()), _dev(free_count, "free_count", _i32()),
+            _dev(err, "err", _i32()), _stream(stream))
+    if page == PA_BLOCK_TOKENS:
+        _check("pa_prefill_append_rope", library().pa_prefill_append_rope(*args, *rest))
+    else:
+        _check("pa_prefill_append_rope_bt",
+               library().pa_prefill_append_rope_bt(*args, page, *rest))
 
 
 def pa_prefill_attention(out, q, cu_tokens, kv_cache, block_table, context_lens, layer, scale,
                          err, stream=None):
-    """out/q [T][32][64] bf16, packed as for pa_prefill_append_rope."""
+    """out/q [T][32][64] bf16, packed as for pa_prefill_append_rope; kv_cache
+    [num_blocks][2][page][8][64] (page 16: pa_prefill_attention; 8 or 32:
+    pa_prefill_attention_bt)."""
     n, n_layers, max_blocks = block_table.shape
     if cu_tokens.numel() != n + 1:
         raise ValueError("cu_tokens must hold num_seqs + 1 entries")
-    rc = library().pa_prefill_attention(
-        _dev(out, "out", _bf16()), _dev(q, "q", _bf16()), int(q.shape[0]),
-        _dev(cu_tokens, "cu_tokens", _i32()), _dev(kv_cache, "kv_cache", _bf16()),
-        int(kv_cache.shape[0]), _dev(block_table, "block_table", _i32()), int(n_layers),
-        int(max_blocks), _dev(context_lens, "context_lens", _i32()), int(n), int(layer),
-        float(scale), _dev(err, "err", _i32()), _stream(stream))
-    _check("pa_prefill_attention", rc)
+    page = _page_tokens(kv_cache)
+    args = (_dev(out, "out", _bf16()), _dev(q, "q", _bf16()), int(q.shape[0]),
+            _dev(cu_tokens, "cu_tokens", _i32()), _dev(kv_cache, "kv_cache", _bf16()),
+            int(kv_cache.shape[0]))
+    rest = (_dev(block_table, "block_table", _i32()), int(n_layers), int(max_blocks),
+            _dev(context_lens, "context_lens", _i32()), int(n), int(layer), float(scale),
+            _dev(err, "err", _i32()), _stream(stream))
+    if page == PA_BLOCK_TOKENS:
+        _check("pa_prefill_attention", library().pa_prefill_attention(*args, *rest))
+    else:
+        _check("pa_prefill_attention_bt", library().pa_prefill_attention_bt(*args, page, *rest))
 
 
 def pa_decode_workspace_size(num_seqs: int, max_blocks_per_seq: int,

@@ -283,16 +283,19 @@ struct PrefillAppendParams {
   int layer;
 };
 
-// Whether sequence s's chunk is accepted: it fits the sequence's table and
-// its rows lie inside [0, total_tokens).  Sets the context and chunk length.
+// Whether sequence s's chunk is accepted: it fits the sequence's table (of
+// max_blocks pages of BT tokens) and its rows lie inside [0, total_tokens).
+// Sets the context and chunk length.
+template <int BT>
 __device__ __forceinline__ bool chunk_fits(const PrefillAppendParams &p, int s, int *ctx, int *n) {
   const int c0 = p.cu_tokens[s], c1 = p.cu_tokens[s + 1];
   *ctx = p.context_lens[s];
   *n = c1 - c0;
   return *ctx >= 0 && *n >= 0 && c0 >= 0 && c1 <= p.total_tokens &&
-         static_cast<long long>(*ctx) + *n <= static_cast<long long>(p.max_blocks) * kBs;
+         static_cast<long long>(*ctx) + *n <= static_cast<long long>(p.max_blocks) * BT;
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendParams p) {
   __shared__ int tot[kScanCta / 32];
   __shared__ int incl_s[kScanCta];    // pages of the batch's sequences up to and including each
@@ -306,11 +309,11 @@ __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendPa
     const int s = base + threadIdx.x;
     int ctx = 0, n = 0, first = 0, pages = 0;
     if (s < p.num_seqs) {
-      if (!chunk_fits(p, s, &ctx, &n)) {
+      if (!chunk_fits<BT>(p, s, &ctx, &n)) {
         report(p.err, PA_DEV_CTX_RANGE);
       } else {
-        first = (ctx + kBs - 1) / kBs;                 // pages already open
-        pages = (ctx + n + kBs - 1) / kBs - first;     // pages this chunk opens
+        first = (ctx + BT - 1) / BT;                 // pages already open
+        pages = (ctx + n + BT - 1) / BT - first;     // pages this chunk opens
       }
     }
     // pages are ranked over the sequences in order: a prefix sum
@@ -359,7 +362,10 @@ __global__ void __launch_bounds__(kScanCta) prefill_alloc_kernel(PrefillAppendPa
   if (threadIdx.x == 0) *p.free_count = max(fc0 - served, 0);
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillAppendParams p) {
+  constexpr size_t kPageBytes = static_cast<size_t>(BT) * 2 * kTokRowBytes;   // K and V
+  constexpr size_t kHalfPageBytes = static_cast<size_t>(BT) * kTokRowBytes;
   __shared__ float2 cs[kStoreRows][kD / 2];
   __shared__ int row_seq[kStoreRows];     // -1: the row lies in no accepted chunk
   __shared__ int row_pos[kStoreRows];
@@ -383,10 +389,10 @@ __global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillApp
       }
       int ctx, n;
       // a refused chunk is reported by the allocation kernel
-      if (chunk_fits(p, lo, &ctx, &n) && r >= p.cu_tokens[lo] && r < p.cu_tokens[lo + 1]) {
+      if (chunk_fits<BT>(p, lo, &ctx, &n) && r >= p.cu_tokens[lo] && r < p.cu_tokens[lo + 1]) {
         seq = lo;
         pos = ctx + (r - p.cu_tokens[lo]);
-        open = (ctx + kBs - 1) / kBs;
+        open = (ctx + BT - 1) / BT;
       }
     }
     row_seq[tid] = seq;
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillApp
     int blk = -1;
     const int s = row_seq[tid];
     if (s >= 0) {
-      const int page = row_pos[tid] / kBs;
+      const int page = row_pos[tid] / BT;
       const bool new_page = page >= row_open[tid];
       if (new_page) pdl_wait_primary();   // its entry comes from the allocation kernel
       blk = p.block_table[table_row(s, p.n_layers, p.layer, p.max_blocks) + page];
@@ -451,15 +457,15 @@ __global__ void __launch_bounds__(kStoreThreads) prefill_store_kernel(PrefillApp
     }
     const int blk = row_blk[i];
     if (blk < 0) continue;
-    unsigned char *block = p.kv + static_cast<size_t>(blk) * kBlockBytes;
-    const int slot = row_pos[i] % kBs;
+    unsigned char *block = p.kv + static_cast<size_t>(blk) * kPageBytes;
+    const int slot = row_pos[i] % BT;
     if (head < kHkv) {
       unsigned char *krow = block + slot * kTokRowBytes + head * kHeadRowBytes;
       *reinterpret_cast<uint2 *>(krow + 8 * j) = rlo;
       *reinterpret_cast<uint2 *>(krow + kD + 8 * j) = rhi;
     }
     if (tid < kTokRowBytes / 16)
-      reinterpret_cast<uint4 *>(block + kHalfBlockBytes + slot * kTokRowBytes)[tid] = v[i];
+      reinterpret_cast<uint4 *>(block + kHalfPageBytes + slot * kTokRowBytes)[tid] = v[i];
   }
   pdl_wait_primary();   // this grid ends after the allocation kernel
 }
@@ -625,17 +631,19 @@ extern "C" int pa_kv_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new
   }
 }
 
-extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
-                                      uint16_t *q_or_null, int total_tokens,
-                                      const int32_t *cu_tokens, uint16_t *kv_cache, int num_blocks,
-                                      int32_t *block_table, int n_layers, int max_blocks_per_seq,
-                                      const int32_t *context_lens, int num_seqs, int layer,
-                                      int32_t *free_list, int32_t *free_count, int32_t *err,
-                                      void *stream) {
+namespace {
+
+template <int BT>
+int prefill_append_impl(const uint16_t *k_new, const uint16_t *v_new, uint16_t *q_or_null,
+                        int total_tokens, const int32_t *cu_tokens, uint16_t *kv_cache,
+                        int num_blocks, int32_t *block_table, int n_layers,
+                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                        int layer, int32_t *free_list, int32_t *free_count, int32_t *err,
+                        void *stream) {
   if (num_seqs < 0 || total_tokens < 0 || num_blocks <= 0 || n_layers <= 0 ||
       max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * BT > INT_MAX) return PA_ERR_ARG;
   if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
   if (num_seqs == 0 || total_tokens == 0) return PA_OK;
   if (!k_new || !v_new || !cu_tokens || !kv_cache || !block_table || !context_lens ||
@@ -667,13 +675,57 @@ extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_n
   prm.num_seqs = num_seqs;
   prm.layer = layer;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(prefill_alloc_kernel, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
+  if (launch_pdl(prefill_alloc_kernel<BT>, dim3(1), dim3(kScanCta), 0, st, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_pdl(prefill_store_kernel, dim3((total_tokens + kStoreRows - 1) / kStoreRows),
+  if (launch_pdl(prefill_store_kernel<BT>, dim3((total_tokens + kStoreRows - 1) / kStoreRows),
                  dim3(kStoreThreads), 0, st, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_prefill_append_rope(const uint16_t *k_new, const uint16_t *v_new,
+                                      uint16_t *q_or_null, int total_tokens,
+                                      const int32_t *cu_tokens, uint16_t *kv_cache, int num_blocks,
+                                      int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int layer,
+                                      int32_t *free_list, int32_t *free_count, int32_t *err,
+                                      void *stream) {
+  return prefill_append_impl<kBs>(k_new, v_new, q_or_null, total_tokens, cu_tokens, kv_cache,
+                                  num_blocks, block_table, n_layers, max_blocks_per_seq,
+                                  context_lens, num_seqs, layer, free_list, free_count, err,
+                                  stream);
+}
+
+extern "C" int pa_prefill_append_rope_bt(const uint16_t *k_new, const uint16_t *v_new,
+                                         uint16_t *q_or_null, int total_tokens,
+                                         const int32_t *cu_tokens, uint16_t *kv_cache,
+                                         int num_blocks, int block_tokens, int32_t *block_table,
+                                         int n_layers, int max_blocks_per_seq,
+                                         const int32_t *context_lens, int num_seqs, int layer,
+                                         int32_t *free_list, int32_t *free_count, int32_t *err,
+                                         void *stream) {
+  switch (block_tokens) {
+    case 8:
+      return prefill_append_impl<8>(k_new, v_new, q_or_null, total_tokens, cu_tokens, kv_cache,
+                                    num_blocks, block_table, n_layers, max_blocks_per_seq,
+                                    context_lens, num_seqs, layer, free_list, free_count, err,
+                                    stream);
+    case 16:
+      return prefill_append_impl<16>(k_new, v_new, q_or_null, total_tokens, cu_tokens, kv_cache,
+                                     num_blocks, block_table, n_layers, max_blocks_per_seq,
+                                     context_lens, num_seqs, layer, free_list, free_count, err,
+                                     stream);
+    case 32:
+      return prefill_append_impl<32>(k_new, v_new, q_or_null, total_tokens, cu_tokens, kv_cache,
+                                     num_blocks, block_table, n_layers, max_blocks_per_seq,
+                                     context_lens, num_seqs, layer, free_list, free_count, err,
+                                     stream);
+    default:
+      return PA_ERR_ARG;
+  }
 }
 
 namespace {

@@ -668,11 +668,17 @@ int make_kv_page_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
 }
 
 int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
+  return make_kv_rows_map_bt(map, kv_cache, num_blocks, kBs);
+}
+
+int make_kv_rows_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
-  const cuuint64_t dims[5] = {kD, kHkv, kBs, 2, static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[4] = {kHeadRowBytes, kTokRowBytes, kHalfBlockBytes, kBlockBytes};
-  const cuuint32_t box[5] = {kD, 1, kBs, 1, 1};
+  const cuuint64_t row = kTokRowBytes;
+  const cuuint64_t dims[5] = {kD, kHkv, static_cast<cuuint64_t>(bt), 2,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kHeadRowBytes, row, row * bt, row * bt * 2};
+  const cuuint32_t box[5] = {kD, 1, static_cast<cuuint32_t>(bt), 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -39,6 +39,8 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
 // Over a pool of 16-token pages, box (64, 1, 16, 1, 1): one kv head's K rows
 // (or V rows) of one page, 2 KiB.
 int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
+// The same for pages of bt (8, 16 or 32) tokens: box (64, 1, bt, 1, 1).
+int make_kv_rows_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt);
 
 // Decode attention with one thread-block cluster per (sequence, kv head)
 // (pa_decode_pair.cu), for 16-token pages.  decode_pair_cluster: the cluster

@@ -54,8 +54,7 @@ constexpr int kQTok = 32;                     // query tokens per half
 constexpr int kHalves = 2;
 constexpr int kCtaTok = kQTok * kHalves;      // query tokens per CTA
 constexpr int kRows = kQTok * kGqa;           // 128 MMA rows per half
-constexpr int kChunk = 128;                   // keys per chunk
-constexpr int kPagesPerChunk = kChunk / kBs;  // 8
+constexpr int kChunk = 128;                   // keys per chunk (8 pages of 16 tokens)
 constexpr int kStagesP = 5;
 constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
 constexpr int kProducerWarp = 8;
@@ -172,12 +171,21 @@ __device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams
   return it;
 }
 
+// Pages of BT tokens: a chunk spans kChunk / BT pages; bit l of a stage's
+// pmask says whether its page l was loaded.
+template <int BT>
+struct PageGeom {
+  static constexpr int kPages = kChunk / BT;
+  static constexpr int kAll = (1 << kPages) - 1;
+};
+
 // Chunk gc (counted over the CTA's items; kbase: its first key within its
 // item) has V rows that must be zeroed: rows past the tile's last key or in
 // a page that was not loaded meet P = 0 but may hold anything (NaN
 // included).
+template <int BT>
 __device__ __forceinline__ bool chunk_needs_zero(const PSmem &sm, int gc, int kbase, int n_keys) {
-  return sm.pmask[gc % kStagesP] != 0xff || kbase + kChunk > n_keys;
+  return sm.pmask[gc % kStagesP] != PageGeom<BT>::kAll || kbase + kChunk > n_keys;
 }
 
 // MMA warp: waits until chunk gc has landed (every MMA warp does, for every
@@ -185,6 +193,7 @@ __device__ __forceinline__ bool chunk_needs_zero(const PSmem &sm, int gc, int kb
 // can run ahead of the stage's fill).  The zeroing warp clears the rows above
 // before any MMA reads the stage and, with `handover`, signals the other
 // half's MMA warp through v_zeroed.
+template <int BT>
 __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, int n_keys,
                                                   bool zeroer, bool handover, int lane) {
   const int st = gc % kStagesP;
@@ -193,11 +202,11 @@ __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, 
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   __syncwarp();
-  if (zeroer && chunk_needs_zero(sm, gc, kbase, n_keys)) {
+  if (zeroer && chunk_needs_zero<BT>(sm, gc, kbase, n_keys)) {
     const int pm = sm.pmask[st];
     for (int e = lane; e < kChunk * (kTileRowBytes / 16); e += 32) {
       const int key = e >> 3;
-      if (kbase + key >= n_keys || !((pm >> (key >> 4)) & 1))
+      if (kbase + key >= n_keys || !((pm >> (key / BT)) & 1))
         reinterpret_cast<uint4 *>(sm.v[st])[e] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
@@ -234,6 +243,7 @@ __device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, in
   tc::mma_commit(&sm.o_full[h]);
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
     PrefillParams p) {
@@ -265,7 +275,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   pdl_wait_primary();   // q and the cache come from the kernels before
 
   // ---- query tiles per sequence, laid end to end
-  const long long cap = static_cast<long long>(p.max_blocks) * kBs;
+  constexpr int kPagesPerChunk = PageGeom<BT>::kPages;
+  constexpr unsigned kAllPages = PageGeom<BT>::kAll;
+  const long long cap = static_cast<long long>(p.max_blocks) * BT;
   int carry = 0;
   for (int base = 0; base < p.num_seqs; base += kPThreads) {
     const int i = base + tid;
@@ -323,14 +335,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       bool ok = true;
       int gc = 0, k = 0;
       uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last fill
-      // Lane l < 8 holds the block id of page l of a chunk.  The ids of the
+      // Lane l < kPagesPerChunk holds the block id of page l of a chunk.  The ids of the
       // next chunk (of this item or the next) are read while this chunk's
       // copies are issued, so the table read is off the producer's path.
       auto chunk_ids = [&](const Item &x, int j) -> int {
         const int32_t *row =
             p.block_table + (static_cast<size_t>(x.s) * p.n_layers + p.layer) * p.max_blocks;
-        const int pg = j * kPagesPerChunk + (lane & 7);
-        return (lane < kPagesPerChunk && pg * kBs < x.n_keys) ? row[pg] : -1;
+        const int pg = j * kPagesPerChunk + (lane & (kPagesPerChunk - 1));
+        return (lane < kPagesPerChunk && pg * BT < x.n_keys) ? row[pg] : -1;
       };
       int blk_next = -1;
       bool next_read = false;
@@ -354,8 +366,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
           const int st = gc % kStagesP;
           const uint32_t ph = (gc / kStagesP) & 1;
-          const int pg = j * kPagesPerChunk + (lane & 7);
-          const bool needed = lane < kPagesPerChunk && pg * kBs < it.n_keys;
+          const int pg = j * kPagesPerChunk + (lane & (kPagesPerChunk - 1));
+          const bool needed = lane < kPagesPerChunk && pg * BT < it.n_keys;
           const int blk = blk_next;
           if (j + 1 < it.n_chunks) {
             blk_next = chunk_ids(it, j + 1);
@@ -365,8 +377,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
             next_read = true;
           }
           const bool valid = needed && blk >= 0 && blk < p.num_blocks;
-          const unsigned vm = __ballot_sync(0xffffffffu, valid) & 0xffu;
-          const unsigned nm = __ballot_sync(0xffffffffu, needed) & 0xffu;
+          const unsigned vm = __ballot_sync(0xffffffffu, valid) & kAllPages;
+          const unsigned nm = __ballot_sync(0xffffffffu, needed) & kAllPages;
           good = 1;
           if (lane == 0) {
             if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
             } else {
               if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
               sm.pmask[st] = static_cast<int>(vm);
-              mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * kBs * kTileRowBytes);
+              mbar_arrive_expect_tx(&sm.kv_full[st], __popc(vm) * 2 * BT * kTileRowBytes);
               issued |= 1u << st;
               issued_parity = (issued_parity & ~(1u << st)) | (ph << st);
             }
@@ -382,11 +394,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           ok = __shfl_sync(0xffffffffu, good, 0) != 0;
           if (!ok) break;
           __syncwarp();
-          // lanes 0-7: K rows of page l; lanes 8-15: V rows of page l - 8
-          const int pl = lane & 7, kv = (lane >> 3) & 1;
+          // lane l < 2 kPagesPerChunk: the K rows (l < kPagesPerChunk) or the
+          // V rows of page l mod kPagesPerChunk
+          const int pl = lane & (kPagesPerChunk - 1), kv = (lane / kPagesPerChunk) & 1;
           const int pblk = __shfl_sync(0xffffffffu, blk, pl);
-          if (lane < 16 && ((vm >> pl) & 1u)) {
-            unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * kBs * kTileRowBytes;
+          if (lane < 2 * kPagesPerChunk && ((vm >> pl) & 1u)) {
+            unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * BT * kTileRowBytes;
             tma_load_5d(dst, &kv_map, 0, it.g, 0, kv, pblk, &sm.kv_full[st]);
           }
         }
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         const bool zeroer = h == (it.halves == 2 ? 1 : 0);
         if (lane == 0) ok = mbar_wait_short(&sm.q_full, k & 1) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ok = mma_prepare_chunk(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
+        if (ok) ok = mma_prepare_chunk<BT>(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
         if (ok && nch > 0) {
           int good = 1;
           if (lane == 0) {
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         }
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
           if (j + 1 < it.n_chunks &&
-              !mma_prepare_chunk(sm, gc + 1, (j + 1) * kChunk, it.n_keys, zeroer,
+              !mma_prepare_chunk<BT>(sm, gc + 1, (j + 1) * kChunk, it.n_keys, zeroer,
                                  it.halves == 2 && j + 1 < it.nc0, lane)) {
             ok = 0;
             break;
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
               // the half's softmax has written P
               if (good && !mbar_wait_short(&sm.p_full[h], n_p & 1)) good = 0;
               // V rows zeroed by the other half's warp
-              if (good && !zeroer && chunk_needs_zero(sm, gc, j * kChunk, it.n_keys)) {
+              if (good && !zeroer && chunk_needs_zero<BT>(sm, gc, j * kChunk, it.n_keys)) {
                 if (!mbar_wait_short(&sm.v_zeroed[st], (vz_parity >> st) & 1u)) good = 0;
                 vz_parity ^= 1u << st;
               }
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         const int pm = sm.pmask[st];
         const int kbase = j * kChunk;
         // every key of the chunk is visible to every row of the half and was loaded
-        const bool full = pm == 0xff && kbase + kChunk - 1 <= first_pos;
+        const bool full = pm == static_cast<int>(kAllPages) && kbase + kChunk - 1 <= first_pos;
         const int lim = qpos - kbase;           // keys c <= lim are at or before the row
         uint32_t v[kChunk];
 #pragma unroll
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
 #pragma unroll
           for (int c = 0; c < kChunk; ++c)
-            if (!((c <= lim) && ((pm >> (c >> 4)) & 1))) v[c] = 0xff800000u;
+            if (!((c <= lim) && ((pm >> (c / BT)) & 1))) v[c] = 0xff800000u;
         }
         float mx8[8];
 #pragma unroll
@@ -676,16 +689,18 @@ int make_q_map(CUtensorMap *map, const void *q, int total_tokens) {
 
 using namespace pa;
 
-extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_tokens,
-                                    const int32_t *cu_tokens, const uint16_t *kv_cache,
-                                    int num_blocks, const int32_t *block_table, int n_layers,
-                                    int max_blocks_per_seq, const int32_t *context_lens,
-                                    int num_seqs, int layer, float scale, int32_t *err,
-                                    void *stream) {
+namespace {
+
+template <int BT>
+int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
+                           const int32_t *cu_tokens, const uint16_t *kv_cache, int num_blocks,
+                           const int32_t *block_table, int n_layers, int max_blocks_per_seq,
+                           const int32_t *context_lens, int num_seqs, int layer, float scale,
+                           int32_t *err, void *stream) {
   if (num_seqs < 0 || num_seqs > kMaxSeqsP || total_tokens < 0 || num_blocks <= 0 ||
       n_layers <= 0 || max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > INT_MAX) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * BT > INT_MAX) return PA_ERR_ARG;
   if (layer < 0 || layer >= n_layers) return PA_ERR_LAYER;
   if (num_seqs == 0 || total_tokens == 0) return PA_OK;
   if (!out || !q || !cu_tokens || !kv_cache || !block_table || !context_lens || !err)
@@ -699,7 +714,8 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   static bool attr_done[64] = {};
   const size_t smem = sizeof(PSmem) + 1024;
   if (!attr_done[di.device]) {
-    if (cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(prefill_attention_kernel<BT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_done[di.device] = true;
@@ -710,7 +726,7 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   static thread_local int map_blocks = 0;
   alignas(64) static thread_local CUtensorMap kv_map;
   if (map_pool != kv_cache || map_blocks != num_blocks) {
-    rc = make_kv_rows_map(&kv_map, kv_cache, num_blocks);
+    rc = make_kv_rows_map_bt(&kv_map, kv_cache, num_blocks, BT);
     if (rc != PA_OK) return rc;
     map_pool = kv_cache;
     map_blocks = num_blocks;
@@ -742,9 +758,47 @@ extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_
   prm.layer = layer;
   prm.total_tokens = total_tokens;
   prm.qscale = scale * kLog2eP;
-  if (launch_pdl(prefill_attention_kernel, dim3(static_cast<unsigned>(grid)),
+  if (launch_pdl(prefill_attention_kernel<BT>, dim3(static_cast<unsigned>(grid)),
                  dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_tokens,
+                                    const int32_t *cu_tokens, const uint16_t *kv_cache,
+                                    int num_blocks, const int32_t *block_table, int n_layers,
+                                    int max_blocks_per_seq, const int32_t *context_lens,
+                                    int num_seqs, int layer, float scale, int32_t *err,
+                                    void *stream) {
+  return prefill_attention_impl<kBs>(out, q, total_tokens, cu_tokens, kv_cache, num_blocks,
+                                     block_table, n_layers, max_blocks_per_seq, context_lens,
+                                     num_seqs, layer, scale, err, stream);
+}
+
+extern "C" int pa_prefill_attention_bt(uint16_t *out, const uint16_t *q, int total_tokens,
+                                       const int32_t *cu_tokens, const uint16_t *kv_cache,
+                                       int num_blocks, int block_tokens,
+                                       const int32_t *block_table, int n_layers,
+                                       int max_blocks_per_seq, const int32_t *context_lens,
+                                       int num_seqs, int layer, float scale, int32_t *err,
+                                       void *stream) {
+  switch (block_tokens) {
+    case 8:
+      return prefill_attention_impl<8>(out, q, total_tokens, cu_tokens, kv_cache, num_blocks,
+                                       block_table, n_layers, max_blocks_per_seq, context_lens,
+                                       num_seqs, layer, scale, err, stream);
+    case 16:
+      return prefill_attention_impl<16>(out, q, total_tokens, cu_tokens, kv_cache, num_blocks,
+                                        block_table, n_layers, max_blocks_per_seq, context_lens,
+                                        num_seqs, layer, scale, err, stream);
+    case 32:
+      return prefill_attention_impl<32>(out, q, total_tokens, cu_tokens, kv_cache, num_blocks,
+                                        block_table, n_layers, max_blocks_per_seq, context_lens,
+                                        num_seqs, layer, scale, err, stream);
+    default:
+      return PA_ERR_ARG;
+  }
 }

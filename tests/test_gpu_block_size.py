@@ -1,6 +1,7 @@
 """GPU parity of the page-size entry points (pa_kv_append_rope_bt,
-pa_decode_attention_bt, pa_free_bt with 8- and 32-token pages) against the
-oracle run with the same page size, through the C ABI.
+pa_decode_attention_bt, pa_free_bt, pa_prefill_append_rope_bt,
+pa_prefill_attention_bt with 8- and 32-token pages) against the oracle run
+with the same page size, through the C ABI.
 
 Page: "An Inference Engine in 1,500 Lines of CUDA: The Map", "What is in the
 box" (16-token pages + block_table; the page size taken as a tunable).
@@ -18,6 +19,7 @@ import pa_workloads as wl
 from helpers import (assert_attention_close, dev_bf16, dev_i32, gather_for_oracle, host_bits,
                      host_f64)
 from test_gpu_append import DevState, _compare_pools, assert_rope_close
+import test_gpu_prefill as tp
 
 pytestmark = pytest.mark.gpu
 
@@ -245,3 +247,73 @@ def test_full_size_workloads_sampled(name, page):
     del pool
     torch.cuda.empty_cache()
 
+
+
+# ---------------------------------------------------------------- prefill
+# pa_prefill_append_rope_bt / pa_prefill_attention_bt (the binding picks them
+# from the pool's page dimension) against the oracle at the same page size.
+
+
+@pytest.mark.parametrize("page", PAGES)
+@pytest.mark.parametrize("ctx,lens", [
+    ([0, 0], [17, 14]),                                # the page's two prompts
+    ([0, 7, 8, 31, 100, 5], [1, 3, 16, 33, 40, 0]),    # page starts at 8 and 32, empty chunk
+    ([2047, 0, 4000], [300, 1000, 96]),                # long prompts, chunks after long contexts
+])
+def test_prefill_append_matches_oracle(page, ctx, lens):
+    tp._run_append_case(tp._append_case(40 + page + len(ctx), ctx, lens, page=page))
+
+
+@pytest.mark.parametrize("page", PAGES)
+def test_prefill_append_underflow_refuses_the_last_pages(page):
+    c = tp._append_case(44 + page, [0, 10, 0], [40, 30, 20], spare=0, free_short=3, page=page)
+    _, ref = tp._run_append_case(c)
+    assert ref[5] & oracle.ERR_FREE_UNDERFLOW
+
+
+@pytest.mark.parametrize("page", PAGES)
+@pytest.mark.parametrize("ctx,lens,q_scale", [
+    ([0, 0], [17, 14], 1.0),
+    ([0, 3, 8, 100, 31, 7], [16, 45, 1, 64, 33, 0], 2.0),    # tile edges, ragged tails, empty chunk
+    ([250, 0, 1000], [7, 130, 48], 3.0),                      # chunks after a cached context
+])
+def test_prefill_attention_matches_oracle(page, ctx, lens, q_scale):
+    pool, bt, ctx, cu, q = tp._attention_state(60 + page + len(lens), ctx, lens, q_scale=q_scale,
+                                               page=page)
+    out, err = tp._gpu_prefill_attention(pool, bt, ctx, cu, q)
+    ref, e_ref = oracle.prefill_attention(q, cu, pool, bt, ctx, 0, tp.SCALE, block_tokens=page)
+    assert err == e_ref == 0
+    tp._close(host_f64(out), ref, f"page={page} ctx={ctx.tolist()} lens={lens}")
+
+
+@pytest.mark.parametrize("page", PAGES)
+def test_prefill_attention_bad_page_is_dropped_and_reported(page):
+    pool, bt, ctx, cu, q = tp._attention_state(70 + page, [60, 0], [10, 20], extra_blocks=2,
+                                               page=page)
+    bt[0, 0, 1] = pool.shape[0] + 7         # page 1 of sequence 0 lies outside the pool
+    out, err = tp._gpu_prefill_attention(pool, bt, ctx, cu, q)
+    ref, e_ref = oracle.prefill_attention(q, cu, pool, bt, ctx, 0, tp.SCALE, block_tokens=page)
+    assert e_ref == oracle.ERR_BAD_BLOCK and err == e_ref
+    tp._close(host_f64(out), ref, f"bad page, page={page}")
+
+
+@pytest.mark.parametrize("page", PAGES)
+def test_prefill_append_then_attention_chain(page):
+    """Append the chunks (RoPE on k and q), then causal attention over the
+    cache, on both sides, with pages of `page` tokens."""
+    import torch
+    c = tp._append_case(80 + page, [0, 37, 0, 16], [17, 40, 14, 1], n_layers=2, layer=0,
+                        page=page)
+    st = DevState(c["pool"], c["bt"], c["fl"], c["fc"])
+    qd = tp._prefill_append(st, c["k"], c["v"], c["q"], c["cu"], c["ctx"], 0)
+    out = torch.empty((qd.shape[0], N_Q, D), dtype=torch.bfloat16, device="cuda")
+    _pk().pa_prefill_attention(out, qd, dev_i32(c["cu"]), st.pool, st.bt, dev_i32(c["ctx"]), 0,
+                               tp.SCALE, st.err)
+    q_ref, p_ref, b_ref, _, _, e_ref = oracle.prefill_append_rope(
+        c["k"], c["v"], c["q"], c["cu"], c["pool"], c["bt"], c["ctx"], 0, c["fl"], c["fc"],
+        block_tokens=page)
+    ref, e2 = oracle.prefill_attention(q_ref, c["cu"], p_ref, b_ref, c["ctx"], 0, tp.SCALE,
+                                       block_tokens=page)
+    torch.cuda.synchronize()
+    assert int(st.err.item()) == e_ref == e2 == 0
+    tp._close(host_f64(out), ref, f"append -> attention, page={page}")

@@ -87,16 +87,17 @@ def test_worked_example_page_order():
     _check_append(st, qd, ref)
 
 
-def _append_case(seed, ctx, lens, n_layers=2, layer=1, spare=4, free_short=0, with_q=True):
+def _append_case(seed, ctx, lens, n_layers=2, layer=1, spare=4, free_short=0, with_q=True,
+                 page=BS):
     """Sequences with `ctx` tokens already paged in `layer`, appending chunks
     of `lens` tokens; the free list holds what they need plus `spare`, minus
     `free_short`."""
     rng = np.random.default_rng(seed)
     ctx = np.asarray(ctx, dtype=np.int32)
     lens = np.asarray(lens, dtype=np.int32)
-    old_pages = (ctx + BS - 1) // BS
-    new_pages = (ctx + lens + BS - 1) // BS - old_pages
-    mb = int(max(1, ((ctx + lens + BS - 1) // BS).max())) + 1
+    old_pages = (ctx + page - 1) // page
+    new_pages = (ctx + lens + page - 1) // page - old_pages
+    mb = int(max(1, ((ctx + lens + page - 1) // page).max())) + 1
     nb = int(old_pages.sum() + new_pages.sum()) + spare
     perm = rng.permutation(nb).astype(np.int32)
     bt = np.full((len(ctx), n_layers, mb), -1, dtype=np.int32)
@@ -108,17 +109,18 @@ def _append_case(seed, ctx, lens, n_layers=2, layer=1, spare=4, free_short=0, wi
     fc = max(len(free) - free_short, 0)
     fl = np.full(nb, -1, dtype=np.int32)
     fl[:fc] = free[:fc]
-    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    pool = wl.normal_bf16(rng, (nb, 2, page, N_KV, D))
     k, v, q = _chunk(rng, int(lens.sum()))
     return dict(pool=pool, bt=bt, fl=fl, fc=fc, ctx=ctx, cu=_cu(lens), k=k, v=v,
-                q=q if with_q else None, layer=layer)
+                q=q if with_q else None, layer=layer, page=page)
 
 
 def _run_append_case(c):
     st = DevState(c["pool"], c["bt"], c["fl"], c["fc"])
     qd = _prefill_append(st, c["k"], c["v"], c["q"], c["cu"], c["ctx"], c["layer"])
     ref = oracle.prefill_append_rope(c["k"], c["v"], c["q"], c["cu"], c["pool"], c["bt"],
-                                     c["ctx"], c["layer"], c["fl"], c["fc"])
+                                     c["ctx"], c["layer"], c["fl"], c["fc"],
+                                     block_tokens=c["page"])
     _check_append(st, qd, ref)
     return st, ref
 
@@ -153,18 +155,18 @@ def test_prefill_append_refuses_a_chunk_past_the_table():
 
 
 # ---------------------------------------------------------------- attention
-def _attention_state(seed, ctx, lens, n_layers=1, layer=0, q_scale=1.0, extra_blocks=5):
-    """Pages of ctx + len tokens per sequence scattered over a NaN-poisoned
-    pool (slots past a sequence's last token stay NaN)."""
+def _attention_state(seed, ctx, lens, n_layers=1, layer=0, q_scale=1.0, extra_blocks=5, page=BS):
+    """Pages (of `page` tokens) of ctx + len tokens per sequence scattered
+    over a NaN-poisoned pool (slots past a sequence's last token stay NaN)."""
     rng = np.random.default_rng(seed)
     ctx = np.asarray(ctx, dtype=np.int32)
     lens = np.asarray(lens, dtype=np.int32)
     total = ctx + lens
-    pages = (total + BS - 1) // BS
+    pages = (total + page - 1) // page
     mb = int(max(1, pages.max())) + 1
     nb = int(pages.sum()) + extra_blocks
     perm = rng.permutation(nb).astype(np.int32)
-    pool = np.full((nb, 2, BS, N_KV, D), wl.BF16_NAN, dtype=np.uint16)
+    pool = np.full((nb, 2, page, N_KV, D), wl.BF16_NAN, dtype=np.uint16)
     bt = np.full((len(ctx), n_layers, mb), -1, dtype=np.int32)
     used = 0
     for s in range(len(ctx)):
@@ -173,13 +175,13 @@ def _attention_state(seed, ctx, lens, n_layers=1, layer=0, q_scale=1.0, extra_bl
         bt[s, layer, :pages[s]] = ids
         t = int(total[s])
         kv = wl.normal_bf16(rng, (2, t, N_KV, D))
-        full = t // BS
+        full = t // page
         if full:
-            pool[ids[:full], 0] = kv[0, :full * BS].reshape(full, BS, N_KV, D)
-            pool[ids[:full], 1] = kv[1, :full * BS].reshape(full, BS, N_KV, D)
-        if t % BS:
-            pool[ids[full], 0, :t % BS] = kv[0, full * BS:]
-            pool[ids[full], 1, :t % BS] = kv[1, full * BS:]
+            pool[ids[:full], 0] = kv[0, :full * page].reshape(full, page, N_KV, D)
+            pool[ids[:full], 1] = kv[1, :full * page].reshape(full, page, N_KV, D)
+        if t % page:
+            pool[ids[full], 0, :t % page] = kv[0, full * page:]
+            pool[ids[full], 1, :t % page] = kv[1, full * page:]
     q = wl.normal_bf16(rng, (int(lens.sum()), N_Q, D), scale=q_scale)
     return pool, bt, ctx, _cu(lens), q
 
