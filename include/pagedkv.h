@@ -446,8 +446,10 @@ int pa_decode_set_grid_limit(int max_ctas);
  *                      Fastest when the batch's contexts are of similar
  *                      length; slow when a few contexts are much longer
  *                      than the rest (their clusters finish last).
- * The cluster kernels need 16-token pages; with other page sizes every path
- * runs the split-context kernel.  Returns PA_ERR_ARG for any other value.
+ * The per-sequence kernel needs 16-token pages, the per-head one 16- or
+ * 32-token pages (a 16-token tile is then half a page); where a path's
+ * kernel does not take the page size the call runs the split-context
+ * kernel.  Returns PA_ERR_ARG for any other value.
  */
 #define PA_DECODE_AUTO     0
 #define PA_DECODE_SPLIT    1

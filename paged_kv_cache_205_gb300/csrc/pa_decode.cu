@@ -652,6 +652,21 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_kv_tile_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const cuuint64_t row = kTokRowBytes;
+  const cuuint64_t dims[5] = {kD, kHkv, static_cast<cuuint64_t>(bt), 2,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[4] = {kHeadRowBytes, row, row * bt, row * bt * 2};
+  const cuuint32_t box[5] = {kD, 1, kBs, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int make_kv_page_map(CUtensorMap *map, const void *kv_cache, int num_blocks) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
@@ -742,8 +757,10 @@ extern "C" int pa_decode_set_grid_limit(int max_ctas) {
 
 extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
   if (num_seqs < 0 || !page_size_ok(block_tokens)) return PA_ERR_ARG;
-  if (block_tokens != kBs || g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
-  if (g_decode_path == PA_DECODE_CLUSTER || g_decode_path == PA_DECODE_SEQ) return g_decode_path;
+  // the per-sequence kernel takes 16-token pages, the per-head one 16 or 32
+  if (block_tokens == kBs / 2 || g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
+  if (g_decode_path == PA_DECODE_SEQ) return block_tokens == kBs ? PA_DECODE_SEQ : PA_DECODE_SPLIT;
+  if (g_decode_path == PA_DECODE_CLUSTER) return PA_DECODE_CLUSTER;
   DeviceInfo di;
   const int rc = current_device(&di);
   if (rc != PA_OK) return rc;
@@ -829,12 +846,29 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
     return launch_decode_seq(pmap, out, q, kv_cache, num_blocks, block_table, n_layers,
                              max_blocks_per_seq, context_lens, num_seqs, layer, scale, err, c, st);
   }
-  if (BT == kBs && g_decode_path != PA_DECODE_SPLIT) {
+  // (16-token pages; with 32-token pages a tile is half a page)
+  if ((BT == kBs && g_decode_path != PA_DECODE_SPLIT) ||
+      (BT == 2 * kBs && (g_decode_path == PA_DECODE_AUTO || g_decode_path == PA_DECODE_CLUSTER))) {
     int c = decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit);
     if (c == 0 && g_decode_path == PA_DECODE_CLUSTER) c = 1;
-    if (c > 0)
-      return launch_decode_pair(map, out, q, num_blocks, block_table, n_layers, max_blocks_per_seq,
-                                context_lens, num_seqs, layer, scale, err, c, st);
+    if (c > 0) {
+      const CUtensorMap *tmap = &map;   // 16-token pages: the split kernel's map is the tile map
+      if (BT != kBs) {
+        static thread_local const void *tmap_pool = nullptr;
+        static thread_local int tmap_blocks = 0;
+        alignas(64) static thread_local CUtensorMap tile_map;
+        if (tmap_pool != kv_cache || tmap_blocks != num_blocks) {
+          rc = make_kv_tile_map_bt(&tile_map, kv_cache, num_blocks, BT);
+          if (rc != PA_OK) return rc;
+          tmap_pool = kv_cache;
+          tmap_blocks = num_blocks;
+        }
+        tmap = &tile_map;
+      }
+      return launch_decode_pair(*tmap, out, q, num_blocks, BT, block_table, n_layers,
+                                max_blocks_per_seq, context_lens, num_seqs, layer, scale, err, c,
+                                st);
+    }
   }
 
   DecodeParams prm;

@@ -158,14 +158,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   }
 }
 
-// L2 prefetch of one tile: the box of the tensor map at (head h, page blk).
-__device__ __forceinline__ void prefetch_tile_l2(const void *tmap, int h, int blk) {
+// L2 prefetch of one tile: the box of the tensor map at (head h, first
+// token tok0 of page blk).
+__device__ __forceinline__ void prefetch_tile_l2(const void *tmap, int h, int tok0, int blk) {
   asm volatile(
       "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
           reinterpret_cast<uint64_t>(tmap)),
-      "r"(0), "r"(h), "r"(0), "r"(0), "r"(blk)
+      "r"(0), "r"(h), "r"(tok0), "r"(0), "r"(blk)
       : "memory");
 }
+
+// Pages of BT tokens hold BT / 16 tiles: tile j is tokens 16 (j mod that)
+// .. of page j / that.
+template <int BT>
+struct TileOfPage {
+  static constexpr int kTiles = BT / kBs;
+  __device__ static int page(int j) { return j / kTiles; }
+  __device__ static int tok0(int j) { return (j % kTiles) * kBs; }
+};
 
 // Tiles [t0, t1) of a head with nb tiles, for CTA `rank` of c.
 __device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int &t1) {
@@ -176,6 +186,7 @@ __device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int
 // One stage: wait until it is free, write its descriptor, issue the copies
 // of tiles j0 .. j0+n-1 (lane w < n holds the page id of tile j0 + w).
 // Returns the slots whose page id is out of range, or -1 if the wait timed out.
+template <int BT>
 __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *map, int stage,
                                              uint32_t phase, int h, int j0, int n, int blk,
                                              int last, int tail, int flags, int num_blocks,
@@ -202,12 +213,16 @@ __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *ma
     else mbar_arrive(&sm.full[stage]);
   }
   __syncwarp();
-  if (valid) tma_load_5d(sm.kv[stage] + lane * kSlotBytes, map, 0, h, 0, 0, blk, &sm.full[stage]);
+  if (valid)
+    tma_load_5d(sm.kv[stage] + lane * kSlotBytes, map, 0, h, TileOfPage<BT>::tok0(j0 + lane), 0,
+                blk, &sm.full[stage]);
   return static_cast<int>(bad);
 }
 
+template <int BT>
 __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     decode_pair_kernel(const __grid_constant__ CUtensorMap kv_map, PairParams p) {
+  using TP = TileOfPage<BT>;
   extern __shared__ unsigned char smem_raw[];
   PairSmem &sm = *reinterpret_cast<PairSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -243,9 +258,9 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     // the SM's TMA unit with the copies, so only the first 3 stages' worth)
     const int j = spec_t0 + lane;
     if (j < spec_t1) {
-      spec_blk = row[j];
+      spec_blk = row[TP::page(j)];
       if (lane < kPrefetchTiles && spec_blk >= 0 && spec_blk < p.num_blocks)
-        prefetch_tile_l2(&kv_map, h, spec_blk);
+        prefetch_tile_l2(&kv_map, h, TP::tok0(j), spec_blk);
     }
   }
   if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     // current values, read now and checked against the speculative ones
     // once the first stages are on their way
     const int ctx_raw = p.context_lens[s];
-    const int blk_now = spec_t0 + lane < spec_t1 ? row[spec_t0 + lane] : -1;
+    const int blk_now = spec_t0 + lane < spec_t1 ? row[TP::page(spec_t0 + lane)] : -1;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
@@ -269,9 +284,9 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     for (int e = 0; e < spec_stages && ok; ++e) {
       const int j0 = spec_t0 + e * kPairWarps;
       const int blk = __shfl_sync(0xffffffffu, spec_blk, (e * kPairWarps + lane) & 31);
-      const int bad = publish_stage(sm, &kv_map, stage, phase, h, j0, min(kPairWarps, spec_t1 - j0),
-                                    blk, spec_nb - 1, spec_ctx - (spec_nb - 1) * kBs, 0,
-                                    p.num_blocks, lane);
+      const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j0,
+                                        min(kPairWarps, spec_t1 - j0), blk, spec_nb - 1,
+                                        spec_ctx - (spec_nb - 1) * kBs, 0, p.num_blocks, lane);
       if (bad < 0) {
         ok = false;
         break;
@@ -299,21 +314,21 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       // consumers drop what they accumulated from the speculative stages
       tile_range(nb, rank, c, t0, t1);
       j = base = t0;
-      ids = t0 + lane < t1 ? row[t0 + lane] : -1;
+      ids = t0 + lane < t1 ? row[TP::page(t0 + lane)] : -1;
       flags = kReset;
     } else if (bad_seen && lane == 0) {
       report(p.err, PA_DEV_BAD_BLOCK);
     }
-    int ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+    int ids_next = base + kIdBatch + lane < t1 ? row[TP::page(base + kIdBatch + lane)] : -1;
     while (ok && j < t1) {
       if (j >= base + kIdBatch) {
         base += kIdBatch;
         ids = ids_next;
-        ids_next = base + kIdBatch + lane < t1 ? row[base + kIdBatch + lane] : -1;
+        ids_next = base + kIdBatch + lane < t1 ? row[TP::page(base + kIdBatch + lane)] : -1;
       }
       const int blk = __shfl_sync(0xffffffffu, ids, (j - base + lane) & 31);
-      const int bad = publish_stage(sm, &kv_map, stage, phase, h, j, min(kPairWarps, t1 - j), blk,
-                                    last, tail, flags, p.num_blocks, lane);
+      const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j, min(kPairWarps, t1 - j),
+                                        blk, last, tail, flags, p.num_blocks, lane);
       if (bad < 0) {
         ok = false;
         break;
@@ -812,20 +827,24 @@ int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas) {
 }
 
 int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
-                       int num_blocks, const int32_t *block_table, int n_layers,
+                       int num_blocks, int block_tokens, const int32_t *block_table, int n_layers,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                        int layer, float scale, int32_t *err, int cluster, cudaStream_t stream) {
   if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return PA_ERR_ARG;
+  if (block_tokens != kBs && block_tokens != 2 * kBs) return PA_ERR_ARG;
+  const int bi = block_tokens == kBs ? 0 : 1;
+  void (*kern)(const CUtensorMap, PairParams) =
+      bi == 0 ? decode_pair_kernel<kBs> : decode_pair_kernel<2 * kBs>;
   DeviceInfo di;
   int rc = current_device(&di);
   if (rc != PA_OK) return rc;
-  static bool attr_done[64] = {};
+  static bool attr_done[2][64] = {};
   const size_t smem = decode_pair_smem_bytes();
-  if (!attr_done[di.device]) {
-    if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!attr_done[bi][di.device]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_done[di.device] = true;
+    attr_done[bi][di.device] = true;
   }
   PairParams prm;
   prm.kv = nullptr;
@@ -838,7 +857,7 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
   prm.n_layers = n_layers;
   prm.max_blocks = max_blocks_per_seq;
   prm.layer = layer;
-  prm.cap_tokens = max_blocks_per_seq * kBs;
+  prm.cap_tokens = max_blocks_per_seq * block_tokens;
   prm.qscale = scale * kLog2e;
 
   cudaLaunchConfig_t cfg = {};
@@ -855,7 +874,7 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, decode_pair_kernel, map, prm) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, map, prm) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 

@@ -41,6 +41,9 @@ int make_kv_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int b
 int make_kv_rows_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 // The same for pages of bt (8, 16 or 32) tokens: box (64, 1, bt, 1, 1).
 int make_kv_rows_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt);
+// Over a pool of bt-token pages (16 or 32), box (64, 1, 16, 2, 1): one kv
+// head's K and V rows of a 16-token tile (tokens tok0 .. tok0+15 of a page).
+int make_kv_tile_map_bt(CUtensorMap *map, const void *kv_cache, int num_blocks, int bt);
 
 // Decode attention with one thread-block cluster per (sequence, kv head)
 // (pa_decode_pair.cu), for 16-token pages.  decode_pair_cluster: the cluster
@@ -60,7 +63,7 @@ int launch_decode_seq(const CUtensorMap &page_map, uint16_t *out, const uint16_t
 // [K|V][head][token][64] with each head's 16 token rows 128-byte swizzled.
 int make_kv_page_map(CUtensorMap *map, const void *kv_cache, int num_blocks);
 int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
-                       int num_blocks, const int32_t *block_table, int n_layers,
+                       int num_blocks, int block_tokens, const int32_t *block_table, int n_layers,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                        int layer, float scale, int32_t *err, int cluster, cudaStream_t stream);
 

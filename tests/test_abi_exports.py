@@ -48,9 +48,11 @@ def test_host_validation_without_a_device():
 
 
 def test_decode_path_switch_without_a_device():
-    """The kernel choice: only the three path values are accepted; pages
-    other than 16 tokens always take the split-context kernel; a forced path
-    is reported as is; a bad count or page size is refused."""
+    """The kernel choice: only the three path values are accepted; 8-token
+    pages always take the split-context kernel, the per-sequence kernel
+    16-token pages only (32 fall back to the split kernel), the per-head
+    kernel 16 or 32; a forced path is reported as is; a bad count or page
+    size is refused."""
     import paged_kv_cache_205_gb300 as pk
     lib = pk.library()
     assert lib.pa_decode_set_path(4) == -2 and lib.pa_decode_set_path(-1) == -2
@@ -58,12 +60,16 @@ def test_decode_path_switch_without_a_device():
         assert lib.pa_decode_kernel_for(-1, 16) == -2
         assert lib.pa_decode_kernel_for(4, 12) == -2
         assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
-        assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_SPLIT
         assert lib.pa_decode_set_path(pk.PA_DECODE_SPLIT) == 0
         assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_SPLIT
         assert lib.pa_decode_set_path(pk.PA_DECODE_CLUSTER) == 0
         assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_CLUSTER
+        assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_CLUSTER
         assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_set_path(pk.PA_DECODE_SEQ) == 0
+        assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_SEQ
+        assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_SPLIT
     finally:
         assert lib.pa_decode_set_path(pk.PA_DECODE_AUTO) == 0
 

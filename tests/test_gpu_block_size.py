@@ -91,6 +91,30 @@ def test_edge_contexts_and_splits(page, grid):
 
 
 @pytest.mark.parametrize("page", PAGES)
+@pytest.mark.parametrize("n", [4, 20])
+def test_per_head_cluster_kernel_forced(page, n):
+    """The per-head cluster kernel forced (clusters of 8 CTAs at 4
+    sequences, of 1 at 20): with 32-token pages it runs, a tile being half a
+    page; with 8-token pages the call falls back to the split kernel.  A page
+    id out of range in one sequence is reported and its tokens dropped."""
+    pk = _pk()
+    ctx_list = EDGE[-n:]
+    pool, table, ctx, q = _case(90 + page + n, ctx_list, page, q_scale=2.0)
+    s_bad = len(ctx) - 2                    # a sequence of 65 tokens or more
+    table[s_bad, 0, 1] = pool.shape[0] + 3
+    pk.pa_decode_set_path(pk.PA_DECODE_CLUSTER)
+    try:
+        want = pk.PA_DECODE_CLUSTER if page == 32 else pk.PA_DECODE_SPLIT
+        assert pk.pa_decode_kernel_for(n, page) == want
+        ref, e_ref = oracle.decode_attention(q, pool, table, ctx, 0, block_tokens=page)
+        out, err = _gpu_attention(pool, table, ctx, q)
+    finally:
+        pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
+    assert e_ref == oracle.ERR_BAD_BLOCK and err == e_ref
+    assert_attention_close(out, ref, f"page {page}, {n} sequences, cluster kernel forced")
+
+
+@pytest.mark.parametrize("page", PAGES)
 def test_page_size_does_not_change_attention(page):
     """The same tokens under 8-, 16- and 32-token pages give the same output
     (up to rounding order) on the GPU too."""

@@ -310,8 +310,9 @@ def test_large_batch_merge_shape(grid):
 def test_automatic_kernel_choice(decode_path):
     """Automatic choice: the per-head cluster kernel while every (sequence,
     kv head) pair gets two CTAs (two CTAs per SM in all), the split-context
-    kernel beyond; a grid limit lowers the bound; other page sizes always
-    take the split kernel; a forced path is reported as forced."""
+    kernel beyond, for 16- and 32-token pages; a grid limit lowers the
+    bound; 8-token pages always take the split kernel; a forced path is
+    reported as forced."""
     import torch
     pk = _pk()
     pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
@@ -321,6 +322,8 @@ def test_automatic_kernel_choice(decode_path):
     assert pk.pa_decode_kernel_for(fit) == pk.PA_DECODE_CLUSTER
     assert pk.pa_decode_kernel_for(fit + 1) == pk.PA_DECODE_SPLIT
     assert pk.pa_decode_kernel_for(16, 8) == pk.PA_DECODE_SPLIT
+    assert pk.pa_decode_kernel_for(fit, 32) == pk.PA_DECODE_CLUSTER
+    assert pk.pa_decode_kernel_for(fit + 1, 32) == pk.PA_DECODE_SPLIT
     pk.pa_decode_set_grid_limit(64)
     assert pk.pa_decode_kernel_for(4) == pk.PA_DECODE_CLUSTER
     assert pk.pa_decode_kernel_for(5) == pk.PA_DECODE_SPLIT
