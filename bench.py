@@ -558,17 +558,25 @@ def run_gpu(args, rank, world, dist):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("pa_decode_attention (decode_pair_kernel: one thread-block cluster per "
-                       "(sequence, kv head))" if cluster else
-                       "pa_decode_attention (decode_split_kernel + decode_merge_kernel)"),
+            "kernel": {
+                st.pk.PA_DECODE_CLUSTER: "pa_decode_attention (decode_pair_kernel: one "
+                                         "thread-block cluster per (sequence, kv head))",
+                st.pk.PA_DECODE_SEQ: "pa_decode_attention (decode_seq_kernel: one "
+                                     "thread-block cluster per sequence)",
+            }.get(kern, "pa_decode_attention (decode_split_kernel + decode_merge_kernel)"),
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": (profiled_traffic(args.workload, "decode_pair_kernel",
-                                         ("pa_decode_pair.cu", "pa_device.cuh")) if cluster
-                        else profiled_traffic(args.workload)),
+            # (the committed ncu summaries are of 16-token pages)
+            "traffic": (None if w.block_tokens != BS else
+                        profiled_traffic(args.workload, "decode_pair_kernel",
+                                         ("pa_decode_pair.cu", "pa_device.cuh"))
+                        if kern == st.pk.PA_DECODE_CLUSTER else
+                        profiled_traffic(args.workload, "decode_seq_kernel",
+                                         ("pa_decode_pair.cu", "pa_device.cuh"))
+                        if kern == st.pk.PA_DECODE_SEQ else profiled_traffic(args.workload)),
             "bytes_per_launch": attn_bytes,
             "ms_per_launch": attn_ms,
             "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "
