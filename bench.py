@@ -210,8 +210,9 @@ def oracle_unit(w: wl.Workload, s: int, layer: int, rng, max_tokens=None):
     ctx = int(w.attn_context_lens[s])
     if max_tokens is not None:
         ctx = max(1, min(ctx, int(max_tokens)))
-    nb = (ctx + BS - 1) // BS + 1
-    pool = wl.normal_bf16(rng, (nb, 2, BS, N_KV, D))
+    page = w.block_tokens
+    nb = (ctx + page - 1) // page + 1
+    pool = wl.normal_bf16(rng, (nb, 2, page, N_KV, D))
     bt = np.full((1, 1, nb), -1, dtype=np.int32)
     bt[0, 0, :] = rng.permutation(nb).astype(np.int32)
     q = wl.normal_bf16(rng, (1, N_Q, D), scale=w.q_scale)
@@ -226,16 +227,19 @@ def oracle_run_unit(u, w: wl.Workload):
     the algorithmic bytes it stands for."""
     import oracle
     ctx = u["ctx"]
+    page = w.block_tokens
     if w.append:
         pos = ctx - 1   # the unit's context includes the appended token
         bt = u["bt"].copy()
         # the new token's page exists already unless it starts one
         oracle.kv_append_rope(u["k"], u["v"], u["q"], u["pool"], bt, np.array([pos]), 0,
-                              u["fl"], 1 if pos % BS == 0 else 0)
-        oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale)
-        return attention_bytes(np.array([ctx])) + append_bytes(1)
-    oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale)
-    return attention_bytes(np.array([ctx]))
+                              u["fl"], 1 if pos % page == 0 else 0, block_tokens=page)
+        oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale,
+                                block_tokens=page)
+        return attention_bytes(np.array([ctx]), page) + append_bytes(1)
+    oracle.decode_attention(u["q"], u["pool"], u["bt"], np.array([ctx]), 0, scale=w.scale,
+                            block_tokens=page)
+    return attention_bytes(np.array([ctx]), page)
 
 
 def cpu_baseline(w: wl.Workload, budget_s: float = 12.0):
@@ -272,7 +276,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    w = wl.make_workload(args.workload)
+    w = wl.make_workload(args.workload, block_tokens=args.block_tokens)
     rng = np.random.default_rng(w.seed + 91)
     # size each step so the whole run stays within a few minutes
     per_step_budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
@@ -309,6 +313,7 @@ def run_reference(args, rank, world):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "block_tokens": w.block_tokens,
                    "sample_per_step": f"one (sequence, layer) unit, context capped at {max_tokens} tokens"},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} units, one per step, single-threaded C (fp64)",

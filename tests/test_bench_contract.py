@@ -37,3 +37,23 @@ def test_warmup_below_three_is_refused():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--warmup", "2"],
                        cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+@pytest.mark.parametrize("path", ["decode", "prefill"])
+def test_reference_arm_line_with_32_token_pages(path):
+    """--block-tokens reaches the workload on both paths: the line names the
+    page size and keeps its keys."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    wk = "llama1b" if path == "decode" else "prefill8x2k"
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--path", path,
+                        "--workload", wk, "--block-tokens", "32", "--steps", "3", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in KEYS:
+        assert k in d, k
+    assert d["value"] > 0
+    text = json.dumps(d["config"])
+    assert "32" in text and ("block_tokens" in text or "32-token" in text), d["config"]
