@@ -431,8 +431,8 @@ int pa_decode_set_grid_limit(int max_ctas);
  *   PA_DECODE_AUTO     the per-head cluster kernel when every (sequence, kv
  *                      head) pair of the call gets at least two CTAs at once
  *                      (num_seqs * 16 <= 2 CTAs per SM, within the grid
- *                      limit) and pages hold 16 tokens; the split-context
- *                      kernel otherwise.
+ *                      limit) and pages hold 16 or 32 tokens; the
+ *                      split-context kernel otherwise.
  *   PA_DECODE_SPLIT    always the split-context kernel: the batch's blocks
  *                      laid end to end and cut into chunks over all CTAs,
  *                      fp32 partials merged by a second kernel.  Balances any
