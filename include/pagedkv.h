@@ -138,18 +138,21 @@ int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cac
  * pa_decode_attention_static -- pa_decode_attention for callers that cannot
  * allocate device memory where they run the decode step.
  *
- * The pages have no counterpart: tiny-vllm allocates its buffers once in
- * main().  This entry point serves callers that may not call cudaMalloc at
- * that point -- an engine whose memory map is fixed at start-up, a serving
- * thread that must not trigger the device-wide synchronisation an allocation
- * can cause, a plugin handed only its tensors.  It computes exactly what
- * pa_decode_attention computes, with the same arguments minus the workspace:
- * the scratch is a 16 MiB array in the library's device memory, held by every
- * GPU that loads the library until the process exits.
+ * The paper has no counterpart to this entry point.  It serves callers that
+ * may not call cudaMalloc at that point -- an engine whose memory map is fixed
+ * at start-up, a serving thread that must not trigger the device-wide
+ * synchronisation an allocation can cause, a plugin handed only its tensors.
+ * It computes exactly what pa_decode_attention computes, with the same
+ * arguments minus the workspace: the split partials and the work counter live
+ * in a 16 MiB array in the library's device memory, held by every GPU that
+ * loads the library until the process exits.
  *   - num_seqs at most PA_STATIC_MAX_SEQS; more returns PA_ERR_WORKSPACE.
- *   - Allocates nothing: no cudaMalloc / cudaFree or allocating library call.
+ *   - Calls no cudaMalloc / cudaFree or allocating library routine.
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current).  Under CUDA's lazy module loading that first call
+ *     may also load the library's device code and back the 16 MiB array, which
+ *     can allocate and synchronise the device: make one warm-up call on each
+ *     device at start-up, before serving and before any stream capture.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents; each call clears its work counter on `stream` first.  Calls
  *     whose kernels could overlap on the GPU race on the array: serialise them.

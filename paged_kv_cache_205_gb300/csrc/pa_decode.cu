@@ -30,6 +30,7 @@
 #include <cstdio>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <mutex>
 
 #include "pa_decode_tile.cuh"
@@ -958,20 +959,26 @@ __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of the array on the current device, looked up once per
 // device (host code may not use the symbol itself: on the host it names a
-// stand-in, not device memory).
+// stand-in, not device memory).  Later calls read the cached address without
+// taking the lock.
 int static_scratch(int device, void **ptr) {
-  static void *addr[64] = {};
+  static std::atomic<void *> addr[64] = {};
   static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[device]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return PA_ERR_CUDA;
+  void *a = addr[device].load(std::memory_order_acquire);
+  if (!a) {
+    std::lock_guard<std::mutex> lock(mu);
+    a = addr[device].load(std::memory_order_relaxed);
+    if (!a) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return PA_ERR_CUDA;
+      }
+      addr[device].store(p, std::memory_order_release);
+      a = p;
     }
-    addr[device] = p;
   }
-  *ptr = addr[device];
+  *ptr = a;
   return PA_OK;
 }
 
