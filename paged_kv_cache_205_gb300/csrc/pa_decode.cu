@@ -476,12 +476,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 p.out + (static_cast<size_t>(d.seq) * kHq + h) * kD);
 #pragma unroll
             for (int t = 0; t < 8; ++t)
-              dst[(8 * t + c2) / 2] = float2_to_bf16x2(ts.o[t][0] * inv, ts.o[t][1] * inv);
+              dst[(8 * t + c2) / 2] = float2_to_bf16x2(ts.out(t, 0) * inv, ts.out(t, 1) * inv);
           } else {
             const size_t slot = static_cast<size_t>(d.slot);
             float2 *dst = p.acc + (slot * kHq + h) * (kD / 2);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(ts.o[t][0], ts.o[t][1]);
+            for (int t = 0; t < 8; ++t) dst[(8 * t + c2) / 2] = make_float2(ts.out(t, 0), ts.out(t, 1));
             if ((lane & 3) == 0) p.ml[slot * kHq + h] = make_float2(ts.m, lt);
           }
         }

@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     if (real_row) {
 #pragma unroll
       for (int t = 0; t < 8; ++t)
-        *reinterpret_cast<float2 *>(my_o + r * kD + 8 * t + c2) = make_float2(ts.o[t][0], ts.o[t][1]);
+        *reinterpret_cast<float2 *>(my_o + r * kD + 8 * t + c2) = make_float2(ts.out(t, 0), ts.out(t, 1));
       if ((lane & 3) == 0) my_ml[r] = make_float2(timed_out ? neg_inf() : ts.m, timed_out ? 0.f : lt);
     }
   }
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
 #pragma unroll
     for (int t = 0; t < 8; ++t)
       st_cluster_f32x2(map_to_rank(&sm.part_o[slot][8 * t + c2], owner),
-                       make_float2(ts.o[t][0], ts.o[t][1]));
+                       make_float2(ts.out(t, 0), ts.out(t, 1)));
     if ((lane & 3) == 0)
       st_cluster_f32x2(map_to_rank(&sm.part_ml[slot], owner),
                        make_float2(timed_out ? neg_inf() : ts.m, timed_out ? 0.f : lt));

@@ -6,11 +6,17 @@
 // the box": softmax(q . K^T * scale) V per query head with an online softmax,
 // GQA_Q_TO_K_RATIO = 4.
 //
-// The 4 q heads are the M rows of m16n8k16 bf16 tensor-core MMAs (rows 4..15
-// are zero): S = Q K^T (8 MMAs) and O += P V (8 MMAs) per tile, fed by
+// The 4 q heads are the M rows of m16n8k16 bf16 tensor-core MMAs: S = Q K^T
+// (8 MMAs, rows 4..15 of Q are zero) and O += P V (8 MMAs) per tile, fed by
 // ldmatrix from shared memory.  The softmax runs on the S fragments in fp32
-// in the log2 domain (2 shuffles per tile); P is rounded to bf16 for the PV
-// MMA and l sums the rounded weights, so numerator and denominator agree.
+// in the log2 domain (2 shuffles per tile).  The PV MMA takes P as two bf16
+// parts: rows 0..3 of its A operand hold bf16(P) and rows 8..11 the bf16
+// rounding of the remainder P - bf16(P), so D rows r and r + 8 accumulate
+// the two parts of the same q head's output and their sum carries P to
+// about 16 significant bits, at no extra MMA (the rows were idle).  l sums
+// the fp32 weights.  With P in bf16 alone, short contexts (a few keys,
+// outputs the size of single V entries) would add up to ~2e-3 of weight
+// rounding to the output's own bf16 rounding.
 #pragma once
 
 #include "pa_device.cuh"
@@ -44,9 +50,13 @@ __device__ __forceinline__ void load_q_fragments(const uint16_t *q_token, int g,
 }
 
 struct TileState {
-  float o[8][4];   // O fragments, 8 tiles of 8 dims (rows r and r+8; r+8 stays zero)
+  float o[8][4];   // O fragments, 8 tiles of 8 dims: row r (P's bf16 part) and
+                   // row r + 8 (the remainder's part) of q head r
   float m;         // running max (log2 domain) of row r
   float l;         // running sum of this lane's columns of row r
+
+  // Unnormalised output of q head r at dims 8t + c2 + k (k = 0, 1).
+  __device__ __forceinline__ float out(int t, int k) const { return o[t][k] + o[t][k + 2]; }
 
   __device__ __forceinline__ void reset() {
     m = neg_inf();
@@ -106,15 +116,21 @@ __device__ __forceinline__ void attend_tile(uint32_t ktile, uint32_t vtile, int 
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   const float m_new = fmaxf(st.m, mx);
   const float alpha = fast_exp2(st.m - m_new);
-  const uint32_t pa = float2_to_bf16x2(fast_exp2(x0 - m_new), fast_exp2(x1 - m_new));
-  const uint32_t pc = float2_to_bf16x2(fast_exp2(x2 - m_new), fast_exp2(x3 - m_new));
+  const float p0 = fast_exp2(x0 - m_new), p1 = fast_exp2(x1 - m_new);
+  const float p2 = fast_exp2(x2 - m_new), p3 = fast_exp2(x3 - m_new);
+  const uint32_t pa = float2_to_bf16x2(p0, p1);
+  const uint32_t pc = float2_to_bf16x2(p2, p3);
   const float2 fa = bf16x2_to_float2(pa), fc = bf16x2_to_float2(pc);
-  st.l = fmaf(st.l, alpha, (fa.x + fa.y) + (fc.x + fc.y));
+  const uint32_t pa_lo = float2_to_bf16x2(p0 - fa.x, p1 - fa.y);
+  const uint32_t pc_lo = float2_to_bf16x2(p2 - fc.x, p3 - fc.y);
+  st.l = fmaf(st.l, alpha, (p0 + p1) + (p2 + p3));
   st.m = m_new;
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
     st.o[t][0] *= alpha;
     st.o[t][1] *= alpha;
+    st.o[t][2] *= alpha;
+    st.o[t][3] *= alpha;
   }
   // ---- O += P V, dims in 4 pairs of 8-dim tiles
 #pragma unroll
@@ -123,8 +139,8 @@ __device__ __forceinline__ void attend_tile(uint32_t ktile, uint32_t vtile, int 
     const int chunk = 2 * dp + (lm_i >> 1);
     uint32_t v0, v1, v2, v3;
     ldsm_x4_trans(vtile + tok * kHeadRowBytes + ((chunk ^ lm_r) << 4), v0, v1, v2, v3);
-    mma_bf16_16816(st.o[2 * dp], pa, 0u, pc, 0u, v0, v1);
-    mma_bf16_16816(st.o[2 * dp + 1], pa, 0u, pc, 0u, v2, v3);
+    mma_bf16_16816(st.o[2 * dp], pa, pa_lo, pc, pc_lo, v0, v1);
+    mma_bf16_16816(st.o[2 * dp + 1], pa, pa_lo, pc, pc_lo, v2, v3);
   }
 }
 

@@ -10,6 +10,9 @@ import pa_workloads as wl
 # attention output tolerances against the fp64 oracle (bf16 output)
 ATOL_MAX = 1e-2
 ATOL_MEAN = 1e-3
+# arithmetic error allowed on top of the output's own bf16 rounding where
+# that rounding alone exceeds ATOL_MAX (|output| >= 4)
+ROUNDING_SLACK = 1e-3
 
 
 def dev_bf16(bits: np.ndarray):
@@ -52,16 +55,26 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 def assert_attention_close(gpu_out_f64: np.ndarray, ref: np.ndarray, what: str = "",
                            output_rounding: bool = False):
     """Max and mean absolute error of a bf16 output against the fp64 oracle.
-    With output_rounding, each element may also carry the rounding of its
-    exact value to bf16 (half an ulp at |ref|), which alone exceeds ATOL_MAX
-    once |ref| >= 4: outputs that large come from rows attending over a few
-    keys (the first tokens of a prompt)."""
+
+    Decode (default): each element within 1e-2, except where the bf16 format
+    itself cannot hold that: an output with |ref| >= 4 (a short context whose
+    output is about one V entry) lies up to half a bf16 ulp (1/64 at [4, 8))
+    from the nearest bf16 number, so there the bound is that half ulp plus
+    1e-3 of arithmetic.  Below 4 this is the plain 1e-2.
+    With output_rounding (prefill, whose P enters the tensor-core MMA as bf16),
+    each element may carry the rounding of its exact value on top of 1e-2."""
     assert gpu_out_f64.shape == ref.shape, (gpu_out_f64.shape, ref.shape)
     assert np.all(np.isfinite(gpu_out_f64)), f"{what}: non-finite output"
     d = np.abs(gpu_out_f64 - ref)
-    dm = d - bf16_half_ulp(ref) if output_rounding else d
-    assert dm.max() <= ATOL_MAX, \
-        f"{what}: max abs err {d.max():.3e} ({dm.max():.3e} beyond the output rounding)"
+    if output_rounding:
+        dm = d - bf16_half_ulp(ref)
+    else:
+        dm = d - np.maximum(0.0, bf16_half_ulp(ref) + ROUNDING_SLACK - ATOL_MAX)
+    if dm.max() > ATOL_MAX:
+        i = np.unravel_index(int(np.argmax(dm)), d.shape)
+        raise AssertionError(f"{what}: max abs err {d.max():.3e} ({dm.max():.3e} beyond the "
+                             f"bound) at {tuple(int(x) for x in i)}: got {gpu_out_f64[i]!r}, "
+                             f"oracle {ref[i]!r}")
     assert d.mean() <= ATOL_MEAN, f"{what}: mean abs err {d.mean():.3e}"
     return float(d.max()), float(d.mean())
 
@@ -72,10 +85,11 @@ def workspace_for(n, max_blocks):
     return pk.decode_workspace(n, max_blocks)
 
 
-def gather_for_oracle(pool_dev, block_table: np.ndarray, seqs, ctx, layer):
+def gather_for_oracle(pool_dev, block_table: np.ndarray, seqs, ctx, layer, return_ids=False):
     """Copy the blocks that sequences `seqs` read in `layer` from a device pool
     [num_blocks][2][page][8][64] into a compact host pool, with the table rows
-    renumbered to it."""
+    renumbered to it.  With return_ids, also the device block id of every
+    compact block."""
     import torch
     page = int(pool_dev.shape[2])
     rows = []
@@ -94,4 +108,35 @@ def gather_for_oracle(pool_dev, block_table: np.ndarray, seqs, ctx, layer):
         bt[i, 0, :len(r)] = [remap[b] for b in r.tolist()]
     if sub.shape[0] == 0:
         sub = np.zeros((1, 2, page, 8, 64), np.uint16)
+    if return_ids:
+        return sub, bt, np.asarray(uniq, dtype=np.int64)
     return sub, bt
+
+
+def oracle_attention_threads(q, pool, block_table, context_lens, layer, scale=0.125,
+                             block_tokens=16, threads=None):
+    """oracle.decode_attention over all sequences, the sequences shared out
+    over host threads (the oracle's C runs without the GIL and keeps no
+    state between calls); the result is the same as one call."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    n = int(np.asarray(context_lens).shape[0])
+    out = np.zeros((n, 32, 64), dtype=np.float64)
+    if n == 0:
+        return out, 0
+    threads = threads or max(1, min(16, os.cpu_count() or 1))
+    parts = [p for p in np.array_split(np.arange(n), min(n, 4 * threads)) if len(p)]
+
+    def run(idx):
+        o, e = oracle.decode_attention(q[idx], pool, block_table[idx], context_lens[idx], layer,
+                                       scale=scale, block_tokens=block_tokens)
+        return idx, o, e
+
+    err = 0
+    with ThreadPoolExecutor(threads) as ex:
+        for idx, o, e in ex.map(run, parts):
+            out[idx] = o
+            err |= e
+    return out, err

@@ -8,8 +8,7 @@ import pytest
 
 import oracle
 import pa_workloads as wl
-from helpers import (assert_attention_close, dev_bf16, dev_i32, gather_for_oracle,
-                     host_f64, workspace_for)
+from helpers import assert_attention_close, dev_bf16, dev_i32, host_f64, workspace_for
 
 pytestmark = pytest.mark.gpu
 
@@ -190,42 +189,6 @@ def test_host_argument_errors():
     with pytest.raises(pk.PagedKVError) as e:
         pk.pa_decode_attention(flat[1:].view(1, N_Q, D), qd, poold, btd, ctxd, 0, 0.125, ws, err)
     assert e.value.code == -5
-
-
-# ---------------------------------------------------------------------------
-# Full-size workloads, in the launch configuration the benchmark times:
-# device pools drawn by torch, oracle on a sample of sequences.
-FULL = [("llama1b", [0, 7, 15]), ("pool2g", [0, 31, 63]), ("long32k", [1]), ("ragged", None)]
-
-
-@pytest.mark.parametrize("name,sample", FULL)
-def test_full_size_workload_sampled(name, sample):
-    import torch
-    pk = _pk()
-    w = wl.make_workload(name)
-    pool = wl.make_pool_torch(w, "cuda", seed=w.seed)
-    ctx = w.attn_context_lens if name != "ragged" else w.context_lens
-    rng = np.random.default_rng(w.seed + 1000)
-    q = wl.normal_bf16(rng, (w.num_seqs, N_Q, D), scale=w.q_scale)
-    if sample is None:   # ragged: shortest, longest and a few in between
-        order = np.argsort(ctx)
-        sample = sorted({int(order[0]), int(order[-1]), *rng.choice(w.num_seqs, 4, replace=False).tolist()})
-    qd, btd, ctxd = dev_bf16(q), dev_i32(w.block_table), dev_i32(ctx)
-    out = torch.empty((w.num_seqs, N_Q, D), dtype=torch.bfloat16, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = workspace_for(w.num_seqs, w.max_blocks_per_seq)
-    for layer in (0, w.n_layers - 1):
-        pk.pa_decode_attention(out, qd, pool, btd, ctxd, layer, w.scale, ws, err)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        got = host_f64(out)
-        assert np.all(np.isfinite(got))
-        sub, bt = gather_for_oracle(pool, w.block_table, sample, ctx, layer)
-        ref, e = oracle.decode_attention(q[sample], sub, bt, ctx[sample], 0, scale=w.scale)
-        assert e == 0
-        assert_attention_close(got[sample], ref, f"{name} layer {layer}")
-    del pool
-    torch.cuda.empty_cache()
 
 
 def test_workspace_reused_across_calls_and_grids():
