@@ -173,9 +173,13 @@ __device__ __forceinline__ void rotate4(uint2 lo, uint2 hi, const float2 *cs, in
 }
 
 // (cos, sin) of the angle pos * f.  The angle is formed and reduced modulo
-// 2*pi in fp64, so that positions in the tens of thousands keep their phase;
-// the reduced angle (|r| <= pi) goes through fp32 sincosf, with a first-order
-// correction for the part of it fp32 could not hold.
+// 2*pi in fp64, so that positions in the tens of thousands keep their phase.
+// The reduction is Cody and Waite's (W. J. Cody, W. Waite, "Software Manual
+// for the Elementary Functions", 1980): 2*pi is split into a double head and
+// the double nearest to the rest, and k*2*pi is taken off in two fused
+// multiply-adds, head first.  The reduced angle (|r| <= pi) goes through
+// fp32 sincosf, with a first-order correction for the part of it fp32 could
+// not hold.
 __device__ __forceinline__ float2 rope_cos_sin(int pos, double f) {
   const double two_pi_hi = 6.283185307179586232, two_pi_lo = 2.4492935982947064e-16;
   const double a = static_cast<double>(pos) * f;
