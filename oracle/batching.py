@@ -24,10 +24,11 @@ the rest of the page supports):
     step (``free`` over their rows in ascending row order), then closes the
     gaps: the remaining rows keep their order and move down.
   * Admission is first-in first-out and stops at the first queued request
-    that does not fit: it needs a free row, ``L * ceil((P + G) / 16)`` pages
-    not promised to the requests already admitted (its whole life, so a
-    decode step never runs out of pages), and P tokens of the step's
-    prefill budget.
+    that does not fit: it needs a free row, ``L * ceil((P + G) / B)`` pages
+    of B tokens (16, the page's BLOCK_SIZE, unless chosen otherwise) not
+    promised to the requests already admitted (its whole life, so a decode
+    step never runs out of pages), and P tokens of the step's prefill
+    budget.
   * The admitted prompts are prefilled together (all layers), then every
     active row (the new ones included) takes one decode step (all layers):
     append at position ctx, attention over ctx + 1.
@@ -42,9 +43,11 @@ import numpy as np
 BLOCK = 16
 
 
-def pages_needed(prompt_len: int, decode_steps: int, n_layers: int) -> int:
-    """Pages a request holds at the end of its life: P + G tokens per layer."""
-    return n_layers * ((prompt_len + decode_steps + BLOCK - 1) // BLOCK)
+def pages_needed(prompt_len: int, decode_steps: int, n_layers: int,
+                 block_tokens: int = BLOCK) -> int:
+    """Pages a request holds at the end of its life: P + G tokens per layer,
+    in pages of block_tokens tokens."""
+    return n_layers * ((prompt_len + decode_steps + block_tokens - 1) // block_tokens)
 
 
 @dataclasses.dataclass
@@ -69,11 +72,13 @@ class StepPlan:
 class Scheduler:
     """The loop's host decisions, without numbers."""
 
-    def __init__(self, max_slots: int, n_layers: int, pages_free: int, prefill_budget: int):
+    def __init__(self, max_slots: int, n_layers: int, pages_free: int, prefill_budget: int,
+                 block_tokens: int = BLOCK):
         self.max_slots = max_slots
         self.n_layers = n_layers
         self.pages_free = pages_free
         self.prefill_budget = prefill_budget
+        self.block_tokens = block_tokens
         self.queue = collections.deque()
         self.rows: list[Row] = []
         self.promised = 0
@@ -81,7 +86,8 @@ class Scheduler:
     def submit(self, rid: int, prompt_len: int, decode_steps: int):
         if prompt_len < 1 or decode_steps < 1 or prompt_len > self.prefill_budget:
             raise ValueError("request cannot be served")
-        if pages_needed(prompt_len, decode_steps, self.n_layers) > self.pages_free:
+        if pages_needed(prompt_len, decode_steps, self.n_layers,
+                        self.block_tokens) > self.pages_free:
             raise ValueError("request needs more pages than the pool holds")
         self.queue.append((rid, prompt_len, decode_steps))
 
@@ -94,14 +100,15 @@ class Scheduler:
         retired = [self.rows[i].rid for i in retired_rows]
         for i in retired_rows:
             r = self.rows[i]
-            self.promised -= pages_needed(r.prompt_len, r.decode_steps, self.n_layers)
+            self.promised -= pages_needed(r.prompt_len, r.decode_steps, self.n_layers,
+                                          self.block_tokens)
         retired_ctx = [self.rows[i].ctx for i in retired_rows]
         self.rows = [r for r in self.rows if r.done < r.decode_steps]
         n_keep = len(self.rows)
         admitted, budget = [], self.prefill_budget
         while self.queue:
             rid, p, g = self.queue[0]
-            need = pages_needed(p, g, self.n_layers)
+            need = pages_needed(p, g, self.n_layers, self.block_tokens)
             if len(self.rows) >= self.max_slots or self.promised + need > self.pages_free \
                     or p > budget:
                 break
@@ -126,8 +133,8 @@ class Scheduler:
 
 
 class PagedState:
-    """The oracle's copy of the device state: pool, block table (one row per
-    slot), free list and count."""
+    """The oracle's copy of the device state: pool [pages][2][B][8][64], block
+    table (one row per slot), free list and count."""
 
     def __init__(self, pool, block_table, free_list, free_count):
         self.pool = np.array(pool, dtype=np.uint16, copy=True)
@@ -146,13 +153,14 @@ def run_step(sched: Scheduler, st: PagedState, plan: StepPlan, inputs, scale: fl
     The loop's last step only releases what finished in the one before."""
     import oracle
     L = sched.n_layers
+    B = sched.block_tokens
     err = 0
     # 1. release the finished requests, then close the gaps (order kept)
     if plan.retired_rows:
         ctx = np.zeros(st.bt.shape[0], dtype=np.int32)
         ctx[plan.retired_rows] = plan.retired_ctx
         st.bt, st.fl, st.fc, e = oracle.free(np.array(plan.retired_rows, np.int32), st.bt, ctx,
-                                             st.fl, st.fc, st.pool.shape[0])
+                                             st.fl, st.fc, st.pool.shape[0], block_tokens=B)
         err |= e
         n_prev = plan.n_keep + len(plan.retired_rows)
         gone = set(plan.retired_rows)
@@ -180,10 +188,11 @@ def run_step(sched: Scheduler, st: PagedState, plan: StepPlan, inputs, scale: fl
             q, k, v = np.concatenate(qs), np.concatenate(ks), np.concatenate(vs)
             sub = st.bt[k0:n]
             q2, st.pool, sub2, st.fl, st.fc, e = oracle.prefill_append_rope(
-                k, v, q, cu, st.pool, sub, zero, layer, st.fl, st.fc)
+                k, v, q, cu, st.pool, sub, zero, layer, st.fl, st.fc, block_tokens=B)
             st.bt[k0:n] = sub2
             err |= e
-            out, e = oracle.prefill_attention(q2, cu, st.pool, st.bt[k0:n], zero, layer, scale)
+            out, e = oracle.prefill_attention(q2, cu, st.pool, st.bt[k0:n], zero, layer, scale,
+                                              block_tokens=B)
             err |= e
             pre_out.append(out)
         pre_out = np.stack(pre_out)
@@ -203,10 +212,12 @@ def run_step(sched: Scheduler, st: PagedState, plan: StepPlan, inputs, scale: fl
         q, k, v = np.concatenate(qs), np.concatenate(ks), np.concatenate(vs)
         sub = st.bt[:n]
         q2, st.pool, sub2, st.fl, st.fc, e = oracle.kv_append_rope(k, v, q, st.pool, sub, ctx,
-                                                                   layer, st.fl, st.fc)
+                                                                   layer, st.fl, st.fc,
+                                                                   block_tokens=B)
         st.bt[:n] = sub2
         err |= e
-        out, e = oracle.decode_attention(q2, st.pool, st.bt[:n], ctx + 1, layer, scale)
+        out, e = oracle.decode_attention(q2, st.pool, st.bt[:n], ctx + 1, layer, scale,
+                                         block_tokens=B)
         err |= e
         dec_out.append(out)
     sched.finish_step(plan)

@@ -23,14 +23,14 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "batching_worked_exam
 
 
 def _run(w_layers, max_slots, num_blocks, mb, budget, requests, free_list=None, seed=0,
-         pool=None, record=None, scale=0.125):
-    sched = batching.Scheduler(max_slots, w_layers, num_blocks, budget)
+         pool=None, record=None, scale=0.125, block_tokens=BS):
+    sched = batching.Scheduler(max_slots, w_layers, num_blocks, budget, block_tokens)
     for rid, p, g in requests:
         sched.submit(rid, p, g)
     if free_list is None:
         free_list = np.random.default_rng(seed).permutation(num_blocks).astype(np.int32)
     if pool is None:
-        pool = np.full((num_blocks, 2, BS, 8, 64), wl.BF16_NAN, dtype=np.uint16)
+        pool = np.full((num_blocks, 2, block_tokens, 8, 64), wl.BF16_NAN, dtype=np.uint16)
     st = batching.PagedState(pool, np.full((max_slots, w_layers, mb), -1, np.int32),
                              free_list, len(free_list))
 
@@ -51,11 +51,17 @@ def _run(w_layers, max_slots, num_blocks, mb, budget, requests, free_list=None, 
     return steps, st
 
 
-def test_worked_example_schedule_and_pages():
-    g = json.load(open(GOLDEN))
+@pytest.mark.parametrize("golden", ["batching_worked_example.json",
+                                    "batching_worked_example_8.json"])
+def test_worked_example_schedule_and_pages(golden):
+    """Hand-worked schedules: 16-token pages, and 8-token pages (a request's
+    lifetime pages, the positions that open a page and the pages it returns
+    all follow the page size)."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", golden)))
     steps, st = _run(g["n_layers"], g["max_slots"], g["num_blocks"], g["max_blocks_per_seq"],
                      g["prefill_budget"], [tuple(r) for r in g["requests"]],
-                     free_list=np.array(g["free_list"], np.int32))
+                     free_list=np.array(g["free_list"], np.int32),
+                     block_tokens=g.get("block_tokens", BS))
     assert len(steps) == len(g["expect_steps"])
     for i, ((plan, _, _, bt, fc, _, _), e) in enumerate(zip(steps, g["expect_steps"])):
         assert plan.retired == e["retired"], i
@@ -175,10 +181,20 @@ def _direct_attention(seed, rid, layer, pos, scale=0.125):
     return out
 
 
-def test_loop_outputs_equal_attention_without_pages():
+def _pages_at(w, block_tokens):
+    """serve_tiny's pool in pages of block_tokens tokens (the same bytes) and
+    the table row length that holds its longest request."""
+    nb = w.num_blocks * BS // block_tokens
+    mb = max((p + g + block_tokens - 1) // block_tokens for _, p, g in w.requests) + 1
+    return nb, mb
+
+
+@pytest.mark.parametrize("block_tokens", [8, 16, 32])
+def test_loop_outputs_equal_attention_without_pages(block_tokens):
     """Every prefill row and decode row the loop produced on serve_tiny
     (pages recycled through the free list, rows moved as requests leave)
-    equals attention over the request's own tokens laid out contiguously."""
+    equals attention over the request's own tokens laid out contiguously,
+    whatever the page size."""
     w = wl.make_serve_workload("serve_tiny")
     seed = 3
     checked = 0
@@ -202,25 +218,28 @@ def test_loop_outputs_equal_attention_without_pages():
                 worst = max(worst, np.abs(dec[layer, i] - ref).max())
                 checked += 1
 
-    _run(w.n_layers, w.max_slots, w.num_blocks, w.max_blocks_per_seq, w.prefill_budget,
-         w.requests, seed=seed, record=record)
+    nb, mb = _pages_at(w, block_tokens)
+    _run(w.n_layers, w.max_slots, nb, mb, w.prefill_budget, w.requests, seed=seed, record=record,
+         block_tokens=block_tokens)
     assert checked > 100
     assert worst < 1e-9, worst
 
 
-def test_pages_conserved_and_never_shared():
+@pytest.mark.parametrize("block_tokens", [8, 16, 32])
+def test_pages_conserved_and_never_shared(block_tokens):
     w = wl.make_serve_workload("serve_tiny")
+    nb, mb = _pages_at(w, block_tokens)
 
     def record(plan, pre, dec, st, sched):
         live = st.bt[st.bt >= 0]
         assert len(live) == len(set(live.tolist())), "a page is owned twice"
-        assert len(live) + st.fc == w.num_blocks
+        assert len(live) + st.fc == nb
         for i, r in enumerate(sched.rows):
             for layer in range(w.n_layers):
-                assert (st.bt[i, layer] >= 0).sum() == (r.ctx + BS - 1) // BS
+                assert (st.bt[i, layer] >= 0).sum() == (r.ctx + block_tokens - 1) // block_tokens
         assert (st.bt[len(sched.rows):] == -1).all()
 
-    _, st = _run(w.n_layers, w.max_slots, w.num_blocks, w.max_blocks_per_seq, w.prefill_budget,
-                 w.requests, seed=4, record=record)
-    assert st.fc == w.num_blocks and (st.bt == -1).all()
-    assert sorted(st.fl.tolist()) == list(range(w.num_blocks))
+    _, st = _run(w.n_layers, w.max_slots, nb, mb, w.prefill_budget, w.requests, seed=4,
+                 record=record, block_tokens=block_tokens)
+    assert st.fc == nb and (st.bt == -1).all()
+    assert sorted(st.fl.tolist()) == list(range(nb))
