@@ -178,7 +178,11 @@ def measured_tensor_peak():
         return 1900.0, "fallback"
 
 
-def kernel_source_hash(sources=("pa_decode.cu", "pa_device.cuh")) -> str:
+SPLIT_SOURCES = ("pa_decode.cu", "pa_decode_tile.cuh", "pa_device.cuh")
+PAIR_SOURCES = ("pa_decode_pair.cu", "pa_decode_tile.cuh", "pa_device.cuh")
+
+
+def kernel_source_hash(sources=SPLIT_SOURCES) -> str:
     h = hashlib.sha256()
     for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_205_gb300", "csrc", name), "rb") as f:
@@ -187,7 +191,7 @@ def kernel_source_hash(sources=("pa_decode.cu", "pa_device.cuh")) -> str:
 
 
 def profiled_traffic(workload: str, kernel: str = "decode_split_kernel",
-                     sources=("pa_decode.cu", "pa_device.cuh")):
+                     sources=SPLIT_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, valid only while
     the kernel source hash recorded there matches the current source."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
@@ -383,20 +387,60 @@ class DeviceStep:
         return b
 
 
-def run_gpu(args, rank, world, dist):
+# the other workloads the decode path is specified on, measured in the same
+# process as the headline one and reported under "per_config"
+PER_CONFIG = ("pool2g", "long32k", "ragged")
+MIN_REPLAYS = 200   # roofline and end-to-end passes: at least this many replays
+
+
+def decode_kernel_name(pk, kern) -> str:
+    return {pk.PA_DECODE_CLUSTER: "pa_decode_attention (decode_pair_kernel: one thread-block "
+                                  "cluster per (sequence, kv head))",
+            pk.PA_DECODE_SEQ: "pa_decode_attention (decode_seq_kernel: one thread-block cluster "
+                              "per sequence)"}.get(
+        kern, "pa_decode_attention (decode_split_kernel + decode_merge_kernel)")
+
+
+def decode_traffic(pk, workload, kern, block_tokens):
+    """ncu DRAM bytes per launch of the workload's attention kernel, from the
+    committed summary of that kernel (16-token pages only), or None."""
+    if block_tokens != BS:
+        return None
+    if kern == pk.PA_DECODE_CLUSTER:
+        return profiled_traffic(workload, "decode_pair_kernel", PAIR_SOURCES)
+    if kern == pk.PA_DECODE_SEQ:
+        return profiled_traffic(workload, "decode_seq_kernel", PAIR_SOURCES)
+    return profiled_traffic(workload, "decode_split_kernel", SPLIT_SOURCES)
+
+
+def decode_workload(name: str, block_tokens: int = BS, layers: int = 0) -> wl.Workload:
+    """The named workload; with layers > 0 only its first `layers` layers, in
+    a pool just large enough for their pages (the same contexts: a small
+    device footprint for profiler captures of single launches)."""
+    w = wl.make_workload(name, block_tokens=block_tokens)
+    if layers <= 0 or layers >= w.n_layers:
+        return w
+    pages = int(((w.context_lens.astype(np.int64) + 1 + block_tokens - 1) // block_tokens).sum())
+    nb = pages * layers + 1024
+    if name == "pool2g":   # each layer draws its own subset of the pool
+        nb = max(nb, int(((w.context_lens + block_tokens - 1) // block_tokens).sum()))
+    return wl.make_workload(name, block_tokens=block_tokens, n_layers=layers, num_blocks=nb)
+
+
+def measure_decode(args, w, rank, dist, sampler, k_steps):
+    """Device step of one workload: the timed K steps (one graph of all
+    layers per step), the attention launches alone (roofline), and the
+    end-to-end step with host copies.  Returns the raw figures."""
     import torch
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    w = wl.make_workload(args.workload, block_tokens=args.block_tokens)
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
-    st.pk.pa_decode_set_grid_limit(args.grid)
-    st.pk.pa_decode_set_path({"auto": st.pk.PA_DECODE_AUTO, "split": st.pk.PA_DECODE_SPLIT,
-                              "cluster": st.pk.PA_DECODE_CLUSTER,
-                              "seq": st.pk.PA_DECODE_SEQ}[args.decode_kernel])
-    # which decode kernel the library runs for this batch: one cluster per
-    # (sequence, kv head), or split-context chunks + a merge kernel
-    kern = st.pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens)
-    cluster = kern in (st.pk.PA_DECODE_CLUSTER, st.pk.PA_DECODE_SEQ)
+    pk = st.pk
+    pk.pa_decode_set_grid_limit(args.grid)
+    pk.pa_decode_set_path({"auto": pk.PA_DECODE_AUTO, "split": pk.PA_DECODE_SPLIT,
+                           "cluster": pk.PA_DECODE_CLUSTER,
+                           "seq": pk.PA_DECODE_SEQ}[args.decode_kernel])
+    # which decode kernel the library runs for this batch
+    kern = pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens)
+    cluster = kern in (pk.PA_DECODE_CLUSTER, pk.PA_DECODE_SEQ)
     st.launches_per_step = attn_launches(cluster) * w.n_layers + (2 * w.n_layers if w.append else 0)
     L, n = w.n_layers, w.num_seqs
 
@@ -407,14 +451,14 @@ def run_gpu(args, rank, world, dist):
     def check(where):
         torch.cuda.synchronize()
         if int(st.err.item()) != 0:
-            raise RuntimeError(f"device error bits {int(st.err.item())} {where}")
+            raise RuntimeError(f"device error bits {int(st.err.item())} {where} ({w.name})")
 
     # eager warm-up (also sets the library's per-device attributes)
     for _ in range(3):
         st.step()
     check("during eager warm-up")
 
-    # one step = one CUDA graph of the 16 layers' launches
+    # one step = one CUDA graph of the layers' launches
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     g_step = torch.cuda.CUDAGraph()
@@ -427,43 +471,43 @@ def run_gpu(args, rank, world, dist):
         g_step.replay()
     check("during warm-up")
 
-    sampler = ClockSampler(local)
-    sampler.start()
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     sampler.mark(True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(k_steps):
         g_step.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark(False)
     barrier()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / k_steps
     check("in the timed region")
 
-    # dominant kernel: the 16 decode-attention launches of a step alone,
-    # back to back in one graph, CUDA events on the replay stream
+    # dominant kernel: the attention launches of a step alone, back to back
+    # in one graph, CUDA events on the replay stream
     g_attn = torch.cuda.CUDAGraph()
     with torch.cuda.stream(side):
         with torch.cuda.graph(g_attn, stream=side):
             for l in range(L):
-                st.pk.pa_decode_attention(st.out[l], st.q[l], st.pool, st.bt, st.ctx_attn, l,
-                                          w.scale, st.ws, st.err)
+                pk.pa_decode_attention(st.out[l], st.q[l], st.pool, st.bt, st.ctx_attn, l,
+                                       w.scale, st.ws, st.err)
     torch.cuda.current_stream().wait_stream(side)
-    k_roof = min(args.steps, 500)
+    k_roof = max(MIN_REPLAYS, min(k_steps, 500))
     for _ in range(3):
         g_attn.replay()
     torch.cuda.synchronize()
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
     a0.record(stream)
     for _ in range(k_roof):
         g_attn.replay()
     a1.record(stream)
     torch.cuda.synchronize()
+    sampler.mark(False)
     attn_ms = a0.elapsed_time(a1) / (k_roof * L)
     check("in the roofline pass")
 
@@ -490,10 +534,10 @@ def run_gpu(args, rank, world, dist):
             st.fc.copy_(st.fc0)
         for l in range(L):
             if w.append:
-                st.pk.pa_kv_append_rope(d_k[l], d_v[l], d_q[l], st.pool, st.bt, st.ctx, l, st.fl,
-                                        st.fc, st.err)
-            st.pk.pa_decode_attention(st.out[l], d_q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
-                                      st.ws, st.err)
+                pk.pa_kv_append_rope(d_k[l], d_v[l], d_q[l], st.pool, st.bt, st.ctx, l, st.fl,
+                                     st.fc, st.err)
+            pk.pa_decode_attention(st.out[l], d_q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
+                                   st.ws, st.err)
         h_out.copy_(st.out, non_blocking=True)
 
     g_e2e = torch.cuda.CUDAGraph()
@@ -501,106 +545,151 @@ def run_gpu(args, rank, world, dist):
         with torch.cuda.graph(g_e2e, stream=side):
             e2e_step()
     torch.cuda.current_stream().wait_stream(side)
-    k_e2e = min(args.steps, 500)
+    k_e2e = max(MIN_REPLAYS, min(k_steps, 500))
     for _ in range(3):
         g_e2e.replay()
     torch.cuda.synchronize()
     barrier()
+    sampler.mark(True)
     t0 = time.perf_counter()
     for _ in range(k_e2e):
         g_e2e.replay()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / k_e2e
+    sampler.mark(False)
     check("in the end-to-end pass")
     h2d = h_q.numel() * 2 + h_ctx.numel() * 4
     if w.append:
         h2d += h_kv[0].numel() * 2 + h_kv[1].numel() * 2 + h_kv[2].numel() * 4
     d2h = h_out.numel() * 2
+    res = dict(ms=ms, e2e_s=e2e_s, attn_ms=attn_ms, k_roof=k_roof, k_e2e=k_e2e, h2d=h2d, d2h=d2h,
+               bytes_step=st.bytes_per_step(), kern=kern, launches_per_step=st.launches_per_step)
+    del st, g_step, g_attn, g_e2e
+    pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
+    pk.pa_decode_set_grid_limit(0)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
-    bytes_step = st.bytes_per_step()
-    agg = aggregate_ranks(ms, e2e_s, bytes_step, w.num_seqs, dist)
-    ms, e2e_s, gbs = agg["ms_per_step"], agg["e2e_s"], agg["gbs"]
+
+def decode_roofline(pk, w, workload, r, peak, peak_kind):
+    attn_bytes = attention_bytes(w.attn_context_lens, w.block_tokens)
+    achieved = attn_bytes / (r["attn_ms"] / 1e3) / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": decode_kernel_name(pk, r["kern"]),
+        "achieved": achieved,
+        "peak": peak,
+        "peak_kind": f"{peak_kind} HBM copy bandwidth",
+        "unit": "GB/s",
+        "frac": achieved / peak,
+        # (the committed ncu summaries are of 16-token pages)
+        "traffic": decode_traffic(pk, workload, r["kern"], w.block_tokens),
+        "bytes_per_launch": attn_bytes,
+        "ms_per_launch": r["attn_ms"],
+        "timing": f"{r['k_roof']} replays of a graph of the {w.n_layers} attention launches, "
+                  "events on the replay stream",
+    }
+
+
+def decode_e2e(agg, r):
+    return {
+        "value": agg["e2e_gbs"],
+        "unit": "GB/s",
+        "h2d_bytes_per_step": r["h2d"],
+        "d2h_bytes_per_step": r["d2h"],
+        "ms_per_step": agg["e2e_s"] * 1e3,
+        "how": f"pinned H2D of the step inputs + the step + D2H of all outputs, one graph replay "
+               f"per step, {r['k_e2e']} steps, host wall clock",
+    }
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import paged_kv_cache_205_gb300 as pk
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = decode_workload(args.workload, args.block_tokens, args.layers)
+    sampler = ClockSampler(local)
+    sampler.start()
+    r = measure_decode(args, w, rank, dist, sampler, args.steps)
+    agg = aggregate_ranks(r["ms"], r["e2e_s"], r["bytes_step"], w.num_seqs, dist)
+    # the other specified workloads, in the same process and launch configuration
+    others = []
+    if (args.per_config and args.workload == "llama1b" and args.block_tokens == BS
+            and args.decode_kernel == "auto" and args.grid == 0 and args.layers == 0):
+        for name in PER_CONFIG:
+            wo = wl.make_workload(name)
+            ro = measure_decode(args, wo, rank, dist, sampler, args.steps)
+            others.append((name, wo, ro,
+                           aggregate_ranks(ro["ms"], ro["e2e_s"], ro["bytes_step"], wo.num_seqs,
+                                           dist)))
     sampler.stop()
     if rank != 0:
         return
 
     peak, peak_kind = measured_hbm_peak()
-    attn_bytes = attention_bytes(w.attn_context_lens, w.block_tokens)
     ctx_a = w.attn_context_lens.astype(np.int64)
     page_fill = float(ctx_a.sum() / (((ctx_a + w.block_tokens - 1) // w.block_tokens).sum()
                                      * w.block_tokens))
-    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
-    clocks = sampler.summary()
     line = {
         "metric": METRIC,
-        "value": gbs,
+        "value": agg["gbs"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms,
+        "ms_per_step": agg["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "accumulate": "fp32",
         "data": "synthetic",
-        "pct_of_peak": 100.0 * gbs / (peak * world),
+        "pct_of_peak": 100.0 * agg["gbs"] / (peak * world),
         "seq_steps_per_s": agg["seq_steps_per_s"],
         "config": {
-            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" +
+                        (f" (first {w.n_layers} layers only, {w.num_blocks}-block pool)"
+                         if args.layers else ""),
             "num_seqs": w.num_seqs,
             "n_layers": w.n_layers,
-            "algorithmic_bytes_per_step": bytes_step,
+            "algorithmic_bytes_per_step": r["bytes_step"],
             "l2": "inputs larger than L2: each step reads "
-                  f"{bytes_step / 2**20:.0f} MiB of distinct K/V (L2 129 MB)",
-            "launch": "one CUDA graph per step (the 16 layers' C-ABI launches, captured)",
+                  f"{r['bytes_step'] / 2**20:.0f} MiB of distinct K/V (L2 129 MB)",
+            "launch": "one CUDA graph per step (the layers' C-ABI launches, captured)",
             "parallelism": f"replicas x{world}",
             "decode_grid_cap": args.grid,
-            "decode_kernel": {1: "split", 2: "cluster", 3: "seq"}.get(kern, str(kern)),
+            "decode_kernel": {1: "split", 2: "cluster", 3: "seq"}.get(r["kern"], str(r["kern"])),
             "block_tokens": w.block_tokens,
             "page_fill": page_fill,
         },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": {
-                st.pk.PA_DECODE_CLUSTER: "pa_decode_attention (decode_pair_kernel: one "
-                                         "thread-block cluster per (sequence, kv head))",
-                st.pk.PA_DECODE_SEQ: "pa_decode_attention (decode_seq_kernel: one "
-                                     "thread-block cluster per sequence)",
-            }.get(kern, "pa_decode_attention (decode_split_kernel + decode_merge_kernel)"),
-            "achieved": achieved,
-            "peak": peak,
-            "peak_kind": f"{peak_kind} HBM copy bandwidth",
-            "unit": "GB/s",
-            "frac": achieved / peak,
-            # (the committed ncu summaries are of 16-token pages)
-            "traffic": (None if w.block_tokens != BS else
-                        profiled_traffic(args.workload, "decode_pair_kernel",
-                                         ("pa_decode_pair.cu", "pa_device.cuh"))
-                        if kern == st.pk.PA_DECODE_CLUSTER else
-                        profiled_traffic(args.workload, "decode_seq_kernel",
-                                         ("pa_decode_pair.cu", "pa_device.cuh"))
-                        if kern == st.pk.PA_DECODE_SEQ else profiled_traffic(args.workload)),
-            "bytes_per_launch": attn_bytes,
-            "ms_per_launch": attn_ms,
-            "timing": f"{k_roof} replays of a graph of the {L} attention launches, events on the "
-                      "replay stream",
-        },
-        "e2e": {
-            "value": agg["e2e_gbs"],
-            "unit": "GB/s",
-            "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "ms_per_step": e2e_s * 1e3,
-            "how": "pinned H2D of the step inputs + the step + D2H of all outputs, one graph "
-                   "replay per step, host wall clock",
-        },
-        "gpu_launches": st.launches_per_step * args.steps,
-        "clocks": clocks,
+        "roofline": decode_roofline(pk, w, args.workload, r, peak, peak_kind),
+        "e2e": decode_e2e(agg, r),
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": sampler.summary(),
     }
+    if others:
+        line["per_config"] = {}
+        for name, wo, ro, ao in others:
+            entry = {
+                "workload": f"{name}: {DESCRIPTIONS[name]}",
+                "value": ao["gbs"],
+                "unit": "GB/s",
+                "pct_of_peak": 100.0 * ao["gbs"] / (peak * world),
+                "seq_steps_per_s": ao["seq_steps_per_s"],
+                "ms_per_step": ao["ms_per_step"],
+                "steps": args.steps,
+                "decode_kernel": {1: "split", 2: "cluster", 3: "seq"}.get(ro["kern"],
+                                                                         str(ro["kern"])),
+                "roofline": decode_roofline(pk, wo, name, ro, peak, peak_kind),
+                "e2e": decode_e2e(ao, ro),
+            }
+            if world == 1 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline(wo, budget_s=args.cpu_budget / 2)
+            line["per_config"][name] = entry
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     print(json.dumps(line))
 
 
@@ -829,17 +918,19 @@ def run_prefill_gpu(args, rank, world, dist):
             for l in range(L):
                 pk.pa_prefill_attention(out[l], q[l], cu, pool, bt, ctx, l, w.scale, err)
     torch.cuda.current_stream().wait_stream(side)
-    k_roof = max(3, min(args.steps, 50))
+    k_roof = max(MIN_REPLAYS, min(args.steps, 500))
     for _ in range(3):
         g_attn.replay()
     torch.cuda.synchronize()
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark(True)
     a0.record(stream)
     for _ in range(k_roof):
         g_attn.replay()
     a1.record(stream)
     torch.cuda.synchronize()
+    sampler.mark(False)
     attn_ms = a0.elapsed_time(a1) / (k_roof * L)
     check("in the roofline pass")
 
@@ -861,16 +952,18 @@ def run_prefill_gpu(args, rank, world, dist):
         with torch.cuda.graph(g_e2e, stream=side):
             e2e_step()
     torch.cuda.current_stream().wait_stream(side)
-    k_e2e = max(3, min(args.steps, 20))
+    k_e2e = max(MIN_REPLAYS, min(args.steps, 500))
     for _ in range(2):
         g_e2e.replay()
     torch.cuda.synchronize()
     barrier()
+    sampler.mark(True)
     t0 = time.perf_counter()
     for _ in range(k_e2e):
         g_e2e.replay()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / k_e2e
+    sampler.mark(False)
     check("in the end-to-end pass")
     h2d = (h_q.numel() + h_k.numel() + h_v.numel()) * 2
     d2h = h_out.numel() * 2
@@ -976,7 +1069,7 @@ class ServeLoop:
         S, L, mb, B = w.max_slots, w.n_layers, w.max_blocks_per_seq, w.prefill_budget
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
-        self.pool = torch.randn((w.num_blocks, 2, BS, N_KV, D), generator=g,
+        self.pool = torch.randn((w.num_blocks, 2, w.block_tokens, N_KV, D), generator=g,
                                 device=dev).to(torch.bfloat16)
         self.fl0 = torch.from_numpy(
             np.random.default_rng(seed).permutation(w.num_blocks).astype(np.int32)).to(dev)
@@ -986,7 +1079,7 @@ class ServeLoop:
         self.fl = self.fl0.clone()
         self.fc = torch.tensor([w.num_blocks], dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = pk.decode_workspace(S, mb)
+        self.ws = pk.decode_workspace(S, mb, block_tokens=w.block_tokens)
         bf = torch.bfloat16
 
         def rnd(shape):
@@ -1010,7 +1103,7 @@ class ServeLoop:
         each pa_batcher_run."""
         w = self.w
         b = self.pk.Batcher(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
-                            w.prefill_budget)
+                            w.prefill_budget, block_tokens=w.block_tokens)
         for r in w.requests:
             b.submit(*r)
         steps = launches = 0
@@ -1074,7 +1167,7 @@ def serve_cpu_baseline(w, budget_s: float = 12.0):
 def run_serve_reference(args, rank, world):
     if rank != 0:
         return
-    w = wl.make_serve_workload(args.workload)
+    w = wl.make_serve_workload(args.workload, block_tokens=args.block_tokens)
     base = serve_cpu_baseline(w, budget_s=min(20.0, 2.0 + 0.5 * args.steps))
     out_tokens = serve_totals(w)[0]
     line = {
@@ -1092,6 +1185,7 @@ def run_serve_reference(args, rank, world):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: {SERVE_DESCRIPTIONS[args.workload]}",
+                   "block_tokens": w.block_tokens,
                    "sample_per_step": base["sample"]},
         "cpu_baseline": base,
         "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -1104,7 +1198,7 @@ def run_serve_gpu(args, rank, world, dist):
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    w = wl.make_serve_workload(args.workload)
+    w = wl.make_serve_workload(args.workload, block_tokens=args.block_tokens)
     loop = ServeLoop(w, seed=w.seed + 1000 * rank)
     stream = torch.cuda.current_stream()
 
@@ -1167,7 +1261,7 @@ def run_serve_gpu(args, rank, world, dist):
     # book-keeping (the oracle-free count: every row advances one token)
     dec_ms, dec_bytes = 0.0, 0
     sim = loop.pk.Batcher(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
-                          w.prefill_budget)
+                          w.prefill_budget, block_tokens=w.block_tokens)
     for r in w.requests:
         sim.submit(*r)
     i = 0
@@ -1244,6 +1338,7 @@ def run_serve_gpu(args, rank, world, dist):
         "prompt_tokens_per_s": world * prompt_tokens / (ms / 1e3),
         "config": {
             "workload": f"{args.workload}: {SERVE_DESCRIPTIONS[args.workload]}",
+            "block_tokens": w.block_tokens,
             "step": "one complete serving run of the workload (every request admitted, "
                     "prefilled, decoded and released)",
             "loop_steps_per_run": steps_per_run,
@@ -1299,11 +1394,19 @@ def main():
                          " (default prefill8x2k); serve: " +
                          ", ".join(sorted(SERVE_DESCRIPTIONS)) + " (default serve256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for each CPU baseline")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="decode path: measure the headline workload only (by default the "
+                         "llama1b line also carries pool2g, long32k and ragged)")
     ap.add_argument("--block-tokens", type=int, default=BS, choices=[8, 16, 32],
                     help="decode path: tokens per page (the page size as a tunable)")
     ap.add_argument("--decode-kernel", default="auto", choices=["auto", "split", "cluster", "seq"],
                     help="decode-attention kernel (pa_decode_set_path): automatic choice, the "
                          "split-context kernel, or one cluster per (sequence, kv head)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="decode path: only the first N layers, in a pool sized for them "
+                         "(profiler captures of one launch on a small footprint; not a bench line)")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")
     args = ap.parse_args()

@@ -382,11 +382,18 @@ size_t pa_batcher_ctl_bytes(int max_slots);
  * tokens prefilled per step at most.  PA_ERR_ARG on bad sizes. */
 int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per_seq, int pages_free,
                       int prefill_budget, pa_batcher **out);
+/* The same with pages of block_tokens = 8, 16 or 32 tokens ("The path of one
+ * inference" marks BLOCK_SIZE as a tunable): lifetime pages are counted in
+ * such pages, and every step runs the page-size (_bt) entry points over a
+ * kv_cache of [num_blocks][2][block_tokens][8][64].  PA_ERR_ARG for another
+ * size. */
+int pa_batcher_create_bt(int max_slots, int n_layers, int max_blocks_per_seq, int pages_free,
+                         int prefill_budget, int block_tokens, pa_batcher **out);
 int pa_batcher_destroy(pa_batcher *b);
 
 /* Queue a request.  PA_ERR_ARG when it could never run: P < 1, G < 1,
- * P > prefill_budget, P + G beyond max_blocks_per_seq * 16, or more pages
- * than pages_free. */
+ * P > prefill_budget, P + G beyond max_blocks_per_seq * block_tokens, or
+ * more pages than pages_free. */
 int pa_batcher_submit(pa_batcher *b, int64_t request_id, int prompt_len, int decode_steps);
 
 /* Decide the next step.  PA_ERR_STATE if the previous plan was not run. */
@@ -449,10 +456,12 @@ int pa_decode_set_grid_limit(int max_ctas);
  *                      Fastest when the batch's contexts are of similar
  *                      length; slow when a few contexts are much longer
  *                      than the rest (their clusters finish last).
- * The per-sequence kernel needs 16-token pages, the per-head one 16- or
- * 32-token pages (a 16-token tile is then half a page); where a path's
- * kernel does not take the page size the call runs the split-context
- * kernel.  Returns PA_ERR_ARG for any other value.
+ * The per-sequence kernel needs 16-token pages; the per-head one takes 8-,
+ * 16- or 32-token pages (a 16-token tile is two pages or half a page), 8
+ * only when forced (its four 1 KiB copies per tile make it slower than the
+ * split kernel there); where a path's kernel does not take the page size
+ * the call runs the split-context kernel.  Returns PA_ERR_ARG for any other
+ * value.
  */
 #define PA_DECODE_AUTO     0
 #define PA_DECODE_SPLIT    1
@@ -466,6 +475,19 @@ int pa_decode_set_path(int path);
  * PA_ERR_ARG for a bad count or page size, PA_ERR_CUDA / PA_ERR_DEVICE when
  * no sm_103 device answers. */
 int pa_decode_kernel_for(int num_seqs, int block_tokens);
+
+/*
+ * Test hook for the bounded waits (no counterpart in the paper; the pages
+ * build no failure detection).  With stage >= 0 the split-context kernel's
+ * CTA 0 publishes its stage-th shared-memory stage without issuing the copies
+ * for it, so the barrier the consumers wait on never completes; every wait of
+ * the split kernel then gives up after wait_limit_ns (1 us .. 1 s), sets
+ * PA_DEV_TIMEOUT in *err and returns, and the outputs of that call are
+ * undefined.  No other kernel is affected.  stage = -1 restores normal
+ * operation (waits of 1 s, no copy left out).  Process-wide; for tests only.
+ * Returns PA_ERR_ARG for a bad stage or limit.
+ */
+int pa_decode_set_test_fault(int stage, long long wait_limit_ns);
 
 /* Human-readable name of a PA_ERR_* code. */
 const char *pa_error_string(int code);

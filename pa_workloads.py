@@ -383,6 +383,7 @@ class ServeWorkload:
     requests: list                    # [(rid, prompt_len, decode_steps)]
     scale: float = 0.125
     seed: int = 0
+    block_tokens: int = BLOCK         # tokens per page
 
 
 SERVE_WORKLOADS = {
@@ -393,13 +394,14 @@ SERVE_WORKLOADS = {
 }
 
 
-def make_serve_workload(name: str) -> ServeWorkload:
+def make_serve_workload(name: str, block_tokens: int = BLOCK) -> ServeWorkload:
     """serve_tiny: 7 requests through 3 slots of a 2-layer model with a
     12-page pool and 32 prompt tokens per step, so admissions wait for
     slots, for pages and for the prefill budget.  serve256: 256
     requests through 64 slots of the 16-layer model, prompts and decode
     lengths log-uniform in [16, 2048] and [16, 512], a 65,536-block pool and
-    8192 prompt tokens per step."""
+    8192 prompt tokens per step.  With block_tokens other than 16 the pool
+    keeps its bytes (16 / page times the pages)."""
     sd, L, slots, nb, budget, n_req, (p0, p1), (g0, g1) = SERVE_WORKLOADS[name]
     rng = np.random.default_rng(sd)
     p = np.floor(np.exp(rng.uniform(np.log(p0), np.log(p1 + 1), size=n_req))).astype(int)
@@ -407,8 +409,12 @@ def make_serve_workload(name: str) -> ServeWorkload:
     p = np.clip(p, p0, p1)
     g = np.clip(g, g0, g1)
     reqs = [(i, int(p[i]), int(g[i])) for i in range(n_req)]
-    mb = int(max((a + b + BLOCK - 1) // BLOCK for _, a, b in reqs)) + 1
-    return ServeWorkload(name, L, slots, nb, mb, budget, reqs, seed=sd)
+    if block_tokens not in (8, 16, 32):
+        raise ValueError("pages of 8, 16 or 32 tokens")
+    # the pool keeps its bytes: 16 / page times the pages
+    nb = nb * BLOCK // block_tokens
+    mb = int(max((a + b + block_tokens - 1) // block_tokens for _, a, b in reqs)) + 1
+    return ServeWorkload(name, L, slots, nb, mb, budget, reqs, seed=sd, block_tokens=block_tokens)
 
 
 def request_token_inputs(seed: int, rid: int, layer: int, positions):

@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     pa_decode_attention,
     pa_decode_set_grid_limit,
     pa_decode_set_path,
+    pa_decode_set_test_fault,
     pa_decode_kernel_for,
     PA_DECODE_AUTO,
     PA_DECODE_SPLIT,

@@ -41,6 +41,7 @@ _EXPORTS = (
     "pa_error_string",
     "pa_batcher_ctl_bytes",
     "pa_batcher_create",
+    "pa_batcher_create_bt",
     "pa_batcher_destroy",
     "pa_batcher_submit",
     "pa_batcher_plan",
@@ -129,6 +130,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_set_grid_limit.restype = I
         lib.pa_decode_set_path.argtypes = [I]
         lib.pa_decode_set_path.restype = I
+        lib.pa_decode_set_test_fault.argtypes = [I, ctypes.c_longlong]
+        lib.pa_decode_set_test_fault.restype = I
         lib.pa_decode_kernel_for.argtypes = [I, I]
         lib.pa_decode_kernel_for.restype = I
         lib.pa_error_string.argtypes = [I]
@@ -138,6 +141,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_batcher_ctl_bytes.restype = Z
         lib.pa_batcher_create.argtypes = [I, I, I, I, I, PP]
         lib.pa_batcher_create.restype = I
+        lib.pa_batcher_create_bt.argtypes = [I, I, I, I, I, I, PP]
+        lib.pa_batcher_create_bt.restype = I
         lib.pa_batcher_destroy.argtypes = [P]
         lib.pa_batcher_destroy.restype = I
         lib.pa_batcher_submit.argtypes = [P, ctypes.c_int64, I, I]
@@ -353,6 +358,14 @@ def pa_decode_kernel_for(num_seqs: int, block_tokens: int = PA_BLOCK_TOKENS) -> 
     return int(r)
 
 
+def pa_decode_set_test_fault(stage: int, wait_limit_ns: int = 0) -> None:
+    """Test hook of the bounded waits (see include/pagedkv.h): stage >= 0
+    leaves that stage of the split kernel's CTA 0 without its copies and
+    shortens every wait of the split kernel to wait_limit_ns; -1 restores."""
+    _check("pa_decode_set_test_fault",
+           library().pa_decode_set_test_fault(int(stage), int(wait_limit_ns)))
+
+
 def pa_decode_set_path(path: int) -> None:
     """Selects the decode-attention kernel: PA_DECODE_AUTO (default),
     PA_DECODE_SPLIT or PA_DECODE_CLUSTER (process-wide)."""
@@ -368,12 +381,14 @@ class Batcher:
     """The library's continuous-batching loop (pa_batcher_*): a queue of
     requests, block-table rows as slots, one planned step at a time."""
 
-    def __init__(self, max_slots, n_layers, max_blocks_per_seq, pages_free, prefill_budget):
+    def __init__(self, max_slots, n_layers, max_blocks_per_seq, pages_free, prefill_budget,
+                 block_tokens=PA_BLOCK_TOKENS):
         h = ctypes.c_void_p()
-        _check("pa_batcher_create", library().pa_batcher_create(
+        _check("pa_batcher_create_bt", library().pa_batcher_create_bt(
             int(max_slots), int(n_layers), int(max_blocks_per_seq), int(pages_free),
-            int(prefill_budget), ctypes.byref(h)))
+            int(prefill_budget), int(block_tokens), ctypes.byref(h)))
         self._h = h
+        self.block_tokens = int(block_tokens)
         self.max_slots = int(max_slots)
         self.n_layers = int(n_layers)
         self.max_blocks_per_seq = int(max_blocks_per_seq)

@@ -16,7 +16,8 @@
 //     releases the requests that finished in the step before (pa_free over
 //     their rows, ascending), then closes the gaps keeping the order.
 //   * Admission is first-in first-out and stops at the first request that
-//     lacks a free row, L * ceil((P + G) / 16) pages not yet promised to the
+//     lacks a free row, L * ceil((P + G) / B) pages (B tokens per page, 16
+//     unless the batcher was created with another size) not yet promised to the
 //     admitted requests (so a decode step never runs out of pages), or P
 //     tokens of the step's prefill budget.
 //   * The admitted prompts are prefilled together (all layers:
@@ -123,6 +124,7 @@ struct DecodeGraph {
 
 struct pa_batcher {
   int max_slots, n_layers, max_blocks, pages_free, prefill_budget;
+  int block_tokens = kBs;   // tokens per page
   std::deque<Request> queue;
   std::vector<Row> rows;
   long long promised = 0;
@@ -146,7 +148,8 @@ struct pa_batcher {
 namespace {
 
 long long pages_needed(const pa_batcher *b, int prompt_len, int decode_steps) {
-  return static_cast<long long>(b->n_layers) * ((prompt_len + decode_steps + kBs - 1) / kBs);
+  const int B = b->block_tokens;
+  return static_cast<long long>(b->n_layers) * ((prompt_len + decode_steps + B - 1) / B);
 }
 
 }  // namespace
@@ -156,16 +159,19 @@ extern "C" size_t pa_batcher_ctl_bytes(int max_slots) {
   return CtlLayout{max_slots}.bytes();
 }
 
-extern "C" int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per_seq,
-                                 int pages_free, int prefill_budget, pa_batcher **out) {
+extern "C" int pa_batcher_create_bt(int max_slots, int n_layers, int max_blocks_per_seq,
+                                    int pages_free, int prefill_budget, int block_tokens,
+                                    pa_batcher **out) {
   if (!out) return PA_ERR_NULL;
   *out = nullptr;
   if (max_slots <= 0 || max_slots > 2048 || n_layers <= 0 || max_blocks_per_seq <= 0 ||
       pages_free < 0 || prefill_budget <= 0)
     return PA_ERR_ARG;
-  if (static_cast<long long>(max_blocks_per_seq) * kBs > (1LL << 30)) return PA_ERR_ARG;
+  if (block_tokens != 8 && block_tokens != 16 && block_tokens != 32) return PA_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * block_tokens > (1LL << 30)) return PA_ERR_ARG;
   pa_batcher *b = new (std::nothrow) pa_batcher;
   if (!b) return PA_ERR_ARG;
+  b->block_tokens = block_tokens;
   b->max_slots = max_slots;
   b->n_layers = n_layers;
   b->max_blocks = max_blocks_per_seq;
@@ -174,6 +180,12 @@ extern "C" int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per
   b->ctl.assign(CtlLayout{max_slots}.words(), 0);
   *out = b;
   return PA_OK;
+}
+
+extern "C" int pa_batcher_create(int max_slots, int n_layers, int max_blocks_per_seq,
+                                 int pages_free, int prefill_budget, pa_batcher **out) {
+  return pa_batcher_create_bt(max_slots, n_layers, max_blocks_per_seq, pages_free,
+                              prefill_budget, kBs, out);
 }
 
 extern "C" int pa_batcher_destroy(pa_batcher *b) {
@@ -205,7 +217,7 @@ extern "C" int pa_batcher_submit(pa_batcher *b, int64_t request_id, int prompt_l
   if (!b) return PA_ERR_NULL;
   if (prompt_len < 1 || decode_steps < 1 || prompt_len > b->prefill_budget) return PA_ERR_ARG;
   if (static_cast<long long>(prompt_len) + decode_steps >
-      static_cast<long long>(b->max_blocks) * kBs)
+      static_cast<long long>(b->max_blocks) * b->block_tokens)
     return PA_ERR_ARG;
   if (pages_needed(b, prompt_len, decode_steps) > b->pages_free) return PA_ERR_ARG;
   b->queue.push_back(Request{request_id, prompt_len, decode_steps});
@@ -336,15 +348,15 @@ int enqueue_decode(pa_batcher *b, const pa_batch_buffers *buf, int32_t *ctl, int
   const size_t dq = static_cast<size_t>(b->max_slots) * kHq * kD;
   const size_t dk = static_cast<size_t>(b->max_slots) * kHkv * kD;
   for (int l = 0; l < Lyr && n_rows > 0; ++l) {
-    int rc = pa_kv_append_rope(buf->decode_k + l * dk, buf->decode_v + l * dk,
-                               buf->decode_q + l * dq, buf->kv_cache, buf->num_blocks,
-                               buf->block_table, Lyr, mb, ctl + L.pos(), n_rows, l,
-                               buf->free_list, buf->free_count, buf->err, stream);
+    int rc = pa_kv_append_rope_bt(buf->decode_k + l * dk, buf->decode_v + l * dk,
+                                  buf->decode_q + l * dq, buf->kv_cache, buf->num_blocks,
+                                  b->block_tokens, buf->block_table, Lyr, mb, ctl + L.pos(),
+                                  n_rows, l, buf->free_list, buf->free_count, buf->err, stream);
     if (rc != PA_OK) return rc;
-    rc = pa_decode_attention(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
-                             buf->num_blocks, buf->block_table, Lyr, mb, ctl + L.attn(),
-                             n_rows, l, buf->scale, buf->decode_workspace,
-                             buf->decode_workspace_bytes, buf->err, stream);
+    rc = pa_decode_attention_bt(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
+                                buf->num_blocks, b->block_tokens, buf->block_table, Lyr, mb,
+                                ctl + L.attn(), n_rows, l, buf->scale, buf->decode_workspace,
+                                buf->decode_workspace_bytes, buf->err, stream);
     if (rc != PA_OK) return rc;
   }
   return PA_OK;
@@ -463,8 +475,9 @@ extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *
   int rc;
   // 1. release, then close the gaps
   if (p.n_retired > 0) {
-    rc = pa_free(ctl + L.retired(), p.n_retired, buf->block_table, Lyr, mb, ctl + L.free_ctx(),
-                 buf->free_list, buf->free_count, buf->num_blocks, buf->err, stream);
+    rc = pa_free_bt(ctl + L.retired(), p.n_retired, b->block_tokens, buf->block_table, Lyr, mb,
+                    ctl + L.free_ctx(), buf->free_list, buf->free_count, buf->num_blocks,
+                    buf->err, stream);
     if (rc != PA_OK) return rc;
     const int first = b->first_moved;
     if (first < b->n_prev) {
@@ -484,16 +497,16 @@ extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *
   const size_t tk = static_cast<size_t>(b->prefill_budget) * kHkv * kD;
   int32_t *table_new = buf->block_table + static_cast<size_t>(p.n_keep) * row_words;
   for (int l = 0; l < Lyr && p.n_admitted > 0; ++l) {
-    rc = pa_prefill_append_rope(buf->prefill_k + l * tk, buf->prefill_v + l * tk,
-                                buf->prefill_q + l * tq, p.prefill_tokens, ctl + L.cu(),
-                                buf->kv_cache, buf->num_blocks, table_new, Lyr, mb,
-                                ctl + L.zero(), p.n_admitted, l, buf->free_list, buf->free_count,
-                                buf->err, stream);
+    rc = pa_prefill_append_rope_bt(buf->prefill_k + l * tk, buf->prefill_v + l * tk,
+                                   buf->prefill_q + l * tq, p.prefill_tokens, ctl + L.cu(),
+                                   buf->kv_cache, buf->num_blocks, b->block_tokens, table_new,
+                                   Lyr, mb, ctl + L.zero(), p.n_admitted, l, buf->free_list,
+                                   buf->free_count, buf->err, stream);
     if (rc != PA_OK) return rc;
-    rc = pa_prefill_attention(buf->prefill_out + l * tq, buf->prefill_q + l * tq,
-                              p.prefill_tokens, ctl + L.cu(), buf->kv_cache, buf->num_blocks,
-                              table_new, Lyr, mb, ctl + L.zero(), p.n_admitted, l, buf->scale,
-                              buf->err, stream);
+    rc = pa_prefill_attention_bt(buf->prefill_out + l * tq, buf->prefill_q + l * tq,
+                                 p.prefill_tokens, ctl + L.cu(), buf->kv_cache, buf->num_blocks,
+                                 b->block_tokens, table_new, Lyr, mb, ctl + L.zero(),
+                                 p.n_admitted, l, buf->scale, buf->err, stream);
     if (rc != PA_OK) return rc;
   }
   // 3. one decode step for every active row

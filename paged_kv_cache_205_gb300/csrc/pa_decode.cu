@@ -100,6 +100,11 @@ struct DecodeParams {
   int layer;
   int cap_tokens;      // max_blocks * tokens per page: the largest context
   float qscale;        // scale * log2(e), applied to the fp32 scores
+  long long n_slots;   // partial slots the workspace holds
+  // test hook (pa_decode_set_test_fault): the stage of CTA 0 whose copies are
+  // left out (-1: none), and the limit of every wait of the split kernel
+  int fault_stage;
+  unsigned long long wait_ns;
 };
 
 __device__ __forceinline__ int clamped_ctx(const DecodeParams &p, int s) {
@@ -289,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t phase = 0;
     bool ok = true;
     uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
+    int published = 0;                        // stages published so far
     int k = blockIdx.x;
     while (k < n_chunks && ok) {
       // the next chunk's index is asked for once the chunk's first copy is in
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                              : __shfl_sync(0xffffffffu, my_blk2, e);
             }
             int good = 1;
-            if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
+            if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1, p.wait_ns) ? 1 : 0;
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) {
               ok = false;
@@ -376,7 +382,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
             __syncwarp();
-            if (BT == 16) {
+            // test hook: this stage's copies are left out, so its barrier
+            // never completes and every wait on it runs out
+            const bool fault = p.fault_stage == published && blockIdx.x == 0;
+            ++published;
+            if (fault) {
+              // (no copy)
+            } else if (BT == 16) {
               if (valid && lane < kHkv)   // one 4 KiB tile per kv head, 8 lanes in parallel
                 tma_load_5d(sm.kv[stage] + lane * kHeadTileBytes, &kv_map, 0, lane, 0, 0, blk,
                             &sm.full[stage]);
@@ -414,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (k < G) k = n_chunks;   // a counter that was never zeroed
     }
     if (lane == 0) {
-      if (ok && mbar_wait(&sm.empty[stage], phase ^ 1)) {
+      if (ok && mbar_wait(&sm.empty[stage], phase ^ 1, p.wait_ns)) {
         sm.desc[stage].flags = kEndOfWork;
         mbar_arrive(&sm.full[stage]);
         // this arrive is now the stage's last phase; the copy before it on
@@ -427,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // no copy may still be landing in shared memory when the CTA exits
       for (int st = 0; st < kStages; ++st)
         if ((issued >> st) & 1u)
-          if (!mbar_wait(&sm.full[st], (issued_parity >> st) & 1u)) report(p.err, PA_DEV_TIMEOUT);
+          if (!mbar_wait(&sm.full[st], (issued_parity >> st) & 1u, p.wait_ns))
+            report(p.err, PA_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int stage = 0;
     uint32_t phase = 0;
     while (true) {
-      if (!mbar_wait(&sm.full[stage], phase)) {
+      if (!mbar_wait(&sm.full[stage], phase, p.wait_ns)) {
         report(p.err, PA_DEV_TIMEOUT);
         break;
       }
@@ -525,6 +538,9 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
   const int2 mt = p.meta[s];
   const int np = mt.y;
   if (np <= 1) return;
+  // partials left by an aborted or earlier call may name slots beyond this
+  // workspace: read none of them (the call has reported its error)
+  if (mt.x < 0 || static_cast<long long>(mt.x) + np > p.n_slots) return;
   const size_t slot0 = static_cast<size_t>(mt.x);
   float m = neg_inf(), l = 0.f, so, sn;
   float2 o = make_float2(0.f, 0.f);
@@ -579,6 +595,8 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
 
 
 int g_grid_limit = 0;
+int g_fault_stage = -1;                        // test hook, see pa_decode_set_test_fault
+unsigned long long g_fault_wait_ns = kWaitLimitNs;
 int g_decode_path = 0;   // 0 automatic, 1 split-context kernel, 2 cluster kernel
 
 struct WsLayout {
@@ -758,8 +776,11 @@ extern "C" int pa_decode_set_grid_limit(int max_ctas) {
 
 extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
   if (num_seqs < 0 || !page_size_ok(block_tokens)) return PA_ERR_ARG;
-  // the per-sequence kernel takes 16-token pages, the per-head one 16 or 32
-  if (block_tokens == kBs / 2 || g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
+  // the per-sequence kernel takes 16-token pages, the per-head one 8, 16 or
+  // 32 (with 8, four 1 KiB copies per tile make it slower than the split
+  // kernel: only when forced)
+  if (g_decode_path == PA_DECODE_SPLIT) return PA_DECODE_SPLIT;
+  if (block_tokens == kBs / 2 && g_decode_path == PA_DECODE_AUTO) return PA_DECODE_SPLIT;
   if (g_decode_path == PA_DECODE_SEQ) return block_tokens == kBs ? PA_DECODE_SEQ : PA_DECODE_SPLIT;
   if (g_decode_path == PA_DECODE_CLUSTER) return PA_DECODE_CLUSTER;
   DeviceInfo di;
@@ -767,6 +788,14 @@ extern "C" int pa_decode_kernel_for(int num_seqs, int block_tokens) {
   if (rc != PA_OK) return rc;
   return decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit) > 0 ? PA_DECODE_CLUSTER
                                                                       : PA_DECODE_SPLIT;
+}
+
+extern "C" int pa_decode_set_test_fault(int stage, long long wait_limit_ns) {
+  if (stage < -1 || (stage >= 0 && (wait_limit_ns < 1000 || wait_limit_ns > 1000000000LL)))
+    return PA_ERR_ARG;
+  g_fault_stage = stage;
+  g_fault_wait_ns = stage >= 0 ? static_cast<unsigned long long>(wait_limit_ns) : kWaitLimitNs;
+  return PA_OK;
 }
 
 extern "C" int pa_decode_set_path(int path) {
@@ -847,14 +876,18 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
     return launch_decode_seq(pmap, out, q, kv_cache, num_blocks, block_table, n_layers,
                              max_blocks_per_seq, context_lens, num_seqs, layer, scale, err, c, st);
   }
-  // (16-token pages; with 32-token pages a tile is half a page)
+  // (16-token pages; with 32-token pages a tile is half a page, with 8 two
+  // pages: forced only, see pa_decode_kernel_for)
   if ((BT == kBs && g_decode_path != PA_DECODE_SPLIT) ||
-      (BT == 2 * kBs && (g_decode_path == PA_DECODE_AUTO || g_decode_path == PA_DECODE_CLUSTER))) {
+      (BT == 2 * kBs && (g_decode_path == PA_DECODE_AUTO || g_decode_path == PA_DECODE_CLUSTER)) ||
+      (BT == kBs / 2 && g_decode_path == PA_DECODE_CLUSTER)) {
     int c = decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit);
     if (c == 0 && g_decode_path == PA_DECODE_CLUSTER) c = 1;
     if (c > 0) {
-      const CUtensorMap *tmap = &map;   // 16-token pages: the split kernel's map is the tile map
-      if (BT != kBs) {
+      // 16-token pages: the split kernel's map is the tile map; 8-token pages:
+      // its map (one page's K or V rows of a head) serves both kernels
+      const CUtensorMap *tmap = &map;
+      if (BT == 2 * kBs) {
         static thread_local const void *tmap_pool = nullptr;
         static thread_local int tmap_blocks = 0;
         alignas(64) static thread_local CUtensorMap tile_map;
@@ -891,6 +924,9 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
   prm.layer = layer;
   prm.cap_tokens = max_blocks_per_seq * BT;
   prm.qscale = scale * kLog2e;
+  prm.n_slots = max_slots(num_seqs, G);
+  prm.fault_stage = g_fault_stage;
+  prm.wait_ns = g_fault_stage >= 0 ? g_fault_wait_ns : kWaitLimitNs;
 
   if (launch_pdl(decode_split_kernel<BT>, dim3(G), dim3(kThreads), smem, st, map, prm) !=
       cudaSuccess)

@@ -21,7 +21,8 @@
 //    and keep their own online-softmax state (the 4 q heads of the group are
 //    the M rows of m16n8k16 bf16 MMAs, as in the split-context kernel); at the
 //    end the 8 warp states are combined in shared memory, then the c CTA
-//    states in the cluster leader's shared memory.
+//    states in the cluster leader's shared memory (asynchronous stores that
+//    complete the leader's barrier by their byte count).
 //  * Before the dependency wait the CTA reads its sequence's context length
 //    and first page ids as they are then and prefetches those tiles into L2.
 //    Right after the wait the first stages are fetched from those ids while
@@ -59,14 +60,16 @@ struct PairStage {
   int n;       // slots holding a tile (slot w: tile j0 + w)
   int last;    // the sequence's last tile
   int tail;    // tokens in it (1..16)
-  int bad;     // bit w: slot w's page id was out of range (tile skipped)
+  int bad;     // bit w: slot w's page id was out of range (16/32-token pages: tile skipped)
   int flags;
+  int va, vb;  // 8-token pages, bit w: slot w's first / second page was loaded
 };
 
 struct __align__(1024) PairSmem {
   unsigned char kv[kPairStages][kPairStageBytes];
   float part_o[kMaxCluster][kGqa][kD];   // cluster leader: each CTA's unnormalised result
   float2 part_ml[kMaxCluster][kGqa];     // and its (m, l), m in the log2 domain
+  // (part_o rows are 16-byte aligned: the stages before them are 1 KiB multiples)
   PairStage desc[kPairStages];
   uint64_t full[kPairStages];
   uint64_t empty[kPairStages];
@@ -119,10 +122,6 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
   return a;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                : "memory");
@@ -158,6 +157,46 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   }
 }
 
+// Asynchronous stores into the shared memory of a CTA of the cluster,
+// counted as transaction bytes on that CTA's mbarrier: the receiver sees the
+// data once the barrier's phase completes; the sender needs no fence and no
+// arrival of its own.  Addresses from map_to_rank.
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float2 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::
+                   "r"(addr),
+               "f"(v.x), "f"(v.y), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fma4(float4 &acc, const float4 &o, float sc) {
+  acc.x = fmaf(o.x, sc, acc.x);
+  acc.y = fmaf(o.y, sc, acc.y);
+  acc.z = fmaf(o.z, sc, acc.z);
+  acc.w = fmaf(o.w, sc, acc.w);
+}
+
+__device__ __forceinline__ uint2 bf16x4_scaled(const float4 &o, float s) {
+  return make_uint2(float2_to_bf16x2(o.x * s, o.y * s), float2_to_bf16x2(o.z * s, o.w * s));
+}
+
+// L2 prefetch of the box of the tensor map at (head h, K|V kv, page blk):
+// with 8-token pages one page's K or V rows of the head.
+__device__ __forceinline__ void prefetch_rows_l2(const void *tmap, int h, int kv, int blk) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(0), "r"(h), "r"(0), "r"(kv), "r"(blk)
+      : "memory");
+}
+
 // L2 prefetch of one tile: the box of the tensor map at (head h, first
 // token tok0 of page blk).
 __device__ __forceinline__ void prefetch_tile_l2(const void *tmap, int h, int tok0, int blk) {
@@ -169,13 +208,28 @@ __device__ __forceinline__ void prefetch_tile_l2(const void *tmap, int h, int to
 }
 
 // Pages of BT tokens hold BT / 16 tiles: tile j is tokens 16 (j mod that)
-// .. of page j / that.
+// .. of page j / that.  With 8-token pages a tile is two pages, 2j and 2j+1
+// (page() is the first, tok0() 0).
 template <int BT>
 struct TileOfPage {
-  static constexpr int kTiles = BT / kBs;
-  __device__ static int page(int j) { return j / kTiles; }
-  __device__ static int tok0(int j) { return (j % kTiles) * kBs; }
+  static constexpr int kTiles = BT >= kBs ? BT / kBs : 1;
+  __device__ static int page(int j) { return BT >= kBs ? j / kTiles : 2 * j; }
+  __device__ static int tok0(int j) { return BT >= kBs ? (j % kTiles) * kBs : 0; }
 };
+
+// Page ids of tile j of a table row: blk (the tile's page, or with 8-token
+// pages its first) and, with 8-token pages, blk2 = the second page when the
+// context reaches into it (else -1).  -1 for both when j >= t1.
+template <int BT>
+__device__ __forceinline__ void tile_ids(const int32_t *row, int j, int t1, int ctx, int &blk,
+                                         int &blk2) {
+  blk = -1;
+  blk2 = -1;
+  if (j < t1) {
+    blk = row[TileOfPage<BT>::page(j)];
+    if (BT < kBs && j * kBs + BT < ctx) blk2 = row[2 * j + 1];
+  }
+}
 
 // Tiles [t0, t1) of a head with nb tiles, for CTA `rank` of c.
 __device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int &t1) {
@@ -184,21 +238,27 @@ __device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int
 }
 
 // One stage: wait until it is free, write its descriptor, issue the copies
-// of tiles j0 .. j0+n-1 (lane w < n holds the page id of tile j0 + w).
-// Returns the slots whose page id is out of range, or -1 if the wait timed out.
+// of tiles j0 .. j0+n-1 (lane w < n holds the page ids of tile j0 + w, see
+// tile_ids).  Returns the slots with a page id out of range, or -1 if the
+// wait timed out.
 template <int BT>
 __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *map, int stage,
                                              uint32_t phase, int h, int j0, int n, int blk,
-                                             int last, int tail, int flags, int num_blocks,
-                                             int lane) {
+                                             int blk2, int last, int tail, int flags,
+                                             int num_blocks, int lane) {
   int good = 1;
   if (lane == 0) good = mbar_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return -1;
   const bool mine = lane < n;
   const bool valid = mine && blk >= 0 && blk < num_blocks;
+  // 8-token pages: the tile's second page, where its tokens reach into it
+  const int n_tok = (j0 + lane == last) ? tail : kBs;
+  const bool need2 = BT < kBs && mine && n_tok > BT;
+  const bool valid2 = need2 && blk2 >= 0 && blk2 < num_blocks;
   const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-  const unsigned bad = __ballot_sync(0xffffffffu, mine && !valid);
+  const unsigned vmask2 = __ballot_sync(0xffffffffu, valid2);
+  const unsigned bad = __ballot_sync(0xffffffffu, (mine && !valid) || (need2 && !valid2));
   if (lane == 0) {
     PairStage d;
     d.j0 = j0;
@@ -207,15 +267,31 @@ __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *ma
     d.tail = tail;
     d.bad = static_cast<int>(bad);
     d.flags = flags;
+    d.va = static_cast<int>(vmask);
+    d.vb = static_cast<int>(vmask2);
     sm.desc[stage] = d;
-    const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * kSlotBytes;
+    const uint32_t bytes =
+        BT < kBs ? static_cast<uint32_t>(__popc(vmask) + __popc(vmask2)) * (kSlotBytes / 2)
+                 : static_cast<uint32_t>(__popc(vmask)) * kSlotBytes;
     if (bytes) mbar_arrive_expect_tx(&sm.full[stage], bytes);
     else mbar_arrive(&sm.full[stage]);
   }
   __syncwarp();
-  if (valid)
-    tma_load_5d(sm.kv[stage] + lane * kSlotBytes, map, 0, h, TileOfPage<BT>::tok0(j0 + lane), 0,
-                blk, &sm.full[stage]);
+  unsigned char *slot = sm.kv[stage] + lane * kSlotBytes;
+  if (BT < kBs) {
+    // K and V rows of each 8-token page, 1 KiB each: the first page's to
+    // token rows 0..7 of the slot's K and V halves, the second's to 8..15
+    if (valid) {
+      tma_load_5d(slot, map, 0, h, 0, 0, blk, &sm.full[stage]);
+      tma_load_5d(slot + kSlotBytes / 2, map, 0, h, 0, 1, blk, &sm.full[stage]);
+    }
+    if (valid2) {
+      tma_load_5d(slot + kSlotBytes / 4, map, 0, h, 0, 0, blk2, &sm.full[stage]);
+      tma_load_5d(slot + 3 * kSlotBytes / 4, map, 0, h, 0, 1, blk2, &sm.full[stage]);
+    }
+  } else if (valid) {
+    tma_load_5d(slot, map, 0, h, TileOfPage<BT>::tok0(j0 + lane), 0, blk, &sm.full[stage]);
+  }
   return static_cast<int>(bad);
 }
 
@@ -245,22 +321,32 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       mbar_init(&sm.full[st], 1);
       mbar_init(&sm.empty[st], kPairWarps);
     }
-    mbar_init(&sm.parts_full, c * kPairWarps * 32);
+    // the leader expects every CTA's state (O and (m, l) of 4 q heads) as bytes
+    mbar_init(&sm.parts_full, 1);
+    if (rank == 0 && c > 1)
+      mbar_arrive_expect_tx(&sm.parts_full, static_cast<uint32_t>(c * kGqa * (kD * 4 + 8)));
     fence_mbar_init();
   }
   // the speculative plan: this CTA's range under the context length as it
   // reads now, and its first page ids; their tiles are prefetched into L2
-  int spec_ctx = 0, spec_t0 = 0, spec_t1 = 0, spec_blk = -1;
+  int spec_ctx = 0, spec_t0 = 0, spec_t1 = 0, spec_blk = -1, spec_blk2 = -1;
   if (warp == kPairWarps) {
     spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
     tile_range((spec_ctx + kBs - 1) / kBs, rank, c, spec_t0, spec_t1);
     // (the first 32 ids are kept for the first stages; the prefetches share
     // the SM's TMA unit with the copies, so only the first 3 stages' worth)
     const int j = spec_t0 + lane;
-    if (j < spec_t1) {
-      spec_blk = row[TP::page(j)];
-      if (lane < kPrefetchTiles && spec_blk >= 0 && spec_blk < p.num_blocks)
+    tile_ids<BT>(row, j, spec_t1, spec_ctx, spec_blk, spec_blk2);
+    if (spec_blk >= 0 && spec_blk < p.num_blocks) {
+      if (BT < kBs) {
+        // (the first page's K and V of a third as many tiles: the same count of requests)
+        if (lane < kPrefetchTiles / 3) {
+          prefetch_rows_l2(&kv_map, h, 0, spec_blk);
+          prefetch_rows_l2(&kv_map, h, 1, spec_blk);
+        }
+      } else if (lane < kPrefetchTiles) {
         prefetch_tile_l2(&kv_map, h, TP::tok0(j), spec_blk);
+      }
     }
   }
   if (c > 1) cluster_sync_all();   // every CTA's barriers exist before any remote arrival
@@ -273,7 +359,8 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     // current values, read now and checked against the speculative ones
     // once the first stages are on their way
     const int ctx_raw = p.context_lens[s];
-    const int blk_now = spec_t0 + lane < spec_t1 ? row[TP::page(spec_t0 + lane)] : -1;
+    int blk_now, blk_now2;
+    tile_ids<BT>(row, spec_t0 + lane, spec_t1, spec_ctx, blk_now, blk_now2);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, issued_parity = 0;   // per stage: used / parity of its last phase
@@ -284,8 +371,9 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     for (int e = 0; e < spec_stages && ok; ++e) {
       const int j0 = spec_t0 + e * kPairWarps;
       const int blk = __shfl_sync(0xffffffffu, spec_blk, (e * kPairWarps + lane) & 31);
+      const int blk2 = __shfl_sync(0xffffffffu, spec_blk2, (e * kPairWarps + lane) & 31);
       const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j0,
-                                        min(kPairWarps, spec_t1 - j0), blk, spec_nb - 1,
+                                        min(kPairWarps, spec_t1 - j0), blk, blk2, spec_nb - 1,
                                         spec_ctx - (spec_nb - 1) * kBs, 0, p.num_blocks, lane);
       if (bad < 0) {
         ok = false;
@@ -304,31 +392,35 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     const int ctx = min(max(ctx_raw, 0), p.cap_tokens);
     if (lane == 0 && rank == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
       report(p.err, PA_DEV_CTX_RANGE);
-    const bool same = ctx == spec_ctx && __all_sync(0xffffffffu, blk_now == spec_blk);
+    const bool same =
+        ctx == spec_ctx && __all_sync(0xffffffffu, blk_now == spec_blk && blk_now2 == spec_blk2);
     const int nb = (ctx + kBs - 1) / kBs;
     const int last = nb - 1, tail = ctx - (nb - 1) * kBs;
     int t0 = spec_t0, t1 = spec_t1, j = spec_t0 + spec_stages * kPairWarps, base = spec_t0;
-    int ids = blk_now, flags = 0;
+    int ids = blk_now, ids2 = blk_now2, flags = 0;
     if (!same) {
       // the plan moved: stream the current range from its start; the
       // consumers drop what they accumulated from the speculative stages
       tile_range(nb, rank, c, t0, t1);
       j = base = t0;
-      ids = t0 + lane < t1 ? row[TP::page(t0 + lane)] : -1;
+      tile_ids<BT>(row, t0 + lane, t1, ctx, ids, ids2);
       flags = kReset;
     } else if (bad_seen && lane == 0) {
       report(p.err, PA_DEV_BAD_BLOCK);
     }
-    int ids_next = base + kIdBatch + lane < t1 ? row[TP::page(base + kIdBatch + lane)] : -1;
+    int ids_next, ids_next2;
+    tile_ids<BT>(row, base + kIdBatch + lane, t1, ctx, ids_next, ids_next2);
     while (ok && j < t1) {
       if (j >= base + kIdBatch) {
         base += kIdBatch;
         ids = ids_next;
-        ids_next = base + kIdBatch + lane < t1 ? row[TP::page(base + kIdBatch + lane)] : -1;
+        ids2 = ids_next2;
+        tile_ids<BT>(row, base + kIdBatch + lane, t1, ctx, ids_next, ids_next2);
       }
       const int blk = __shfl_sync(0xffffffffu, ids, (j - base + lane) & 31);
+      const int blk2 = __shfl_sync(0xffffffffu, ids2, (j - base + lane) & 31);
       const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j, min(kPairWarps, t1 - j),
-                                        blk, last, tail, flags, p.num_blocks, lane);
+                                        blk, blk2, last, tail, flags, p.num_blocks, lane);
       if (bad < 0) {
         ok = false;
         break;
@@ -354,6 +446,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         d.tail = 0;
         d.bad = 0;
         d.flags = kEnd | flags;
+        d.va = d.vb = 0;
         sm.desc[stage] = d;
         mbar_arrive(&sm.full[stage]);
         issued |= 1u << stage;
@@ -391,7 +484,16 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     const PairStage d = sm.desc[stage];
     if (d.flags & kReset) ts.reset();
     if (d.flags & kEnd) break;
-    if (w < d.n && !((d.bad >> w) & 1)) {
+    if (BT < kBs) {
+      // 8-token pages: the rows of the pages that were loaded
+      const unsigned ld = ((d.va >> w) & 1u ? 0x00ffu : 0u) | ((d.vb >> w) & 1u ? 0xff00u : 0u);
+      if (w < d.n && ld) {
+        const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
+        const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
+        attend_tile<true>(ktile, ktile + kBs * kHeadRowBytes, n_valid,
+                          ld & ((1u << n_valid) - 1u), qa, qc, p.qscale, lane, ts);
+      }
+    } else if (w < d.n && !((d.bad >> w) & 1)) {
       const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
       const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
       attend_tile<false>(ktile, ktile + kBs * kHeadRowBytes, n_valid, 0u, qa, qc, p.qscale, lane,
@@ -420,52 +522,58 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kPairWarps * 32) : "memory");
-  const int ct = tid;               // 0..255: row ct / 64, dim ct % 64
-  const int rr = ct >> 6, dd = ct & 63;
+  // threads 0..63: q head row qrow, dims d0 .. d0+3
+  if (tid >= kGqa * 16) return;
+  const int qrow = tid >> 4, d0 = 4 * (tid & 15);
   float M = neg_inf();
 #pragma unroll
   for (int k = 0; k < kPairWarps; ++k) {
     const float2 ml = reinterpret_cast<const float2 *>(
-        reinterpret_cast<const float *>(sm.kv[0] + k * kSlotBytes) + kGqa * kD)[rr];
+        reinterpret_cast<const float *>(sm.kv[0] + k * kSlotBytes) + kGqa * kD)[qrow];
     M = fmaxf(M, ml.x);
   }
-  float L = 0.f, O = 0.f;
+  float L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != neg_inf()) {
 #pragma unroll
     for (int k = 0; k < kPairWarps; ++k) {
       const float *ko = reinterpret_cast<const float *>(sm.kv[0] + k * kSlotBytes);
-      const float2 ml = reinterpret_cast<const float2 *>(ko + kGqa * kD)[rr];
+      const float2 ml = reinterpret_cast<const float2 *>(ko + kGqa * kD)[qrow];
       const float sc = fast_exp2(ml.x - M);   // empty warp states carry m = -inf: weight 0
       L = fmaf(ml.y, sc, L);
-      O = fmaf(ko[rr * kD + dd], sc, O);
+      fma4(O, *reinterpret_cast<const float4 *>(ko + qrow * kD + d0), sc);
     }
   }
-  __nv_bfloat16 *dst = p.out + (static_cast<size_t>(s) * kHq + h * kGqa + rr) * kD + dd;
+  uint2 *dst = reinterpret_cast<uint2 *>(
+      p.out + (static_cast<size_t>(s) * kHq + h * kGqa + qrow) * kD + d0);
   if (c == 1) {
-    *dst = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    *dst = bf16x4_scaled(O, L > 0.f ? 1.f / L : 0.f);
     return;
   }
 
-  // ---- the c CTA states -> the output, in the cluster leader's shared memory
-  st_cluster_f32(map_to_rank(&sm.part_o[rank][rr][dd], 0), O);
-  if (dd == 0) st_cluster_f32x2(map_to_rank(&sm.part_ml[rank][rr], 0), make_float2(M, L));
-  mbar_arrive_cluster(map_to_rank(&sm.parts_full, 0));
+  // ---- the c CTA states -> the output, in the cluster leader's shared
+  // memory: 64 asynchronous 16-byte stores and 4 of 8 bytes per CTA, which
+  // complete the leader's barrier by their byte count
+  const uint32_t bar = map_to_rank(&sm.parts_full, 0);
+  st_async_f32x4(map_to_rank(&sm.part_o[rank][qrow][d0], 0), O, bar);
+  if ((tid & 15) == 0) st_async_f32x2(map_to_rank(&sm.part_ml[rank][qrow], 0), make_float2(M, L), bar);
   if (rank != 0) return;
   if (!mbar_wait_cluster(&sm.parts_full, 0)) {
     report(p.err, PA_DEV_TIMEOUT);
     return;
   }
   float Mc = neg_inf();
-  for (int k = 0; k < c; ++k) Mc = fmaxf(Mc, sm.part_ml[k][rr].x);
-  float Lc = 0.f, Oc = 0.f;
+  for (int k = 0; k < c; ++k) Mc = fmaxf(Mc, sm.part_ml[k][qrow].x);
+  float Lc = 0.f;
+  float4 Oc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (Mc != neg_inf()) {
     for (int k = 0; k < c; ++k) {
-      const float sc = fast_exp2(sm.part_ml[k][rr].x - Mc);
-      Lc = fmaf(sm.part_ml[k][rr].y, sc, Lc);
-      Oc = fmaf(sm.part_o[k][rr][dd], sc, Oc);
+      const float sc = fast_exp2(sm.part_ml[k][qrow].x - Mc);
+      Lc = fmaf(sm.part_ml[k][qrow].y, sc, Lc);
+      fma4(Oc, *reinterpret_cast<const float4 *>(&sm.part_o[k][qrow][d0]), sc);
     }
   }
-  *dst = __float2bfloat16_rn(Lc > 0.f ? Oc / Lc : 0.f);
+  *dst = bf16x4_scaled(Oc, Lc > 0.f ? 1.f / Lc : 0.f);
 }
 
 // ===========================================================================
@@ -831,14 +939,15 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                        int layer, float scale, int32_t *err, int cluster, cudaStream_t stream) {
   if (cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return PA_ERR_ARG;
-  if (block_tokens != kBs && block_tokens != 2 * kBs) return PA_ERR_ARG;
-  const int bi = block_tokens == kBs ? 0 : 1;
+  if (block_tokens != kBs / 2 && block_tokens != kBs && block_tokens != 2 * kBs) return PA_ERR_ARG;
+  const int bi = block_tokens == kBs ? 0 : (block_tokens == 2 * kBs ? 1 : 2);
   void (*kern)(const CUtensorMap, PairParams) =
-      bi == 0 ? decode_pair_kernel<kBs> : decode_pair_kernel<2 * kBs>;
+      bi == 0 ? decode_pair_kernel<kBs>
+              : (bi == 1 ? decode_pair_kernel<2 * kBs> : decode_pair_kernel<kBs / 2>);
   DeviceInfo di;
   int rc = current_device(&di);
   if (rc != PA_OK) return rc;
-  static bool attr_done[2][64] = {};
+  static bool attr_done[3][64] = {};
   const size_t smem = decode_pair_smem_bytes();
   if (!attr_done[bi][di.device]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

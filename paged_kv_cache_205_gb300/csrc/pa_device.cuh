@@ -76,13 +76,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity,
 // the barrier instead of spinning, so they leave the issue slots to the warps
 // doing work.  Returns false when the time limit ran out (the caller then
 // reports PA_DEV_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   constexpr uint32_t kSuspendNs = 200000;   // re-check the time limit every 0.2 ms
   if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

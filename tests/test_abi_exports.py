@@ -45,14 +45,20 @@ def test_host_validation_without_a_device():
     assert lib.pa_free(z, 2, z, 1, 4, z, z, z, 8, z, z) == -1
     assert lib.pa_decode_set_grid_limit(-1) == -2
     assert lib.pa_decode_set_grid_limit(0) == 0
+    # the bounded-wait test hook: a stage >= -1 and a limit of 1 us .. 1 s
+    assert lib.pa_decode_set_test_fault(-2, 0) == -2
+    assert lib.pa_decode_set_test_fault(0, 10) == -2
+    assert lib.pa_decode_set_test_fault(0, 2_000_000_000) == -2
+    assert lib.pa_decode_set_test_fault(0, 50_000) == 0
+    assert lib.pa_decode_set_test_fault(-1, 0) == 0
 
 
 def test_decode_path_switch_without_a_device():
     """The kernel choice: only the three path values are accepted; 8-token
-    pages always take the split-context kernel, the per-sequence kernel
-    16-token pages only (32 fall back to the split kernel), the per-head
-    kernel 16 or 32; a forced path is reported as is; a bad count or page
-    size is refused."""
+    pages take the split kernel unless the per-head kernel is forced; the
+    per-sequence kernel takes 16-token pages only (8 and 32 fall back to the
+    split kernel), the per-head kernel 8, 16 or 32; a forced path is
+    reported as is; a bad count or page size is refused."""
     import paged_kv_cache_205_gb300 as pk
     lib = pk.library()
     assert lib.pa_decode_set_path(4) == -2 and lib.pa_decode_set_path(-1) == -2
@@ -66,10 +72,11 @@ def test_decode_path_switch_without_a_device():
         assert lib.pa_decode_set_path(pk.PA_DECODE_CLUSTER) == 0
         assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_CLUSTER
         assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_CLUSTER
-        assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_CLUSTER
         assert lib.pa_decode_set_path(pk.PA_DECODE_SEQ) == 0
         assert lib.pa_decode_kernel_for(4, 16) == pk.PA_DECODE_SEQ
         assert lib.pa_decode_kernel_for(4, 32) == pk.PA_DECODE_SPLIT
+        assert lib.pa_decode_kernel_for(4, 8) == pk.PA_DECODE_SPLIT
     finally:
         assert lib.pa_decode_set_path(pk.PA_DECODE_AUTO) == 0
 

@@ -11,13 +11,10 @@ import pytest
 from oracle import batching
 import pa_workloads as wl
 
-GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "batching_worked_example.json")
-
-
-def _compare(max_slots, n_layers, mb, pages, budget, requests):
+def _compare(max_slots, n_layers, mb, pages, budget, requests, block_tokens=16):
     import paged_kv_cache_205_gb300 as pk
-    nat = pk.Batcher(max_slots, n_layers, mb, pages, budget)
-    ref = batching.Scheduler(max_slots, n_layers, pages, budget)
+    nat = pk.Batcher(max_slots, n_layers, mb, pages, budget, block_tokens=block_tokens)
+    ref = batching.Scheduler(max_slots, n_layers, pages, budget, block_tokens)
     for r in requests:
         nat.submit(*r)
         ref.submit(*r)
@@ -45,24 +42,34 @@ def _compare(max_slots, n_layers, mb, pages, budget, requests):
     return steps
 
 
-def test_worked_example():
-    g = json.load(open(GOLDEN))
+@pytest.mark.parametrize("golden", ["batching_worked_example.json",
+                                    "batching_worked_example_8.json"])
+def test_worked_example(golden):
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", golden)))
     n = _compare(g["max_slots"], g["n_layers"], g["max_blocks_per_seq"], g["num_blocks"],
-                 g["prefill_budget"], [tuple(r) for r in g["requests"]])
+                 g["prefill_budget"], [tuple(r) for r in g["requests"]],
+                 g.get("block_tokens", 16))
     assert n == len(g["expect_steps"])
 
 
+@pytest.mark.parametrize("block_tokens", [8, 16, 32])
 @pytest.mark.parametrize("name", ["serve_tiny", "serve256"])
-def test_serving_workloads(name):
+def test_serving_workloads(name, block_tokens):
+    """The serving workloads with pages of 8, 16 and 32 tokens: the pool
+    keeps its bytes (16 / page times the pages)."""
     w = wl.make_serve_workload(name)
-    assert _compare(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
-                    w.prefill_budget, w.requests) > 0
+    pages = w.num_blocks * 16 // block_tokens
+    mb = max((p + g + block_tokens - 1) // block_tokens for _, p, g in w.requests) + 1
+    assert _compare(w.max_slots, w.n_layers, mb, pages, w.prefill_budget, w.requests,
+                    block_tokens) > 0
 
 
 def test_argument_checks():
     import paged_kv_cache_205_gb300 as pk
     with pytest.raises(pk.PagedKVError):
         pk.Batcher(0, 2, 4, 12, 32)
+    with pytest.raises(pk.PagedKVError):
+        pk.Batcher(2, 2, 4, 12, 32, block_tokens=24)
     b = pk.Batcher(2, 2, 4, 12, 32)
     for bad in [(0, 0, 1), (1, 5, 0), (2, 33, 1), (3, 40, 30), (4, 30, 40)]:
         with pytest.raises(pk.PagedKVError):

@@ -33,11 +33,12 @@ def _pk():
 class DeviceLoop:
     """The buffers of one batcher on the GPU."""
 
-    def __init__(self, w, pool, free_list):
+    def __init__(self, w, pool, free_list, block_tokens=BS, max_blocks_per_seq=None):
         import torch
         pk = _pk()
         dev = torch.device("cuda")
-        S, L, mb, B = w.max_slots, w.n_layers, w.max_blocks_per_seq, w.prefill_budget
+        S, L, B = w.max_slots, w.n_layers, w.prefill_budget
+        mb = w.max_blocks_per_seq if max_blocks_per_seq is None else max_blocks_per_seq
         self.w = w
         self.pool = pool
         self.bt = torch.full((S, L, mb), -1, dtype=torch.int32, device=dev)
@@ -46,7 +47,7 @@ class DeviceLoop:
         self.fl = dev_i32(free_list)
         self.fc = torch.tensor([len(free_list)], dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = pk.decode_workspace(S, mb)
+        self.ws = pk.decode_workspace(S, mb, block_tokens=block_tokens)
         bf = torch.bfloat16
         self.pq = torch.zeros((L, B, N_Q, D), dtype=bf, device=dev)
         self.pk_ = torch.zeros((L, B, N_KV, D), dtype=bf, device=dev)
@@ -59,7 +60,7 @@ class DeviceLoop:
         self.bufs = pk.batch_buffers(self.pool, self.bt, self.bt_tmp, self.ctl, self.fl, self.fc,
                                      self.err, self.ws, self.pq, self.pk_, self.pv, self.po,
                                      self.dq, self.dk, self.dv, self.do, w.scale)
-        self.b = pk.Batcher(S, L, mb, len(free_list), B)
+        self.b = pk.Batcher(S, L, mb, len(free_list), B, block_tokens=block_tokens)
         for r in w.requests:
             self.b.submit(*r)
 
@@ -69,16 +70,21 @@ def _put(t, bits):
     t.copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16))
 
 
-def test_serve_tiny_step_by_step():
+@pytest.mark.parametrize("block_tokens", [8, 16, 32])
+def test_serve_tiny_step_by_step(block_tokens):
+    """serve_tiny with pages of 8, 16 and 32 tokens (the pool keeps its
+    bytes), step by step against the oracle's loop."""
     import torch
     w = wl.make_serve_workload("serve_tiny")
     seed = 11
+    nb = w.num_blocks * BS // block_tokens
+    mb = max((p + g + block_tokens - 1) // block_tokens for _, p, g in w.requests) + 1
     rng = np.random.default_rng(w.seed)
-    free_list = rng.permutation(w.num_blocks).astype(np.int32)
-    pool0 = np.full((w.num_blocks, 2, BS, N_KV, D), wl.BF16_NAN, dtype=np.uint16)
+    free_list = rng.permutation(nb).astype(np.int32)
+    pool0 = np.full((nb, 2, block_tokens, N_KV, D), wl.BF16_NAN, dtype=np.uint16)
     dl = DeviceLoop(w, torch.from_numpy(pool0.view(np.int16)).view(torch.bfloat16).cuda(),
-                    free_list)
-    ref = batching.Scheduler(w.max_slots, w.n_layers, w.num_blocks, w.prefill_budget)
+                    free_list, block_tokens, mb)
+    ref = batching.Scheduler(w.max_slots, w.n_layers, nb, w.prefill_budget, block_tokens)
     for r in w.requests:
         ref.submit(*r)
     st = batching.PagedState(pool0, np.full(tuple(dl.bt.shape), -1, np.int32), free_list,
@@ -128,7 +134,7 @@ def test_serve_tiny_step_by_step():
             got = host_f64(dl.do[:, :p.n_rows])
             assert_attention_close(got, dec, f"decode step {steps}")
     assert steps > 10 and prefills > 2
-    assert int(dl.fc.item()) == w.num_blocks and (dl.bt.cpu().numpy() == -1).all()
+    assert int(dl.fc.item()) == nb and (dl.bt.cpu().numpy() == -1).all()
     dl.b.close()
 
 

@@ -94,9 +94,9 @@ def test_edge_contexts_and_splits(page, grid):
 @pytest.mark.parametrize("n", [4, 20])
 def test_per_head_cluster_kernel_forced(page, n):
     """The per-head cluster kernel forced (clusters of 8 CTAs at 4
-    sequences, of 1 at 20): with 32-token pages it runs, a tile being half a
-    page; with 8-token pages the call falls back to the split kernel.  A page
-    id out of range in one sequence is reported and its tokens dropped."""
+    sequences, of 1 at 20): with 32-token pages a tile is half a page, with
+    8-token pages two pages (four 1 KiB copies).  A page id out of range in
+    one sequence is reported and its tokens dropped."""
     pk = _pk()
     ctx_list = EDGE[-n:]
     pool, table, ctx, q = _case(90 + page + n, ctx_list, page, q_scale=2.0)
@@ -104,8 +104,7 @@ def test_per_head_cluster_kernel_forced(page, n):
     table[s_bad, 0, 1] = pool.shape[0] + 3
     pk.pa_decode_set_path(pk.PA_DECODE_CLUSTER)
     try:
-        want = pk.PA_DECODE_CLUSTER if page == 32 else pk.PA_DECODE_SPLIT
-        assert pk.pa_decode_kernel_for(n, page) == want
+        assert pk.pa_decode_kernel_for(n, page) == pk.PA_DECODE_CLUSTER
         ref, e_ref = oracle.decode_attention(q, pool, table, ctx, 0, block_tokens=page)
         out, err = _gpu_attention(pool, table, ctx, q)
     finally:

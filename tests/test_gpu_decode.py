@@ -274,8 +274,9 @@ def test_automatic_kernel_choice(decode_path):
     """Automatic choice: the per-head cluster kernel while every (sequence,
     kv head) pair gets two CTAs (two CTAs per SM in all), the split-context
     kernel beyond, for 16- and 32-token pages; a grid limit lowers the
-    bound; 8-token pages always take the split kernel; a forced path is
-    reported as forced."""
+    bound; 8-token pages take the split kernel unless the per-head kernel is
+    forced (four 1 KiB copies per tile make it slower there); a forced path
+    is reported as forced."""
     import torch
     pk = _pk()
     pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
@@ -292,3 +293,25 @@ def test_automatic_kernel_choice(decode_path):
     assert pk.pa_decode_kernel_for(5) == pk.PA_DECODE_SPLIT
     pk.pa_decode_set_path(pk.PA_DECODE_SEQ)
     assert pk.pa_decode_kernel_for(300) == pk.PA_DECODE_SEQ
+
+
+@pytest.mark.parametrize("grid", [0, 24, 64, 152, 304])
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 16, 19, 32])
+def test_mixed_lengths_every_cluster_size(decode_path, n, grid):
+    """Batches of 1..32 sequences with heavy-tailed lengths (empty, single
+    tokens, page edges, long), under grid limits that give the per-head
+    cluster kernel clusters of 1, 2, 4 and 8 CTAs (or hand larger batches to
+    the split-context kernel)."""
+    rng = np.random.default_rng(1000 + 37 * n + grid)
+    ctx = np.floor(np.exp(rng.uniform(0, np.log(3000), size=n))).astype(np.int64)
+    ctx[rng.random(n) < 0.15] = 0
+    if n >= 3:
+        ctx[:3] = [1, 16, 2900]
+    w, pool, q = _small_case(2000 + n + grid, ctx, q_scale=2.0)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0, grid=grid)
+    assert err == 0
+    assert_attention_close(out, ref, f"n={n} grid={grid}")
+    for s, t in enumerate(ctx):
+        if t == 0:
+            assert np.all(out[s] == 0.0)
