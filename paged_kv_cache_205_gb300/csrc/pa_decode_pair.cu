@@ -60,9 +60,9 @@ struct PairStage {
   int n;       // slots holding a tile (slot w: tile j0 + w)
   int last;    // the sequence's last tile
   int tail;    // tokens in it (1..16)
-  int bad;     // bit w: slot w's page id was out of range (16/32-token pages: tile skipped)
+  int bad;     // bit w: slot w's page id was out of range (tile skipped); with 8-token
+               // pages instead bit w / 8 + w: slot w's first / second page was loaded
   int flags;
-  int va, vb;  // 8-token pages, bit w: slot w's first / second page was loaded
 };
 
 struct __align__(1024) PairSmem {
@@ -252,33 +252,29 @@ __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *ma
   if (!good) return -1;
   const bool mine = lane < n;
   const bool valid = mine && blk >= 0 && blk < num_blocks;
-  // 8-token pages: the tile's second page, where its tokens reach into it
-  const int n_tok = (j0 + lane == last) ? tail : kBs;
-  const bool need2 = BT < kBs && mine && n_tok > BT;
-  const bool valid2 = need2 && blk2 >= 0 && blk2 < num_blocks;
-  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-  const unsigned vmask2 = __ballot_sync(0xffffffffu, valid2);
-  const unsigned bad = __ballot_sync(0xffffffffu, (mine && !valid) || (need2 && !valid2));
-  if (lane == 0) {
-    PairStage d;
-    d.j0 = j0;
-    d.n = n;
-    d.last = last;
-    d.tail = tail;
-    d.bad = static_cast<int>(bad);
-    d.flags = flags;
-    d.va = static_cast<int>(vmask);
-    d.vb = static_cast<int>(vmask2);
-    sm.desc[stage] = d;
-    const uint32_t bytes =
-        BT < kBs ? static_cast<uint32_t>(__popc(vmask) + __popc(vmask2)) * (kSlotBytes / 2)
-                 : static_cast<uint32_t>(__popc(vmask)) * kSlotBytes;
-    if (bytes) mbar_arrive_expect_tx(&sm.full[stage], bytes);
-    else mbar_arrive(&sm.full[stage]);
-  }
-  __syncwarp();
   unsigned char *slot = sm.kv[stage] + lane * kSlotBytes;
-  if (BT < kBs) {
+  if constexpr (BT < kBs) {
+    // the tile's second page, where its tokens reach into it
+    const int n_tok = (j0 + lane == last) ? tail : kBs;
+    const bool need2 = mine && n_tok > BT;
+    const bool valid2 = need2 && blk2 >= 0 && blk2 < num_blocks;
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    const unsigned vmask2 = __ballot_sync(0xffffffffu, valid2);
+    const unsigned bad = __ballot_sync(0xffffffffu, (mine && !valid) || (need2 && !valid2));
+    if (lane == 0) {
+      PairStage d;
+      d.j0 = j0;
+      d.n = n;
+      d.last = last;
+      d.tail = tail;
+      d.bad = static_cast<int>(vmask | (vmask2 << kPairWarps));   // pages loaded
+      d.flags = flags;
+      sm.desc[stage] = d;
+      const uint32_t bytes = static_cast<uint32_t>(__popc(vmask) + __popc(vmask2)) * (kSlotBytes / 2);
+      if (bytes) mbar_arrive_expect_tx(&sm.full[stage], bytes);
+      else mbar_arrive(&sm.full[stage]);
+    }
+    __syncwarp();
     // K and V rows of each 8-token page, 1 KiB each: the first page's to
     // token rows 0..7 of the slot's K and V halves, the second's to 8..15
     if (valid) {
@@ -289,10 +285,28 @@ __device__ __forceinline__ int publish_stage(PairSmem &sm, const CUtensorMap *ma
       tma_load_5d(slot + kSlotBytes / 4, map, 0, h, 0, 0, blk2, &sm.full[stage]);
       tma_load_5d(slot + 3 * kSlotBytes / 4, map, 0, h, 0, 1, blk2, &sm.full[stage]);
     }
-  } else if (valid) {
-    tma_load_5d(slot, map, 0, h, TileOfPage<BT>::tok0(j0 + lane), 0, blk, &sm.full[stage]);
+    return static_cast<int>(bad);
+  } else {
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    const unsigned bad = __ballot_sync(0xffffffffu, mine && !valid);
+    if (lane == 0) {
+      PairStage d;
+      d.j0 = j0;
+      d.n = n;
+      d.last = last;
+      d.tail = tail;
+      d.bad = static_cast<int>(bad);
+      d.flags = flags;
+      sm.desc[stage] = d;
+      const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * kSlotBytes;
+      if (bytes) mbar_arrive_expect_tx(&sm.full[stage], bytes);
+      else mbar_arrive(&sm.full[stage]);
+    }
+    __syncwarp();
+    if (valid)
+      tma_load_5d(slot, map, 0, h, TileOfPage<BT>::tok0(j0 + lane), 0, blk, &sm.full[stage]);
+    return static_cast<int>(bad);
   }
-  return static_cast<int>(bad);
 }
 
 template <int BT>
@@ -371,7 +385,8 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     for (int e = 0; e < spec_stages && ok; ++e) {
       const int j0 = spec_t0 + e * kPairWarps;
       const int blk = __shfl_sync(0xffffffffu, spec_blk, (e * kPairWarps + lane) & 31);
-      const int blk2 = __shfl_sync(0xffffffffu, spec_blk2, (e * kPairWarps + lane) & 31);
+      const int blk2 = BT < kBs ? __shfl_sync(0xffffffffu, spec_blk2, (e * kPairWarps + lane) & 31)
+                                : -1;
       const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j0,
                                         min(kPairWarps, spec_t1 - j0), blk, blk2, spec_nb - 1,
                                         spec_ctx - (spec_nb - 1) * kBs, 0, p.num_blocks, lane);
@@ -393,7 +408,8 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     if (lane == 0 && rank == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
       report(p.err, PA_DEV_CTX_RANGE);
     const bool same =
-        ctx == spec_ctx && __all_sync(0xffffffffu, blk_now == spec_blk && blk_now2 == spec_blk2);
+        ctx == spec_ctx &&
+        __all_sync(0xffffffffu, blk_now == spec_blk && (BT >= kBs || blk_now2 == spec_blk2));
     const int nb = (ctx + kBs - 1) / kBs;
     const int last = nb - 1, tail = ctx - (nb - 1) * kBs;
     int t0 = spec_t0, t1 = spec_t1, j = spec_t0 + spec_stages * kPairWarps, base = spec_t0;
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         tile_ids<BT>(row, base + kIdBatch + lane, t1, ctx, ids_next, ids_next2);
       }
       const int blk = __shfl_sync(0xffffffffu, ids, (j - base + lane) & 31);
-      const int blk2 = __shfl_sync(0xffffffffu, ids2, (j - base + lane) & 31);
+      const int blk2 = BT < kBs ? __shfl_sync(0xffffffffu, ids2, (j - base + lane) & 31) : -1;
       const int bad = publish_stage<BT>(sm, &kv_map, stage, phase, h, j, min(kPairWarps, t1 - j),
                                         blk, blk2, last, tail, flags, p.num_blocks, lane);
       if (bad < 0) {
@@ -446,7 +462,6 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         d.tail = 0;
         d.bad = 0;
         d.flags = kEnd | flags;
-        d.va = d.vb = 0;
         sm.desc[stage] = d;
         mbar_arrive(&sm.full[stage]);
         issued |= 1u << stage;
@@ -484,9 +499,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     const PairStage d = sm.desc[stage];
     if (d.flags & kReset) ts.reset();
     if (d.flags & kEnd) break;
-    if (BT < kBs) {
+    if constexpr (BT < kBs) {
       // 8-token pages: the rows of the pages that were loaded
-      const unsigned ld = ((d.va >> w) & 1u ? 0x00ffu : 0u) | ((d.vb >> w) & 1u ? 0xff00u : 0u);
+      const unsigned ld = ((d.bad >> w) & 1u ? 0x00ffu : 0u) |
+                          ((d.bad >> (kPairWarps + w)) & 1u ? 0xff00u : 0u);
       if (w < d.n && ld) {
         const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
         const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
