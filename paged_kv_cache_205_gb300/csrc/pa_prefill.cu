@@ -121,6 +121,24 @@ __device__ __forceinline__ float p_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Packed two-lane fp32 add.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int c0, int c1,
                                             int c2, uint64_t *bar) {
   asm volatile(
@@ -553,11 +571,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           for (int c = 0; c < kChunk; ++c)
             if (!((c <= lim) && ((pm >> (c / BT)) & 1))) v[c] = 0xff800000u;
         }
+        // row maximum: 8 chains of three-input maxima over keys q, q+8, ..
         float mx8[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) mx8[q] = p_neg_inf();
 #pragma unroll
-        for (int c = 0; c < kChunk; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(v[c]));
+        for (int c = 0; c < kChunk; c += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            mx8[q] = fmax3(mx8[q], __uint_as_float(v[c + q]), __uint_as_float(v[c + 8 + q]));
         const float mc = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.qscale;
         const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
@@ -600,7 +622,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
             const float2 x = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
                                   qs2, nb2);
             const float e0 = p_exp2(x.x), e1 = p_exp2(x.y);
-            ls[q] = make_float2(ls[q].x + e0, ls[q].y + e1);
+            ls[q] = add2(ls[q], make_float2(e0, e1));
             pw[c >> 1] = float2_to_bf16x2(e0, e1);
           }
         }
