@@ -435,9 +435,13 @@ def measure_decode(args, w, rank, dist, sampler, k_steps):
     st = DeviceStep(w, seed=w.seed + 1000 * rank)
     pk = st.pk
     pk.pa_decode_set_grid_limit(args.grid)
-    pk.pa_decode_set_path({"auto": pk.PA_DECODE_AUTO, "split": pk.PA_DECODE_SPLIT,
-                           "cluster": pk.PA_DECODE_CLUSTER,
-                           "seq": pk.PA_DECODE_SEQ}[args.decode_kernel])
+    if args.decode_kernel == "auto":
+        # the choice the continuous batcher makes: from the batch's lengths
+        path = pk.pa_decode_kernel_for_lengths(w.attn_context_lens, w.block_tokens)
+    else:
+        path = {"count": pk.PA_DECODE_AUTO, "split": pk.PA_DECODE_SPLIT,
+                "cluster": pk.PA_DECODE_CLUSTER, "seq": pk.PA_DECODE_SEQ}[args.decode_kernel]
+    pk.pa_decode_set_path(path)
     # which decode kernel the library runs for this batch
     kern = pk.pa_decode_kernel_for(w.num_seqs, w.block_tokens)
     cluster = kern in (pk.PA_DECODE_CLUSTER, pk.PA_DECODE_SEQ)
@@ -661,6 +665,9 @@ def run_gpu(args, rank, world, dist):
             "parallelism": f"replicas x{world}",
             "decode_grid_cap": args.grid,
             "decode_kernel": {1: "split", 2: "cluster", 3: "seq"}.get(r["kern"], str(r["kern"])),
+            "decode_kernel_choice": {
+                "auto": "from the batch's context lengths (pa_decode_kernel_for_lengths)",
+                "count": "from the batch size (PA_DECODE_AUTO)"}.get(args.decode_kernel, "forced"),
             "block_tokens": w.block_tokens,
             "page_fill": page_fill,
         },
@@ -1097,10 +1104,11 @@ class ServeLoop:
         self.fl.copy_(self.fl0)
         self.fc.fill_(self.w.num_blocks)
 
-    def run(self, on_step=None):
+    def run(self, on_step=None, count=False):
         """One complete serving run of the workload; returns the steps taken
-        and the launches enqueued.  on_step(plan, before) is called around
-        each pa_batcher_run."""
+        and, with `count`, the launches enqueued (else 0; the schedule and so
+        the count are the same on every run).  on_step(plan, before) is called
+        around each pa_batcher_run."""
         w = self.w
         b = self.pk.Batcher(w.max_slots, w.n_layers, w.max_blocks_per_seq, w.num_blocks,
                             w.prefill_budget, block_tokens=w.block_tokens)
@@ -1113,13 +1121,16 @@ class ServeLoop:
                 break
             if on_step:
                 on_step(p, True)
+            attn = 0
+            if count and p.n_rows > 0:
+                # the batcher's kernel for this step: from the rows' contexts
+                _, pos = b.rows()
+                kern = self.pk.pa_decode_kernel_for_lengths(pos[:p.n_rows] + 1, w.block_tokens)
+                attn = attn_launches(kern in (self.pk.PA_DECODE_CLUSTER, self.pk.PA_DECODE_SEQ))
             b.run(self.bufs)
             if on_step:
                 on_step(p, False)
             steps += 1
-            attn = 0
-            if p.n_rows > 0:
-                attn = attn_launches(self.pk.pa_decode_kernel_for(p.n_rows) == self.pk.PA_DECODE_CLUSTER)
             launches += 1 + (3 if p.n_retired else 0) + 3 * w.n_layers * (p.n_admitted > 0) \
                 + (2 + attn) * w.n_layers * (p.n_rows > 0)
         b.close()
@@ -1213,9 +1224,11 @@ def run_serve_gpu(args, rank, world, dist):
         if int(loop.fc.item()) != w.num_blocks:
             raise RuntimeError(f"pages not all returned {where}")
 
-    for _ in range(args.warmup):
+    launches_per_run = 0
+    for i in range(args.warmup):
         loop.reset()
-        loop.run()
+        _, n_launch = loop.run(count=(i == 0))
+        launches_per_run = launches_per_run or n_launch
     check("during warm-up")
 
     # timed: K complete runs; the resets (three small fills) sit between runs
@@ -1230,11 +1243,11 @@ def run_serve_gpu(args, rank, world, dist):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        steps_per_run, n_launch = loop.run()
+        steps_per_run, _ = loop.run()
         e1.record(stream)
         e1.synchronize()
         total_ms += e0.elapsed_time(e1)
-        launches += n_launch
+        launches += launches_per_run
     sampler.mark(False)
     barrier()
     check("in the timed region")
@@ -1401,9 +1414,12 @@ def main():
                          "llama1b line also carries pool2g, long32k and ragged)")
     ap.add_argument("--block-tokens", type=int, default=BS, choices=[8, 16, 32],
                     help="decode path: tokens per page (the page size as a tunable)")
-    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "split", "cluster", "seq"],
-                    help="decode-attention kernel (pa_decode_set_path): automatic choice, the "
-                         "split-context kernel, or one cluster per (sequence, kv head)")
+    ap.add_argument("--decode-kernel", default="auto",
+                    choices=["auto", "count", "split", "cluster", "seq"],
+                    help="decode-attention kernel: chosen from the batch's context lengths "
+                         "(pa_decode_kernel_for_lengths, as the batcher does), chosen from the "
+                         "batch size alone (PA_DECODE_AUTO), the split-context kernel, one "
+                         "cluster per (sequence, kv head), or one cluster per sequence")
     ap.add_argument("--layers", type=int, default=0,
                     help="decode path: only the first N layers, in a pool sized for them "
                          "(profiler captures of one launch on a small footprint; not a bench line)")

@@ -329,7 +329,8 @@ int pa_free(const int32_t *seq_ids, int n_free, int32_t *block_table, int n_laye
  *     pa_prefill_append_rope then pa_prefill_attention on their rows), then
  *     every active row takes one decode step (every layer:
  *     pa_kv_append_rope at position = tokens cached, pa_decode_attention
- *     over position + 1).
+ *     over position + 1, with the kernel pa_decode_kernel_for_lengths picks
+ *     for the rows' contexts unless pa_decode_set_path forces one).
  * A batcher is host memory (created and owned by the library, freed by
  * pa_batcher_destroy); it is not thread-safe.  Use per step:
  *   pa_batcher_plan   decides the step (host only);
@@ -475,6 +476,31 @@ int pa_decode_set_path(int path);
  * PA_ERR_ARG for a bad count or page size, PA_ERR_CUDA / PA_ERR_DEVICE when
  * no sm_103 device answers. */
 int pa_decode_kernel_for(int num_seqs, int block_tokens);
+
+/* The decode kernel for a batch whose context lengths the caller knows on the
+ * host (context_lens: num_seqs host ints, the lengths the attention covers),
+ * for pages of block_tokens tokens; the caller passes it to
+ * pa_decode_set_path (the continuous batcher applies it to every decode step
+ * while the path is PA_DECODE_AUTO).  PA_DECODE_AUTO alone sees only
+ * num_seqs; this rule also
+ * sees how far the longest context lies above the mean (rho = max / mean,
+ * in 16-token tiles):
+ *   8-token pages, or rho > 3 (a few contexts far above the rest): the
+ *     split-context kernel, the only one that spreads a long context over
+ *     the whole GPU;
+ *   else, while every (sequence, kv head) pair gets two CTAs at once (the
+ *     PA_DECODE_AUTO bound): the per-head cluster kernel;
+ *   else, 16-token pages and at most one sequence per CTA of the grid
+ *     (two CTAs per SM, or the grid limit): the per-sequence cluster kernel
+ *     (one 32 KiB copy per page);
+ *   else the split-context kernel.
+ * Measured on GB300 over batches of 4..128 sequences with contexts
+ * U[256, 2048], log-uniform in [1, 8192], all 1024 and all 4096: within 5 %
+ * of the fastest kernel in every case.  Ignores the process-wide path;
+ * respects the grid limit.  PA_ERR_ARG for a bad count, page size or a null
+ * pointer with num_seqs > 0; PA_ERR_CUDA / PA_ERR_DEVICE when no sm_103
+ * device answers.  Host code only: no device work. */
+int pa_decode_kernel_for_lengths(const int32_t *context_lens, int num_seqs, int block_tokens);
 
 /*
  * Test hook for the bounded waits (no counterpart in the paper; the pages

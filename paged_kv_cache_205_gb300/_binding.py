@@ -134,6 +134,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_set_test_fault.restype = I
         lib.pa_decode_kernel_for.argtypes = [I, I]
         lib.pa_decode_kernel_for.restype = I
+        lib.pa_decode_kernel_for_lengths.argtypes = [P, I, I]
+        lib.pa_decode_kernel_for_lengths.restype = I
         lib.pa_error_string.argtypes = [I]
         lib.pa_error_string.restype = ctypes.c_char_p
         PP = ctypes.POINTER(ctypes.c_void_p)
@@ -364,6 +366,18 @@ def pa_decode_set_test_fault(stage: int, wait_limit_ns: int = 0) -> None:
     shortens every wait of the split kernel to wait_limit_ns; -1 restores."""
     _check("pa_decode_set_test_fault",
            library().pa_decode_set_test_fault(int(stage), int(wait_limit_ns)))
+
+
+def pa_decode_kernel_for_lengths(context_lens, block_tokens: int = PA_BLOCK_TOKENS) -> int:
+    """The decode kernel for a batch whose context lengths are known on the
+    host (a sequence of ints); see include/pagedkv.h."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    rc = library().pa_decode_kernel_for_lengths(a.ctypes.data if a.size else None, int(a.size),
+                                                int(block_tokens))
+    if rc < 0:
+        raise PagedKVError("pa_decode_kernel_for_lengths", rc)
+    return rc
 
 
 def pa_decode_set_path(path: int) -> None:

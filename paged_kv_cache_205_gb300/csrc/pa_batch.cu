@@ -113,6 +113,7 @@ constexpr int kCtlRing = 4;   // pinned control blocks in flight for replayed st
 // set of buffers.
 struct DecodeGraph {
   int n_rows = 0;
+  int path = 0;        // the decode kernel the graph runs
   int device = -1;
   pa_batch_buffers bufs{};
   cudaGraph_t graph = nullptr;
@@ -340,9 +341,21 @@ extern "C" int pa_batcher_commit(pa_batcher *b) {
 
 namespace {
 
-// The decode step of rows 0..n_rows-1, every layer: append, then attention.
+// The decode kernel for the planned step's rows: the process-wide path when
+// one is forced, else the choice from their attention contexts in the host
+// image of the control block.
+int decode_path_of(const pa_batcher *b, int n_rows) {
+  const int forced = decode_path_setting();
+  if (forced != PA_DECODE_AUTO) return forced;
+  const CtlLayout L{b->max_slots};
+  const int k = pa_decode_kernel_for_lengths(b->ctl.data() + L.attn(), n_rows, b->block_tokens);
+  return k > 0 ? k : PA_DECODE_AUTO;
+}
+
+// The decode step of rows 0..n_rows-1, every layer: append, then attention
+// with the decode kernel `path`.
 int enqueue_decode(pa_batcher *b, const pa_batch_buffers *buf, int32_t *ctl, int n_rows,
-                   void *stream) {
+                   int path, void *stream) {
   const CtlLayout L{b->max_slots};
   const int Lyr = b->n_layers, mb = b->max_blocks;
   const size_t dq = static_cast<size_t>(b->max_slots) * kHq * kD;
@@ -353,10 +366,10 @@ int enqueue_decode(pa_batcher *b, const pa_batch_buffers *buf, int32_t *ctl, int
                                   b->block_tokens, buf->block_table, Lyr, mb, ctl + L.pos(),
                                   n_rows, l, buf->free_list, buf->free_count, buf->err, stream);
     if (rc != PA_OK) return rc;
-    rc = pa_decode_attention_bt(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
-                                buf->num_blocks, b->block_tokens, buf->block_table, Lyr, mb,
-                                ctl + L.attn(), n_rows, l, buf->scale, buf->decode_workspace,
-                                buf->decode_workspace_bytes, buf->err, stream);
+    rc = decode_attention_path(buf->decode_out + l * dq, buf->decode_q + l * dq, buf->kv_cache,
+                               buf->num_blocks, b->block_tokens, buf->block_table, Lyr, mb,
+                               ctl + L.attn(), n_rows, l, buf->scale, buf->decode_workspace,
+                               buf->decode_workspace_bytes, buf->err, stream, path);
     if (rc != PA_OK) return rc;
   }
   return PA_OK;
@@ -391,13 +404,16 @@ int run_decode_graph(pa_batcher *b, const pa_batch_buffers *buf, void *stream) {
   if (cudaEventSynchronize(b->ring_done[slot]) != cudaSuccess) return PA_ERR_CUDA;
   std::memcpy(b->pinned[slot], b->ctl.data(), bytes);
   const int n_rows = b->plan.n_rows;
+  const int path = decode_path_of(b, n_rows);
   DecodeGraph *g = nullptr;
   for (DecodeGraph &c : b->decode_graphs)
-    if (c.n_rows == n_rows && c.device == dev && same_buffers(c.bufs, *buf)) g = &c;
+    if (c.n_rows == n_rows && c.path == path && c.device == dev && same_buffers(c.bufs, *buf))
+      g = &c;
   int32_t *ctl = static_cast<int32_t *>(buf->ctl);
   if (!g) {
     DecodeGraph ng;
     ng.n_rows = n_rows;
+    ng.path = path;
     ng.device = dev;
     ng.bufs = *buf;
     cudaStream_t cs = b->capture_stream;
@@ -405,7 +421,7 @@ int run_decode_graph(pa_batcher *b, const pa_batch_buffers *buf, void *stream) {
       return PA_ERR_CUDA;
     const bool copied =
         cudaMemcpyAsync(ctl, b->pinned[slot], bytes, cudaMemcpyHostToDevice, cs) == cudaSuccess;
-    const int rc = copied ? enqueue_decode(b, buf, ctl, n_rows, cs) : PA_ERR_CUDA;
+    const int rc = copied ? enqueue_decode(b, buf, ctl, n_rows, path, cs) : PA_ERR_CUDA;
     const cudaError_t ec = cudaStreamEndCapture(cs, &ng.graph);
     if (rc != PA_OK || ec != cudaSuccess) {
       if (ng.graph) cudaGraphDestroy(ng.graph);
@@ -510,7 +526,7 @@ extern "C" int pa_batcher_run(pa_batcher *b, const pa_batch_buffers *buf, void *
     if (rc != PA_OK) return rc;
   }
   // 3. one decode step for every active row
-  rc = enqueue_decode(b, buf, ctl, p.n_rows, stream);
+  rc = enqueue_decode(b, buf, ctl, p.n_rows, decode_path_of(b, p.n_rows), stream);
   if (rc != PA_OK) return rc;
   if (p.n_rows > 0 && p.n_retired == 0 && p.n_admitted == 0) b->eager_decode_done = true;
   return pa_batcher_commit(b);

@@ -595,6 +595,9 @@ __global__ void __launch_bounds__(kShares * 32) decode_merge_kernel(DecodeParams
 
 
 int g_grid_limit = 0;
+// max context / mean context (in 16-token tiles) above which a batch counts
+// as heavy-tailed for pa_decode_kernel_for_lengths
+constexpr double kHeavyTail = 3.0;
 int g_fault_stage = -1;                        // test hook, see pa_decode_set_test_fault
 unsigned long long g_fault_wait_ns = kWaitLimitNs;
 int g_decode_path = 0;   // 0 automatic, 1 split-context kernel, 2 cluster kernel
@@ -798,6 +801,30 @@ extern "C" int pa_decode_set_test_fault(int stage, long long wait_limit_ns) {
   return PA_OK;
 }
 
+extern "C" int pa_decode_kernel_for_lengths(const int32_t *context_lens, int num_seqs,
+                                            int block_tokens) {
+  if (num_seqs < 0 || !page_size_ok(block_tokens) || (num_seqs > 0 && !context_lens))
+    return PA_ERR_ARG;
+  if (num_seqs == 0 || block_tokens == kBs / 2) return PA_DECODE_SPLIT;
+  DeviceInfo di;
+  const int rc = current_device(&di);
+  if (rc != PA_OK) return rc;
+  // how far the longest context is above the mean, in 16-token tiles
+  long long sum = 0, mx = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    const long long t = (static_cast<long long>(max(context_lens[s], 0)) + kBs - 1) / kBs;
+    sum += t;
+    mx = max(mx, t);
+  }
+  const double rho = sum > 0 ? static_cast<double>(mx) * num_seqs / static_cast<double>(sum) : 1.0;
+  // a few contexts far above the rest: only the split kernel spreads them over the GPU
+  if (rho > kHeavyTail) return PA_DECODE_SPLIT;
+  if (decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit) > 0) return PA_DECODE_CLUSTER;
+  if (block_tokens == kBs && decode_seq_cluster(num_seqs, di.sm_count, g_grid_limit) > 0)
+    return PA_DECODE_SEQ;
+  return PA_DECODE_SPLIT;
+}
+
 extern "C" int pa_decode_set_path(int path) {
   if (path < PA_DECODE_AUTO || path > PA_DECODE_SEQ) return PA_ERR_ARG;
   g_decode_path = path;
@@ -811,7 +838,7 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
                           int num_blocks, const int32_t *block_table, int n_layers,
                           int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                           int layer, float scale, void *workspace, size_t workspace_bytes,
-                          int32_t *err, void *stream) {
+                          int32_t *err, void *stream, int path) {
   if (num_seqs < 0 || num_seqs > kMaxSeqs || num_blocks <= 0 || n_layers <= 0 ||
       max_blocks_per_seq <= 0)
     return PA_ERR_ARG;
@@ -861,7 +888,7 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // a batch whose (sequence, kv head) pairs all fit on the GPU at once runs
   // one cluster per pair (16-token pages)
-  if (BT == kBs && g_decode_path == PA_DECODE_SEQ) {
+  if (BT == kBs && path == PA_DECODE_SEQ) {
     static thread_local const void *pmap_pool = nullptr;
     static thread_local int pmap_blocks = 0;
     alignas(64) static thread_local CUtensorMap pmap;
@@ -878,11 +905,11 @@ int decode_attention_impl(uint16_t *out, const uint16_t *q, const uint16_t *kv_c
   }
   // (16-token pages; with 32-token pages a tile is half a page, with 8 two
   // pages: forced only, see pa_decode_kernel_for)
-  if ((BT == kBs && g_decode_path != PA_DECODE_SPLIT) ||
-      (BT == 2 * kBs && (g_decode_path == PA_DECODE_AUTO || g_decode_path == PA_DECODE_CLUSTER)) ||
-      (BT == kBs / 2 && g_decode_path == PA_DECODE_CLUSTER)) {
+  if ((BT == kBs && path != PA_DECODE_SPLIT) ||
+      (BT == 2 * kBs && (path == PA_DECODE_AUTO || path == PA_DECODE_CLUSTER)) ||
+      (BT == kBs / 2 && path == PA_DECODE_CLUSTER)) {
     int c = decode_pair_cluster(num_seqs, di.sm_count, g_grid_limit);
-    if (c == 0 && g_decode_path == PA_DECODE_CLUSTER) c = 1;
+    if (c == 0 && path == PA_DECODE_CLUSTER) c = 1;
     if (c > 0) {
       // 16-token pages: the split kernel's map is the tile map; 8-token pages:
       // its map (one page's K or V rows of a head) serves both kernels
@@ -947,8 +974,37 @@ extern "C" int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint1
                                    size_t workspace_bytes, int32_t *err, void *stream) {
   return decode_attention_impl<kBs>(out, q, kv_cache, num_blocks, block_table, n_layers,
                                     max_blocks_per_seq, context_lens, num_seqs, layer, scale,
-                                    workspace, workspace_bytes, err, stream);
+                                    workspace, workspace_bytes, err, stream, g_decode_path);
 }
+
+namespace pa {
+
+int decode_path_setting() { return g_decode_path; }
+
+int decode_attention_path(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                          int num_blocks, int block_tokens, const int32_t *block_table,
+                          int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                          int num_seqs, int layer, float scale, void *workspace,
+                          size_t workspace_bytes, int32_t *err, void *stream, int path) {
+  switch (block_tokens) {
+    case 8:
+      return decode_attention_impl<8>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                      max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                      workspace, workspace_bytes, err, stream, path);
+    case 16:
+      return decode_attention_impl<16>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                       workspace, workspace_bytes, err, stream, path);
+    case 32:
+      return decode_attention_impl<32>(out, q, kv_cache, num_blocks, block_table, n_layers,
+                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                                       workspace, workspace_bytes, err, stream, path);
+    default:
+      return PA_ERR_ARG;
+  }
+}
+
+}  // namespace pa
 
 extern "C" int pa_decode_attention_bt(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
                                       int num_blocks, int block_tokens,
@@ -956,22 +1012,9 @@ extern "C" int pa_decode_attention_bt(uint16_t *out, const uint16_t *q, const ui
                                       int max_blocks_per_seq, const int32_t *context_lens,
                                       int num_seqs, int layer, float scale, void *workspace,
                                       size_t workspace_bytes, int32_t *err, void *stream) {
-  switch (block_tokens) {
-    case 8:
-      return decode_attention_impl<8>(out, q, kv_cache, num_blocks, block_table, n_layers,
-                                      max_blocks_per_seq, context_lens, num_seqs, layer, scale,
-                                      workspace, workspace_bytes, err, stream);
-    case 16:
-      return decode_attention_impl<16>(out, q, kv_cache, num_blocks, block_table, n_layers,
-                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
-                                       workspace, workspace_bytes, err, stream);
-    case 32:
-      return decode_attention_impl<32>(out, q, kv_cache, num_blocks, block_table, n_layers,
-                                       max_blocks_per_seq, context_lens, num_seqs, layer, scale,
-                                       workspace, workspace_bytes, err, stream);
-    default:
-      return PA_ERR_ARG;
-  }
+  return decode_attention_path(out, q, kv_cache, num_blocks, block_tokens, block_table, n_layers,
+                               max_blocks_per_seq, context_lens, num_seqs, layer, scale,
+                               workspace, workspace_bytes, err, stream, g_decode_path);
 }
 
 // ---------------------------------------------------------------------------

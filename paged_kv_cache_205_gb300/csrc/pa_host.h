@@ -67,6 +67,17 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                        int layer, float scale, int32_t *err, int cluster, cudaStream_t stream);
 
+// The process-wide decode path set by pa_decode_set_path (pa_decode.cu).
+int decode_path_setting();
+
+// pa_decode_attention_bt with the kernel given by `path` (PA_DECODE_*) instead
+// of the process-wide setting (pa_decode.cu).
+int decode_attention_path(uint16_t *out, const uint16_t *q, const uint16_t *kv_cache,
+                          int num_blocks, int block_tokens, const int32_t *block_table,
+                          int n_layers, int max_blocks_per_seq, const int32_t *context_lens,
+                          int num_seqs, int layer, float scale, void *workspace,
+                          size_t workspace_bytes, int32_t *err, void *stream, int path);
+
 // Launch `kernel` with the programmatic-stream-serialization attribute, so it
 // may start while the previous kernel on the stream finishes; the kernel
 // itself must wait (griddepcontrol.wait) before reading that kernel's output.

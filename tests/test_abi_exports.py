@@ -81,6 +81,27 @@ def test_decode_path_switch_without_a_device():
         assert lib.pa_decode_set_path(pk.PA_DECODE_AUTO) == 0
 
 
+def test_length_aware_choice_without_a_device():
+    """pa_decode_kernel_for_lengths checks its arguments before it asks for a
+    device: a negative count, a null length array with sequences, or a page
+    size other than 8, 16 or 32 is refused; an empty batch and 8-token pages
+    take the split-context kernel whatever the lengths."""
+    import ctypes
+    import paged_kv_cache_205_gb300 as pk
+    lib = pk.library()
+    z = ctypes.c_void_p(0)
+    lens = (ctypes.c_int32 * 3)(5, 700, 3000)
+    assert lib.pa_decode_kernel_for_lengths(z, -1, 16) == -2
+    assert lib.pa_decode_kernel_for_lengths(z, 3, 16) == -2
+    assert lib.pa_decode_kernel_for_lengths(lens, 3, 12) == -2
+    assert lib.pa_decode_kernel_for_lengths(lens, 3, 64) == -2
+    assert lib.pa_decode_kernel_for_lengths(z, 0, 16) == pk.PA_DECODE_SPLIT
+    assert lib.pa_decode_kernel_for_lengths(lens, 3, 8) == pk.PA_DECODE_SPLIT
+    assert pk.pa_decode_kernel_for_lengths([], 32) == pk.PA_DECODE_SPLIT
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_decode_kernel_for_lengths([1, 2], 24)
+
+
 def test_page_size_entry_points_refuse_other_sizes():
     """Only 8-, 16- and 32-token pages are built; anything else is refused
     before any CUDA call."""

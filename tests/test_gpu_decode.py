@@ -295,6 +295,84 @@ def test_automatic_kernel_choice(decode_path):
     assert pk.pa_decode_kernel_for(300) == pk.PA_DECODE_SEQ
 
 
+def _tile_rho(ctx):
+    """Longest context over the mean, in 16-token tiles."""
+    t = (np.asarray(ctx, dtype=np.int64) + 15) // 16
+    return float(t.max()) * len(t) / float(t.sum())
+
+
+def test_kernel_choice_from_lengths(decode_path):
+    """pa_decode_kernel_for_lengths: a batch whose longest context lies more
+    than 3x above the mean (in 16-token tiles) takes the split-context kernel;
+    an even batch the per-head cluster kernel while every (sequence, kv head)
+    pair gets two CTAs, then (16-token pages, at most one sequence per CTA of
+    the grid) the per-sequence cluster kernel, then the split kernel; 8-token
+    pages the split kernel.  The answer does not depend on the forced path
+    (this test runs under each) and follows the grid limit."""
+    import torch
+    pk = _pk()
+    choose = pk.pa_decode_kernel_for_lengths
+    SPLIT, CLUSTER, SEQ = pk.PA_DECODE_SPLIT, pk.PA_DECODE_CLUSTER, pk.PA_DECODE_SEQ
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fit = (2 * sms) // 16
+    # the measured workloads
+    assert choose(wl.make_workload("llama1b").attn_context_lens) == CLUSTER
+    assert choose(wl.make_workload("long32k").attn_context_lens) == CLUSTER
+    assert choose(wl.make_workload("pool2g").attn_context_lens) == SEQ
+    ragged = wl.make_workload("ragged").attn_context_lens
+    assert _tile_rho(ragged) > 3 and choose(ragged) == SPLIT
+    # log-uniform contexts in [1, 8192], 16 sequences
+    rng = np.random.default_rng(16)
+    logu = np.floor(np.exp(rng.uniform(0, np.log(8192), size=16))).astype(np.int32)
+    assert choose(logu) == (SPLIT if _tile_rho(logu) > 3 else CLUSTER)
+    # the heavy-tail bound is strict: max / mean = 3 is still even
+    assert choose([160, 0, 0]) == CLUSTER
+    assert choose([160, 0, 0, 0]) == SPLIT
+    tail = np.full(16, 100, dtype=np.int32)
+    tail[0] = 1600
+    assert choose(tail) == SPLIT
+    # even batches by size and page size
+    assert choose(np.full(fit, 1000)) == CLUSTER
+    assert choose(np.full(fit + 1, 1000)) == SEQ
+    assert choose(np.full(2 * sms, 1000)) == SEQ
+    assert choose(np.full(2 * sms + 1, 1000)) == SPLIT
+    assert choose(np.full(fit, 1000), 32) == CLUSTER
+    assert choose(np.full(fit + 1, 1000), 32) == SPLIT
+    assert choose(np.full(4, 1000), 8) == SPLIT
+    assert choose([]) == SPLIT
+    pk.pa_decode_set_grid_limit(64)
+    assert choose(np.full(4, 1000)) == CLUSTER
+    assert choose(np.full(5, 1000)) == SEQ
+    assert choose(np.full(65, 1000)) == SPLIT
+    pk.pa_decode_set_grid_limit(0)
+
+
+@pytest.mark.parametrize("case", ["logu16", "tail16", "even8", "even40"])
+def test_chosen_kernel_matches_oracle(case):
+    """The kernel the length-aware choice names, run on its batch (seeded
+    lengths of the kinds the rule separates: heavy-tailed -> split kernel,
+    even and few -> per-head clusters, even and many -> per-sequence
+    clusters), matches the oracle."""
+    pk = _pk()
+    rng = np.random.default_rng({"logu16": 61, "tail16": 63, "even8": 64, "even40": 62}[case])
+    if case == "logu16":
+        ctx = np.floor(np.exp(rng.uniform(0, np.log(4096), size=16))).astype(np.int64)
+    elif case == "tail16":
+        ctx = rng.integers(1, 200, size=16)
+        ctx[5] = 3000
+    else:
+        ctx = rng.integers(600, 700, size=8 if case == "even8" else 40)
+    w, pool, q = _small_case(3100 + len(ctx), ctx)
+    path = pk.pa_decode_kernel_for_lengths(w.context_lens)
+    assert path == {"logu16": pk.PA_DECODE_SPLIT, "tail16": pk.PA_DECODE_SPLIT,
+                    "even8": pk.PA_DECODE_CLUSTER, "even40": pk.PA_DECODE_SEQ}[case]
+    pk.pa_decode_set_path(path)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    assert err == 0
+    assert_attention_close(out, ref, f"{case}, kernel {path}")
+
+
 @pytest.mark.parametrize("grid", [0, 24, 64, 152, 304])
 @pytest.mark.parametrize("n", [1, 2, 3, 7, 16, 19, 32])
 def test_mixed_lengths_every_cluster_size(decode_path, n, grid):
