@@ -55,7 +55,10 @@ constexpr int kHalves = 2;
 constexpr int kCtaTok = kQTok * kHalves;      // query tokens per CTA
 constexpr int kRows = kQTok * kGqa;           // 128 MMA rows per half
 constexpr int kChunk = 128;                   // keys per chunk (8 pages of 16 tokens)
-constexpr int kStagesP = 5;
+constexpr int kStagesP = 4;
+constexpr int kQBufs = 2;                     // Q tiles in flight: the next item's loads early
+constexpr int kSortTiles = 4096;              // tiles ordered by weight; beyond, by index
+constexpr int kWeightBins = 512;              // weight classes (see tile_bin)
 constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -93,12 +96,14 @@ struct PrefillParams {
 };
 
 struct __align__(1024) PSmem {
-  unsigned char q[kHalves][kOperandBytes];         // per half [32 tok][4 heads][64], swizzled
+  unsigned char q[kQBufs][kHalves][kOperandBytes]; // per half [32 tok][4 heads][64], swizzled
   unsigned char k[kStagesP][kOperandBytes];        // [128 keys][64]
   unsigned char v[kStagesP][kOperandBytes];        // [128 keys][64]
   int tile_prefix[kMaxSeqsP + 1];
-  uint64_t q_full;
-  uint64_t q_empty;
+  int bin_start[kWeightBins];                      // counting sort of the tiles by weight
+  uint16_t order[kSortTiles];                      // tiles, heaviest first
+  uint64_t q_full[kQBufs];
+  uint64_t q_empty[kQBufs];
   uint64_t kv_full[kStagesP];
   uint64_t kv_empty[kStagesP];
   uint64_t s_full[kHalves];
@@ -148,10 +153,14 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
-// A work item is (64-token query tile, kv head).  Items go heavy first (the
-// last tiles of a sequence see the most keys); CTA b takes items b, b + G,
-// b + 2G, ... of that order and keeps its pipeline running from one item into
-// the next.
+// A work item is (64-token query tile, kv head).  The tiles are ordered by
+// weight class (the weight: the 128-key chunks its two halves go through),
+// heaviest first, ties in tile order (a stable counting sort every CTA
+// computes alike); with more than kSortTiles tiles, by tile index from the
+// last (the last tiles of a sequence see the most keys).  The items of that order are dealt out in
+// rounds of G, every other round backwards (CTA b takes positions b,
+// 2G - 1 - b, 2G + b, ...), so that each CTA's sum of weights comes close to
+// the mean; a CTA keeps its pipeline running from one item into the next.
 struct Item {
   int g;                    // kv head
   int ctx, row0, t0;        // the tile's sequence: cached tokens, first row; tile start
@@ -162,17 +171,53 @@ struct Item {
   int s;
 };
 
-__device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams &p,
-                                            int total_tiles, int i) {
-  Item it;
-  const int t = total_tiles - 1 - i / kHkv;
-  it.g = i % kHkv;
-  int lo = 0, hi = p.num_seqs - 1;   // the sequence s with prefix[s] <= t < prefix[s+1]
+// The sequence s whose tiles hold tile t: prefix[s] <= t < prefix[s+1].
+__device__ __forceinline__ int tile_seq(const PSmem &sm, int num_seqs, int t) {
+  int lo = 0, hi = num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (sm.tile_prefix[mid] <= t) lo = mid;
     else hi = mid - 1;
   }
+  return lo;
+}
+
+// Sort bin of tile t: kWeightBins - 1 - the class of its weight w, so that
+// bins in ascending order hold the tiles heaviest first.  The class is w
+// itself below 16 and w's leading four bits with its exponent above (classes
+// at most 1/8 wide): a class then holds several tiles of one long sequence,
+// which stay in tile order, so the CTAs of one round share more K/V in L2.
+__device__ __forceinline__ int tile_bin(const PSmem &sm, const PrefillParams &p, int t) {
+  const int s = tile_seq(sm, p.num_seqs, t);
+  const long long t0 = static_cast<long long>(t - sm.tile_prefix[s]) * kCtaTok;
+  const long long ctx = p.context_lens[s];
+  const long long n = p.cu_tokens[s + 1] - p.cu_tokens[s];
+  const long long r0 = min(static_cast<long long>(kQTok), n - t0);
+  const long long r1 = min(static_cast<long long>(kQTok), n - t0 - kQTok);
+  long long w = (ctx + t0 + r0 + kChunk - 1) / kChunk;
+  if (r1 > 0) w += (ctx + t0 + kQTok + r1 + kChunk - 1) / kChunk;
+  w = max(w, 1LL);
+  const int e = 63 - __clzll(w);                        // w < 2^62: e <= 61
+  const int cls = e < 3 ? static_cast<int>(w) : 8 * (e - 3) + static_cast<int>(w >> (e - 3));
+  return kWeightBins - 1 - min(cls, kWeightBins - 1);
+}
+
+// Position in the work order of this CTA's k-th item, or -1 past the end.
+__device__ __forceinline__ int item_position(int k, int n_items) {
+  // the walks stop at the first position past the end, so pos <= n_items +
+  // 2 G, which the launch keeps below INT_MAX
+  const int G = gridDim.x, b = blockIdx.x;
+  const int pos = k * G + ((k & 1) ? G - 1 - b : b);
+  return pos < n_items ? pos : -1;
+}
+
+__device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams &p,
+                                            int total_tiles, bool sorted, int i) {
+  Item it;
+  const int rank = i / kHkv;
+  const int t = sorted ? static_cast<int>(sm.order[rank]) : total_tiles - 1 - rank;
+  it.g = i % kHkv;
+  const int lo = tile_seq(sm, p.num_seqs, t);
   it.s = lo;
   it.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
   it.ctx = p.context_lens[lo];
@@ -236,10 +281,10 @@ __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, 
 }
 
 // S of half h = Q_h K^T for chunk gc into the half's S columns (one thread).
-__device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int h, int gc,
+__device__ __forceinline__ void mma_issue_s(PSmem &sm, uint32_t tmem, int qb, int h, int gc,
                                             uint32_t id_s) {
   const uint32_t k_addr = smem_u32(sm.k[gc % kStagesP]);
-  const uint32_t q_addr = smem_u32(sm.q[h]);
+  const uint32_t q_addr = smem_u32(sm.q[qb][h]);
 #pragma unroll
   for (int ks = 0; ks < kD / 16; ++ks)
     tc::mma_bf16(tmem + h * kChunk, tc::sdesc_sw128(q_addr + 32 * ks, 16, 1024),
@@ -272,8 +317,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   if (tid == 0) {
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, kHalves);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_empty[b], kHalves);
+    }
     for (int st = 0; st < kStagesP; ++st) {
       mbar_init(&sm.kv_full[st], 1);
       mbar_init(&sm.kv_empty[st], kHalves);     // one release per MMA warp
@@ -336,6 +383,55 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   __syncthreads();
   if (static_cast<int>(blockIdx.x) >= n_items) return;
 
+  // ---- the tiles heaviest first: a stable counting sort by weight
+  const bool sorted = total_tiles <= kSortTiles;
+  if (sorted) {
+    for (int b = tid; b < kWeightBins; b += kPThreads) sm.bin_start[b] = 0;
+    __syncthreads();
+    for (int t = tid; t < total_tiles; t += kPThreads) atomicAdd(&sm.bin_start[tile_bin(sm, p, t)], 1);
+    __syncthreads();
+    if (warp == 0) {
+      // exclusive prefix sum over the bins (16 consecutive bins per lane)
+      constexpr int kPer = kWeightBins / 32;
+      int cnt[kPer];
+      int sum = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        cnt[e] = sm.bin_start[lane * kPer + e];
+        sum += cnt[e];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        sm.bin_start[lane * kPer + e] = run;
+        run += cnt[e];
+      }
+      __syncwarp();
+      // 32 tiles at a time in tile order: a tile's place is its bin's next
+      // free place plus the number of lower lanes with the same bin
+      for (int base = 0; base < total_tiles; base += 32) {
+        const int t = base + lane;
+        const int bn = t < total_tiles ? tile_bin(sm, p, t) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, bn);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int at = t < total_tiles ? sm.bin_start[bn] + rank : 0;
+        __syncwarp();
+        if (t < total_tiles) {
+          sm.order[at] = static_cast<uint16_t>(t);
+          if (rank == 0) sm.bin_start[bn] += __popc(peers);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
     tc::tmem_relinquish();
@@ -344,7 +440,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const int G = gridDim.x;
   if (warp >= 8) {
     // the producer/MMA warpgroup gives registers to the softmax warpgroups
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
@@ -364,20 +459,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       };
       int blk_next = -1;
       bool next_read = false;
-      for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
-        const Item it = decode_item(sm, p, total_tiles, i);
+      for (; ok; ++k) {
+        const int i = item_position(k, n_items);
+        if (i < 0) break;
+        const Item it = decode_item(sm, p, total_tiles, sorted, i);
         if (!next_read && it.n_chunks > 0) blk_next = chunk_ids(it, 0);
         next_read = false;
         int good = 1;
         if (lane == 0) {
-          // the previous item's Q has been read by all its MMAs
-          if (k > 0 && !mbar_wait(&sm.q_empty, (k - 1) & 1)) {
+          // Q buffer k % 2: the MMAs of the item before last have read it
+          const int qb = k % kQBufs;
+          if (k >= kQBufs && !mbar_wait(&sm.q_empty[qb], (k / kQBufs - 1) & 1)) {
             good = 0;
           } else {
-            mbar_arrive_expect_tx(&sm.q_full, it.halves * kOperandBytes);
+            mbar_arrive_expect_tx(&sm.q_full[qb], it.halves * kOperandBytes);
             for (int h = 0; h < it.halves; ++h)
-              tma_load_3d(sm.q[h], &q_map, 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok,
-                          &sm.q_full);
+              tma_load_3d(sm.q[qb][h], &q_map, 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok,
+                          &sm.q_full[qb]);
           }
         }
         ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -389,8 +487,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           const int blk = blk_next;
           if (j + 1 < it.n_chunks) {
             blk_next = chunk_ids(it, j + 1);
-          } else if (i + G < n_items) {
-            const Item nx = decode_item(sm, p, total_tiles, i + G);
+          } else if (item_position(k + 1, n_items) >= 0) {
+            const Item nx = decode_item(sm, p, total_tiles, sorted, item_position(k + 1, n_items));
             if (nx.n_chunks > 0) blk_next = chunk_ids(nx, 0);
             next_read = true;
           }
@@ -425,7 +523,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       if (lane == 0) {
         if (!ok) report(p.err, PA_DEV_TIMEOUT);
         // no copy may still be landing in shared memory when the CTA exits
-        if (k > 0 && !mbar_wait(&sm.q_full, (k - 1) & 1)) report(p.err, PA_DEV_TIMEOUT);
+        for (int kk = max(0, k - kQBufs); kk < k; ++kk)
+          if (!mbar_wait(&sm.q_full[kk % kQBufs], (kk / kQBufs) & 1)) report(p.err, PA_DEV_TIMEOUT);
         for (int st = 0; st < kStagesP; ++st)
           if ((issued >> st) & 1u)
             if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u))
@@ -445,21 +544,25 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       int n_s = 0;             // S chunks issued
       int n_started = 0;       // two-half items (half 1's warp)
       // S of chunk gcs once the softmax has read the previous S (lane 0)
+      int qb = 0;              // the item's Q buffer
       auto issue_s = [&](int gcs) -> bool {
         if (n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) return false;
         tc::fence_after_sync();
-        mma_issue_s(sm, tmem, h, gcs, id_s);
+        mma_issue_s(sm, tmem, qb, h, gcs, id_s);
         ++n_s;
         return true;
       };
-      for (int i = blockIdx.x; i < n_items && ok; i += G, ++k) {
-        const Item it = decode_item(sm, p, total_tiles, i);
+      for (; ok; ++k) {
+        const int i = item_position(k, n_items);
+        if (i < 0) break;
+        const Item it = decode_item(sm, p, total_tiles, sorted, i);
+        qb = k % kQBufs;
         const int nch = h == 0 ? it.nc0 : it.nc1;
         // half 1 sees every chunk of a two-half tile, half 0 every chunk of
         // a one-half tile: that half's warp zeroes, and with two halves hands
         // the chunks half 0 also reads over to it
         const bool zeroer = h == (it.halves == 2 ? 1 : 0);
-        if (lane == 0) ok = mbar_wait_short(&sm.q_full, k & 1) ? 1 : 0;
+        if (lane == 0) ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) ok = mma_prepare_chunk<BT>(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
         if (ok && nch > 0) {
@@ -507,7 +610,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[gc % kStagesP]);
           __syncwarp();
         }
-        if (ok && lane == 0) tc::mma_commit(&sm.q_empty);   // every MMA that reads Q is issued
+        if (ok && lane == 0) tc::mma_commit(&sm.q_empty[qb]);   // every MMA that reads Q is issued
         if (nch > 0) ++n_active;
       }
       if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
@@ -531,8 +634,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const uint32_t p_addr = lane_addr + kTmemP + h * (kChunk / 2);
     bool ok = true;
     int gc = 0, n_s = 0, n_o = 0;   // S chunks read; PV commits waited for
-    for (int i = blockIdx.x; i < n_items && ok; i += G) {
-      const Item it = decode_item(sm, p, total_tiles, i);
+    for (int k = 0; ok; ++k) {
+      const int i = item_position(k, n_items);
+      if (i < 0) break;
+      const Item it = decode_item(sm, p, total_tiles, sorted, i);
       const int rows = h == 0 ? it.rows0 : it.rows1;
       const int nch = h == 0 ? it.nc0 : it.nc1;
       if (nch == 0) {
@@ -765,8 +870,8 @@ int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
   // every sequence's chunk ends in at most one partial tile; one CTA per SM
   // works through the (tile, kv head) items
   const long long tiles = (static_cast<long long>(total_tokens) + kCtaTok - 1) / kCtaTok + num_seqs;
-  if (tiles * kHkv > INT_MAX) return PA_ERR_ARG;
   const int grid = static_cast<int>(min(static_cast<long long>(di.sm_count), tiles * kHkv));
+  if (tiles * kHkv + 2LL * grid > INT_MAX) return PA_ERR_ARG;   // item positions stay in int
   PrefillParams prm;
   prm.out = reinterpret_cast<__nv_bfloat16 *>(out);
   prm.cu_tokens = cu_tokens;

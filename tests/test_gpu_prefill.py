@@ -382,3 +382,60 @@ def test_bench_prefill_workload_sampled(name):
         assert e_ref == 0
         got = host_f64(out[layer][torch.from_numpy(rows).to(dev)])
         _close(got, ref, f"{name} layer {layer}")
+
+
+@pytest.mark.parametrize("tiles", [4096, 4097])
+def test_prefill_attention_at_and_past_the_sorted_tile_count(tiles):
+    """2048 prompts of 65..129 tokens: 4096 query tiles (the most the kernel
+    orders by weight) and 4097 (past it, the items go in tile order).  Every
+    output row is written (none stays NaN) and sampled rows of every length
+    match the oracle's attention over the same pages."""
+    import torch
+    from helpers import gather_for_oracle
+    n = 2048
+    lens = np.full(n, 65, dtype=np.int32)
+    lens[n // 2:] = 64 + (np.arange(n - n // 2) % 2)      # 1 or 2 tiles alternating in the tail
+    lens[: n // 2] = 65
+    extra = tiles - int(((lens + 63) // 64).sum())
+    assert 0 <= extra <= n
+    lens[:extra] = 129                                     # 3 tiles each
+    assert int(((lens + 63) // 64).sum()) == tiles
+    ctx = np.zeros(n, dtype=np.int32)
+    cu = _cu(lens)
+    T = int(cu[-1])
+    pages = (lens + BS - 1) // BS
+    mb = int(pages.max())
+    nb = int(pages.sum())
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(4000 + tiles)
+    pool = torch.randn((nb, 2, BS, N_KV, D), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((T, N_Q, D), generator=g, device=dev).to(torch.bfloat16)
+    bt = np.full((n, 1, mb), -1, dtype=np.int32)
+    perm = np.random.default_rng(tiles).permutation(nb).astype(np.int32)
+    start = np.concatenate([[0], np.cumsum(pages)])
+    for s in range(n):
+        bt[s, 0, :pages[s]] = perm[start[s]:start[s + 1]]
+    out = torch.full((T, N_Q, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _pk().pa_prefill_attention(out, q, dev_i32(cu), pool, dev_i32(bt), dev_i32(ctx), 0, SCALE,
+                               err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert bool(torch.isfinite(out.float()).all()), "rows left unwritten"
+    rng = np.random.default_rng(tiles + 1)
+    seqs = sorted({0, extra - 1 if extra else 1, n // 2, n - 2, n - 1,
+                   *rng.integers(n, size=6).tolist()})
+    sub, sub_bt = gather_for_oracle(pool, bt, seqs, lens, 0)
+    rows, pos, which = [], [], []
+    for i, s in enumerate(seqs):
+        for t in sorted({0, 31, 32, 63, int(lens[s]) - 1, int(rng.integers(lens[s]))}):
+            if t < lens[s]:
+                rows.append(int(cu[s]) + t)
+                pos.append(t)
+                which.append(i)
+    rows_t = torch.from_numpy(np.array(rows)).to(dev)
+    ref, e_ref = oracle.decode_attention(host_bits(q[rows_t]), sub, sub_bt[np.array(which)],
+                                         np.array(pos, dtype=np.int32) + 1, 0, SCALE)
+    assert e_ref == 0
+    _close(host_f64(out[rows_t]), ref, f"{tiles} tiles")
