@@ -58,7 +58,7 @@ constexpr int kChunk = 128;                   // keys per chunk (8 pages of 16 t
 constexpr int kStagesP = 4;
 constexpr int kQBufs = 2;                     // Q tiles in flight: the next item's loads early
 constexpr int kSortTiles = 4096;              // tiles ordered by weight; beyond, by index
-constexpr int kWeightBins = 512;              // weight classes (see tile_bin)
+constexpr int kWeightBins = 256;              // weight classes (see tile_bin)
 constexpr int kSoftThreads = kRows;           // one softmax warpgroup per half
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -102,6 +102,7 @@ struct __align__(1024) PSmem {
   int tile_prefix[kMaxSeqsP + 1];
   int bin_start[kWeightBins];                      // counting sort of the tiles by weight
   uint16_t order[kSortTiles];                      // tiles, heaviest first
+  uint8_t tile_bins[kSortTiles];                   // each tile's bin
   uint64_t q_full[kQBufs];
   uint64_t q_empty[kQBufs];
   uint64_t kv_full[kStagesP];
@@ -113,10 +114,13 @@ struct __align__(1024) PSmem {
   uint64_t o_free[kHalves];
   uint64_t v_zeroed[kStagesP];                     // zeroing warp -> the other half's MMA warp
   uint64_t h0_started;                             // half 0 has read an item's first S
+  uint64_t staged[kHalves];                        // the half's output rows are in shared memory
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
 };
+
+static_assert(sizeof(PSmem) + 1024 <= 227 * 1024, "shared memory above the per-CTA limit");
 
 __device__ __forceinline__ float p_neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -151,6 +155,28 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Shared -> global 3-D tiled tensor copy (TMA store) in the thread's bulk
+// async-group.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *smem_src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... and have completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // A work item is (64-token query tile, kv head).  The tiles are ordered by
@@ -190,8 +216,8 @@ __device__ __forceinline__ int tile_seq(const PSmem &sm, int num_seqs, int t) {
 __device__ __forceinline__ int tile_bin(const PSmem &sm, const PrefillParams &p, int t) {
   const int s = tile_seq(sm, p.num_seqs, t);
   const long long t0 = static_cast<long long>(t - sm.tile_prefix[s]) * kCtaTok;
-  const long long ctx = p.context_lens[s];
-  const long long n = p.cu_tokens[s + 1] - p.cu_tokens[s];
+  const long long ctx = __ldg(p.context_lens + s);
+  const long long n = __ldg(p.cu_tokens + s + 1) - __ldg(p.cu_tokens + s);
   const long long r0 = min(static_cast<long long>(kQTok), n - t0);
   const long long r1 = min(static_cast<long long>(kQTok), n - t0 - kQTok);
   long long w = (ctx + t0 + r0 + kChunk - 1) / kChunk;
@@ -220,9 +246,11 @@ __device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams
   const int lo = tile_seq(sm, p.num_seqs, t);
   it.s = lo;
   it.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
-  it.ctx = p.context_lens[lo];
-  it.row0 = p.cu_tokens[lo];
-  const int n = p.cu_tokens[lo + 1] - it.row0;
+  // (read-only for the kernel's lifetime: through the non-coherent path,
+  // which keeps them in L1 for the items that follow)
+  it.ctx = __ldg(p.context_lens + lo);
+  it.row0 = __ldg(p.cu_tokens + lo);
+  const int n = __ldg(p.cu_tokens + lo + 1) - it.row0;
   it.rows0 = min(kQTok, n - it.t0);
   it.rows1 = min(kQTok, n - it.t0 - kQTok);
   it.halves = it.rows1 > 0 ? 2 : 1;
@@ -309,7 +337,7 @@ __device__ __forceinline__ void mma_issue_pv(PSmem &sm, uint32_t tmem, int h, in
 template <int BT>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-    PrefillParams p) {
+    const __grid_constant__ CUtensorMap out_map, PrefillParams p) {
   extern __shared__ unsigned char smem_raw[];
   PSmem &sm = *reinterpret_cast<PSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -317,9 +345,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   if (tid == 0) {
     prefetch_tensormap(&kv_map);
     prefetch_tensormap(&q_map);
+    prefetch_tensormap(&out_map);
     for (int b = 0; b < kQBufs; ++b) {
       mbar_init(&sm.q_full[b], 1);
-      mbar_init(&sm.q_empty[b], kHalves);
+      // the MMA warps' commits and each softmax half once its output left
+      // the buffer (it stages the half's output tile there)
+      mbar_init(&sm.q_empty[b], 2 * kHalves);
     }
     for (int st = 0; st < kStagesP; ++st) {
       mbar_init(&sm.kv_full[st], 1);
@@ -334,6 +365,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.o_free[h], kSoftThreads);
     }
     mbar_init(&sm.h0_started, kSoftThreads);
+    for (int h = 0; h < kHalves; ++h) mbar_init(&sm.staged[h], kSoftThreads);
     fence_mbar_init();
   }
   pdl_launch_dependents();
@@ -388,7 +420,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
   if (sorted) {
     for (int b = tid; b < kWeightBins; b += kPThreads) sm.bin_start[b] = 0;
     __syncthreads();
-    for (int t = tid; t < total_tiles; t += kPThreads) atomicAdd(&sm.bin_start[tile_bin(sm, p, t)], 1);
+    for (int t = tid; t < total_tiles; t += kPThreads) {
+      const int bn = tile_bin(sm, p, t);
+      sm.tile_bins[t] = static_cast<uint8_t>(bn);
+      atomicAdd(&sm.bin_start[bn], 1);
+    }
     __syncthreads();
     if (warp == 0) {
       // exclusive prefix sum over the bins (16 consecutive bins per lane)
@@ -417,7 +453,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       // free place plus the number of lower lanes with the same bin
       for (int base = 0; base < total_tiles; base += 32) {
         const int t = base + lane;
-        const int bn = t < total_tiles ? tile_bin(sm, p, t) : -1;
+        const int bn = t < total_tiles ? static_cast<int>(sm.tile_bins[t]) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, bn);
         const int rank = __popc(peers & ((1u << lane) - 1u));
         const int at = t < total_tiles ? sm.bin_start[bn] + rank : 0;
@@ -634,13 +670,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     const uint32_t p_addr = lane_addr + kTmemP + h * (kChunk / 2);
     bool ok = true;
     int gc = 0, n_s = 0, n_o = 0;   // S chunks read; PV commits waited for
+    int n_staged = 0;               // output tiles staged
     for (int k = 0; ok; ++k) {
       const int i = item_position(k, n_items);
       if (i < 0) break;
       const Item it = decode_item(sm, p, total_tiles, sorted, i);
       const int rows = h == 0 ? it.rows0 : it.rows1;
       const int nch = h == 0 ? it.nc0 : it.nc1;
+      const int qb = k % kQBufs;
       if (nch == 0) {
+        // nothing staged: release the Q buffer, once it holds this item's Q
+        // (an earlier arrival would count for the item before last)
+        if (r == 0) {
+          ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1);
+          if (ok) mbar_arrive(&sm.q_empty[qb]);
+        }
         gc += it.n_chunks;
         continue;
       }
@@ -760,23 +804,49 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       mbar_arrive(&sm.o_free[h]);   // the next item's first PV may clear O
-      if (tok < rows) {
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            p.out + ((static_cast<size_t>(it.row0) + it.t0 + h * kQTok + tok) * kHq +
-                     it.g * kGqa + hh) * kD);
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      auto row_chunk = [&](int e) {
+        const float *f = reinterpret_cast<const float *>(&ov[8 * e]);
+        return make_uint4(float2_to_bf16x2(f[0] * inv, f[1] * inv),
+                          float2_to_bf16x2(f[2] * inv, f[3] * inv),
+                          float2_to_bf16x2(f[4] * inv, f[5] * inv),
+                          float2_to_bf16x2(f[6] * inv, f[7] * inv));
+      };
+      if (rows == kQTok) {
+        // a whole half tile: the rows go into the half's part of this item's
+        // Q buffer (no MMA reads it any more), in the layout of the output's
+        // tensor map (row r, 16-byte chunk e at e ^ (r mod 8)), and leave in
+        // one TMA store, whose writes are whole 128-byte lines
+        unsigned char *stg = sm.q[qb][h] + r * kTileRowBytes;
 #pragma unroll
-        for (int e = 0; e < kD / 8; ++e) {
-          const float *f = reinterpret_cast<const float *>(&ov[8 * e]);
-          dst[e] = make_uint4(float2_to_bf16x2(f[0] * inv, f[1] * inv),
-                              float2_to_bf16x2(f[2] * inv, f[3] * inv),
-                              float2_to_bf16x2(f[4] * inv, f[5] * inv),
-                              float2_to_bf16x2(f[6] * inv, f[7] * inv));
+        for (int e = 0; e < kD / 8; ++e)
+          *reinterpret_cast<uint4 *>(stg + ((e ^ (r & 7)) << 4)) = row_chunk(e);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.staged[h]);
+        if (r == 0) {
+          ok = mbar_wait_short(&sm.staged[h], n_staged & 1);
+          if (ok) {
+            tma_store_3d(&out_map, sm.q[qb][h], 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(&sm.q_empty[qb]);
+          }
         }
+        ++n_staged;
+      } else {
+        if (tok < rows) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              p.out + ((static_cast<size_t>(it.row0) + it.t0 + h * kQTok + tok) * kHq +
+                       it.g * kGqa + hh) * kD);
+#pragma unroll
+          for (int e = 0; e < kD / 8; ++e) dst[e] = row_chunk(e);
+        }
+        if (r == 0) mbar_arrive(&sm.q_empty[qb]);
       }
       gc += it.n_chunks;
     }
     if (!ok) report(p.err, PA_DEV_TIMEOUT);
+    if (r == 0) bulk_wait_group0();   // the output stores are complete
   }
   // every TMEM read and MMA is done (or given up on) before the columns go back
   tc::fence_before_sync();
@@ -858,6 +928,15 @@ int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
     map_pool = kv_cache;
     map_blocks = num_blocks;
   }
+  static thread_local const void *map_out = nullptr;
+  static thread_local int map_out_tokens = 0;
+  alignas(64) static thread_local CUtensorMap out_map;
+  if (map_out != out || map_out_tokens != total_tokens) {
+    rc = make_q_map(&out_map, out, total_tokens);   // out has q's layout
+    if (rc != PA_OK) return rc;
+    map_out = out;
+    map_out_tokens = total_tokens;
+  }
   static thread_local const void *map_q = nullptr;
   static thread_local int map_q_tokens = 0;
   alignas(64) static thread_local CUtensorMap q_map;
@@ -886,7 +965,8 @@ int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
   prm.total_tokens = total_tokens;
   prm.qscale = scale * kLog2eP;
   if (launch_pdl(prefill_attention_kernel<BT>, dim3(static_cast<unsigned>(grid)),
-                 dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, prm) !=
+                 dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, out_map,
+                 prm) !=
       cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
