@@ -494,9 +494,10 @@ int pa_decode_kernel_for(int num_seqs, int block_tokens);
  *     (two CTAs per SM, or the grid limit): the per-sequence cluster kernel
  *     (one 32 KiB copy per page);
  *   else the split-context kernel.
- * Measured on GB300 over batches of 4..128 sequences with contexts
+ * Measured on GB300 over 36 batches of 4..128 sequences with contexts
  * U[256, 2048], log-uniform in [1, 8192], all 1024 and all 4096: within 5 %
- * of the fastest kernel in every case.  Ignores the process-wide path;
+ * of the fastest kernel in 34 of them (the two others at 12 sequences: 5.0
+ * and 9 % above the per-sequence kernel).  Ignores the process-wide path;
  * respects the grid limit.  PA_ERR_ARG for a bad count, page size or a null
  * pointer with num_seqs > 0; PA_ERR_CUDA / PA_ERR_DEVICE when no sm_103
  * device answers.  Host code only: no device work. */
