@@ -70,13 +70,14 @@ def _put(t, bits):
     t.copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16))
 
 
-@pytest.mark.parametrize("block_tokens", [8, 16, 32])
-def test_serve_tiny_step_by_step(block_tokens):
-    """serve_tiny with pages of 8, 16 and 32 tokens (the pool keeps its
-    bytes), step by step against the oracle's loop."""
+def _step_by_step(w, block_tokens, seed=11, kernels=None):
+    """Runs workload w through the library's loop and the oracle's, step by
+    step with the same keyed token inputs, comparing plans, tables, free
+    list, pool and outputs after every step.  With `kernels` (a list), the
+    decode kernel the length rule picks for each step's rows is appended.
+    Returns (steps, prefill steps)."""
     import torch
-    w = wl.make_serve_workload("serve_tiny")
-    seed = 11
+    pk = _pk()
     nb = w.num_blocks * BS // block_tokens
     mb = max((p + g + block_tokens - 1) // block_tokens for _, p, g in w.requests) + 1
     rng = np.random.default_rng(w.seed)
@@ -103,6 +104,8 @@ def test_serve_tiny_step_by_step(block_tokens):
         steps += 1
         ids, pos = dl.b.rows()
         assert ids.tolist() == rp.rows and dl.b.retired() == rp.retired
+        if kernels is not None and p.n_rows > 0:
+            kernels.append(pk.pa_decode_kernel_for_lengths(pos[:p.n_rows] + 1, block_tokens))
         # the step's inputs, from the rows the library planned
         for layer in range(w.n_layers):
             off = 0
@@ -133,9 +136,38 @@ def test_serve_tiny_step_by_step(block_tokens):
         if dec is not None:
             got = host_f64(dl.do[:, :p.n_rows])
             assert_attention_close(got, dec, f"decode step {steps}")
-    assert steps > 10 and prefills > 2
     assert int(dl.fc.item()) == nb and (dl.bt.cpu().numpy() == -1).all()
     dl.b.close()
+    return steps, prefills
+
+
+@pytest.mark.parametrize("block_tokens", [8, 16, 32])
+def test_serve_tiny_step_by_step(block_tokens):
+    """serve_tiny with pages of 8, 16 and 32 tokens (the pool keeps its
+    bytes), step by step against the oracle's loop."""
+    steps, prefills = _step_by_step(wl.make_serve_workload("serve_tiny"), block_tokens)
+    assert steps > 10 and prefills > 2
+
+
+def test_decode_steps_switch_kernels():
+    """A loop whose decode steps take all three kernels, step by step against
+    the oracle: 24 even rows (the per-sequence kernel), then 5 short rows and
+    one 1200-token prompt (a heavy tail: the split kernel), then the long
+    request alone (the per-head kernel).  The batcher picks each step's
+    kernel from its rows' contexts and captures one graph per (rows,
+    kernel)."""
+    import torch
+    pk = _pk()
+    # 24 rows exceed the per-head kernel's bound (two CTAs per (row, kv head))
+    assert 24 * 16 > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    reqs = [(i, 120, 4) for i in range(19)] + [(19 + i, 120, 12) for i in range(5)]
+    reqs.append((24, 1200, 16))
+    w = wl.ServeWorkload("switch", 1, 24, 400, 0, 4096, reqs, seed=12)
+    kernels = []
+    steps, prefills = _step_by_step(w, BS, seed=13, kernels=kernels)
+    seen = set(kernels)
+    assert seen == {pk.PA_DECODE_SPLIT, pk.PA_DECODE_CLUSTER, pk.PA_DECODE_SEQ}, kernels
+    assert prefills >= 2
 
 
 def test_serve256_full_size_sampled():
