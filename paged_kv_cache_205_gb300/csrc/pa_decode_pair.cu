@@ -29,6 +29,15 @@
 //    the length and ids are read again; if either changed, the consumers drop
 //    what they accumulated (a reset stage) and the range is streamed again
 //    from the current values.  Nothing is written before that check.
+//  * Packed plan (batches with two CTAs per pair on average, the c = 2
+//    case): rather than 2 CTAs for every pair, a sequence gets 1, 2 or 4 CTAs
+//    per kv head by its length (the longest the most, within the same total),
+//    in clusters of 4, so that the longest heads' CTAs stream fewer tiles
+//    (llama1b's contexts, 256 to 2048 tokens: 54 tiles at most instead of 64).
+//    Every CTA's producer warp works the plan out from all the context lengths
+//    before the dependency wait and again after it; if the plan moved, the
+//    first stage streamed after the check carries the final role to the
+//    consumers (who started on q of the planned one).
 #include <cfloat>
 #include <climits>
 #include <cuda.h>
@@ -54,6 +63,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kReset = 1;   // consumers drop their state before this stage
 constexpr int kEnd = 2;     // no more tiles; the stage carries no data
+constexpr int kMoved = 4;   // packed plan: the CTA's role changed after the wait (see role[])
+constexpr int kIdle = 8;    // packed plan: the CTA has no part of it
 
 struct PairStage {
   int j0;      // tile of slot 0
@@ -71,6 +82,7 @@ struct __align__(1024) PairSmem {
   float2 part_ml[kMaxCluster][kGqa];     // and its (m, l), m in the log2 domain
   // (part_o rows are 16-byte aligned: the stages before them are 1 KiB multiples)
   PairStage desc[kPairStages];
+  int role[4];                           // packed plan: sequence (-1: idle), kv head, parts, part
   uint64_t full[kPairStages];
   uint64_t empty[kPairStages];
   uint64_t parts_full;                   // cluster leader: every CTA's result has landed
@@ -89,6 +101,8 @@ struct PairParams {
   int layer;
   int cap_tokens;
   float qscale;
+  int num_seqs;
+  int packed;                // clusters of 4 CTAs shared out by the packed plan
 };
 
 // ------------------------------------------------------------- clusters
@@ -237,6 +251,65 @@ __device__ __forceinline__ void tile_range(int nb, int rank, int c, int &t0, int
   t1 = static_cast<int>(static_cast<long long>(nb) * (rank + 1) / c);
 }
 
+// Barrier `id` over `count` threads that also returns whether v held for all.
+__device__ __forceinline__ bool bar_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// The packed plan (one warp; n <= 32 sequences, lane s holding sequence s's
+// 16-token tiles).  Sequence s gets k_s in {1, 2, 4} CTAs per kv head: for the
+// smallest M (binary search) with every k_s = 1 if T_s <= M, 2 if T_s <= 2M,
+// else 4 (T_s <= 4M), and sum k_s <= 2n, so that no CTA takes more than M
+// tiles where a uniform 2 CTAs per pair would give the longest head's CTAs
+// T_max / 2.  Sequence s's 8 k_s CTAs follow sequence s-1's in the grid
+// (clusters of 4: a part never straddles one), kv head e / k_s taking part
+// e mod k_s of them.  Writes the role of grid CTA g: the sequence (-1 past
+// the plan's CTAs: nothing to do), kv head, parts and part.
+__device__ __forceinline__ void packed_role(int tiles, int n, int g, int lane, int (&role)[4]) {
+  const bool live = lane < n;
+  int tmax = live ? tiles : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  auto parts_for = [&](int m) { return !live ? 0 : (tiles <= m ? 1 : (tiles <= 2 * m ? 2 : 4)); };
+  int lo = (tmax + 3) / 4, hi = max(tmax, 1);
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    if (warp_sum(parts_for(mid)) <= 2 * n) hi = mid;
+    else lo = mid + 1;
+  }
+  const int k = parts_for(max(lo, 1));
+  int incl = 8 * k;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - 8 * k;
+  const unsigned hit = __ballot_sync(0xffffffffu, live && g >= excl && g < incl);
+  const int sl = hit ? __ffs(hit) - 1 : 0;
+  const int ks = __shfl_sync(0xffffffffu, k, sl);
+  const int e = g - __shfl_sync(0xffffffffu, excl, sl);
+  role[0] = hit ? sl : -1;
+  role[1] = hit ? e / ks : 0;
+  role[2] = hit ? ks : 1;
+  role[3] = hit ? e % ks : 0;
+}
+
 // One stage: wait until it is free, write its descriptor, issue the copies
 // of tiles j0 .. j0+n-1 (lane w < n holds the page ids of tile j0 + w, see
 // tile_ids).  Returns the slots with a page id out of range, or -1 if the
@@ -321,9 +394,17 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int lane = tid & 31;
   const int c = static_cast<int>(cluster_size());
   const int rank = static_cast<int>(cluster_rank());
-  const int pair = static_cast<int>(cluster_id());
-  const int s = pair / kHkv, h = pair % kHkv;
-  const int32_t *row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+  const bool packed = p.packed != 0;
+  // this CTA's (sequence, kv head), and its part of the kparts CTAs that
+  // share that pair's tiles; with the packed plan the producer warp works
+  // them out (below) and hands them to the consumers through role[]
+  int s = -1, h = 0, kparts = c, part = rank;
+  if (!packed) {
+    const int pair = static_cast<int>(cluster_id());
+    s = pair / kHkv;
+    h = pair % kHkv;
+  }
+  const int32_t *row = nullptr;
   // the next kernel on the stream may be scheduled at once: it waits for
   // this one to finish before it reads anything this one writes
   pdl_launch_dependents();
@@ -335,31 +416,52 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       mbar_init(&sm.full[st], 1);
       mbar_init(&sm.empty[st], kPairWarps);
     }
-    // the leader expects every CTA's state (O and (m, l) of 4 q heads) as bytes
+    // the leader expects every CTA's state (O and (m, l) of 4 q heads) as
+    // bytes (with the packed plan, once it knows how many parts it has)
     mbar_init(&sm.parts_full, 1);
-    if (rank == 0 && c > 1)
+    if (!packed && rank == 0 && c > 1)
       mbar_arrive_expect_tx(&sm.parts_full, static_cast<uint32_t>(c * kGqa * (kD * 4 + 8)));
     fence_mbar_init();
   }
   // the speculative plan: this CTA's range under the context length as it
   // reads now, and its first page ids; their tiles are prefetched into L2
   int spec_ctx = 0, spec_t0 = 0, spec_t1 = 0, spec_blk = -1, spec_blk2 = -1;
+  int spec_len = 0;   // packed plan: lane s's sequence length as read before the wait
   if (warp == kPairWarps) {
-    spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
-    tile_range((spec_ctx + kBs - 1) / kBs, rank, c, spec_t0, spec_t1);
-    // (the first 32 ids are kept for the first stages; the prefetches share
-    // the SM's TMA unit with the copies, so only the first 3 stages' worth)
-    const int j = spec_t0 + lane;
-    tile_ids<BT>(row, j, spec_t1, spec_ctx, spec_blk, spec_blk2);
-    if (spec_blk >= 0 && spec_blk < p.num_blocks) {
-      if (BT < kBs) {
-        // (the first page's K and V of a third as many tiles: the same count of requests)
-        if (lane < kPrefetchTiles / 3) {
-          prefetch_rows_l2(&kv_map, h, 0, spec_blk);
-          prefetch_rows_l2(&kv_map, h, 1, spec_blk);
+    if (packed) {
+      spec_len = lane < p.num_seqs ? min(max(p.context_lens[lane], 0), p.cap_tokens) : 0;
+      int role[4];
+      packed_role((spec_len + kBs - 1) / kBs, p.num_seqs,
+                  static_cast<int>(cluster_id()) * c + rank, lane, role);
+      s = role[0];
+      h = role[1];
+      kparts = role[2];
+      part = role[3];
+      if (lane == 0) {   // for the consumers' first q load (the barrier below publishes it)
+        sm.role[0] = s;
+        sm.role[1] = h;
+        sm.role[2] = kparts;
+        sm.role[3] = part;
+      }
+    }
+    if (s >= 0) {
+      row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
+      spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
+      tile_range((spec_ctx + kBs - 1) / kBs, part, kparts, spec_t0, spec_t1);
+      // (the first 32 ids are kept for the first stages; the prefetches share
+      // the SM's TMA unit with the copies, so only the first 3 stages' worth)
+      const int j = spec_t0 + lane;
+      tile_ids<BT>(row, j, spec_t1, spec_ctx, spec_blk, spec_blk2);
+      if (spec_blk >= 0 && spec_blk < p.num_blocks) {
+        if (BT < kBs) {
+          // (the first page's K and V of a third as many tiles: the same count of requests)
+          if (lane < kPrefetchTiles / 3) {
+            prefetch_rows_l2(&kv_map, h, 0, spec_blk);
+            prefetch_rows_l2(&kv_map, h, 1, spec_blk);
+          }
+        } else if (lane < kPrefetchTiles) {
+          prefetch_tile_l2(&kv_map, h, TP::tok0(j), spec_blk);
         }
-      } else if (lane < kPrefetchTiles) {
-        prefetch_tile_l2(&kv_map, h, TP::tok0(j), spec_blk);
       }
     }
   }
@@ -371,8 +473,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   if (warp == kPairWarps) {
     // ===================================================== producer warp ==
     // current values, read now and checked against the speculative ones
-    // once the first stages are on their way
-    const int ctx_raw = p.context_lens[s];
+    // once the first stages are on their way (with the packed plan, every
+    // sequence's length: the plan itself may have moved)
+    const int now_raw = packed ? (lane < p.num_seqs ? p.context_lens[lane] : 0)
+                               : (s >= 0 ? p.context_lens[s] : 0);
     int blk_now, blk_now2;
     tile_ids<BT>(row, spec_t0 + lane, spec_t1, spec_ctx, blk_now, blk_now2);
     int stage = 0;
@@ -404,11 +508,38 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         phase ^= 1;
       }
     }
-    const int ctx = min(max(ctx_raw, 0), p.cap_tokens);
-    if (lane == 0 && rank == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
+    int ctx_raw = now_raw;
+    bool moved = false;   // the packed plan gave this CTA another role
+    if (packed) {
+      const int now_len = min(max(now_raw, 0), p.cap_tokens);
+      if (!__all_sync(0xffffffffu, now_len == spec_len)) {
+        int role[4];
+        packed_role((now_len + kBs - 1) / kBs, p.num_seqs,
+                    static_cast<int>(cluster_id()) * c + rank, lane, role);
+        moved = role[0] != s || role[1] != h || role[2] != kparts || role[3] != part;
+        s = role[0];
+        h = role[1];
+        kparts = role[2];
+        part = role[3];
+        row = s >= 0 ? p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks
+                     : nullptr;
+      }
+      ctx_raw = __shfl_sync(0xffffffffu, now_raw, s >= 0 ? s : 0);
+      // the final role, for the consumers: written before any later stage
+      // is published, so a consumer that sees kMoved or the end reads it
+      if (moved && lane == 0) {
+        sm.role[0] = s;
+        sm.role[1] = h;
+        sm.role[2] = kparts;
+        sm.role[3] = part;
+      }
+    }
+    const bool idle = s < 0;   // no part of the plan: only the end stage follows
+    const int ctx = idle ? 0 : min(max(ctx_raw, 0), p.cap_tokens);
+    if (!idle && lane == 0 && part == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.cap_tokens))
       report(p.err, PA_DEV_CTX_RANGE);
     const bool same =
-        ctx == spec_ctx &&
+        !moved && ctx == spec_ctx &&
         __all_sync(0xffffffffu, blk_now == spec_blk && (BT >= kBs || blk_now2 == spec_blk2));
     const int nb = (ctx + kBs - 1) / kBs;
     const int last = nb - 1, tail = ctx - (nb - 1) * kBs;
@@ -417,10 +548,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     if (!same) {
       // the plan moved: stream the current range from its start; the
       // consumers drop what they accumulated from the speculative stages
-      tile_range(nb, rank, c, t0, t1);
+      tile_range(nb, part, kparts, t0, t1);
       j = base = t0;
       tile_ids<BT>(row, t0 + lane, t1, ctx, ids, ids2);
-      flags = kReset;
+      flags = kReset | (moved ? kMoved : 0);
     } else if (bad_seen && lane == 0) {
       report(p.err, PA_DEV_BAD_BLOCK);
     }
@@ -461,7 +592,7 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         d.last = -1;
         d.tail = 0;
         d.bad = 0;
-        d.flags = kEnd | flags;
+        d.flags = kEnd | flags | (idle ? kIdle : 0);
         sm.desc[stage] = d;
         mbar_arrive(&sm.full[stage]);
         issued |= 1u << stage;
@@ -484,7 +615,13 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const int c2 = 2 * (lane & 3);         // fragment column pair
   const bool real_row = r < kGqa;
   uint32_t qa[4], qc[4];
-  load_q_fragments(p.q + static_cast<size_t>(s) * kHq * kD, h, lane, qa, qc);
+  // with the packed plan: the role as planned before the wait (a stage
+  // flagged kMoved hands over the final one)
+  if (packed) {
+    s = sm.role[0];
+    h = sm.role[1];
+  }
+  if (s >= 0) load_q_fragments(p.q + static_cast<size_t>(s) * kHq * kD, h, lane, qa, qc);
   TileState ts;
   ts.reset();
   int stage = 0;
@@ -497,19 +634,24 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       break;
     }
     const PairStage d = sm.desc[stage];
+    if (d.flags & kMoved) {
+      s = sm.role[0];
+      h = sm.role[1];
+      if (s >= 0) load_q_fragments(p.q + static_cast<size_t>(s) * kHq * kD, h, lane, qa, qc);
+    }
     if (d.flags & kReset) ts.reset();
     if (d.flags & kEnd) break;
     if constexpr (BT < kBs) {
       // 8-token pages: the rows of the pages that were loaded
       const unsigned ld = ((d.bad >> w) & 1u ? 0x00ffu : 0u) |
                           ((d.bad >> (kPairWarps + w)) & 1u ? 0xff00u : 0u);
-      if (w < d.n && ld) {
+      if (s >= 0 && w < d.n && ld) {
         const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
         const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
         attend_tile<true>(ktile, ktile + kBs * kHeadRowBytes, n_valid,
                           ld & ((1u << n_valid) - 1u), qa, qc, p.qscale, lane, ts);
       }
-    } else if (w < d.n && !((d.bad >> w) & 1)) {
+    } else if (s >= 0 && w < d.n && !((d.bad >> w) & 1)) {
       const int n_valid = (d.j0 + w == d.last) ? d.tail : kBs;
       const uint32_t ktile = smem_u32(sm.kv[stage] + w * kSlotBytes);
       attend_tile<false>(ktile, ktile + kBs * kHeadRowBytes, n_valid, 0u, qa, qc, p.qscale, lane,
@@ -521,6 +663,18 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
       stage = 0;
       phase ^= 1;
     }
+  }
+
+  if (packed) {
+    // the consumer warps agree: all of them saw the end (then the final role
+    // is in role[]), or the CTA writes nothing (the wait that ran out is
+    // reported; the pair's leader, missing this part, reports its own)
+    if (!bar_and(1, kPairWarps * 32, !timed_out)) return;
+    s = sm.role[0];
+    h = sm.role[1];
+    kparts = sm.role[2];
+    part = sm.role[3];
+    if (s < 0) return;
   }
 
   // ---- the 8 warp states -> one CTA state.  Each warp parks its state in
@@ -562,28 +716,34 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   }
   uint2 *dst = reinterpret_cast<uint2 *>(
       p.out + (static_cast<size_t>(s) * kHq + h * kGqa + qrow) * kD + d0);
-  if (c == 1) {
+  if (kparts == 1) {
     *dst = bf16x4_scaled(O, L > 0.f ? 1.f / L : 0.f);
     return;
   }
 
-  // ---- the c CTA states -> the output, in the cluster leader's shared
-  // memory: 64 asynchronous 16-byte stores and 4 of 8 bytes per CTA, which
-  // complete the leader's barrier by their byte count
-  const uint32_t bar = map_to_rank(&sm.parts_full, 0);
-  st_async_f32x4(map_to_rank(&sm.part_o[rank][qrow][d0], 0), O, bar);
-  if ((tid & 15) == 0) st_async_f32x2(map_to_rank(&sm.part_ml[rank][qrow], 0), make_float2(M, L), bar);
-  if (rank != 0) return;
+  // ---- the kparts CTA states -> the output, in the shared memory of the
+  // pair's first CTA (the leader): 64 asynchronous 16-byte stores and 4 of
+  // 8 bytes per CTA, which complete the leader's barrier by their byte count
+  const uint32_t lead = static_cast<uint32_t>(rank - part);
+  const uint32_t bar = map_to_rank(&sm.parts_full, lead);
+  st_async_f32x4(map_to_rank(&sm.part_o[part][qrow][d0], lead), O, bar);
+  if ((tid & 15) == 0)
+    st_async_f32x2(map_to_rank(&sm.part_ml[part][qrow], lead), make_float2(M, L), bar);
+  if (part != 0) return;
+  // (with the packed plan the leader learns its part count only now; bytes
+  // that land before it says how many to expect are counted all the same)
+  if (packed && tid == 0)
+    mbar_arrive_expect_tx(&sm.parts_full, static_cast<uint32_t>(kparts * kGqa * (kD * 4 + 8)));
   if (!mbar_wait_cluster(&sm.parts_full, 0)) {
     report(p.err, PA_DEV_TIMEOUT);
     return;
   }
   float Mc = neg_inf();
-  for (int k = 0; k < c; ++k) Mc = fmaxf(Mc, sm.part_ml[k][qrow].x);
+  for (int k = 0; k < kparts; ++k) Mc = fmaxf(Mc, sm.part_ml[k][qrow].x);
   float Lc = 0.f;
   float4 Oc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (Mc != neg_inf()) {
-    for (int k = 0; k < c; ++k) {
+    for (int k = 0; k < kparts; ++k) {
       const float sc = fast_exp2(sm.part_ml[k][qrow].x - Mc);
       Lc = fmaf(sm.part_ml[k][qrow].y, sc, Lc);
       fma4(Oc, *reinterpret_cast<const float4 *>(&sm.part_o[k][qrow][d0]), sc);
@@ -984,6 +1144,11 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
   prm.layer = layer;
   prm.cap_tokens = max_blocks_per_seq * block_tokens;
   prm.qscale = scale * kLog2e;
+  prm.num_seqs = num_seqs;
+  // two CTAs per pair on average: the packed plan shares them out by length
+  // (1, 2 or 4 per kv head of a sequence) in clusters of 4
+  const bool packed = cluster == 2 && num_seqs <= 32;
+  prm.packed = packed ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_seqs) * kHkv * cluster);
@@ -992,7 +1157,7 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(packed ? 4 : cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
