@@ -265,11 +265,7 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
+__device__ __forceinline__ int warp_sum(int v) { return __reduce_add_sync(0xffffffffu, v); }
 
 // The packed plan (one warp; n <= 32 sequences, lane s holding sequence s's
 // 16-token tiles).  Sequence s gets k_s in {1, 2, 4} CTAs per kv head: for the
@@ -282,9 +278,7 @@ __device__ __forceinline__ int warp_sum(int v) {
 // the plan's CTAs: nothing to do), kv head, parts and part.
 __device__ __forceinline__ void packed_role(int tiles, int n, int g, int lane, int (&role)[4]) {
   const bool live = lane < n;
-  int tmax = live ? tiles : 0;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  const int tmax = __reduce_max_sync(0xffffffffu, live ? tiles : 0);
   auto parts_for = [&](int m) { return !live ? 0 : (tiles <= m ? 1 : (tiles <= 2 * m ? 2 : 4)); };
   int lo = (tmax + 3) / 4, hi = max(tmax, 1);
   while (lo < hi) {
@@ -446,7 +440,11 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
     }
     if (s >= 0) {
       row = p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer) * p.max_blocks;
-      spec_ctx = min(max(p.context_lens[s], 0), p.cap_tokens);
+      // (the packed plan has every length already: one dependent read less
+      // before the first copies, whose chain of reads is on the critical
+      // path of the CTAs that start late)
+      spec_ctx = packed ? __shfl_sync(0xffffffffu, spec_len, s)
+                        : min(max(p.context_lens[s], 0), p.cap_tokens);
       tile_range((spec_ctx + kBs - 1) / kBs, part, kparts, spec_t0, spec_t1);
       // (the first 32 ids are kept for the first stages; the prefetches share
       // the SM's TMA unit with the copies, so only the first 3 stages' worth)
@@ -507,6 +505,14 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
         stage = 0;
         phase ^= 1;
       }
+    }
+    // the next layer's table row of this sequence into L2 (one CTA per
+    // sequence): the next call's CTAs read it before their dependency wait,
+    // while this call streams, and a miss to DRAM there is on their path
+    if (s >= 0 && part == 0 && h == 0 && p.layer + 1 < p.n_layers) {
+      const int32_t *next =
+          p.block_table + (static_cast<size_t>(s) * p.n_layers + p.layer + 1) * p.max_blocks;
+      for (int i = lane * 32; i < p.max_blocks; i += 32 * 32) prefetch_l2(next + i);
     }
     int ctx_raw = now_raw;
     bool moved = false;   // the packed plan gave this CTA another role
