@@ -516,6 +516,19 @@ int pa_decode_kernel_for_lengths(const int32_t *context_lens, int num_seqs, int 
  */
 int pa_decode_set_test_fault(int stage, long long wait_limit_ns);
 
+/*
+ * Test hook of the per-head cluster kernel's speculative plan (no
+ * counterpart in the paper).  With mode = 1, its packed plan (the batches
+ * where every (sequence, kv head) pair gets two CTAs on average) is first
+ * worked out from the first sequence's length in place of every length, as
+ * if the lengths had changed after they were read, so that the check after
+ * the dependency wait finds the plan moved: CTAs change role mid-call (the
+ * consumers drop what they accumulated and reload q) or are left without a
+ * part.  Outputs stay exact.  mode = 0 restores normal operation.
+ * Process-wide; for tests only.  PA_ERR_ARG for another mode.
+ */
+int pa_decode_set_test_plan(int mode);
+
 /* Human-readable name of a PA_ERR_* code. */
 const char *pa_error_string(int code);
 

@@ -132,6 +132,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_set_path.restype = I
         lib.pa_decode_set_test_fault.argtypes = [I, ctypes.c_longlong]
         lib.pa_decode_set_test_fault.restype = I
+        lib.pa_decode_set_test_plan.argtypes = [I]
+        lib.pa_decode_set_test_plan.restype = I
         lib.pa_decode_kernel_for.argtypes = [I, I]
         lib.pa_decode_kernel_for.restype = I
         lib.pa_decode_kernel_for_lengths.argtypes = [P, I, I]
@@ -366,6 +368,13 @@ def pa_decode_set_test_fault(stage: int, wait_limit_ns: int = 0) -> None:
     shortens every wait of the split kernel to wait_limit_ns; -1 restores."""
     _check("pa_decode_set_test_fault",
            library().pa_decode_set_test_fault(int(stage), int(wait_limit_ns)))
+
+
+def pa_decode_set_test_plan(mode: int) -> None:
+    """Test hook of the per-head kernel's speculative plan (see
+    include/pagedkv.h): 1 makes the plan move after the dependency wait, 0
+    restores."""
+    _check("pa_decode_set_test_plan", library().pa_decode_set_test_plan(int(mode)))
 
 
 def pa_decode_kernel_for_lengths(context_lens, block_tokens: int = PA_BLOCK_TOKENS) -> int:

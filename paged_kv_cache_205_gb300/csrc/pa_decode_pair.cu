@@ -103,6 +103,7 @@ struct PairParams {
   float qscale;
   int num_seqs;
   int packed;                // clusters of 4 CTAs shared out by the packed plan
+  int test_plan;             // test hook: plan first from the first length (pa_decode_set_test_plan)
 };
 
 // ------------------------------------------------------------- clusters
@@ -424,6 +425,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   if (warp == kPairWarps) {
     if (packed) {
       spec_len = lane < p.num_seqs ? min(max(p.context_lens[lane], 0), p.cap_tokens) : 0;
+      if (p.test_plan) {   // (every lane takes part in the shuffle)
+        const int first = __shfl_sync(0xffffffffu, spec_len, 0);
+        spec_len = lane < p.num_seqs ? first : 0;
+      }
       int role[4];
       packed_role((spec_len + kBs - 1) / kBs, p.num_seqs,
                   static_cast<int>(cluster_id()) * c + rank, lane, role);
@@ -1116,6 +1121,8 @@ int decode_pair_cluster(int num_seqs, int sm_count, int max_ctas) {
   return c;
 }
 
+int g_test_plan = 0;   // pa_decode_set_test_plan
+
 int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
                        int num_blocks, int block_tokens, const int32_t *block_table, int n_layers,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
@@ -1155,6 +1162,7 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
   // (1, 2 or 4 per kv head of a sequence) in clusters of 4
   const bool packed = cluster == 2 && num_seqs <= 32;
   prm.packed = packed ? 1 : 0;
+  prm.test_plan = g_test_plan;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_seqs) * kHkv * cluster);
@@ -1175,3 +1183,9 @@ int launch_decode_pair(const CUtensorMap &map, uint16_t *out, const uint16_t *q,
 }
 
 }  // namespace pa
+
+extern "C" int pa_decode_set_test_plan(int mode) {
+  if (mode != 0 && mode != 1) return PA_ERR_ARG;
+  pa::g_test_plan = mode;
+  return PA_OK;
+}

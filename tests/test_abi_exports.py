@@ -51,6 +51,9 @@ def test_host_validation_without_a_device():
     assert lib.pa_decode_set_test_fault(0, 2_000_000_000) == -2
     assert lib.pa_decode_set_test_fault(0, 50_000) == 0
     assert lib.pa_decode_set_test_fault(-1, 0) == 0
+    # the speculative-plan test hook: modes 0 and 1 only
+    assert lib.pa_decode_set_test_plan(2) == -2 and lib.pa_decode_set_test_plan(-1) == -2
+    assert lib.pa_decode_set_test_plan(1) == 0 and lib.pa_decode_set_test_plan(0) == 0
 
 
 def test_decode_path_switch_without_a_device():

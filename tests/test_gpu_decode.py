@@ -373,6 +373,35 @@ def test_chosen_kernel_matches_oracle(case):
     assert_attention_close(out, ref, f"{case}, kernel {path}")
 
 
+@pytest.mark.parametrize("n,law", [(10, "u"), (16, "u"), (19, "u"), (16, "logu"), (12, "even")])
+def test_packed_plan_that_moves_after_the_wait(decode_path, n, law):
+    """The per-head kernel's packed plan (two CTAs per pair on average) first
+    worked out from a wrong length (the test hook makes every sequence look
+    like the first), so that after the dependency wait the plan moves: CTAs
+    take another (sequence, kv head) or part mid-call, or are left idle.  The
+    result still matches the oracle."""
+    pk = _pk()
+    rng = np.random.default_rng(500 + n)
+    if law == "u":
+        ctx = rng.integers(256, 2049, size=n)
+    elif law == "logu":
+        ctx = np.floor(np.exp(rng.uniform(0, np.log(3000), size=n))).astype(np.int64)
+        ctx[0] = 1
+    else:
+        ctx = np.full(n, 700)
+        ctx[0] = 40
+    w, pool, q = _small_case(4100 + n, ctx, q_scale=2.0)
+    ref, _ = oracle.decode_attention(q, pool, w.block_table, w.context_lens, 0)
+    pk.pa_decode_set_path(pk.PA_DECODE_CLUSTER)
+    pk.pa_decode_set_test_plan(1)
+    try:
+        out, err = _run_gpu(q, pool, w.block_table, w.context_lens, 0)
+    finally:
+        pk.pa_decode_set_test_plan(0)
+    assert err == 0
+    assert_attention_close(out, ref, f"moved plan n={n} {law}")
+
+
 @pytest.mark.parametrize("grid", [0, 24, 64, 152, 304])
 @pytest.mark.parametrize("n", [1, 2, 3, 7, 16, 19, 32])
 def test_mixed_lengths_every_cluster_size(decode_path, n, grid):
