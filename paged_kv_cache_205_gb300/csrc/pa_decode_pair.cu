@@ -627,7 +627,10 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm)
   const bool real_row = r < kGqa;
   uint32_t qa[4], qc[4];
   // with the packed plan: the role as planned before the wait (a stage
-  // flagged kMoved hands over the final one)
+  // flagged kMoved hands over the final one; a consumer that reads role[]
+  // after the producer rewrote it starts on the final role, or on a mix of
+  // the two, and the kMoved stage, which comes before any stage of the new
+  // range, sets it right and drops what it accumulated)
   if (packed) {
     s = sm.role[0];
     h = sm.role[1];
