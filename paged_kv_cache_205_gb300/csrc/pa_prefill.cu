@@ -27,7 +27,9 @@
 //               MN-major operand) into its O columns.  S_{j+1} is thus
 //               computed while the softmax works on S_j.  A tcgen05.mma issue
 //               blocks while the tensor core's queue is full, so each half
-//               has its own issuing thread.  The warp of the half that sees
+//               has its own issuing warp; an elected lane of the converged
+//               warp issues (the lane-index branch that did before took two
+//               to three times as long per MMA).  The warp of the half that sees
 //               every chunk also zeroes the V rows that lie past the tile's
 //               last key or in a page that was not loaded;
 //   warps 0-3, 4-7   softmax of half 0 / half 1, one thread per row (TMEM
@@ -113,7 +115,6 @@ struct __align__(1024) PSmem {
   uint64_t o_full[kHalves];
   uint64_t o_free[kHalves];
   uint64_t v_zeroed[kStagesP];                     // zeroing warp -> the other half's MMA warp
-  uint64_t h0_started;                             // half 0 has read an item's first S
   uint64_t staged[kHalves];                        // the half's output rows are in shared memory
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
@@ -237,20 +238,49 @@ __device__ __forceinline__ int item_position(int k, int n_items) {
   return pos < n_items ? pos : -1;
 }
 
-__device__ __forceinline__ Item decode_item(const PSmem &sm, const PrefillParams &p,
-                                            int total_tiles, bool sorted, int i) {
+// The item at position k of this CTA's walk: its place in the work order,
+// tile and sequence, and the sequence's three values in global memory.  The
+// roles that are on the pipeline's path fetch the next item while the
+// current one runs, so that the loads' latency is not paid between items.
+struct ItemRef {
+  int i;                      // position in the work order; -1 past the end
+  int t, s;                   // tile, sequence
+  int ctx, row0, row_end;     // cached tokens; the sequence's rows [row0, row_end)
+};
+
+// A load that stays where it is written (the compiler may move a read-only
+// __ldg down to its first use, which would put its latency back between
+// the items).
+__device__ __forceinline__ int load_early(const int32_t *ptr) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
+__device__ __forceinline__ ItemRef fetch_item(const PSmem &sm, const PrefillParams &p,
+                                              int total_tiles, bool sorted, int k, int n_items) {
+  ItemRef r;
+  r.i = item_position(k, n_items);
+  r.t = r.s = r.ctx = r.row0 = r.row_end = 0;
+  if (r.i < 0) return r;
+  const int rank = r.i / kHkv;
+  r.t = sorted ? static_cast<int>(sm.order[rank]) : total_tiles - 1 - rank;
+  r.s = tile_seq(sm, p.num_seqs, r.t);
+  // (read-only for the kernel's lifetime: through the non-coherent path)
+  r.ctx = load_early(p.context_lens + r.s);
+  r.row0 = load_early(p.cu_tokens + r.s);
+  r.row_end = load_early(p.cu_tokens + r.s + 1);
+  return r;
+}
+
+__device__ __forceinline__ Item decode_item(const PSmem &sm, const ItemRef &r) {
   Item it;
-  const int rank = i / kHkv;
-  const int t = sorted ? static_cast<int>(sm.order[rank]) : total_tiles - 1 - rank;
-  it.g = i % kHkv;
-  const int lo = tile_seq(sm, p.num_seqs, t);
-  it.s = lo;
-  it.t0 = (t - sm.tile_prefix[lo]) * kCtaTok;
-  // (read-only for the kernel's lifetime: through the non-coherent path,
-  // which keeps them in L1 for the items that follow)
-  it.ctx = __ldg(p.context_lens + lo);
-  it.row0 = __ldg(p.cu_tokens + lo);
-  const int n = __ldg(p.cu_tokens + lo + 1) - it.row0;
+  it.g = r.i % kHkv;
+  it.s = r.s;
+  it.t0 = (r.t - sm.tile_prefix[r.s]) * kCtaTok;
+  it.ctx = r.ctx;
+  it.row0 = r.row0;
+  const int n = r.row_end - r.row0;
   it.rows0 = min(kQTok, n - it.t0);
   it.rows1 = min(kQTok, n - it.t0 - kQTok);
   it.halves = it.rows1 > 0 ? 2 : 1;
@@ -364,7 +394,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.o_full[h], 1);
       mbar_init(&sm.o_free[h], kSoftThreads);
     }
-    mbar_init(&sm.h0_started, kSoftThreads);
     for (int h = 0; h < kHalves; ++h) mbar_init(&sm.staged[h], kSoftThreads);
     fence_mbar_init();
   }
@@ -496,9 +525,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       int blk_next = -1;
       bool next_read = false;
       for (; ok; ++k) {
-        const int i = item_position(k, n_items);
-        if (i < 0) break;
-        const Item it = decode_item(sm, p, total_tiles, sorted, i);
+        const ItemRef ref = fetch_item(sm, p, total_tiles, sorted, k, n_items);
+        if (ref.i < 0) break;
+        const Item it = decode_item(sm, ref);
         if (!next_read && it.n_chunks > 0) blk_next = chunk_ids(it, 0);
         next_read = false;
         int good = 1;
@@ -523,10 +552,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           const int blk = blk_next;
           if (j + 1 < it.n_chunks) {
             blk_next = chunk_ids(it, j + 1);
-          } else if (item_position(k + 1, n_items) >= 0) {
-            const Item nx = decode_item(sm, p, total_tiles, sorted, item_position(k + 1, n_items));
-            if (nx.n_chunks > 0) blk_next = chunk_ids(nx, 0);
-            next_read = true;
+          } else {
+            const ItemRef nr = fetch_item(sm, p, total_tiles, sorted, k + 1, n_items);
+            if (nr.i >= 0) {
+              const Item nx = decode_item(sm, nr);
+              if (nx.n_chunks > 0) blk_next = chunk_ids(nx, 0);
+              next_read = true;
+            }
           }
           const bool valid = needed && blk >= 0 && blk < p.num_blocks;
           const unsigned vm = __ballot_sync(0xffffffffu, valid) & kAllPages;
@@ -578,20 +610,25 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       int n_active = 0;        // items in which the half had work
       uint32_t vz_parity = 0;  // per stage: parity of the next zeroing hand-over
       int n_s = 0;             // S chunks issued
-      int n_started = 0;       // two-half items (half 1's warp)
-      // S of chunk gcs once the softmax has read the previous S (lane 0)
+      // Lane 0 waits on the mbarriers and the warp takes its verdict; the
+      // MMAs and commits are issued by one elected lane of the converged
+      // warp, which keeps the tensor core fed at its own rate.
       int qb = 0;              // the item's Q buffer
+      // S of chunk gcs once the softmax has read the previous S (whole warp)
       auto issue_s = [&](int gcs) -> bool {
-        if (n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) return false;
+        int good = 1;
+        if (lane == 0 && n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) good = 0;
+        if (!__shfl_sync(0xffffffffu, good, 0)) return false;
         tc::fence_after_sync();
-        mma_issue_s(sm, tmem, qb, h, gcs, id_s);
+        if (tc::elect_one()) mma_issue_s(sm, tmem, qb, h, gcs, id_s);
+        __syncwarp();
         ++n_s;
         return true;
       };
+      ItemRef ref = fetch_item(sm, p, total_tiles, sorted, 0, n_items);
       for (; ok; ++k) {
-        const int i = item_position(k, n_items);
-        if (i < 0) break;
-        const Item it = decode_item(sm, p, total_tiles, sorted, i);
+        if (ref.i < 0) break;
+        const Item it = decode_item(sm, ref);
         qb = k % kQBufs;
         const int nch = h == 0 ? it.nc0 : it.nc1;
         // half 1 sees every chunk of a two-half tile, half 0 every chunk of
@@ -601,17 +638,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (lane == 0) ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) ok = mma_prepare_chunk<BT>(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
-        if (ok && nch > 0) {
-          int good = 1;
-          if (lane == 0) {
-            // half 1 starts an item once half 0 is under way: the halves'
-            // softmax passes then alternate instead of running side by side
-            if (h == 1 && !mbar_wait_short(&sm.h0_started, n_started & 1)) good = 0;
-            if (good) good = issue_s(gc) ? 1 : 0;
-          }
-          if (h == 1) ++n_started;
-          ok = __shfl_sync(0xffffffffu, good, 0);
-        }
+        if (ok && nch > 0) ok = issue_s(gc) ? 1 : 0;
+        // the next item's loads are in flight while this item's chunks run
+        ref = fetch_item(sm, p, total_tiles, sorted, k + 1, n_items);
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
           if (j + 1 < it.n_chunks &&
               !mma_prepare_chunk<BT>(sm, gc + 1, (j + 1) * kChunk, it.n_keys, zeroer,
@@ -621,9 +650,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           }
           if (j < nch) {
             int good = 1;
+            if (j + 1 < nch && !issue_s(gc + 1)) good = 0;
             if (lane == 0) {
               const int st = gc % kStagesP;
-              if (j + 1 < nch && !issue_s(gc + 1)) good = 0;
               // the half's previous item has read its O (the first PV clears it)
               if (good && j == 0 && n_active > 0 &&
                   !mbar_wait_short(&sm.o_free[h], (n_active - 1) & 1))
@@ -635,18 +664,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
                 if (!mbar_wait_short(&sm.v_zeroed[st], (vz_parity >> st) & 1u)) good = 0;
                 vz_parity ^= 1u << st;
               }
-              if (good) {
-                tc::fence_after_sync();
-                mma_issue_pv(sm, tmem, h, gc, j == 0, id_o);
-              }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (good) {
+              tc::fence_after_sync();
+              if (tc::elect_one()) mma_issue_pv(sm, tmem, h, gc, j == 0, id_o);
+              __syncwarp();
             }
             ++n_p;
-            ok = __shfl_sync(0xffffffffu, good, 0);
+            ok = good;
           }
-          if (ok && lane == 0) tc::mma_commit(&sm.kv_empty[gc % kStagesP]);
+          if (ok && tc::elect_one()) tc::mma_commit(&sm.kv_empty[gc % kStagesP]);
           __syncwarp();
         }
-        if (ok && lane == 0) tc::mma_commit(&sm.q_empty[qb]);   // every MMA that reads Q is issued
+        if (ok && tc::elect_one()) tc::mma_commit(&sm.q_empty[qb]);   // every MMA that reads Q is issued
+        __syncwarp();
         if (nch > 0) ++n_active;
       }
       if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
@@ -671,10 +703,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
     bool ok = true;
     int gc = 0, n_s = 0, n_o = 0;   // S chunks read; PV commits waited for
     int n_staged = 0;               // output tiles staged
+    // Thread r == 0: the Q buffer its last output store reads from, released
+    // to the producer only after the next item's first P (the store has read
+    // it long before), so that the wait for the read is off the warp's path.
+    int pend_qb = -1;
+    auto release_stored = [&]() {
+      if (pend_qb >= 0) {
+        bulk_wait_group_read0();
+        mbar_arrive(&sm.q_empty[pend_qb]);
+        pend_qb = -1;
+      }
+    };
+    ItemRef ref = fetch_item(sm, p, total_tiles, sorted, 0, n_items);
     for (int k = 0; ok; ++k) {
-      const int i = item_position(k, n_items);
-      if (i < 0) break;
-      const Item it = decode_item(sm, p, total_tiles, sorted, i);
+      if (ref.i < 0) break;
+      const Item it = decode_item(sm, ref);
+      // the next item's loads are in flight while this item's chunks run
+      ref = fetch_item(sm, p, total_tiles, sorted, k + 1, n_items);
       const int rows = h == 0 ? it.rows0 : it.rows1;
       const int nch = h == 0 ? it.nc0 : it.nc1;
       const int qb = k % kQBufs;
@@ -682,6 +727,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         // nothing staged: release the Q buffer, once it holds this item's Q
         // (an earlier arrival would count for the item before last)
         if (r == 0) {
+          release_stored();
           ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1);
           if (ok) mbar_arrive(&sm.q_empty[qb]);
         }
@@ -713,7 +759,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         mbar_arrive(&sm.s_free[h]);             // S_{j+1} may land in the S columns
-        if (h == 0 && j == 0 && it.halves == 2) mbar_arrive(&sm.h0_started);
         if (!full) {
           // masked keys: -inf (loaded K rows past the tile or in a missing page may be anything)
 #pragma unroll
@@ -789,6 +834,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         tc::tmem_st_wait();
         tc::fence_before_sync();    // P, for the tensor core
         mbar_arrive(&sm.p_full[h]);
+        if (j == 0) release_stored();
       }
       if (!ok) break;
       // O is complete once the item's last PV is
@@ -826,10 +872,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (r == 0) {
           ok = mbar_wait_short(&sm.staged[h], n_staged & 1);
           if (ok) {
+            release_stored();
             tma_store_3d(&out_map, sm.q[qb][h], 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok);
             bulk_commit_group();
-            bulk_wait_group_read0();
-            mbar_arrive(&sm.q_empty[qb]);
+            pend_qb = qb;
           }
         }
         ++n_staged;
@@ -841,11 +887,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
 #pragma unroll
           for (int e = 0; e < kD / 8; ++e) dst[e] = row_chunk(e);
         }
-        if (r == 0) mbar_arrive(&sm.q_empty[qb]);
+        if (r == 0) {
+          release_stored();
+          mbar_arrive(&sm.q_empty[qb]);
+        }
       }
       gc += it.n_chunks;
     }
     if (!ok) report(p.err, PA_DEV_TIMEOUT);
+    release_stored();
     if (r == 0) bulk_wait_group0();   // the output stores are complete
   }
   // every TMEM read and MMA is done (or given up on) before the columns go back

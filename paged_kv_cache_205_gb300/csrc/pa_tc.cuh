@@ -64,6 +64,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// One lane of a converged warp (every lane must take part): the lane that
+// issues tcgen05 operations.  Issued this way, from a warp known to be
+// converged, back-to-back MMAs reach the tensor core's own rate; from a
+// branch on the lane index they took two to three times as long each.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // D[tmem] (+)= A[smem] x B[smem]; issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
