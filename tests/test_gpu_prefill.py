@@ -215,7 +215,7 @@ def test_prefill_attention_many_short_two_half_tiles():
     """200 prompts of 33..64 tokens: every (tile, kv head) item has both
     halves and a single, partial chunk, so each CTA runs some 10 items in a
     row in which one MMA warp zeroes V rows and hands the stage to the
-    other, and half 1 waits for half 0 at every item."""
+    other."""
     lens = [33 + (i * 7) % 32 for i in range(200)]
     pool, bt, ctx, cu, q = _attention_state(13, [0] * 200, lens, q_scale=2.0, extra_blocks=3)
     out, err = _gpu_prefill_attention(pool, bt, ctx, cu, q)
