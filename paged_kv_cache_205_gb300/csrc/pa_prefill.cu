@@ -116,6 +116,7 @@ struct __align__(1024) PSmem {
   uint64_t o_free[kHalves];
   uint64_t v_zeroed[kStagesP];                     // zeroing warp -> the other half's MMA warp
   uint64_t staged[kHalves];                        // the half's output rows are in shared memory
+  uint64_t mma_done[kHalves];                      // every MMA of the half's warp has completed
   uint32_t tmem_base;
   int pmask[kStagesP];                             // pages of the stage that were loaded
   int warp_sum[kPThreads / 32];
@@ -394,7 +395,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       mbar_init(&sm.o_full[h], 1);
       mbar_init(&sm.o_free[h], kSoftThreads);
     }
-    for (int h = 0; h < kHalves; ++h) mbar_init(&sm.staged[h], kSoftThreads);
+    for (int h = 0; h < kHalves; ++h) {
+      mbar_init(&sm.staged[h], kSoftThreads);
+      mbar_init(&sm.mma_done[h], 1);
+    }
     fence_mbar_init();
   }
   pdl_launch_dependents();
@@ -682,6 +686,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (nch > 0) ++n_active;
       }
       if (!ok && lane == 0) report(p.err, PA_DEV_TIMEOUT);
+      // the tensor core has finished every MMA this warp issued before the
+      // TMEM columns go back (after a time-out too)
+      if (tc::elect_one()) tc::mma_commit(&sm.mma_done[h]);
+      __syncwarp();
+      if (lane == 0 && !mbar_wait(&sm.mma_done[h], 0)) report(p.err, PA_DEV_TIMEOUT);
       __syncwarp();
     }
   } else {
