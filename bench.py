@@ -734,7 +734,7 @@ def run_gpu(args, rank, world, dist):
 
 # ================================================================ prefill
 PREFILL_METRIC = "prefill tokens/s (paged append + causal paged attention, 16 layers)"
-PREFILL_SOURCES = ("pa_prefill.cu", "pa_device.cuh")
+PREFILL_SOURCES = ("pa_prefill.cu", "pa_device.cuh", "pa_tc.cuh")
 
 
 def prefill_keys(ctx: np.ndarray, lens: np.ndarray) -> int:
