@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       int n_active = 0;        // items in which the half had work
       uint32_t vz_parity = 0;  // per stage: parity of the next zeroing hand-over
       int n_s = 0;             // S chunks issued
-      // Lane 0 waits on the mbarriers and the warp takes its verdict; the
+      // Lane 0 waits on the mbarriers and the warp takes its result; the
       // MMAs and commits are issued by one elected lane of the converged
       // warp, which keeps the tensor core fed at its own rate.
       int qb = 0;              // the item's Q buffer
