@@ -138,7 +138,7 @@ int pa_decode_attention(uint16_t *out, const uint16_t *q, const uint16_t *kv_cac
  * pa_decode_attention_static -- pa_decode_attention for callers that cannot
  * allocate device memory where they run the decode step.
  *
- * The paper has no counterpart to this entry point.  It serves callers that
+ * The pages have no counterpart to this entry point.  It serves callers that
  * may not call cudaMalloc at that point -- an engine whose memory map is fixed
  * at start-up, a serving thread that must not trigger the device-wide
  * synchronisation an allocation can cause, a plugin handed only its tensors.
@@ -283,6 +283,20 @@ int pa_prefill_attention_bt(uint16_t *out, const uint16_t *q, int total_tokens,
                             int block_tokens, const int32_t *block_table, int n_layers,
                             int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                             int layer, float scale, int32_t *err, void *stream);
+
+/*
+ * Test hook for the prefill kernel's bounded waits (no counterpart on the
+ * pages).  With chunk >= 0 the prefill attention kernel's CTA 0 announces the
+ * bytes of its chunk-th 128-key chunk (counted over its items) without
+ * issuing the copies, so the barriers waited on for that chunk never
+ * complete; every wait of the kernel then gives up after wait_limit_ns
+ * (1 us .. 1 s), sets PA_DEV_TIMEOUT in *err, and each warp waits (again
+ * bounded) for its own copies and MMAs in flight before the CTA frees its
+ * tensor memory and exits; the outputs of that call are undefined.  chunk =
+ * -1 restores normal operation (waits of 1 s, no copy left out).
+ * Process-wide; for tests only.  Returns PA_ERR_ARG for a bad chunk or limit.
+ */
+int pa_prefill_set_test_fault(int chunk, long long wait_limit_ns);
 
 /* Bytes of workspace pa_decode_attention needs on the current device. */
 size_t pa_decode_workspace_size(int num_seqs, int max_blocks_per_seq);
@@ -504,7 +518,7 @@ int pa_decode_kernel_for(int num_seqs, int block_tokens);
 int pa_decode_kernel_for_lengths(const int32_t *context_lens, int num_seqs, int block_tokens);
 
 /*
- * Test hook for the bounded waits (no counterpart in the paper; the pages
+ * Test hook for the bounded waits (no counterpart on the pages; they
  * build no failure detection).  With stage >= 0 the split-context kernel's
  * CTA 0 publishes its stage-th shared-memory stage without issuing the copies
  * for it, so the barrier the consumers wait on never completes; every wait of
@@ -518,7 +532,7 @@ int pa_decode_set_test_fault(int stage, long long wait_limit_ns);
 
 /*
  * Test hook of the per-head cluster kernel's speculative plan (no
- * counterpart in the paper).  With mode = 1, its packed plan (the batches
+ * counterpart on the pages).  With mode = 1, its packed plan (the batches
  * where every (sequence, kv head) pair gets two CTAs on average) is first
  * worked out from the first sequence's length in place of every length, as
  * if the lengths had changed after they were read, so that the check after

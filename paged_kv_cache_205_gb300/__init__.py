@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     pa_decode_set_path,
     pa_decode_set_test_fault,
     pa_decode_set_test_plan,
+    pa_prefill_set_test_fault,
     pa_decode_kernel_for,
     pa_decode_kernel_for_lengths,
     PA_DECODE_AUTO,

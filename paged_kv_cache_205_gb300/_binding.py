@@ -37,6 +37,7 @@ _EXPORTS = (
     "pa_decode_workspace_size_bt",
     "pa_prefill_append_rope_bt",
     "pa_prefill_attention_bt",
+    "pa_prefill_set_test_fault",
     "pa_decode_set_grid_limit",
     "pa_error_string",
     "pa_batcher_ctl_bytes",
@@ -132,6 +133,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pa_decode_set_path.restype = I
         lib.pa_decode_set_test_fault.argtypes = [I, ctypes.c_longlong]
         lib.pa_decode_set_test_fault.restype = I
+        lib.pa_prefill_set_test_fault.argtypes = [I, ctypes.c_longlong]
+        lib.pa_prefill_set_test_fault.restype = I
         lib.pa_decode_set_test_plan.argtypes = [I]
         lib.pa_decode_set_test_plan.restype = I
         lib.pa_decode_kernel_for.argtypes = [I, I]
@@ -368,6 +371,15 @@ def pa_decode_set_test_fault(stage: int, wait_limit_ns: int = 0) -> None:
     shortens every wait of the split kernel to wait_limit_ns; -1 restores."""
     _check("pa_decode_set_test_fault",
            library().pa_decode_set_test_fault(int(stage), int(wait_limit_ns)))
+
+
+def pa_prefill_set_test_fault(chunk: int, wait_limit_ns: int = 0) -> None:
+    """Test hook of the prefill kernel's bounded waits (see
+    include/pagedkv.h): chunk >= 0 leaves that chunk of CTA 0 without its
+    copies and shortens every wait of the kernel to wait_limit_ns; -1
+    restores."""
+    _check("pa_prefill_set_test_fault",
+           library().pa_prefill_set_test_fault(int(chunk), int(wait_limit_ns)))
 
 
 def pa_decode_set_test_plan(mode: int) -> None:

@@ -102,12 +102,13 @@ __device__ __forceinline__ bool mbar_try_wait_short(uint64_t *bar, uint32_t pari
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_short(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_short(uint64_t *bar, uint32_t parity,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_short(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_short(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

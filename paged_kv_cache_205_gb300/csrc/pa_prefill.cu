@@ -95,6 +95,10 @@ struct PrefillParams {
   int layer;
   int total_tokens;        // rows of q and out
   float qscale;
+  // test hook (pa_prefill_set_test_fault): the chunk of CTA 0 whose copies
+  // are left out (-1: none), and the limit of every wait
+  int fault_chunk;
+  unsigned long long wait_ns;
 };
 
 struct __align__(1024) PSmem {
@@ -317,10 +321,11 @@ __device__ __forceinline__ bool chunk_needs_zero(const PSmem &sm, int gc, int kb
 // half's MMA warp through v_zeroed.
 template <int BT>
 __device__ __forceinline__ bool mma_prepare_chunk(PSmem &sm, int gc, int kbase, int n_keys,
-                                                  bool zeroer, bool handover, int lane) {
+                                                  bool zeroer, bool handover, int lane,
+                                                  unsigned long long wait_ns) {
   const int st = gc % kStagesP;
   int good = 1;
-  if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (gc / kStagesP) & 1) ? 1 : 0;
+  if (lane == 0) good = mbar_wait_short(&sm.kv_full[st], (gc / kStagesP) & 1, wait_ns) ? 1 : 0;
   good = __shfl_sync(0xffffffffu, good, 0);
   if (!good) return false;
   __syncwarp();
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (lane == 0) {
           // Q buffer k % 2: the MMAs of the item before last have read it
           const int qb = k % kQBufs;
-          if (k >= kQBufs && !mbar_wait(&sm.q_empty[qb], (k / kQBufs - 1) & 1)) {
+          if (k >= kQBufs && !mbar_wait(&sm.q_empty[qb], (k / kQBufs - 1) & 1, p.wait_ns)) {
             good = 0;
           } else {
             mbar_arrive_expect_tx(&sm.q_full[qb], it.halves * kOperandBytes);
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           const unsigned nm = __ballot_sync(0xffffffffu, needed) & kAllPages;
           good = 1;
           if (lane == 0) {
-            if (!mbar_wait(&sm.kv_empty[st], ph ^ 1)) {
+            if (!mbar_wait(&sm.kv_empty[st], ph ^ 1, p.wait_ns)) {
               good = 0;
             } else {
               if (vm != nm) report(p.err, PA_DEV_BAD_BLOCK);
@@ -586,7 +591,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           // V rows of page l mod kPagesPerChunk
           const int pl = lane & (kPagesPerChunk - 1), kv = (lane / kPagesPerChunk) & 1;
           const int pblk = __shfl_sync(0xffffffffu, blk, pl);
-          if (lane < 2 * kPagesPerChunk && ((vm >> pl) & 1u)) {
+          // (test hook: CTA 0 leaves this chunk's copies out, so that the
+          // waits on it run out)
+          const bool fault = p.fault_chunk == gc && blockIdx.x == 0;
+          if (!fault && lane < 2 * kPagesPerChunk && ((vm >> pl) & 1u)) {
             unsigned char *dst = (kv ? sm.v[st] : sm.k[st]) + pl * BT * kTileRowBytes;
             tma_load_5d(dst, &kv_map, 0, it.g, 0, kv, pblk, &sm.kv_full[st]);
           }
@@ -596,10 +604,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         if (!ok) report(p.err, PA_DEV_TIMEOUT);
         // no copy may still be landing in shared memory when the CTA exits
         for (int kk = max(0, k - kQBufs); kk < k; ++kk)
-          if (!mbar_wait(&sm.q_full[kk % kQBufs], (kk / kQBufs) & 1)) report(p.err, PA_DEV_TIMEOUT);
+          if (!mbar_wait(&sm.q_full[kk % kQBufs], (kk / kQBufs) & 1, p.wait_ns)) report(p.err, PA_DEV_TIMEOUT);
         for (int st = 0; st < kStagesP; ++st)
           if ((issued >> st) & 1u)
-            if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u))
+            if (!mbar_wait(&sm.kv_full[st], (issued_parity >> st) & 1u, p.wait_ns))
               report(p.err, PA_DEV_TIMEOUT);
       }
       __syncwarp();
@@ -621,7 +629,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       // S of chunk gcs once the softmax has read the previous S (whole warp)
       auto issue_s = [&](int gcs) -> bool {
         int good = 1;
-        if (lane == 0 && n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1)) good = 0;
+        if (lane == 0 && n_s > 0 && !mbar_wait_short(&sm.s_free[h], (n_s - 1) & 1, p.wait_ns)) good = 0;
         if (!__shfl_sync(0xffffffffu, good, 0)) return false;
         tc::fence_after_sync();
         if (tc::elect_one()) mma_issue_s(sm, tmem, qb, h, gcs, id_s);
@@ -639,16 +647,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         // a one-half tile: that half's warp zeroes, and with two halves hands
         // the chunks half 0 also reads over to it
         const bool zeroer = h == (it.halves == 2 ? 1 : 0);
-        if (lane == 0) ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1) ? 1 : 0;
+        if (lane == 0) ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1, p.wait_ns) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ok = mma_prepare_chunk<BT>(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane);
+        if (ok) ok = mma_prepare_chunk<BT>(sm, gc, 0, it.n_keys, zeroer, it.halves == 2 && it.nc0 > 0, lane,
+                                           p.wait_ns);
         if (ok && nch > 0) ok = issue_s(gc) ? 1 : 0;
         // the next item's loads are in flight while this item's chunks run
         ref = fetch_item(sm, p, total_tiles, sorted, k + 1, n_items);
         for (int j = 0; j < it.n_chunks && ok; ++j, ++gc) {
           if (j + 1 < it.n_chunks &&
               !mma_prepare_chunk<BT>(sm, gc + 1, (j + 1) * kChunk, it.n_keys, zeroer,
-                                 it.halves == 2 && j + 1 < it.nc0, lane)) {
+                                 it.halves == 2 && j + 1 < it.nc0, lane, p.wait_ns)) {
             ok = 0;
             break;
           }
@@ -659,13 +668,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
               const int st = gc % kStagesP;
               // the half's previous item has read its O (the first PV clears it)
               if (good && j == 0 && n_active > 0 &&
-                  !mbar_wait_short(&sm.o_free[h], (n_active - 1) & 1))
+                  !mbar_wait_short(&sm.o_free[h], (n_active - 1) & 1, p.wait_ns))
                 good = 0;
               // the half's softmax has written P
-              if (good && !mbar_wait_short(&sm.p_full[h], n_p & 1)) good = 0;
+              if (good && !mbar_wait_short(&sm.p_full[h], n_p & 1, p.wait_ns)) good = 0;
               // V rows zeroed by the other half's warp
               if (good && !zeroer && chunk_needs_zero<BT>(sm, gc, j * kChunk, it.n_keys)) {
-                if (!mbar_wait_short(&sm.v_zeroed[st], (vz_parity >> st) & 1u)) good = 0;
+                if (!mbar_wait_short(&sm.v_zeroed[st], (vz_parity >> st) & 1u, p.wait_ns)) good = 0;
                 vz_parity ^= 1u << st;
               }
             }
@@ -690,7 +699,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       // TMEM columns go back (after a time-out too)
       if (tc::elect_one()) tc::mma_commit(&sm.mma_done[h]);
       __syncwarp();
-      if (lane == 0 && !mbar_wait(&sm.mma_done[h], 0)) report(p.err, PA_DEV_TIMEOUT);
+      if (lane == 0 && !mbar_wait(&sm.mma_done[h], 0, p.wait_ns)) report(p.err, PA_DEV_TIMEOUT);
       __syncwarp();
     }
   } else {
@@ -737,7 +746,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         // (an earlier arrival would count for the item before last)
         if (r == 0) {
           release_stored();
-          ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1);
+          ok = mbar_wait_short(&sm.q_full[qb], (k / kQBufs) & 1, p.wait_ns);
           if (ok) mbar_arrive(&sm.q_empty[qb]);
         }
         gc += it.n_chunks;
@@ -749,8 +758,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       float m = p_neg_inf(), l = 0.f;
       for (int j = 0; j < nch; ++j) {
         const int st = (gc + j) % kStagesP;
-        if (!mbar_wait_short(&sm.s_full[h], n_s & 1) ||
-            !mbar_wait_short(&sm.kv_full[st], ((gc + j) / kStagesP) & 1)) {
+        if (!mbar_wait_short(&sm.s_full[h], n_s & 1, p.wait_ns) ||
+            !mbar_wait_short(&sm.kv_full[st], ((gc + j) / kStagesP) & 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -788,7 +797,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         const bool move = mc > m + kRescale || (m == p_neg_inf() && mc != p_neg_inf());
         bool pv_done = j == 0;                  // PV_{j-1} complete: O stable, P columns read
         if (__any_sync(0xffffffffu, move) && j > 0) {
-          if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
+          if (!mbar_wait_short(&sm.o_full[h], n_o & 1, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -830,7 +839,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
           }
         }
         if (!pv_done) {
-          if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
+          if (!mbar_wait_short(&sm.o_full[h], n_o & 1, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -847,7 +856,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
       }
       if (!ok) break;
       // O is complete once the item's last PV is
-      if (!mbar_wait_short(&sm.o_full[h], n_o & 1)) {
+      if (!mbar_wait_short(&sm.o_full[h], n_o & 1, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -879,7 +888,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attention_kernel(
         fence_proxy_async_smem();
         mbar_arrive(&sm.staged[h]);
         if (r == 0) {
-          ok = mbar_wait_short(&sm.staged[h], n_staged & 1);
+          ok = mbar_wait_short(&sm.staged[h], n_staged & 1, p.wait_ns);
           if (ok) {
             release_stored();
             tma_store_3d(&out_map, sm.q[qb][h], 0, it.g * kGqa, it.row0 + it.t0 + h * kQTok);
@@ -946,6 +955,9 @@ int make_q_map(CUtensorMap *map, const void *q, int total_tokens) {
 using namespace pa;
 
 namespace {
+
+int g_pf_fault_chunk = -1;                     // test hook, see pa_prefill_set_test_fault
+unsigned long long g_pf_fault_wait_ns = kWaitLimitNs;
 
 template <int BT>
 int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
@@ -1023,6 +1035,8 @@ int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
   prm.layer = layer;
   prm.total_tokens = total_tokens;
   prm.qscale = scale * kLog2eP;
+  prm.fault_chunk = g_pf_fault_chunk;
+  prm.wait_ns = g_pf_fault_chunk >= 0 ? g_pf_fault_wait_ns : kWaitLimitNs;
   if (launch_pdl(prefill_attention_kernel<BT>, dim3(static_cast<unsigned>(grid)),
                  dim3(kPThreads), smem, static_cast<cudaStream_t>(stream), kv_map, q_map, out_map,
                  prm) !=
@@ -1032,6 +1046,14 @@ int prefill_attention_impl(uint16_t *out, const uint16_t *q, int total_tokens,
 }
 
 }  // namespace
+
+extern "C" int pa_prefill_set_test_fault(int chunk, long long wait_limit_ns) {
+  if (chunk < -1 || (chunk >= 0 && (wait_limit_ns < 1000 || wait_limit_ns > 1000000000LL)))
+    return PA_ERR_ARG;
+  g_pf_fault_chunk = chunk;
+  g_pf_fault_wait_ns = chunk >= 0 ? static_cast<unsigned long long>(wait_limit_ns) : kWaitLimitNs;
+  return PA_OK;
+}
 
 extern "C" int pa_prefill_attention(uint16_t *out, const uint16_t *q, int total_tokens,
                                     const int32_t *cu_tokens, const uint16_t *kv_cache,

@@ -51,6 +51,12 @@ def test_host_validation_without_a_device():
     assert lib.pa_decode_set_test_fault(0, 2_000_000_000) == -2
     assert lib.pa_decode_set_test_fault(0, 50_000) == 0
     assert lib.pa_decode_set_test_fault(-1, 0) == 0
+    # the prefill kernel's bounded-wait hook: a chunk >= -1 and a limit of 1 us .. 1 s
+    assert lib.pa_prefill_set_test_fault(-2, 0) == -2
+    assert lib.pa_prefill_set_test_fault(0, 10) == -2
+    assert lib.pa_prefill_set_test_fault(0, 2_000_000_000) == -2
+    assert lib.pa_prefill_set_test_fault(0, 50_000) == 0
+    assert lib.pa_prefill_set_test_fault(-1, 0) == 0
     # the speculative-plan test hook: modes 0 and 1 only
     assert lib.pa_decode_set_test_plan(2) == -2 and lib.pa_decode_set_test_plan(-1) == -2
     assert lib.pa_decode_set_test_plan(1) == 0 and lib.pa_decode_set_test_plan(0) == 0

@@ -61,3 +61,32 @@ def test_wait_that_nothing_completes_runs_out_and_the_next_call_is_clean():
     finally:
         pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
         pk.pa_decode_set_grid_limit(0)
+
+
+def test_prefill_wait_that_nothing_completes_runs_out_and_the_next_call_is_clean():
+    """The same for the prefill attention kernel: CTA 0 announces the bytes of
+    its second 128-key chunk without issuing the copies; every role's wait on
+    it runs out after 50 us, the CTA waits for its own copies, stores and MMAs
+    in flight before it frees its tensor memory, and the call reports
+    PA_DEV_TIMEOUT; the next call, with the hook cleared, matches the
+    oracle."""
+    import torch
+    import paged_kv_cache_205_gb300 as pk
+    from test_gpu_prefill import SCALE, _attention_state, _close, _gpu_prefill_attention
+    # the heaviest item (the first in the work order, CTA 0's) runs through
+    # 4 chunks: 300 cached tokens and the second tile of a 100-token chunk
+    pool, bt, ctx, cu, q = _attention_state(41, [300, 0, 150], [100, 64, 40])
+    try:
+        pk.pa_prefill_set_test_fault(1, 50_000)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        _, err = _gpu_prefill_attention(pool, bt, ctx, cu, q)
+        dt = time.perf_counter() - t0
+        assert err & pk.PA_DEV_TIMEOUT, err
+        assert dt < 1.0, f"the call took {dt:.3f} s"
+    finally:
+        pk.pa_prefill_set_test_fault(-1)
+    out, err = _gpu_prefill_attention(pool, bt, ctx, cu, q)
+    ref, e_ref = oracle.prefill_attention(q, cu, pool, bt, ctx, 0, SCALE)
+    assert err == e_ref == 0
+    _close(host_f64(out), ref, "the call after the timeout")
