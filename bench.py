@@ -1350,10 +1350,18 @@ def run_serve_gpu(args, rank, world, dist):
     sim.close()
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9 if dec_ms > 0 else 0.0
 
-    # end to end: every step's q/k/v from pinned host memory, outputs back
-    h = {name: getattr(loop, name).cpu().pin_memory() for name in ("pq", "pk_", "pv", "dq", "dk", "dv")}
-    h_po = torch.empty_like(loop.po, device="cpu").pin_memory()
-    h_do = torch.empty_like(loop.do, device="cpu").pin_memory()
+    # end to end: every step's q/k/v from pinned host memory, outputs back.
+    # The host side is kept rows first ([row][layer][...]), so that a step's
+    # rows are one contiguous block each way (one direct copy at the link's
+    # rate; the batcher's buffers are layer first, and a device-side copy
+    # moves the block between the two orders)
+    names = ("pq", "pk_", "pv", "dq", "dk", "dv")
+    h = {name: getattr(loop, name).transpose(0, 1).contiguous().cpu().pin_memory() for name in names}
+    g = {name: torch.empty_like(h[name], device="cuda") for name in names}
+    h_po = torch.empty_like(loop.po.transpose(0, 1), device="cpu").contiguous().pin_memory()
+    h_do = torch.empty_like(loop.do.transpose(0, 1), device="cpu").contiguous().pin_memory()
+    g_po = torch.empty_like(h_po, device="cuda")
+    g_do = torch.empty_like(h_do, device="cuda")
     io = {"h2d": 0, "d2h": 0}
 
     def e2e_step(p, before):
@@ -1361,20 +1369,26 @@ def run_serve_gpu(args, rank, world, dist):
             if p.n_admitted:
                 t = p.prefill_tokens
                 for name in ("pq", "pk_", "pv"):
-                    getattr(loop, name)[:, :t].copy_(h[name][:, :t], non_blocking=True)
-                    io["h2d"] += h[name][:, :t].numel() * 2
+                    g[name][:t].copy_(h[name][:t], non_blocking=True)
+                    getattr(loop, name)[:, :t].copy_(g[name][:t].transpose(0, 1))
+                    io["h2d"] += h[name][:t].numel() * 2
             if p.n_rows:
                 n = p.n_rows
                 for name in ("dq", "dk", "dv"):
-                    getattr(loop, name)[:, :n].copy_(h[name][:, :n], non_blocking=True)
-                    io["h2d"] += h[name][:, :n].numel() * 2
+                    g[name][:n].copy_(h[name][:n], non_blocking=True)
+                    getattr(loop, name)[:, :n].copy_(g[name][:n].transpose(0, 1))
+                    io["h2d"] += h[name][:n].numel() * 2
         else:
             if p.n_admitted:
-                h_po[:, :p.prefill_tokens].copy_(loop.po[:, :p.prefill_tokens], non_blocking=True)
-                io["d2h"] += h_po[:, :p.prefill_tokens].numel() * 2
+                t = p.prefill_tokens
+                g_po[:t].copy_(loop.po[:, :t].transpose(0, 1))
+                h_po[:t].copy_(g_po[:t], non_blocking=True)
+                io["d2h"] += h_po[:t].numel() * 2
             if p.n_rows:
-                h_do[:, :p.n_rows].copy_(loop.do[:, :p.n_rows], non_blocking=True)
-                io["d2h"] += h_do[:, :p.n_rows].numel() * 2
+                n = p.n_rows
+                g_do[:n].copy_(loop.do[:, :n].transpose(0, 1))
+                h_do[:n].copy_(g_do[:n], non_blocking=True)
+                io["d2h"] += h_do[:n].numel() * 2
 
     loop.reset()
     torch.cuda.synchronize()
@@ -1440,7 +1454,8 @@ def run_serve_gpu(args, rank, world, dist):
             "d2h_bytes_per_step": io["d2h"],
             "ms_per_step": e2e_s * 1e3,
             "how": "one run with every loop step's q/k/v copied from pinned host memory and its "
-                   "outputs copied back, host wall clock",
+                   "outputs copied back (one contiguous block per tensor and direction, host "
+                   "buffers rows first, reordered on the device), host wall clock",
         },
         "gpu_launches": launches,
         "clocks": sampler.summary(),
