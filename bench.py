@@ -1364,31 +1364,58 @@ def run_serve_gpu(args, rank, world, dist):
     g_do = torch.empty_like(h_do, device="cuda")
     io = {"h2d": 0, "d2h": 0}
 
+    # Each step's rows go in on their own stream, beside the previous step's
+    # kernels (the plan of step i + 1 is known once step i is enqueued), and
+    # its outputs go back on another, beside the next step's kernels; the
+    # device scratch is reused only once the copy or reorder that read it is
+    # done.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {"reordered": None, "sent": None}
+
     def e2e_step(p, before):
+        cur = torch.cuda.current_stream()
         if before:
+            moves = []
             if p.n_admitted:
-                t = p.prefill_tokens
-                for name in ("pq", "pk_", "pv"):
-                    g[name][:t].copy_(h[name][:t], non_blocking=True)
-                    getattr(loop, name)[:, :t].copy_(g[name][:t].transpose(0, 1))
-                    io["h2d"] += h[name][:t].numel() * 2
+                moves += [(name, p.prefill_tokens) for name in ("pq", "pk_", "pv")]
             if p.n_rows:
-                n = p.n_rows
-                for name in ("dq", "dk", "dv"):
-                    g[name][:n].copy_(h[name][:n], non_blocking=True)
-                    getattr(loop, name)[:, :n].copy_(g[name][:n].transpose(0, 1))
-                    io["h2d"] += h[name][:n].numel() * 2
+                moves += [(name, p.n_rows) for name in ("dq", "dk", "dv")]
+            if not moves:
+                return
+            if ev["reordered"] is not None:
+                s_in.wait_event(ev["reordered"])
+            with torch.cuda.stream(s_in):
+                for name, k in moves:
+                    g[name][:k].copy_(h[name][:k], non_blocking=True)
+                    io["h2d"] += h[name][:k].numel() * 2
+                arrived = torch.cuda.Event()
+                arrived.record(s_in)
+            cur.wait_event(arrived)
+            for name, k in moves:
+                getattr(loop, name)[:, :k].copy_(g[name][:k].transpose(0, 1))
+            ev["reordered"] = torch.cuda.Event()
+            ev["reordered"].record(cur)
         else:
+            moves = []
             if p.n_admitted:
-                t = p.prefill_tokens
-                g_po[:t].copy_(loop.po[:, :t].transpose(0, 1))
-                h_po[:t].copy_(g_po[:t], non_blocking=True)
-                io["d2h"] += h_po[:t].numel() * 2
+                moves.append((loop.po, g_po, h_po, p.prefill_tokens))
             if p.n_rows:
-                n = p.n_rows
-                g_do[:n].copy_(loop.do[:, :n].transpose(0, 1))
-                h_do[:n].copy_(g_do[:n], non_blocking=True)
-                io["d2h"] += h_do[:n].numel() * 2
+                moves.append((loop.do, g_do, h_do, p.n_rows))
+            if not moves:
+                return
+            if ev["sent"] is not None:
+                cur.wait_event(ev["sent"])
+            for src, gs, hs, k in moves:
+                gs[:k].copy_(src[:, :k].transpose(0, 1))
+            ready = torch.cuda.Event()
+            ready.record(cur)
+            s_out.wait_event(ready)
+            with torch.cuda.stream(s_out):
+                for src, gs, hs, k in moves:
+                    hs[:k].copy_(gs[:k], non_blocking=True)
+                    io["d2h"] += hs[:k].numel() * 2
+                ev["sent"] = torch.cuda.Event()
+                ev["sent"].record(s_out)
 
     loop.reset()
     torch.cuda.synchronize()
@@ -1455,7 +1482,9 @@ def run_serve_gpu(args, rank, world, dist):
             "ms_per_step": e2e_s * 1e3,
             "how": "one run with every loop step's q/k/v copied from pinned host memory and its "
                    "outputs copied back (one contiguous block per tensor and direction, host "
-                   "buffers rows first, reordered on the device), host wall clock",
+                   "buffers rows first, reordered on the device; a step's inputs on their own "
+                   "stream beside the previous step's kernels, its outputs on another beside "
+                   "the next step's), host wall clock",
         },
         "gpu_launches": launches,
         "clocks": sampler.summary(),
