@@ -515,80 +515,77 @@ def measure_decode(args, w, rank, dist, sampler, k_steps):
     attn_ms = a0.elapsed_time(a1) / (k_roof * L)
     check("in the roofline pass")
 
-    # end to end: the step's inputs from pinned host memory, the step, the
-    # outputs back to pinned host memory -- captured as one graph
+    # end to end: every step's inputs from pinned host memory and its outputs
+    # back, pipelined over two sets of device inputs and outputs.  The graph
+    # of step i computes from one set while a side stream brings step i + 1's
+    # inputs into the other set and sends step i - 1's outputs back from it,
+    # so the layers' kernels keep their dependent-launch chain and the copies
+    # run beside them (one graph per set; replays on one stream follow each
+    # other, so a set is free when its turn comes).  The first step's inputs
+    # come in before the timed region, the last step's outputs go back
+    # inside it: one input copy and one output copy per timed step.
     h_q = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16).pin_memory()
     h_q.copy_(st.q.cpu())
     h_ctx = torch.from_numpy(w.attn_context_lens.copy()).pin_memory()
     h_out = torch.empty((L, n, N_Q, D), dtype=torch.bfloat16).pin_memory()
-    d_q = torch.empty_like(st.q)
     h_kv = None
     if w.append:
         h_kv = (st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(),
                 torch.from_numpy(st.ctx_host.copy()).pin_memory())
-        d_k, d_v = torch.empty_like(st.k_new), torch.empty_like(st.v_new)
-
-    # the copies of all but the first layer's inputs and the last layer's
-    # output run on their own streams beside the layers' kernels (one
-    # dependency each way, so that the kernels keep their dependent-launch
-    # chain): the lengths and layer 0's inputs first, the rest of the inputs
-    # while layer 0 computes, layers 0 .. L-2's outputs while layer L-1 does
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in, ev_att = torch.cuda.Event(), torch.cuda.Event()
-
-    def layer(l):
+    sets = []
+    for _ in range(2):
+        ds = {"q": torch.empty_like(st.q), "out": torch.empty_like(st.out),
+              "ctx_attn": torch.empty_like(st.ctx_attn)}
         if w.append:
-            pk.pa_kv_append_rope(d_k[l], d_v[l], d_q[l], st.pool, st.bt, st.ctx, l, st.fl,
-                                 st.fc, st.err)
-        pk.pa_decode_attention(st.out[l], d_q[l], st.pool, st.bt, st.ctx_attn, l, w.scale,
-                               st.ws, st.err)
+            ds.update(k=torch.empty_like(st.k_new), v=torch.empty_like(st.v_new),
+                      ctx=torch.empty_like(st.ctx))
+        sets.append(ds)
+    s_side = torch.cuda.Stream()
 
-    def e2e_step():
+    def fill(ds):
+        ds["ctx_attn"].copy_(h_ctx, non_blocking=True)
+        ds["q"].copy_(h_q, non_blocking=True)
+        if w.append:
+            ds["ctx"].copy_(h_kv[2], non_blocking=True)
+            ds["k"].copy_(h_kv[0], non_blocking=True)
+            ds["v"].copy_(h_kv[1], non_blocking=True)
+
+    def e2e_step(ds, other):
         cur = torch.cuda.current_stream()
-        st.ctx_attn.copy_(h_ctx, non_blocking=True)
-        d_q[0].copy_(h_q[0], non_blocking=True)
+        s_side.wait_stream(cur)
+        with torch.cuda.stream(s_side):
+            h_out.copy_(other["out"], non_blocking=True)   # the previous step's result
+            fill(other)                                     # the next step's inputs
         if w.append:
-            st.ctx.copy_(h_kv[2], non_blocking=True)
             st.fc.copy_(st.fc0)
-            d_k[0].copy_(h_kv[0][0], non_blocking=True)
-            d_v[0].copy_(h_kv[1][0], non_blocking=True)
-        if L > 1:
-            s_in.wait_stream(cur)
-            with torch.cuda.stream(s_in):
-                d_q[1:].copy_(h_q[1:], non_blocking=True)
-                if w.append:
-                    d_k[1:].copy_(h_kv[0][1:], non_blocking=True)
-                    d_v[1:].copy_(h_kv[1][1:], non_blocking=True)
-                ev_in.record(s_in)
-        layer(0)
-        if L > 1:
-            cur.wait_event(ev_in)
-        for l in range(1, L - 1):
-            layer(l)
-        if L > 1:
-            ev_att.record(cur)
-            s_out.wait_event(ev_att)
-            with torch.cuda.stream(s_out):
-                h_out[:L - 1].copy_(st.out[:L - 1], non_blocking=True)
-            layer(L - 1)
-        h_out[L - 1].copy_(st.out[L - 1], non_blocking=True)
-        if L > 1:
-            cur.wait_stream(s_out)
+        for l in range(L):
+            if w.append:
+                pk.pa_kv_append_rope(ds["k"][l], ds["v"][l], ds["q"][l], st.pool, st.bt, ds["ctx"],
+                                     l, st.fl, st.fc, st.err)
+            pk.pa_decode_attention(ds["out"][l], ds["q"][l], st.pool, st.bt, ds["ctx_attn"], l,
+                                   w.scale, st.ws, st.err)
+        cur.wait_stream(s_side)
 
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_e2e, stream=side):
-            e2e_step()
-    torch.cuda.current_stream().wait_stream(side)
+    graphs = []
+    for i in range(2):
+        g_i = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g_i, stream=side):
+                e2e_step(sets[i], sets[1 - i])
+        torch.cuda.current_stream().wait_stream(side)
+        graphs.append(g_i)
     k_e2e = max(MIN_REPLAYS, min(k_steps, 500))
-    for _ in range(3):
-        g_e2e.replay()
+    k_e2e += k_e2e % 2
+    fill(sets[0])
+    for i in range(4):
+        graphs[i % 2].replay()
     torch.cuda.synchronize()
     barrier()
     sampler.mark(True)
     t0 = time.perf_counter()
-    for _ in range(k_e2e):
-        g_e2e.replay()
+    for i in range(k_e2e):
+        graphs[i % 2].replay()
+    h_out.copy_(sets[1]["out"], non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / k_e2e
     sampler.mark(False)
@@ -599,7 +596,7 @@ def measure_decode(args, w, rank, dist, sampler, k_steps):
     d2h = h_out.numel() * 2
     res = dict(ms=ms, e2e_s=e2e_s, attn_ms=attn_ms, k_roof=k_roof, k_e2e=k_e2e, h2d=h2d, d2h=d2h,
                bytes_step=st.bytes_per_step(), kern=kern, launches_per_step=st.launches_per_step)
-    del st, g_step, g_attn, g_e2e
+    del st, g_step, g_attn, graphs, sets
     pk.pa_decode_set_path(pk.PA_DECODE_AUTO)
     pk.pa_decode_set_grid_limit(0)
     torch.cuda.synchronize()
@@ -634,9 +631,11 @@ def decode_e2e(agg, r):
         "h2d_bytes_per_step": r["h2d"],
         "d2h_bytes_per_step": r["d2h"],
         "ms_per_step": agg["e2e_s"] * 1e3,
-        "how": f"pinned H2D of the step inputs + the step + D2H of all outputs (all but layer "
-               f"0's inputs and the last layer's output copied on their own streams beside the "
-               f"kernels), one graph replay per step, {r['k_e2e']} steps, host wall clock",
+        "how": f"pinned H2D of the step inputs + the step + D2H of all outputs, pipelined over two "
+               f"sets of device buffers (step i's graph brings step i+1's inputs in and sends step "
+               f"i-1's outputs back on a side stream beside its kernels), {r['k_e2e']} steps, one "
+               f"graph replay each, the last outputs copied inside the timed region, host wall "
+               f"clock",
     }
 
 
