@@ -28,8 +28,8 @@
 //               computed while the softmax works on S_j.  A tcgen05.mma issue
 //               blocks while the tensor core's queue is full, so each half
 //               has its own issuing warp; an elected lane of the converged
-//               warp issues (the lane-index branch that did before took two
-//               to three times as long per MMA).  The warp of the half that sees
+//               warp issues (from a branch on the lane index, each MMA takes
+//               two to three times as long).  The warp of the half that sees
 //               every chunk also zeroes the V rows that lie past the tile's
 //               last key or in a page that was not loaded;
 //   warps 0-3, 4-7   softmax of half 0 / half 1, one thread per row (TMEM
