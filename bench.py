@@ -818,7 +818,8 @@ def prefill_cpu_baseline(w, budget_s: float = 12.0):
 def run_prefill_reference(args, rank, world):
     if rank != 0:
         return
-    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens)
+    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens,
+                                  layers=args.layers)
     rng = np.random.default_rng(w.seed + 91)
     per_step_budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
     _, m, _ = prefill_cpu_rate(w, rng, per_step_budget * 4)
@@ -873,6 +874,8 @@ def prefill_description(name, w):
     d = PREFILL_DESCRIPTIONS[name]
     if w.block_tokens != BS:
         d += f"; here {w.block_tokens}-token pages ({w.num_blocks:,} blocks, the same bytes)"
+    if w.n_layers != wl.PREFILL_WORKLOADS[name][1]:
+        d += f" (first {w.n_layers} layers only, {w.num_blocks:,}-block pool)"
     return d
 
 
@@ -882,7 +885,8 @@ def run_prefill_gpu(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda")
-    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens)
+    w = wl.make_prefill_workload(args.workload, block_tokens=args.block_tokens,
+                                  layers=args.layers)
     L, T, n = w.n_layers, w.total_tokens, w.num_seqs
     seed = w.seed + 1000 * rank
     pool = wl.make_prefill_pool_torch(w, dev, seed)
@@ -1521,7 +1525,7 @@ def main():
                          "batch size alone (PA_DECODE_AUTO), the split-context kernel, one "
                          "cluster per (sequence, kv head), or one cluster per sequence")
     ap.add_argument("--layers", type=int, default=0,
-                    help="decode path: only the first N layers, in a pool sized for them "
+                    help="decode and prefill paths: only the first N layers, in a pool sized for them "
                          "(profiler captures of one launch on a small footprint; not a bench line)")
     ap.add_argument("--grid", type=int, default=0,
                     help="cap on decode CTAs per launch (0 = two per SM)")

@@ -254,7 +254,7 @@ PREFILL_WORKLOADS = {
 
 
 def make_prefill_workload(name: str, seed: int | None = None,
-                          block_tokens: int = BLOCK) -> PrefillWorkload:
+                          block_tokens: int = BLOCK, layers: int = 0) -> PrefillWorkload:
     """prompts17_14: the page's two prompts (17 and 14 tokens), one layer.
     prefill8x2k: 8 fresh 2048-token prompts through 16 layers, 65,536-block
     pool.  chunked32x512: 32 sequences with 4096 tokens paged already append
@@ -262,10 +262,17 @@ def make_prefill_workload(name: str, seed: int | None = None,
     popped from a shuffled free list; the chunks' pages come from what is
     left of it.  With block_tokens other than 16 the pool keeps its bytes
     (16 / page times the blocks) and the tables hold pages of that many
-    tokens."""
+    tokens.  layers > 0 keeps only the first `layers` layers, in a pool
+    scaled down with them (the same work per layer call, a smaller device
+    footprint)."""
     if block_tokens not in (8, 16, 32):
         raise ValueError("pages of 8, 16 or 32 tokens")
     sd, n_layers, ctx, lens, num_blocks = PREFILL_WORKLOADS[name]
+    if layers > 0:
+        if layers > n_layers:
+            raise ValueError(f"{name} has {n_layers} layers")
+        num_blocks = -(-num_blocks * layers // n_layers)
+        n_layers = layers
     num_blocks = num_blocks * BLOCK // block_tokens
     rng = np.random.default_rng(sd if seed is None else seed)
     ctx = np.array(ctx, dtype=np.int32)
