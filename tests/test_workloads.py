@@ -61,3 +61,23 @@ def test_page_sizes_other_than_8_16_32_are_refused():
         wl.make_prefill_workload("prefill8x2k", block_tokens=12)
     with pytest.raises(ValueError):
         wl.make_workload("llama1b", block_tokens=64)
+
+
+@pytest.mark.parametrize("name", ["prefill8x2k", "chunked32x512"])
+def test_prefill_workload_first_layers_only(name):
+    """layers=k keeps the prompts, chunks and cached contexts, the first k
+    layers' tables and a pool scaled by k / n_layers (rounded up), and the
+    free list still serves every page the chunks open (the one-layer case is
+    the small-footprint profile of a workload)."""
+    full = wl.make_prefill_workload(name)
+    for k in (1, 3):
+        w = wl.make_prefill_workload(name, layers=k)
+        assert w.n_layers == k
+        assert w.num_blocks == -(-full.num_blocks * k // full.n_layers)
+        assert np.array_equal(w.context_lens, full.context_lens)
+        assert np.array_equal(w.chunk_lens, full.chunk_lens)
+        _check_tables(w.block_table, w.context_lens, w.num_blocks, 16, w.free_list, w.free_count)
+        opened = ((w.context_lens + w.chunk_lens + 15) // 16 - (w.context_lens + 15) // 16).sum() * k
+        assert w.free_count >= opened
+    with pytest.raises(ValueError):
+        wl.make_prefill_workload(name, layers=full.n_layers + 1)
